@@ -1,0 +1,162 @@
+"""Oracle: MXFP8 (E4M3 elements, E8M0 block scales, 32-element blocks).
+
+TEST INFRASTRUCTURE ONLY (see ``oracle/__init__.py``).
+
+The pages ask for an MXFP8 output and its transposed copy written from the
+FC1 epilogue ([CuTe] "무엇을 해결하려는가" and "핵심 아이디어": MXFP8 needs the
+quantised output and a transposed output), for quantisation that respects
+expert-group boundaries and for an MXFP8 grouped GEMM ([TE] "Transformer
+Engine이 제공하는 세 가지 구성 요소").  The block rule is the OCP Microscaling
+(MX) v1.0 one: per block of 32 values, shared scale X = 2^(floor(log2 amax) -
+emax_elem) with emax_elem = 8 for E4M3, element codes E4M3(v / X) with round
+to nearest, ties to even, saturating to the largest finite magnitude 448.
+
+E4M3 here is the OCP "fn" variant: 1 sign, 4 exponent (bias 7), 3 mantissa
+bits, no infinities, NaN = S.1111.111; subnormals 2^-6 * m/8.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+__all__ = [
+    "E4M3_MAX", "e4m3_decode_table", "e4m3_decode", "e4m3_encode",
+    "e8m0_exponent", "mx_quantize_blocks", "mx_quantize_rows",
+    "mx_quantize_cols", "mx_quantize_weights", "mx_dequantize", "mx_fc2",
+]
+
+E4M3_MAX = 448.0
+
+
+def e4m3_decode_table() -> np.ndarray:
+    """Value of each of the 256 codes (NaN for the two NaN codes)."""
+    vals = np.empty(256, dtype=np.float64)
+    for c in range(256):
+        s = -1.0 if c & 0x80 else 1.0
+        ex = (c >> 3) & 0xF
+        m = c & 0x7
+        if ex == 0xF and m == 0x7:
+            vals[c] = np.nan
+        elif ex == 0:
+            vals[c] = s * (m / 8.0) * 2.0 ** -6
+        else:
+            vals[c] = s * (1.0 + m / 8.0) * 2.0 ** (ex - 7)
+    return vals
+
+
+_DEC = e4m3_decode_table()
+# positive finite codes 0x00..0x7E in increasing value order
+_POS_CODES = np.arange(0x7F)
+_POS_VALS = _DEC[:0x7F]
+
+
+def e4m3_decode(codes) -> np.ndarray:
+    return _DEC[np.asarray(codes, dtype=np.uint8)]
+
+
+def e4m3_encode(v) -> np.ndarray:
+    """Brute-force nearest finite E4M3 code, ties to the even code (even
+    mantissa), magnitudes above 448 saturate to 448; the sign bit is kept
+    (so -0 and negative values that round to zero give 0x80)."""
+    v = np.asarray(v, dtype=np.float64)
+    a = np.abs(v).reshape(-1)
+    dist = np.abs(a[:, None] - _POS_VALS[None, :])
+    best = dist.min(axis=1, keepdims=True)
+    cand = dist == best
+    # among equally near codes prefer the even one (ties-to-even); two
+    # adjacent codes always differ in their lowest bit
+    even = cand & ((_POS_CODES[None, :] & 1) == 0)
+    pick = np.where(even.any(axis=1), even.argmax(axis=1), cand.argmax(axis=1))
+    code = _POS_CODES[pick].astype(np.uint8)
+    code = code | np.where(np.signbit(v.reshape(-1)), 0x80, 0).astype(np.uint8)
+    return code.reshape(v.shape)
+
+
+def e8m0_exponent(amax) -> np.ndarray:
+    """Shared-scale exponent e = clamp(floor(log2 amax) - 8, -127, 127);
+    amax = 0 gives -127.  floor(log2) is read exactly from frexp."""
+    amax = np.asarray(amax, dtype=np.float64)
+    _, ex = np.frexp(amax)          # amax = m 2^ex, m in [0.5, 1)
+    e = (ex - 1) - 8
+    e = np.where(amax == 0, -127, e)
+    return np.clip(e, -127, 127).astype(np.int64)
+
+
+def mx_quantize_blocks(blocks):
+    """``blocks`` [..., 32] float64 -> (codes uint8 [..., 32], scale codes
+    uint8 [...]) where the scale code is e + 127."""
+    blocks = np.asarray(blocks, dtype=np.float64)
+    amax = np.abs(blocks).max(axis=-1)
+    e = e8m0_exponent(amax)
+    scaled = blocks * np.ldexp(1.0, -e)[..., None]   # exact (power of two)
+    return e4m3_encode(scaled), (e + 127).astype(np.uint8)
+
+
+def mx_quantize_rows(A):
+    """Row-wise MX: blocks of 32 consecutive columns of each row.
+    A [M, n] (n % 32 == 0) -> codes [M, n], scales [M, n/32]."""
+    A = np.asarray(A, dtype=np.float64)
+    M, n = A.shape
+    q, s = mx_quantize_blocks(A.reshape(M, n // 32, 32))
+    return q.reshape(M, n), s
+
+
+def mx_quantize_cols(A, offsets, M_cap=None):
+    """Column-wise MX for the transposed copy: blocks of 32 consecutive rows
+    of each column.  Blocks are taken inside each expert's row range
+    [offsets[e], offsets[e+1]) (group-aware; with 32-row alignment every
+    range starts on a block boundary and no block crosses two experts).
+
+    Returns (codes_T uint8 [n, M_cap], scales_T uint8 [n, M_cap/32]); rows
+    outside every expert are left 0."""
+    A = np.asarray(A, dtype=np.float64)
+    M = A.shape[0] if M_cap is None else M_cap
+    n = A.shape[1]
+    qT = np.zeros((n, M), dtype=np.uint8)
+    sT = np.zeros((n, M // 32), dtype=np.uint8)
+    E = len(offsets) - 1
+    for e in range(E):
+        r0, r1 = int(offsets[e]), int(offsets[e + 1])
+        assert r0 % 32 == 0 and r1 % 32 == 0, "column blocks need 32-row alignment"
+        for b0 in range(r0, r1, 32):
+            blk = A[b0:b0 + 32, :].T             # [n, 32]
+            q, s = mx_quantize_blocks(blk)
+            qT[:, b0:b0 + 32] = q
+            sT[:, b0 // 32] = s
+    return qT, sT
+
+
+def mx_quantize_weights(W2):
+    """W2 [E, n, d]: blocks of 32 consecutive rows (FC2's reduction index)
+    for each column.  Returns codes [E, n, d] and scales [E, n/32, d]."""
+    W2 = np.asarray(W2, dtype=np.float64)
+    E, n, d = W2.shape
+    blk = W2.reshape(E, n // 32, 32, d).transpose(0, 1, 3, 2)   # [E, n/32, d, 32]
+    q, s = mx_quantize_blocks(blk)
+    return q.transpose(0, 1, 3, 2).reshape(E, n, d), s
+
+
+def mx_dequantize(codes, scale_codes, axis_block: int):
+    """Decode codes with their block scales; ``axis_block`` is the axis of
+    ``codes`` along which 32 consecutive elements share a scale."""
+    v = e4m3_decode(codes)
+    s = np.ldexp(1.0, scale_codes.astype(np.int64) - 127)
+    s = np.repeat(s, 32, axis=axis_block)
+    return v * s
+
+
+def mx_fc2(A_q, A_s, W2_q, W2_s, offsets):
+    """MXFP8 down-projection Y_e = sum over 32-blocks b of
+    (s_A s_W) * sum_{i in b} qA qW, float64; Y rounded to bf16 by the caller.
+    Products of dequantised values are exact in float64."""
+    from .moe import bf16_round
+    A = mx_dequantize(A_q, A_s, axis_block=1)
+    M = A.shape[0]
+    E, n, d = W2_q.shape
+    Y = np.full((M, d), np.nan)
+    for e in range(E):
+        r0, r1 = int(offsets[e]), int(offsets[e + 1])
+        if r1 <= r0:
+            continue
+        W = mx_dequantize(W2_q[e], W2_s[e], axis_block=0)
+        Y[r0:r1] = A[r0:r1] @ W
+    return bf16_round(Y)

@@ -1,0 +1,186 @@
+"""Pins for the oracle's grouped expert MLP (forward and backward).
+
+Pinned by brute-force scalar loops on tiny inputs, the interleaved-vs-split
+weight equivalence, closed forms of the activations, central finite
+differences of the activations and of the whole layer, and the empty-group
+and zero-token invariants."""
+import math
+
+import numpy as np
+import pytest
+
+import oracle as O
+
+ACTS = ["swiglu", "geglu", "srelu"]
+
+
+def _scalar_act(h_row, act):
+    """Pure-Python activation of one H row (brute force)."""
+    out = []
+    if act == "srelu":
+        return [max(v, 0.0) ** 2 for v in h_row]
+    for j in range(len(h_row) // 2):
+        g, u = h_row[2 * j], h_row[2 * j + 1]
+        if act == "swiglu":
+            ph = g / (1.0 + math.exp(-g))
+        else:
+            ph = 0.5 * g * (1.0 + math.tanh(math.sqrt(2 / math.pi) * (g + 0.044715 * g ** 3)))
+        out.append(ph * u)
+    return out
+
+
+def _tiny(act, rng, rows=(2, 0, 3), d=4, n=3):
+    E = len(rows)
+    off = np.concatenate([[0], np.cumsum(rows)])
+    M = int(off[-1])
+    n1 = 2 * n if act != "srelu" else n
+    x = rng.standard_normal((M, d))
+    W1 = rng.standard_normal((E, d, n1)) * 0.5
+    W2 = rng.standard_normal((E, n, d)) * 0.5
+    return off, x, W1, W2
+
+
+@pytest.mark.parametrize("act", ACTS)
+def test_fwd_brute_force(act):
+    rng = np.random.default_rng(10)
+    off, x, W1, W2 = _tiny(act, rng)
+    H, A, Y = O.grouped_mlp_fwd(x, off, W1, W2, act, round_bf16=False)
+    E = len(off) - 1
+    for e in range(E):
+        for r in range(off[e], off[e + 1]):
+            h = [sum(x[r][i] * W1[e][i][c] for i in range(x.shape[1])) for c in range(W1.shape[2])]
+            a = _scalar_act(h, act)
+            y = [sum(a[j] * W2[e][j][c] for j in range(len(a))) for c in range(W2.shape[2])]
+            assert np.allclose(H[r], h, rtol=0, atol=1e-12)
+            assert np.allclose(A[r], a, rtol=0, atol=1e-12)
+            assert np.allclose(Y[r], y, rtol=0, atol=1e-12)
+
+
+@pytest.mark.parametrize("act", ["swiglu", "geglu"])
+def test_interleaved_equals_split(act):
+    """Interleaving is a column permutation of concatenated [gate | up]
+    weights (the TE page's prefused (E, d, 2*mlp) layout): A from the
+    interleaved layout equals phi(X Wg) * (X Wu)."""
+    rng = np.random.default_rng(11)
+    E, d, n = 3, 8, 5
+    Wg = rng.standard_normal((E, d, n))
+    Wu = rng.standard_normal((E, d, n))
+    W1 = O.interleave_gate_up(Wg, Wu)
+    g2, u2 = O.split_gate_up(W1)
+    assert (g2 == Wg).all() and (u2 == Wu).all()
+    assert (W1[..., :: 2] == Wg).all()
+    W2 = rng.standard_normal((E, n, d))
+    off = np.array([0, 4, 4, 9])
+    x = rng.standard_normal((9, d))
+    _, A, _ = O.grouped_mlp_fwd(x, off, W1, W2, act, round_bf16=False)
+    concat = np.concatenate([Wg, Wu], axis=2)        # [gate | up]
+    for e in range(E):
+        xe = x[off[e]:off[e + 1]]
+        hc = xe @ concat[e]
+        g, u = hc[:, :n], hc[:, n:]
+        assert np.allclose(A[off[e]:off[e + 1]], O.phi(g, act) * u, rtol=1e-13, atol=1e-13)
+
+
+def test_activation_closed_forms():
+    g = np.linspace(-8, 8, 2001)
+    silu = O.phi(g, "swiglu")
+    assert O.phi(np.array([0.0]), "swiglu")[0] == 0.0
+    assert np.allclose(O.phi(-g, "swiglu"), silu - g, atol=1e-12)   # silu(-x) = silu(x) - x
+    assert abs(O.phi(np.array([50.0]), "swiglu")[0] - 50.0) < 1e-18 + 1e-12
+    # tanh-GELU against exact erf-GELU x*Phi(x): a wrong constant breaks this
+    exact = np.array([0.5 * v * (1 + math.erf(v / math.sqrt(2))) for v in g])
+    assert np.abs(O.phi(g, "geglu") - exact).max() < 1e-3
+    assert O.phi(np.array([0.0]), "geglu")[0] == 0.0
+    h = np.array([-2.0, -0.0, 0.0, 0.5, 3.0])
+    assert O.act_forward(h, "srelu").tolist() == [0.0, 0.0, 0.0, 0.25, 9.0]
+
+
+@pytest.mark.parametrize("act", ["swiglu", "geglu"])
+def test_dphi_finite_difference(act):
+    g = np.linspace(-7, 7, 301)
+    eps = 1e-5
+    fd = (O.phi(g + eps, act) - O.phi(g - eps, act)) / (2 * eps)
+    assert np.abs(fd - O.dphi(g, act)).max() < 1e-8
+
+
+@pytest.mark.parametrize("act", ACTS)
+def test_act_backward_finite_difference(act):
+    rng = np.random.default_rng(12)
+    h = rng.standard_normal((3, 8)) * 2
+    dA = rng.standard_normal((3, 8 if act == "srelu" else 4))
+    dH = O.act_backward(h, dA, act)
+    eps = 1e-6
+    for idx in np.ndindex(h.shape):
+        hp, hm = h.copy(), h.copy()
+        hp[idx] += eps
+        hm[idx] -= eps
+        fd = ((O.act_forward(hp, act) - O.act_forward(hm, act)) * dA).sum() / (2 * eps)
+        assert abs(fd - dH[idx]) < 1e-6
+
+
+@pytest.mark.parametrize("act", ACTS)
+def test_layer_gradient_finite_difference(act):
+    """L = sum(dY * Y) on an unrounded tiny layer with an empty expert:
+    dX, dW1, dW2 from grouped_mlp_bwd equal central differences."""
+    rng = np.random.default_rng(13)
+    off, x, W1, W2 = _tiny(act, rng, rows=(3, 0, 2), d=5, n=3)
+    dY = rng.standard_normal((x.shape[0], W2.shape[2]))
+
+    def L(x_, W1_, W2_):
+        _, _, Y = O.grouped_mlp_fwd(x_, off, W1_, W2_, act, round_bf16=False)
+        return float((dY * Y).sum())
+
+    H, A, _ = O.grouped_mlp_fwd(x, off, W1, W2, act, round_bf16=False)
+    dH, dX, dW1, dW2 = O.grouped_mlp_bwd(x, H, A, dY, off, W1, W2, act, round_bf16=False)
+    eps = 1e-6
+    for arr, grad, name in [(x, dX, "x"), (W1, dW1, "W1"), (W2, dW2, "W2")]:
+        for idx in np.ndindex(arr.shape):
+            p, m = arr.copy(), arr.copy()
+            p[idx] += eps
+            m[idx] -= eps
+            args_p = {"x": (p, W1, W2), "W1": (x, p, W2), "W2": (x, W1, p)}[name]
+            args_m = {"x": (m, W1, W2), "W1": (x, m, W2), "W2": (x, W1, m)}[name]
+            fd = (L(*args_p) - L(*args_m)) / (2 * eps)
+            assert abs(fd - grad[idx]) < 1e-5, (name, idx)
+    # the empty expert's weight gradients are exactly zero
+    assert (dW1[1] == 0).all() and (dW2[1] == 0).all()
+
+
+def test_special_cases_zero_grads():
+    h = np.array([[-1.0, 2.0, -0.5, 0.0]])
+    dA = np.ones((1, 4))
+    assert (O.act_backward(h, dA, "srelu")[0] == [0, 4.0, 0, 0]).all()
+    # SwiGLU with up = 0: output 0 and gate gradient 0
+    hg = np.array([[1.3, 0.0, -2.0, 0.0]])
+    assert (O.act_forward(hg, "swiglu") == 0).all()
+    assert (O.act_backward(hg, np.ones((1, 2)), "swiglu")[0, 0::2] == 0).all()
+
+
+@pytest.mark.parametrize("act", ACTS)
+def test_zero_tokens(act):
+    rng = np.random.default_rng(14)
+    E, d, n = 3, 4, 2
+    n1 = n if act == "srelu" else 2 * n
+    off = np.zeros(E + 1, np.int64)
+    x = np.zeros((0, d))
+    W1 = rng.standard_normal((E, d, n1))
+    W2 = rng.standard_normal((E, n, d))
+    H, A, Y = O.grouped_mlp_fwd(x, off, W1, W2, act)
+    assert H.shape == (0, n1) and A.shape == (0, n) and Y.shape == (0, d)
+    dH, dX, dW1, dW2 = O.grouped_mlp_bwd(x, H, A, np.zeros((0, d)), off, W1, W2, act)
+    assert (dW1 == 0).all() and (dW2 == 0).all() and dX.shape == (0, d)
+
+
+def test_rounding_points():
+    """With round_bf16=True every stored tensor is bf16-representable, and A
+    is computed from the unrounded H."""
+    rng = np.random.default_rng(15)
+    off, x, W1, W2 = _tiny("swiglu", rng, rows=(5, 3, 4), d=16, n=8)
+    x = O.bf16_round(x)
+    W1 = O.bf16_round(W1)
+    W2 = O.bf16_round(W2)
+    H, A, Y = O.grouped_mlp_fwd(x, off, W1, W2, "swiglu")
+    for t in (H, A, Y):
+        assert (O.bf16_round(t) == t).all()
+    Hr, Ar, _ = O.grouped_mlp_fwd(x, off, W1, W2, "swiglu", round_bf16=False)
+    assert (A == O.bf16_round(Ar)).all()
