@@ -1,0 +1,549 @@
+#!/usr/bin/env python
+"""Benchmark of the dropless MoE expert-MLP path on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+                    [--impl ours|reference]
+
+Metric: grouped MoE MLP forward + backward useful TFLOP/s (FLOPs of real
+rows only: 18 M d n for gated activations, 12 M d n for squared ReLU, M =
+routed (token, expert) pairs), and the fraction of GB300 dense BF16 peak.
+
+Default workload: the pages' grouped-GEMM benchmark shape (E=8 experts, 4096
+tokens each, K=d=8192, N=2n=4096, SwiGLU forward + dSwiGLU backward, BF16;
+counts fixed, equal and device-resident).  A step is one
+moe_grouped_mlp_fwd (FC1+SwiGLU, FC2) plus one moe_grouped_mlp_bwd
+(FC2-dgrad+dSwiGLU, FC2-wgrad, FC1-dgrad, FC1-wgrad).  Workloads with
+routing (zipf_*) time the whole layer: routing layout, permute, forward,
+combine, and their backward with the router-score gradient.
+
+Inputs are seeded and synthetic (``workloads``), resident in HBM before the
+timed region, and larger than L2 (no flush needed).  Timing: W warm-up
+steps, then K steps between CUDA events on the launching stream, bracketed
+by a barrier and a synchronize, max over ranks.  Under torchrun each rank
+runs an independent replica (the path does not shard; there is no
+collective in the data path).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads as WL  # noqa: E402
+
+METRIC = "grouped MoE MLP fwd+bwd useful TFLOP/s and % of GB300 dense BF16/FP8 peak"
+DEFAULT_WORKLOAD = "balanced_e8_m4096_k8192_n4096_swiglu"
+KERNELS_FWD = ["fc1_act", "fc2"]
+KERNELS_BWD = ["fc2_dgrad_dact", "fc2_wgrad", "fc1_dgrad", "fc1_wgrad"]
+
+
+# ---------------------------------------------------------------- accounting
+def useful_flops(w, M):
+    """fwd + bwd FLOPs of real rows (the pages' arithmetic-intensity model
+    counts the same terms: [Sonic] section on MoE arithmetic intensity)."""
+    n1 = w.n1
+    fwd = 2 * M * w.d * n1 + 2 * M * w.n * w.d
+    bwd = 2 * M * w.d * w.n + 2 * M * w.n * w.d + 2 * M * n1 * w.d + 2 * M * w.d * n1
+    return fwd, bwd
+
+
+def kernel_work(w, M, E_ne):
+    """Algorithmic FLOPs and bytes per launch of each grouped GEMM (bf16 =
+    2 B; weights of non-empty experts only; weight gradients of all
+    experts, written as zeros for empty ones)."""
+    d, n, n1, E = w.d, w.n, w.n1, w.E
+    B = 2
+    return {
+        "fc1_act": (2 * M * d * n1, B * (M * d + E_ne * d * n1 + M * n + M * n1)),
+        "fc2": (2 * M * n * d, B * (M * n + E_ne * n * d + M * d)),
+        "fc2_dgrad_dact": (2 * M * d * n, B * (M * d + E_ne * n * d + 2 * M * n1)),
+        "fc2_wgrad": (2 * M * n * d, B * (M * n + M * d + E * n * d)),
+        "fc1_dgrad": (2 * M * n1 * d, B * (M * n1 + E_ne * d * n1 + M * d)),
+        "fc1_wgrad": (2 * M * d * n1, B * (M * d + M * n1 + E * d * n1)),
+    }
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        j = json.load(open(p))
+        return {"hbm_gbs": j["hbm_gbs"], "bf16_tflops": j["bf16_tflops"],
+                "bf16_tflops_sustained": j.get("bf16_tflops_sustained", j["bf16_tflops"]),
+                "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+            "source": "fallback"}
+
+
+def kernel_src_hash():
+    h = hashlib.sha256()
+    for f in ("gemm.cu", "gemm.cuh", "ptx.cuh"):
+        h.update(open(os.path.join(ROOT, "dropless_grouped_gemm_gb300", "csrc", f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(kernel, workload):
+    """DRAM bytes per launch from a committed ncu summary, if it was taken
+    on the current kernel source; else None."""
+    p = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    if not os.path.exists(p):
+        return None
+    j = json.load(open(p))
+    rec = j.get(workload, {}).get(kernel)
+    if not rec or rec.get("src_hash") != kernel_src_hash():
+        return None
+    return rec.get("dram_bytes_per_launch")
+
+
+# ---------------------------------------------------------------- clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id):
+        self.p = None
+        try:
+            self.p = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100", "-i", str(gpu_id)],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, ValueError):
+            self.p = None
+
+    def stop(self):
+        if self.p is None:
+            return None
+        self.p.terminate()
+        try:
+            out, _ = self.p.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.p.kill()
+            out, _ = self.p.communicate()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(nm)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+# ---------------------------------------------------------------- inputs
+def make_inputs(w, dev):
+    import torch
+    import dropless_grouped_gemm_gb300 as M
+    d, n, E = w.d, w.n, w.E
+    inp = {}
+    if w.gated:
+        inp["W1"] = WL.w1_interleaved(w.cfg_id, E, d, n, w.w_std, dev)
+    else:
+        inp["W1"] = WL.w1_plain(w.cfg_id, E, d, n, w.w_std, dev)
+    inp["W2"] = WL.w2(w.cfg_id, E, n, d, w.w_std, dev)
+    if w.routing == "identity":
+        m = w.T // E
+        inp["offsets"] = torch.arange(0, w.T + 1, m, dtype=torch.int32, device=dev)
+        inp["x_perm"] = WL.normal((w.M_cap, d), (w.cfg_id, WL.X, 0), w.x_std, dev)
+        inp["dy_perm"] = WL.normal((w.M_cap, d), (w.cfg_id, WL.DY, 0), w.dy_std, dev)
+        inp["M"] = w.T
+        inp["E_ne"] = E
+    else:
+        idx, probs = WL.route_inputs(w)
+        inp["topk_idx"] = torch.from_numpy(idx).to(dev)
+        inp["probs"] = torch.from_numpy(probs).to(dev)
+        inp["x"] = WL.normal((w.T, d), (w.cfg_id, WL.X, 0), w.x_std, dev)
+        inp["dO"] = WL.normal((w.T, d), (w.cfg_id, WL.DO, 0), w.dy_std, dev)
+        counts = np.bincount(idx.reshape(-1), minlength=E)
+        inp["M"] = int(counts.sum())
+        inp["E_ne"] = int((counts > 0).sum())
+    # outputs / intermediates, allocated once
+    Mc, n1 = w.M_cap, w.n1
+    bf = torch.bfloat16
+    o = {k: torch.empty(s, dtype=bf, device=dev) for k, s in [
+        ("h", (Mc, n1)), ("a", (Mc, n)), ("y_perm", (Mc, d)), ("dh", (Mc, n1)),
+        ("dx_perm", (Mc, d)), ("dW1", tuple(inp["W1"].shape)), ("dW2", tuple(inp["W2"].shape))]}
+    o["err"] = torch.zeros(1, dtype=torch.int32, device=dev)
+    if w.routing != "identity":
+        o["x_perm"] = torch.empty((Mc, d), dtype=bf, device=dev)
+        o["dy_perm"] = torch.empty((Mc, d), dtype=bf, device=dev)
+        o["out"] = torch.empty((w.T, d), dtype=bf, device=dev)
+        o["dx"] = torch.empty((w.T, d), dtype=bf, device=dev)
+        o["dprobs"] = torch.empty((w.T, w.k), dtype=torch.float32, device=dev)
+        o["ws"] = torch.empty(max(16, M.route_workspace_size(w.T, w.k, E)), dtype=torch.uint8,
+                              device=dev)
+        o["route"] = {
+            "counts": torch.empty(E, dtype=torch.int32, device=dev),
+            "offsets": torch.empty(E + 1, dtype=torch.int32, device=dev),
+            "row_of_pair": torch.empty(w.T * w.k, dtype=torch.int32, device=dev),
+            "pair_of_row": torch.empty(Mc, dtype=torch.int32, device=dev),
+            "true_total": torch.empty(1, dtype=torch.int32, device=dev),
+            "err": o["err"],
+        }
+    return inp, o
+
+
+def make_step(w, inp, o):
+    """One pass of the path; returns the number of libmoe kernel launches."""
+    import dropless_grouped_gemm_gb300 as M
+    act = w.act
+
+    if w.routing == "identity":
+        def step():
+            M.grouped_mlp_fwd(inp["x_perm"], inp["offsets"], inp["W1"], inp["W2"], act,
+                              save_h=True, h_saved=o["h"], a=o["a"], y_perm=o["y_perm"],
+                              err=o["err"])
+            n = M.last_launch_count()
+            M.grouped_mlp_bwd(inp["x_perm"], o["h"], o["a"], inp["dy_perm"], inp["offsets"],
+                              inp["W1"], inp["W2"], act, dh=o["dh"], dx_perm=o["dx_perm"],
+                              dW1=o["dW1"], dW2=o["dW2"], err=o["err"])
+            return n + M.last_launch_count()
+        return step
+
+    T, k = w.T, w.k
+
+    def step():
+        n = 0
+        r = M.route_offsets(inp["topk_idx"], w.E, w.align, w.M_cap, out=o["route"],
+                            workspace=o["ws"])
+        n += M.last_launch_count()
+        M.permute(inp["x"], r["pair_of_row"], k, out=o["x_perm"])
+        n += M.last_launch_count()
+        M.grouped_mlp_fwd(o["x_perm"], r["offsets"], inp["W1"], inp["W2"], act, save_h=True,
+                          h_saved=o["h"], a=o["a"], y_perm=o["y_perm"], err=o["err"])
+        n += M.last_launch_count()
+        M.unpermute(o["y_perm"], r["row_of_pair"], T, k, probs=inp["probs"], out=o["out"])
+        n += M.last_launch_count()
+        # backward: combine -> (scaled permute of dO, router-score gradient)
+        M.permute(inp["dO"], r["pair_of_row"], k, scale=inp["probs"].view(-1), out=o["dy_perm"])
+        n += M.last_launch_count()
+        M.unpermute(o["y_perm"], r["row_of_pair"], T, k, dO=inp["dO"], dprobs=o["dprobs"],
+                    combine=False)
+        n += M.last_launch_count()
+        M.grouped_mlp_bwd(o["x_perm"], o["h"], o["a"], o["dy_perm"], r["offsets"], inp["W1"],
+                          inp["W2"], act, dh=o["dh"], dx_perm=o["dx_perm"], dW1=o["dW1"],
+                          dW2=o["dW2"], err=o["err"])
+        n += M.last_launch_count()
+        M.unpermute(o["dx_perm"], r["row_of_pair"], T, k, out=o["dx"])
+        n += M.last_launch_count()
+        return n
+    return step
+
+
+def event_names(w):
+    if w.routing == "identity":
+        return KERNELS_FWD + KERNELS_BWD
+    return (["route", "permute"] + KERNELS_FWD + ["combine", "permute_bwd", "router_grad"] +
+            KERNELS_BWD + ["unpermute_bwd"])
+
+
+# ---------------------------------------------------------------- CPU oracle
+def oracle_sample(w, rows):
+    """A bounded sample of the workload for the oracle: ``rows`` routed rows
+    of expert 0 with that expert's weights (regenerated on the CPU)."""
+    import torch
+    d, n = w.d, w.n
+    cpu = "cpu"
+    f = lambda t: t.to(torch.float64).numpy()
+    x = f(WL.normal((rows, d), (w.cfg_id, WL.X, 0), w.x_std, cpu))
+    dy = f(WL.normal((rows, d), (w.cfg_id, WL.DY, 0), w.dy_std, cpu))
+    W1 = f(WL.w1_interleaved(w.cfg_id, 1, d, n, w.w_std, cpu) if w.gated else
+           WL.w1_plain(w.cfg_id, 1, d, n, w.w_std, cpu))
+    W2 = f(WL.w2(w.cfg_id, 1, n, d, w.w_std, cpu))
+    return x, dy, W1, W2
+
+
+def time_oracle(w, rows, reps=1):
+    import oracle as O
+    x, dy, W1, W2 = oracle_sample(w, rows)
+    off = np.array([0, rows])
+    t0 = time.perf_counter()
+    for _ in range(reps):
+        H, A, _ = O.grouped_mlp_fwd(x, off, W1, W2, w.act)
+        O.grouped_mlp_bwd(x, H, A, dy, off, W1, W2, w.act)
+    dt = (time.perf_counter() - t0) / reps
+    fwd, bwd = useful_flops(w, rows)
+    return (fwd + bwd) / dt / 1e12, dt
+
+
+def cpu_cores():
+    for v in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS"):
+        if os.environ.get(v, "").isdigit():
+            return int(os.environ[v])
+    return os.cpu_count()
+
+
+# ---------------------------------------------------------------- main
+def dist_setup(gpus):
+    import torch
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    lrank = int(os.environ.get("LOCAL_RANK", "0"))
+    if ws > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(lrank)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", lrank))
+    return ws, rank, lrank
+
+
+def barrier(ws):
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(v, ws):
+    if ws == 1:
+        return v
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def run_reference(args, w):
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    rows = args.ref_rows
+    import oracle as O
+    x, dy, W1, W2 = oracle_sample(w, rows)
+    off = np.array([0, rows])
+
+    def step():
+        H, A, _ = O.grouped_mlp_fwd(x, off, W1, W2, w.act)
+        O.grouped_mlp_bwd(x, H, A, dy, off, W1, W2, w.act)
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    dt = (time.perf_counter() - t0) / args.steps
+    fwd, bwd = useful_flops(w, rows)
+    v = (fwd + bwd) / dt / 1e12
+    sample = (f"{rows} rows of expert 0 ({w.d}x{w.n1} W1, {w.n}x{w.d} W2), oracle float64 "
+              f"fwd+bwd per step")
+    line = {"impl": "reference", "metric": METRIC, "value": v, "unit": "TFLOP/s",
+            "n_gpus": ws, "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": {"workload": w.name, "sample": sample},
+            "cpu_baseline": {"value": v, "unit": "TFLOP/s", "cores": cpu_cores(),
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": v, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=60)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(WL.WORKLOADS))
+    ap.add_argument("--e2e-steps", type=int, default=10)
+    ap.add_argument("--cpu-rows", type=int, default=512,
+                    help="rows of the oracle's cpu_baseline sample")
+    ap.add_argument("--ref-rows", type=int, default=64,
+                    help="rows per step of the --impl reference sample")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+    w = WL.WORKLOADS[args.workload]
+    if w.mxfp8:
+        raise SystemExit(f"{w.name}: not a bench workload of this build")
+
+    if args.impl == "reference":
+        return run_reference(args, w)
+
+    import torch
+    ws, rank, lrank = dist_setup(args.gpus)
+    dev = f"cuda:{lrank}"
+    torch.cuda.set_device(lrank)
+    if rank == 0:
+        from dropless_grouped_gemm_gb300 import build as B
+        B.build()
+    barrier(ws)
+    import dropless_grouped_gemm_gb300 as M
+    M.lib()
+
+    inp, o = make_inputs(w, dev)
+    step = make_step(w, inp, o)
+    names = event_names(w)
+    stream = torch.cuda.current_stream()
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    if int(o["err"].item()) != 0:
+        raise SystemExit(f"device error bits {int(o['err'].item())}")
+
+    # per-launch events for the timed region
+    import ctypes
+    per = len(names)
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(2 * per * args.steps)]
+    handles = (ctypes.c_void_p * len(evs))(*[e.cuda_event for e in evs])
+    try:
+        uuid = str(torch.cuda.get_device_properties(lrank).uuid)
+        gpu_id = uuid if uuid.startswith("GPU-") else f"GPU-{uuid}"
+    except Exception:
+        gpu_id = lrank
+    sampler = ClockSampler(gpu_id)
+    time.sleep(0.3)
+    launches = 0
+    barrier(ws)
+    torch.cuda.synchronize()
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    M.lib().moe_set_launch_events(handles, len(evs))
+    t_start.record(stream)
+    for _ in range(args.steps):
+        launches += step()
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    used = M.lib().moe_launch_events_used()
+    M.lib().moe_set_launch_events(None, 0)
+    barrier(ws)
+    clocks = sampler.stop()
+    ms = t_start.elapsed_time(t_end) / args.steps
+    ms = max_over_ranks(ms, ws)
+
+    Mrows = inp["M"]
+    fwd_f, bwd_f = useful_flops(w, Mrows)
+    per_rank_tf = (fwd_f + bwd_f) / (ms * 1e-3) / 1e12
+    value = per_rank_tf * ws
+    peaks = load_peaks()
+
+    # per-kernel durations
+    dur = {nm: [] for nm in names}
+    for i in range(used // 2):
+        dur[names[i % per]].append(evs[2 * i].elapsed_time(evs[2 * i + 1]))
+    work = kernel_work(w, Mrows, inp["E_ne"])
+    kern = {}
+    for nm in names:
+        if not dur[nm]:
+            continue
+        avg = sum(dur[nm]) / len(dur[nm])
+        rec = {"ms": round(avg, 4), "share": None}
+        if nm in work:
+            fl, by = work[nm]
+            rec["tflops"] = round(fl / (avg * 1e-3) / 1e12, 1)
+            rec["gbs"] = round(by / (avg * 1e-3) / 1e9, 1)
+        kern[nm] = rec
+    tot = sum(r["ms"] for r in kern.values())
+    for r in kern.values():
+        r["share"] = round(r["ms"] / tot, 4) if tot else None
+    gemms = [nm for nm in kern if nm in work]
+    dom = max(gemms, key=lambda nm: kern[nm]["ms"])
+    fl, by = work[dom]
+    t_dom = kern[dom]["ms"] * 1e-3
+    tensor_time = fl / (peaks["bf16_tflops_sustained"] * 1e12)
+    hbm_time = by / (peaks["hbm_gbs"] * 1e9)
+    if tensor_time >= hbm_time:
+        roof = {"kernel": dom, "bound": "tensor", "achieved": round(fl / t_dom / 1e12, 1),
+                "peak": peaks["bf16_tflops_sustained"], "unit": "TFLOP/s",
+                "peak_kind": f"bf16_tflops_sustained ({peaks['source']})"}
+        algo = fl
+    else:
+        roof = {"kernel": dom, "bound": "hbm", "achieved": round(by / t_dom / 1e9, 1),
+                "peak": peaks["hbm_gbs"], "unit": "GB/s", "peak_kind": f"hbm_gbs ({peaks['source']})"}
+        algo = by
+    roof["frac"] = round(roof["achieved"] / roof["peak"], 4)
+    roof["algorithmic_per_launch"] = algo
+    roof["traffic"] = ncu_traffic(dom, w.name)
+
+    # end to end through the public API with host buffers
+    e2e = run_e2e(w, inp, o, step, args.e2e_steps, ws, fwd_f + bwd_f)
+
+    cpu = None
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        v, dt = time_oracle(w, args.cpu_rows)
+        cpu = {"value": v, "unit": "TFLOP/s", "cores": cpu_cores(), "kind": "oracle",
+               "sample": f"{args.cpu_rows} rows of expert 0, float64 fwd+bwd ({dt:.1f} s)"}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": ws,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 4),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic",
+            "pct_of_bf16_peak": round(100 * per_rank_tf / peaks["bf16_tflops"], 2),
+            "config": {"workload": w.name, "E": w.E, "T": w.T, "top_k": w.k, "d": w.d, "n": w.n,
+                       "act": w.act, "rows": Mrows, "nonempty_experts": inp["E_ne"],
+                       "step": ("grouped_mlp_fwd + grouped_mlp_bwd" if w.routing == "identity"
+                                else "route + permute + fwd + combine + bwd (+ router grad)"),
+                       "l2": "inputs larger than L2 (no flush)", "parallelism": "replicas"},
+            "roofline": roof, "kernels": kern, "cpu_baseline": cpu, "e2e": e2e,
+            "clocks": clocks, "gpu_launches": launches,
+        }
+        print(json.dumps(line), flush=True)
+    barrier(ws)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+def run_e2e(w, inp, o, step, steps, ws, flops):
+    """Same metric through the public API from pinned host buffers: every
+    step copies its inputs host->device and reads its result back."""
+    import torch
+    if w.routing == "identity":
+        names_in = ["x_perm", "dy_perm", "offsets"]
+        out_name = "dx_perm"
+        res = o
+    else:
+        names_in = ["x", "dO", "topk_idx", "probs"]
+        out_name = "dx"
+        res = o
+    host = {nm: torch.empty(inp[nm].shape, dtype=inp[nm].dtype, pin_memory=True)
+            for nm in names_in}
+    for nm in names_in:
+        host[nm].copy_(inp[nm])
+    out_host = torch.empty(res[out_name].shape, dtype=res[out_name].dtype, pin_memory=True)
+    h2d = sum(host[nm].numel() * host[nm].element_size() for nm in names_in)
+    d2h = out_host.numel() * out_host.element_size()
+
+    def e2e_step():
+        for nm in names_in:
+            inp[nm].copy_(host[nm], non_blocking=True)
+        step()
+        out_host.copy_(res[out_name], non_blocking=True)
+
+    e2e_step()
+    torch.cuda.synchronize()
+    barrier(ws)
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s.record()
+    for _ in range(steps):
+        e2e_step()
+    e.record()
+    torch.cuda.synchronize()
+    ms = max_over_ranks(s.elapsed_time(e) / steps, ws)
+    return {"value": round(flops / (ms * 1e-3) / 1e12 * ws, 2), "unit": "TFLOP/s",
+            "ms_per_step": round(ms, 4), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,256 @@
+"""GB300-native dropless MoE expert MLP: Python binding of libmoe.
+
+Argument marshalling only: every step of the path runs in libmoe's CUDA
+kernels (``csrc/``).  PyTorch supplies device memory and the current CUDA
+stream.  There is no CPU fallback: if ``libmoe.so`` is missing or a call
+fails, an exception is raised.
+
+Functions mirror the C ABI in ``include/moe.h``:
+
+    route_offsets      -> moe_route_offsets
+    permute            -> moe_permute
+    unpermute          -> moe_unpermute
+    grouped_mlp_fwd    -> moe_grouped_mlp_fwd
+    grouped_mlp_bwd    -> moe_grouped_mlp_bwd
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+__all__ = [
+    "ACT", "FLAG_SAVE_H", "DEV_BAD_EXPERT", "DEV_OVERFLOW", "DEV_TIMEOUT", "DEV_BAD_OFFSETS",
+    "lib", "lib_path", "version", "last_launch_count", "route_workspace_size", "route_offsets",
+    "permute", "unpermute", "grouped_mlp_fwd", "grouped_mlp_bwd", "MoeError",
+]
+
+ACT = {"swiglu": 0, "geglu": 1, "srelu": 2}
+FLAG_SAVE_H = 1
+DEV_BAD_EXPERT, DEV_OVERFLOW, DEV_TIMEOUT, DEV_BAD_OFFSETS = 1, 2, 4, 8
+_RC = {-1: "MOE_E_NULL", -2: "MOE_E_ALIGN", -3: "MOE_E_SIZE", -4: "MOE_E_ARG",
+       -5: "MOE_E_CUDA", -6: "MOE_E_WORKSPACE"}
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_LIB = None
+
+
+class MoeError(RuntimeError):
+    pass
+
+
+def lib_path() -> str:
+    return os.path.join(_HERE, "libmoe.so")
+
+
+def lib():
+    """The loaded libmoe (raises if it has not been built)."""
+    global _LIB
+    if _LIB is None:
+        p = lib_path()
+        if not os.path.exists(p):
+            raise MoeError(f"{p} is missing: build it with dropless_grouped_gemm_gb300.build.build()")
+        L = ctypes.CDLL(p)
+        vp, i32, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
+        L.moe_version.restype = ctypes.c_char_p
+        L.moe_version.argtypes = []
+        L.moe_last_launch_count.restype = i32
+        L.moe_last_launch_count.argtypes = []
+        L.moe_route_workspace_size.restype = sz
+        L.moe_route_workspace_size.argtypes = [i32, i32, i32]
+        L.moe_route_offsets.restype = i32
+        L.moe_route_offsets.argtypes = [vp, i32, i32, i32, i32, i32, vp, vp, vp, vp, vp, vp, sz,
+                                        vp, vp]
+        L.moe_permute.restype = i32
+        L.moe_permute.argtypes = [vp, vp, vp, i32, i32, i32, i32, vp, vp]
+        L.moe_unpermute.restype = i32
+        L.moe_unpermute.argtypes = [vp, vp, vp, i32, i32, i32, i32, vp, vp, vp, vp]
+        L.moe_grouped_mlp_fwd.restype = i32
+        L.moe_grouped_mlp_fwd.argtypes = [vp, vp, i32, i32, i32, i32, vp, vp, i32, i32, vp, vp, vp,
+                                          vp, vp]
+        L.moe_grouped_mlp_bwd.restype = i32
+        L.moe_grouped_mlp_bwd.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, vp, vp, i32, i32,
+                                          vp, vp, vp, vp, vp, vp]
+        _LIB = L
+    return _LIB
+
+
+def version() -> str:
+    return lib().moe_version().decode()
+
+
+def last_launch_count() -> int:
+    return int(lib().moe_last_launch_count())
+
+
+def _check(rc: int, what: str):
+    if rc != 0:
+        raise MoeError(f"{what} failed: {_RC.get(rc, rc)}")
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream=None):
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _need(t, dtype, name, ndim=None):
+    if t is None:
+        return
+    if not t.is_cuda:
+        raise MoeError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise MoeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise MoeError(f"{name} must be contiguous")
+    if ndim is not None and t.dim() != ndim:
+        raise MoeError(f"{name} must have {ndim} dims")
+
+
+def _err_word(err, device):
+    if err is None:
+        err = torch.zeros(1, dtype=torch.int32, device=device)
+    _need(err, torch.int32, "err")
+    return err
+
+
+def route_workspace_size(T: int, k: int, E: int) -> int:
+    return int(lib().moe_route_workspace_size(T, k, E))
+
+
+def route_offsets(topk_idx: torch.Tensor, E: int, align: int = 1, M_cap: int | None = None,
+                  err: torch.Tensor | None = None, out: dict | None = None,
+                  workspace: torch.Tensor | None = None, stream=None) -> dict:
+    """Routing layout on the device (see moe_route_offsets).  Returns a dict
+    of device tensors: counts, offsets, row_of_pair, pair_of_row, true_total,
+    err."""
+    _need(topk_idx, torch.int32, "topk_idx", 2)
+    T, k = topk_idx.shape
+    if M_cap is None:
+        M_cap = T * k + E * (align - 1)
+    dev = topk_idx.device
+    o = out if out is not None else {
+        "counts": torch.empty(E, dtype=torch.int32, device=dev),
+        "offsets": torch.empty(E + 1, dtype=torch.int32, device=dev),
+        "row_of_pair": torch.empty(T * k, dtype=torch.int32, device=dev),
+        "pair_of_row": torch.empty(M_cap, dtype=torch.int32, device=dev),
+        "true_total": torch.empty(1, dtype=torch.int32, device=dev),
+    }
+    o["err"] = _err_word(err if err is not None else o.get("err"), dev)
+    ws_bytes = route_workspace_size(T, k, E)
+    if workspace is None:
+        workspace = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=dev)
+    rc = lib().moe_route_offsets(_ptr(topk_idx), T, k, E, align, M_cap, _ptr(o["counts"]),
+                                 _ptr(o["offsets"]), _ptr(o["row_of_pair"]), _ptr(o["pair_of_row"]),
+                                 _ptr(o["true_total"]), _ptr(workspace), workspace.numel(),
+                                 _ptr(o["err"]), _stream(stream))
+    _check(rc, "moe_route_offsets")
+    return o
+
+
+def permute(src: torch.Tensor, pair_of_row: torch.Tensor, k: int, scale: torch.Tensor | None = None,
+            out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """Expert-major gather (see moe_permute)."""
+    _need(src, torch.bfloat16, "src", 2)
+    _need(pair_of_row, torch.int32, "pair_of_row")
+    _need(scale, torch.float32, "scale")
+    T, d = src.shape
+    M_cap = pair_of_row.numel()
+    if out is None:
+        out = torch.empty((M_cap, d), dtype=torch.bfloat16, device=src.device)
+    _need(out, torch.bfloat16, "out", 2)
+    rc = lib().moe_permute(_ptr(src), _ptr(scale), _ptr(pair_of_row), T, k, d, M_cap, _ptr(out),
+                           _stream(stream))
+    _check(rc, "moe_permute")
+    return out
+
+
+def unpermute(src: torch.Tensor, row_of_pair: torch.Tensor, T: int, k: int,
+              probs: torch.Tensor | None = None, out: torch.Tensor | None = None,
+              dO: torch.Tensor | None = None, dprobs: torch.Tensor | None = None,
+              combine: bool = True, stream=None):
+    """Combine and/or router-score gradient (see moe_unpermute).  Returns
+    (out, dprobs); either may be None."""
+    _need(src, torch.bfloat16, "src", 2)
+    _need(row_of_pair, torch.int32, "row_of_pair")
+    _need(probs, torch.float32, "probs")
+    _need(dO, torch.bfloat16, "dO")
+    d = src.shape[1]
+    if combine and out is None:
+        out = torch.empty((T, d), dtype=torch.bfloat16, device=src.device)
+    if not combine:
+        out = None
+    if dO is not None and dprobs is None:
+        dprobs = torch.empty((T, k), dtype=torch.float32, device=src.device)
+    _need(out, torch.bfloat16, "out")
+    _need(dprobs, torch.float32, "dprobs")
+    rc = lib().moe_unpermute(_ptr(src), _ptr(probs), _ptr(row_of_pair), T, k, d, src.shape[0],
+                             _ptr(out),
+                             _ptr(dO), _ptr(dprobs), _stream(stream))
+    _check(rc, "moe_unpermute")
+    return out, dprobs
+
+
+def grouped_mlp_fwd(x_perm: torch.Tensor, offsets: torch.Tensor, W1: torch.Tensor,
+                    W2: torch.Tensor, act: str = "swiglu", save_h: bool = False,
+                    h_saved: torch.Tensor | None = None, a: torch.Tensor | None = None,
+                    y_perm: torch.Tensor | None = None, err: torch.Tensor | None = None,
+                    stream=None):
+    """Grouped expert MLP forward (see moe_grouped_mlp_fwd).  Returns
+    (h_saved or None, a, y_perm, err)."""
+    _need(x_perm, torch.bfloat16, "x_perm", 2)
+    _need(offsets, torch.int32, "offsets", 1)
+    _need(W1, torch.bfloat16, "W1", 3)
+    _need(W2, torch.bfloat16, "W2", 3)
+    M_cap, d = x_perm.shape
+    E, n, d2 = W2.shape
+    n1 = n if act == "srelu" else 2 * n
+    if d2 != d or tuple(W1.shape) != (E, d, n1) or offsets.numel() != E + 1:
+        raise MoeError("inconsistent shapes")
+    dev = x_perm.device
+    if save_h and h_saved is None:
+        h_saved = torch.empty((M_cap, n1), dtype=torch.bfloat16, device=dev)
+    if a is None:
+        a = torch.empty((M_cap, n), dtype=torch.bfloat16, device=dev)
+    if y_perm is None:
+        y_perm = torch.empty((M_cap, d), dtype=torch.bfloat16, device=dev)
+    err = _err_word(err, dev)
+    rc = lib().moe_grouped_mlp_fwd(_ptr(x_perm), _ptr(offsets), E, M_cap, d, n, _ptr(W1), _ptr(W2),
+                                   ACT[act], FLAG_SAVE_H if save_h else 0,
+                                   _ptr(h_saved) if save_h else None, _ptr(a), _ptr(y_perm),
+                                   _ptr(err), _stream(stream))
+    _check(rc, "moe_grouped_mlp_fwd")
+    return (h_saved if save_h else None), a, y_perm, err
+
+
+def grouped_mlp_bwd(x_perm, h_saved, a, dy_perm, offsets, W1, W2, act: str = "swiglu",
+                    dh=None, dx_perm=None, dW1=None, dW2=None, err=None, stream=None):
+    """Grouped expert MLP backward (see moe_grouped_mlp_bwd).  Returns
+    (dh, dx_perm, dW1, dW2, err)."""
+    for t, nm in ((x_perm, "x_perm"), (h_saved, "h_saved"), (a, "a"), (dy_perm, "dy_perm"),
+                  (W1, "W1"), (W2, "W2")):
+        _need(t, torch.bfloat16, nm)
+    _need(offsets, torch.int32, "offsets", 1)
+    M_cap, d = x_perm.shape
+    E, n, _ = W2.shape
+    n1 = n if act == "srelu" else 2 * n
+    dev = x_perm.device
+    if dh is None:
+        dh = torch.empty((M_cap, n1), dtype=torch.bfloat16, device=dev)
+    if dx_perm is None:
+        dx_perm = torch.empty((M_cap, d), dtype=torch.bfloat16, device=dev)
+    if dW1 is None:
+        dW1 = torch.empty((E, d, n1), dtype=torch.bfloat16, device=dev)
+    if dW2 is None:
+        dW2 = torch.empty((E, n, d), dtype=torch.bfloat16, device=dev)
+    err = _err_word(err, dev)
+    rc = lib().moe_grouped_mlp_bwd(_ptr(x_perm), _ptr(h_saved), _ptr(a), _ptr(dy_perm),
+                                   _ptr(offsets), E, M_cap, d, n, _ptr(W1), _ptr(W2), ACT[act], 0,
+                                   _ptr(dh), _ptr(dx_perm), _ptr(dW1), _ptr(dW2), _ptr(err),
+                                   _stream(stream))
+    _check(rc, "moe_grouped_mlp_bwd")
+    return dh, dx_perm, dW1, dW2, err

@@ -1,0 +1,302 @@
+// api.cu - the extern "C" entry points of libmoe (declared in include/moe.h):
+// host-side argument checks, TMA tensor-map encoding, launch sequencing.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <cstdint>
+#include <mutex>
+
+#include "../../include/moe.h"
+#include "gemm.cuh"
+#include "route.cuh"
+
+namespace {
+
+thread_local int g_last_launches = 0;
+thread_local cudaEvent_t const* g_events = nullptr;
+thread_local int g_events_n = 0;
+thread_local int g_events_used = 0;
+
+// measurement hook: events around one launch (or one whole call)
+void ev_begin(cudaStream_t s) {
+  if (g_events && g_events_used + 1 < g_events_n) cudaEventRecord(g_events[g_events_used], s);
+}
+void ev_end(cudaStream_t s) {
+  if (g_events && g_events_used + 1 < g_events_n) {
+    cudaEventRecord(g_events[g_events_used + 1], s);
+    g_events_used += 2;
+  }
+}
+cudaError_t gemm(moe::GemmKind kind, int act, const CUtensorMap& ta, const CUtensorMap& tb,
+                 const moe::GemmArgs& g, int sms, cudaStream_t s) {
+  ev_begin(s);
+  const cudaError_t e = moe::launch_grouped_gemm(kind, act, ta, tb, g, sms, s);
+  ev_end(s);
+  return e;
+}
+
+bool misaligned(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) != 0; }
+
+int num_sms_current() {
+  static int cache[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return -1;
+  if (dev < 64 && cache[dev] > 0) return cache[dev];
+  int n = 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return -1;
+  if (dev < 64) cache[dev] = n;
+  return n;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// bf16 tensor map, 128-byte swizzle; dims/box listed innermost first.
+bool make_map(CUtensorMap* m, const void* base, int rank, const uint64_t* dims,
+              const uint32_t* box) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t gdim[3], gstride[2];
+  cuuint32_t bdim[3], estr[3] = {1, 1, 1};
+  uint64_t stride = 2;
+  for (int i = 0; i < rank; ++i) {
+    gdim[i] = dims[i];
+    bdim[i] = box[i];
+    if (i > 0) gstride[i - 1] = stride;
+    stride *= dims[i];
+  }
+  const CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(base), gdim,
+                        gstride, bdim, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+// [rows, cols] activation matrix, box (64 cols) x (box_rows rows)
+bool map_act(CUtensorMap* m, const void* p, int rows, int cols, int box_rows) {
+  const uint64_t dims[2] = {static_cast<uint64_t>(cols), static_cast<uint64_t>(rows)};
+  const uint32_t box[2] = {64, static_cast<uint32_t>(box_rows)};
+  return make_map(m, p, 2, dims, box);
+}
+// [E, rows, cols] weights, box (64 cols) x (box_rows rows) x 1
+bool map_w(CUtensorMap* m, const void* p, int E, int rows, int cols, int box_rows) {
+  const uint64_t dims[3] = {static_cast<uint64_t>(cols), static_cast<uint64_t>(rows),
+                            static_cast<uint64_t>(E)};
+  const uint32_t box[3] = {64, static_cast<uint32_t>(box_rows), 1};
+  return make_map(m, p, 3, dims, box);
+}
+
+int cuda_rc(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_E_CUDA; }
+
+int check_mlp_sizes(int E, int M_cap, int d, int n) {
+  if (E < 1 || E > MOE_MAX_EXPERTS) return MOE_E_SIZE;
+  if (M_cap < 0 || d <= 0 || n <= 0 || d % 64 || n % 64) return MOE_E_SIZE;
+  if (static_cast<long long>(M_cap) * 2 * n >= (1LL << 40)) return MOE_E_SIZE;
+  return MOE_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* moe_version(void) { return "libmoe 0.1.0 (sm_103a, tcgen05/TMA grouped GEMM)"; }
+
+int moe_last_launch_count(void) { return g_last_launches; }
+
+int moe_set_launch_events(void* const* events, int n) {
+  g_events = reinterpret_cast<cudaEvent_t const*>(events);
+  g_events_n = (events && n > 0) ? n : 0;
+  if (!g_events_n) g_events = nullptr;
+  g_events_used = 0;
+  return MOE_OK;
+}
+
+int moe_launch_events_used(void) { return g_events_used; }
+
+size_t moe_route_workspace_size(int T, int k, int E) {
+  if (T < 0 || k < 1 || E < 1) return 0;
+  return moe::route_workspace_bytes(T, k, E);
+}
+
+int moe_route_offsets(const int32_t* topk_idx, int T, int k, int E, int align, int M_cap,
+                      int32_t* counts, int32_t* offsets, int32_t* row_of_pair,
+                      int32_t* pair_of_row, int32_t* true_total, void* workspace,
+                      size_t ws_bytes, int32_t* err, void* stream) {
+  g_last_launches = 0;
+  if (T < 0 || k < 1 || E < 1 || E > MOE_MAX_EXPERTS || k > E || align < 1 || align > 4096 ||
+      M_cap < 0)
+    return MOE_E_SIZE;
+  if (static_cast<long long>(T) * k + static_cast<long long>(E) * align >= (1LL << 31))
+    return MOE_E_SIZE;
+  if (!counts || !offsets || !true_total || !err) return MOE_E_NULL;
+  if (T > 0 && (!topk_idx || !row_of_pair)) return MOE_E_NULL;
+  if (M_cap > 0 && !pair_of_row) return MOE_E_NULL;
+  if (ws_bytes < moe::route_workspace_bytes(T, k, E)) return MOE_E_WORKSPACE;
+  if (!workspace) return MOE_E_NULL;
+  const int sms = num_sms_current();
+  if (sms <= 0) return MOE_E_CUDA;
+  int launches = 0;
+  ev_begin(static_cast<cudaStream_t>(stream));
+  const cudaError_t e = moe::launch_route(topk_idx, T, k, E, align, M_cap, counts, offsets,
+                                          row_of_pair, pair_of_row, true_total, workspace, err,
+                                          sms, static_cast<cudaStream_t>(stream), &launches);
+  ev_end(static_cast<cudaStream_t>(stream));
+  g_last_launches = launches;
+  return cuda_rc(e);
+}
+
+int moe_permute(const moe_bf16* src, const float* scale, const int32_t* pair_of_row, int T, int k,
+                int d, int M_cap, moe_bf16* dst, void* stream) {
+  g_last_launches = 0;
+  if (T < 0 || k < 1 || d <= 0 || d % 64 || M_cap < 0) return MOE_E_SIZE;
+  if (M_cap == 0) return MOE_OK;
+  if (!pair_of_row || !dst || (T > 0 && !src)) return MOE_E_NULL;
+  if (misaligned(src) || misaligned(dst)) return MOE_E_ALIGN;
+  const int sms = num_sms_current();
+  if (sms <= 0) return MOE_E_CUDA;
+  ev_begin(static_cast<cudaStream_t>(stream));
+  const cudaError_t e = moe::launch_permute(src, scale, pair_of_row, T, k, d, M_cap, dst, sms,
+                                            static_cast<cudaStream_t>(stream));
+  ev_end(static_cast<cudaStream_t>(stream));
+  g_last_launches = 1;
+  return cuda_rc(e);
+}
+
+int moe_unpermute(const moe_bf16* src, const float* probs, const int32_t* row_of_pair, int T,
+                  int k, int d, int M_cap, moe_bf16* dst, const moe_bf16* dO, float* dprobs,
+                  void* stream) {
+  g_last_launches = 0;
+  if (T < 0 || k < 1 || d <= 0 || d % 64 || M_cap < 0) return MOE_E_SIZE;
+  if (T == 0) return MOE_OK;
+  if (!src || !row_of_pair) return MOE_E_NULL;
+  if (!dst && !dprobs) return MOE_E_NULL;
+  if (dprobs && !dO) return MOE_E_NULL;
+  if (misaligned(src) || misaligned(dst) || misaligned(dO)) return MOE_E_ALIGN;
+  const int sms = num_sms_current();
+  if (sms <= 0) return MOE_E_CUDA;
+  int launches = 0;
+  ev_begin(static_cast<cudaStream_t>(stream));
+  const cudaError_t e = moe::launch_unpermute(src, probs, row_of_pair, T, k, d, M_cap, dst, dO,
+                                              dprobs, sms, static_cast<cudaStream_t>(stream),
+                                              &launches);
+  ev_end(static_cast<cudaStream_t>(stream));
+  g_last_launches = launches;
+  return cuda_rc(e);
+}
+
+int moe_grouped_mlp_fwd(const moe_bf16* x_perm, const int32_t* offsets, int E, int M_cap, int d,
+                        int n, const moe_bf16* W1, const moe_bf16* W2, int act, int flags,
+                        moe_bf16* h_saved, moe_bf16* a, moe_bf16* y_perm, int32_t* err,
+                        void* stream) {
+  g_last_launches = 0;
+  int rc = check_mlp_sizes(E, M_cap, d, n);
+  if (rc) return rc;
+  if (act < MOE_ACT_SWIGLU || act > MOE_ACT_SRELU || (flags & ~MOE_FLAG_SAVE_H)) return MOE_E_ARG;
+  const bool save_h = flags & MOE_FLAG_SAVE_H;
+  if (!offsets || !W1 || !W2 || !err) return MOE_E_NULL;
+  if (M_cap == 0) return MOE_OK;
+  if (!x_perm || !a || !y_perm || (save_h && !h_saved)) return MOE_E_NULL;
+  if (misaligned(x_perm) || misaligned(W1) || misaligned(W2) || misaligned(a) ||
+      misaligned(y_perm) || (save_h && misaligned(h_saved)))
+    return MOE_E_ALIGN;
+  const int n1 = (act == MOE_ACT_SRELU) ? n : 2 * n;
+  const int sms = num_sms_current();
+  if (sms <= 0) return MOE_E_CUDA;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  CUtensorMap tx, tw1, ta, tw2;
+  if (!map_act(&tx, x_perm, M_cap, d, moe::kBM) || !map_w(&tw1, W1, E, d, n1, 64) ||
+      !map_act(&ta, a, M_cap, n, moe::kBM) || !map_w(&tw2, W2, E, n, d, 64))
+    return MOE_E_CUDA;
+  moe::GemmArgs g1{};
+  g1.offsets = offsets; g1.E = E; g1.M_cap = M_cap; g1.K = d; g1.N = n1; g1.R = 0;
+  g1.out = a; g1.ldo = n; g1.out2 = save_h ? h_saved : nullptr; g1.ldo2 = n1; g1.err = err;
+  cudaError_t e = gemm(moe::GemmKind::kFc1Act, act, tx, tw1, g1, sms, s);
+  if (e != cudaSuccess) return MOE_E_CUDA;
+  moe::GemmArgs g2{};
+  g2.offsets = offsets; g2.E = E; g2.M_cap = M_cap; g2.K = n; g2.N = d; g2.R = 0;
+  g2.out = y_perm; g2.ldo = d; g2.err = err;
+  e = gemm(moe::GemmKind::kFc2, 0, ta, tw2, g2, sms, s);
+  if (e != cudaSuccess) return MOE_E_CUDA;
+  g_last_launches = 2;
+  return MOE_OK;
+}
+
+int moe_grouped_mlp_bwd(const moe_bf16* x_perm, const moe_bf16* h_saved, const moe_bf16* a,
+                        const moe_bf16* dy_perm, const int32_t* offsets, int E, int M_cap, int d,
+                        int n, const moe_bf16* W1, const moe_bf16* W2, int act, int flags,
+                        moe_bf16* dh, moe_bf16* dx_perm, moe_bf16* dW1, moe_bf16* dW2,
+                        int32_t* err, void* stream) {
+  g_last_launches = 0;
+  int rc = check_mlp_sizes(E, M_cap, d, n);
+  if (rc) return rc;
+  if (act < MOE_ACT_SWIGLU || act > MOE_ACT_SRELU || flags != 0) return MOE_E_ARG;
+  if (!offsets || !W1 || !W2 || !dW1 || !dW2 || !err) return MOE_E_NULL;
+  const int n1 = (act == MOE_ACT_SRELU) ? n : 2 * n;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (M_cap == 0) {
+    // no rows at all: the weight gradients are exactly zero
+    cudaError_t e = cudaMemsetAsync(dW1, 0, static_cast<size_t>(E) * d * n1 * 2, s);
+    if (e == cudaSuccess) e = cudaMemsetAsync(dW2, 0, static_cast<size_t>(E) * n * d * 2, s);
+    return cuda_rc(e);
+  }
+  if (!x_perm || !h_saved || !a || !dy_perm || !dh || !dx_perm) return MOE_E_NULL;
+  if (misaligned(x_perm) || misaligned(h_saved) || misaligned(a) || misaligned(dy_perm) ||
+      misaligned(dh) || misaligned(dx_perm) || misaligned(dW1) || misaligned(dW2) ||
+      misaligned(W1) || misaligned(W2))
+    return MOE_E_ALIGN;
+  const int sms = num_sms_current();
+  if (sms <= 0) return MOE_E_CUDA;
+
+  // operand maps
+  CUtensorMap t_dy_k, t_w2_k, t_a_mn, t_dy_mn, t_dh_k, t_w1_k, t_x_mn, t_dh_mn;
+  if (!map_act(&t_dy_k, dy_perm, M_cap, d, moe::kBM) ||      // FC2-dgrad A (K = d)
+      !map_w(&t_w2_k, W2, E, n, d, moe::kBN) ||               // FC2-dgrad B rows = n
+      !map_act(&t_a_mn, a, M_cap, n, 64) ||                   // FC2-wgrad A (MN = n)
+      !map_act(&t_dy_mn, dy_perm, M_cap, d, 64) ||            // FC2-wgrad B (MN = d)
+      !map_act(&t_dh_k, dh, M_cap, n1, moe::kBM) ||           // FC1-dgrad A (K = n1)
+      !map_w(&t_w1_k, W1, E, d, n1, moe::kBN) ||              // FC1-dgrad B rows = d
+      !map_act(&t_x_mn, x_perm, M_cap, d, 64) ||              // FC1-wgrad A (MN = d)
+      !map_act(&t_dh_mn, dh, M_cap, n1, 64))                  // FC1-wgrad B (MN = n1)
+    return MOE_E_CUDA;
+
+  // 1. dH = act'(H; dY W2^T)
+  moe::GemmArgs g{};
+  g.offsets = offsets; g.E = E; g.M_cap = M_cap; g.K = d; g.N = n;
+  g.out = dh; g.ldo = n1; g.aux = h_saved; g.ld_aux = n1; g.err = err;
+  cudaError_t e = gemm(moe::GemmKind::kDgradAct, act, t_dy_k, t_w2_k, g, sms, s);
+  if (e != cudaSuccess) return MOE_E_CUDA;
+  // 2. dW2_e = A_e^T dY_e
+  moe::GemmArgs gw2{};
+  gw2.offsets = offsets; gw2.E = E; gw2.M_cap = M_cap; gw2.N = d; gw2.R = n;
+  gw2.out = dW2; gw2.ldo = d; gw2.out_estride = static_cast<long long>(n) * d; gw2.err = err;
+  e = gemm(moe::GemmKind::kWgrad, 0, t_a_mn, t_dy_mn, gw2, sms, s);
+  if (e != cudaSuccess) return MOE_E_CUDA;
+  // 3. dX = dH W1^T
+  moe::GemmArgs gd{};
+  gd.offsets = offsets; gd.E = E; gd.M_cap = M_cap; gd.K = n1; gd.N = d;
+  gd.out = dx_perm; gd.ldo = d; gd.err = err;
+  e = gemm(moe::GemmKind::kDgrad, 0, t_dh_k, t_w1_k, gd, sms, s);
+  if (e != cudaSuccess) return MOE_E_CUDA;
+  // 4. dW1_e = X_e^T dH_e
+  moe::GemmArgs gw1{};
+  gw1.offsets = offsets; gw1.E = E; gw1.M_cap = M_cap; gw1.N = n1; gw1.R = d;
+  gw1.out = dW1; gw1.ldo = n1; gw1.out_estride = static_cast<long long>(d) * n1; gw1.err = err;
+  e = gemm(moe::GemmKind::kWgrad, 0, t_x_mn, t_dh_mn, gw1, sms, s);
+  if (e != cudaSuccess) return MOE_E_CUDA;
+  g_last_launches = 4;
+  return MOE_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,510 @@
+// gemm.cu - persistent grouped GEMM over ragged expert groups (sm_103a).
+//
+// One kernel template covers the six contractions of the expert MLP:
+//   FC1 + activation, FC2, FC2-dgrad + dActivation, FC1-dgrad (ragged rows)
+//   and the two weight gradients (ragged reduction).
+// [TE] "최적화 1: grouped GEMM": one launch over all experts with their real
+// row counts; counts/offsets are read on the device, so nothing is copied to
+// the host.  [CuTe] "핵심 아이디어": the GLU is applied in the epilogue.
+// [Sonic] "IO 숨기기" / "GEMM Overlapping": warp specialisation (producer,
+// MMA, epilogue) and software pipelining hide the epilogue's IO.
+//
+// Roles (192 threads, one CTA per SM, persistent over a static tile order):
+//   warp 0     TMA producer (one lane): 4-stage ring of 48 KB stages
+//   warp 1     TMEM owner + MMA issuer (one lane): tcgen05.mma 128x256x16
+//   warps 2-5  epilogue: tcgen05.ld (warp w reads TMEM lanes 32*(w%4)..),
+//              activation / derivative math, stores to global
+// Two 256-column fp32 accumulators in TMEM let tile i+1's MMAs overlap
+// tile i's epilogue.
+#include <cuda_runtime.h>
+
+#include "gemm.cuh"
+#include "ptx.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int BM = kBM, BN = kBN, BK = kBK, UK = 16;
+constexpr int STAGES = 4;
+constexpr int A_BYTES = BM * BK * 2;  // 16 KB
+constexpr int B_BYTES = BN * BK * 2;  // 32 KB
+constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr int MN_BOX_BYTES = 64 * BK * 2;  // one 64(MN) x 64(K) box: 8 KB
+constexpr int NUM_THREADS = 192;
+constexpr int TMEM_COLS = 2 * BN;
+
+constexpr size_t smem_bytes(int E) {
+  return 1024 /*align slack*/ + static_cast<size_t>(STAGES) * STAGE_BYTES +
+         (2 * STAGES + 5) * 8 /*barriers*/ + 16 + 2 * (E + 1) * 4 /*scheduler*/;
+}
+
+// ------------------------------------------------------------ activations
+__device__ __forceinline__ float sigmoidf_(float g) { return 1.0f / (1.0f + __expf(-g)); }
+constexpr float kGeluC = 0.7978845608028654f;  // sqrt(2/pi)
+constexpr float kGeluA = 0.044715f;
+
+template <int ACT>
+__device__ __forceinline__ float gate_phi(float g) {
+  if constexpr (ACT == MOE_ACT_SWIGLU) {
+    return g * sigmoidf_(g);
+  } else {
+    const float z = kGeluC * (g + kGeluA * g * g * g);
+    return 0.5f * g * (1.0f + tanhf(z));
+  }
+}
+// phi and phi' together
+template <int ACT>
+__device__ __forceinline__ void gate_phi_dphi(float g, float& ph, float& dph) {
+  if constexpr (ACT == MOE_ACT_SWIGLU) {
+    const float s = sigmoidf_(g);
+    ph = g * s;
+    dph = s * (1.0f + g * (1.0f - s));
+  } else {
+    const float z = kGeluC * (g + kGeluA * g * g * g);
+    const float th = tanhf(z);
+    ph = 0.5f * g * (1.0f + th);
+    dph = 0.5f * (1.0f + th) + 0.5f * g * (1.0f - th * th) * kGeluC * (1.0f + 3.0f * kGeluA * g * g);
+  }
+}
+
+// ------------------------------------------------------------ scheduling
+struct Tile {
+  int e;
+  int row0;     // ragged-row kinds: first global row of the tile
+  int rows;     // ragged-row kinds: valid rows in the tile
+  int m0;       // kWgrad: first output row (within the expert)
+  int n0;       // first output column
+  int kblocks;  // BK-blocks of the reduction
+  int krow0;    // kWgrad: first row of the reduction (global)
+  int klast;    // kWgrad: valid rows in the last reduction block
+};
+
+template <GemmKind KIND>
+__device__ __forceinline__ int tiles_of_expert(const GemmArgs& g, const int* s_off, int e) {
+  const int nt = (g.N + BN - 1) / BN;
+  if constexpr (KIND == GemmKind::kWgrad) {
+    return ((g.R + BM - 1) / BM) * nt;
+  } else {
+    const int rows = s_off[e + 1] - s_off[e];
+    return ((rows + BM - 1) / BM) * nt;
+  }
+}
+
+template <GemmKind KIND>
+__device__ __forceinline__ Tile decode_tile(const GemmArgs& g, const int* s_off,
+                                            const int* s_ts, int t) {
+  // expert e with s_ts[e] <= t < s_ts[e+1]
+  int lo = 0, hi = g.E - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi) >> 1;
+    if (s_ts[mid + 1] <= t) lo = mid + 1;
+    else hi = mid;
+  }
+  Tile tl;
+  tl.e = lo;
+  const int local = t - s_ts[lo];
+  const int nt = (g.N + BN - 1) / BN;
+  const int mi = local / nt;
+  tl.n0 = (local - mi * nt) * BN;
+  if constexpr (KIND == GemmKind::kWgrad) {
+    tl.m0 = mi * BM;
+    tl.krow0 = s_off[lo];
+    const int kr = s_off[lo + 1] - s_off[lo];
+    tl.kblocks = (kr + BK - 1) / BK;
+    tl.klast = kr - (tl.kblocks - 1) * BK;
+    tl.row0 = 0;
+    tl.rows = 0;
+  } else {
+    tl.row0 = s_off[lo] + mi * BM;
+    tl.rows = min(BM, s_off[lo + 1] - tl.row0);
+    tl.kblocks = g.K / BK;
+    tl.m0 = 0;
+    tl.krow0 = 0;
+    tl.klast = BK;
+  }
+  return tl;
+}
+
+// ------------------------------------------------------------ epilogues
+__device__ __forceinline__ void st_global_v4(uint16_t* p, uint32_t a, uint32_t b, uint32_t c,
+                                             uint32_t d) {
+  *reinterpret_cast<uint4*>(p) = make_uint4(a, b, c, d);
+}
+
+// 32 fp32 accumulator columns -> 32 bf16 at p (64 bytes)
+__device__ __forceinline__ void store_row32(uint16_t* p, const uint32_t (&r)[32]) {
+#pragma unroll
+  for (int v = 0; v < 4; ++v) {
+    st_global_v4(p + 8 * v, pack_bf16x2(__uint_as_float(r[8 * v + 0]), __uint_as_float(r[8 * v + 1])),
+                 pack_bf16x2(__uint_as_float(r[8 * v + 2]), __uint_as_float(r[8 * v + 3])),
+                 pack_bf16x2(__uint_as_float(r[8 * v + 4]), __uint_as_float(r[8 * v + 5])),
+                 pack_bf16x2(__uint_as_float(r[8 * v + 6]), __uint_as_float(r[8 * v + 7])));
+  }
+}
+
+template <GemmKind KIND, int ACT>
+__device__ __forceinline__ void epilogue_chunk(const GemmArgs& g, const Tile& tl, int row_in_tile,
+                                               int c, const uint32_t (&r)[32]) {
+  const int col = tl.n0 + c * 32;  // first accumulator column of the chunk
+  if (col >= g.N) return;
+  if constexpr (KIND == GemmKind::kWgrad) {
+    const int orow = tl.m0 + row_in_tile;
+    if (orow >= g.R) return;
+    uint16_t* p = g.out + static_cast<long long>(tl.e) * g.out_estride + orow * g.ldo + col;
+    store_row32(p, r);
+  } else {
+    if (row_in_tile >= tl.rows) return;
+    const long long grow = tl.row0 + row_in_tile;
+    if constexpr (KIND == GemmKind::kFc1Act) {
+      if (g.out2) store_row32(g.out2 + grow * g.ldo2 + col, r);
+      if constexpr (ACT == MOE_ACT_SRELU) {
+        uint32_t o[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const float h0 = fmaxf(__uint_as_float(r[2 * i]), 0.f);
+          const float h1 = fmaxf(__uint_as_float(r[2 * i + 1]), 0.f);
+          o[i] = pack_bf16x2(h0 * h0, h1 * h1);
+        }
+        uint16_t* p = g.out + grow * g.ldo + col;
+#pragma unroll
+        for (int v = 0; v < 4; ++v) st_global_v4(p + 8 * v, o[4 * v], o[4 * v + 1], o[4 * v + 2], o[4 * v + 3]);
+      } else {
+        uint32_t o[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const float a0 = gate_phi<ACT>(__uint_as_float(r[4 * i + 0])) * __uint_as_float(r[4 * i + 1]);
+          const float a1 = gate_phi<ACT>(__uint_as_float(r[4 * i + 2])) * __uint_as_float(r[4 * i + 3]);
+          o[i] = pack_bf16x2(a0, a1);
+        }
+        uint16_t* p = g.out + grow * g.ldo + col / 2;
+        st_global_v4(p, o[0], o[1], o[2], o[3]);
+        st_global_v4(p + 8, o[4], o[5], o[6], o[7]);
+      }
+    } else if constexpr (KIND == GemmKind::kDgradAct) {
+      if constexpr (ACT == MOE_ACT_SRELU) {
+        const uint16_t* hp = g.aux + grow * g.ld_aux + col;
+        uint16_t* p = g.out + grow * g.ldo + col;
+#pragma unroll
+        for (int v = 0; v < 4; ++v) {
+          const uint4 hv = *reinterpret_cast<const uint4*>(hp + 8 * v);
+          const uint32_t hw[4] = {hv.x, hv.y, hv.z, hv.w};
+          uint32_t o[4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const float d0 = __uint_as_float(r[8 * v + 2 * i]);
+            const float d1 = __uint_as_float(r[8 * v + 2 * i + 1]);
+            o[i] = pack_bf16x2(2.f * fmaxf(bf16_lo(hw[i]), 0.f) * d0,
+                               2.f * fmaxf(bf16_hi(hw[i]), 0.f) * d1);
+          }
+          st_global_v4(p + 8 * v, o[0], o[1], o[2], o[3]);
+        }
+      } else {
+        // dA columns j = col..col+31 -> H / dH columns 2j, 2j+1
+        const uint16_t* hp = g.aux + grow * g.ld_aux + 2 * col;
+        uint16_t* p = g.out + grow * g.ldo + 2 * col;
+#pragma unroll
+        for (int v = 0; v < 8; ++v) {
+          const uint4 hv = *reinterpret_cast<const uint4*>(hp + 8 * v);
+          const uint32_t hw[4] = {hv.x, hv.y, hv.z, hv.w};  // (g,u) pairs
+          uint32_t o[4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const float gg = bf16_lo(hw[i]);
+            const float uu = bf16_hi(hw[i]);
+            const float da = __uint_as_float(r[4 * v + i]);
+            float ph, dph;
+            gate_phi_dphi<ACT>(gg, ph, dph);
+            o[i] = pack_bf16x2(da * uu * dph, da * ph);
+          }
+          st_global_v4(p + 8 * v, o[0], o[1], o[2], o[3]);
+        }
+      }
+    } else {  // kFc2, kDgrad
+      store_row32(g.out + grow * g.ldo + col, r);
+    }
+  }
+}
+
+// ------------------------------------------------------------ the kernel
+template <GemmKind KIND, int ACT>
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+    grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
+                        const __grid_constant__ CUtensorMap tmB, const GemmArgs g) {
+  constexpr bool A_MN = (KIND == GemmKind::kWgrad);
+  constexpr bool B_MN = (KIND == GemmKind::kFc1Act || KIND == GemmKind::kFc2 ||
+                         KIND == GemmKind::kWgrad);
+  constexpr bool B_3D = (KIND != GemmKind::kWgrad);
+  constexpr uint32_t IDESC = idesc_bf16(BM, BN, A_MN, B_MN);
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
+  uint64_t* empty_bar = full_bar + STAGES;
+  uint64_t* tfull_bar = empty_bar + STAGES;
+  uint64_t* tempty_bar = tfull_bar + 2;
+  uint64_t* drain_bar = tempty_bar + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain_bar + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  int* s_off = reinterpret_cast<int*>(tmem_slot + 4);
+  int* s_ts = s_off + (g.E + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < STAGES; ++i) {
+      mbar_init(&full_bar[i], 1);
+      mbar_init(&empty_bar[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&tfull_bar[i], 1);
+      mbar_init(&tempty_bar[i], 4);
+    }
+    mbar_init(drain_bar, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+    prefetch_tmap(&tmA);
+    prefetch_tmap(&tmB);
+  }
+  if (warp == 1) tmem_alloc(tmem_slot, TMEM_COLS);
+  if (warp == 2) {
+    // offsets -> smem, made safe: non-decreasing and within [0, M_cap]
+    bool bad = false;
+    for (int i = lane; i <= g.E; i += 32) {
+      int v = g.offsets[i];
+      if (v < 0 || v > g.M_cap) bad = true;
+      s_off[i] = min(max(v, 0), g.M_cap);
+    }
+    __syncwarp();
+    if (lane == 0) {
+      int prev = 0;
+      for (int i = 0; i <= g.E; ++i) {
+        if (s_off[i] < prev) { bad = true; s_off[i] = prev; }
+        prev = s_off[i];
+      }
+      if (s_off[0] != 0) bad = true;
+    }
+    if (__any_sync(0xffffffffu, bad) && lane == 0 && blockIdx.x == 0) set_err(g.err, MOE_DEV_BAD_OFFSETS);
+    __syncwarp();
+    // exclusive prefix of per-expert tile counts (warp scan, 32 experts a step)
+    int carry = 0;
+    for (int base = 0; base < g.E; base += 32) {
+      const int e = base + lane;
+      const int t = (e < g.E) ? tiles_of_expert<KIND>(g, s_off, e) : 0;
+      int v = t;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, v, o);
+        if (lane >= o) v += y;
+      }
+      if (e < g.E) s_ts[e] = carry + v - t;
+      carry += __shfl_sync(0xffffffffu, v, 31);
+    }
+    if (lane == 0) s_ts[g.E] = carry;
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+
+  const uint32_t tmem_base = *tmem_slot;
+  const int total_tiles = s_ts[g.E];
+
+  if (warp == 0) {
+    // ---------------------------------------------------------- producer
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t issued_parity[STAGES];
+      bool issued[STAGES];
+      for (int i = 0; i < STAGES; ++i) { issued[i] = false; issued_parity[i] = 0; }
+      bool ok = true;
+      for (int t = blockIdx.x; t < total_tiles && ok; t += gridDim.x) {
+        const Tile tl = decode_tile<KIND>(g, s_off, s_ts, t);
+        for (int kb = 0; kb < tl.kblocks; ++kb) {
+          if (!mbar_wait(&empty_bar[stage], phase ^ 1, abort_flag)) { ok = false; break; }
+          uint8_t* sa = smem + stage * STAGE_BYTES;
+          uint8_t* sb = sa + A_BYTES;
+          uint64_t* fb = &full_bar[stage];
+          mbar_arrive_expect_tx(fb, STAGE_BYTES);
+          if constexpr (A_MN) {
+            const int kr = tl.krow0 + kb * BK;
+            tma_load_2d(sa, &tmA, fb, tl.m0, kr);
+            tma_load_2d(sa + MN_BOX_BYTES, &tmA, fb, tl.m0 + 64, kr);
+          } else {
+            tma_load_2d(sa, &tmA, fb, kb * BK, tl.row0);
+          }
+          if constexpr (B_MN) {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              if constexpr (B_3D) tma_load_3d(sb + i * MN_BOX_BYTES, &tmB, fb, tl.n0 + 64 * i, kb * BK, tl.e);
+              else tma_load_2d(sb + i * MN_BOX_BYTES, &tmB, fb, tl.n0 + 64 * i, tl.krow0 + kb * BK);
+            }
+          } else {
+            tma_load_3d(sb, &tmB, fb, kb * BK, tl.n0, tl.e);
+          }
+          issued[stage] = true;
+          issued_parity[stage] = phase;
+          if (++stage == STAGES) { stage = 0; phase ^= 1; }
+        }
+      }
+      if (!ok) {
+        // give up: wait (bounded) for our copies in flight before exiting
+        for (int i = 0; i < STAGES; ++i)
+          if (issued[i]) {
+            const uint32_t a = smem_u32(&full_bar[i]);
+            const uint64_t t0 = globaltimer_ns();
+            while (!mbar_try_wait(a, issued_parity[i]) && globaltimer_ns() - t0 < kWaitLimitNs) {}
+          }
+      }
+    }
+  } else if (warp == 1) {
+    // ---------------------------------------------------------- MMA issuer
+    int stage = 0;
+    uint32_t phase = 0;
+    int local = 0;
+    bool ok = true;
+    for (int t = blockIdx.x; t < total_tiles && ok; t += gridDim.x, ++local) {
+      const Tile tl = decode_tile<KIND>(g, s_off, s_ts, t);
+      const int buf = local & 1;
+      const uint32_t aph = (local >> 1) & 1;
+      if (lane == 0) ok = mbar_wait(&tempty_bar[buf], aph ^ 1, abort_flag);
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok) break;
+      tc_fence_after();
+      const uint32_t d_tmem = tmem_base + buf * BN;
+      for (int kb = 0; kb < tl.kblocks; ++kb) {
+        if (lane == 0) ok = mbar_wait(&full_bar[stage], phase, abort_flag);
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (!ok) break;
+        tc_fence_after();
+        uint8_t* sa = smem + stage * STAGE_BYTES;
+        uint8_t* sb = sa + A_BYTES;
+        if constexpr (KIND == GemmKind::kWgrad) {
+          if (kb == tl.kblocks - 1 && tl.klast < BK) {
+            // rows past the expert's end belong to the next expert: zero them
+            // in all six 64x64 boxes (2 of A, 4 of B) before the MMAs read them
+            const int zr = BK - tl.klast;
+            const int units = 6 * zr * 8;  // 16-byte units
+            for (int u = lane; u < units; u += 32) {
+              const int box = u / (zr * 8);
+              const int rem = u - box * (zr * 8);
+              const int row = tl.klast + rem / 8;
+              const int ch = rem & 7;
+              uint8_t* p = (box < 2 ? sa + box * MN_BOX_BYTES : sb + (box - 2) * MN_BOX_BYTES) +
+                           row * 128 + ch * 16;
+              *reinterpret_cast<uint4*>(p) = make_uint4(0, 0, 0, 0);
+            }
+            fence_proxy_async_smem();
+          }
+        }
+        __syncwarp();
+        if (lane == 0) {
+          const uint32_t a0 = smem_u32(sa), b0 = smem_u32(sb);
+#pragma unroll
+          for (int kk = 0; kk < BK / UK; ++kk) {
+            const uint64_t ad = A_MN ? sdesc_sw128(a0 + kk * 2048, MN_BOX_BYTES, 1024)
+                                     : sdesc_sw128(a0 + kk * 32, 16, 1024);
+            const uint64_t bd = B_MN ? sdesc_sw128(b0 + kk * 2048, MN_BOX_BYTES, 1024)
+                                     : sdesc_sw128(b0 + kk * 32, 16, 1024);
+            umma_bf16(d_tmem, ad, bd, IDESC, (kb > 0 || kk > 0) ? 1u : 0u);
+          }
+          umma_commit(&empty_bar[stage]);
+        }
+        __syncwarp();
+        if (++stage == STAGES) { stage = 0; phase ^= 1; }
+      }
+      if (!ok) break;
+      if (lane == 0) umma_commit(&tfull_bar[buf]);
+      __syncwarp();
+    }
+    if (!ok && lane == 0) {
+      // give up: let every MMA already issued finish before TMEM is freed
+      umma_commit(drain_bar);
+      const uint32_t a = smem_u32(drain_bar);
+      const uint64_t t0 = globaltimer_ns();
+      while (!mbar_try_wait(a, 0) && globaltimer_ns() - t0 < kWaitLimitNs) {}
+    }
+    __syncwarp();
+  } else {
+    // ---------------------------------------------------------- epilogue
+    const int q = warp & 3;
+    const int row_in_tile = q * 32 + lane;
+    int local = 0;
+    for (int t = blockIdx.x; t < total_tiles; t += gridDim.x, ++local) {
+      const Tile tl = decode_tile<KIND>(g, s_off, s_ts, t);
+      const int buf = local & 1;
+      const uint32_t aph = (local >> 1) & 1;
+      bool ok = true;
+      if (lane == 0) ok = mbar_wait(&tfull_bar[buf], aph, abort_flag);
+      if (!__shfl_sync(0xffffffffu, ok, 0)) break;
+      tc_fence_after();
+      const uint32_t tb = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + buf * BN;
+      if (KIND == GemmKind::kWgrad && tl.kblocks == 0) {
+        uint32_t z[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) z[i] = 0;
+        for (int c = 0; c < BN / 32; ++c) epilogue_chunk<KIND, ACT>(g, tl, row_in_tile, c, z);
+      } else {
+        for (int c = 0; c < BN / 32; ++c) {
+          uint32_t r[32];
+          tmem_ld32(tb + c * 32, r);
+          tmem_wait_ld();
+          epilogue_chunk<KIND, ACT>(g, tl, row_in_tile, c, r);
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&tempty_bar[buf]);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (*abort_flag && threadIdx.x == 0) set_err(g.err, MOE_DEV_TIMEOUT);
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, TMEM_COLS);
+  }
+}
+
+template <GemmKind KIND, int ACT>
+cudaError_t launch_t(const CUtensorMap& ta, const CUtensorMap& tb, const GemmArgs& g, int num_sms,
+                     cudaStream_t s) {
+  auto kern = grouped_gemm_kernel<KIND, ACT>;
+  const size_t smem = smem_bytes(MOE_MAX_EXPERTS);
+  static bool attr_set = false;  // per process; the library drives one device
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  kern<<<num_sms, NUM_THREADS, smem, s>>>(ta, tb, g);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_grouped_gemm(GemmKind kind, int act, const CUtensorMap& ta,
+                                const CUtensorMap& tb, const GemmArgs& g, int num_sms,
+                                cudaStream_t s) {
+#define MOE_ACT_SWITCH(KIND)                                                         \
+  switch (act) {                                                                     \
+    case MOE_ACT_SWIGLU: return launch_t<KIND, MOE_ACT_SWIGLU>(ta, tb, g, num_sms, s); \
+    case MOE_ACT_GEGLU: return launch_t<KIND, MOE_ACT_GEGLU>(ta, tb, g, num_sms, s);   \
+    case MOE_ACT_SRELU: return launch_t<KIND, MOE_ACT_SRELU>(ta, tb, g, num_sms, s);   \
+    default: return cudaErrorInvalidValue;                                           \
+  }
+  switch (kind) {
+    case GemmKind::kFc1Act: MOE_ACT_SWITCH(GemmKind::kFc1Act)
+    case GemmKind::kDgradAct: MOE_ACT_SWITCH(GemmKind::kDgradAct)
+    case GemmKind::kFc2: return launch_t<GemmKind::kFc2, 0>(ta, tb, g, num_sms, s);
+    case GemmKind::kDgrad: return launch_t<GemmKind::kDgrad, 0>(ta, tb, g, num_sms, s);
+    case GemmKind::kWgrad: return launch_t<GemmKind::kWgrad, 0>(ta, tb, g, num_sms, s);
+  }
+#undef MOE_ACT_SWITCH
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace moe

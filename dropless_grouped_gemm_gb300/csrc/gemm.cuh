@@ -1,0 +1,46 @@
+// gemm.cuh - host-side interface of the grouped GEMM kernels (gemm.cu).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+namespace moe {
+
+// Which contraction a launch performs; fixes the operand majorness and the
+// epilogue.
+enum class GemmKind : int {
+  kFc1Act = 0,    // A = x_perm (K-major), B = W1 (N-major, 3-D); act epilogue
+  kFc2 = 1,       // A = a (K-major),      B = W2 (N-major, 3-D); store
+  kDgradAct = 2,  // A = dy_perm (K-major), B = W2^T (K-major, 3-D); dAct epilogue
+  kDgrad = 3,     // A = dh (K-major),     B = W1^T (K-major, 3-D); store
+  kWgrad = 4,     // A = act^T (M-major),  B = grad (N-major); ragged K
+};
+
+struct GemmArgs {
+  const int32_t* offsets;  // [E+1] device
+  int E;
+  int M_cap;
+  int K;                   // reduction length (ragged-row kinds)
+  int N;                   // output columns
+  int R;                   // output rows per expert (kWgrad)
+  uint16_t* out;           // bf16 output
+  long long ldo;           // output row stride, elements
+  long long out_estride;   // elements between experts' outputs (kWgrad)
+  uint16_t* out2;          // kFc1Act: H (optional)
+  long long ldo2;
+  const uint16_t* aux;     // kDgradAct: saved H
+  long long ld_aux;
+  int32_t* err;
+};
+
+// Launches the persistent grouped GEMM of `kind` (act: MOE_ACT_*) on `s`.
+cudaError_t launch_grouped_gemm(GemmKind kind, int act, const CUtensorMap& ta,
+                                const CUtensorMap& tb, const GemmArgs& args, int num_sms,
+                                cudaStream_t s);
+
+// Box shapes (elements) the kernels expect for each operand's tensor map.
+constexpr int kBM = 128, kBN = 256, kBK = 64;
+
+}  // namespace moe

@@ -1,0 +1,198 @@
+// route.cu - device-side routing layout: per-expert counts, ragged prefix
+// offsets, and the stable pair <-> row maps of the expert-major buffer.
+//
+// [TE] "MoE 학습이 밀집 모델보다 어려운 이유: 래그드 텐서" and "최적화 1: grouped
+// GEMM": the per-expert token counts are known only at run time and must stay
+// on the device (no device-to-host copy, CUDA-graph capturable).
+// [TE] ""드롭리스"의 실제 경계": expert-major rows, one per (token, expert)
+// pair, each expert's region padded to the alignment unit; overflow past the
+// buffer drops rows and reports the true total.
+//
+// Three kernels, all deterministic (every output is a function of the input
+// alone; counting uses integer atomics only where order cannot matter):
+//   1. route_hist:  chunk c of kChunk pairs -> ws[c][e] = #pairs of e in c
+//   2. route_scan:  one block: exclusive prefix of ws over chunks (per e),
+//                   counts, aligned offsets, true total, overflow flag
+//   3. route_rank:  chunk c again, in pair order: stable rank of each pair
+//                   among the pairs of its expert -> row_of_pair, pair_of_row
+// pair_of_row is first filled with -1 (route_fill).
+#include <cuda_runtime.h>
+
+#include "ptx.cuh"
+#include "route.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kPerThread = 16;
+constexpr int kChunk = kThreads * kPerThread;  // 4096 pairs per chunk
+constexpr int kWarps = kThreads / 32;
+
+__global__ void route_fill(int32_t* __restrict__ p, int n, int32_t v) {
+  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x) p[i] = v;
+}
+
+__global__ void __launch_bounds__(kThreads) route_hist(const int32_t* __restrict__ idx, int P, int E,
+                                                       int32_t* __restrict__ ws,
+                                                       int32_t* __restrict__ err) {
+  extern __shared__ int32_t hist[];
+  for (int e = threadIdx.x; e < E; e += kThreads) hist[e] = 0;
+  __syncthreads();
+  const int base = blockIdx.x * kChunk;
+  const int end = min(P, base + kChunk);
+  bool bad = false;
+  for (int p = base + threadIdx.x; p < end; p += kThreads) {
+    const int e = idx[p];
+    if (e >= 0 && e < E) atomicAdd(&hist[e], 1);
+    else if (e != -1) bad = true;
+  }
+  if (__any_sync(0xffffffffu, bad) && (threadIdx.x & 31) == 0) set_err(err, MOE_DEV_BAD_EXPERT);
+  __syncthreads();
+  int32_t* out = ws + static_cast<long long>(blockIdx.x) * E;
+  for (int e = threadIdx.x; e < E; e += kThreads) out[e] = hist[e];
+}
+
+// one block of 1024 threads; E <= 1024
+__global__ void __launch_bounds__(1024) route_scan(int32_t* __restrict__ ws, int nchunks, int E,
+                                                   int align, int M_cap,
+                                                   int32_t* __restrict__ counts,
+                                                   int32_t* __restrict__ offsets,
+                                                   int32_t* __restrict__ demanded,
+                                                   int32_t* __restrict__ true_total,
+                                                   int32_t* __restrict__ err) {
+  __shared__ int32_t s_warp[32];
+  const int e = threadIdx.x;
+  int total_e = 0;
+  if (e < E) {
+    // exclusive prefix over chunks, in place
+    for (int c = 0; c < nchunks; ++c) {
+      int32_t* p = ws + static_cast<long long>(c) * E + e;
+      const int v = *p;
+      *p = total_e;
+      total_e += v;
+    }
+    counts[e] = total_e;
+  }
+  // aligned count, block-wide exclusive scan over experts
+  const long long aligned = (e < E) ? (static_cast<long long>(total_e) + align - 1) / align * align : 0;
+  int v = static_cast<int>(aligned);  // T*k + E*align fits in int32 (checked on the host)
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int incl = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += y;
+  }
+  if (lane == 31) s_warp[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    int w = s_warp[lane];
+    int wi = w;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, wi, o);
+      if (lane >= o) wi += y;
+    }
+    s_warp[lane] = wi - w;  // exclusive warp base
+  }
+  __syncthreads();
+  const int excl = s_warp[warp] + incl - v;
+  if (e < E) {
+    demanded[e] = excl;
+    offsets[e] = min(excl, M_cap);
+  }
+  if (e == E - 1) {
+    const int tot = excl + v;
+    offsets[E] = min(tot, M_cap);
+    *true_total = tot;
+    if (tot > M_cap) set_err(err, MOE_DEV_OVERFLOW);
+  }
+}
+
+__global__ void __launch_bounds__(kThreads) route_rank(const int32_t* __restrict__ idx, int P, int E,
+                                                       int M_cap, const int32_t* __restrict__ ws,
+                                                       const int32_t* __restrict__ demanded,
+                                                       int32_t* __restrict__ row_of_pair,
+                                                       int32_t* __restrict__ pair_of_row) {
+  extern __shared__ int32_t sm[];
+  int32_t* running = sm;            // [E] rows already given to e (chunk base + rounds)
+  int32_t* wcnt = sm + E;           // [kWarps][E] per-round, per-warp counts
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int32_t* base_c = ws + static_cast<long long>(blockIdx.x) * E;
+  for (int e = threadIdx.x; e < E; e += kThreads) running[e] = demanded[e] + base_c[e];
+  for (int i = threadIdx.x; i < kWarps * E; i += kThreads) wcnt[i] = 0;
+  __syncthreads();
+  const int base = blockIdx.x * kChunk;
+  for (int r = 0; r < kPerThread; ++r) {
+    const int p = base + r * kThreads + threadIdx.x;
+    int e = -1;
+    if (p < P) {
+      e = idx[p];
+      if (e < 0 || e >= E) e = -1;
+    }
+    const unsigned mask = __match_any_sync(0xffffffffu, e);
+    const int leader = __ffs(mask) - 1;
+    const int rank = __popc(mask & ((1u << lane) - 1u));
+    if (e >= 0 && lane == leader) wcnt[warp * E + e] = __popc(mask);
+    __syncthreads();
+    int row = -1;
+    if (e >= 0) {
+      int before = 0;
+      for (int w = 0; w < warp; ++w) before += wcnt[w * E + e];
+      row = running[e] + before + rank;
+    }
+    __syncthreads();
+    if (e >= 0 && lane == leader) {
+      atomicAdd(&running[e], __popc(mask));
+      wcnt[warp * E + e] = 0;
+    }
+    if (p < P) {
+      const int out = (row >= 0 && row < M_cap) ? row : -1;
+      row_of_pair[p] = out;
+      if (out >= 0) pair_of_row[out] = p;
+    }
+    __syncthreads();
+  }
+}
+
+}  // namespace
+
+size_t route_workspace_bytes(int T, int k, int E) {
+  const long long P = static_cast<long long>(T) * k;
+  const long long nchunks = (P + kChunk - 1) / kChunk;
+  return static_cast<size_t>((nchunks * E + E) * sizeof(int32_t));
+}
+
+cudaError_t launch_route(const int32_t* topk_idx, int T, int k, int E, int align, int M_cap,
+                         int32_t* counts, int32_t* offsets, int32_t* row_of_pair,
+                         int32_t* pair_of_row, int32_t* true_total, void* workspace,
+                         int32_t* err, int num_sms, cudaStream_t s, int* launches) {
+  const int P = T * k;
+  const int nchunks = (P + kChunk - 1) / kChunk;
+  int32_t* ws = static_cast<int32_t*>(workspace);
+  int32_t* demanded = ws + static_cast<long long>(nchunks) * E;
+  *launches = 0;
+  if (M_cap > 0) {
+    const int blocks = min((M_cap + 255) / 256, 4 * num_sms);
+    route_fill<<<blocks, 256, 0, s>>>(pair_of_row, M_cap, -1);
+    ++*launches;
+  }
+  if (nchunks > 0) {
+    route_hist<<<nchunks, kThreads, E * sizeof(int32_t), s>>>(topk_idx, P, E, ws, err);
+    ++*launches;
+  }
+  route_scan<<<1, 1024, 0, s>>>(ws, nchunks, E, align, M_cap, counts, offsets, demanded,
+                                true_total, err);
+  ++*launches;
+  if (nchunks > 0) {
+    // at most (1 + 8) * 1024 * 4 = 36 KB: below the default 48 KB limit
+    const size_t sm = static_cast<size_t>(E) * (1 + kWarps) * sizeof(int32_t);
+    route_rank<<<nchunks, kThreads, sm, s>>>(topk_idx, P, E, M_cap, ws, demanded, row_of_pair,
+                                             pair_of_row);
+    ++*launches;
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -1,0 +1,29 @@
+// route.cuh - host-side interface of the routing-layout kernels (route.cu).
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include <cstddef>
+#include <cstdint>
+
+namespace moe {
+
+size_t route_workspace_bytes(int T, int k, int E);
+
+// Enqueues the routing-layout kernels; *launches receives their number.
+cudaError_t launch_route(const int32_t* topk_idx, int T, int k, int E, int align, int M_cap,
+                         int32_t* counts, int32_t* offsets, int32_t* row_of_pair,
+                         int32_t* pair_of_row, int32_t* true_total, void* workspace,
+                         int32_t* err, int num_sms, cudaStream_t s, int* launches);
+
+cudaError_t launch_permute(const uint16_t* src, const float* scale, const int32_t* pair_of_row,
+                           int T, int k, int d, int M_cap, uint16_t* dst, int num_sms,
+                           cudaStream_t s);
+
+cudaError_t launch_unpermute(const uint16_t* src, const float* probs,
+                             const int32_t* row_of_pair, int T, int k, int d, int M_cap,
+                             uint16_t* dst,
+                             const uint16_t* dO, float* dprobs, int num_sms, cudaStream_t s,
+                             int* launches);
+
+}  // namespace moe

@@ -1,0 +1,241 @@
+/*
+ * moe.h - C ABI of libmoe, the GB300 (sm_103a) dropless MoE expert-MLP path.
+ *
+ * The path: a device-side routing layout (per-expert counts and prefix
+ * offsets that never leave device memory), an expert-major permute, a
+ * grouped FC1 GEMM with the gated activation applied in its epilogue, a
+ * grouped FC2 GEMM, the combine, and the backward of all of these with the
+ * activation derivative fused into the FC2-dgrad epilogue.
+ *
+ * Pages cited (title, section):
+ *   [CuTe]  "NVIDIA CuTe DSL 융합 커널은 MoE 학습의 CPU·메모리 병목을 지운다"
+ *   [Sonic] "SonicMoE로 보는 GPU 커널 최적화"
+ *   [TE]    "NVIDIA Transformer Engine JAX dropless MoE 105→1,025 TFLOPs"
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - Every tensor argument is a DEVICE pointer owned by the caller.  Unless
+ *    an entry point says otherwise the library allocates nothing, keeps no
+ *    pointer after the call returns, and never synchronises the device or
+ *    the stream: work is only enqueued on `stream` (a cudaStream_t passed as
+ *    void*; NULL = legacy default stream).  No call copies anything to the
+ *    host, so a whole forward + backward can be captured in a CUDA graph.
+ *  - Layouts are row-major and dense (innermost dimension contiguous).
+ *    bf16 tensors are passed as moe_bf16 (raw 16-bit patterns).
+ *  - Pointers must be 16-byte aligned; d and n must be positive multiples
+ *    of 64.
+ *  - Return value: MOE_OK, or a negative MOE_E_* code for an error found
+ *    on the host before anything is enqueued (null pointer, misalignment,
+ *    unsupported size, CUDA launch failure).  Nothing is enqueued when a
+ *    negative code is returned, except for MOE_E_CUDA, which reports the
+ *    first failing launch.
+ *  - Errors found on the device are OR-ed into the caller's int32 `err`
+ *    word (MOE_DEV_* bits, sticky: the library never clears it).  No kernel
+ *    traps; every wait inside a kernel is bounded in time and sets
+ *    MOE_DEV_TIMEOUT when its limit runs out.
+ */
+#ifndef MOE_H_
+#define MOE_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef uint16_t moe_bf16;
+
+/* host-side return codes */
+#define MOE_OK 0
+#define MOE_E_NULL (-1)        /* a required pointer is NULL            */
+#define MOE_E_ALIGN (-2)       /* a pointer is not 16-byte aligned      */
+#define MOE_E_SIZE (-3)        /* unsupported or inconsistent size      */
+#define MOE_E_ARG (-4)         /* bad enum / flag value                 */
+#define MOE_E_CUDA (-5)        /* CUDA runtime / launch error           */
+#define MOE_E_WORKSPACE (-6)   /* workspace too small                   */
+
+/* device-side error bits (OR-ed into *err) */
+#define MOE_DEV_BAD_EXPERT 1   /* an expert id outside [-1, E) was skipped     */
+#define MOE_DEV_OVERFLOW 2     /* rows past M_cap were dropped                  */
+#define MOE_DEV_TIMEOUT 4      /* a bounded wait inside a kernel ran out        */
+#define MOE_DEV_BAD_OFFSETS 8  /* offsets not non-decreasing within [0, M_cap];
+                                  they were clamped before use                  */
+
+/* activations ([CuTe] "무엇을 해결하려는가": SwiGLU, GeGLU, sReLU) */
+#define MOE_ACT_SWIGLU 0       /* A_j = silu(H_2j) * H_2j+1                    */
+#define MOE_ACT_GEGLU 1        /* A_j = gelu_tanh(H_2j) * H_2j+1               */
+#define MOE_ACT_SRELU 2        /* A_j = max(H_j, 0)^2  (not gated)             */
+
+/* flags */
+#define MOE_FLAG_SAVE_H 1      /* forward also stores H (needed by backward)   */
+
+/* Limits. */
+#define MOE_MAX_EXPERTS 1024
+
+/*
+ * moe_route_offsets - routing layout of the expert-major permuted buffer.
+ *
+ * Defined by [TE] "MoE 학습이 밀집 모델보다 어려운 이유: 래그드 텐서" (experts'
+ * rows stored back to back in one ragged buffer), "용량 기반 MoE와 드롭리스
+ * MoE" (dropless: no drop, no pad), "최적화 1: grouped GEMM" (per-expert
+ * blocks aligned to a token unit; counts stay on the device) and
+ * ""드롭리스"의 실제 경계" (one slot per (token, expert) pair, each expert
+ * region padded to the alignment unit; a DROP policy that reports the
+ * pre-truncation total).
+ *
+ *   topk_idx    [T, k] int32   expert of pair p = t*k + j; -1 = no route
+ *                              (skipped silently); other ids outside [0, E)
+ *                              are skipped and set MOE_DEV_BAD_EXPERT.
+ *   align       >= 1           each expert's row count is rounded up to a
+ *                              multiple of align (1 = no padding at all).
+ *   M_cap                      rows of the permuted buffer; T*k + E*(align-1)
+ *                              always suffices.
+ * Outputs (device):
+ *   counts      [E]   int32    pairs routed to each expert (before any drop).
+ *   offsets     [E+1] int32    offsets[0] = 0, offsets[e+1] = offsets[e] +
+ *                              roundup(counts[e], align), clamped to M_cap.
+ *                              Rows of expert e: [offsets[e], offsets[e+1]).
+ *   row_of_pair [T*k] int32    offsets[e] + rank of p among the pairs of e in
+ *                              increasing p; -1 if skipped or dropped.
+ *   pair_of_row [M_cap] int32  inverse of row_of_pair; -1 for pad and unused
+ *                              rows.
+ *   true_total  [1]   int32    rows demanded before truncation (the DROP
+ *                              policy's true total); if it exceeds M_cap the
+ *                              rows at or past M_cap are dropped and
+ *                              MOE_DEV_OVERFLOW is set.
+ *   workspace   device scratch of moe_route_workspace_size(T, k, E) bytes
+ *               (contents need not be initialised; not kept after the call).
+ * Every output is bit-exact and deterministic (no order depends on timing).
+ * Limits: 1 <= E <= MOE_MAX_EXPERTS, 1 <= k <= E, T >= 0, 1 <= align <= 4096.
+ */
+size_t moe_route_workspace_size(int T, int k, int E);
+int moe_route_offsets(const int32_t* topk_idx, int T, int k, int E, int align,
+                      int M_cap, int32_t* counts, int32_t* offsets,
+                      int32_t* row_of_pair, int32_t* pair_of_row,
+                      int32_t* true_total, void* workspace, size_t ws_bytes,
+                      int32_t* err, void* stream);
+
+/*
+ * moe_permute - expert-major gather ([TE] "최적화 2: NCCL EP": dispatch
+ * permutes the token rows; here without communication).
+ *
+ *   src [T, d] bf16, dst [M_cap, d] bf16.
+ *   dst[r] = src[pair_of_row[r] / k]                 (scale == NULL, exact copy)
+ *   dst[r] = bf16_rn(scale[p] * src[p / k]), p = pair_of_row[r]
+ *                                                    (scale [T*k] float32; the
+ *                                                    backward of the combine)
+ *   dst[r] = 0 where pair_of_row[r] == -1 (pad and unused rows) or is
+ *   otherwise outside [0, T*k).
+ */
+int moe_permute(const moe_bf16* src, const float* scale,
+                const int32_t* pair_of_row, int T, int k, int d, int M_cap,
+                moe_bf16* dst, void* stream);
+
+/*
+ * moe_unpermute - combine ([TE] "최적화 2: NCCL EP": results return to token
+ * order and each token accumulates its experts' outputs) and, optionally,
+ * the router-score gradient ([Sonic] "역전파 계산 그래프 재작성하기":
+ * dS_{t,e} = <dO_t, Y_{e,t}>).
+ *
+ *   src [M_cap, d] bf16 (expert-major rows), row_of_pair [T*k]; rows outside
+ *   [0, M_cap) are treated like -1.
+ *   If dst != NULL:   dst[t] = bf16_rn( sum_{j=0..k-1} w_tj * src[row(t,j)] ),
+ *                     w = probs[t*k+j] (float32) or 1 when probs == NULL;
+ *                     accumulated in float32 in increasing j; pairs with
+ *                     row -1 contribute nothing.
+ *   If dprobs != NULL: dprobs[t*k+j] = <dO[t], src[row(t,j)]> (float32; 0 for
+ *                     row -1); dO [T, d] bf16 is then required.
+ */
+int moe_unpermute(const moe_bf16* src, const float* probs,
+                  const int32_t* row_of_pair, int T, int k, int d, int M_cap,
+                  moe_bf16* dst, const moe_bf16* dO, float* dprobs,
+                  void* stream);
+
+/*
+ * moe_grouped_mlp_fwd - grouped expert MLP forward over ragged groups.
+ *
+ * [TE] "최적화 1: grouped GEMM" (one call over all experts with their real
+ * row counts, no padding to a capacity, no device-to-host copy);
+ * [CuTe] "핵심 아이디어 / 구조 / 동작 방식" (gate/up weight columns
+ * interleaved so the GLU is computed in the GEMM epilogue and the 2n-wide
+ * FC1 output need not be written).
+ *
+ * For each expert e, rows R_e = [offsets[e], offsets[e+1]) of x_perm:
+ *   H_e = X_e W1_e         (float32 accumulation)
+ *   A_e = act(H_e)         (from the float32 H; stored as bf16)
+ *   Y_e = A_e W2_e         (A read back as bf16; stored as bf16)
+ *
+ *   x_perm  [M_cap, d] bf16       offsets [E+1] int32 (device, non-decreasing,
+ *                                 offsets[E] <= M_cap)
+ *   W1      [E, d, n1] bf16       n1 = 2n for gated acts, column 2j = gate_j,
+ *                                 column 2j+1 = up_j; n1 = n for SRELU
+ *   W2      [E, n, d]  bf16
+ *   h_saved [M_cap, n1] bf16      written only with MOE_FLAG_SAVE_H (else may
+ *                                 be NULL)
+ *   a       [M_cap, n]  bf16      written
+ *   y_perm  [M_cap, d]  bf16      written
+ * Rows outside every expert's range are not written.  An expert with no
+ * rows costs (almost) nothing.
+ */
+int moe_grouped_mlp_fwd(const moe_bf16* x_perm, const int32_t* offsets,
+                        int E, int M_cap, int d, int n, const moe_bf16* W1,
+                        const moe_bf16* W2, int act, int flags,
+                        moe_bf16* h_saved, moe_bf16* a, moe_bf16* y_perm,
+                        int32_t* err, void* stream);
+
+/*
+ * moe_grouped_mlp_bwd - backward of moe_grouped_mlp_fwd.
+ *
+ * The FC2-dgrad GEMM carries the activation derivative in its epilogue
+ * ([CuTe] kernel family "GroupGemm + dActivation"; [Sonic] "GEMM
+ * Overlapping": the dH kernel's epilogue reloads H and writes dH).
+ * For each expert e:
+ *   dA_e  = dY_e W2_e^T                     (float32, never stored)
+ *   dH_e  = act'(H_e; dA_e)                 gated: dg = dA u phi'(g),
+ *                                           du = dA phi(g); SRELU:
+ *                                           dh = 2 max(h,0) dA  -> bf16
+ *   dW2_e = A_e^T dY_e                      -> bf16
+ *   dX_e  = dH_e W1_e^T                     -> bf16
+ *   dW1_e = X_e^T dH_e                      -> bf16
+ * An expert with no rows gets dW1_e = dW2_e = 0.
+ *
+ *   x_perm [M_cap, d], h_saved [M_cap, n1], a [M_cap, n], dy_perm [M_cap, d]
+ *   dh [M_cap, n1] (written), dx_perm [M_cap, d] (written),
+ *   dW1 [E, d, n1] (written), dW2 [E, n, d] (written); all bf16.
+ */
+int moe_grouped_mlp_bwd(const moe_bf16* x_perm, const moe_bf16* h_saved,
+                        const moe_bf16* a, const moe_bf16* dy_perm,
+                        const int32_t* offsets, int E, int M_cap, int d,
+                        int n, const moe_bf16* W1, const moe_bf16* W2,
+                        int act, int flags, moe_bf16* dh, moe_bf16* dx_perm,
+                        moe_bf16* dW1, moe_bf16* dW2, int32_t* err,
+                        void* stream);
+
+/*
+ * Measurement hook (per host thread; no counterpart on the pages).
+ * moe_set_launch_events(events, n): events points to n caller-created
+ * cudaEvent_t handles (passed as void*).  From then on every grouped-GEMM
+ * kernel launch, and every other entry-point call as a whole, records
+ * events[2i] on its stream just before and events[2i+1] just after it, for
+ * i = 0, 1, ... while 2i+1 < n; later launches record nothing.  The order
+ * is the launch order: moe_grouped_mlp_fwd = FC1, FC2; moe_grouped_mlp_bwd
+ * = FC2-dgrad+dAct, FC2-wgrad, FC1-dgrad, FC1-wgrad.  Passing (NULL, 0)
+ * turns the hook off.  moe_launch_events_used() returns the number of
+ * events recorded since the last moe_set_launch_events call.
+ */
+int moe_set_launch_events(void* const* events, int n);
+int moe_launch_events_used(void);
+
+/* Library version string (static storage). */
+const char* moe_version(void);
+
+/* Number of kernel launches the last successful call on this host thread
+ * enqueued (for launch accounting; 0 before any call). */
+int moe_last_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_H_ */

@@ -1,0 +1,57 @@
+"""The C-ABI library loads and exports every entry point include/moe.h
+declares; host-side argument checks work without a GPU."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import dropless_grouped_gemm_gb300 as M
+from dropless_grouped_gemm_gb300 import build as B
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared():
+    src = open(os.path.join(ROOT, "include", "moe.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(moe_\w+)\s*\(", src)))
+
+
+@pytest.fixture(scope="module")
+def L():
+    B.build()
+    return M.lib()
+
+
+def test_every_declared_symbol_is_exported(L):
+    names = _declared()
+    assert "moe_grouped_mlp_fwd" in names and len(names) >= 8
+    for n in names:
+        assert hasattr(L, n), n
+
+
+def test_version(L):
+    assert "sm_103a" in M.version()
+
+
+def test_host_argument_errors(L):
+    vp = ctypes.c_void_p
+    # E = 0, k > E, bad align: rejected before anything touches the GPU
+    assert L.moe_grouped_mlp_fwd(None, None, 0, 0, 64, 64, None, None, 0, 0, None, None, None,
+                                 None, None) == -3
+    assert L.moe_grouped_mlp_fwd(None, None, 4, 128, 96, 64, None, None, 0, 0, None, None, None,
+                                 None, None) == -3          # d not a multiple of 64
+    assert L.moe_grouped_mlp_fwd(None, None, 4, 128, 64, 64, None, None, 7, 0, None, None, None,
+                                 None, None) == -4          # bad act
+    assert L.moe_route_offsets(None, 4, 3, 2, 1, 12, None, None, None, None, None, None, 0, None,
+                               None) == -3                  # k > E
+    assert L.moe_route_offsets(None, 4, 2, 8, 0, 12, None, None, None, None, None, None, 0, None,
+                               None) == -3                  # align 0
+    assert L.moe_permute(None, None, None, 4, 1, 100, 4, None, None) == -3
+    assert L.moe_unpermute(vp(16), None, vp(16), 2, 1, 64, 4, None, None, None, None) == -1
+
+
+def test_workspace_size_host_only(L):
+    assert M.route_workspace_size(4096, 8, 256) >= 8 * 256 * 4
+    assert M.route_workspace_size(0, 1, 4) == 4 * 4

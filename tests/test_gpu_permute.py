@@ -1,0 +1,70 @@
+"""GPU permute / unpermute / router-score gradient vs the oracle."""
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+import workloads as W
+from _helpers import assert_rms_close, cuda_i32, f64
+
+pytestmark = pytest.mark.gpu
+
+
+def _setup(T, k, E, d, align, seed):
+    rng = np.random.default_rng(seed)
+    idx = np.stack([rng.permutation(E)[:k] for _ in range(T)]).astype(np.int32)
+    r = O.route_offsets(idx, E, align)
+    x = W.normal((T, d), (seed, W.X, 0), 1.0, "cuda")
+    p = rng.random((T, k)).astype(np.float32)
+    p /= p.sum(1, keepdims=True)
+    return idx, r, x, p
+
+
+@pytest.mark.parametrize("T,k,E,d,align", [(512, 2, 4, 128, 1), (300, 8, 64, 7168, 32),
+                                           (77, 1, 3, 64, 8)])
+def test_permute_exact(T, k, E, d, align):
+    import dropless_grouped_gemm_gb300 as M
+    idx, r, x, _ = _setup(T, k, E, d, align, 1)
+    xp = M.permute(x, cuda_i32(r["pair_of_row"]), k)
+    ref = O.permute(f64(x), r["pair_of_row"], k)
+    assert np.array_equal(f64(xp), ref)           # bit-exact copy, zero pad rows
+
+
+def test_permute_scaled():
+    import dropless_grouped_gemm_gb300 as M
+    T, k, E, d = 257, 4, 16, 512
+    idx, r, x, p = _setup(T, k, E, d, 1, 2)
+    xp = M.permute(x, cuda_i32(r["pair_of_row"]), k, scale=torch.from_numpy(p.reshape(-1)).cuda())
+    ref = O.permute(f64(x), r["pair_of_row"], k, scale=p.reshape(-1))
+    got = f64(xp)
+    assert_rms_close(got, ref, "scaled permute")
+    # float32 product then bf16 rounding: at most one bf16 step from the oracle
+    ulp = np.abs(ref) * 2.0 ** -7 + 1e-30
+    assert (np.abs(got - ref) <= ulp).all()
+
+
+@pytest.mark.parametrize("T,k,E,d", [(512, 2, 4, 128), (200, 8, 256, 7168), (33, 1, 2, 64)])
+def test_unpermute_and_router_grad(T, k, E, d):
+    import dropless_grouped_gemm_gb300 as M
+    idx, r, _, p = _setup(T, k, E, d, 1, 3)
+    M_cap = len(r["pair_of_row"])
+    y = W.normal((M_cap, d), (3, W.DY, 0), 1.0, "cuda")
+    dO = W.normal((T, d), (3, W.DO, 0), 1.0, "cuda")
+    rop = cuda_i32(r["row_of_pair"])
+    pt = torch.from_numpy(p).cuda()
+    out, _ = M.unpermute(y, rop, T, k, probs=pt)
+    out1, _ = M.unpermute(y, rop, T, k)
+    _, dp = M.unpermute(y, rop, T, k, dO=dO, combine=False)
+    assert_rms_close(f64(out), O.unpermute(f64(y), r["row_of_pair"], T, k, p), "combine")
+    assert_rms_close(f64(out1), O.unpermute(f64(y), r["row_of_pair"], T, k), "combine (no probs)")
+    assert_rms_close(dp.cpu().numpy(), O.router_grad(f64(dO), f64(y), r["row_of_pair"], T, k),
+                     "dprobs", rtol=0)
+
+
+def test_roundtrip_identity():
+    import dropless_grouped_gemm_gb300 as M
+    T, k, E, d = 1000, 2, 8, 256
+    idx, r, x, _ = _setup(T, k, E, d, 8, 4)
+    xp = M.permute(x, cuda_i32(r["pair_of_row"]), k)
+    back, _ = M.unpermute(xp, cuda_i32(r["row_of_pair"]), T, k)
+    assert torch.equal(back.float(), 2 * x.float())     # k = 2: exact

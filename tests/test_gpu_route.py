@@ -1,0 +1,84 @@
+"""GPU routing layout (moe_route_offsets) vs the oracle: bit-exact."""
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+import workloads as W
+from _helpers import cuda_i32
+
+pytestmark = pytest.mark.gpu
+
+
+def _run(idx, E, align, M_cap=None):
+    import dropless_grouped_gemm_gb300 as M
+    T, k = idx.shape
+    r = M.route_offsets(cuda_i32(idx), E, align, M_cap)
+    torch.cuda.synchronize()
+    o = O.route_offsets(idx, E, align, M_cap)
+    return {k_: v.cpu().numpy() for k_, v in r.items()}, o
+
+
+def _check(g, o):
+    assert g["counts"].tolist() == o["counts"].tolist()
+    assert g["offsets"].tolist() == o["offsets"].tolist()
+    assert g["row_of_pair"].tolist() == o["row_of_pair"].tolist()
+    assert g["pair_of_row"].tolist() == o["pair_of_row"].tolist()
+    assert int(g["true_total"][0]) == o["true_total"]
+    assert int(g["err"][0]) == o["err"]
+
+
+def _rand_route(seed, T, k, E):
+    rng = np.random.default_rng(seed)
+    return np.stack([rng.permutation(E)[:k] for _ in range(T)]).astype(np.int32) if T else \
+        np.zeros((0, k), np.int32)
+
+
+@pytest.mark.parametrize("align", [1, 8, 32, 128])
+def test_tiny_workload_routing(align):
+    w = W.WORKLOADS["tiny_t512_d128_e4_top2_n256_swiglu_fwd"]
+    idx, _ = W.route_inputs(w)
+    g, o = _run(idx, w.E, align)
+    _check(g, o)
+    assert g["counts"][3] == 0
+
+
+@pytest.mark.parametrize("align", [1, 32])
+def test_zipf_256_experts_top8(align):
+    w = W.WORKLOADS["zipf_t4096_d7168_e256_top8_n2048_swiglu"]
+    idx, _ = W.route_inputs(w)
+    g, o = _run(idx, w.E, align)
+    _check(g, o)
+
+
+@pytest.mark.parametrize("T,k,E", [(20000, 4, 64), (3, 1, 1), (1000, 8, 1024), (4097, 2, 5)])
+def test_random_multi_chunk(T, k, E):
+    g, o = _run(_rand_route(T + E, T, k, E), E, 1)
+    _check(g, o)
+
+
+def test_no_route_bad_ids_and_overflow():
+    idx = _rand_route(7, 300, 2, 6)
+    idx[5, 0] = -1
+    idx[9, 1] = 6          # out of range -> flagged, skipped
+    idx[11, 0] = -7
+    g, o = _run(idx, 6, 1)
+    _check(g, o)
+    assert int(g["err"][0]) == O.ERR_BAD_EXPERT
+    g, o = _run(_rand_route(8, 300, 2, 6), 6, 4, M_cap=500)   # demands up to 600 + pad
+    _check(g, o)
+    assert int(g["err"][0]) & O.ERR_OVERFLOW
+
+
+def test_zero_tokens():
+    g, o = _run(np.zeros((0, 2), np.int32), 4, 8)
+    _check(g, o)
+
+
+def test_deterministic():
+    import dropless_grouped_gemm_gb300 as M
+    idx = cuda_i32(_rand_route(9, 5000, 8, 256))
+    a = M.route_offsets(idx, 256, 1)
+    b = M.route_offsets(idx, 256, 1)
+    for k_ in ("offsets", "row_of_pair", "pair_of_row"):
+        assert torch.equal(a[k_], b[k_])
