@@ -403,6 +403,9 @@ def main():
     import ctypes
     per = len(names)
     evs = [torch.cuda.Event(enable_timing=True) for _ in range(2 * per * args.steps)]
+    for e in evs:          # torch creates the CUDA event on its first record
+        e.record(stream)
+    torch.cuda.synchronize()
     handles = (ctypes.c_void_p * len(evs))(*[e.cuda_event for e in evs])
     try:
         uuid = str(torch.cuda.get_device_properties(lrank).uuid)

@@ -24,10 +24,12 @@ __all__ = [
     "ACT", "FLAG_SAVE_H", "DEV_BAD_EXPERT", "DEV_OVERFLOW", "DEV_TIMEOUT", "DEV_BAD_OFFSETS",
     "lib", "lib_path", "version", "last_launch_count", "route_workspace_size", "route_offsets",
     "permute", "unpermute", "grouped_mlp_fwd", "grouped_mlp_bwd", "MoeError",
+    "FLAG_MXFP8", "MxFwd", "mx_quantize_weights", "mx_quantize", "mx_buffers",
 ]
 
 ACT = {"swiglu": 0, "geglu": 1, "srelu": 2}
 FLAG_SAVE_H = 1
+FLAG_MXFP8 = 2
 DEV_BAD_EXPERT, DEV_OVERFLOW, DEV_TIMEOUT, DEV_BAD_OFFSETS = 1, 2, 4, 8
 _RC = {-1: "MOE_E_NULL", -2: "MOE_E_ALIGN", -3: "MOE_E_SIZE", -4: "MOE_E_ARG",
        -5: "MOE_E_CUDA", -6: "MOE_E_WORKSPACE"}
@@ -38,6 +40,12 @@ _LIB = None
 
 class MoeError(RuntimeError):
     pass
+
+
+class MxFwd(ctypes.Structure):
+    """moe_mx_fwd: MXFP8 buffers of the forward (device pointers)."""
+    _fields_ = [("w2_q", ctypes.c_void_p), ("w2_s", ctypes.c_void_p), ("a_q", ctypes.c_void_p),
+                ("a_s", ctypes.c_void_p), ("a_qT", ctypes.c_void_p), ("a_sT", ctypes.c_void_p)]
 
 
 def lib_path() -> str:
@@ -68,7 +76,15 @@ def lib():
         L.moe_unpermute.argtypes = [vp, vp, vp, i32, i32, i32, i32, vp, vp, vp, vp]
         L.moe_grouped_mlp_fwd.restype = i32
         L.moe_grouped_mlp_fwd.argtypes = [vp, vp, i32, i32, i32, i32, vp, vp, i32, i32, vp, vp, vp,
-                                          vp, vp]
+                                          vp, vp, vp]
+        L.moe_mx_quantize_weights.restype = i32
+        L.moe_mx_quantize_weights.argtypes = [vp, i32, i32, i32, vp, vp, vp]
+        L.moe_mx_quantize.restype = i32
+        L.moe_mx_quantize.argtypes = [vp, i32, i32, vp, i32, vp, vp, vp, vp, vp, vp]
+        L.moe_set_launch_events.restype = i32
+        L.moe_set_launch_events.argtypes = [vp, i32]
+        L.moe_launch_events_used.restype = i32
+        L.moe_launch_events_used.argtypes = []
         L.moe_grouped_mlp_bwd.restype = i32
         L.moe_grouped_mlp_bwd.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, vp, vp, i32, i32,
                                           vp, vp, vp, vp, vp, vp]
@@ -199,8 +215,10 @@ def grouped_mlp_fwd(x_perm: torch.Tensor, offsets: torch.Tensor, W1: torch.Tenso
                     W2: torch.Tensor, act: str = "swiglu", save_h: bool = False,
                     h_saved: torch.Tensor | None = None, a: torch.Tensor | None = None,
                     y_perm: torch.Tensor | None = None, err: torch.Tensor | None = None,
-                    stream=None):
-    """Grouped expert MLP forward (see moe_grouped_mlp_fwd).  Returns
+                    mx: dict | None = None, stream=None):
+    """Grouped expert MLP forward (see moe_grouped_mlp_fwd).  With ``mx`` (a
+    dict of uint8 device tensors w2_q, w2_s, a_q, a_s and optionally a_qT,
+    a_sT; see ``mx_buffers``) the MXFP8 path runs.  Returns
     (h_saved or None, a, y_perm, err)."""
     _need(x_perm, torch.bfloat16, "x_perm", 2)
     _need(offsets, torch.int32, "offsets", 1)
@@ -219,9 +237,17 @@ def grouped_mlp_fwd(x_perm: torch.Tensor, offsets: torch.Tensor, W1: torch.Tenso
     if y_perm is None:
         y_perm = torch.empty((M_cap, d), dtype=torch.bfloat16, device=dev)
     err = _err_word(err, dev)
+    flags = FLAG_SAVE_H if save_h else 0
+    mxs = None
+    if mx is not None:
+        for k_ in ("w2_q", "w2_s", "a_q", "a_s", "a_qT", "a_sT"):
+            _need(mx.get(k_), torch.uint8, k_)
+        mxs = MxFwd(*[(mx[k_].data_ptr() if mx.get(k_) is not None else None)
+                      for k_ in ("w2_q", "w2_s", "a_q", "a_s", "a_qT", "a_sT")])
+        flags |= FLAG_MXFP8
     rc = lib().moe_grouped_mlp_fwd(_ptr(x_perm), _ptr(offsets), E, M_cap, d, n, _ptr(W1), _ptr(W2),
-                                   ACT[act], FLAG_SAVE_H if save_h else 0,
-                                   _ptr(h_saved) if save_h else None, _ptr(a), _ptr(y_perm),
+                                   ACT[act], flags, _ptr(h_saved) if save_h else None, _ptr(a),
+                                   _ptr(y_perm), ctypes.byref(mxs) if mxs is not None else None,
                                    _ptr(err), _stream(stream))
     _check(rc, "moe_grouped_mlp_fwd")
     return (h_saved if save_h else None), a, y_perm, err
@@ -254,3 +280,51 @@ def grouped_mlp_bwd(x_perm, h_saved, a, dy_perm, offsets, W1, W2, act: str = "sw
                                    _stream(stream))
     _check(rc, "moe_grouped_mlp_bwd")
     return dh, dx_perm, dW1, dW2, err
+
+
+def mx_buffers(E: int, n: int, d: int, M_cap: int, device, transposed: bool = True) -> dict:
+    """Allocate the uint8 buffers of moe_mx_fwd (sizes as moe.h states)."""
+    u8 = torch.uint8
+    b = {"w2_q": torch.empty((E, n, d), dtype=u8, device=device),
+         "w2_s": torch.empty(E * (n // 32) * d, dtype=u8, device=device),
+         "a_q": torch.empty((M_cap, n), dtype=u8, device=device),
+         "a_s": torch.empty((M_cap // 32) * (n // 128) * 512, dtype=u8, device=device)}
+    if transposed:
+        b["a_qT"] = torch.empty((n, M_cap), dtype=u8, device=device)
+        b["a_sT"] = torch.empty((n, M_cap // 32), dtype=u8, device=device)
+    return b
+
+
+def mx_quantize_weights(W2: torch.Tensor, w2_q: torch.Tensor | None = None,
+                        w2_s: torch.Tensor | None = None, stream=None):
+    """MXFP8 codes and MMA-tiled scales of W2 [E, n, d] (moe_mx_quantize_weights)."""
+    _need(W2, torch.bfloat16, "W2", 3)
+    E, n, d = W2.shape
+    if w2_q is None:
+        w2_q = torch.empty((E, n, d), dtype=torch.uint8, device=W2.device)
+    if w2_s is None:
+        w2_s = torch.empty(E * (n // 32) * d, dtype=torch.uint8, device=W2.device)
+    _need(w2_q, torch.uint8, "w2_q")
+    _need(w2_s, torch.uint8, "w2_s")
+    rc = lib().moe_mx_quantize_weights(_ptr(W2), E, n, d, _ptr(w2_q), _ptr(w2_s), _stream(stream))
+    _check(rc, "moe_mx_quantize_weights")
+    return w2_q, w2_s
+
+
+def mx_quantize(src: torch.Tensor, offsets: torch.Tensor, transposed: bool = True,
+                err: torch.Tensor | None = None, stream=None):
+    """Group-aware MXFP8 quantisation (moe_mx_quantize).  Returns
+    (q, s, qT, sT, err); qT/sT are None unless ``transposed``."""
+    _need(src, torch.bfloat16, "src", 2)
+    _need(offsets, torch.int32, "offsets", 1)
+    rows, cols = src.shape
+    dev = src.device
+    q = torch.empty((rows, cols), dtype=torch.uint8, device=dev)
+    s = torch.empty((rows, cols // 32), dtype=torch.uint8, device=dev)
+    qT = torch.empty((cols, rows), dtype=torch.uint8, device=dev) if transposed else None
+    sT = torch.empty((cols, rows // 32), dtype=torch.uint8, device=dev) if transposed else None
+    err = _err_word(err, dev)
+    rc = lib().moe_mx_quantize(_ptr(src), rows, cols, _ptr(offsets), offsets.numel() - 1, _ptr(q),
+                               _ptr(s), _ptr(qT), _ptr(sT), _ptr(err), _stream(stream))
+    _check(rc, "moe_mx_quantize")
+    return q, s, qT, sT, err

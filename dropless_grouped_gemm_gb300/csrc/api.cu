@@ -9,6 +9,7 @@
 
 #include "../../include/moe.h"
 #include "gemm.cuh"
+#include "mxgemm.cuh"
 #include "route.cuh"
 
 namespace {
@@ -63,39 +64,41 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-// bf16 tensor map, 128-byte swizzle; dims/box listed innermost first.
+// tensor map (bf16 or u8), 128-byte swizzle; dims/box listed innermost first.
 bool make_map(CUtensorMap* m, const void* base, int rank, const uint64_t* dims,
-              const uint32_t* box) {
+              const uint32_t* box, bool u8 = false) {
   auto fn = encode_fn();
   if (!fn) return false;
   cuuint64_t gdim[3], gstride[2];
   cuuint32_t bdim[3], estr[3] = {1, 1, 1};
-  uint64_t stride = 2;
+  uint64_t stride = u8 ? 1 : 2;
   for (int i = 0; i < rank; ++i) {
     gdim[i] = dims[i];
     bdim[i] = box[i];
     if (i > 0) gstride[i - 1] = stride;
     stride *= dims[i];
   }
-  const CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(base), gdim,
+  const CUresult r = fn(m, u8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                        rank, const_cast<void*>(base), gdim,
                         gstride, bdim, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                         CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
 
-// [rows, cols] activation matrix, box (64 cols) x (box_rows rows)
-bool map_act(CUtensorMap* m, const void* p, int rows, int cols, int box_rows) {
+// [rows, cols] activation matrix, box (128 bytes of cols) x (box_rows rows)
+bool map_act(CUtensorMap* m, const void* p, int rows, int cols, int box_rows, bool u8 = false) {
   const uint64_t dims[2] = {static_cast<uint64_t>(cols), static_cast<uint64_t>(rows)};
-  const uint32_t box[2] = {64, static_cast<uint32_t>(box_rows)};
-  return make_map(m, p, 2, dims, box);
+  const uint32_t box[2] = {u8 ? 128u : 64u, static_cast<uint32_t>(box_rows)};
+  return make_map(m, p, 2, dims, box, u8);
 }
-// [E, rows, cols] weights, box (64 cols) x (box_rows rows) x 1
-bool map_w(CUtensorMap* m, const void* p, int E, int rows, int cols, int box_rows) {
+// [E, rows, cols] weights, box (128 bytes of cols) x (box_rows rows) x 1
+bool map_w(CUtensorMap* m, const void* p, int E, int rows, int cols, int box_rows,
+           bool u8 = false) {
   const uint64_t dims[3] = {static_cast<uint64_t>(cols), static_cast<uint64_t>(rows),
                             static_cast<uint64_t>(E)};
-  const uint32_t box[3] = {64, static_cast<uint32_t>(box_rows), 1};
-  return make_map(m, p, 3, dims, box);
+  const uint32_t box[3] = {u8 ? 128u : 64u, static_cast<uint32_t>(box_rows), 1};
+  return make_map(m, p, 3, dims, box, u8);
 }
 
 int cuda_rc(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_E_CUDA; }
@@ -198,14 +201,25 @@ int moe_unpermute(const moe_bf16* src, const float* probs, const int32_t* row_of
 
 int moe_grouped_mlp_fwd(const moe_bf16* x_perm, const int32_t* offsets, int E, int M_cap, int d,
                         int n, const moe_bf16* W1, const moe_bf16* W2, int act, int flags,
-                        moe_bf16* h_saved, moe_bf16* a, moe_bf16* y_perm, int32_t* err,
-                        void* stream) {
+                        moe_bf16* h_saved, moe_bf16* a, moe_bf16* y_perm, const moe_mx_fwd* mx,
+                        int32_t* err, void* stream) {
   g_last_launches = 0;
   int rc = check_mlp_sizes(E, M_cap, d, n);
   if (rc) return rc;
-  if (act < MOE_ACT_SWIGLU || act > MOE_ACT_SRELU || (flags & ~MOE_FLAG_SAVE_H)) return MOE_E_ARG;
+  if (act < MOE_ACT_SWIGLU || act > MOE_ACT_SRELU ||
+      (flags & ~(MOE_FLAG_SAVE_H | MOE_FLAG_MXFP8)))
+    return MOE_E_ARG;
   const bool save_h = flags & MOE_FLAG_SAVE_H;
-  if (!offsets || !W1 || !W2 || !err) return MOE_E_NULL;
+  const bool use_mx = flags & MOE_FLAG_MXFP8;
+  if (use_mx) {
+    if (!mx || !mx->w2_q || !mx->w2_s || !mx->a_q || !mx->a_s || (mx->a_qT && !mx->a_sT))
+      return MOE_E_NULL;
+    if (n % 128 || d % 128 || M_cap % 32) return MOE_E_SIZE;
+    if (misaligned(mx->w2_q) || misaligned(mx->w2_s) || misaligned(mx->a_q) ||
+        misaligned(mx->a_s) || misaligned(mx->a_qT))
+      return MOE_E_ALIGN;
+  }
+  if (!offsets || !W1 || (!W2 && !use_mx) || !err) return MOE_E_NULL;
   if (M_cap == 0) return MOE_OK;
   if (!x_perm || !a || !y_perm || (save_h && !h_saved)) return MOE_E_NULL;
   if (misaligned(x_perm) || misaligned(W1) || misaligned(W2) || misaligned(a) ||
@@ -216,14 +230,36 @@ int moe_grouped_mlp_fwd(const moe_bf16* x_perm, const int32_t* offsets, int E, i
   if (sms <= 0) return MOE_E_CUDA;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   CUtensorMap tx, tw1, ta, tw2;
-  if (!map_act(&tx, x_perm, M_cap, d, moe::kBM) || !map_w(&tw1, W1, E, d, n1, 64) ||
-      !map_act(&ta, a, M_cap, n, moe::kBM) || !map_w(&tw2, W2, E, n, d, 64))
+  if (!map_act(&tx, x_perm, M_cap, d, moe::kBM) || !map_w(&tw1, W1, E, d, n1, 64))
     return MOE_E_CUDA;
+  if (use_mx) {
+    if (!map_act(&ta, mx->a_q, M_cap, n, 128, true) || !map_w(&tw2, mx->w2_q, E, n, d, 128, true))
+      return MOE_E_CUDA;
+  } else if (!map_act(&ta, a, M_cap, n, moe::kBM) || !map_w(&tw2, W2, E, n, d, 64)) {
+    return MOE_E_CUDA;
+  }
   moe::GemmArgs g1{};
   g1.offsets = offsets; g1.E = E; g1.M_cap = M_cap; g1.K = d; g1.N = n1; g1.R = 0;
   g1.out = a; g1.ldo = n; g1.out2 = save_h ? h_saved : nullptr; g1.ldo2 = n1; g1.err = err;
-  cudaError_t e = gemm(moe::GemmKind::kFc1Act, act, tx, tw1, g1, sms, s);
+  if (use_mx) {
+    g1.mx_q = mx->a_q; g1.mx_s = mx->a_s; g1.mx_qT = mx->a_qT;
+    g1.mx_sT = mx->a_qT ? mx->a_sT : nullptr; g1.n_a = n;
+  }
+  ev_begin(s);
+  cudaError_t e = moe::launch_grouped_gemm(moe::GemmKind::kFc1Act, act, tx, tw1, g1, sms, s, use_mx);
+  ev_end(s);
   if (e != cudaSuccess) return MOE_E_CUDA;
+  if (use_mx) {
+    moe::MxFc2Args q{};
+    q.offsets = offsets; q.E = E; q.M_cap = M_cap; q.n = n; q.d = d;
+    q.a_s = mx->a_s; q.w2_s = mx->w2_s; q.out = y_perm; q.err = err;
+    ev_begin(s);
+    e = moe::launch_mx_fc2(ta, tw2, q, sms, s);
+    ev_end(s);
+    if (e != cudaSuccess) return MOE_E_CUDA;
+    g_last_launches = 2;
+    return MOE_OK;
+  }
   moe::GemmArgs g2{};
   g2.offsets = offsets; g2.E = E; g2.M_cap = M_cap; g2.K = n; g2.N = d; g2.R = 0;
   g2.out = y_perm; g2.ldo = d; g2.err = err;
@@ -297,6 +333,42 @@ int moe_grouped_mlp_bwd(const moe_bf16* x_perm, const moe_bf16* h_saved, const m
   if (e != cudaSuccess) return MOE_E_CUDA;
   g_last_launches = 4;
   return MOE_OK;
+}
+
+int moe_mx_quantize_weights(const moe_bf16* W2, int E, int n, int d, uint8_t* w2_q,
+                            uint8_t* w2_s, void* stream) {
+  g_last_launches = 0;
+  if (E < 1 || E > MOE_MAX_EXPERTS || n <= 0 || d <= 0 || n % 128 || d % 128) return MOE_E_SIZE;
+  if (!W2 || !w2_q || !w2_s) return MOE_E_NULL;
+  if (misaligned(W2) || misaligned(w2_q) || misaligned(w2_s)) return MOE_E_ALIGN;
+  const int sms = num_sms_current();
+  if (sms <= 0) return MOE_E_CUDA;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  ev_begin(s);
+  const cudaError_t e = moe::launch_mx_quantize_weights(W2, E, n, d, w2_q, w2_s, sms, s);
+  ev_end(s);
+  g_last_launches = 1;
+  return cuda_rc(e);
+}
+
+int moe_mx_quantize(const moe_bf16* src, int rows, int cols, const int32_t* offsets, int E,
+                    uint8_t* q, uint8_t* sc, uint8_t* qT, uint8_t* sT, int32_t* err,
+                    void* stream) {
+  g_last_launches = 0;
+  if (E < 1 || E > MOE_MAX_EXPERTS || rows < 0 || cols <= 0 || rows % 32 || cols % 32)
+    return MOE_E_SIZE;
+  if (rows == 0) return MOE_OK;
+  if (!src || !offsets || !q || !sc || !err || (qT && !sT)) return MOE_E_NULL;
+  if (misaligned(src) || misaligned(q)) return MOE_E_ALIGN;
+  const int sms = num_sms_current();
+  if (sms <= 0) return MOE_E_CUDA;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  ev_begin(s);
+  const cudaError_t e = moe::launch_mx_quantize_act(src, rows, cols, offsets, E, q, sc, qT, sT,
+                                                    err, sms, s);
+  ev_end(s);
+  g_last_launches = 1;
+  return cuda_rc(e);
 }
 
 }  // extern "C"

@@ -19,6 +19,7 @@
 #include <cuda_runtime.h>
 
 #include "gemm.cuh"
+#include "mx.cuh"
 #include "ptx.cuh"
 
 namespace moe {
@@ -225,8 +226,74 @@ __device__ __forceinline__ void epilogue_chunk(const GemmArgs& g, const Tile& tl
   }
 }
 
+// FC1 epilogue with MXFP8 output: one 32-value block of A per call (64
+// accumulator columns when gated, 32 for squared ReLU).  A is rounded to
+// bf16 first; the codes quantise those bf16 values.
+template <int ACT>
+__device__ __forceinline__ void fc1_mx_block(const GemmArgs& g, const Tile& tl, int row_in_tile,
+                                             int lane, int q, int cb, const uint32_t (&r0)[32],
+                                             const uint32_t (&r1)[32]) {
+  constexpr bool GATED = (ACT != MOE_ACT_SRELU);
+  const int acc_col = tl.n0 + cb * (GATED ? 64 : 32);
+  if (acc_col >= g.N) return;                       // uniform across the CTA
+  const bool valid = row_in_tile < tl.rows;
+  const long long grow = tl.row0 + row_in_tile;
+  float a[32];
+  if constexpr (GATED) {
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      a[i] = gate_phi<ACT>(__uint_as_float(r0[2 * i])) * __uint_as_float(r0[2 * i + 1]);
+      a[16 + i] = gate_phi<ACT>(__uint_as_float(r1[2 * i])) * __uint_as_float(r1[2 * i + 1]);
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      const float h = fmaxf(__uint_as_float(r0[i]), 0.f);
+      a[i] = h * h;
+    }
+  }
+  uint32_t pk[16];
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    pk[i] = pack_bf16x2(a[2 * i], a[2 * i + 1]);
+    a[2 * i] = bf16_lo(pk[i]);
+    a[2 * i + 1] = bf16_hi(pk[i]);
+  }
+  const int acol = GATED ? acc_col / 2 : acc_col;  // first A column of the block
+  const int b = acol / 32;
+  uint32_t qw[8];
+  const uint32_t sc = mx_quant32(a, qw);
+  if (valid) {
+    uint16_t* pa = g.out + grow * g.ldo + acol;
+#pragma unroll
+    for (int v = 0; v < 4; ++v) st_global_v4(pa + 8 * v, pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+    if (g.out2) {
+      store_row32(g.out2 + grow * g.ldo2 + acc_col, r0);
+      if constexpr (GATED) store_row32(g.out2 + grow * g.ldo2 + acc_col + 32, r1);
+    }
+    uint4* pq = reinterpret_cast<uint4*>(g.mx_q + grow * g.n_a + acol);
+    pq[0] = make_uint4(qw[0], qw[1], qw[2], qw[3]);
+    pq[1] = make_uint4(qw[4], qw[5], qw[6], qw[7]);
+    const long long chunk = static_cast<long long>(tl.row0 / 32) * (g.n_a / 128) + b / 4;
+    g.mx_s[chunk * 512 + mx_chunk_off(row_in_tile, b & 3)] = static_cast<uint8_t>(sc);
+  }
+  // transposed copy: this warp's 32 rows form one column block
+  if (g.mx_qT != nullptr && q * 32 < tl.rows) {
+    uint32_t my_sc = 0;
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+      uint32_t code;
+      const uint32_t scj = mx_quant_lanes(a[j], code);
+      g.mx_qT[static_cast<long long>(acol + j) * g.M_cap + grow] = static_cast<uint8_t>(code);
+      if (lane == j) my_sc = scj;
+    }
+    g.mx_sT[static_cast<long long>(acol + lane) * (g.M_cap / 32) + grow / 32] =
+        static_cast<uint8_t>(my_sc);
+  }
+}
+
 // ------------------------------------------------------------ the kernel
-template <GemmKind KIND, int ACT>
+template <GemmKind KIND, int ACT, bool MX = false>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                         const __grid_constant__ CUtensorMap tmB, const GemmArgs g) {
@@ -273,8 +340,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     bool bad = false;
     for (int i = lane; i <= g.E; i += 32) {
       int v = g.offsets[i];
-      if (v < 0 || v > g.M_cap) bad = true;
+      if (v < 0 || v > g.M_cap || (MX && (v & 31))) bad = true;
       s_off[i] = min(max(v, 0), g.M_cap);
+      if (MX) s_off[i] &= ~31;
     }
     __syncwarp();
     if (lane == 0) {
@@ -440,7 +508,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       if (!__shfl_sync(0xffffffffu, ok, 0)) break;
       tc_fence_after();
       const uint32_t tb = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + buf * BN;
-      if (KIND == GemmKind::kWgrad && tl.kblocks == 0) {
+      if constexpr (KIND == GemmKind::kFc1Act && MX) {
+        constexpr int STEP = (ACT == MOE_ACT_SRELU) ? 32 : 64;
+        for (int cb = 0; cb < BN / STEP; ++cb) {
+          uint32_t r0[32], r1[32];
+          tmem_ld32(tb + cb * STEP, r0);
+          if constexpr (STEP == 64) tmem_ld32(tb + cb * STEP + 32, r1);
+          tmem_wait_ld();
+          fc1_mx_block<ACT>(g, tl, row_in_tile, lane, q, cb, r0, r1);
+        }
+      } else if (KIND == GemmKind::kWgrad && tl.kblocks == 0) {
         uint32_t z[32];
 #pragma unroll
         for (int i = 0; i < 32; ++i) z[i] = 0;
@@ -468,10 +545,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   }
 }
 
-template <GemmKind KIND, int ACT>
+template <GemmKind KIND, int ACT, bool MX = false>
 cudaError_t launch_t(const CUtensorMap& ta, const CUtensorMap& tb, const GemmArgs& g, int num_sms,
                      cudaStream_t s) {
-  auto kern = grouped_gemm_kernel<KIND, ACT>;
+  auto kern = grouped_gemm_kernel<KIND, ACT, MX>;
   const size_t smem = smem_bytes(MOE_MAX_EXPERTS);
   static bool attr_set = false;  // per process; the library drives one device
   if (!attr_set) {
@@ -488,7 +565,16 @@ cudaError_t launch_t(const CUtensorMap& ta, const CUtensorMap& tb, const GemmArg
 
 cudaError_t launch_grouped_gemm(GemmKind kind, int act, const CUtensorMap& ta,
                                 const CUtensorMap& tb, const GemmArgs& g, int num_sms,
-                                cudaStream_t s) {
+                                cudaStream_t s, bool mx) {
+  if (mx) {
+    if (kind != GemmKind::kFc1Act) return cudaErrorInvalidValue;
+    switch (act) {
+      case MOE_ACT_SWIGLU: return launch_t<GemmKind::kFc1Act, MOE_ACT_SWIGLU, true>(ta, tb, g, num_sms, s);
+      case MOE_ACT_GEGLU: return launch_t<GemmKind::kFc1Act, MOE_ACT_GEGLU, true>(ta, tb, g, num_sms, s);
+      case MOE_ACT_SRELU: return launch_t<GemmKind::kFc1Act, MOE_ACT_SRELU, true>(ta, tb, g, num_sms, s);
+      default: return cudaErrorInvalidValue;
+    }
+  }
 #define MOE_ACT_SWITCH(KIND)                                                         \
   switch (act) {                                                                     \
     case MOE_ACT_SWIGLU: return launch_t<KIND, MOE_ACT_SWIGLU>(ta, tb, g, num_sms, s); \

@@ -33,12 +33,18 @@ struct GemmArgs {
   const uint16_t* aux;     // kDgradAct: saved H
   long long ld_aux;
   int32_t* err;
+  // kFc1Act with MXFP8 output (all NULL otherwise)
+  uint8_t* mx_q;           // [M_cap, n] E4M3 codes of A (row-wise 1x32 blocks)
+  uint8_t* mx_s;           // row-wise scales, MMA-tiled by 128-row tile start
+  uint8_t* mx_qT;          // [n, M_cap] codes of A^T (32x1 blocks) or NULL
+  uint8_t* mx_sT;          // [n, M_cap/32] scales of mx_qT
+  int n_a;                 // columns of A (n)
 };
 
 // Launches the persistent grouped GEMM of `kind` (act: MOE_ACT_*) on `s`.
 cudaError_t launch_grouped_gemm(GemmKind kind, int act, const CUtensorMap& ta,
                                 const CUtensorMap& tb, const GemmArgs& args, int num_sms,
-                                cudaStream_t s);
+                                cudaStream_t s, bool mx = false);
 
 // Box shapes (elements) the kernels expect for each operand's tensor map.
 constexpr int kBM = 128, kBN = 256, kBK = 64;

@@ -69,6 +69,39 @@ typedef uint16_t moe_bf16;
 
 /* flags */
 #define MOE_FLAG_SAVE_H 1      /* forward also stores H (needed by backward)   */
+#define MOE_FLAG_MXFP8 2       /* FC1 also emits MXFP8 A; FC2 is block-scaled
+                                  MXFP8 (arguments in moe_mx_fwd)              */
+
+/*
+ * MXFP8 data ([CuTe] "무엇을 해결하려는가" / "핵심 아이디어": an MXFP8 output
+ * and its transposed copy written by the GEMM; [TE] "Transformer Engine이
+ * 제공하는 세 가지 구성 요소": group-aware MXFP8 quantisation and an MXFP8
+ * grouped GEMM).  Block rule (OCP MX v1.0): 32 values share a scale
+ * X = 2^e, e = clamp(floor(log2 amax) - 8, -127, 127), stored as the E8M0
+ * byte e + 127; each value is stored as E4M3(v / X), round to nearest even,
+ * saturated to +-448.
+ *
+ * "MMA-tiled" scale layout: 128 rows (of A, or columns of W2) x 4
+ * consecutive 32-blocks of the reduction index form one 512-byte chunk; the
+ * scale of row r (0..127 inside the chunk) and block b (0..3) is byte
+ * (r % 32) * 16 + (r / 32) * 4 + b.
+ *   A scales:  chunk (g, c) at byte (g * (n/128) + c) * 512, where g =
+ *              row0 / 32 for the 128-row tile [row0, row0+128) that holds
+ *              the row (tiles start at offsets[e] + 128 i), c = block / 4.
+ *              Size (M_cap/32) * (n/128) * 512 bytes.
+ *   W2 scales: expert e, block b of rows (b = k / 32), column c: chunk
+ *              (b/4, c/128) at byte e*(n/32)*d + ((b/4)*(d/128) + c/128)*512.
+ *              Size E * (n/32) * d bytes.
+ */
+typedef struct moe_mx_fwd {
+  const uint8_t* w2_q;  /* [E, n, d] E4M3 codes of W2 (moe_mx_quantize_weights) */
+  const uint8_t* w2_s;  /* W2 scales, MMA-tiled                                   */
+  uint8_t* a_q;         /* [M_cap, n] E4M3 codes of A, row-wise 1x32 blocks        */
+  uint8_t* a_s;         /* A row-wise scales, MMA-tiled                            */
+  uint8_t* a_qT;        /* [n, M_cap] codes of A^T, 32x1 blocks inside one expert,
+                           or NULL (then a_sT is ignored)                          */
+  uint8_t* a_sT;        /* [n, M_cap/32] E8M0 scales of a_qT                       */
+} moe_mx_fwd;
 
 /* Limits. */
 #define MOE_MAX_EXPERTS 1024
@@ -177,12 +210,20 @@ int moe_unpermute(const moe_bf16* src, const float* probs,
  *   y_perm  [M_cap, d]  bf16      written
  * Rows outside every expert's range are not written.  An expert with no
  * rows costs (almost) nothing.
+ *
+ * With MOE_FLAG_MXFP8 (`mx` required): FC1's epilogue also writes the
+ * MXFP8 codes/scales of the bf16-rounded A (row-wise, and the transposed
+ * copy if mx->a_qT != NULL), and FC2 computes Y_e from mx->a_q / a_s and
+ * mx->w2_q / w2_s with block-scaled MXFP8 MMAs (W2 is then not read).
+ * Requires n and d multiples of 128, M_cap a multiple of 32 and offsets
+ * that are multiples of 32 (route with align = 32; otherwise
+ * MOE_DEV_BAD_OFFSETS is set).
  */
 int moe_grouped_mlp_fwd(const moe_bf16* x_perm, const int32_t* offsets,
                         int E, int M_cap, int d, int n, const moe_bf16* W1,
                         const moe_bf16* W2, int act, int flags,
                         moe_bf16* h_saved, moe_bf16* a, moe_bf16* y_perm,
-                        int32_t* err, void* stream);
+                        const moe_mx_fwd* mx, int32_t* err, void* stream);
 
 /*
  * moe_grouped_mlp_bwd - backward of moe_grouped_mlp_fwd.
@@ -211,6 +252,28 @@ int moe_grouped_mlp_bwd(const moe_bf16* x_perm, const moe_bf16* h_saved,
                         int act, int flags, moe_bf16* dh, moe_bf16* dx_perm,
                         moe_bf16* dW1, moe_bf16* dW2, int32_t* err,
                         void* stream);
+
+/*
+ * moe_mx_quantize_weights - MXFP8 copy of W2 for the block-scaled FC2
+ * (blocks of 32 consecutive rows, FC2's reduction index, per column).
+ *   W2 [E, n, d] bf16 -> w2_q [E, n, d] E4M3 codes, w2_s MMA-tiled scales
+ *   (E * (n/32) * d bytes).  n, d multiples of 128.
+ */
+int moe_mx_quantize_weights(const moe_bf16* W2, int E, int n, int d,
+                            uint8_t* w2_q, uint8_t* w2_s, void* stream);
+
+/*
+ * moe_mx_quantize - group-aware MXFP8 quantisation of a ragged activation
+ * ([TE] "Transformer Engine이 제공하는 세 가지 구성 요소").
+ *   src [rows, cols] bf16, offsets [E+1] (multiples of 32; rows at or past
+ *   offsets[E] are not touched).  Writes q [rows, cols] codes with row-wise
+ *   1x32 blocks and s [rows, cols/32] scales; and, if qT != NULL, the
+ *   transposed copy qT [cols, rows] with column-wise 32x1 blocks inside one
+ *   expert and sT [cols, rows/32].  cols, rows multiples of 32.
+ */
+int moe_mx_quantize(const moe_bf16* src, int rows, int cols,
+                    const int32_t* offsets, int E, uint8_t* q, uint8_t* s,
+                    uint8_t* qT, uint8_t* sT, int32_t* err, void* stream);
 
 /*
  * Measurement hook (per host thread; no counterpart on the pages).

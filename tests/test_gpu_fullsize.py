@@ -1,0 +1,212 @@
+"""Full-size parity at the benchmark's sizes and launch configuration.
+
+The GPU runs exactly the step bench.py times (its inputs and call
+sequence).  The oracle then recomputes sampled outputs one row or one
+element at a time from the same seeded inputs.  The inputs are drawn from
+the ``workloads`` generator (integer hashing + a table gather, so the CPU
+and GPU produce identical bits, checked below); the oracle's copies are
+generated on the device by that module and moved to the host, never read
+from libmoe's outputs."""
+import numpy as np
+import pytest
+import torch
+
+import bench as BE
+import oracle as O
+import workloads as WL
+from _helpers import assert_rms_close, f64
+
+pytestmark = [pytest.mark.gpu, pytest.mark.slow]
+
+C1 = "balanced_e8_m4096_k8192_n4096_swiglu"
+C2 = "zipf_t4096_d7168_e256_top8_n2048_swiglu"
+
+
+def test_generator_cpu_equals_gpu():
+    idx = torch.randint(0, 1 << 40, (100000,), dtype=torch.int64)
+    a = WL.normal_at(idx, (3, WL.W_GATE, 7), 0.02)
+    b = WL.normal_at(idx.cuda(), (3, WL.W_GATE, 7), 0.02).cpu()
+    assert torch.equal(a, b)
+
+
+def _expert_weights(w, e):
+    d, n = w.d, w.n
+    W1 = (WL.w1_interleaved(w.cfg_id, 1, d, n, w.w_std, "cuda", experts=[e]) if w.gated else
+          WL.w1_plain(w.cfg_id, 1, d, n, w.w_std, "cuda", experts=[e]))[0]
+    W2 = WL.w2(w.cfg_id, 1, n, d, w.w_std, "cuda", experts=[e])[0]
+    return f64(W1), f64(W2)
+
+
+def _rows(shape_cols, key, std, rows):
+    idx = (torch.as_tensor(rows, dtype=torch.int64)[:, None] * shape_cols +
+           torch.arange(shape_cols, dtype=torch.int64)[None, :]).cuda()
+    return f64(WL.normal_at(idx, key, std))
+
+
+@pytest.fixture(scope="module")
+def c1_run():
+    import dropless_grouped_gemm_gb300 as M
+    M.lib()
+    w = WL.WORKLOADS[C1]
+    inp, o = BE.make_inputs(w, "cuda")
+    step = BE.make_step(w, inp, o)
+    assert step() == 6
+    torch.cuda.synchronize()
+    assert int(o["err"].item()) == 0
+    yield w, inp, o
+    del inp, o
+    torch.cuda.empty_cache()
+
+
+def test_c1_rows_forward_backward(c1_run):
+    w, inp, o = c1_run
+    m = w.T // w.E
+    rng = np.random.default_rng(0)
+    for e in (0, 5):
+        W1, W2 = _expert_weights(w, e)
+        rows = e * m + np.sort(rng.choice(m, 6, replace=False))
+        x = _rows(w.d, (w.cfg_id, WL.X, 0), w.x_std, rows)
+        dy = _rows(w.d, (w.cfg_id, WL.DY, 0), w.dy_std, rows)
+        off = np.array([0, len(rows)])
+        H, A, Y = O.grouped_mlp_fwd(x, off, W1[None], W2[None], w.act)
+        dH, dX, _, _ = O.grouped_mlp_bwd(x, H, A, dy, off, W1[None], W2[None], w.act)
+        r = torch.as_tensor(rows).cuda()
+        assert_rms_close(f64(o["h"][r]), H, f"C1 e{e} H")
+        assert_rms_close(f64(o["a"][r]), A, f"C1 e{e} A")
+        assert_rms_close(f64(o["y_perm"][r]), Y, f"C1 e{e} Y")
+        assert_rms_close(f64(o["dh"][r]), dH, f"C1 e{e} dH")
+        assert_rms_close(f64(o["dx_perm"][r]), dX, f"C1 e{e} dX")
+
+
+def test_c1_weight_gradient_entries(c1_run):
+    """dW2[e][i, c] and dW1[e][k, c] for sampled (i|k, c): full reductions
+    over the expert's 4096 rows."""
+    w, inp, o = c1_run
+    m = w.T // w.E
+    e = 3
+    W1, W2 = _expert_weights(w, e)
+    rows = np.arange(e * m, (e + 1) * m)
+    x = _rows(w.d, (w.cfg_id, WL.X, 0), w.x_std, rows)
+    dy = _rows(w.d, (w.cfg_id, WL.DY, 0), w.dy_std, rows)
+    rng = np.random.default_rng(1)
+    js = np.sort(rng.choice(w.n, 16, replace=False))         # A / dA columns
+    cs = np.sort(rng.choice(w.d, 16, replace=False))         # d columns
+    ks = np.sort(rng.choice(w.d, 16, replace=False))
+    # H columns of the sampled gate/up pairs, A, dA, dH (rounding as stored)
+    hcols = np.stack([2 * js, 2 * js + 1], 1).reshape(-1)
+    h = O.bf16_round(x @ W1[:, hcols])
+    a = O.bf16_round(O.act_forward(x @ W1[:, hcols], w.act))
+    dA = dy @ W2[js, :].T
+    dh = O.bf16_round(O.act_backward(h, dA, w.act))
+    dW2_ref = O.bf16_round(a.T @ dy[:, cs])                    # [16, 16]
+    dW1_ref = O.bf16_round(x[:, ks].T @ dh)                    # [16, 32]
+    got2 = f64(o["dW2"][e][torch.as_tensor(js).cuda()][:, torch.as_tensor(cs).cuda()])
+    got1 = f64(o["dW1"][e][torch.as_tensor(ks).cuda()][:, torch.as_tensor(hcols).cuda()])
+    assert_rms_close(got2, dW2_ref, "C1 dW2 entries")
+    assert_rms_close(got1, dW1_ref, "C1 dW1 entries")
+
+
+@pytest.fixture(scope="module")
+def c2_run():
+    import dropless_grouped_gemm_gb300 as M
+    M.lib()
+    w = WL.WORKLOADS[C2]
+    inp, o = BE.make_inputs(w, "cuda")
+    step = BE.make_step(w, inp, o)
+    step()
+    torch.cuda.synchronize()
+    assert int(o["err"].item()) == 0
+    yield w, inp, o
+    del inp, o
+    torch.cuda.empty_cache()
+
+
+def test_c2_routing_bit_exact(c2_run):
+    w, inp, o = c2_run
+    idx, _ = WL.route_inputs(w)
+    ro = O.route_offsets(idx, w.E, w.align, w.M_cap)
+    r = o["route"]
+    for k_ in ("counts", "offsets", "row_of_pair", "pair_of_row"):
+        assert r[k_].cpu().numpy().tolist() == ro[k_].tolist(), k_
+    # the permuted activations are exact copies of the token rows
+    rows = np.random.default_rng(2).choice(w.T * w.k, 64, replace=False)
+    xp = f64(o["x_perm"][torch.as_tensor(ro["row_of_pair"][rows]).cuda()])
+    tok = _rows(w.d, (w.cfg_id, WL.X, 0), w.x_std, rows // w.k)
+    assert np.array_equal(xp, tok)
+
+
+def test_c2_expert_rows_and_token_outputs(c2_run):
+    """Hot expert (~4000 rows), a small one and a one-row one: H/A/Y rows and
+    dX rows; then whole-layer outputs of sampled tokens (combine over their
+    8 experts) and their router-score gradients."""
+    w, inp, o = c2_run
+    idx, probs = WL.route_inputs(w)
+    ro = O.route_offsets(idx, w.E, w.align, w.M_cap)
+    counts = ro["counts"]
+    off = ro["offsets"]
+    small = [int(e) for e in np.argsort(counts) if counts[e] > 0][:2]
+    cache = {}
+
+    def wts(e):
+        if e not in cache:
+            cache[e] = _expert_weights(w, e)
+        return cache[e]
+
+    rng = np.random.default_rng(3)
+    for e in [0] + small:
+        W1, W2 = wts(e)
+        rr = np.arange(off[e], off[e + 1])
+        rows = rr if len(rr) <= 6 else np.sort(rng.choice(rr, 6, replace=False))
+        pairs = ro["pair_of_row"][rows]
+        x = _rows(w.d, (w.cfg_id, WL.X, 0), w.x_std, pairs // w.k)
+        dO = _rows(w.d, (w.cfg_id, WL.DO, 0), w.dy_std, pairs // w.k)
+        dy = O.bf16_round(probs.reshape(-1)[pairs].astype(np.float64)[:, None] * dO)
+        o1 = np.array([0, len(rows)])
+        H, A, Y = O.grouped_mlp_fwd(x, o1, W1[None], W2[None], w.act)
+        dH, dX, _, _ = O.grouped_mlp_bwd(x, H, A, dy, o1, W1[None], W2[None], w.act)
+        r = torch.as_tensor(rows).cuda()
+        assert_rms_close(f64(o["a"][r]), A, f"C2 e{e} A")
+        assert_rms_close(f64(o["y_perm"][r]), Y, f"C2 e{e} Y")
+        assert_rms_close(f64(o["dh"][r]), dH, f"C2 e{e} dH")
+        assert_rms_close(f64(o["dx_perm"][r]), dX, f"C2 e{e} dX")
+    # whole-layer outputs of two tokens
+    toks = [5, 4000]
+    ys, dss, outs = [], [], []
+    for t in toks:
+        x = _rows(w.d, (w.cfg_id, WL.X, 0), w.x_std, [t])
+        dO = _rows(w.d, (w.cfg_id, WL.DO, 0), w.dy_std, [t])
+        acc = np.zeros(w.d)
+        for j in range(w.k):
+            e = int(idx[t, j])
+            W1, W2 = wts(e)
+            _, _, Y = O.grouped_mlp_fwd(x, np.array([0, 1]), W1[None], W2[None], w.act)
+            acc += float(probs[t, j]) * Y[0]
+            dss.append(float(dO[0] @ Y[0]))
+        outs.append(O.bf16_round(acc))
+    got = f64(o["out"][torch.as_tensor(toks).cuda()])
+    assert_rms_close(got, np.stack(outs), "C2 token outputs")
+    assert_rms_close(o["dprobs"][torch.as_tensor(toks).cuda()].cpu().numpy().reshape(-1),
+                     np.array(dss), "C2 router-score gradients", rtol=0)
+
+
+def test_c2_weight_gradients_small_expert_and_empty(c2_run):
+    w, inp, o = c2_run
+    idx, probs = WL.route_inputs(w)
+    ro = O.route_offsets(idx, w.E, w.align, w.M_cap)
+    counts, off = ro["counts"], ro["offsets"]
+    e = int([e for e in np.argsort(counts) if counts[e] > 1][0])
+    W1, W2 = _expert_weights(w, e)
+    rows = np.arange(off[e], off[e + 1])
+    pairs = ro["pair_of_row"][rows]
+    x = _rows(w.d, (w.cfg_id, WL.X, 0), w.x_std, pairs // w.k)
+    dO = _rows(w.d, (w.cfg_id, WL.DO, 0), w.dy_std, pairs // w.k)
+    dy = O.bf16_round(probs.reshape(-1)[pairs].astype(np.float64)[:, None] * dO)
+    o1 = np.array([0, len(rows)])
+    H, A, _ = O.grouped_mlp_fwd(x, o1, W1[None], W2[None], w.act)
+    _, _, dW1, dW2 = O.grouped_mlp_bwd(x, H, A, dy, o1, W1[None], W2[None], w.act)
+    assert_rms_close(f64(o["dW2"][e]), dW2[0], f"C2 dW2[{e}]")
+    assert_rms_close(f64(o["dW1"][e]), dW1[0], f"C2 dW1[{e}]")
+    empty = [int(e) for e in range(w.E) if counts[e] == 0][:3]
+    for e in empty:
+        assert float(o["dW1"][e].abs().max()) == 0.0
+        assert float(o["dW2"][e].abs().max()) == 0.0
