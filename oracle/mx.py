@@ -19,7 +19,7 @@ from __future__ import annotations
 import numpy as np
 
 __all__ = [
-    "E4M3_MAX", "e4m3_decode_table", "e4m3_decode", "e4m3_encode",
+    "E4M3_MAX", "e4m3_decode_table", "e4m3_decode", "e4m3_encode", "e4m3_encode_bruteforce",
     "e8m0_exponent", "mx_quantize_blocks", "mx_quantize_rows",
     "mx_quantize_cols", "mx_quantize_weights", "mx_dequantize", "mx_fc2",
 ]
@@ -53,12 +53,15 @@ def e4m3_decode(codes) -> np.ndarray:
     return _DEC[np.asarray(codes, dtype=np.uint8)]
 
 
-def e4m3_encode(v) -> np.ndarray:
+def e4m3_encode_bruteforce(v) -> np.ndarray:
     """Brute-force nearest finite E4M3 code, ties to the even code (even
     mantissa), magnitudes above 448 saturate to 448; the sign bit is kept
-    (so -0 and negative values that round to zero give 0x80)."""
+    (so -0 and negative values that round to zero give 0x80).  This is the
+    definition; ``e4m3_encode`` computes the same function faster."""
     v = np.asarray(v, dtype=np.float64)
-    a = np.abs(v).reshape(-1)
+    # saturate first: beyond 448 every magnitude maps to 448 (measuring
+    # distances from huge values would also lose the codes' spacing)
+    a = np.minimum(np.abs(v).reshape(-1), E4M3_MAX)
     dist = np.abs(a[:, None] - _POS_VALS[None, :])
     best = dist.min(axis=1, keepdims=True)
     cand = dist == best
@@ -68,6 +71,23 @@ def e4m3_encode(v) -> np.ndarray:
     pick = np.where(even.any(axis=1), even.argmax(axis=1), cand.argmax(axis=1))
     code = _POS_CODES[pick].astype(np.uint8)
     code = code | np.where(np.signbit(v.reshape(-1)), 0x80, 0).astype(np.uint8)
+    return code.reshape(v.shape)
+
+
+def e4m3_encode(v) -> np.ndarray:
+    """Same function as ``e4m3_encode_bruteforce`` (nearest finite code,
+    ties to even, saturating, sign kept), found by bisection in the sorted
+    table of the 127 non-negative finite values instead of a full scan."""
+    v = np.asarray(v, dtype=np.float64)
+    a = np.minimum(np.abs(v).reshape(-1), E4M3_MAX)
+    hi = np.clip(np.searchsorted(_POS_VALS, a, side="left"), 0, 0x7E)   # first value >= a
+    lo = np.clip(hi - 1, 0, 0x7E)
+    dlo = a - _POS_VALS[lo]
+    dhi = _POS_VALS[hi] - a
+    pick = np.where(dhi < dlo, hi, lo)
+    tie = (dhi == dlo) & (hi != lo)
+    pick = np.where(tie, np.where((hi & 1) == 0, hi, lo), pick)
+    code = pick.astype(np.uint8) | np.where(np.signbit(v.reshape(-1)), 0x80, 0).astype(np.uint8)
     return code.reshape(v.shape)
 
 

@@ -47,6 +47,22 @@ def test_e4m3_encode_exhaustive_bf16_vs_library():
     assert (ours == lib).all()
 
 
+def test_fast_encoder_equals_bruteforce_definition():
+    """Every finite bf16 value (both signs, beyond 448 too), random doubles,
+    and every exact tie between neighbouring codes."""
+    bits = np.arange(1 << 16, dtype=np.uint32)
+    with np.errstate(invalid="ignore"):
+        v = (bits << 16).view(np.float32).astype(np.float64)
+    v = v[np.isfinite(v)]
+    assert (O.e4m3_encode(v) == O.e4m3_encode_bruteforce(v)).all()
+    rng = np.random.default_rng(24)
+    r = rng.standard_normal(200000) * np.exp(rng.uniform(-25, 8, 200000))
+    assert (O.e4m3_encode(r) == O.e4m3_encode_bruteforce(r)).all()
+    t = O.e4m3_decode_table()[:0x7F]
+    mids = np.concatenate([(t[:-1] + t[1:]) / 2, -(t[:-1] + t[1:]) / 2])
+    assert (O.e4m3_encode(mids) == O.e4m3_encode_bruteforce(mids)).all()
+
+
 def test_e4m3_saturation_and_ties():
     enc = lambda x: int(O.e4m3_encode(np.array([x]))[0])
     for v in (448.0, 460.0, 464.0, 480.0, 511.0, 1e6):
