@@ -18,6 +18,8 @@
 // pair_of_row is first filled with -1 (route_fill).
 #include <cuda_runtime.h>
 
+#include <mutex>
+
 #include "ptx.cuh"
 #include "route.cuh"
 
@@ -193,6 +195,36 @@ cudaError_t launch_route(const int32_t* topk_idx, int T, int k, int E, int align
     ++*launches;
   }
   return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------- no-alloc
+// Scratch for callers that cannot allocate device memory: a fixed array in
+// the library's own device image.  Every GPU that loads libmoe holds it
+// (kRouteScratchWords * 4 bytes) until the process exits.  Host code must not
+// pass the array's name to a kernel (on the host it is only a stand-in);
+// the device address comes from cudaGetSymbolAddress, looked up once per
+// device with that device current.
+static __device__ __align__(256) int32_t g_route_scratch[kRouteScratchWords];
+
+namespace {
+std::mutex g_scratch_mu;
+void* g_scratch_ptr[64] = {nullptr};
+}  // namespace
+
+cudaError_t route_scratch_address(void** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(g_scratch_mu);
+  if (g_scratch_ptr[dev] == nullptr) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_route_scratch);
+    if (e != cudaSuccess) return e;
+    g_scratch_ptr[dev] = p;
+  }
+  *out = g_scratch_ptr[dev];
+  return cudaSuccess;
 }
 
 }  // namespace moe

@@ -10,6 +10,13 @@ namespace moe {
 
 size_t route_workspace_bytes(int T, int k, int E);
 
+// Fixed scratch of the no-allocation routing entry point: 1 MiB.
+constexpr size_t kRouteScratchWords = 262144;
+
+// Device address of that scratch on the current device (looked up once per
+// device, then cached).
+cudaError_t route_scratch_address(void** out);
+
 // Enqueues the routing-layout kernels; *launches receives their number.
 cudaError_t launch_route(const int32_t* topk_idx, int T, int k, int E, int align, int M_cap,
                          int32_t* counts, int32_t* offsets, int32_t* row_of_pair,

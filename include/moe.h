@@ -150,6 +150,34 @@ int moe_route_offsets(const int32_t* topk_idx, int T, int k, int E, int align,
                       int32_t* err, void* stream);
 
 /*
+ * moe_route_offsets_noalloc - moe_route_offsets for callers that cannot
+ * allocate device memory.  The pages have no counterpart; this exists for
+ * code that runs where cudaMalloc is off limits: inside a CUDA-graph
+ * capture that must not grow a memory pool, under an allocator-free
+ * runtime, or in a plugin whose host framework owns every allocation and
+ * offers no scratch.  Same arguments and results as moe_route_offsets,
+ * minus the workspace: the scratch is a fixed 1 MiB array inside the
+ * library's device image (every GPU that loads the library holds it until
+ * the process exits).
+ *   - Limit: moe_route_workspace_size(T, k, E) =
+ *     (ceil(T*k / 4096) + 1) * E * 4 bytes must be <= 1 MiB (E = 1024:
+ *     T*k <= 1,044,480 pairs; E = 256: T*k <= 4,190,208); larger sizes
+ *     return MOE_E_WORKSPACE and enqueue nothing.
+ *   - The first call on each device looks the array's device address up
+ *     (cudaGetSymbolAddress, with that device current) and caches it; make
+ *     that first call before any stream capture.
+ *   - No cudaMalloc, cudaFree or allocating library call is made.  Nothing
+ *     in the scratch needs to start at zero (each call writes every word it
+ *     reads), but all calls share it: calls whose kernels can overlap on the
+ *     GPU (different streams without ordering between them) race.
+ */
+int moe_route_offsets_noalloc(const int32_t* topk_idx, int T, int k, int E,
+                              int align, int M_cap, int32_t* counts,
+                              int32_t* offsets, int32_t* row_of_pair,
+                              int32_t* pair_of_row, int32_t* true_total,
+                              int32_t* err, void* stream);
+
+/*
  * moe_permute - expert-major gather ([TE] "최적화 2: NCCL EP": dispatch
  * permutes the token rows; here without communication).
  *
