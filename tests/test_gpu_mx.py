@@ -1,0 +1,174 @@
+"""MXFP8 path vs the oracle's OCP MX quantiser.
+
+* The weight quantiser and the standalone group-aware quantiser run on
+  generator inputs (plus planted edge blocks): codes and scales must be
+  bit-exact.
+* The fused FC1 epilogue quantises its own bf16 A.  The oracle computes A
+  independently (float64, rounded to bf16 once); the two agree except for
+  one-step rounding differences.  Where a 32-value block of A agrees bit for
+  bit, the quantisation decision is taken on the same input by both sides,
+  so codes and scale must be bit-exact there; the test requires most blocks
+  to qualify and checks the rest through the tolerance on the decoded values.
+* The block-scaled FC2 output is compared with the oracle's MX FC2 on the
+  oracle's own quantised A and W2, within the bf16 tolerance."""
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+import workloads as WL
+from _helpers import assert_rms_close, cuda_i32, f64
+
+pytestmark = pytest.mark.gpu
+
+
+def _lib():
+    import dropless_grouped_gemm_gb300 as M
+    M.lib()
+    return M
+
+
+def decode_w2_scales(s, E, n, d):
+    s = s.cpu().numpy()
+    e, b, c = np.meshgrid(np.arange(E), np.arange(n // 32), np.arange(d), indexing="ij")
+    off = (e * (n // 32) * d + ((b // 4) * (d // 128) + c // 128) * 512 + (c % 32) * 16 +
+           ((c % 128) // 32) * 4 + b % 4)
+    return s[off]
+
+
+def decode_a_scales(s, offsets, M_cap, n):
+    """[M_cap, n/32] row-wise scales from the MMA-tiled layout (-1 outside
+    every expert)."""
+    s = s.cpu().numpy()
+    out = -np.ones((M_cap, n // 32), np.int64)
+    E = len(offsets) - 1
+    b = np.arange(n // 32)
+    for e in range(E):
+        for row0 in range(int(offsets[e]), int(offsets[e + 1]), 128):
+            for r in range(row0, min(row0 + 128, int(offsets[e + 1]))):
+                rr = r - row0
+                off = ((row0 // 32) * (n // 128) + b // 4) * 512 + (rr % 32) * 16 + (rr // 32) * 4 + b % 4
+                out[r] = s[off]
+    return out
+
+
+def _plant(v):
+    """Edge blocks into a float64 [rows, cols] array (values stay bf16)."""
+    v = v.copy()
+    v[0, 0:32] = 0.0                                      # all-zero block
+    v[1, 0:32] = 2.0 ** np.arange(-10, 22)[:32] * 1e-3    # wide range -> many subnormal codes
+    v[1, 0:32] = O.bf16_round(v[1, 0:32])
+    v[2, 0:32] = 2.0 ** 5 * np.linspace(-1.9, 1.9, 32)    # saturating maximum
+    v[2, 0:32] = O.bf16_round(v[2, 0:32])
+    v[3, 32:64] = np.ldexp(1.0, np.arange(32) % 13 - 6) * np.where(np.arange(32) % 2, -1, 1)
+    v[4, 32:64] = -0.0
+    v[4, 40] = 3.0
+    v[5, 0:32] = 1e-30                                    # tiny: code 0 scales
+    v[5, 0:32] = O.bf16_round(v[5, 0:32])
+    return v
+
+
+def test_weight_quantiser_bit_exact():
+    M = _lib()
+    E, n, d = 3, 256, 384
+    W2 = WL.w2(21, E, n, d, 0.02, "cuda")
+    w = f64(W2)
+    w[0] = _plant(w[0])
+    w[2, :, 7] = 0.0                                      # an all-zero column
+    W2 = torch.from_numpy(w).to(torch.bfloat16).cuda()
+    q, s = M.mx_quantize_weights(W2)
+    torch.cuda.synchronize()
+    qo, so = O.mx_quantize_weights(w)
+    assert np.array_equal(q.cpu().numpy(), qo)
+    assert np.array_equal(decode_w2_scales(s, E, n, d), so)
+
+
+def test_group_aware_quantiser_bit_exact():
+    M = _lib()
+    rows, cols = 256, 256
+    offsets = np.array([0, 64, 64, 192, 256 - 32])       # empty expert; last 32 rows unused
+    src = f64(WL.normal((rows, cols), (22, WL.X, 0), 1.0, "cuda"))
+    src = _plant(src)
+    src_t = torch.from_numpy(src).to(torch.bfloat16).cuda()
+    q, s, qT, sT, err = M.mx_quantize(src_t, cuda_i32(offsets))
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    R = int(offsets[-1])
+    qo, so = O.mx_quantize_rows(src[:R])
+    assert np.array_equal(q.cpu().numpy()[:R], qo)
+    assert np.array_equal(s.cpu().numpy()[:R], so)
+    qTo, sTo = O.mx_quantize_cols(src, offsets, rows)
+    assert np.array_equal(qT.cpu().numpy()[:, :R], qTo[:, :R])
+    assert np.array_equal(sT.cpu().numpy()[:, :R // 32], sTo[:, :R // 32])
+
+
+def _mx_case(act, E=4, d=256, n=256, counts=(96, 0, 160, 32), seed=23):
+    off = np.concatenate([[0], np.cumsum(counts)]).astype(np.int64)
+    M_cap = int(off[-1]) + 32
+    x = WL.normal((M_cap, d), (seed, WL.X, 0), 1.0, "cuda")
+    W1 = (WL.w1_plain(seed, E, d, n, 0.05, "cuda") if act == "srelu" else
+          WL.w1_interleaved(seed, E, d, n, 0.05, "cuda"))
+    W2 = WL.w2(seed, E, n, d, 0.05, "cuda")
+    return off, M_cap, x, W1, W2
+
+
+def _check_blocks(gpu_a, ref_a, gpu_q, gpu_s, rows_axis):
+    """Bit-exact codes/scales on blocks whose bf16 input agrees.  Blocks are
+    32 consecutive entries along the last axis; returns the compared count."""
+    ga = gpu_a.reshape(gpu_a.shape[0], -1, 32)
+    ra = ref_a.reshape(ref_a.shape[0], -1, 32)
+    same = (ga == ra).all(axis=2)
+    qo, so = O.mx_quantize_blocks(ga)
+    gq = gpu_q.reshape(gpu_q.shape[0], -1, 32)
+    assert np.array_equal(gq[same], qo[same]), rows_axis
+    assert np.array_equal(gpu_s[same], so[same]), rows_axis
+    return int(same.sum()), same.size
+
+
+@pytest.mark.parametrize("act", ["swiglu", "geglu", "srelu"])
+def test_fused_fc1_mx_epilogue_and_block_scaled_fc2(act):
+    M = _lib()
+    E, d, n = 4, 256, 256
+    off, M_cap, x, W1, W2 = _mx_case(act, E, d, n)
+    buf = M.mx_buffers(E, n, d, M_cap, "cuda")
+    M.mx_quantize_weights(W2, buf["w2_q"], buf["w2_s"])
+    h, a, y, err = M.grouped_mlp_fwd(x, cuda_i32(off), W1, W2, act, save_h=True, mx=buf)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    R = int(off[-1])
+    H, A, _ = O.grouped_mlp_fwd(f64(x), off, f64(W1), f64(W2), act)
+    ga = f64(a)[:R]
+    assert_rms_close(ga, A[:R], f"{act} A (bf16)")
+    # row-wise codes / scales (MMA-tiled scales decoded)
+    gs = decode_a_scales(buf["a_s"], off, M_cap, n)[:R]
+    done, total = _check_blocks(ga, A[:R], buf["a_q"].cpu().numpy()[:R], gs, "rows")
+    assert done >= 0.5 * total, (done, total)
+    # transposed copy: column blocks of 32 rows inside each expert
+    gT = buf["a_qT"].cpu().numpy()[:, :R]
+    gsT = buf["a_sT"].cpu().numpy()[:, :R // 32]
+    done_t, total_t = _check_blocks(ga.T.copy(), A[:R].T.copy(), gT, gsT, "cols")
+    assert done_t >= 0.3 * total_t, (done_t, total_t)
+    # decoded codes everywhere within the MX error of the oracle's A
+    deq = O.mx_dequantize(buf["a_q"].cpu().numpy()[:R], gs.astype(np.uint8), axis_block=1)
+    assert np.linalg.norm(deq - A[:R]) <= 0.05 * np.linalg.norm(A[:R])
+    # block-scaled FC2 vs the oracle's MX FC2 on its own quantised operands
+    qa, sa = O.mx_quantize_rows(A[:R])
+    qw, sw = O.mx_quantize_weights(f64(W2))
+    Yo = O.mx_fc2(qa, sa, qw, sw, off)
+    assert_rms_close(f64(y)[:R], Yo[:R], f"{act} Y (MXFP8 FC2)")
+    # and close to the bf16 product (the MX error is small)
+    _, _, Yb = O.grouped_mlp_fwd(f64(x), off, f64(W1), f64(W2), act)
+    assert np.linalg.norm(f64(y)[:R] - Yb[:R]) <= 0.08 * np.linalg.norm(Yb[:R])
+
+
+def test_mx_requires_32_aligned_offsets():
+    M = _lib()
+    off, M_cap, x, W1, W2 = _mx_case("swiglu", counts=(96, 0, 150, 32))   # 96+150 not aligned
+    Mc = 320                                                             # multiple of 32
+    buf = M.mx_buffers(4, 256, 256, Mc, "cuda")
+    M.mx_quantize_weights(W2, buf["w2_q"], buf["w2_s"])
+    x2 = torch.zeros((Mc, 256), dtype=torch.bfloat16, device="cuda")
+    x2[:M_cap] = x
+    _, _, _, err = M.grouped_mlp_fwd(x2, cuda_i32(off), W1, W2, "swiglu", mx=buf)
+    torch.cuda.synchronize()
+    assert int(err.item()) & M.DEV_BAD_OFFSETS
