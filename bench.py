@@ -50,11 +50,12 @@ KERNELS_BWD = ["fc2_dgrad_dact", "fc2_wgrad", "fc1_dgrad", "fc1_wgrad"]
 # ---------------------------------------------------------------- accounting
 def useful_flops(w, M):
     """fwd + bwd FLOPs of real rows (the pages' arithmetic-intensity model
-    counts the same terms: [Sonic] section on MoE arithmetic intensity)."""
+    counts the same terms: [Sonic] section on MoE arithmetic intensity).
+    Forward-only workloads (the MXFP8 one) have no backward term."""
     n1 = w.n1
     fwd = 2 * M * w.d * n1 + 2 * M * w.n * w.d
     bwd = 2 * M * w.d * w.n + 2 * M * w.n * w.d + 2 * M * n1 * w.d + 2 * M * w.d * n1
-    return fwd, bwd
+    return fwd, (bwd if w.backward else 0)
 
 
 def kernel_work(w, M, E_ne):
@@ -63,6 +64,14 @@ def kernel_work(w, M, E_ne):
     experts, written as zeros for empty ones)."""
     d, n, n1, E = w.d, w.n, w.n1, w.E
     B = 2
+    if w.mxfp8:
+        # FC1 (bf16 MMA) writes bf16 A and MX codes (row-wise and transposed,
+        # 1 B each) and scales; FC2 streams E4M3 codes of A and W2
+        return {
+            "mx_quantize_weights": (0, E * n * d * (2 + 1) + E * (n // 32) * d),
+            "fc1_act": (2 * M * d * n1, B * (M * d + E_ne * d * n1 + M * n) + 2 * M * n + M * n // 16),
+            "fc2": (2 * M * n * d, M * n + M * n // 32 + E_ne * n * d + E_ne * (n // 32) * d + B * M * d),
+        }
     return {
         "fc1_act": (2 * M * d * n1, B * (M * d + E_ne * d * n1 + M * n + M * n1)),
         "fc2": (2 * M * n * d, B * (M * n + E_ne * n * d + M * d)),
@@ -191,6 +200,8 @@ def make_inputs(w, dev):
         o["dprobs"] = torch.empty((w.T, w.k), dtype=torch.float32, device=dev)
         o["ws"] = torch.empty(max(16, M.route_workspace_size(w.T, w.k, E)), dtype=torch.uint8,
                               device=dev)
+        if w.mxfp8:
+            o["mx"] = M.mx_buffers(E, n, d, Mc, dev)
         o["route"] = {
             "counts": torch.empty(E, dtype=torch.int32, device=dev),
             "offsets": torch.empty(E + 1, dtype=torch.int32, device=dev),
@@ -220,6 +231,24 @@ def make_step(w, inp, o):
         return step
 
     T, k = w.T, w.k
+
+    if w.mxfp8:
+        def step_mx():
+            n = 0
+            r = M.route_offsets(inp["topk_idx"], w.E, w.align, w.M_cap, out=o["route"],
+                                workspace=o["ws"])
+            n += M.last_launch_count()
+            M.permute(inp["x"], r["pair_of_row"], k, out=o["x_perm"])
+            n += M.last_launch_count()
+            M.mx_quantize_weights(inp["W2"], o["mx"]["w2_q"], o["mx"]["w2_s"])
+            n += M.last_launch_count()
+            M.grouped_mlp_fwd(o["x_perm"], r["offsets"], inp["W1"], inp["W2"], act, a=o["a"],
+                              y_perm=o["y_perm"], err=o["err"], mx=o["mx"])
+            n += M.last_launch_count()
+            M.unpermute(o["y_perm"], r["row_of_pair"], T, k, probs=inp["probs"], out=o["out"])
+            n += M.last_launch_count()
+            return n
+        return step_mx
 
     def step():
         n = 0
@@ -252,6 +281,8 @@ def make_step(w, inp, o):
 def event_names(w):
     if w.routing == "identity":
         return KERNELS_FWD + KERNELS_BWD
+    if w.mxfp8:
+        return ["route", "permute", "mx_quantize_weights"] + KERNELS_FWD + ["combine"]
     return (["route", "permute"] + KERNELS_FWD + ["combine", "permute_bwd", "router_grad"] +
             KERNELS_BWD + ["unpermute_bwd"])
 
@@ -272,14 +303,25 @@ def oracle_sample(w, rows):
     return x, dy, W1, W2
 
 
-def time_oracle(w, rows, reps=1):
+def oracle_step(w, x, dy, W1, W2, off):
+    """One oracle pass over the sample: fwd+bwd, or for the MXFP8 workload
+    the forward with the MX quantiser and the MXFP8 FC2."""
     import oracle as O
+    H, A, _ = O.grouped_mlp_fwd(x, off, W1, W2, w.act)
+    if w.mxfp8:
+        qa, sa = O.mx_quantize_rows(A)
+        qw, sw = O.mx_quantize_weights(W2)
+        O.mx_fc2(qa, sa, qw, sw, off)
+    else:
+        O.grouped_mlp_bwd(x, H, A, dy, off, W1, W2, w.act)
+
+
+def time_oracle(w, rows, reps=1):
     x, dy, W1, W2 = oracle_sample(w, rows)
     off = np.array([0, rows])
     t0 = time.perf_counter()
     for _ in range(reps):
-        H, A, _ = O.grouped_mlp_fwd(x, off, W1, W2, w.act)
-        O.grouped_mlp_bwd(x, H, A, dy, off, W1, W2, w.act)
+        oracle_step(w, x, dy, W1, W2, off)
     dt = (time.perf_counter() - t0) / reps
     fwd, bwd = useful_flops(w, rows)
     return (fwd + bwd) / dt / 1e12, dt
@@ -327,13 +369,11 @@ def run_reference(args, w):
     if rank != 0:
         return 0
     rows = args.ref_rows
-    import oracle as O
     x, dy, W1, W2 = oracle_sample(w, rows)
     off = np.array([0, rows])
 
     def step():
-        H, A, _ = O.grouped_mlp_fwd(x, off, W1, W2, w.act)
-        O.grouped_mlp_bwd(x, H, A, dy, off, W1, W2, w.act)
+        oracle_step(w, x, dy, W1, W2, off)
     for _ in range(args.warmup):
         step()
     t0 = time.perf_counter()
@@ -343,7 +383,7 @@ def run_reference(args, w):
     fwd, bwd = useful_flops(w, rows)
     v = (fwd + bwd) / dt / 1e12
     sample = (f"{rows} rows of expert 0 ({w.d}x{w.n1} W1, {w.n}x{w.d} W2), oracle float64 "
-              f"fwd+bwd per step")
+              f"{'fwd (MXFP8 FC2)' if w.mxfp8 else 'fwd+bwd'} per step")
     line = {"impl": "reference", "metric": METRIC, "value": v, "unit": "TFLOP/s",
             "n_gpus": ws, "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
@@ -372,8 +412,6 @@ def main():
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     w = WL.WORKLOADS[args.workload]
-    if w.mxfp8:
-        raise SystemExit(f"{w.name}: not a bench workload of this build")
 
     if args.impl == "reference":
         return run_reference(args, w)
@@ -461,12 +499,15 @@ def main():
     dom = max(gemms, key=lambda nm: kern[nm]["ms"])
     fl, by = work[dom]
     t_dom = kern[dom]["ms"] * 1e-3
-    tensor_time = fl / (peaks["bf16_tflops_sustained"] * 1e12)
+    fp8 = w.mxfp8 and dom == "fc2"
+    tpeak = peaks["bf16_tflops_sustained"] * (2.0 if fp8 else 1.0)   # dense fp8 = 2x bf16 (nominal ratio)
+    tensor_time = fl / (tpeak * 1e12)
     hbm_time = by / (peaks["hbm_gbs"] * 1e9)
     if tensor_time >= hbm_time:
         roof = {"kernel": dom, "bound": "tensor", "achieved": round(fl / t_dom / 1e12, 1),
-                "peak": peaks["bf16_tflops_sustained"], "unit": "TFLOP/s",
-                "peak_kind": f"bf16_tflops_sustained ({peaks['source']})"}
+                "peak": tpeak, "unit": "TFLOP/s",
+                "peak_kind": (f"2 x bf16_tflops_sustained (fp8, {peaks['source']})" if fp8 else
+                              f"bf16_tflops_sustained ({peaks['source']})")}
         algo = fl
     else:
         roof = {"kernel": dom, "bound": "hbm", "achieved": round(by / t_dom / 1e9, 1),
@@ -483,7 +524,8 @@ def main():
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
         v, dt = time_oracle(w, args.cpu_rows)
         cpu = {"value": v, "unit": "TFLOP/s", "cores": cpu_cores(), "kind": "oracle",
-               "sample": f"{args.cpu_rows} rows of expert 0, float64 fwd+bwd ({dt:.1f} s)"}
+               "sample": f"{args.cpu_rows} rows of expert 0, float64 "
+                         f"{'fwd (MXFP8 FC2)' if w.mxfp8 else 'fwd+bwd'} ({dt:.1f} s)"}
 
     if rank == 0:
         line = {
@@ -495,6 +537,8 @@ def main():
             "config": {"workload": w.name, "E": w.E, "T": w.T, "top_k": w.k, "d": w.d, "n": w.n,
                        "act": w.act, "rows": Mrows, "nonempty_experts": inp["E_ne"],
                        "step": ("grouped_mlp_fwd + grouped_mlp_bwd" if w.routing == "identity"
+                                else ("route + permute + W2 MXFP8 quantise + fwd (FC1 + MX epilogue, "
+                                      "block-scaled FC2) + combine") if w.mxfp8
                                 else "route + permute + fwd + combine + bwd (+ router grad)"),
                        "l2": "inputs larger than L2 (no flush)", "parallelism": "replicas"},
             "roofline": roof, "kernels": kern, "cpu_baseline": cpu, "e2e": e2e,
@@ -515,6 +559,10 @@ def run_e2e(w, inp, o, step, steps, ws, flops):
     if w.routing == "identity":
         names_in = ["x_perm", "dy_perm", "offsets"]
         out_name = "dx_perm"
+        res = o
+    elif w.mxfp8:
+        names_in = ["x", "topk_idx", "probs"]
+        out_name = "out"
         res = o
     else:
         names_in = ["x", "dO", "topk_idx", "probs"]

@@ -30,9 +30,9 @@ void ev_end(cudaStream_t s) {
   }
 }
 cudaError_t gemm(moe::GemmKind kind, int act, const CUtensorMap& ta, const CUtensorMap& tb,
-                 const moe::GemmArgs& g, int sms, cudaStream_t s) {
+                 const CUtensorMap& tc, const moe::GemmArgs& g, int sms, cudaStream_t s) {
   ev_begin(s);
-  const cudaError_t e = moe::launch_grouped_gemm(kind, act, ta, tb, g, sms, s);
+  const cudaError_t e = moe::launch_grouped_gemm(kind, act, ta, tb, tc, g, sms, s);
   ev_end(s);
   return e;
 }
@@ -66,7 +66,8 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 
 // tensor map (bf16 or u8), 128-byte swizzle; dims/box listed innermost first.
 bool make_map(CUtensorMap* m, const void* base, int rank, const uint64_t* dims,
-              const uint32_t* box, bool u8 = false) {
+              const uint32_t* box, bool u8 = false,
+              CUtensorMapSwizzle swz = CU_TENSOR_MAP_SWIZZLE_128B) {
   auto fn = encode_fn();
   if (!fn) return false;
   cuuint64_t gdim[3], gstride[2];
@@ -81,7 +82,7 @@ bool make_map(CUtensorMap* m, const void* base, int rank, const uint64_t* dims,
   const CUresult r = fn(m, u8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
                         rank, const_cast<void*>(base), gdim,
                         gstride, bdim, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
@@ -99,6 +100,16 @@ bool map_w(CUtensorMap* m, const void* p, int E, int rows, int cols, int box_row
                             static_cast<uint64_t>(E)};
   const uint32_t box[3] = {u8 ? 128u : 64u, static_cast<uint32_t>(box_rows), 1};
   return make_map(m, p, 3, dims, box, u8);
+}
+
+// [E, rows, cols] bf16 output written by staged TMA stores: box (64 cols,
+// 128-byte swizzle) or (32 cols, 64-byte swizzle) x 32 rows x 1
+bool map_out3(CUtensorMap* m, const void* p, int E, int rows, int cols, bool wide) {
+  const uint64_t dims[3] = {static_cast<uint64_t>(cols), static_cast<uint64_t>(rows),
+                            static_cast<uint64_t>(E)};
+  const uint32_t box[3] = {wide ? 64u : 32u, 32, 1};
+  return make_map(m, p, 3, dims, box, false,
+                  wide ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B);
 }
 
 int cuda_rc(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_E_CUDA; }
@@ -276,7 +287,8 @@ int moe_grouped_mlp_fwd(const moe_bf16* x_perm, const int32_t* offsets, int E, i
     g1.mx_sT = mx->a_qT ? mx->a_sT : nullptr; g1.n_a = n;
   }
   ev_begin(s);
-  cudaError_t e = moe::launch_grouped_gemm(moe::GemmKind::kFc1Act, act, tx, tw1, g1, sms, s, use_mx);
+  cudaError_t e = moe::launch_grouped_gemm(moe::GemmKind::kFc1Act, act, tx, tw1, tx, g1, sms, s,
+                                           use_mx);
   ev_end(s);
   if (e != cudaSuccess) return MOE_E_CUDA;
   if (use_mx) {
@@ -293,7 +305,7 @@ int moe_grouped_mlp_fwd(const moe_bf16* x_perm, const int32_t* offsets, int E, i
   moe::GemmArgs g2{};
   g2.offsets = offsets; g2.E = E; g2.M_cap = M_cap; g2.K = n; g2.N = d; g2.R = 0;
   g2.out = y_perm; g2.ldo = d; g2.err = err;
-  e = gemm(moe::GemmKind::kFc2, 0, ta, tw2, g2, sms, s);
+  e = gemm(moe::GemmKind::kFc2, 0, ta, tw2, ta, g2, sms, s);
   if (e != cudaSuccess) return MOE_E_CUDA;
   g_last_launches = 2;
   return MOE_OK;
@@ -325,41 +337,46 @@ int moe_grouped_mlp_bwd(const moe_bf16* x_perm, const moe_bf16* h_saved, const m
   const int sms = num_sms_current();
   if (sms <= 0) return MOE_E_CUDA;
 
+  moe::GemmArgs probe{};
+  probe.M_cap = M_cap;
+  probe.E = E;
+  const bool skinny = moe::wgrad_skinny(probe);
   // operand maps
-  CUtensorMap t_dy_k, t_w2_k, t_a_mn, t_dy_mn, t_dh_k, t_w1_k, t_x_mn, t_dh_mn;
+  CUtensorMap t_dy_k, t_w2_k, t_a_mn, t_dy_mn, t_dh_k, t_w1_k, t_x_mn, t_dh_mn, t_dw1, t_dw2;
   if (!map_act(&t_dy_k, dy_perm, M_cap, d, moe::kBM) ||      // FC2-dgrad A (K = d)
-      !map_w(&t_w2_k, W2, E, n, d, moe::kBN) ||               // FC2-dgrad B rows = n
+      !map_w(&t_w2_k, W2, E, n, d, 128) ||                    // FC2-dgrad B rows = n (halves)
       !map_act(&t_a_mn, a, M_cap, n, 64) ||                   // FC2-wgrad A (MN = n)
       !map_act(&t_dy_mn, dy_perm, M_cap, d, 64) ||            // FC2-wgrad B (MN = d)
       !map_act(&t_dh_k, dh, M_cap, n1, moe::kBM) ||           // FC1-dgrad A (K = n1)
-      !map_w(&t_w1_k, W1, E, d, n1, moe::kBN) ||              // FC1-dgrad B rows = d
+      !map_w(&t_w1_k, W1, E, d, n1, 128) ||                   // FC1-dgrad B rows = d (halves)
       !map_act(&t_x_mn, x_perm, M_cap, d, 64) ||              // FC1-wgrad A (MN = d)
-      !map_act(&t_dh_mn, dh, M_cap, n1, 64))                  // FC1-wgrad B (MN = n1)
+      !map_act(&t_dh_mn, dh, M_cap, n1, 64) ||                // FC1-wgrad B (MN = n1)
+      !map_out3(&t_dw2, dW2, E, n, d, skinny) || !map_out3(&t_dw1, dW1, E, d, n1, skinny))
     return MOE_E_CUDA;
 
   // 1. dH = act'(H; dY W2^T)
   moe::GemmArgs g{};
   g.offsets = offsets; g.E = E; g.M_cap = M_cap; g.K = d; g.N = n;
   g.out = dh; g.ldo = n1; g.aux = h_saved; g.ld_aux = n1; g.err = err;
-  cudaError_t e = gemm(moe::GemmKind::kDgradAct, act, t_dy_k, t_w2_k, g, sms, s);
+  cudaError_t e = gemm(moe::GemmKind::kDgradAct, act, t_dy_k, t_w2_k, t_dy_k, g, sms, s);
   if (e != cudaSuccess) return MOE_E_CUDA;
   // 2. dW2_e = A_e^T dY_e
   moe::GemmArgs gw2{};
   gw2.offsets = offsets; gw2.E = E; gw2.M_cap = M_cap; gw2.N = d; gw2.R = n;
   gw2.out = dW2; gw2.ldo = d; gw2.out_estride = static_cast<long long>(n) * d; gw2.err = err;
-  e = gemm(moe::GemmKind::kWgrad, 0, t_a_mn, t_dy_mn, gw2, sms, s);
+  e = gemm(moe::GemmKind::kWgrad, 0, t_a_mn, t_dy_mn, t_dw2, gw2, sms, s);
   if (e != cudaSuccess) return MOE_E_CUDA;
   // 3. dX = dH W1^T
   moe::GemmArgs gd{};
   gd.offsets = offsets; gd.E = E; gd.M_cap = M_cap; gd.K = n1; gd.N = d;
   gd.out = dx_perm; gd.ldo = d; gd.err = err;
-  e = gemm(moe::GemmKind::kDgrad, 0, t_dh_k, t_w1_k, gd, sms, s);
+  e = gemm(moe::GemmKind::kDgrad, 0, t_dh_k, t_w1_k, t_dh_k, gd, sms, s);
   if (e != cudaSuccess) return MOE_E_CUDA;
   // 4. dW1_e = X_e^T dH_e
   moe::GemmArgs gw1{};
   gw1.offsets = offsets; gw1.E = E; gw1.M_cap = M_cap; gw1.N = n1; gw1.R = d;
   gw1.out = dW1; gw1.ldo = n1; gw1.out_estride = static_cast<long long>(d) * n1; gw1.err = err;
-  e = gemm(moe::GemmKind::kWgrad, 0, t_x_mn, t_dh_mn, gw1, sms, s);
+  e = gemm(moe::GemmKind::kWgrad, 0, t_x_mn, t_dh_mn, t_dw1, gw1, sms, s);
   if (e != cudaSuccess) return MOE_E_CUDA;
   g_last_launches = 4;
   return MOE_OK;

@@ -9,11 +9,12 @@
 // [Sonic] "IO 숨기기" / "GEMM Overlapping": warp specialisation (producer,
 // MMA, epilogue) and software pipelining hide the epilogue's IO.
 //
-// Roles (192 threads, one CTA per SM, persistent over a static tile order):
+// Roles (320 threads, one CTA per SM, persistent over a static tile order):
 //   warp 0     TMA producer (one lane): 4-stage ring of 48 KB stages
 //   warp 1     TMEM owner + MMA issuer (one lane): tcgen05.mma 128x256x16
-//   warps 2-5  epilogue: tcgen05.ld (warp w reads TMEM lanes 32*(w%4)..),
-//              activation / derivative math, stores to global
+//   warps 2-9  epilogue, two warpgroups splitting the tile's columns:
+//              tcgen05.ld (warp w reads TMEM lanes 32*(w%4)..), activation /
+//              derivative math, stores to global
 // Two 256-column fp32 accumulators in TMEM let tile i+1's MMAs overlap
 // tile i's epilogue.
 #include <cuda_runtime.h>
@@ -31,12 +32,33 @@ constexpr int A_BYTES = BM * BK * 2;  // 16 KB
 constexpr int B_BYTES = BN * BK * 2;  // 32 KB
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int MN_BOX_BYTES = 64 * BK * 2;  // one 64(MN) x 64(K) box: 8 KB
-constexpr int NUM_THREADS = 192;
+constexpr int NUM_THREADS = 320;
+constexpr int EPI_WARPS = 8;
 constexpr int TMEM_COLS = 2 * BN;
 
+// Weight-gradient kernels stage their output in shared memory and write it
+// with TMA stores.  Two configurations:
+//  * skinny experts (few rows, one reduction block per 64 KB output tile):
+//    the epilogue is the bottleneck, so one pipeline stage is traded for
+//    double-buffered staging, two 32-row x 64-column boxes per epilogue warp
+//    (128-byte swizzle);
+//  * large experts (long reductions, tensor-bound): four stages and one
+//    32 x 32 box per warp (64-byte swizzle).
+// Each also keeps one box of zeros for experts with no rows.
+template <GemmKind KIND, bool SKINNY>
+struct Cfg {
+  static constexpr bool W = (KIND == GemmKind::kWgrad);
+  static constexpr int stages = (W && SKINNY) ? 3 : STAGES;
+  static constexpr int box_cols = SKINNY ? 64 : 32;
+  static constexpr int box_bytes = 32 * box_cols * 2;
+  static constexpr int nbuf = SKINNY ? 2 : 1;
+  static constexpr int stg_bytes = W ? (nbuf * EPI_WARPS + 1) * box_bytes : 0;
+};
+template <GemmKind KIND, bool SKINNY>
 constexpr size_t smem_bytes(int E) {
-  return 1024 /*align slack*/ + static_cast<size_t>(STAGES) * STAGE_BYTES +
-         (2 * STAGES + 5) * 8 /*barriers*/ + 16 + 2 * (E + 1) * 4 /*scheduler*/;
+  return 1024 /*align slack*/ + static_cast<size_t>(Cfg<KIND, SKINNY>::stages) * STAGE_BYTES +
+         Cfg<KIND, SKINNY>::stg_bytes + (2 * Cfg<KIND, SKINNY>::stages + 5) * 8 /*barriers*/ +
+         16 + 2 * (E + 1) * 4 /*scheduler*/;
 }
 
 // ------------------------------------------------------------ activations
@@ -71,6 +93,7 @@ __device__ __forceinline__ void gate_phi_dphi(float g, float& ph, float& dph) {
 // ------------------------------------------------------------ scheduling
 struct Tile {
   int e;
+  bool mc;      // 2-CTA unit that shares (multicasts) its B block
   int row0;     // ragged-row kinds: first global row of the tile
   int rows;     // ragged-row kinds: valid rows in the tile
   int m0;       // kWgrad: first output row (within the expert)
@@ -80,20 +103,28 @@ struct Tile {
   int klast;    // kWgrad: valid rows in the last reduction block
 };
 
+// Work units of a CL-CTA cluster.  With CL = 2 and at least two 128-row
+// blocks, a unit is two consecutive row blocks sharing one 256-column block
+// of B (CTA r takes row block 2i + r; each CTA fetches half of B and
+// multicasts it).  An expert with a single row block (skinny experts of a
+// fine-grained layer) pairs along N instead: CTA r takes column block 2i + r
+// and loads everything itself, so no CTA of the pair sits idle.
 template <GemmKind KIND>
+__device__ __forceinline__ int row_blocks(const GemmArgs& g, const int* s_off, int e) {
+  return (KIND == GemmKind::kWgrad) ? (g.R + BM - 1) / BM
+                                    : (s_off[e + 1] - s_off[e] + BM - 1) / BM;
+}
+template <GemmKind KIND, int CL>
 __device__ __forceinline__ int tiles_of_expert(const GemmArgs& g, const int* s_off, int e) {
   const int nt = (g.N + BN - 1) / BN;
-  if constexpr (KIND == GemmKind::kWgrad) {
-    return ((g.R + BM - 1) / BM) * nt;
-  } else {
-    const int rows = s_off[e + 1] - s_off[e];
-    return ((rows + BM - 1) / BM) * nt;
-  }
+  const int mt = row_blocks<KIND>(g, s_off, e);
+  if (CL == 2 && mt == 1) return (nt + 1) / 2;
+  return ((mt + CL - 1) / CL) * nt;
 }
 
-template <GemmKind KIND>
+template <GemmKind KIND, int CL>
 __device__ __forceinline__ Tile decode_tile(const GemmArgs& g, const int* s_off,
-                                            const int* s_ts, int t) {
+                                            const int* s_ts, int t, int rank) {
   // expert e with s_ts[e] <= t < s_ts[e+1]
   int lo = 0, hi = g.E - 1;
   while (lo < hi) {
@@ -105,8 +136,17 @@ __device__ __forceinline__ Tile decode_tile(const GemmArgs& g, const int* s_off,
   tl.e = lo;
   const int local = t - s_ts[lo];
   const int nt = (g.N + BN - 1) / BN;
-  const int mi = local / nt;
-  tl.n0 = (local - mi * nt) * BN;
+  int mi;
+  if (CL == 2 && row_blocks<KIND>(g, s_off, lo) == 1) {
+    tl.mc = false;
+    mi = 0;
+    tl.n0 = (2 * local + rank) * BN;
+  } else {
+    const int pm = local / nt;
+    tl.n0 = (local - pm * nt) * BN;
+    mi = CL * pm + rank;
+    tl.mc = (CL == 2);
+  }
   if constexpr (KIND == GemmKind::kWgrad) {
     tl.m0 = mi * BM;
     tl.krow0 = s_off[lo];
@@ -117,7 +157,7 @@ __device__ __forceinline__ Tile decode_tile(const GemmArgs& g, const int* s_off,
     tl.rows = 0;
   } else {
     tl.row0 = s_off[lo] + mi * BM;
-    tl.rows = min(BM, s_off[lo + 1] - tl.row0);
+    tl.rows = max(0, min(BM, s_off[lo + 1] - tl.row0));
     tl.kblocks = g.K / BK;
     tl.m0 = 0;
     tl.krow0 = 0;
@@ -293,10 +333,11 @@ __device__ __forceinline__ void fc1_mx_block(const GemmArgs& g, const Tile& tl, 
 }
 
 // ------------------------------------------------------------ the kernel
-template <GemmKind KIND, int ACT, bool MX = false>
+template <GemmKind KIND, int ACT, bool MX, int CL, bool SKINNY>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
-                        const __grid_constant__ CUtensorMap tmB, const GemmArgs g) {
+                        const __grid_constant__ CUtensorMap tmB,
+                        const __grid_constant__ CUtensorMap tmC, const GemmArgs g) {
   constexpr bool A_MN = (KIND == GemmKind::kWgrad);
   constexpr bool B_MN = (KIND == GemmKind::kFc1Act || KIND == GemmKind::kFc2 ||
                          KIND == GemmKind::kWgrad);
@@ -306,9 +347,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
-  uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
-  uint64_t* empty_bar = full_bar + STAGES;
-  uint64_t* tfull_bar = empty_bar + STAGES;
+  using C = Cfg<KIND, SKINNY>;
+  constexpr int NST = C::stages;
+  constexpr int BOX = C::box_bytes;
+  constexpr int BOXC = C::box_cols;
+  uint8_t* staging = smem + NST * STAGE_BYTES;            // C::nbuf boxes per epilogue warp
+  uint8_t* zero_box = staging + C::nbuf * EPI_WARPS * BOX;  // 32 x BOXC bf16 zeros
+  uint64_t* full_bar = reinterpret_cast<uint64_t*>(staging + C::stg_bytes);
+  uint64_t* empty_bar = full_bar + NST;
+  uint64_t* tfull_bar = empty_bar + NST;
   uint64_t* tempty_bar = tfull_bar + 2;
   uint64_t* drain_bar = tempty_bar + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain_bar + 1);
@@ -318,21 +365,31 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  const int rank = (CL == 2) ? static_cast<int>(cluster_ctarank()) : 0;
+  const int unit0 = blockIdx.x / CL;        // this cluster's first work unit
+  const int unit_step = gridDim.x / CL;     // clusters in the grid
+  constexpr uint16_t kPair = 0x3;
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < STAGES; ++i) {
+    for (int i = 0; i < NST; ++i) {
       mbar_init(&full_bar[i], 1);
-      mbar_init(&empty_bar[i], 1);
+      mbar_init(&empty_bar[i], CL);         // one commit from each CTA's MMA
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&tfull_bar[i], 1);
-      mbar_init(&tempty_bar[i], 4);
+      mbar_init(&tempty_bar[i], EPI_WARPS);
     }
     mbar_init(drain_bar, 1);
     *abort_flag = 0;
     fence_mbar_init();
     prefetch_tmap(&tmA);
     prefetch_tmap(&tmB);
+    if (KIND == GemmKind::kWgrad) prefetch_tmap(&tmC);
+  }
+  if (KIND == GemmKind::kWgrad && warp >= 2) {  // epilogue threads clear the zero box
+    for (int i = threadIdx.x - 64; i < BOX / 16; i += 32 * EPI_WARPS)
+      reinterpret_cast<uint4*>(zero_box)[i] = make_uint4(0, 0, 0, 0);
+    fence_proxy_async_smem();
   }
   if (warp == 1) tmem_alloc(tmem_slot, TMEM_COLS);
   if (warp == 2) {
@@ -359,7 +416,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     int carry = 0;
     for (int base = 0; base < g.E; base += 32) {
       const int e = base + lane;
-      const int t = (e < g.E) ? tiles_of_expert<KIND>(g, s_off, e) : 0;
+      const int t = (e < g.E) ? tiles_of_expert<KIND, CL>(g, s_off, e) : 0;
       int v = t;
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
@@ -372,7 +429,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     if (lane == 0) s_ts[g.E] = carry;
   }
   tc_fence_before();
-  __syncthreads();
+  if constexpr (CL == 2) cluster_sync();   // peers' barriers initialised before any multicast
+  else __syncthreads();
   tc_fence_after();
 
   const uint32_t tmem_base = *tmem_slot;
@@ -383,12 +441,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     if (lane == 0) {
       int stage = 0;
       uint32_t phase = 0;
-      uint32_t issued_parity[STAGES];
-      bool issued[STAGES];
-      for (int i = 0; i < STAGES; ++i) { issued[i] = false; issued_parity[i] = 0; }
+      uint32_t issued_parity[NST];
+      bool issued[NST];
+      for (int i = 0; i < NST; ++i) { issued[i] = false; issued_parity[i] = 0; }
       bool ok = true;
-      for (int t = blockIdx.x; t < total_tiles && ok; t += gridDim.x) {
-        const Tile tl = decode_tile<KIND>(g, s_off, s_ts, t);
+      for (int t = unit0; t < total_tiles && ok; t += unit_step) {
+        const Tile tl = decode_tile<KIND, CL>(g, s_off, s_ts, t, rank);
         for (int kb = 0; kb < tl.kblocks; ++kb) {
           if (!mbar_wait(&empty_bar[stage], phase ^ 1, abort_flag)) { ok = false; break; }
           uint8_t* sa = smem + stage * STAGE_BYTES;
@@ -402,23 +460,40 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           } else {
             tma_load_2d(sa, &tmA, fb, kb * BK, tl.row0);
           }
+          // B: with a 2-CTA cluster each CTA fetches half of the shared B
+          // block and multicasts it into both CTAs' stage
           if constexpr (B_MN) {
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
-              if constexpr (B_3D) tma_load_3d(sb + i * MN_BOX_BYTES, &tmB, fb, tl.n0 + 64 * i, kb * BK, tl.e);
-              else tma_load_2d(sb + i * MN_BOX_BYTES, &tmB, fb, tl.n0 + 64 * i, tl.krow0 + kb * BK);
+              if (tl.mc && (i >> 1) != rank) continue;
+              uint8_t* dst = sb + i * MN_BOX_BYTES;
+              const int kc = B_3D ? kb * BK : tl.krow0 + kb * BK;
+              if (CL == 2 && tl.mc) {
+                if constexpr (B_3D) tma_load_3d_mc(dst, &tmB, fb, tl.n0 + 64 * i, kc, tl.e, kPair);
+                else tma_load_2d_mc(dst, &tmB, fb, tl.n0 + 64 * i, kc, kPair);
+              } else {
+                if constexpr (B_3D) tma_load_3d(dst, &tmB, fb, tl.n0 + 64 * i, kc, tl.e);
+                else tma_load_2d(dst, &tmB, fb, tl.n0 + 64 * i, kc);
+              }
             }
           } else {
-            tma_load_3d(sb, &tmB, fb, kb * BK, tl.n0, tl.e);
+            // K-major B: two 128-row halves
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              if (tl.mc && h != rank) continue;
+              uint8_t* dst = sb + h * (B_BYTES / 2);
+              if (CL == 2 && tl.mc) tma_load_3d_mc(dst, &tmB, fb, kb * BK, tl.n0 + 128 * h, tl.e, kPair);
+              else tma_load_3d(dst, &tmB, fb, kb * BK, tl.n0 + 128 * h, tl.e);
+            }
           }
           issued[stage] = true;
           issued_parity[stage] = phase;
-          if (++stage == STAGES) { stage = 0; phase ^= 1; }
+          if (++stage == NST) { stage = 0; phase ^= 1; }
         }
       }
       if (!ok) {
         // give up: wait (bounded) for our copies in flight before exiting
-        for (int i = 0; i < STAGES; ++i)
+        for (int i = 0; i < NST; ++i)
           if (issued[i]) {
             const uint32_t a = smem_u32(&full_bar[i]);
             const uint64_t t0 = globaltimer_ns();
@@ -432,8 +507,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     uint32_t phase = 0;
     int local = 0;
     bool ok = true;
-    for (int t = blockIdx.x; t < total_tiles && ok; t += gridDim.x, ++local) {
-      const Tile tl = decode_tile<KIND>(g, s_off, s_ts, t);
+    for (int t = unit0; t < total_tiles && ok; t += unit_step, ++local) {
+      const Tile tl = decode_tile<KIND, CL>(g, s_off, s_ts, t, rank);
       const int buf = local & 1;
       const uint32_t aph = (local >> 1) & 1;
       if (lane == 0) ok = mbar_wait(&tempty_bar[buf], aph ^ 1, abort_flag);
@@ -448,11 +523,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         tc_fence_after();
         uint8_t* sa = smem + stage * STAGE_BYTES;
         uint8_t* sb = sa + A_BYTES;
+        // In an expert's last reduction block only ceil(klast/16) MMAs touch
+        // its rows; the rows after klast up to that 16-row boundary belong to
+        // the next expert and are zeroed in all six 64x64 boxes (2 of A, 4 of
+        // B) before the MMAs read them.
+        int kk_n = BK / UK;
         if constexpr (KIND == GemmKind::kWgrad) {
           if (kb == tl.kblocks - 1 && tl.klast < BK) {
-            // rows past the expert's end belong to the next expert: zero them
-            // in all six 64x64 boxes (2 of A, 4 of B) before the MMAs read them
-            const int zr = BK - tl.klast;
+            kk_n = (tl.klast + UK - 1) / UK;
+            const int zr = kk_n * UK - tl.klast;
             const int units = 6 * zr * 8;  // 16-byte units
             for (int u = lane; u < units; u += 32) {
               const int box = u / (zr * 8);
@@ -469,18 +548,18 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         __syncwarp();
         if (lane == 0) {
           const uint32_t a0 = smem_u32(sa), b0 = smem_u32(sb);
-#pragma unroll
-          for (int kk = 0; kk < BK / UK; ++kk) {
+          for (int kk = 0; kk < kk_n; ++kk) {
             const uint64_t ad = A_MN ? sdesc_sw128(a0 + kk * 2048, MN_BOX_BYTES, 1024)
                                      : sdesc_sw128(a0 + kk * 32, 16, 1024);
             const uint64_t bd = B_MN ? sdesc_sw128(b0 + kk * 2048, MN_BOX_BYTES, 1024)
                                      : sdesc_sw128(b0 + kk * 32, 16, 1024);
             umma_bf16(d_tmem, ad, bd, IDESC, (kb > 0 || kk > 0) ? 1u : 0u);
           }
-          umma_commit(&empty_bar[stage]);
+          if constexpr (CL == 2) umma_commit_mc(&empty_bar[stage], kPair);  // frees it in both CTAs
+          else umma_commit(&empty_bar[stage]);
         }
         __syncwarp();
-        if (++stage == STAGES) { stage = 0; phase ^= 1; }
+        if (++stage == NST) { stage = 0; phase ^= 1; }
       }
       if (!ok) break;
       if (lane == 0) umma_commit(&tfull_bar[buf]);
@@ -496,11 +575,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     __syncwarp();
   } else {
     // ---------------------------------------------------------- epilogue
-    const int q = warp & 3;
+    const int q = warp & 3;            // TMEM lane quadrant of this warp
+    const int wg = (warp - 2) >> 2;    // warpgroup: columns [wg*128, wg*128+128) of the tile
     const int row_in_tile = q * 32 + lane;
     int local = 0;
-    for (int t = blockIdx.x; t < total_tiles; t += gridDim.x, ++local) {
-      const Tile tl = decode_tile<KIND>(g, s_off, s_ts, t);
+    uint32_t stg_slot = 0;
+    for (int t = unit0; t < total_tiles; t += unit_step, ++local) {
+      const Tile tl = decode_tile<KIND, CL>(g, s_off, s_ts, t, rank);
       const int buf = local & 1;
       const uint32_t aph = (local >> 1) & 1;
       bool ok = true;
@@ -510,20 +591,74 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const uint32_t tb = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + buf * BN;
       if constexpr (KIND == GemmKind::kFc1Act && MX) {
         constexpr int STEP = (ACT == MOE_ACT_SRELU) ? 32 : 64;
-        for (int cb = 0; cb < BN / STEP; ++cb) {
+        for (int cb = wg * (BN / STEP / 2); cb < (wg + 1) * (BN / STEP / 2); ++cb) {
           uint32_t r0[32], r1[32];
           tmem_ld32(tb + cb * STEP, r0);
           if constexpr (STEP == 64) tmem_ld32(tb + cb * STEP + 32, r1);
           tmem_wait_ld();
           fc1_mx_block<ACT>(g, tl, row_in_tile, lane, q, cb, r0, r1);
         }
+      } else if (KIND == GemmKind::kWgrad && tl.m0 + q * 32 + 32 <= g.R && tl.kblocks == 0) {
+        // expert with no rows: its weight gradient is zero; store the zero box
+        if (lane == 0) {
+          for (int c = wg * (128 / BOXC); c < (wg + 1) * (128 / BOXC); ++c) {
+            const int col = tl.n0 + c * BOXC;
+            if (col >= g.N) break;
+            tma_store_3d(&tmC, zero_box, col, tl.m0 + q * 32, tl.e);
+          }
+          bulk_commit();
+        }
+        __syncwarp();
+      } else if (KIND == GemmKind::kWgrad && tl.m0 + q * 32 + 32 <= g.R) {
+        // whole 32-row slab valid: stage each 32-row box in shared memory
+        // (swizzled like the tensor map) and let TMA write it with full-line
+        // stores
+        for (int c = wg * (128 / BOXC); c < (wg + 1) * (128 / BOXC); ++c) {
+          const int col = tl.n0 + c * BOXC;
+          if (col >= g.N) break;
+          uint32_t r0[32], r1[32];
+          tmem_ld32(tb + c * BOXC, r0);
+          if constexpr (BOXC == 64) tmem_ld32(tb + c * BOXC + 32, r1);
+          tmem_wait_ld();
+          uint8_t* buf = staging + ((warp - 2) * C::nbuf + (stg_slot % C::nbuf)) * BOX;
+          if (lane == 0) {                     // the box is free once its last store read it
+            if constexpr (C::nbuf == 2) bulk_wait_read_1();
+            else bulk_wait_read_0();
+          }
+          __syncwarp();
+          uint8_t* row = buf + lane * (BOXC * 2);
+          // 128-byte swizzle: 16-byte chunk j of row r at j ^ (r % 8);
+          // 64-byte swizzle: at j ^ ((r / 2) % 4)
+          const int sw = (BOXC == 64) ? (lane & 7) : ((lane >> 1) & 3);
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            *reinterpret_cast<uint4*>(row + ((j ^ sw) * 16)) = make_uint4(
+                pack_bf16x2(__uint_as_float(r0[8 * j + 0]), __uint_as_float(r0[8 * j + 1])),
+                pack_bf16x2(__uint_as_float(r0[8 * j + 2]), __uint_as_float(r0[8 * j + 3])),
+                pack_bf16x2(__uint_as_float(r0[8 * j + 4]), __uint_as_float(r0[8 * j + 5])),
+                pack_bf16x2(__uint_as_float(r0[8 * j + 6]), __uint_as_float(r0[8 * j + 7])));
+            if constexpr (BOXC == 64)
+              *reinterpret_cast<uint4*>(row + (((j + 4) ^ sw) * 16)) = make_uint4(
+                  pack_bf16x2(__uint_as_float(r1[8 * j + 0]), __uint_as_float(r1[8 * j + 1])),
+                  pack_bf16x2(__uint_as_float(r1[8 * j + 2]), __uint_as_float(r1[8 * j + 3])),
+                  pack_bf16x2(__uint_as_float(r1[8 * j + 4]), __uint_as_float(r1[8 * j + 5])),
+                  pack_bf16x2(__uint_as_float(r1[8 * j + 6]), __uint_as_float(r1[8 * j + 7])));
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            tma_store_3d(&tmC, buf, col, tl.m0 + q * 32, tl.e);
+            bulk_commit();
+          }
+          ++stg_slot;
+        }
       } else if (KIND == GemmKind::kWgrad && tl.kblocks == 0) {
         uint32_t z[32];
 #pragma unroll
         for (int i = 0; i < 32; ++i) z[i] = 0;
-        for (int c = 0; c < BN / 32; ++c) epilogue_chunk<KIND, ACT>(g, tl, row_in_tile, c, z);
+        for (int c = wg * 4; c < wg * 4 + 4; ++c) epilogue_chunk<KIND, ACT>(g, tl, row_in_tile, c, z);
       } else {
-        for (int c = 0; c < BN / 32; ++c) {
+        for (int c = wg * 4; c < wg * 4 + 4; ++c) {
           uint32_t r[32];
           tmem_ld32(tb + c * 32, r);
           tmem_wait_ld();
@@ -534,10 +669,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(&tempty_bar[buf]);
     }
+    if (KIND == GemmKind::kWgrad && lane == 0) bulk_wait_all();  // staged stores done
+    __syncwarp();
   }
 
   tc_fence_before();
-  __syncthreads();
+  // no CTA leaves while its peer may still multicast into it or arrive on it
+  if constexpr (CL == 2) cluster_sync();
+  else __syncthreads();
   if (*abort_flag && threadIdx.x == 0) set_err(g.err, MOE_DEV_TIMEOUT);
   if (warp == 1) {
     tc_fence_after();
@@ -545,49 +684,85 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   }
 }
 
-template <GemmKind KIND, int ACT, bool MX = false>
-cudaError_t launch_t(const CUtensorMap& ta, const CUtensorMap& tb, const GemmArgs& g, int num_sms,
-                     cudaStream_t s) {
-  auto kern = grouped_gemm_kernel<KIND, ACT, MX>;
-  const size_t smem = smem_bytes(MOE_MAX_EXPERTS);
-  static bool attr_set = false;  // per process; the library drives one device
-  if (!attr_set) {
+// Cluster size of the grouped GEMM launches: pairs of CTAs share B tiles
+// through TMA multicast.
+constexpr int kCluster = 2;
+
+template <GemmKind KIND, int ACT, bool MX = false, bool SKINNY = false>
+cudaError_t launch_t(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tc,
+                     const GemmArgs& g, int num_sms, cudaStream_t s) {
+  auto kern = grouped_gemm_kernel<KIND, ACT, MX, kCluster, SKINNY>;
+  const size_t smem = smem_bytes<KIND, SKINNY>(MOE_MAX_EXPERTS);
+  static int grid = 0;  // per process; the library drives one device
+  if (grid == 0) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
     if (e != cudaSuccess) return e;
-    attr_set = true;
+    cudaLaunchConfig_t q = {};
+    q.gridDim = dim3(num_sms);
+    q.blockDim = dim3(NUM_THREADS);
+    q.dynamicSmemBytes = smem;
+    cudaLaunchAttribute qa[1];
+    qa[0].id = cudaLaunchAttributeClusterDimension;
+    qa[0].val.clusterDim.x = kCluster;
+    qa[0].val.clusterDim.y = 1;
+    qa[0].val.clusterDim.z = 1;
+    q.attrs = qa;
+    q.numAttrs = 1;
+    int clusters = 0;
+    e = cudaOccupancyMaxActiveClusters(&clusters, kern, &q);
+    if (e != cudaSuccess) return e;
+    const int most = num_sms / kCluster;
+    grid = kCluster * ((clusters > 0 && clusters < most) ? clusters : most);
   }
-  kern<<<num_sms, NUM_THREADS, smem, s>>>(ta, tb, g);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(NUM_THREADS);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeClusterDimension;
+  at[0].val.clusterDim.x = kCluster;
+  at[0].val.clusterDim.y = 1;
+  at[0].val.clusterDim.z = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, ta, tb, tc, g);
 }
 
 }  // namespace
 
+bool wgrad_skinny(const GemmArgs& g) {
+  return static_cast<long long>(g.M_cap) < static_cast<long long>(kSkinnyRows) * g.E;
+}
+
 cudaError_t launch_grouped_gemm(GemmKind kind, int act, const CUtensorMap& ta,
-                                const CUtensorMap& tb, const GemmArgs& g, int num_sms,
-                                cudaStream_t s, bool mx) {
+                                const CUtensorMap& tb, const CUtensorMap& tc, const GemmArgs& g,
+                                int num_sms, cudaStream_t s, bool mx) {
   if (mx) {
     if (kind != GemmKind::kFc1Act) return cudaErrorInvalidValue;
     switch (act) {
-      case MOE_ACT_SWIGLU: return launch_t<GemmKind::kFc1Act, MOE_ACT_SWIGLU, true>(ta, tb, g, num_sms, s);
-      case MOE_ACT_GEGLU: return launch_t<GemmKind::kFc1Act, MOE_ACT_GEGLU, true>(ta, tb, g, num_sms, s);
-      case MOE_ACT_SRELU: return launch_t<GemmKind::kFc1Act, MOE_ACT_SRELU, true>(ta, tb, g, num_sms, s);
+      case MOE_ACT_SWIGLU: return launch_t<GemmKind::kFc1Act, MOE_ACT_SWIGLU, true>(ta, tb, tc, g, num_sms, s);
+      case MOE_ACT_GEGLU: return launch_t<GemmKind::kFc1Act, MOE_ACT_GEGLU, true>(ta, tb, tc, g, num_sms, s);
+      case MOE_ACT_SRELU: return launch_t<GemmKind::kFc1Act, MOE_ACT_SRELU, true>(ta, tb, tc, g, num_sms, s);
       default: return cudaErrorInvalidValue;
     }
   }
 #define MOE_ACT_SWITCH(KIND)                                                         \
   switch (act) {                                                                     \
-    case MOE_ACT_SWIGLU: return launch_t<KIND, MOE_ACT_SWIGLU>(ta, tb, g, num_sms, s); \
-    case MOE_ACT_GEGLU: return launch_t<KIND, MOE_ACT_GEGLU>(ta, tb, g, num_sms, s);   \
-    case MOE_ACT_SRELU: return launch_t<KIND, MOE_ACT_SRELU>(ta, tb, g, num_sms, s);   \
+    case MOE_ACT_SWIGLU: return launch_t<KIND, MOE_ACT_SWIGLU>(ta, tb, tc, g, num_sms, s); \
+    case MOE_ACT_GEGLU: return launch_t<KIND, MOE_ACT_GEGLU>(ta, tb, tc, g, num_sms, s);   \
+    case MOE_ACT_SRELU: return launch_t<KIND, MOE_ACT_SRELU>(ta, tb, tc, g, num_sms, s);   \
     default: return cudaErrorInvalidValue;                                           \
   }
   switch (kind) {
     case GemmKind::kFc1Act: MOE_ACT_SWITCH(GemmKind::kFc1Act)
     case GemmKind::kDgradAct: MOE_ACT_SWITCH(GemmKind::kDgradAct)
-    case GemmKind::kFc2: return launch_t<GemmKind::kFc2, 0>(ta, tb, g, num_sms, s);
-    case GemmKind::kDgrad: return launch_t<GemmKind::kDgrad, 0>(ta, tb, g, num_sms, s);
-    case GemmKind::kWgrad: return launch_t<GemmKind::kWgrad, 0>(ta, tb, g, num_sms, s);
+    case GemmKind::kFc2: return launch_t<GemmKind::kFc2, 0>(ta, tb, tc, g, num_sms, s);
+    case GemmKind::kDgrad: return launch_t<GemmKind::kDgrad, 0>(ta, tb, tc, g, num_sms, s);
+    case GemmKind::kWgrad:
+      return wgrad_skinny(g) ? launch_t<GemmKind::kWgrad, 0, false, true>(ta, tb, tc, g, num_sms, s)
+                             : launch_t<GemmKind::kWgrad, 0, false, false>(ta, tb, tc, g, num_sms, s);
   }
 #undef MOE_ACT_SWITCH
   return cudaErrorInvalidValue;

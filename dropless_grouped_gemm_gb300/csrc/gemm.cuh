@@ -42,9 +42,19 @@ struct GemmArgs {
 };
 
 // Launches the persistent grouped GEMM of `kind` (act: MOE_ACT_*) on `s`.
+// tc: the output's tensor map for kWgrad ([E, R, N] bf16, see wgrad_skinny
+// for its box); unused (any valid map) for the other kinds.
 cudaError_t launch_grouped_gemm(GemmKind kind, int act, const CUtensorMap& ta,
-                                const CUtensorMap& tb, const GemmArgs& args, int num_sms,
-                                cudaStream_t s, bool mx = false);
+                                const CUtensorMap& tb, const CUtensorMap& tc,
+                                const GemmArgs& args, int num_sms, cudaStream_t s,
+                                bool mx = false);
+
+// Weight gradients use the skinny-expert configuration when the average
+// rows per expert (M_cap / E, known on the host without reading counts) is
+// below kSkinnyRows; its output tensor map box is then 64 x 32 (128-byte
+// swizzle), else 32 x 32 (64-byte swizzle).
+constexpr int kSkinnyRows = 512;
+bool wgrad_skinny(const GemmArgs& g);
 
 // Box shapes (elements) the kernels expect for each operand's tensor map.
 constexpr int kBM = 128, kBN = 256, kBK = 64;

@@ -30,6 +30,8 @@ def main():
     ap.add_argument("--workload", default=BE.DEFAULT_WORKLOAD, choices=sorted(WL.WORKLOADS))
     ap.add_argument("--rows-per-expert", type=int, default=None)
     ap.add_argument("--tokens", type=int, default=None)
+    ap.add_argument("--experts", type=int, default=None,
+                    help="fewer experts (routed workloads), for captures that must stay small")
     ap.add_argument("--what", choices=["fwd", "bwd", "step"], default="step")
     ap.add_argument("--reps", type=int, default=3)
     a = ap.parse_args()
@@ -40,6 +42,8 @@ def main():
         w = WL.scaled(w, T=w.E * a.rows_per_expert)
     if a.tokens is not None and w.routing != "identity":
         w = WL.scaled(w, T=a.tokens)
+    if a.experts is not None and w.routing != "identity":
+        w = WL.scaled(w, E=a.experts, k=min(w.k, a.experts))
     inp, o = BE.make_inputs(w, "cuda")
     step = BE.make_step(w, inp, o)
     if a.what == "step":

@@ -70,6 +70,9 @@ BWD_CASES = [
     ("ragged_tail_k", 1, 128, 128, [200]),
     ("ragged_empty_one_row", 4, 256, 192, [300, 0, 129, 1]),
     ("many_small_experts", 64, 128, 64, [(i * 7) % 41 for i in range(64)]),
+    # >= 512 rows per expert on average: the weight gradients take the
+    # large-expert configuration (four stages, 32-column staging)
+    ("large_experts_ragged", 3, 128, 128, [700, 0, 900]),
 ]
 
 
