@@ -353,12 +353,14 @@ def barrier(ws):
         dist.barrier()
 
 
-def max_over_ranks(v, ws):
+def max_over_ranks(v, ws, device="cuda"):
+    """Max of a per-rank scalar over all ranks (the job's time is the
+    slowest replica's)."""
     if ws == 1:
         return v
     import torch
     import torch.distributed as dist
-    t = torch.tensor([v], dtype=torch.float64, device="cuda")
+    t = torch.tensor([v], dtype=torch.float64, device=device)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
 

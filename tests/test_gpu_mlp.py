@@ -135,3 +135,41 @@ def test_deterministic_bitwise():
         if p.shape[0] == x.shape[0]:
             p, q = p[:R], q[:R]
         assert torch.equal(p, q)
+
+
+def test_zero_rows_layer():
+    """No rows at all: the forward writes nothing and the weight gradients
+    are exactly zero."""
+    import dropless_grouped_gemm_gb300 as M
+    E, d, n = 4, 128, 64
+    W1 = W.w1_interleaved(14, E, d, n, 0.05, "cuda")
+    W2 = W.w2(14, E, n, d, 0.05, "cuda")
+    x = torch.empty((0, d), dtype=torch.bfloat16, device="cuda")
+    off = cuda_i32(np.zeros(E + 1))
+    h, a, y, err = M.grouped_mlp_fwd(x, off, W1, W2, "swiglu", save_h=True)
+    dW1 = torch.full_like(W1, 7.0)
+    dW2 = torch.full_like(W2, 7.0)
+    _, _, dW1, dW2, err = M.grouped_mlp_bwd(x, h, a, torch.empty_like(x), off, W1, W2, "swiglu",
+                                            dW1=dW1, dW2=dW2, err=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    assert float(dW1.abs().max()) == 0 and float(dW2.abs().max()) == 0
+
+
+def test_maximum_experts():
+    """E = 1024 (the library's limit) with a sparse ragged routing."""
+    import dropless_grouped_gemm_gb300 as M
+    E, d, n = 1024, 64, 64
+    counts = [(7 * i) % 23 if i % 5 else 0 for i in range(E)]
+    off, x, W1, W2, dy = _case(E, d, n, counts, "swiglu", seed=15)
+    h, a, y = _fwd(off, x, W1, W2, "swiglu")
+    dh, dx, dW1, dW2, err = M.grouped_mlp_bwd(x, h, a, dy, cuda_i32(off), W1, W2, "swiglu")
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    H, A, Y = O.grouped_mlp_fwd(f64(x), off, f64(W1), f64(W2), "swiglu")
+    dH, dX, dW1r, dW2r = O.grouped_mlp_bwd(f64(x), H, A, f64(dy), off, f64(W1), f64(W2), "swiglu")
+    R = int(off[-1])
+    assert_rms_close(f64(y)[:R], Y[:R], "E=1024 Y")
+    assert_rms_close(f64(dx)[:R], dX[:R], "E=1024 dX")
+    assert_rms_close(f64(dW1), dW1r, "E=1024 dW1")
+    assert_rms_close(f64(dW2), dW2r, "E=1024 dW2")
