@@ -23,6 +23,7 @@ import torch
 __all__ = [
     "ACT", "FLAG_SAVE_H", "DEV_BAD_EXPERT", "DEV_OVERFLOW", "DEV_TIMEOUT", "DEV_BAD_OFFSETS",
     "lib", "lib_path", "version", "last_launch_count", "route_workspace_size", "route_offsets",
+    "router_topk",
     "permute", "unpermute", "grouped_mlp_fwd", "grouped_mlp_bwd", "MoeError",
     "FLAG_MXFP8", "MxFwd", "mx_quantize_weights", "mx_quantize", "mx_buffers",
 ]
@@ -65,6 +66,8 @@ def lib():
         L.moe_version.argtypes = []
         L.moe_last_launch_count.restype = i32
         L.moe_last_launch_count.argtypes = []
+        L.moe_router_topk.restype = i32
+        L.moe_router_topk.argtypes = [vp, i32, i32, i32, vp, vp, vp]
         L.moe_route_workspace_size.restype = sz
         L.moe_route_workspace_size.argtypes = [i32, i32, i32]
         L.moe_route_offsets.restype = i32
@@ -132,6 +135,18 @@ def _err_word(err, device):
         err = torch.zeros(1, dtype=torch.int32, device=device)
     _need(err, torch.int32, "err")
     return err
+
+
+def router_topk(logits: torch.Tensor, k: int, stream=None):
+    """Top-k experts per token and their softmax weights (moe_router_topk).
+    Returns (topk_idx int32 [T, k], probs float32 [T, k])."""
+    _need(logits, torch.float32, "logits", 2)
+    T, E = logits.shape
+    idx = torch.empty((T, k), dtype=torch.int32, device=logits.device)
+    probs = torch.empty((T, k), dtype=torch.float32, device=logits.device)
+    rc = lib().moe_router_topk(_ptr(logits), T, E, k, _ptr(idx), _ptr(probs), _stream(stream))
+    _check(rc, "moe_router_topk")
+    return idx, probs
 
 
 def route_workspace_size(T: int, k: int, E: int) -> int:

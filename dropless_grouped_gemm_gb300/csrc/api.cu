@@ -139,6 +139,22 @@ int moe_set_launch_events(void* const* events, int n) {
 
 int moe_launch_events_used(void) { return g_events_used; }
 
+int moe_router_topk(const float* logits, int T, int E, int k, int32_t* topk_idx, float* probs,
+                    void* stream) {
+  g_last_launches = 0;
+  if (T < 0 || E < 1 || E > MOE_MAX_EXPERTS || k < 1 || k > E) return MOE_E_SIZE;
+  if (T == 0) return MOE_OK;
+  if (!logits || !topk_idx || !probs) return MOE_E_NULL;
+  const int sms = num_sms_current();
+  if (sms <= 0) return MOE_E_CUDA;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  ev_begin(s);
+  const cudaError_t e = moe::launch_router_topk(logits, T, E, k, topk_idx, probs, sms, s);
+  ev_end(s);
+  g_last_launches = 1;
+  return cuda_rc(e);
+}
+
 size_t moe_route_workspace_size(int T, int k, int E) {
   if (T < 0 || k < 1 || E < 1) return 0;
   return moe::route_workspace_bytes(T, k, E);

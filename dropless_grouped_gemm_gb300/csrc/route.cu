@@ -158,7 +158,69 @@ __global__ void __launch_bounds__(kThreads) route_rank(const int32_t* __restrict
   }
 }
 
+// Router: top-k experts of each token and the softmax of their logits.
+// One warp per token; lane l holds logits l, l+32, ... (E <= 1024).  Each of
+// the k rounds takes the warp-wide largest logit not yet chosen, ties going
+// to the lower expert index, so the choice is exact and deterministic.
+__global__ void __launch_bounds__(256) router_topk_kernel(const float* __restrict__ logits, int T,
+                                                          int E, int k, int32_t* __restrict__ idx,
+                                                          float* __restrict__ probs) {
+  const int lane = threadIdx.x & 31;
+  const int warps = gridDim.x * (blockDim.x >> 5);
+  for (int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); t < T; t += warps) {
+    float v[32];
+    const float* row = logits + static_cast<long long>(t) * E;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      const int e = lane + 32 * i;
+      v[i] = (e < E) ? row[e] : -INFINITY;
+    }
+    uint32_t taken = 0;
+    float top = 0.f, sum = 0.f;
+    for (int j = 0; j < k; ++j) {
+      float bv = -INFINITY;
+      int bi = 0x7fffffff;
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        const int e = lane + 32 * i;
+        if (e < E && !((taken >> i) & 1u) && (v[i] > bv || bi == 0x7fffffff)) {
+          bv = v[i];
+          bi = e;
+        }
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+        const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+        if (ov > bv || (ov == bv && oi < bi)) {
+          bv = ov;
+          bi = oi;
+        }
+      }
+      if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
+      if (j == 0) top = bv;
+      const float ex = expf(bv - top);
+      sum += ex;
+      if (lane == 0) {
+        idx[static_cast<long long>(t) * k + j] = bi;
+        probs[static_cast<long long>(t) * k + j] = ex;   // normalised below
+      }
+    }
+    __syncwarp();
+    for (int j = lane; j < k; j += 32) probs[static_cast<long long>(t) * k + j] /= sum;
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_router_topk(const float* logits, int T, int E, int k, int32_t* idx,
+                              float* probs, int num_sms, cudaStream_t s) {
+  if (T <= 0) return cudaSuccess;
+  const long long want = (static_cast<long long>(T) + 7) / 8;
+  const int blocks = static_cast<int>(want < 16LL * num_sms ? want : 16LL * num_sms);
+  router_topk_kernel<<<blocks, 256, 0, s>>>(logits, T, E, k, idx, probs);
+  return cudaGetLastError();
+}
 
 size_t route_workspace_bytes(int T, int k, int E) {
   const long long P = static_cast<long long>(T) * k;

@@ -10,6 +10,9 @@ namespace moe {
 
 size_t route_workspace_bytes(int T, int k, int E);
 
+cudaError_t launch_router_topk(const float* logits, int T, int E, int k, int32_t* idx,
+                              float* probs, int num_sms, cudaStream_t s);
+
 // Fixed scratch of the no-allocation routing entry point: 1 MiB.
 constexpr size_t kRouteScratchWords = 262144;
 

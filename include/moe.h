@@ -107,6 +107,21 @@ typedef struct moe_mx_fwd {
 #define MOE_MAX_EXPERTS 1024
 
 /*
+ * moe_router_topk - the router's selection: the top-k experts of each token
+ * and the softmax of their logits ([TE] intro: a learned router activates
+ * the top-K experts of each token; "Transformer Engine이 제공하는 세 가지
+ * 구성 요소": gate, top-K, then dispatch).  The weighting is the softmax over
+ * the k selected logits (the pages do not fix it).
+ *   logits   [T, E] float32 (device).
+ *   topk_idx [T, k] int32, written in decreasing logit order; ties go to the
+ *            lower expert index.  The choice is exact and deterministic.
+ *   probs    [T, k] float32, softmax of the selected logits.
+ * Limits: 1 <= k <= E <= MOE_MAX_EXPERTS.
+ */
+int moe_router_topk(const float* logits, int T, int E, int k,
+                    int32_t* topk_idx, float* probs, void* stream);
+
+/*
  * moe_route_offsets - routing layout of the expert-major permuted buffer.
  *
  * Defined by [TE] "MoE 학습이 밀집 모델보다 어려운 이유: 래그드 텐서" (experts'

@@ -16,7 +16,7 @@ import numpy as np
 __all__ = [
     "ERR_BAD_EXPERT", "ERR_OVERFLOW", "ERR_TIMEOUT",
     "bf16_round", "bf16_bits", "bf16_from_bits",
-    "route_offsets", "permute", "unpermute", "router_grad",
+    "router_topk", "route_offsets", "permute", "unpermute", "router_grad",
     "interleave_gate_up", "split_gate_up",
     "act_forward", "act_backward", "phi", "dphi",
     "grouped_mlp_fwd", "grouped_mlp_bwd",
@@ -61,6 +61,39 @@ def bf16_bits(v) -> np.ndarray:
 def bf16_from_bits(b) -> np.ndarray:
     b = np.asarray(b, dtype=np.uint16)
     return (b.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+# ---------------------------------------------------------------------------
+# router: top-k experts per token ([TE] intro: the learned router activates
+# the top-K experts of each token; [TE] "Transformer Engine이 제공하는 세 가지
+# 구성 요소": gate, top-K selection, then dispatch).  The pages do not fix the
+# weighting; the reading taken is the softmax over the K selected logits.
+# ---------------------------------------------------------------------------
+
+def router_topk(logits, k: int):
+    """For each token, the k largest logits (ties: lower expert index first,
+    in decreasing logit order) and the softmax of those k logits.
+
+    Returns (topk_idx int64 [T, k], probs float64 [T, k])."""
+    logits = np.asarray(logits, dtype=np.float64)
+    T, E = logits.shape
+    idx = np.zeros((T, k), dtype=np.int64)
+    probs = np.zeros((T, k), dtype=np.float64)
+    for t in range(T):
+        taken = np.zeros(E, dtype=bool)
+        for j in range(k):
+            best = -1
+            for e in range(E):
+                if taken[e]:
+                    continue
+                if best < 0 or logits[t, e] > logits[t, best]:
+                    best = e
+            taken[best] = True
+            idx[t, j] = best
+        sel = logits[t, idx[t]]
+        ex = np.exp(sel - sel.max())
+        probs[t] = ex / ex.sum()
+    return idx, probs
 
 
 # ---------------------------------------------------------------------------

@@ -82,3 +82,34 @@ def test_deterministic():
     b = M.route_offsets(idx, 256, 1)
     for k_ in ("offsets", "row_of_pair", "pair_of_row"):
         assert torch.equal(a[k_], b[k_])
+
+
+@pytest.mark.parametrize("T,E,k", [(4096, 256, 8), (300, 1024, 4), (64, 5, 5), (1000, 3, 1)])
+def test_router_topk(T, E, k):
+    """Device top-k: the chosen experts match the oracle exactly (ties to the
+    lower index); the softmax weights within float32 rounding."""
+    import dropless_grouped_gemm_gb300 as M
+    rng = np.random.default_rng(T + E)
+    lg = rng.standard_normal((T, E)).astype(np.float32)
+    lg[0, :] = 0.25                                   # all tied
+    lg[1, [3 % E, (E - 1)]] = 9.0                     # tie at the top
+    if E > 4:
+        lg[2, 4] = -np.inf
+    idx, p = M.router_topk(torch.from_numpy(lg).cuda(), k)
+    oi, op = O.router_topk(lg.astype(np.float64), k)
+    assert idx.cpu().numpy().tolist() == oi.tolist()
+    assert np.abs(p.cpu().numpy() - op).max() < 1e-6
+
+
+def test_router_then_layout_on_zipf_logits():
+    """Router on the Zipf layer's logits, then the routing layout: equal to
+    the oracle's router followed by the oracle's layout."""
+    import dropless_grouped_gemm_gb300 as M
+    w = W.WORKLOADS["zipf_t4096_d7168_e256_top8_n2048_swiglu"]
+    lg = W.logits(w.cfg_id, w.T, w.E, w.zipf_s)
+    idx, p = M.router_topk(torch.from_numpy(lg).cuda(), w.k)
+    r = M.route_offsets(idx, w.E, 1)
+    oi, _ = O.router_topk(lg.astype(np.float64), w.k)
+    ro = O.route_offsets(oi, w.E, 1)
+    assert r["offsets"].cpu().numpy().tolist() == ro["offsets"].tolist()
+    assert r["row_of_pair"].cpu().numpy().tolist() == ro["row_of_pair"].tolist()

@@ -224,3 +224,26 @@ def test_bf16_round_against_float32_truncation_rule():
     one = np.float64(1.0)
     assert O.bf16_round(one + 2.0 ** -8) == 1.0                 # tie -> even (1.0)
     assert O.bf16_round(one + 3 * 2.0 ** -8) == 1.0 + 2.0 ** -6   # tie -> even
+
+
+def test_router_topk_pins():
+    """Top-k against a full stable sort; ties go to the lower index; the
+    probabilities are a softmax (sum to 1, ratios exp(l_i - l_j)); a
+    -inf logit is never chosen while finite ones remain."""
+    rng = np.random.default_rng(30)
+    lg = rng.standard_normal((50, 16))
+    lg[3, :] = 0.5                                  # all tied
+    lg[7, [2, 9]] = 10.0                            # a tie at the top
+    lg[11, 5] = -np.inf
+    idx, p = O.router_topk(lg, 4)
+    ref = np.argsort(-lg, axis=1, kind="stable")[:, :4]
+    assert (idx == ref).all()
+    assert idx[3].tolist() == [0, 1, 2, 3]
+    assert idx[7, :2].tolist() == [2, 9]
+    assert 5 not in idx[11]
+    assert np.allclose(p.sum(1), 1.0, atol=1e-15)
+    t = 20
+    l = lg[t, idx[t]]
+    assert np.allclose(p[t, 0] / p[t, 1], np.exp(l[0] - l[1]), rtol=1e-12)
+    i1, p1 = O.router_topk(lg[:5], 1)
+    assert (p1 == 1.0).all() and (i1[:, 0] == lg[:5].argmax(1)).all()
