@@ -12,6 +12,11 @@
 #include "mxgemm.cuh"
 #include "route.cuh"
 
+namespace moe {
+cudaError_t launch_bounded_wait_selftest(int limit_us, int32_t* err, int32_t* waited_us,
+                                         cudaStream_t s);
+}  // namespace moe
+
 namespace {
 
 thread_local int g_last_launches = 0;
@@ -128,6 +133,16 @@ extern "C" {
 const char* moe_version(void) { return "libmoe 0.1.0 (sm_103a, tcgen05/TMA grouped GEMM)"; }
 
 int moe_last_launch_count(void) { return g_last_launches; }
+
+int moe_selftest_bounded_wait(int limit_us, int32_t* err, int32_t* waited_us, void* stream) {
+  g_last_launches = 0;
+  if (limit_us < 1 || limit_us > 1000000) return MOE_E_SIZE;
+  if (!err || !waited_us) return MOE_E_NULL;
+  const cudaError_t e = moe::launch_bounded_wait_selftest(limit_us, err, waited_us,
+                                                          static_cast<cudaStream_t>(stream));
+  g_last_launches = 1;
+  return cuda_rc(e);
+}
 
 int moe_set_launch_events(void* const* events, int n) {
   g_events = reinterpret_cast<cudaEvent_t const*>(events);

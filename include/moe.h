@@ -333,6 +333,17 @@ int moe_mx_quantize(const moe_bf16* src, int rows, int cols,
 int moe_set_launch_events(void* const* events, int n);
 int moe_launch_events_used(void);
 
+/*
+ * moe_selftest_bounded_wait - diagnostic (no counterpart on the pages).
+ * Runs the bounded wait every kernel of the library uses on an mbarrier
+ * that nothing arrives at, with a limit of limit_us microseconds
+ * (1..1,000,000).  Expected outcome: MOE_DEV_TIMEOUT OR-ed into *err and
+ * *waited_us >= limit_us; the device stays usable.  A completed barrier is
+ * also waited on first and must not time out (else bit 16 is set).
+ */
+int moe_selftest_bounded_wait(int limit_us, int32_t* err, int32_t* waited_us,
+                              void* stream);
+
 /* Library version string (static storage). */
 const char* moe_version(void);
 
