@@ -22,6 +22,7 @@ __all__ = [
     "E4M3_MAX", "e4m3_decode_table", "e4m3_decode", "e4m3_encode", "e4m3_encode_bruteforce",
     "e8m0_exponent", "mx_quantize_blocks", "mx_quantize_rows",
     "mx_quantize_cols", "mx_quantize_weights", "mx_dequantize", "mx_fc2",
+    "mx_dgrad", "mx_wgrad", "mx_grouped_mlp_bwd",
 ]
 
 E4M3_MAX = 448.0
@@ -180,3 +181,107 @@ def mx_fc2(A_q, A_s, W2_q, W2_s, offsets):
         W = mx_dequantize(W2_q[e], W2_s[e], axis_block=0)
         Y[r0:r1] = A[r0:r1] @ W
     return bf16_round(Y)
+
+
+# ---------------------------------------------------------------- backward
+# MXFP8 backward of the expert MLP.  The pages name the fused backward kernel
+# ([TE] "다음 단계: NVFP4, GEMM 융합 양자화, A2A 오버랩": GroupGemm +
+# dActivation + Quantize/Transpose) and the reason a transposed copy is
+# written at all ([CuTe] "무엇을 해결하려는가": low-precision output plus a
+# transposed output): a weight gradient contracts over the rows of an expert,
+# so its operands need blocks that run along the rows.  Reading: every
+# backward GEMM takes MXFP8 operands with 32-element blocks along its own
+# reduction index -
+#   data gradients (reduction over a hidden index): row-wise blocks of the
+#     activation gradient and blocks along the same index of the weight;
+#   weight gradients (reduction over the rows of one expert): the
+#     column-wise, group-aware blocks of the transposed copies.
+# Accumulation is exact here (float64 of exactly decoded values); dH is
+# rounded to bf16 before it is quantised, as a bf16 store would leave it.
+
+def mx_dgrad(G_q, G_s, W_q, W_s, offsets):
+    """Block-scaled data gradient out_e = deq(G)[rows of e] @ deq(W_e)^T.
+
+    G_q [M, K] codes with row-wise scales G_s [M, K/32]; W_q [E, N, K] codes
+    with scales W_s [E, N, K/32] (blocks along K, the last axis).  Returns
+    float64 [M, N], unrounded; rows outside every expert are NaN."""
+    G = mx_dequantize(G_q, G_s, axis_block=1)
+    E, N, K = W_q.shape
+    out = np.full((G.shape[0], N), np.nan)
+    for e in range(E):
+        r0, r1 = int(offsets[e]), int(offsets[e + 1])
+        if r1 <= r0:
+            continue
+        W = mx_dequantize(W_q[e], W_s[e], axis_block=1)       # [N, K]
+        out[r0:r1] = G[r0:r1] @ W.T
+    return out
+
+
+def mx_wgrad(P_qT, P_sT, Q_qT, Q_sT, offsets):
+    """Block-scaled weight gradient dW_e = P_e^T Q_e, summed over the rows of
+    expert e, from the transposed copies: P_qT [p, M] with scales P_sT
+    [p, M/32] (blocks of 32 rows inside one expert), Q_qT [q, M], Q_sT.
+    Returns float64 [E, p, q], unrounded; an expert with no rows gets 0."""
+    P = mx_dequantize(P_qT, P_sT, axis_block=1)              # [p, M]
+    Q = mx_dequantize(Q_qT, Q_sT, axis_block=1)              # [q, M]
+    E = len(offsets) - 1
+    dW = np.zeros((E, P.shape[0], Q.shape[0]))
+    for e in range(E):
+        r0, r1 = int(offsets[e]), int(offsets[e + 1])
+        if r1 > r0:
+            dW[e] = P[:, r0:r1] @ Q[:, r0:r1].T
+    return dW
+
+
+def mx_grouped_mlp_bwd(x_perm, H, A, dY, offsets, W1, W2, act: str):
+    """MXFP8 backward of the grouped expert MLP (see the reading above).
+
+    Inputs are the bf16 values of x_perm [M, d], H [M, n1], A [M, n],
+    dY [M, d], W1 [E, d, n1], W2 [E, n, d]; offsets multiples of 32.  Steps:
+      1. dY -> row-wise blocks (along d) and the group-aware transposed copy;
+      2. W2 -> blocks along d, W1 -> blocks along n1 (each weight's own
+         reduction index in its data gradient);
+      3. dA = deq(dY) deq(W2_e)^T;  dH = act'(H; dA), rounded to bf16;
+      4. dW2_e = deq(A^T) deq(dY^T) over the expert's rows (A's transposed
+         copy is the forward's);
+      5. dH -> row-wise blocks (along n1) and the transposed copy;
+      6. dX = deq(dH) deq(W1_e)^T;
+      7. x -> transposed copy;  dW1_e = deq(x^T) deq(dH^T).
+    Returns a dict with dH, dX, dW1, dW2 (bf16-rounded float64) and the
+    quantised intermediates (codes, scales) of steps 1, 2, 5 and 7."""
+    from .moe import act_backward, bf16_round
+    x_perm = np.asarray(x_perm, dtype=np.float64)
+    H = np.asarray(H, dtype=np.float64)
+    A = np.asarray(A, dtype=np.float64)
+    dY = np.asarray(dY, dtype=np.float64)
+    W1 = np.asarray(W1, dtype=np.float64)
+    W2 = np.asarray(W2, dtype=np.float64)
+    M = x_perm.shape[0]
+    E, d, n1 = W1.shape
+    n = W2.shape[1]
+    dy_q, dy_s = mx_quantize_rows(dY)
+    dy_qT, dy_sT = mx_quantize_cols(dY, offsets, M)
+    w2_q, w2_s = mx_quantize_rows(W2.reshape(E * n, d))
+    w1_q, w1_s = mx_quantize_rows(W1.reshape(E * d, n1))
+    w2_q, w2_s = w2_q.reshape(E, n, d), w2_s.reshape(E, n, d // 32)
+    w1_q, w1_s = w1_q.reshape(E, d, n1), w1_s.reshape(E, d, n1 // 32)
+    dA = mx_dgrad(dy_q, dy_s, w2_q, w2_s, offsets)
+    dH = np.full((M, n1), np.nan)
+    for e in range(E):
+        r0, r1 = int(offsets[e]), int(offsets[e + 1])
+        if r1 > r0:
+            dH[r0:r1] = bf16_round(act_backward(H[r0:r1], dA[r0:r1], act))
+    a_qT, a_sT = mx_quantize_cols(A, offsets, M)
+    dW2 = bf16_round(mx_wgrad(a_qT, a_sT, dy_qT, dy_sT, offsets))
+    used = int(offsets[-1])
+    dH0 = np.where(np.isnan(dH), 0.0, dH)
+    dh_q, dh_s = mx_quantize_rows(dH0)
+    dh_qT, dh_sT = mx_quantize_cols(dH0, offsets, M)
+    dX = bf16_round(mx_dgrad(dh_q, dh_s, w1_q, w1_s, offsets))
+    x_qT, x_sT = mx_quantize_cols(x_perm, offsets, M)
+    dW1 = bf16_round(mx_wgrad(x_qT, x_sT, dh_qT, dh_sT, offsets))
+    return {"dH": dH, "dX": dX, "dW1": dW1, "dW2": dW2,
+            "dy_q": dy_q[:used], "dy_s": dy_s[:used], "dy_qT": dy_qT, "dy_sT": dy_sT,
+            "w2_q": w2_q, "w2_s": w2_s, "w1_q": w1_q, "w1_s": w1_s,
+            "dh_q": dh_q[:used], "dh_s": dh_s[:used], "dh_qT": dh_qT, "dh_sT": dh_sT,
+            "x_qT": x_qT, "x_sT": x_sT}
