@@ -95,7 +95,7 @@ def load_peaks():
 
 def kernel_src_hash():
     h = hashlib.sha256()
-    for f in ("gemm.cu", "gemm.cuh", "ptx.cuh"):
+    for f in ("gemm.cu", "gemm.cuh", "ptx.cuh", "act.cuh"):
         h.update(open(os.path.join(ROOT, "dropless_grouped_gemm_gb300", "csrc", f), "rb").read())
     return h.hexdigest()[:16]
 

@@ -26,6 +26,7 @@ __all__ = [
     "router_topk",
     "permute", "unpermute", "grouped_mlp_fwd", "grouped_mlp_bwd", "MoeError",
     "FLAG_MXFP8", "MxFwd", "mx_quantize_weights", "mx_quantize", "mx_buffers",
+    "MxBwd", "mx_quantize_weights_rowwise", "mx_bwd_workspace_size", "grouped_mlp_bwd_mx",
 ]
 
 ACT = {"swiglu": 0, "geglu": 1, "srelu": 2}
@@ -47,6 +48,13 @@ class MxFwd(ctypes.Structure):
     """moe_mx_fwd: MXFP8 buffers of the forward (device pointers)."""
     _fields_ = [("w2_q", ctypes.c_void_p), ("w2_s", ctypes.c_void_p), ("a_q", ctypes.c_void_p),
                 ("a_s", ctypes.c_void_p), ("a_qT", ctypes.c_void_p), ("a_sT", ctypes.c_void_p)]
+
+
+class MxBwd(ctypes.Structure):
+    """moe_mx_bwd: MXFP8 operands and workspace of the backward (device pointers)."""
+    _fields_ = [("a_qT", ctypes.c_void_p), ("a_sT", ctypes.c_void_p), ("w2_q", ctypes.c_void_p),
+                ("w2_s", ctypes.c_void_p), ("w1_q", ctypes.c_void_p), ("w1_s", ctypes.c_void_p),
+                ("workspace", ctypes.c_void_p), ("ws_bytes", ctypes.c_size_t)]
 
 
 def lib_path() -> str:
@@ -91,6 +99,15 @@ def lib():
         L.moe_grouped_mlp_bwd.restype = i32
         L.moe_grouped_mlp_bwd.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, vp, vp, i32, i32,
                                           vp, vp, vp, vp, vp, vp]
+        L.moe_mx_quantize_weights_rowwise.restype = i32
+        L.moe_mx_quantize_weights_rowwise.argtypes = [vp, i32, i32, vp, vp, vp]
+        L.moe_mx_bwd_workspace_size.restype = sz
+        L.moe_mx_bwd_workspace_size.argtypes = [i32, i32, i32, i32]
+        L.moe_grouped_mlp_bwd_mx.restype = i32
+        L.moe_grouped_mlp_bwd_mx.argtypes = [vp, vp, vp, vp, i32, i32, i32, i32, i32, vp, vp, vp,
+                                             vp, vp, vp, vp]
+        L.moe_selftest_bounded_wait.restype = i32
+        L.moe_selftest_bounded_wait.argtypes = [i32, vp, vp, vp]
         _LIB = L
     return _LIB
 
@@ -343,3 +360,66 @@ def mx_quantize(src: torch.Tensor, offsets: torch.Tensor, transposed: bool = Tru
                                _ptr(s), _ptr(qT), _ptr(sT), _ptr(err), _stream(stream))
     _check(rc, "moe_mx_quantize")
     return q, s, qT, sT, err
+
+
+def mx_quantize_weights_rowwise(W: torch.Tensor, q: torch.Tensor | None = None,
+                                s: torch.Tensor | None = None, stream=None):
+    """MXFP8 codes of a weight with blocks along its last axis and scales in
+    weight tiles (moe_mx_quantize_weights_rowwise); W is [E, R, K] or [R, K]."""
+    _need(W, torch.bfloat16, "W")
+    K = W.shape[-1]
+    rows = W.numel() // K
+    if q is None:
+        q = torch.empty(tuple(W.shape), dtype=torch.uint8, device=W.device)
+    if s is None:
+        s = torch.empty(rows * K // 32, dtype=torch.uint8, device=W.device)
+    _need(q, torch.uint8, "q")
+    _need(s, torch.uint8, "s")
+    rc = lib().moe_mx_quantize_weights_rowwise(_ptr(W), rows, K, _ptr(q), _ptr(s), _stream(stream))
+    _check(rc, "moe_mx_quantize_weights_rowwise")
+    return q, s
+
+
+def mx_bwd_workspace_size(M_cap: int, d: int, n: int, act: str = "swiglu") -> int:
+    return int(lib().moe_mx_bwd_workspace_size(M_cap, d, n, ACT[act]))
+
+
+def grouped_mlp_bwd_mx(x_perm, h_saved, dy_perm, offsets, mx: dict, act: str = "swiglu",
+                       dh=None, dx_perm=None, dW1=None, dW2=None, err=None, workspace=None,
+                       stream=None):
+    """MXFP8 grouped expert MLP backward (moe_grouped_mlp_bwd_mx).  ``mx``
+    holds uint8 tensors a_qT, a_sT (the forward's transposed copy), w2_q, w2_s
+    (W2 with blocks along d) and w1_q, w1_s (W1 with blocks along n1).
+    Returns (dh, dx_perm, dW1, dW2, err)."""
+    for t, nm in ((x_perm, "x_perm"), (h_saved, "h_saved"), (dy_perm, "dy_perm")):
+        _need(t, torch.bfloat16, nm)
+    _need(offsets, torch.int32, "offsets", 1)
+    for k_ in ("a_qT", "a_sT", "w2_q", "w2_s", "w1_q", "w1_s"):
+        _need(mx.get(k_), torch.uint8, k_)
+    M_cap, d = x_perm.shape
+    E = offsets.numel() - 1
+    n = mx["a_qT"].shape[0]
+    n1 = h_saved.shape[1]
+    dev = x_perm.device
+    if dh is None:
+        dh = torch.empty((M_cap, n1), dtype=torch.bfloat16, device=dev)
+    if dx_perm is None:
+        dx_perm = torch.empty((M_cap, d), dtype=torch.bfloat16, device=dev)
+    if dW1 is None:
+        dW1 = torch.empty((E, d, n1), dtype=torch.bfloat16, device=dev)
+    if dW2 is None:
+        dW2 = torch.empty((E, n, d), dtype=torch.bfloat16, device=dev)
+    err = _err_word(err, dev)
+    need = mx_bwd_workspace_size(M_cap, d, n, act)
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=dev)
+    _need(workspace, torch.uint8, "workspace")
+    st = MxBwd(mx["a_qT"].data_ptr(), mx["a_sT"].data_ptr(), mx["w2_q"].data_ptr(),
+               mx["w2_s"].data_ptr(), mx["w1_q"].data_ptr(), mx["w1_s"].data_ptr(),
+               workspace.data_ptr(), workspace.numel())
+    rc = lib().moe_grouped_mlp_bwd_mx(_ptr(x_perm), _ptr(h_saved), _ptr(dy_perm), _ptr(offsets),
+                                      E, M_cap, d, n, ACT[act], ctypes.byref(st), _ptr(dh),
+                                      _ptr(dx_perm), _ptr(dW1), _ptr(dW2), _ptr(err),
+                                      _stream(stream))
+    _check(rc, "moe_grouped_mlp_bwd_mx")
+    return dh, dx_perm, dW1, dW2, err

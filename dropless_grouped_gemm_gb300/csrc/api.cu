@@ -42,7 +42,50 @@ cudaError_t gemm(moe::GemmKind kind, int act, const CUtensorMap& ta, const CUten
   return e;
 }
 
+cudaError_t mx_gemm(moe::MxKind kind, int act, const CUtensorMap& ta, const CUtensorMap& tb,
+                    const CUtensorMap& tc, const moe::MxGemmArgs& g, int sms, cudaStream_t s) {
+  ev_begin(s);
+  const cudaError_t e = moe::launch_mx_gemm(kind, act, ta, tb, tc, g, sms, s);
+  ev_end(s);
+  return e;
+}
+
 bool misaligned(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) != 0; }
+
+// 256-byte aligned carving of a caller-provided workspace
+struct Carve {
+  uint8_t* base;
+  size_t used;
+  uint8_t* take(size_t bytes) {
+    uint8_t* p = base ? base + used : nullptr;
+    used += (bytes + 255) & ~static_cast<size_t>(255);
+    return p;
+  }
+};
+
+// regions of the MXFP8 backward's workspace, in carving order
+struct MxBwdWs {
+  uint8_t *dy_q, *dy_s, *dy_qT, *dy_sT, *x_qT, *x_sT, *a_sT, *dh_q, *dh_s, *dh_qT, *dh_sT;
+  size_t bytes;
+};
+MxBwdWs carve_mx_bwd(void* base, int M_cap, int d, int n1, int n) {
+  Carve c{static_cast<uint8_t*>(base), 0};
+  const size_t M = static_cast<size_t>(M_cap);
+  MxBwdWs w;
+  w.dy_q = c.take(M * d);
+  w.dy_s = c.take(M * d / 8);
+  w.dy_qT = c.take(M * d);
+  w.dy_sT = c.take(M * d / 8);
+  w.x_qT = c.take(M * d);
+  w.x_sT = c.take(M * d / 8);
+  w.a_sT = c.take(M * n / 8);
+  w.dh_q = c.take(M * n1);
+  w.dh_s = c.take(M * n1 / 8);
+  w.dh_qT = c.take(M * n1);
+  w.dh_sT = c.take(M * n1 / 8);
+  w.bytes = c.used;
+  return w;
+}
 
 int num_sms_current() {
   static int cache[64] = {0};
@@ -323,11 +366,11 @@ int moe_grouped_mlp_fwd(const moe_bf16* x_perm, const int32_t* offsets, int E, i
   ev_end(s);
   if (e != cudaSuccess) return MOE_E_CUDA;
   if (use_mx) {
-    moe::MxFc2Args q{};
-    q.offsets = offsets; q.E = E; q.M_cap = M_cap; q.n = n; q.d = d;
-    q.a_s = mx->a_s; q.w2_s = mx->w2_s; q.out = y_perm; q.err = err;
+    moe::MxGemmArgs q{};
+    q.offsets = offsets; q.E = E; q.M_cap = M_cap; q.K = n; q.N = d;
+    q.a_s = mx->a_s; q.b_s = mx->w2_s; q.out = y_perm; q.ldo = d; q.err = err;
     ev_begin(s);
-    e = moe::launch_mx_fc2(ta, tw2, q, sms, s);
+    e = moe::launch_mx_gemm(moe::MxKind::kFc2, 0, ta, tw2, ta, q, sms, s);
     ev_end(s);
     if (e != cudaSuccess) return MOE_E_CUDA;
     g_last_launches = 2;
@@ -429,6 +472,119 @@ int moe_mx_quantize_weights(const moe_bf16* W2, int E, int n, int d, uint8_t* w2
   return cuda_rc(e);
 }
 
+size_t moe_mx_bwd_workspace_size(int M_cap, int d, int n, int act) {
+  if (M_cap < 0 || d <= 0 || n <= 0 || act < MOE_ACT_SWIGLU || act > MOE_ACT_SRELU) return 0;
+  const int n1 = (act == MOE_ACT_SRELU) ? n : 2 * n;
+  return carve_mx_bwd(nullptr, M_cap, d, n1, n).bytes;
+}
+
+int moe_mx_quantize_weights_rowwise(const moe_bf16* W, int rows, int cols, uint8_t* q,
+                                    uint8_t* sc, void* stream) {
+  g_last_launches = 0;
+  if (rows <= 0 || cols <= 0 || rows % 128 || cols % 128) return MOE_E_SIZE;
+  if (!W || !q || !sc) return MOE_E_NULL;
+  if (misaligned(W) || misaligned(q)) return MOE_E_ALIGN;
+  const int sms = num_sms_current();
+  if (sms <= 0) return MOE_E_CUDA;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  ev_begin(s);
+  const cudaError_t e = moe::launch_mx_quantize_rows_w(W, rows, cols, q, sc, sms, s);
+  ev_end(s);
+  g_last_launches = 1;
+  return cuda_rc(e);
+}
+
+int moe_grouped_mlp_bwd_mx(const moe_bf16* x_perm, const moe_bf16* h_saved,
+                           const moe_bf16* dy_perm, const int32_t* offsets, int E, int M_cap,
+                           int d, int n, int act, const moe_mx_bwd* mx, moe_bf16* dh,
+                           moe_bf16* dx_perm, moe_bf16* dW1, moe_bf16* dW2, int32_t* err,
+                           void* stream) {
+  g_last_launches = 0;
+  int rc = check_mlp_sizes(E, M_cap, d, n);
+  if (rc) return rc;
+  if (d % 128 || n % 128 || M_cap % 32) return MOE_E_SIZE;
+  if (act < MOE_ACT_SWIGLU || act > MOE_ACT_SRELU) return MOE_E_ARG;
+  if (!offsets || !mx || !dW1 || !dW2 || !err) return MOE_E_NULL;
+  const int n1 = (act == MOE_ACT_SRELU) ? n : 2 * n;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (M_cap == 0) {
+    cudaError_t e = cudaMemsetAsync(dW1, 0, static_cast<size_t>(E) * d * n1 * 2, s);
+    if (e == cudaSuccess) e = cudaMemsetAsync(dW2, 0, static_cast<size_t>(E) * n * d * 2, s);
+    return cuda_rc(e);
+  }
+  if (!x_perm || !h_saved || !dy_perm || !dh || !dx_perm || !mx->a_qT || !mx->a_sT ||
+      !mx->w2_q || !mx->w2_s || !mx->w1_q || !mx->w1_s || !mx->workspace)
+    return MOE_E_NULL;
+  if (misaligned(x_perm) || misaligned(h_saved) || misaligned(dy_perm) || misaligned(dh) ||
+      misaligned(dx_perm) || misaligned(dW1) || misaligned(dW2) || misaligned(mx->a_qT) ||
+      misaligned(mx->w2_q) || misaligned(mx->w2_s) || misaligned(mx->w1_q) ||
+      misaligned(mx->w1_s) || (reinterpret_cast<uintptr_t>(mx->workspace) & 255u))
+    return MOE_E_ALIGN;
+  const MxBwdWs ws = carve_mx_bwd(mx->workspace, M_cap, d, n1, n);
+  if (mx->ws_bytes < ws.bytes) return MOE_E_WORKSPACE;
+  const int sms = num_sms_current();
+  if (sms <= 0) return MOE_E_CUDA;
+
+  CUtensorMap t_dy, t_w2, t_aT, t_dyT, t_dh, t_w1, t_xT, t_dhT, t_dw2, t_dw1;
+  if (!map_act(&t_dy, ws.dy_q, M_cap, d, 128, true) ||        // FC2-dgrad A [M, d]
+      !map_act(&t_w2, mx->w2_q, E * n, d, 128, true) ||       // FC2-dgrad B [E*n, d]
+      !map_act(&t_aT, mx->a_qT, n, M_cap, 128, true) ||       // FC2-wgrad A [n, M]
+      !map_act(&t_dyT, ws.dy_qT, d, M_cap, 128, true) ||      // FC2-wgrad B [d, M]
+      !map_act(&t_dh, ws.dh_q, M_cap, n1, 128, true) ||       // FC1-dgrad A [M, n1]
+      !map_act(&t_w1, mx->w1_q, E * d, n1, 128, true) ||      // FC1-dgrad B [E*d, n1]
+      !map_act(&t_xT, ws.x_qT, d, M_cap, 128, true) ||        // FC1-wgrad A [d, M]
+      !map_act(&t_dhT, ws.dh_qT, n1, M_cap, 128, true) ||     // FC1-wgrad B [n1, M]
+      !map_out3(&t_dw2, dW2, E, n, d, true) || !map_out3(&t_dw1, dW1, E, d, n1, true))
+    return MOE_E_CUDA;
+
+  auto quant = [&](const moe_bf16* src, int cols, uint8_t* q, uint8_t* sc, uint8_t* qT,
+                   uint8_t* sT) {
+    ev_begin(s);
+    const cudaError_t e = moe::launch_mx_quantize_act(src, M_cap, cols, offsets, E, q, sc, qT, sT,
+                                                      err, true, sms, s);
+    ev_end(s);
+    return e;
+  };
+  // 1-3. operands: dY both ways, x transposed, A's transposed scales re-tiled
+  cudaError_t e = quant(dy_perm, d, ws.dy_q, ws.dy_s, ws.dy_qT, ws.dy_sT);
+  if (e == cudaSuccess) e = quant(x_perm, d, nullptr, nullptr, ws.x_qT, ws.x_sT);
+  if (e == cudaSuccess) {
+    ev_begin(s);
+    e = moe::launch_mx_retile_t(mx->a_sT, M_cap, n, offsets, E, ws.a_sT, sms, s);
+    ev_end(s);
+  }
+  if (e != cudaSuccess) return MOE_E_CUDA;
+  // 4. dH = act'(H; dY W2^T)
+  moe::MxGemmArgs g{};
+  g.offsets = offsets; g.E = E; g.M_cap = M_cap; g.K = d; g.N = n;
+  g.a_s = ws.dy_s; g.b_s = mx->w2_s; g.out = dh; g.ldo = n1; g.aux = h_saved; g.ld_aux = n1;
+  g.err = err;
+  e = mx_gemm(moe::MxKind::kDgradAct, act, t_dy, t_w2, t_dy, g, sms, s);
+  // 5. dH both ways
+  if (e == cudaSuccess) e = quant(dh, n1, ws.dh_q, ws.dh_s, ws.dh_qT, ws.dh_sT);
+  if (e != cudaSuccess) return MOE_E_CUDA;
+  // 6. dW2_e = A_e^T dY_e
+  moe::MxGemmArgs gw2{};
+  gw2.offsets = offsets; gw2.E = E; gw2.M_cap = M_cap; gw2.R = n; gw2.N = d;
+  gw2.a_s = ws.a_sT; gw2.b_s = ws.dy_sT; gw2.err = err;
+  e = mx_gemm(moe::MxKind::kWgrad, 0, t_aT, t_dyT, t_dw2, gw2, sms, s);
+  if (e != cudaSuccess) return MOE_E_CUDA;
+  // 7. dX = dH W1^T
+  moe::MxGemmArgs gd{};
+  gd.offsets = offsets; gd.E = E; gd.M_cap = M_cap; gd.K = n1; gd.N = d;
+  gd.a_s = ws.dh_s; gd.b_s = mx->w1_s; gd.out = dx_perm; gd.ldo = d; gd.err = err;
+  e = mx_gemm(moe::MxKind::kDgrad, 0, t_dh, t_w1, t_dh, gd, sms, s);
+  if (e != cudaSuccess) return MOE_E_CUDA;
+  // 8. dW1_e = X_e^T dH_e
+  moe::MxGemmArgs gw1{};
+  gw1.offsets = offsets; gw1.E = E; gw1.M_cap = M_cap; gw1.R = d; gw1.N = n1;
+  gw1.a_s = ws.x_sT; gw1.b_s = ws.dh_sT; gw1.err = err;
+  e = mx_gemm(moe::MxKind::kWgrad, 0, t_xT, t_dhT, t_dw1, gw1, sms, s);
+  if (e != cudaSuccess) return MOE_E_CUDA;
+  g_last_launches = 8;
+  return MOE_OK;
+}
+
 int moe_mx_quantize(const moe_bf16* src, int rows, int cols, const int32_t* offsets, int E,
                     uint8_t* q, uint8_t* sc, uint8_t* qT, uint8_t* sT, int32_t* err,
                     void* stream) {
@@ -443,7 +599,7 @@ int moe_mx_quantize(const moe_bf16* src, int rows, int cols, const int32_t* offs
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   ev_begin(s);
   const cudaError_t e = moe::launch_mx_quantize_act(src, rows, cols, offsets, E, q, sc, qT, sT,
-                                                    err, sms, s);
+                                                    err, false, sms, s);
   ev_end(s);
   g_last_launches = 1;
   return cuda_rc(e);

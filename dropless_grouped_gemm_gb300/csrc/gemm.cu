@@ -19,6 +19,7 @@
 // tile i's epilogue.
 #include <cuda_runtime.h>
 
+#include "act.cuh"
 #include "gemm.cuh"
 #include "mx.cuh"
 #include "ptx.cuh"
@@ -59,35 +60,6 @@ constexpr size_t smem_bytes(int E) {
   return 1024 /*align slack*/ + static_cast<size_t>(Cfg<KIND, SKINNY>::stages) * STAGE_BYTES +
          Cfg<KIND, SKINNY>::stg_bytes + (2 * Cfg<KIND, SKINNY>::stages + 5) * 8 /*barriers*/ +
          16 + 2 * (E + 1) * 4 /*scheduler*/;
-}
-
-// ------------------------------------------------------------ activations
-__device__ __forceinline__ float sigmoidf_(float g) { return 1.0f / (1.0f + __expf(-g)); }
-constexpr float kGeluC = 0.7978845608028654f;  // sqrt(2/pi)
-constexpr float kGeluA = 0.044715f;
-
-template <int ACT>
-__device__ __forceinline__ float gate_phi(float g) {
-  if constexpr (ACT == MOE_ACT_SWIGLU) {
-    return g * sigmoidf_(g);
-  } else {
-    const float z = kGeluC * (g + kGeluA * g * g * g);
-    return 0.5f * g * (1.0f + tanhf(z));
-  }
-}
-// phi and phi' together
-template <int ACT>
-__device__ __forceinline__ void gate_phi_dphi(float g, float& ph, float& dph) {
-  if constexpr (ACT == MOE_ACT_SWIGLU) {
-    const float s = sigmoidf_(g);
-    ph = g * s;
-    dph = s * (1.0f + g * (1.0f - s));
-  } else {
-    const float z = kGeluC * (g + kGeluA * g * g * g);
-    const float th = tanhf(z);
-    ph = 0.5f * g * (1.0f + th);
-    dph = 0.5f * (1.0f + th) + 0.5f * g * (1.0f - th * th) * kGeluC * (1.0f + 3.0f * kGeluA * g * g);
-  }
 }
 
 // ------------------------------------------------------------ scheduling

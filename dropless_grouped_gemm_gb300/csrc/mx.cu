@@ -2,17 +2,26 @@
 //   * mx_quantize_weights: W2 [E, n, d] bf16 -> E4M3 codes [E, n, d] and
 //     E8M0 scales over 32 consecutive rows (FC2's reduction index) per
 //     column, in the MMA-tiled layout (see mx.cuh).
+//   * mx_quantize_rows_w: any weight viewed as [rows, K] with blocks along
+//     K (the reduction index of a data gradient), scales in weight tiles.
 //   * mx_quantize_act: group-aware quantiser of a ragged [rows, cols]
 //     activation: row-wise 1x32 blocks, plus the transposed copy with
-//     column-wise 32x1 blocks that never cross an expert's rows.
-//   * mx_fc2: block-scaled MXFP8 grouped GEMM Y_e = A_e W2_e
-//     (tcgen05.mma.kind::mxf8f6f4.block_scale), same persistent
-//     warp-specialised structure as the bf16 grouped GEMM.
+//     column-wise 32x1 blocks that never cross an expert's rows; scales
+//     plain or in the tiles the GEMM reads (see mxgemm.cuh).
+//   * mx_retile_t: plain transposed scales -> the weight gradient's K tiles.
+//   * mx_gemm: block-scaled MXFP8 grouped GEMM
+//     (tcgen05.mma.kind::mxf8f6f4.block_scale) for FC2, the two data
+//     gradients (FC2's with the dActivation epilogue) and the ragged-K
+//     weight gradients; same persistent warp-specialised structure as the
+//     bf16 grouped GEMM.
 // [CuTe] "무엇을 해결하려는가" and "핵심 아이디어": MXFP8 output and transposed
 // output; [TE] "Transformer Engine이 제공하는 세 가지 구성 요소": group-aware
-// MXFP8 quantisation and an MXFP8 grouped GEMM.
+// MXFP8 quantisation and an MXFP8 grouped GEMM; [TE] "다음 단계: NVFP4, GEMM
+// 융합 양자화, A2A 오버랩": the backward's GroupGemm + dActivation +
+// Quantize/Transpose.
 #include <cuda_runtime.h>
 
+#include "act.cuh"
 #include "mx.cuh"
 #include "mxgemm.cuh"
 #include "ptx.cuh"
@@ -75,17 +84,46 @@ __global__ void __launch_bounds__(256)
 }
 
 // ---------------------------------------------------------------- activations
+// expert holding row `row` (offsets in shared memory): the last e with
+// s_off[e] <= row; empty experts share their start with the next one, so
+// the last such e is the one whose range contains the row
+__device__ __forceinline__ int expert_of_row(const int* s_off, int E, int row) {
+  int lo = 0, hi = E - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (s_off[mid] <= row) lo = mid;
+    else hi = mid - 1;
+  }
+  return lo;
+}
+
+// start of the 128-row tile (or weight-gradient reduction step) that holds
+// the 32-row block starting at row r32: tiles start at offsets[e] + 128 i.
+// Clamped so that a malformed offsets array (reported separately) still
+// gives an index inside the buffer.
+__device__ __forceinline__ int tile_start(const int* s_off, int E, int r32) {
+  const int e = expert_of_row(s_off, E, r32);
+  const int oe = min(max(s_off[e], 0), r32) & ~31;
+  return oe + ((r32 - oe) & ~127);
+}
+
 // one warp: a 32-row block (inside one expert) x a 32-column block
+template <bool TILED>
 __global__ void __launch_bounds__(256)
     mx_quantize_act_kernel(const uint4* __restrict__ src, int rows, int cols,
                            const int32_t* __restrict__ offsets, int E,
                            uint8_t* __restrict__ q, uint8_t* __restrict__ s,
                            uint8_t* __restrict__ qT, uint8_t* __restrict__ sT,
                            int32_t* __restrict__ err) {
+  __shared__ int s_off[MOE_MAX_EXPERTS + 1];
   const int lane = threadIdx.x & 31;
   const int cb_n = cols / 32;
   const long long nwarps = static_cast<long long>(rows / 32) * cb_n;
   const int used = min(max(offsets[E], 0), rows);
+  if (TILED) {
+    for (int e = threadIdx.x; e <= E; e += blockDim.x) s_off[e] = offsets[e];
+    __syncthreads();
+  }
   // a 32-row block must lie inside one expert: expert starts must be
   // multiples of 32 (reported, not repaired)
   if (blockIdx.x == 0)
@@ -109,12 +147,20 @@ __global__ void __launch_bounds__(256)
         v[8 * k + 2 * j + 1] = bf16_hi(xw[j]);
       }
     }
-    uint32_t qw[8];
-    const uint32_t sc = mx_quant32(v, qw);
-    uint4* qo = reinterpret_cast<uint4*>(q + static_cast<long long>(r) * cols + cb * 32);
-    qo[0] = make_uint4(qw[0], qw[1], qw[2], qw[3]);
-    qo[1] = make_uint4(qw[4], qw[5], qw[6], qw[7]);
-    s[static_cast<long long>(r) * cb_n + cb] = static_cast<uint8_t>(sc);
+    const int t0 = TILED ? tile_start(s_off, E, rb * 32) : 0;
+    if (q) {
+      uint32_t qw[8];
+      const uint32_t sc = mx_quant32(v, qw);
+      uint4* qo = reinterpret_cast<uint4*>(q + static_cast<long long>(r) * cols + cb * 32);
+      qo[0] = make_uint4(qw[0], qw[1], qw[2], qw[3]);
+      qo[1] = make_uint4(qw[4], qw[5], qw[6], qw[7]);
+      if (TILED) {
+        const long long chunk = static_cast<long long>(t0 / 32) * (cols / 128) + cb / 4;
+        s[chunk * 512 + mx_chunk_off(r - t0, cb & 3)] = static_cast<uint8_t>(sc);
+      } else {
+        s[static_cast<long long>(r) * cb_n + cb] = static_cast<uint8_t>(sc);
+      }
+    }
     if (qT) {
       uint32_t my_sc = 0;
 #pragma unroll
@@ -124,24 +170,96 @@ __global__ void __launch_bounds__(256)
         qT[static_cast<long long>(cb * 32 + j) * rows + r] = static_cast<uint8_t>(code);
         if (lane == j) my_sc = scj;
       }
-      sT[static_cast<long long>(cb * 32 + lane) * (rows / 32) + rb] = static_cast<uint8_t>(my_sc);
+      const int c = cb * 32 + lane;
+      if (TILED) {
+        const long long chunk = static_cast<long long>(t0 / 32) * (cols / 128) + c / 128;
+        sT[chunk * 512 + mx_chunk_off(c & 127, (rb * 32 - t0) >> 5)] = static_cast<uint8_t>(my_sc);
+      } else {
+        sT[static_cast<long long>(c) * (rows / 32) + rb] = static_cast<uint8_t>(my_sc);
+      }
     }
   }
 }
 
-// ---------------------------------------------------------------- block-scaled FC2
+// ---------------------------------------------------------------- row-wise weights
+// [rows, cols] with blocks of 32 along cols, scales in weight tiles (128-row
+// tiles from row 0); one thread per 32-value block
+__global__ void __launch_bounds__(256)
+    mx_quantize_rows_w_kernel(const uint4* __restrict__ src, long long rows, int cols,
+                              uint4* __restrict__ q, uint8_t* __restrict__ s) {
+  const int cb_n = cols / 32;
+  const long long total = rows * cb_n;
+  for (long long g = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; g < total;
+       g += static_cast<long long>(gridDim.x) * blockDim.x) {
+    const long long r = g / cb_n;
+    const int cb = static_cast<int>(g - r * cb_n);
+    const uint4* p = src + g * 4;                 // 32 bf16 = 4 x 16 bytes
+    float v[32];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const uint4 x = __ldg(p + k);
+      const uint32_t xw[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        v[8 * k + 2 * j] = bf16_lo(xw[j]);
+        v[8 * k + 2 * j + 1] = bf16_hi(xw[j]);
+      }
+    }
+    uint32_t qw[8];
+    const uint32_t sc = mx_quant32(v, qw);
+    q[2 * g] = make_uint4(qw[0], qw[1], qw[2], qw[3]);
+    q[2 * g + 1] = make_uint4(qw[4], qw[5], qw[6], qw[7]);
+    const long long chunk = (r / 128) * (cols / 128) + cb / 4;
+    s[chunk * 512 + mx_chunk_off(static_cast<int>(r & 127), cb & 3)] = static_cast<uint8_t>(sc);
+  }
+}
+
+// ---------------------------------------------------------------- scale re-tiling
+// plain transposed scales sT [cols, rows/32] -> K tiles (one thread a byte)
+__global__ void __launch_bounds__(256)
+    mx_retile_t_kernel(const uint8_t* __restrict__ sT, int rows, int cols,
+                       const int32_t* __restrict__ offsets, int E, uint8_t* __restrict__ out) {
+  __shared__ int s_off[MOE_MAX_EXPERTS + 1];
+  for (int e = threadIdx.x; e <= E; e += blockDim.x) s_off[e] = offsets[e];
+  __syncthreads();
+  const int rb_n = rows / 32;
+  const int used = min(max(s_off[E], 0), rows);
+  const long long total = static_cast<long long>(cols) * rb_n;
+  for (long long g = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; g < total;
+       g += static_cast<long long>(gridDim.x) * blockDim.x) {
+    const int c = static_cast<int>(g / rb_n);
+    const int rb = static_cast<int>(g - static_cast<long long>(c) * rb_n);
+    if (rb * 32 >= used) continue;
+    const int t0 = tile_start(s_off, E, rb * 32);
+    const long long chunk = static_cast<long long>(t0 / 32) * (cols / 128) + c / 128;
+    out[chunk * 512 + mx_chunk_off(c & 127, (rb * 32 - t0) >> 5)] = sT[g];
+  }
+}
+
+// ---------------------------------------------------------------- block-scaled GEMM
 constexpr int QBM = 128, QBN = 128, QBK = 128;  // QBK: FP8 elements (= bytes) of K
-constexpr int QSTAGES = 6;
 constexpr int QA_BYTES = QBM * QBK;               // 16 KB
 constexpr int QB_BYTES = QBN * QBK;               // 16 KB
 constexpr int QSTAGE_BYTES = QA_BYTES + QB_BYTES + 1024;  // + SFA, SFB chunks
 constexpr int QTHREADS = 192;
+constexpr int QEPI_WARPS = 4;
 constexpr int QTMEM_COLS = 512;
 constexpr int QSF_TMEM = 2 * QBN;                 // scale columns after the accumulators
+constexpr int QBOX_BYTES = 32 * 64 * 2;           // staged output box: 32 rows x 64 bf16
 
+// The weight gradient stages its output for TMA stores (two boxes per
+// epilogue warp, 128-byte swizzle, plus one box of zeros for experts with
+// no rows) and so keeps four stages; the other kinds keep six.
+template <MxKind KIND>
+struct QCfg {
+  static constexpr bool W = (KIND == MxKind::kWgrad);
+  static constexpr int stages = W ? 4 : 6;
+  static constexpr int stg_bytes = W ? (2 * QEPI_WARPS + 1) * QBOX_BYTES : 0;
+};
+template <MxKind KIND>
 constexpr size_t mx_smem_bytes(int E) {
-  return 1024 + static_cast<size_t>(QSTAGES) * QSTAGE_BYTES + (2 * QSTAGES + 5) * 8 + 16 +
-         2 * (E + 1) * 4;
+  return 1024 + static_cast<size_t>(QCfg<KIND>::stages) * QSTAGE_BYTES + QCfg<KIND>::stg_bytes +
+         (2 * QCfg<KIND>::stages + 5) * 8 + 16 + 2 * (E + 1) * 4;
 }
 
 // Instruction descriptor, kind::mxf8f6f4 block-scaled: A/B E4M3 (format 0),
@@ -190,19 +308,125 @@ __device__ __forceinline__ void umma_mx(uint32_t d_tmem, uint64_t a_desc, uint64
 }
 
 struct QTile {
-  int e, row0, rows, n0;
+  int e;
+  int row0, rows;   // ragged-row kinds: first global row, valid rows
+  int m0;           // kWgrad: first output row within the expert
+  int n0;           // first accumulator column
+  int kblocks;      // 128-element reduction steps
+  int k0;           // kWgrad: first reduction row (global)
+  int klast;        // kWgrad: valid rows of the last step (a multiple of 32)
 };
 
+template <MxKind KIND>
+__device__ __forceinline__ int mx_tiles_of_expert(const MxGemmArgs& g, const int* s_off, int e) {
+  const int mt = (KIND == MxKind::kWgrad) ? g.R / QBM : (s_off[e + 1] - s_off[e] + QBM - 1) / QBM;
+  return mt * (g.N / QBN);
+}
+
+template <MxKind KIND>
+__device__ __forceinline__ QTile mx_decode(const MxGemmArgs& g, const int* s_off, const int* s_ts,
+                                           int t) {
+  int lo = 0, hi = g.E - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi) >> 1;
+    if (s_ts[mid + 1] <= t) lo = mid + 1;
+    else hi = mid;
+  }
+  const int nt = g.N / QBN;
+  const int local = t - s_ts[lo];
+  const int mi = local / nt;
+  QTile tl;
+  tl.e = lo;
+  tl.n0 = (local - mi * nt) * QBN;
+  if constexpr (KIND == MxKind::kWgrad) {
+    tl.m0 = mi * QBM;
+    tl.k0 = s_off[lo];
+    const int kr = s_off[lo + 1] - s_off[lo];
+    tl.kblocks = (kr + QBK - 1) / QBK;
+    tl.klast = kr - (tl.kblocks - 1) * QBK;
+    tl.row0 = 0;
+    tl.rows = 0;
+  } else {
+    tl.row0 = s_off[lo] + mi * QBM;
+    tl.rows = min(QBM, s_off[lo + 1] - tl.row0);
+    tl.kblocks = g.K / QBK;
+    tl.klast = QBK;
+    tl.m0 = 0;
+    tl.k0 = 0;
+  }
+  return tl;
+}
+
+// 32 fp32 accumulator columns -> 32 bf16 at p (64 bytes)
+__device__ __forceinline__ void mx_store_row32(uint16_t* p, const uint32_t (&v)[32]) {
+#pragma unroll
+  for (int k = 0; k < 4; ++k)
+    *reinterpret_cast<uint4*>(p + 8 * k) = make_uint4(
+        pack_bf16x2(__uint_as_float(v[8 * k + 0]), __uint_as_float(v[8 * k + 1])),
+        pack_bf16x2(__uint_as_float(v[8 * k + 2]), __uint_as_float(v[8 * k + 3])),
+        pack_bf16x2(__uint_as_float(v[8 * k + 4]), __uint_as_float(v[8 * k + 5])),
+        pack_bf16x2(__uint_as_float(v[8 * k + 6]), __uint_as_float(v[8 * k + 7])));
+}
+
+// dA columns col..col+31 of one row -> dH (same interleaving as H)
+template <int ACT>
+__device__ __forceinline__ void mx_dact_row32(const MxGemmArgs& g, long long grow, int col,
+                                              const uint32_t (&r)[32]) {
+  if constexpr (ACT == MOE_ACT_SRELU) {
+    const uint16_t* hp = g.aux + grow * g.ld_aux + col;
+    uint16_t* p = g.out + grow * g.ldo + col;
+#pragma unroll
+    for (int v = 0; v < 4; ++v) {
+      const uint4 hv = *reinterpret_cast<const uint4*>(hp + 8 * v);
+      const uint32_t hw[4] = {hv.x, hv.y, hv.z, hv.w};
+      uint32_t o[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+        o[i] = pack_bf16x2(2.f * fmaxf(bf16_lo(hw[i]), 0.f) * __uint_as_float(r[8 * v + 2 * i]),
+                           2.f * fmaxf(bf16_hi(hw[i]), 0.f) * __uint_as_float(r[8 * v + 2 * i + 1]));
+      *reinterpret_cast<uint4*>(p + 8 * v) = make_uint4(o[0], o[1], o[2], o[3]);
+    }
+  } else {
+    const uint16_t* hp = g.aux + grow * g.ld_aux + 2 * col;
+    uint16_t* p = g.out + grow * g.ldo + 2 * col;
+#pragma unroll
+    for (int v = 0; v < 8; ++v) {
+      const uint4 hv = *reinterpret_cast<const uint4*>(hp + 8 * v);
+      const uint32_t hw[4] = {hv.x, hv.y, hv.z, hv.w};  // (gate, up) pairs
+      uint32_t o[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float gg = bf16_lo(hw[i]), uu = bf16_hi(hw[i]);
+        const float da = __uint_as_float(r[4 * v + i]);
+        float ph, dph;
+        gate_phi_dphi<ACT>(gg, ph, dph);
+        o[i] = pack_bf16x2(da * uu * dph, da * ph);
+      }
+      *reinterpret_cast<uint4*>(p + 8 * v) = make_uint4(o[0], o[1], o[2], o[3]);
+    }
+  }
+}
+
+// Persistent warp-specialised block-scaled grouped GEMM: warp 0 TMA producer
+// (operand tiles by tensor maps, scale chunks by bulk copies), warp 1 TMEM
+// owner and MMA issuer (128 x 128 x 32 tcgen05.mma ... block_scale; the
+// scale chunks of a stage go to TMEM with tcgen05.cp), warps 2-5 epilogue.
+template <MxKind KIND, int ACT>
 __global__ void __launch_bounds__(QTHREADS, 1)
-    mx_fc2_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                  const MxFc2Args g) {
-  constexpr uint32_t IDESC = idesc_mx(QBM, QBN, false, true);
+    mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                   const __grid_constant__ CUtensorMap tmC, const MxGemmArgs g) {
+  constexpr bool W = (KIND == MxKind::kWgrad);
+  constexpr bool B_MN = (KIND == MxKind::kFc2);
+  constexpr uint32_t IDESC = idesc_mx(QBM, QBN, false, B_MN);
+  constexpr int NST = QCfg<KIND>::stages;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
-  uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem + QSTAGES * QSTAGE_BYTES);
-  uint64_t* empty_bar = full_bar + QSTAGES;
-  uint64_t* tfull_bar = empty_bar + QSTAGES;
+  uint8_t* staging = smem + NST * QSTAGE_BYTES;               // 2 boxes per epilogue warp
+  uint8_t* zero_box = staging + 2 * QEPI_WARPS * QBOX_BYTES;
+  uint64_t* full_bar = reinterpret_cast<uint64_t*>(staging + QCfg<KIND>::stg_bytes);
+  uint64_t* empty_bar = full_bar + NST;
+  uint64_t* tfull_bar = empty_bar + NST;
   uint64_t* tempty_bar = tfull_bar + 2;
   uint64_t* drain_bar = tempty_bar + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain_bar + 1);
@@ -210,23 +434,27 @@ __global__ void __launch_bounds__(QTHREADS, 1)
   int* s_off = reinterpret_cast<int*>(tmem_slot + 4);
   int* s_ts = s_off + (g.E + 1);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int nt = g.d / QBN;
-  const int kblocks = g.n / QBK;
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < QSTAGES; ++i) {
+    for (int i = 0; i < NST; ++i) {
       mbar_init(&full_bar[i], 1);
       mbar_init(&empty_bar[i], 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&tfull_bar[i], 1);
-      mbar_init(&tempty_bar[i], 4);
+      mbar_init(&tempty_bar[i], QEPI_WARPS);
     }
     mbar_init(drain_bar, 1);
     *abort_flag = 0;
     fence_mbar_init();
     prefetch_tmap(&tmA);
     prefetch_tmap(&tmB);
+    if (W) prefetch_tmap(&tmC);
+  }
+  if (W && warp >= 2) {  // epilogue threads clear the zero box
+    for (int i = threadIdx.x - 64; i < QBOX_BYTES / 16; i += 32 * QEPI_WARPS)
+      reinterpret_cast<uint4*>(zero_box)[i] = make_uint4(0, 0, 0, 0);
+    fence_proxy_async_smem();
   }
   if (warp == 1) tmem_alloc(tmem_slot, QTMEM_COLS);
   if (warp == 2) {
@@ -250,7 +478,7 @@ __global__ void __launch_bounds__(QTHREADS, 1)
     int carry = 0;
     for (int base = 0; base < g.E; base += 32) {
       const int e = base + lane;
-      const int t = (e < g.E) ? ((s_off[e + 1] - s_off[e] + QBM - 1) / QBM) * nt : 0;
+      const int t = (e < g.E) ? mx_tiles_of_expert<KIND>(g, s_off, e) : 0;
       int v = t;
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
@@ -268,55 +496,52 @@ __global__ void __launch_bounds__(QTHREADS, 1)
   const uint32_t tmem_base = *tmem_slot;
   const int total = s_ts[g.E];
 
-  auto decode = [&](int t) {
-    int lo = 0, hi = g.E - 1;
-    while (lo < hi) {
-      const int mid = (lo + hi) >> 1;
-      if (s_ts[mid + 1] <= t) lo = mid + 1;
-      else hi = mid;
-    }
-    QTile tl;
-    tl.e = lo;
-    const int local = t - s_ts[lo];
-    const int mi = local / nt;
-    tl.n0 = (local - mi * nt) * QBN;
-    tl.row0 = s_off[lo] + mi * QBM;
-    tl.rows = min(QBM, s_off[lo + 1] - tl.row0);
-    return tl;
-  };
-
   if (warp == 0) {
+    // ---------------------------------------------------------- producer
     if (lane == 0) {
       int stage = 0;
       uint32_t phase = 0;
-      bool issued[QSTAGES];
-      uint32_t ipar[QSTAGES];
-      for (int i = 0; i < QSTAGES; ++i) { issued[i] = false; ipar[i] = 0; }
+      bool issued[NST];
+      uint32_t ipar[NST];
+      for (int i = 0; i < NST; ++i) { issued[i] = false; ipar[i] = 0; }
       bool ok = true;
-      const long long sa_stride = g.n / 128;       // chunks per 32-row group of A scales
-      const long long sw_expert = static_cast<long long>(g.n / 32) * g.d;
+      const long long kc_n = g.K / QBK, nt = g.N / QBN, rt = g.R / QBM;
       for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
-        const QTile tl = decode(t);
-        for (int kb = 0; kb < kblocks; ++kb) {
+        const QTile tl = mx_decode<KIND>(g, s_off, s_ts, t);
+        for (int kb = 0; kb < tl.kblocks; ++kb) {
           if (!mbar_wait(&empty_bar[stage], phase ^ 1, abort_flag)) { ok = false; break; }
           uint8_t* sa = smem + stage * QSTAGE_BYTES;
           uint8_t* sb = sa + QA_BYTES;
           uint8_t* ssf = sb + QB_BYTES;
           uint64_t* fb = &full_bar[stage];
           mbar_arrive_expect_tx(fb, QSTAGE_BYTES);
-          tma_load_2d(sa, &tmA, fb, kb * QBK, tl.row0);
-          tma_load_3d(sb, &tmB, fb, tl.n0, kb * QBK, tl.e);
-          bulk_load(ssf, g.a_s + ((tl.row0 / 32) * sa_stride + kb) * 512, 512, fb);
-          bulk_load(ssf + 512,
-                    g.w2_s + tl.e * sw_expert + (static_cast<long long>(kb) * (g.d / 128) + tl.n0 / 128) * 512,
-                    512, fb);
+          long long ca, cb;  // scale chunks of A and B
+          if constexpr (W) {
+            const int kc = tl.k0 + kb * QBK;
+            tma_load_2d(sa, &tmA, fb, kc, tl.m0);
+            tma_load_2d(sb, &tmB, fb, kc, tl.n0);
+            ca = static_cast<long long>(kc / 32) * rt + tl.m0 / QBM;
+            cb = static_cast<long long>(kc / 32) * nt + tl.n0 / QBN;
+          } else {
+            tma_load_2d(sa, &tmA, fb, kb * QBK, tl.row0);
+            ca = static_cast<long long>(tl.row0 / 32) * kc_n + kb;
+            if constexpr (B_MN) {
+              tma_load_3d(sb, &tmB, fb, tl.n0, kb * QBK, tl.e);
+              cb = (static_cast<long long>(tl.e) * kc_n + kb) * nt + tl.n0 / QBN;
+            } else {
+              tma_load_2d(sb, &tmB, fb, kb * QBK, tl.e * g.N + tl.n0);
+              cb = ((static_cast<long long>(tl.e) * g.N + tl.n0) / QBN) * kc_n + kb;
+            }
+          }
+          bulk_load(ssf, g.a_s + ca * 512, 512, fb);
+          bulk_load(ssf + 512, g.b_s + cb * 512, 512, fb);
           issued[stage] = true;
           ipar[stage] = phase;
-          if (++stage == QSTAGES) { stage = 0; phase ^= 1; }
+          if (++stage == NST) { stage = 0; phase ^= 1; }
         }
       }
       if (!ok) {
-        for (int i = 0; i < QSTAGES; ++i)
+        for (int i = 0; i < NST; ++i)
           if (issued[i]) {
             const uint32_t a = smem_u32(&full_bar[i]);
             const uint64_t t0 = globaltimer_ns();
@@ -325,11 +550,13 @@ __global__ void __launch_bounds__(QTHREADS, 1)
       }
     }
   } else if (warp == 1) {
+    // ---------------------------------------------------------- MMA issuer
     int stage = 0;
     uint32_t phase = 0;
     int local = 0;
     bool ok = true;
     for (int t = blockIdx.x; t < total && ok; t += gridDim.x, ++local) {
+      const QTile tl = mx_decode<KIND>(g, s_off, s_ts, t);
       const int buf = local & 1;
       const uint32_t aph = (local >> 1) & 1;
       if (lane == 0) ok = mbar_wait(&tempty_bar[buf], aph ^ 1, abort_flag);
@@ -337,7 +564,7 @@ __global__ void __launch_bounds__(QTHREADS, 1)
       if (!ok) break;
       tc_fence_after();
       const uint32_t d_tmem = tmem_base + buf * QBN;
-      for (int kb = 0; kb < kblocks; ++kb) {
+      for (int kb = 0; kb < tl.kblocks; ++kb) {
         if (lane == 0) ok = mbar_wait(&full_bar[stage], phase, abort_flag);
         ok = __shfl_sync(0xffffffffu, ok, 0);
         if (!ok) break;
@@ -351,17 +578,20 @@ __global__ void __launch_bounds__(QTHREADS, 1)
           tmem_cp_sf(sfa_t, sdesc_sf(smem_u32(ssf)));
           tmem_cp_sf(sfb_t, sdesc_sf(smem_u32(ssf + 512)));
           const uint32_t a0 = smem_u32(sa), b0 = smem_u32(sb);
-#pragma unroll
-          for (int kk = 0; kk < QBK / 32; ++kk) {
+          // an expert's last reduction step of a weight gradient holds
+          // klast (a multiple of 32) of its rows: one MMA per 32 of them
+          const int kk_n = (W && kb == tl.kblocks - 1) ? tl.klast / 32 : QBK / 32;
+          for (int kk = 0; kk < kk_n; ++kk) {
             const uint64_t ad = sdesc_sw128(a0 + kk * 32, 16, 1024);
-            const uint64_t bd = sdesc_sw128(b0 + kk * 4096, QB_BYTES, 1024);
+            const uint64_t bd = B_MN ? sdesc_sw128(b0 + kk * 4096, QB_BYTES, 1024)
+                                     : sdesc_sw128(b0 + kk * 32, 16, 1024);
             const uint32_t id = IDESC | (static_cast<uint32_t>(kk) << 29) | (static_cast<uint32_t>(kk) << 4);
             umma_mx(d_tmem, ad, bd, id, sfa_t, sfb_t, (kb > 0 || kk > 0) ? 1u : 0u);
           }
           umma_commit(&empty_bar[stage]);
         }
         __syncwarp();
-        if (++stage == QSTAGES) { stage = 0; phase ^= 1; }
+        if (++stage == NST) { stage = 0; phase ^= 1; }
       }
       if (!ok) break;
       if (lane == 0) umma_commit(&tfull_bar[buf]);
@@ -375,11 +605,14 @@ __global__ void __launch_bounds__(QTHREADS, 1)
     }
     __syncwarp();
   } else {
+    // ---------------------------------------------------------- epilogue
     const int q = warp & 3;
     const int r = q * 32 + lane;
+    uint8_t* my_stg = staging + (warp - 2) * 2 * QBOX_BYTES;
+    uint32_t slot = 0;
     int local = 0;
     for (int t = blockIdx.x; t < total; t += gridDim.x, ++local) {
-      const QTile tl = decode(t);
+      const QTile tl = mx_decode<KIND>(g, s_off, s_ts, t);
       const int buf = local & 1;
       const uint32_t aph = (local >> 1) & 1;
       bool ok = true;
@@ -387,26 +620,70 @@ __global__ void __launch_bounds__(QTHREADS, 1)
       if (!__shfl_sync(0xffffffffu, ok, 0)) break;
       tc_fence_after();
       const uint32_t tb = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + buf * QBN;
+      if constexpr (W) {
+        if (tl.kblocks == 0) {
+          // expert with no rows: its weight gradient is zero
+          if (lane == 0) {
+            tma_store_3d(&tmC, zero_box, tl.n0, tl.m0 + q * 32, tl.e);
+            tma_store_3d(&tmC, zero_box, tl.n0 + 64, tl.m0 + q * 32, tl.e);
+            bulk_commit();
+          }
+          __syncwarp();
+        } else {
+          // stage each 32-row x 64-column box (128-byte swizzle: 16-byte
+          // chunk j of row r at j ^ (r % 8)) and write it with a TMA store
 #pragma unroll 1
-      for (int c = 0; c < QBN / 32; ++c) {
-        uint32_t v[32];
-        tmem_ld32(tb + c * 32, v);
-        tmem_wait_ld();
-        if (r < tl.rows) {
-          uint16_t* p = g.out + static_cast<long long>(tl.row0 + r) * g.d + tl.n0 + c * 32;
+          for (int h = 0; h < 2; ++h) {
+            uint32_t v0[32], v1[32];
+            tmem_ld32(tb + h * 64, v0);
+            tmem_ld32(tb + h * 64 + 32, v1);
+            tmem_wait_ld();
+            uint8_t* box = my_stg + (slot & 1) * QBOX_BYTES;
+            if (lane == 0) bulk_wait_read_1();     // the box's previous store has read it
+            __syncwarp();
+            uint8_t* row = box + lane * 128;
+            const int sw = lane & 7;
 #pragma unroll
-          for (int k = 0; k < 4; ++k)
-            *reinterpret_cast<uint4*>(p + 8 * k) = make_uint4(
-                pack_bf16x2(__uint_as_float(v[8 * k + 0]), __uint_as_float(v[8 * k + 1])),
-                pack_bf16x2(__uint_as_float(v[8 * k + 2]), __uint_as_float(v[8 * k + 3])),
-                pack_bf16x2(__uint_as_float(v[8 * k + 4]), __uint_as_float(v[8 * k + 5])),
-                pack_bf16x2(__uint_as_float(v[8 * k + 6]), __uint_as_float(v[8 * k + 7])));
+            for (int j = 0; j < 4; ++j) {
+              *reinterpret_cast<uint4*>(row + ((j ^ sw) * 16)) = make_uint4(
+                  pack_bf16x2(__uint_as_float(v0[8 * j + 0]), __uint_as_float(v0[8 * j + 1])),
+                  pack_bf16x2(__uint_as_float(v0[8 * j + 2]), __uint_as_float(v0[8 * j + 3])),
+                  pack_bf16x2(__uint_as_float(v0[8 * j + 4]), __uint_as_float(v0[8 * j + 5])),
+                  pack_bf16x2(__uint_as_float(v0[8 * j + 6]), __uint_as_float(v0[8 * j + 7])));
+              *reinterpret_cast<uint4*>(row + (((j + 4) ^ sw) * 16)) = make_uint4(
+                  pack_bf16x2(__uint_as_float(v1[8 * j + 0]), __uint_as_float(v1[8 * j + 1])),
+                  pack_bf16x2(__uint_as_float(v1[8 * j + 2]), __uint_as_float(v1[8 * j + 3])),
+                  pack_bf16x2(__uint_as_float(v1[8 * j + 4]), __uint_as_float(v1[8 * j + 5])),
+                  pack_bf16x2(__uint_as_float(v1[8 * j + 6]), __uint_as_float(v1[8 * j + 7])));
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+              tma_store_3d(&tmC, box, tl.n0 + h * 64, tl.m0 + q * 32, tl.e);
+              bulk_commit();
+            }
+            ++slot;
+          }
+        }
+      } else {
+#pragma unroll 1
+        for (int c = 0; c < QBN / 32; ++c) {
+          uint32_t v[32];
+          tmem_ld32(tb + c * 32, v);
+          tmem_wait_ld();
+          if (r < tl.rows) {
+            const long long grow = tl.row0 + r;
+            if constexpr (KIND == MxKind::kDgradAct) mx_dact_row32<ACT>(g, grow, tl.n0 + c * 32, v);
+            else mx_store_row32(g.out + grow * g.ldo + tl.n0 + c * 32, v);
+          }
         }
       }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&tempty_bar[buf]);
     }
+    if (W && lane == 0) bulk_wait_all();  // staged stores done before the CTA exits
+    __syncwarp();
   }
   tc_fence_before();
   __syncthreads();
@@ -415,6 +692,22 @@ __global__ void __launch_bounds__(QTHREADS, 1)
     tc_fence_after();
     tmem_dealloc(tmem_base, QTMEM_COLS);
   }
+}
+
+template <MxKind KIND, int ACT>
+cudaError_t launch_mx_t(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tc,
+                        const MxGemmArgs& g, int num_sms, cudaStream_t st) {
+  auto kern = mx_gemm_kernel<KIND, ACT>;
+  const size_t smem = mx_smem_bytes<KIND>(MOE_MAX_EXPERTS);
+  static bool attr = false;  // per instantiation; the library drives one device
+  if (!attr) {
+    const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                               static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+    attr = true;
+  }
+  kern<<<num_sms, QTHREADS, smem, st>>>(ta, tb, tc, g);
+  return cudaGetLastError();
 }
 
 }  // namespace
@@ -431,28 +724,54 @@ cudaError_t launch_mx_quantize_weights(const uint16_t* w2, int E, int n, int d, 
 
 cudaError_t launch_mx_quantize_act(const uint16_t* src, int rows, int cols, const int32_t* offsets,
                                    int E, uint8_t* q, uint8_t* s, uint8_t* qT, uint8_t* sT,
-                                   int32_t* err, int num_sms, cudaStream_t st) {
+                                   int32_t* err, bool tiled, int num_sms, cudaStream_t st) {
   const long long warps = static_cast<long long>(rows / 32) * (cols / 32);
   const long long want = (warps * 32 + 255) / 256;
   const int blocks = static_cast<int>(want < 16LL * num_sms ? want : 16LL * num_sms);
-  mx_quantize_act_kernel<<<blocks > 0 ? blocks : 1, 256, 0, st>>>(
-      reinterpret_cast<const uint4*>(src), rows, cols, offsets, E, q, s, qT, sT, err);
+  if (tiled)
+    mx_quantize_act_kernel<true><<<blocks > 0 ? blocks : 1, 256, 0, st>>>(
+        reinterpret_cast<const uint4*>(src), rows, cols, offsets, E, q, s, qT, sT, err);
+  else
+    mx_quantize_act_kernel<false><<<blocks > 0 ? blocks : 1, 256, 0, st>>>(
+        reinterpret_cast<const uint4*>(src), rows, cols, offsets, E, q, s, qT, sT, err);
   return cudaGetLastError();
 }
 
-cudaError_t launch_mx_fc2(const CUtensorMap& ta, const CUtensorMap& tb, const MxFc2Args& g,
-                          int num_sms, cudaStream_t st) {
-  const size_t smem = mx_smem_bytes(MOE_MAX_EXPERTS);
-  static bool attr = false;
-  if (!attr) {
-    const cudaError_t e = cudaFuncSetAttribute(mx_fc2_kernel,
-                                               cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                               static_cast<int>(smem));
-    if (e != cudaSuccess) return e;
-    attr = true;
-  }
-  mx_fc2_kernel<<<num_sms, QTHREADS, smem, st>>>(ta, tb, g);
+cudaError_t launch_mx_quantize_rows_w(const uint16_t* src, long long rows, int cols, uint8_t* q,
+                                      uint8_t* s, int num_sms, cudaStream_t st) {
+  const long long threads = rows * (cols / 32);
+  const long long want = (threads + 255) / 256;
+  const int blocks = static_cast<int>(want < 16LL * num_sms ? want : 16LL * num_sms);
+  mx_quantize_rows_w_kernel<<<blocks > 0 ? blocks : 1, 256, 0, st>>>(
+      reinterpret_cast<const uint4*>(src), rows, cols, reinterpret_cast<uint4*>(q), s);
   return cudaGetLastError();
+}
+
+cudaError_t launch_mx_retile_t(const uint8_t* sT, int rows, int cols, const int32_t* offsets,
+                               int E, uint8_t* out, int num_sms, cudaStream_t st) {
+  const long long threads = static_cast<long long>(cols) * (rows / 32);
+  const long long want = (threads + 255) / 256;
+  const int blocks = static_cast<int>(want < 8LL * num_sms ? want : 8LL * num_sms);
+  mx_retile_t_kernel<<<blocks > 0 ? blocks : 1, 256, 0, st>>>(sT, rows, cols, offsets, E, out);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_mx_gemm(MxKind kind, int act, const CUtensorMap& ta, const CUtensorMap& tb,
+                           const CUtensorMap& tc, const MxGemmArgs& g, int num_sms,
+                           cudaStream_t st) {
+  switch (kind) {
+    case MxKind::kFc2: return launch_mx_t<MxKind::kFc2, 0>(ta, tb, tc, g, num_sms, st);
+    case MxKind::kDgrad: return launch_mx_t<MxKind::kDgrad, 0>(ta, tb, tc, g, num_sms, st);
+    case MxKind::kWgrad: return launch_mx_t<MxKind::kWgrad, 0>(ta, tb, tc, g, num_sms, st);
+    case MxKind::kDgradAct:
+      switch (act) {
+        case MOE_ACT_SWIGLU: return launch_mx_t<MxKind::kDgradAct, MOE_ACT_SWIGLU>(ta, tb, tc, g, num_sms, st);
+        case MOE_ACT_GEGLU: return launch_mx_t<MxKind::kDgradAct, MOE_ACT_GEGLU>(ta, tb, tc, g, num_sms, st);
+        case MOE_ACT_SRELU: return launch_mx_t<MxKind::kDgradAct, MOE_ACT_SRELU>(ta, tb, tc, g, num_sms, st);
+        default: return cudaErrorInvalidValue;
+      }
+  }
+  return cudaErrorInvalidValue;
 }
 
 }  // namespace moe

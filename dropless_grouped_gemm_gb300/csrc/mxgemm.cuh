@@ -1,4 +1,21 @@
 // mxgemm.cuh - host-side interface of the MXFP8 kernels (mx.cu).
+//
+// Scale layouts read by the block-scaled GEMM.  All are made of 512-byte
+// chunks in the order tcgen05.cp moves them into TMEM (128 operand rows x 4
+// consecutive 32-blocks of the reduction index; byte mx_chunk_off(r, b), see
+// mx.cuh).  Which 128 rows and which 4 blocks a chunk holds depends on the
+// operand:
+//   row tiles     - an activation [rows, K] with blocks along K, read in
+//                   128-row tiles that start at offsets[e] + 128 i: chunk
+//                   (row0 / 32) * (K / 128) + k / 128.  Size rows * K / 8.
+//   weight tiles  - a weight viewed as [rows, K] (rows = E * N) with blocks
+//                   along K, read in 128-row tiles from row 0: chunk
+//                   (row / 128) * (K / 128) + k / 128.  Size rows * K / 32.
+//   K tiles       - a transposed copy [C, M] with blocks of 32 rows of one
+//                   expert, read by the weight gradient in reduction steps
+//                   of 128 rows that start at offsets[e] + 128 i: chunk
+//                   (k0 / 32) * (C / 128) + c / 128.  Size M * C / 8.
+//   W2 column tiles (forward FC2, moe_mx_quantize_weights) - see moe.h.
 #pragma once
 
 #include <cuda.h>
@@ -8,24 +25,47 @@
 
 namespace moe {
 
-struct MxFc2Args {
+enum class MxKind : int {
+  kFc2 = 0,       // Y = A W2: A row tiles, W2 [E, K, N] N-major with column tiles
+  kDgrad = 1,     // out = G W^T: G row tiles, W [E*N, K] K-major with weight tiles
+  kDgradAct = 2,  // as kDgrad, then dH = act'(H; .) in the epilogue
+  kWgrad = 3,     // dW_e = P_e^T Q_e from transposed copies [R, M], [N, M] (K tiles)
+};
+
+struct MxGemmArgs {
   const int32_t* offsets;  // [E+1], multiples of 32
   int E;
   int M_cap;
-  int n;                   // reduction length (multiple of 128)
-  int d;                   // output columns (multiple of 128)
-  const uint8_t* a_s;      // A row-wise scales, MMA-tiled by 32-row tile start
-  const uint8_t* w2_s;     // W2 scales, MMA-tiled per expert
-  uint16_t* out;           // y_perm [M_cap, d] bf16
+  int K;                   // reduction length of the ragged-row kinds (multiple of 128)
+  int N;                   // accumulator columns (multiple of 128)
+  int R;                   // kWgrad: output rows per expert (multiple of 128)
+  const uint8_t* a_s;      // A scales
+  const uint8_t* b_s;      // B scales
+  uint16_t* out;           // ragged-row kinds: [M_cap, ldo] bf16
+  long long ldo;
+  const uint16_t* aux;     // kDgradAct: H [M_cap, ld_aux]
+  long long ld_aux;
   int32_t* err;
 };
 
 cudaError_t launch_mx_quantize_weights(const uint16_t* w2, int E, int n, int d, uint8_t* q,
                                        uint8_t* s, int num_sms, cudaStream_t st);
+// ragged activation: row-wise codes q / scales s (q may be null: transposed
+// copy only) and the transposed copy qT / sT (may be null).  tiled = false:
+// plain scales s [rows, cols/32], sT [cols, rows/32]; tiled = true: s in row
+// tiles, sT in K tiles.
 cudaError_t launch_mx_quantize_act(const uint16_t* src, int rows, int cols, const int32_t* offsets,
                                    int E, uint8_t* q, uint8_t* s, uint8_t* qT, uint8_t* sT,
-                                   int32_t* err, int num_sms, cudaStream_t st);
-cudaError_t launch_mx_fc2(const CUtensorMap& ta, const CUtensorMap& tb, const MxFc2Args& g,
-                          int num_sms, cudaStream_t st);
+                                   int32_t* err, bool tiled, int num_sms, cudaStream_t st);
+// [rows, cols] (rows a multiple of 128) with blocks along cols, weight tiles
+cudaError_t launch_mx_quantize_rows_w(const uint16_t* src, long long rows, int cols, uint8_t* q,
+                                      uint8_t* s, int num_sms, cudaStream_t st);
+// plain transposed scales sT [cols, rows/32] -> K tiles
+cudaError_t launch_mx_retile_t(const uint8_t* sT, int rows, int cols, const int32_t* offsets,
+                               int E, uint8_t* out, int num_sms, cudaStream_t st);
+// tc: output map of kWgrad ([E, R, N] bf16, box 64 x 32, 128-byte swizzle)
+cudaError_t launch_mx_gemm(MxKind kind, int act, const CUtensorMap& ta, const CUtensorMap& tb,
+                           const CUtensorMap& tc, const MxGemmArgs& g, int num_sms,
+                           cudaStream_t st);
 
 }  // namespace moe

@@ -103,6 +103,35 @@ typedef struct moe_mx_fwd {
   uint8_t* a_sT;        /* [n, M_cap/32] E8M0 scales of a_qT                       */
 } moe_mx_fwd;
 
+/*
+ * MXFP8 backward ([TE] "다음 단계: NVFP4, GEMM 융합 양자화, A2A 오버랩": the
+ * fused GroupGemm + dActivation + Quantize/Transpose kernel; [CuTe]
+ * "무엇을 해결하려는가": the transposed low-precision copy).  Every backward
+ * GEMM takes MXFP8 operands whose 32-blocks run along its own reduction
+ * index:
+ *   FC2-dgrad + dAct  dY row-wise (blocks along d)  x  W2, blocks along d
+ *   FC2-wgrad         A^T (the forward's transposed copy)  x  dY^T
+ *   FC1-dgrad         dH row-wise (blocks along n1) x  W1, blocks along n1
+ *   FC1-wgrad         x^T  x  dH^T
+ * (transposed copies: 32-row blocks inside one expert).  dY, x and dH are
+ * quantised inside moe_grouped_mlp_bwd_mx, into the caller's workspace.
+ * "Weight tiles": W viewed as [rows, K] with blocks along K; 128 rows x 4
+ * blocks per 512-byte chunk (byte layout as above), chunk (row/128) *
+ * (K/128) + k/128; rows*K/32 bytes.
+ */
+typedef struct moe_mx_bwd {
+  const uint8_t* a_qT;  /* [n, M_cap] codes of A^T (moe_mx_fwd.a_qT)             */
+  const uint8_t* a_sT;  /* [n, M_cap/32] their scales (moe_mx_fwd.a_sT)          */
+  const uint8_t* w2_q;  /* [E, n, d] codes of W2 with blocks along d
+                           (moe_mx_quantize_weights_rowwise, rows = E*n)          */
+  const uint8_t* w2_s;  /* weight tiles, E*n*d/32 bytes                            */
+  const uint8_t* w1_q;  /* [E, d, n1] codes of W1 with blocks along n1
+                           (rows = E*d)                                           */
+  const uint8_t* w1_s;  /* weight tiles, E*d*n1/32 bytes                           */
+  void* workspace;      /* device scratch, 256-byte aligned, owned by the caller   */
+  size_t ws_bytes;      /* >= moe_mx_bwd_workspace_size(M_cap, d, n, act)          */
+} moe_mx_bwd;
+
 /* Limits. */
 #define MOE_MAX_EXPERTS 1024
 
@@ -304,6 +333,41 @@ int moe_grouped_mlp_bwd(const moe_bf16* x_perm, const moe_bf16* h_saved,
  */
 int moe_mx_quantize_weights(const moe_bf16* W2, int E, int n, int d,
                             uint8_t* w2_q, uint8_t* w2_s, void* stream);
+
+/*
+ * moe_mx_quantize_weights_rowwise - MXFP8 copy of a weight for a data
+ * gradient: W viewed as [rows, cols] bf16 (W2 [E, n, d] as rows = E*n,
+ * cols = d; W1 [E, d, n1] as rows = E*d, cols = n1), blocks of 32 along
+ * cols.  Writes q [rows, cols] codes and s in weight tiles (rows*cols/32
+ * bytes).  rows, cols multiples of 128.
+ */
+int moe_mx_quantize_weights_rowwise(const moe_bf16* W, int rows, int cols,
+                                    uint8_t* q, uint8_t* s, void* stream);
+
+/*
+ * moe_mx_bwd_workspace_size - bytes of moe_mx_bwd.workspace for a layer
+ * (0 for invalid sizes).  About M_cap * (3.4 d + 2.3 n1 + n/8).
+ */
+size_t moe_mx_bwd_workspace_size(int M_cap, int d, int n, int act);
+
+/*
+ * moe_grouped_mlp_bwd_mx - MXFP8 backward of the grouped expert MLP (same
+ * results as moe_grouped_mlp_bwd up to MXFP8's rounding of the operands).
+ *   x_perm [M_cap, d], h_saved [M_cap, n1], dy_perm [M_cap, d] bf16;
+ *   offsets [E+1] multiples of 32 (route with align = 32); d, n multiples
+ *   of 128, M_cap a multiple of 32.  Outputs dh [M_cap, n1], dx_perm
+ *   [M_cap, d] (rows outside every expert untouched), dW1 [E, d, n1],
+ *   dW2 [E, n, d] bf16 (zero for experts with no rows).  Eight launches:
+ *   three quantisers (dY both ways, x transposed, A's scales re-tiled),
+ *   FC2-dgrad + dAct, the dH quantiser, FC2-wgrad, FC1-dgrad, FC1-wgrad.
+ *   Errors: as moe_grouped_mlp_bwd; MOE_E_WORKSPACE if mx->ws_bytes is too
+ *   small; offsets that are not multiples of 32 raise MOE_DEV_BAD_OFFSETS.
+ */
+int moe_grouped_mlp_bwd_mx(const moe_bf16* x_perm, const moe_bf16* h_saved,
+                           const moe_bf16* dy_perm, const int32_t* offsets, int E,
+                           int M_cap, int d, int n, int act, const moe_mx_bwd* mx,
+                           moe_bf16* dh, moe_bf16* dx_perm, moe_bf16* dW1,
+                           moe_bf16* dW2, int32_t* err, void* stream);
 
 /*
  * moe_mx_quantize - group-aware MXFP8 quantisation of a ragged activation

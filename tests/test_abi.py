@@ -54,6 +54,26 @@ def test_host_argument_errors(L):
                                None) == -3                  # align 0
     assert L.moe_permute(None, None, None, 4, 1, 100, 4, None, None) == -3
     assert L.moe_unpermute(vp(16), None, vp(16), 2, 1, 64, 4, None, None, None, None) == -1
+    # MXFP8 backward: sizes need multiples of 128 (d, n) and 32 (M_cap); mx required
+    assert L.moe_grouped_mlp_bwd_mx(None, None, None, vp(16), 4, 128, 192, 128, 0, None, None,
+                                    None, vp(16), vp(16), vp(16), None) == -3
+    assert L.moe_grouped_mlp_bwd_mx(None, None, None, vp(16), 4, 100, 128, 128, 0, None, None,
+                                    None, vp(16), vp(16), vp(16), None) == -3
+    assert L.moe_grouped_mlp_bwd_mx(None, None, None, vp(16), 4, 128, 128, 128, 0, None, None,
+                                    None, vp(16), vp(16), vp(16), None) == -1
+    assert L.moe_mx_quantize_weights_rowwise(vp(16), 100, 128, vp(16), vp(16), None) == -3
+
+
+def test_mx_bwd_workspace_too_small(L):
+    """A workspace smaller than moe_mx_bwd_workspace_size is refused before
+    any launch (all pointers are dummies: nothing is dereferenced)."""
+    vp = ctypes.c_void_p
+    need = M.mx_bwd_workspace_size(256, 128, 128, "swiglu")
+    assert need >= 256 * (3 * 128 + 2 * 256)
+    st = M.MxBwd(256, 256, 256, 256, 256, 256, 256, need - 1)
+    assert L.moe_grouped_mlp_bwd_mx(vp(256), vp(256), vp(256), vp(256), 2, 256, 128, 128, 0,
+                                    ctypes.byref(st), vp(256), vp(256), vp(256), vp(256),
+                                    vp(256), None) == -6
 
 
 def test_workspace_size_host_only(L):
