@@ -45,13 +45,17 @@ METRIC = "grouped MoE MLP fwd+bwd useful TFLOP/s and % of GB300 dense BF16/FP8 p
 DEFAULT_WORKLOAD = "balanced_e8_m4096_k8192_n4096_swiglu"
 KERNELS_FWD = ["fc1_act", "fc2"]
 KERNELS_BWD = ["fc2_dgrad_dact", "fc2_wgrad", "fc1_dgrad", "fc1_wgrad"]
+# launch order of the MXFP8 backward (weight quantisers, then moe_grouped_mlp_bwd_mx)
+KERNELS_MX_BWD = ["mx_quantize_w2_rows", "mx_quantize_w1_rows", "mx_quantize_dy", "mx_quantize_x",
+                  "mx_retile_a", "fc2_dgrad_dact", "mx_quantize_dh", "fc2_wgrad", "fc1_dgrad",
+                  "fc1_wgrad"]
 
 
 # ---------------------------------------------------------------- accounting
 def useful_flops(w, M):
     """fwd + bwd FLOPs of real rows (the pages' arithmetic-intensity model
     counts the same terms: [Sonic] section on MoE arithmetic intensity).
-    Forward-only workloads (the MXFP8 one) have no backward term."""
+    Forward-only workloads (the MXFP8 forward) have no backward term."""
     n1 = w.n1
     fwd = 2 * M * w.d * n1 + 2 * M * w.n * w.d
     bwd = 2 * M * w.d * w.n + 2 * M * w.n * w.d + 2 * M * n1 * w.d + 2 * M * w.d * n1
@@ -65,13 +69,30 @@ def kernel_work(w, M, E_ne):
     d, n, n1, E = w.d, w.n, w.n1, w.E
     B = 2
     if w.mxfp8:
-        # FC1 (bf16 MMA) writes bf16 A and MX codes (row-wise and transposed,
-        # 1 B each) and scales; FC2 streams E4M3 codes of A and W2
-        return {
-            "mx_quantize_weights": (0, E * n * d * (2 + 1) + E * (n // 32) * d),
-            "fc1_act": (2 * M * d * n1, B * (M * d + E_ne * d * n1 + M * n) + 2 * M * n + M * n // 16),
-            "fc2": (2 * M * n * d, M * n + M * n // 32 + E_ne * n * d + E_ne * (n // 32) * d + B * M * d),
+        # FC1 (bf16 MMA) writes bf16 A (+ H when training) and MX codes
+        # (row-wise and transposed, 1 B each) and scales; the block-scaled
+        # GEMMs stream E4M3 codes (1 B) plus one scale byte per 32 codes
+        mxb = lambda elems: elems + elems // 32
+        work = {
+            "mx_quantize_weights": (0, E * n * d * 2 + mxb(E * n * d)),
+            "fc1_act": (2 * M * d * n1, B * (M * d + E_ne * d * n1 + M * n) + 2 * mxb(M * n) +
+                        (B * M * n1 if w.backward else 0)),
+            "fc2": (2 * M * n * d, mxb(M * n) + mxb(E_ne * n * d) + B * M * d),
         }
+        if w.backward:
+            work.update({
+                "mx_quantize_w2_rows": (0, E * n * d * 2 + mxb(E * n * d)),
+                "mx_quantize_w1_rows": (0, E * d * n1 * 2 + mxb(E * d * n1)),
+                "mx_quantize_dy": (0, B * M * d + 2 * mxb(M * d)),
+                "mx_quantize_x": (0, B * M * d + mxb(M * d)),
+                "mx_retile_a": (0, 2 * (M * n // 32)),
+                "fc2_dgrad_dact": (2 * M * d * n, mxb(M * d) + mxb(E_ne * n * d) + 2 * B * M * n1),
+                "mx_quantize_dh": (0, B * M * n1 + 2 * mxb(M * n1)),
+                "fc2_wgrad": (2 * M * n * d, mxb(M * n) + mxb(M * d) + B * E * n * d),
+                "fc1_dgrad": (2 * M * n1 * d, mxb(M * n1) + mxb(E_ne * d * n1) + B * M * d),
+                "fc1_wgrad": (2 * M * d * n1, mxb(M * d) + mxb(M * n1) + B * E * d * n1),
+            })
+        return work
     return {
         "fc1_act": (2 * M * d * n1, B * (M * d + E_ne * d * n1 + M * n + M * n1)),
         "fc2": (2 * M * n * d, B * (M * n + E_ne * n * d + M * d)),
@@ -95,7 +116,7 @@ def load_peaks():
 
 def kernel_src_hash():
     h = hashlib.sha256()
-    for f in ("gemm.cu", "gemm.cuh", "ptx.cuh", "act.cuh"):
+    for f in ("gemm.cu", "gemm.cuh", "ptx.cuh", "act.cuh", "mx.cu", "mx.cuh", "mxgemm.cuh"):
         h.update(open(os.path.join(ROOT, "dropless_grouped_gemm_gb300", "csrc", f), "rb").read())
     return h.hexdigest()[:16]
 
@@ -200,8 +221,6 @@ def make_inputs(w, dev):
         o["dprobs"] = torch.empty((w.T, w.k), dtype=torch.float32, device=dev)
         o["ws"] = torch.empty(max(16, M.route_workspace_size(w.T, w.k, E)), dtype=torch.uint8,
                               device=dev)
-        if w.mxfp8:
-            o["mx"] = M.mx_buffers(E, n, d, Mc, dev)
         o["route"] = {
             "counts": torch.empty(E, dtype=torch.int32, device=dev),
             "offsets": torch.empty(E + 1, dtype=torch.int32, device=dev),
@@ -210,6 +229,16 @@ def make_inputs(w, dev):
             "true_total": torch.empty(1, dtype=torch.int32, device=dev),
             "err": o["err"],
         }
+    if w.mxfp8:
+        o["mx"] = M.mx_buffers(E, n, d, Mc, dev)
+        if w.backward:
+            u8 = torch.uint8
+            o["mxb"] = {"w2_q": torch.empty((E, n, d), dtype=u8, device=dev),
+                        "w2_s": torch.empty(E * n * d // 32, dtype=u8, device=dev),
+                        "w1_q": torch.empty((E, d, n1), dtype=u8, device=dev),
+                        "w1_s": torch.empty(E * d * n1 // 32, dtype=u8, device=dev),
+                        "ws": torch.empty(M.mx_bwd_workspace_size(Mc, d, n, w.act), dtype=u8,
+                                          device=dev)}
     return inp, o
 
 
@@ -217,6 +246,30 @@ def make_step(w, inp, o):
     """One pass of the path; returns the number of libmoe kernel launches."""
     import dropless_grouped_gemm_gb300 as M
     act = w.act
+
+    def mx_backward(x_perm, dy_perm, offsets):
+        """MXFP8 backward: weights quantised along their data-gradient
+        reduction index, then the eight launches of grouped_mlp_bwd_mx."""
+        mx, mb = o["mx"], o["mxb"]
+        M.mx_quantize_weights_rowwise(inp["W2"], mb["w2_q"], mb["w2_s"])
+        M.mx_quantize_weights_rowwise(inp["W1"], mb["w1_q"], mb["w1_s"])
+        ops = dict(a_qT=mx["a_qT"], a_sT=mx["a_sT"], w2_q=mb["w2_q"], w2_s=mb["w2_s"],
+                   w1_q=mb["w1_q"], w1_s=mb["w1_s"])
+        M.grouped_mlp_bwd_mx(x_perm, o["h"], dy_perm, offsets, ops, act, dh=o["dh"],
+                             dx_perm=o["dx_perm"], dW1=o["dW1"], dW2=o["dW2"], err=o["err"],
+                             workspace=mb["ws"])
+        return 2 + M.last_launch_count()
+
+    if w.routing == "identity" and w.mxfp8:
+        def step_mx_id():
+            M.mx_quantize_weights(inp["W2"], o["mx"]["w2_q"], o["mx"]["w2_s"])
+            n = M.last_launch_count()
+            M.grouped_mlp_fwd(inp["x_perm"], inp["offsets"], inp["W1"], inp["W2"], act,
+                              save_h=True, h_saved=o["h"], a=o["a"], y_perm=o["y_perm"],
+                              err=o["err"], mx=o["mx"])
+            n += M.last_launch_count()
+            return n + mx_backward(inp["x_perm"], inp["dy_perm"], inp["offsets"])
+        return step_mx_id
 
     if w.routing == "identity":
         def step():
@@ -231,6 +284,34 @@ def make_step(w, inp, o):
         return step
 
     T, k = w.T, w.k
+
+    if w.mxfp8 and w.backward:
+        def step_mx_train():
+            n = 0
+            r = M.route_offsets(inp["topk_idx"], w.E, w.align, w.M_cap, out=o["route"],
+                                workspace=o["ws"])
+            n += M.last_launch_count()
+            M.permute(inp["x"], r["pair_of_row"], k, out=o["x_perm"])
+            n += M.last_launch_count()
+            M.mx_quantize_weights(inp["W2"], o["mx"]["w2_q"], o["mx"]["w2_s"])
+            n += M.last_launch_count()
+            M.grouped_mlp_fwd(o["x_perm"], r["offsets"], inp["W1"], inp["W2"], act, save_h=True,
+                              h_saved=o["h"], a=o["a"], y_perm=o["y_perm"], err=o["err"],
+                              mx=o["mx"])
+            n += M.last_launch_count()
+            M.unpermute(o["y_perm"], r["row_of_pair"], T, k, probs=inp["probs"], out=o["out"])
+            n += M.last_launch_count()
+            M.permute(inp["dO"], r["pair_of_row"], k, scale=inp["probs"].view(-1),
+                      out=o["dy_perm"])
+            n += M.last_launch_count()
+            M.unpermute(o["y_perm"], r["row_of_pair"], T, k, dO=inp["dO"], dprobs=o["dprobs"],
+                        combine=False)
+            n += M.last_launch_count()
+            n += mx_backward(o["x_perm"], o["dy_perm"], r["offsets"])
+            M.unpermute(o["dx_perm"], r["row_of_pair"], T, k, out=o["dx"])
+            n += M.last_launch_count()
+            return n
+        return step_mx_train
 
     if w.mxfp8:
         def step_mx():
@@ -279,6 +360,11 @@ def make_step(w, inp, o):
 
 
 def event_names(w):
+    if w.mxfp8 and w.backward:
+        if w.routing == "identity":
+            return ["mx_quantize_weights"] + KERNELS_FWD + KERNELS_MX_BWD
+        return (["route", "permute", "mx_quantize_weights"] + KERNELS_FWD +
+                ["combine", "permute_bwd", "router_grad"] + KERNELS_MX_BWD + ["unpermute_bwd"])
     if w.routing == "identity":
         return KERNELS_FWD + KERNELS_BWD
     if w.mxfp8:
@@ -304,14 +390,18 @@ def oracle_sample(w, rows):
 
 
 def oracle_step(w, x, dy, W1, W2, off):
-    """One oracle pass over the sample: fwd+bwd, or for the MXFP8 workload
-    the forward with the MX quantiser and the MXFP8 FC2."""
+    """One oracle pass over the sample: fwd+bwd; for the MXFP8 workloads the
+    forward with the MX quantiser and the MXFP8 FC2 (and, when training, the
+    MXFP8 backward)."""
     import oracle as O
+    from oracle import mx as OX
     H, A, _ = O.grouped_mlp_fwd(x, off, W1, W2, w.act)
     if w.mxfp8:
         qa, sa = O.mx_quantize_rows(A)
         qw, sw = O.mx_quantize_weights(W2)
         O.mx_fc2(qa, sa, qw, sw, off)
+        if w.backward:
+            OX.mx_grouped_mlp_bwd(x, H, A, dy, off, W1, W2, w.act)
     else:
         O.grouped_mlp_bwd(x, H, A, dy, off, W1, W2, w.act)
 
@@ -385,7 +475,8 @@ def run_reference(args, w):
     fwd, bwd = useful_flops(w, rows)
     v = (fwd + bwd) / dt / 1e12
     sample = (f"{rows} rows of expert 0 ({w.d}x{w.n1} W1, {w.n}x{w.d} W2), oracle float64 "
-              f"{'fwd (MXFP8 FC2)' if w.mxfp8 else 'fwd+bwd'} per step")
+              f"{'fwd (MXFP8 FC2)' if w.mxfp8 and not w.backward else 'fwd+bwd'}"
+              f"{' MXFP8' if w.mxfp8 and w.backward else ''} per step")
     line = {"impl": "reference", "metric": METRIC, "value": v, "unit": "TFLOP/s",
             "n_gpus": ws, "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
@@ -501,7 +592,7 @@ def main():
     dom = max(gemms, key=lambda nm: kern[nm]["ms"])
     fl, by = work[dom]
     t_dom = kern[dom]["ms"] * 1e-3
-    fp8 = w.mxfp8 and dom == "fc2"
+    fp8 = w.mxfp8 and (dom == "fc2" or (w.backward and dom in KERNELS_BWD))
     tpeak = peaks["bf16_tflops_sustained"] * (2.0 if fp8 else 1.0)   # dense fp8 = 2x bf16 (nominal ratio)
     tensor_time = fl / (tpeak * 1e12)
     hbm_time = by / (peaks["hbm_gbs"] * 1e9)
@@ -531,21 +622,20 @@ def main():
         v, dt = time_oracle(w, args.cpu_rows)
         cpu = {"value": v, "unit": "TFLOP/s", "cores": cpu_cores(), "kind": "oracle",
                "sample": f"{args.cpu_rows} rows of expert 0, float64 "
-                         f"{'fwd (MXFP8 FC2)' if w.mxfp8 else 'fwd+bwd'} ({dt:.1f} s)"}
+                         f"{'fwd (MXFP8 FC2)' if w.mxfp8 and not w.backward else 'fwd+bwd'}"
+                         f"{' MXFP8' if w.mxfp8 and w.backward else ''} ({dt:.1f} s)"}
 
     if rank == 0:
         line = {
             "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": ws,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 4),
-            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "e4m3/e8m0 block-scaled (FC1 bf16)" if w.mxfp8 else "bf16",
             "data": "synthetic",
             "pct_of_bf16_peak": round(100 * per_rank_tf / peaks["bf16_tflops"], 2),
             "config": {"workload": w.name, "E": w.E, "T": w.T, "top_k": w.k, "d": w.d, "n": w.n,
                        "act": w.act, "rows": Mrows, "nonempty_experts": inp["E_ne"],
-                       "step": ("grouped_mlp_fwd + grouped_mlp_bwd" if w.routing == "identity"
-                                else ("route + permute + W2 MXFP8 quantise + fwd (FC1 + MX epilogue, "
-                                      "block-scaled FC2) + combine") if w.mxfp8
-                                else "route + permute + fwd + combine + bwd (+ router grad)"),
+                       "step": step_description(w),
                        "l2": "inputs larger than L2 (no flush)", "parallelism": "replicas"},
             "roofline": roof, "kernels": kern, "graph": graph, "cpu_baseline": cpu, "e2e": e2e,
             "clocks": clocks, "gpu_launches": launches,
@@ -556,6 +646,21 @@ def main():
         import torch.distributed as dist
         dist.destroy_process_group()
     return 0
+
+
+def step_description(w):
+    if w.mxfp8 and w.backward:
+        core = ("W2 MXFP8 quantise + fwd (FC1 + MX epilogue, block-scaled FC2) + weight "
+                "quantise + MXFP8 bwd (grouped_mlp_bwd_mx)")
+        return core if w.routing == "identity" else (
+            "route + permute + " + core.replace(" + weight", " + combine + weight") +
+            " (+ router grad)")
+    if w.routing == "identity":
+        return "grouped_mlp_fwd + grouped_mlp_bwd"
+    if w.mxfp8:
+        return ("route + permute + W2 MXFP8 quantise + fwd (FC1 + MX epilogue, block-scaled FC2) "
+                "+ combine")
+    return "route + permute + fwd + combine + bwd (+ router grad)"
 
 
 def time_graph(step, steps, ws, flops):
@@ -597,7 +702,7 @@ def run_e2e(w, inp, o, step, steps, ws, flops):
     if w.routing == "identity":
         names_in = ["x_perm", "dy_perm", "offsets"]
         out_name = "dx_perm"
-    elif w.mxfp8:
+    elif w.mxfp8 and not w.backward:
         names_in = ["x", "topk_idx", "probs"]
         out_name = "out"
     else:

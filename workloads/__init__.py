@@ -282,6 +282,12 @@ WORKLOADS = {
                  "srelu", True, "identity"),
         Workload("zipf_t4096_d7168_e256_top8_n2048_mxfp8", 4, 4096, 7168, 256, 8, 2048,
                  "swiglu", False, "logits", zipf_s=1.2, align=32, mxfp8=True),
+        # MXFP8 training: the forward above plus the MXFP8 backward
+        Workload("zipf_t4096_d7168_e256_top8_n2048_mxfp8_train", 4, 4096, 7168, 256, 8, 2048,
+                 "swiglu", True, "logits", zipf_s=1.2, align=32, mxfp8=True),
+        Workload("balanced_e8_m4096_k8192_n4096_mxfp8_train", 1, 8 * 4096, 8192, 8, 1, 2048,
+                 "swiglu", True, "identity", mxfp8=True,
+                 notes="same tensors as the balanced bf16 layer; MXFP8 forward and backward"),
     ]
 }
 
