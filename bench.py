@@ -114,22 +114,36 @@ def load_peaks():
             "source": "fallback"}
 
 
-def kernel_src_hash():
+# source files of each kernel family; a traffic figure is reported only while
+# the files of the kernel it was measured on are unchanged
+KERNEL_SOURCES = {
+    "bf16": ("gemm.cu", "gemm.cuh", "ptx.cuh", "act.cuh", "mx.cuh"),
+    "mx": ("mx.cu", "mx.cuh", "mxgemm.cuh", "ptx.cuh", "act.cuh"),
+}
+
+
+def kernel_family(w, kernel):
+    """The block-scaled GEMMs of the MXFP8 workloads live in mx.cu; FC1 (and
+    every GEMM of the bf16 workloads) in gemm.cu."""
+    return "mx" if (w.mxfp8 and kernel != "fc1_act") else "bf16"
+
+
+def kernel_src_hash(family="bf16"):
     h = hashlib.sha256()
-    for f in ("gemm.cu", "gemm.cuh", "ptx.cuh", "act.cuh", "mx.cu", "mx.cuh", "mxgemm.cuh"):
+    for f in KERNEL_SOURCES[family]:
         h.update(open(os.path.join(ROOT, "dropless_grouped_gemm_gb300", "csrc", f), "rb").read())
     return h.hexdigest()[:16]
 
 
-def ncu_traffic(kernel, workload):
+def ncu_traffic(kernel, w):
     """DRAM bytes per launch from a committed ncu summary, if it was taken
-    on the current kernel source; else None."""
+    on the current source of that kernel's family; else None."""
     p = os.path.join(ROOT, "profiles", "ncu_traffic.json")
     if not os.path.exists(p):
         return None
     j = json.load(open(p))
-    rec = j.get(workload, {}).get(kernel)
-    if not rec or rec.get("src_hash") != kernel_src_hash():
+    rec = j.get(w.name, {}).get(kernel)
+    if not rec or rec.get("src_hash") != kernel_src_hash(kernel_family(w, kernel)):
         return None
     return rec.get("dram_bytes_per_launch")
 
@@ -608,7 +622,7 @@ def main():
         algo = by
     roof["frac"] = round(roof["achieved"] / roof["peak"], 4)
     roof["algorithmic_per_launch"] = algo
-    roof["traffic"] = ncu_traffic(dom, w.name)
+    roof["traffic"] = ncu_traffic(dom, w)
 
     # the same step captured once as a CUDA graph and replayed (the pages'
     # benchmark times graph replays); the whole path is capturable

@@ -237,29 +237,41 @@ __global__ void __launch_bounds__(256)
 }
 
 // ---------------------------------------------------------------- block-scaled GEMM
-constexpr int QBM = 128, QBN = 128, QBK = 128;  // QBK: FP8 elements (= bytes) of K
+// Output tiles are 128 x 256, computed as two 128 x 128 block-scaled MMAs per
+// 32-element step of K (each half with its own B scale chunk).  A pipeline
+// stage holds one 128-byte swizzle atom of K (128 FP8 elements) of A and of
+// both B halves plus their three scale chunks: 48 KB of operands for 8.4
+// MFLOP, the same bytes-per-FLOP as the bf16 kernel's 128 x 256 x 64 stage
+// at twice the tensor rate.
+constexpr int QBM = 128, QBN = 256, QHN = 128;   // tile rows, tile columns, MMA N
+constexpr int QBK = 128;                          // FP8 elements (= bytes) of K per stage
 constexpr int QA_BYTES = QBM * QBK;               // 16 KB
-constexpr int QB_BYTES = QBN * QBK;               // 16 KB
-constexpr int QSTAGE_BYTES = QA_BYTES + QB_BYTES + 1024;  // + SFA, SFB chunks
-constexpr int QTHREADS = 192;
-constexpr int QEPI_WARPS = 4;
+constexpr int QBH_BYTES = QHN * QBK;              // 16 KB per B half
+constexpr int QSF_OFF = QA_BYTES + 2 * QBH_BYTES; // scale chunks: SFA, SFB half 0, SFB half 1
+constexpr int QSTAGE_BYTES = QSF_OFF + 2048;      // 50 KB (stages stay 1024-byte aligned)
+constexpr int QTHREADS = 320;
+constexpr int QEPI_WARPS = 8;
 constexpr int QTMEM_COLS = 512;
-constexpr int QSF_TMEM = 2 * QBN;                 // scale columns after the accumulators
+constexpr int QSF_TMEM = QBN;                     // scale columns after the accumulator
+constexpr int QSF_COLS = 12;                      // a stage's three chunks, 4 columns each
 constexpr int QBOX_BYTES = 32 * 64 * 2;           // staged output box: 32 rows x 64 bf16
 
-// The weight gradient stages its output for TMA stores (two boxes per
-// epilogue warp, 128-byte swizzle, plus one box of zeros for experts with
-// no rows) and so keeps four stages; the other kinds keep six.
+// TMEM holds one 256-column accumulator (the scale columns leave no room
+// for a second); the epilogue moves it to registers and releases it at once,
+// so the next tile's MMAs overlap the conversion and stores.  The weight
+// gradient stages its output for TMA stores (one box per epilogue warp plus
+// a box of zeros for experts with no rows) and keeps three stages; the other
+// kinds keep four.
 template <MxKind KIND>
 struct QCfg {
   static constexpr bool W = (KIND == MxKind::kWgrad);
-  static constexpr int stages = W ? 4 : 6;
-  static constexpr int stg_bytes = W ? (2 * QEPI_WARPS + 1) * QBOX_BYTES : 0;
+  static constexpr int stages = W ? 3 : 4;
+  static constexpr int stg_bytes = W ? (QEPI_WARPS + 1) * QBOX_BYTES : 0;
 };
 template <MxKind KIND>
 constexpr size_t mx_smem_bytes(int E) {
   return 1024 + static_cast<size_t>(QCfg<KIND>::stages) * QSTAGE_BYTES + QCfg<KIND>::stg_bytes +
-         (2 * QCfg<KIND>::stages + 5) * 8 + 16 + 2 * (E + 1) * 4;
+         (2 * QCfg<KIND>::stages + 4) * 8 + 16 + 2 * (E + 1) * 4;
 }
 
 // Instruction descriptor, kind::mxf8f6f4 block-scaled: A/B E4M3 (format 0),
@@ -312,7 +324,8 @@ struct QTile {
   int row0, rows;   // ragged-row kinds: first global row, valid rows
   int m0;           // kWgrad: first output row within the expert
   int n0;           // first accumulator column
-  int kblocks;      // 128-element reduction steps
+  int nh;           // 128-column halves of the tile inside N (1 or 2)
+  int kblocks;      // QBK-element reduction steps
   int k0;           // kWgrad: first reduction row (global)
   int klast;        // kWgrad: valid rows of the last step (a multiple of 32)
 };
@@ -320,7 +333,7 @@ struct QTile {
 template <MxKind KIND>
 __device__ __forceinline__ int mx_tiles_of_expert(const MxGemmArgs& g, const int* s_off, int e) {
   const int mt = (KIND == MxKind::kWgrad) ? g.R / QBM : (s_off[e + 1] - s_off[e] + QBM - 1) / QBM;
-  return mt * (g.N / QBN);
+  return mt * ((g.N + QBN - 1) / QBN);
 }
 
 template <MxKind KIND>
@@ -332,12 +345,13 @@ __device__ __forceinline__ QTile mx_decode(const MxGemmArgs& g, const int* s_off
     if (s_ts[mid + 1] <= t) lo = mid + 1;
     else hi = mid;
   }
-  const int nt = g.N / QBN;
+  const int nt = (g.N + QBN - 1) / QBN;
   const int local = t - s_ts[lo];
   const int mi = local / nt;
   QTile tl;
   tl.e = lo;
   tl.n0 = (local - mi * nt) * QBN;
+  tl.nh = min(2, (g.N - tl.n0) / QHN);
   if constexpr (KIND == MxKind::kWgrad) {
     tl.m0 = mi * QBM;
     tl.k0 = s_off[lo];
@@ -409,26 +423,27 @@ __device__ __forceinline__ void mx_dact_row32(const MxGemmArgs& g, long long gro
 
 // Persistent warp-specialised block-scaled grouped GEMM: warp 0 TMA producer
 // (operand tiles by tensor maps, scale chunks by bulk copies), warp 1 TMEM
-// owner and MMA issuer (128 x 128 x 32 tcgen05.mma ... block_scale; the
-// scale chunks of a stage go to TMEM with tcgen05.cp), warps 2-5 epilogue.
+// owner and MMA issuer (tcgen05.mma ... block_scale; the scale chunks of a
+// stage go to TMEM with tcgen05.cp), warps 2-9 epilogue in two warpgroups,
+// one per 128-column half of the tile.
 template <MxKind KIND, int ACT>
 __global__ void __launch_bounds__(QTHREADS, 1)
     mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmC, const MxGemmArgs g) {
   constexpr bool W = (KIND == MxKind::kWgrad);
   constexpr bool B_MN = (KIND == MxKind::kFc2);
-  constexpr uint32_t IDESC = idesc_mx(QBM, QBN, false, B_MN);
+  constexpr uint32_t IDESC = idesc_mx(QBM, QHN, false, B_MN);
   constexpr int NST = QCfg<KIND>::stages;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
-  uint8_t* staging = smem + NST * QSTAGE_BYTES;               // 2 boxes per epilogue warp
-  uint8_t* zero_box = staging + 2 * QEPI_WARPS * QBOX_BYTES;
+  uint8_t* staging = smem + NST * QSTAGE_BYTES;               // one box per epilogue warp
+  uint8_t* zero_box = staging + QEPI_WARPS * QBOX_BYTES;
   uint64_t* full_bar = reinterpret_cast<uint64_t*>(staging + QCfg<KIND>::stg_bytes);
   uint64_t* empty_bar = full_bar + NST;
   uint64_t* tfull_bar = empty_bar + NST;
-  uint64_t* tempty_bar = tfull_bar + 2;
-  uint64_t* drain_bar = tempty_bar + 2;
+  uint64_t* tempty_bar = tfull_bar + 1;
+  uint64_t* drain_bar = tempty_bar + 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain_bar + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   int* s_off = reinterpret_cast<int*>(tmem_slot + 4);
@@ -440,10 +455,8 @@ __global__ void __launch_bounds__(QTHREADS, 1)
       mbar_init(&full_bar[i], 1);
       mbar_init(&empty_bar[i], 1);
     }
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(&tfull_bar[i], 1);
-      mbar_init(&tempty_bar[i], QEPI_WARPS);
-    }
+    mbar_init(tfull_bar, 1);
+    mbar_init(tempty_bar, QEPI_WARPS);
     mbar_init(drain_bar, 1);
     *abort_flag = 0;
     fence_mbar_init();
@@ -505,36 +518,43 @@ __global__ void __launch_bounds__(QTHREADS, 1)
       uint32_t ipar[NST];
       for (int i = 0; i < NST; ++i) { issued[i] = false; ipar[i] = 0; }
       bool ok = true;
-      const long long kc_n = g.K / QBK, nt = g.N / QBN, rt = g.R / QBM;
+      const long long kc_n = g.K / QBK, nq = g.N / QHN, rq = g.R / QBM;
       for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
         const QTile tl = mx_decode<KIND>(g, s_off, s_ts, t);
         for (int kb = 0; kb < tl.kblocks; ++kb) {
           if (!mbar_wait(&empty_bar[stage], phase ^ 1, abort_flag)) { ok = false; break; }
           uint8_t* sa = smem + stage * QSTAGE_BYTES;
           uint8_t* sb = sa + QA_BYTES;
-          uint8_t* ssf = sb + QB_BYTES;
+          uint8_t* ssf = sa + QSF_OFF;
           uint64_t* fb = &full_bar[stage];
-          mbar_arrive_expect_tx(fb, QSTAGE_BYTES);
-          long long ca, cb;  // scale chunks of A and B
+          mbar_arrive_expect_tx(fb, QA_BYTES + 512 + tl.nh * (QBH_BYTES + 512));
+          long long ca, cb0, cstep;  // scale chunks: A, B half 0, B half 1 - half 0
           if constexpr (W) {
             const int kc = tl.k0 + kb * QBK;
             tma_load_2d(sa, &tmA, fb, kc, tl.m0);
-            tma_load_2d(sb, &tmB, fb, kc, tl.n0);
-            ca = static_cast<long long>(kc / 32) * rt + tl.m0 / QBM;
-            cb = static_cast<long long>(kc / 32) * nt + tl.n0 / QBN;
+            for (int h = 0; h < tl.nh; ++h)
+              tma_load_2d(sb + h * QBH_BYTES, &tmB, fb, kc, tl.n0 + h * QHN);
+            ca = static_cast<long long>(kc / 32) * rq + tl.m0 / QBM;
+            cb0 = static_cast<long long>(kc / 32) * nq + tl.n0 / QHN;
+            cstep = 1;
           } else {
             tma_load_2d(sa, &tmA, fb, kb * QBK, tl.row0);
             ca = static_cast<long long>(tl.row0 / 32) * kc_n + kb;
             if constexpr (B_MN) {
-              tma_load_3d(sb, &tmB, fb, tl.n0, kb * QBK, tl.e);
-              cb = (static_cast<long long>(tl.e) * kc_n + kb) * nt + tl.n0 / QBN;
+              for (int h = 0; h < tl.nh; ++h)
+                tma_load_3d(sb + h * QBH_BYTES, &tmB, fb, tl.n0 + h * QHN, kb * QBK, tl.e);
+              cb0 = (static_cast<long long>(tl.e) * kc_n + kb) * nq + tl.n0 / QHN;
+              cstep = 1;
             } else {
-              tma_load_2d(sb, &tmB, fb, kb * QBK, tl.e * g.N + tl.n0);
-              cb = ((static_cast<long long>(tl.e) * g.N + tl.n0) / QBN) * kc_n + kb;
+              for (int h = 0; h < tl.nh; ++h)
+                tma_load_2d(sb + h * QBH_BYTES, &tmB, fb, kb * QBK, tl.e * g.N + tl.n0 + h * QHN);
+              cb0 = ((static_cast<long long>(tl.e) * g.N + tl.n0) / QHN) * kc_n + kb;
+              cstep = kc_n;
             }
           }
           bulk_load(ssf, g.a_s + ca * 512, 512, fb);
-          bulk_load(ssf + 512, g.b_s + cb * 512, 512, fb);
+          for (int h = 0; h < tl.nh; ++h)
+            bulk_load(ssf + 512 * (1 + h), g.b_s + (cb0 + h * cstep) * 512, 512, fb);
           issued[stage] = true;
           ipar[stage] = phase;
           if (++stage == NST) { stage = 0; phase ^= 1; }
@@ -557,13 +577,11 @@ __global__ void __launch_bounds__(QTHREADS, 1)
     bool ok = true;
     for (int t = blockIdx.x; t < total && ok; t += gridDim.x, ++local) {
       const QTile tl = mx_decode<KIND>(g, s_off, s_ts, t);
-      const int buf = local & 1;
-      const uint32_t aph = (local >> 1) & 1;
-      if (lane == 0) ok = mbar_wait(&tempty_bar[buf], aph ^ 1, abort_flag);
+      // the accumulator is free once the epilogue has read the previous tile
+      if (lane == 0) ok = mbar_wait(tempty_bar, (local & 1) ^ 1, abort_flag);
       ok = __shfl_sync(0xffffffffu, ok, 0);
       if (!ok) break;
       tc_fence_after();
-      const uint32_t d_tmem = tmem_base + buf * QBN;
       for (int kb = 0; kb < tl.kblocks; ++kb) {
         if (lane == 0) ok = mbar_wait(&full_bar[stage], phase, abort_flag);
         ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -572,21 +590,25 @@ __global__ void __launch_bounds__(QTHREADS, 1)
         if (lane == 0) {
           uint8_t* sa = smem + stage * QSTAGE_BYTES;
           uint8_t* sb = sa + QA_BYTES;
-          uint8_t* ssf = sb + QB_BYTES;
-          const uint32_t sfa_t = tmem_base + QSF_TMEM + stage * 8;
-          const uint32_t sfb_t = sfa_t + 4;
-          tmem_cp_sf(sfa_t, sdesc_sf(smem_u32(ssf)));
-          tmem_cp_sf(sfb_t, sdesc_sf(smem_u32(ssf + 512)));
+          uint8_t* ssf = sa + QSF_OFF;
+          const uint32_t sf_t = tmem_base + QSF_TMEM + stage * QSF_COLS;
+          tmem_cp_sf(sf_t, sdesc_sf(smem_u32(ssf)));
+          for (int h = 0; h < tl.nh; ++h)
+            tmem_cp_sf(sf_t + 4 * (1 + h), sdesc_sf(smem_u32(ssf + 512 * (1 + h))));
           const uint32_t a0 = smem_u32(sa), b0 = smem_u32(sb);
           // an expert's last reduction step of a weight gradient holds
           // klast (a multiple of 32) of its rows: one MMA per 32 of them
           const int kk_n = (W && kb == tl.kblocks - 1) ? tl.klast / 32 : QBK / 32;
           for (int kk = 0; kk < kk_n; ++kk) {
             const uint64_t ad = sdesc_sw128(a0 + kk * 32, 16, 1024);
-            const uint64_t bd = B_MN ? sdesc_sw128(b0 + kk * 4096, QB_BYTES, 1024)
-                                     : sdesc_sw128(b0 + kk * 32, 16, 1024);
             const uint32_t id = IDESC | (static_cast<uint32_t>(kk) << 29) | (static_cast<uint32_t>(kk) << 4);
-            umma_mx(d_tmem, ad, bd, id, sfa_t, sfb_t, (kb > 0 || kk > 0) ? 1u : 0u);
+            for (int h = 0; h < tl.nh; ++h) {
+              const uint32_t bh = b0 + h * QBH_BYTES;
+              const uint64_t bd = B_MN ? sdesc_sw128(bh + kk * 4096, QBH_BYTES, 1024)
+                                       : sdesc_sw128(bh + kk * 32, 16, 1024);
+              umma_mx(tmem_base + h * QHN, ad, bd, id, sf_t, sf_t + 4 * (1 + h),
+                      (kb > 0 || kk > 0) ? 1u : 0u);
+            }
           }
           umma_commit(&empty_bar[stage]);
         }
@@ -594,7 +616,7 @@ __global__ void __launch_bounds__(QTHREADS, 1)
         if (++stage == NST) { stage = 0; phase ^= 1; }
       }
       if (!ok) break;
-      if (lane == 0) umma_commit(&tfull_bar[buf]);
+      if (lane == 0) umma_commit(tfull_bar);
       __syncwarp();
     }
     if (!ok && lane == 0) {
@@ -606,81 +628,78 @@ __global__ void __launch_bounds__(QTHREADS, 1)
     __syncwarp();
   } else {
     // ---------------------------------------------------------- epilogue
-    const int q = warp & 3;
+    const int q = warp & 3;              // TMEM lane quadrant
+    const int wg = (warp - 2) >> 2;      // 128-column half of the tile
     const int r = q * 32 + lane;
-    uint8_t* my_stg = staging + (warp - 2) * 2 * QBOX_BYTES;
-    uint32_t slot = 0;
+    uint8_t* my_box = staging + (warp - 2) * QBOX_BYTES;
     int local = 0;
     for (int t = blockIdx.x; t < total; t += gridDim.x, ++local) {
       const QTile tl = mx_decode<KIND>(g, s_off, s_ts, t);
-      const int buf = local & 1;
-      const uint32_t aph = (local >> 1) & 1;
       bool ok = true;
-      if (lane == 0) ok = mbar_wait(&tfull_bar[buf], aph, abort_flag);
+      if (lane == 0) ok = mbar_wait(tfull_bar, local & 1, abort_flag);
       if (!__shfl_sync(0xffffffffu, ok, 0)) break;
       tc_fence_after();
-      const uint32_t tb = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + buf * QBN;
+      const bool mine = wg < tl.nh;
+      const bool zero = W && tl.kblocks == 0;
+      uint32_t v[4][32];
+      if (mine && !zero) {
+        const uint32_t tb = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + wg * QHN;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) tmem_ld32(tb + c * 32, v[c]);
+        tmem_wait_ld();
+      }
+      // release the accumulator: the next tile's MMAs may start
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(tempty_bar);
+      if (!mine) continue;
+      const int col0 = tl.n0 + wg * QHN;
       if constexpr (W) {
-        if (tl.kblocks == 0) {
+        if (zero) {
           // expert with no rows: its weight gradient is zero
           if (lane == 0) {
-            tma_store_3d(&tmC, zero_box, tl.n0, tl.m0 + q * 32, tl.e);
-            tma_store_3d(&tmC, zero_box, tl.n0 + 64, tl.m0 + q * 32, tl.e);
+            tma_store_3d(&tmC, zero_box, col0, tl.m0 + q * 32, tl.e);
+            tma_store_3d(&tmC, zero_box, col0 + 64, tl.m0 + q * 32, tl.e);
             bulk_commit();
           }
           __syncwarp();
         } else {
           // stage each 32-row x 64-column box (128-byte swizzle: 16-byte
           // chunk j of row r at j ^ (r % 8)) and write it with a TMA store
-#pragma unroll 1
+#pragma unroll
           for (int h = 0; h < 2; ++h) {
-            uint32_t v0[32], v1[32];
-            tmem_ld32(tb + h * 64, v0);
-            tmem_ld32(tb + h * 64 + 32, v1);
-            tmem_wait_ld();
-            uint8_t* box = my_stg + (slot & 1) * QBOX_BYTES;
-            if (lane == 0) bulk_wait_read_1();     // the box's previous store has read it
+            if (lane == 0) bulk_wait_read_0();     // the box's previous store has read it
             __syncwarp();
-            uint8_t* row = box + lane * 128;
+            uint8_t* row = my_box + lane * 128;
             const int sw = lane & 7;
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
+            for (int j = 0; j < 8; ++j) {
+              const uint32_t (&src)[32] = v[2 * h + (j >> 2)];
+              const int b = 8 * (j & 3);
               *reinterpret_cast<uint4*>(row + ((j ^ sw) * 16)) = make_uint4(
-                  pack_bf16x2(__uint_as_float(v0[8 * j + 0]), __uint_as_float(v0[8 * j + 1])),
-                  pack_bf16x2(__uint_as_float(v0[8 * j + 2]), __uint_as_float(v0[8 * j + 3])),
-                  pack_bf16x2(__uint_as_float(v0[8 * j + 4]), __uint_as_float(v0[8 * j + 5])),
-                  pack_bf16x2(__uint_as_float(v0[8 * j + 6]), __uint_as_float(v0[8 * j + 7])));
-              *reinterpret_cast<uint4*>(row + (((j + 4) ^ sw) * 16)) = make_uint4(
-                  pack_bf16x2(__uint_as_float(v1[8 * j + 0]), __uint_as_float(v1[8 * j + 1])),
-                  pack_bf16x2(__uint_as_float(v1[8 * j + 2]), __uint_as_float(v1[8 * j + 3])),
-                  pack_bf16x2(__uint_as_float(v1[8 * j + 4]), __uint_as_float(v1[8 * j + 5])),
-                  pack_bf16x2(__uint_as_float(v1[8 * j + 6]), __uint_as_float(v1[8 * j + 7])));
+                  pack_bf16x2(__uint_as_float(src[b + 0]), __uint_as_float(src[b + 1])),
+                  pack_bf16x2(__uint_as_float(src[b + 2]), __uint_as_float(src[b + 3])),
+                  pack_bf16x2(__uint_as_float(src[b + 4]), __uint_as_float(src[b + 5])),
+                  pack_bf16x2(__uint_as_float(src[b + 6]), __uint_as_float(src[b + 7])));
             }
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) {
-              tma_store_3d(&tmC, box, tl.n0 + h * 64, tl.m0 + q * 32, tl.e);
+              tma_store_3d(&tmC, my_box, col0 + h * 64, tl.m0 + q * 32, tl.e);
               bulk_commit();
             }
-            ++slot;
           }
         }
       } else {
-#pragma unroll 1
-        for (int c = 0; c < QBN / 32; ++c) {
-          uint32_t v[32];
-          tmem_ld32(tb + c * 32, v);
-          tmem_wait_ld();
-          if (r < tl.rows) {
-            const long long grow = tl.row0 + r;
-            if constexpr (KIND == MxKind::kDgradAct) mx_dact_row32<ACT>(g, grow, tl.n0 + c * 32, v);
-            else mx_store_row32(g.out + grow * g.ldo + tl.n0 + c * 32, v);
+        if (r < tl.rows) {
+          const long long grow = tl.row0 + r;
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            if constexpr (KIND == MxKind::kDgradAct) mx_dact_row32<ACT>(g, grow, col0 + c * 32, v[c]);
+            else mx_store_row32(g.out + grow * g.ldo + col0 + c * 32, v[c]);
           }
         }
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&tempty_bar[buf]);
     }
     if (W && lane == 0) bulk_wait_all();  // staged stores done before the CTA exits
     __syncwarp();
