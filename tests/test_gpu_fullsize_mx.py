@@ -1,0 +1,148 @@
+"""Full-size parity of the MXFP8 path (forward and backward) on the Zipf
+layer (T=4096, d=7168, E=256, top-8, n=2048, align 32), in the launch
+configuration bench.py times.
+
+The GPU runs one step of the bench's MXFP8 training workload.  The oracle
+(oracle.moe, oracle.mx) recomputes from the same seeded inputs:
+  * sampled rows of a hot expert, a small one and the smallest: A and the
+    block-scaled FC2 output Y; dH (block-scaled FC2-dgrad + dAct) and dX
+    (block-scaled FC1-dgrad);
+  * the whole MXFP8 weight gradients of a small expert (element-wise on the
+    columns whose quantised operand both sides derive from bit-identical
+    bf16 values, in aggregate on all), and zeros for experts with no rows.
+Rows of an expert include its pad rows (zeros) up to the 32-row boundary:
+the group-aware blocks of the weight gradients see them."""
+import numpy as np
+import pytest
+import torch
+
+import bench as BE
+import oracle as O
+from oracle import mx as X
+import workloads as WL
+from _helpers import assert_rms_close, f64
+
+pytestmark = [pytest.mark.gpu, pytest.mark.slow]
+
+WNAME = "zipf_t4096_d7168_e256_top8_n2048_mxfp8_train"
+
+
+def _expert_weights(w, e):
+    d, n = w.d, w.n
+    W1 = WL.w1_interleaved(w.cfg_id, 1, d, n, w.w_std, "cuda", experts=[e])[0]
+    W2 = WL.w2(w.cfg_id, 1, n, d, w.w_std, "cuda", experts=[e])[0]
+    return f64(W1), f64(W2)
+
+
+def _token_rows(cols, key, std, toks):
+    idx = (torch.as_tensor(toks, dtype=torch.int64)[:, None] * cols +
+           torch.arange(cols, dtype=torch.int64)[None, :]).cuda()
+    return f64(WL.normal_at(idx, key, std))
+
+
+def _expert_inputs(w, ro, probs, rows):
+    """x_perm and dy_perm rows (pad rows zero), from the generator."""
+    pairs = ro["pair_of_row"][rows]
+    real = pairs >= 0
+    x = np.zeros((len(rows), w.d))
+    dy = np.zeros((len(rows), w.d))
+    if real.any():
+        toks = pairs[real] // w.k
+        x[real] = _token_rows(w.d, (w.cfg_id, WL.X, 0), w.x_std, toks)
+        dO = _token_rows(w.d, (w.cfg_id, WL.DO, 0), w.dy_std, toks)
+        dy[real] = O.bf16_round(probs.reshape(-1)[pairs[real]].astype(np.float64)[:, None] * dO)
+    return x, dy
+
+
+@pytest.fixture(scope="module")
+def run():
+    import dropless_grouped_gemm_gb300 as M
+    M.lib()
+    w = WL.WORKLOADS[WNAME]
+    inp, o = BE.make_inputs(w, "cuda")
+    step = BE.make_step(w, inp, o)
+    step()
+    torch.cuda.synchronize()
+    assert int(o["err"].item()) == 0
+    idx, probs = WL.route_inputs(w)
+    ro = O.route_offsets(idx, w.E, w.align, w.M_cap)
+    yield w, o, ro, probs
+    del inp, o
+    torch.cuda.empty_cache()
+
+
+def test_mx_rows_forward_and_data_gradients(run):
+    w, o, ro, probs = run
+    counts, off = ro["counts"], ro["offsets"]
+    nonempty = [int(e) for e in np.argsort(counts) if counts[e] > 0]
+    rng = np.random.default_rng(11)
+    for e in [int(np.argmax(counts)), nonempty[len(nonempty) // 2], nonempty[0]]:
+        W1, W2 = _expert_weights(w, e)
+        rr = np.arange(off[e], off[e] + counts[e])          # real rows
+        rows = rr if len(rr) <= 6 else np.sort(rng.choice(rr, 6, replace=False))
+        x, dy = _expert_inputs(w, ro, probs, rows)
+        o1 = np.array([0, len(rows)])
+        H, A, _ = O.grouped_mlp_fwd(x, o1, W1[None], W2[None], w.act)
+        # forward: Y from row-wise MX A and W2 with blocks along n
+        qa, sa = X.mx_quantize_rows(A)
+        qw, sw = X.mx_quantize_weights(W2[None])
+        Y = X.mx_fc2(qa, sa, qw, sw, o1)
+        # backward data gradients: dY and W2 with blocks along d; dH and W1
+        # with blocks along n1
+        dyq, dys = X.mx_quantize_rows(dy)
+        w2q, w2s = X.mx_quantize_rows(W2)
+        dA = X.mx_dgrad(dyq, dys, w2q[None], w2s[None], o1)
+        dH = O.bf16_round(O.act_backward(H, dA, w.act))
+        dhq, dhs = X.mx_quantize_rows(dH)
+        w1q, w1s = X.mx_quantize_rows(W1)
+        dX = O.bf16_round(X.mx_dgrad(dhq, dhs, w1q[None], w1s[None], o1))
+        r = torch.as_tensor(rows).cuda()
+        assert_rms_close(f64(o["a"][r]), A, f"MX e{e} A")
+        assert_rms_close(f64(o["y_perm"][r]), Y, f"MX e{e} Y")
+        assert_rms_close(f64(o["dh"][r]), dH, f"MX e{e} dH")
+        assert_rms_close(f64(o["dx_perm"][r]), dX, f"MX e{e} dX")
+
+
+def _agree_cols(gpu, ref):
+    """Columns whose bf16 values agree bit for bit on every row."""
+    return np.where((O.bf16_bits(gpu) == O.bf16_bits(ref)).all(axis=0))[0]
+
+
+def test_mx_weight_gradients_small_expert_and_empty(run):
+    """Whole dW1/dW2 of a small expert.  Each side quantises the operands it
+    computed itself (A from its FC1, dH from its FC2-dgrad, dY from the
+    scaled permute); a one-step bf16
+    difference can flip an E4M3 code or a block scale, and with a few dozen
+    rows a flip shows in the sum.  So the element-wise tolerance applies on
+    the columns whose bf16 operand agrees bit for bit on both sides (the
+    quantisers then produce the same codes), and every entry must meet the
+    aggregate bound: relative Frobenius error <= 2e-2."""
+    w, o, ro, probs = run
+    counts, off = ro["counts"], ro["offsets"]
+    e = int([e for e in np.argsort(counts) if counts[e] > 40][0])   # two 32-row blocks or more
+    W1, W2 = _expert_weights(w, e)
+    rows = np.arange(off[e], off[e + 1])                 # padded to a multiple of 32
+    x, dy = _expert_inputs(w, ro, probs, rows)
+    o1 = np.array([0, len(rows)])
+    H, A, _ = O.grouped_mlp_fwd(x, o1, W1[None], W2[None], w.act)
+    ref = X.mx_grouped_mlp_bwd(x, H, A, dy, o1, W1[None], W2[None], w.act)
+    r = torch.as_tensor(rows).cuda()
+    got2, got1 = f64(o["dW2"][e]), f64(o["dW1"][e])
+    for name, got, want in (("dW2", got2, ref["dW2"][0]), ("dW1", got1, ref["dW1"][0])):
+        rel = np.linalg.norm(got - want) / np.linalg.norm(want)
+        assert rel <= 2e-2, (f"MX {name}[{e}] relative error", rel)
+    # dW2 = A^T dY: rows of dW2 follow A's columns, columns follow dY's (the
+    # scaled permute rounds an fp32 product, the oracle an exact one: they
+    # may differ by one step at a few elements)
+    ia = _agree_cols(f64(o["a"][r]), A)
+    jd = _agree_cols(f64(o["dy_perm"][r]), dy)
+    assert len(ia) >= A.shape[1] // 2 and len(jd) >= dy.shape[1] // 2, (len(ia), len(jd))
+    assert_rms_close(got2[np.ix_(ia, jd)], ref["dW2"][0][np.ix_(ia, jd)],
+                     f"MX dW2[{e}] on {len(ia)} x {len(jd)} agreeing rows x columns")
+    # dW1 = x^T dH: columns of dW1 follow dH's columns (x is the generator's on both sides)
+    jh = _agree_cols(f64(o["dh"][r]), ref["dH"][:len(rows)])
+    assert len(jh) >= ref["dH"].shape[1] // 2, len(jh)
+    assert_rms_close(got1[:, jh], ref["dW1"][0][:, jh], f"MX dW1[{e}] on {len(jh)} agreeing columns")
+    for e in [int(e) for e in range(w.E) if counts[e] == 0][:3]:
+        assert float(o["dW1"][e].abs().max()) == 0.0
+        assert float(o["dW2"][e].abs().max()) == 0.0
