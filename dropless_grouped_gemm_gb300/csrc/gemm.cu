@@ -114,8 +114,16 @@ __device__ __forceinline__ Tile decode_tile(const GemmArgs& g, const int* s_off,
     mi = 0;
     tl.n0 = (2 * local + rank) * BN;
   } else {
-    const int pm = local / nt;
-    tl.n0 = (local - pm * nt) * BN;
+    int pm, ni;
+    if (g.col_major) {
+      const int np = (row_blocks<KIND>(g, s_off, lo) + CL - 1) / CL;
+      ni = local / np;
+      pm = local - ni * np;
+    } else {
+      pm = local / nt;
+      ni = local - pm * nt;
+    }
+    tl.n0 = ni * BN;
     mi = CL * pm + rank;
     tl.mc = (CL == 2);
   }
@@ -709,8 +717,24 @@ bool wgrad_skinny(const GemmArgs& g) {
 }
 
 cudaError_t launch_grouped_gemm(GemmKind kind, int act, const CUtensorMap& ta,
-                                const CUtensorMap& tb, const CUtensorMap& tc, const GemmArgs& g,
+                                const CUtensorMap& tb, const CUtensorMap& tc, const GemmArgs& g_in,
                                 int num_sms, cudaStream_t s, bool mx) {
+  // Unit order: when an expert has no more row-pair units than column
+  // tiles, sweep column tiles outermost, so that a wave of clusters reuses
+  // each B column tile across the expert's row pairs while the A block stays
+  // in L2; otherwise row pairs outermost.  Measured on the balanced layer
+  // (E=8 x 4096 rows, d=8192, n=2048), column order against row order:
+  // FC1-dgrad -4.7%, FC2-wgrad -1.4%, FC1 -1.2%, FC2 +2.0%; FC1-wgrad (32
+  // row pairs, 16 column tiles) +1.6%, so it keeps row order.
+  GemmArgs g = g_in;
+  {
+    const long long rows = (kind == GemmKind::kWgrad)
+                               ? g.R
+                               : (static_cast<long long>(g.M_cap) + g.E - 1) / (g.E > 0 ? g.E : 1);
+    const long long units_m = ((rows + BM - 1) / BM + kCluster - 1) / kCluster;
+    const long long nt = (g.N + BN - 1) / BN;
+    g.col_major = units_m <= nt ? 1 : 0;
+  }
   if (mx) {
     if (kind != GemmKind::kFc1Act) return cudaErrorInvalidValue;
     switch (act) {

@@ -39,6 +39,10 @@ struct GemmArgs {
   uint8_t* mx_qT;          // [n, M_cap] codes of A^T (32x1 blocks) or NULL
   uint8_t* mx_sT;          // [n, M_cap/32] scales of mx_qT
   int n_a;                 // columns of A (n)
+  // unit order inside an expert, set by launch_grouped_gemm: 0 = row pairs
+  // outermost (a wave of CTAs sweeps every column tile of B), 1 = column
+  // tiles outermost (a wave reuses each B column tile across all row pairs)
+  int col_major;
 };
 
 // Launches the persistent grouped GEMM of `kind` (act: MOE_ACT_*) on `s`.
