@@ -19,7 +19,7 @@ __all__ = [
     "router_topk", "route_offsets", "permute", "unpermute", "router_grad",
     "interleave_gate_up", "split_gate_up",
     "act_forward", "act_backward", "phi", "dphi",
-    "grouped_mlp_fwd", "grouped_mlp_bwd",
+    "grouped_mlp_fwd", "grouped_mlp_bwd", "grouped_mlp_bwd_routed",
     "fc1_rows", "fc2_rows",
 ]
 
@@ -369,6 +369,57 @@ def grouped_mlp_bwd(x_perm, H, A, dY, offsets, W1, W2, act: str,
         dX[r0:r1] = _rb(dh @ W1[e].T, round_bf16)
         dW1[e] = x_perm[r0:r1].T @ dh
     return dH, dX, _rb(dW1, round_bf16), _rb(dW2, round_bf16)
+
+
+def grouped_mlp_bwd_routed(x_perm, H, dO_perm, row_prob, offsets, W1, W2, act: str,
+                           round_bf16: bool = True):
+    """Backward with the router gradient taken inside the expert MLP
+    ([Sonic] "역전파 계산 그래프 재작성하기": dS_{t,e} = <dO_t, Y_{e,t}> =
+    <dO_t W2_e^T, A_e>, so Y need not be kept; A is recomputed from H, and
+    the dH kernel's epilogue also emits dS and A' = S*A).
+
+    Inputs: dO_perm is the gathered, unscaled output gradient of each row;
+    row_prob the router probability of the row's (token, expert) pair (0
+    for pad rows).  Per expert e (rows R_e):
+      dA'  = dO_e W2_e^T                      (gradient w.r.t. the row's A,
+                                               before the probability)
+      dS   = <dA'_r, A_r> per row, A = act(H) from the stored H
+      dH   = act'(H; p_r dA'_r)
+      A'   = p_r A_r                          (rounded to bf16)
+      dW2_e = A'_e^T dO_e,  dX_e = dH_e W1_e^T,  dW1_e = X_e^T dH_e.
+    Returns dH, dX, dW1, dW2, A', dS (float64 [M], NaN outside every
+    expert)."""
+    x_perm = np.asarray(x_perm, dtype=np.float64)
+    H = np.asarray(H, dtype=np.float64)
+    dO = np.asarray(dO_perm, dtype=np.float64)
+    p = np.asarray(row_prob, dtype=np.float64)
+    W1 = np.asarray(W1, dtype=np.float64)
+    W2 = np.asarray(W2, dtype=np.float64)
+    M_cap = x_perm.shape[0]
+    E = len(offsets) - 1
+    n1, n = W1.shape[2], W2.shape[1]
+    dH = np.full((M_cap, n1), np.nan)
+    dX = np.full(x_perm.shape, np.nan)
+    Ap = np.full((M_cap, n), np.nan)
+    dS = np.full(M_cap, np.nan)
+    dW1 = np.zeros(W1.shape)
+    dW2 = np.zeros(W2.shape)
+    for e in range(E):
+        r0, r1 = int(offsets[e]), int(offsets[e + 1])
+        if r1 <= r0:
+            continue
+        pr = p[r0:r1, None]
+        dAp = dO[r0:r1] @ W2[e].T
+        A = act_forward(H[r0:r1], act)
+        dS[r0:r1] = (dAp * A).sum(axis=1)
+        dh = _rb(act_backward(H[r0:r1], pr * dAp, act), round_bf16)
+        dH[r0:r1] = dh
+        ap = _rb(pr * A, round_bf16)
+        Ap[r0:r1] = ap
+        dW2[e] = ap.T @ dO[r0:r1]
+        dX[r0:r1] = _rb(dh @ W1[e].T, round_bf16)
+        dW1[e] = x_perm[r0:r1].T @ dh
+    return dH, dX, _rb(dW1, round_bf16), _rb(dW2, round_bf16), Ap, dS
 
 
 # sampled-row helpers for full-size parity checks (same arithmetic as above,

@@ -184,3 +184,69 @@ def test_rounding_points():
         assert (O.bf16_round(t) == t).all()
     Hr, Ar, _ = O.grouped_mlp_fwd(x, off, W1, W2, "swiglu", round_bf16=False)
     assert (A == O.bf16_round(Ar)).all()
+
+
+def _routed_case(act, seed=50):
+    rng = np.random.default_rng(seed)
+    E, d, n = 3, 16, 8
+    n1 = n if act == "srelu" else 2 * n
+    off = np.array([0, 5, 5, 12])
+    M = 14                                          # two rows past every expert
+    x = rng.standard_normal((M, d))
+    H = rng.standard_normal((M, n1))
+    dO = rng.standard_normal((M, d))
+    p = rng.random(M)
+    W1 = rng.standard_normal((E, d, n1)) * 0.3
+    W2 = rng.standard_normal((E, n, d)) * 0.3
+    return x, H, dO, p, off, W1, W2
+
+
+@pytest.mark.parametrize("act", ["swiglu", "geglu", "srelu"])
+def test_routed_backward_equals_scaled_backward(act):
+    """With dY = p * dO the routed backward ([Sonic] rewrite) gives the same
+    dH, dX, dW1 and dW2 as the plain backward, and A' = p * act(H)."""
+    x, H, dO, p, off, W1, W2 = _routed_case(act)
+    dH, dX, dW1, dW2, Ap, dS = O.grouped_mlp_bwd_routed(x, H, dO, p, off, W1, W2, act,
+                                                         round_bf16=False)
+    A = O.act_forward(H, act)
+    ref = O.grouped_mlp_bwd(x, H, A, p[:, None] * dO, off, W1, W2, act, round_bf16=False)
+    R = int(off[-1])
+    for got, want in zip((dH, dX, dW1, dW2), ref):
+        if got.shape[0] == x.shape[0]:
+            got, want = got[:R], want[:R]
+        assert np.allclose(got, want, rtol=1e-12, atol=1e-12)
+    assert np.allclose(Ap[:R], p[:R, None] * A[:R], rtol=1e-15, atol=0)
+    assert np.isnan(dS[R:]).all()
+
+
+@pytest.mark.parametrize("act", ["swiglu", "srelu"])
+def test_routed_router_gradient_finite_difference(act):
+    """dS_r is the derivative, w.r.t. the row's router probability p_r, of
+    L(p) = sum_r p_r <dO_r, Y_r> with Y = act(H) W2 computed forward."""
+    x, H, dO, p, off, W1, W2 = _routed_case(act, seed=51)
+    _, _, _, _, _, dS = O.grouped_mlp_bwd_routed(x, H, dO, p, off, W1, W2, act, round_bf16=False)
+    A = O.act_forward(H, act)
+
+    def loss(pv):
+        tot = 0.0
+        for e in range(len(off) - 1):
+            r0, r1 = off[e], off[e + 1]
+            tot += float((pv[r0:r1, None] * dO[r0:r1] * (A[r0:r1] @ W2[e])).sum())
+        return tot
+    eps = 1e-6
+    for r in range(int(off[-1])):
+        pp, pm = p.copy(), p.copy()
+        pp[r] += eps
+        pm[r] -= eps
+        assert abs((loss(pp) - loss(pm)) / (2 * eps) - dS[r]) < 1e-6
+
+
+def test_routed_pad_rows_and_empty_expert():
+    """A pad row (p = 0, dO = 0) contributes nothing; an empty expert gets
+    zero weight gradients."""
+    x, H, dO, p, off, W1, W2 = _routed_case("swiglu", seed=52)
+    p[3] = 0.0
+    dO[3] = 0.0
+    dH, _, dW1, dW2, Ap, dS = O.grouped_mlp_bwd_routed(x, H, dO, p, off, W1, W2, "swiglu")
+    assert dS[3] == 0 and (Ap[3] == 0).all() and (dH[3] == 0).all()
+    assert (dW1[1] == 0).all() and (dW2[1] == 0).all()
