@@ -93,10 +93,13 @@ def kernel_work(w, M, E_ne):
                 "fc1_wgrad": (2 * M * d * n1, mxb(M * d) + mxb(M * n1) + B * E * d * n1),
             })
         return work
+    # routed workloads: the FC2-dgrad epilogue also writes A' (bf16) and the dS partials
+    routed = w.routing != "identity"
     return {
         "fc1_act": (2 * M * d * n1, B * (M * d + E_ne * d * n1 + M * n + M * n1)),
         "fc2": (2 * M * n * d, B * (M * n + E_ne * n * d + M * d)),
-        "fc2_dgrad_dact": (2 * M * d * n, B * (M * d + E_ne * n * d + 2 * M * n1)),
+        "fc2_dgrad_dact": (2 * M * d * n, B * (M * d + E_ne * n * d + 2 * M * n1) +
+                           ((B * M * n + 4 * M * ((n + 127) // 128)) if routed else 0)),
         "fc2_wgrad": (2 * M * n * d, B * (M * n + M * d + E * n * d)),
         "fc1_dgrad": (2 * M * n1 * d, B * (M * n1 + E_ne * d * n1 + M * d)),
         "fc1_wgrad": (2 * M * d * n1, B * (M * d + M * n1 + E * d * n1)),
@@ -233,6 +236,9 @@ def make_inputs(w, dev):
         o["out"] = torch.empty((w.T, d), dtype=bf, device=dev)
         o["dx"] = torch.empty((w.T, d), dtype=bf, device=dev)
         o["dprobs"] = torch.empty((w.T, w.k), dtype=torch.float32, device=dev)
+        if w.backward and not w.mxfp8:
+            o["a_scaled"] = torch.empty((Mc, n), dtype=bf, device=dev)
+            o["ds_part"] = torch.empty((Mc, (n + 127) // 128), dtype=torch.float32, device=dev)
         o["ws"] = torch.empty(max(16, M.route_workspace_size(w.T, w.k, E)), dtype=torch.uint8,
                               device=dev)
         o["route"] = {
@@ -358,14 +364,17 @@ def make_step(w, inp, o):
         M.unpermute(o["y_perm"], r["row_of_pair"], T, k, probs=inp["probs"], out=o["out"])
         n += M.last_launch_count()
         # backward: combine -> (scaled permute of dO, router-score gradient)
-        M.permute(inp["dO"], r["pair_of_row"], k, scale=inp["probs"].view(-1), out=o["dy_perm"])
+        # backward with the router gradient inside the expert MLP ([Sonic]
+        # rewrite): dO gathered without the probability; FC2-dgrad applies it
+        # and emits dS partials and A' = S*A; FC2-wgrad contracts A' with dO
+        M.permute(inp["dO"], r["pair_of_row"], k, out=o["dy_perm"])
         n += M.last_launch_count()
-        M.unpermute(o["y_perm"], r["row_of_pair"], T, k, dO=inp["dO"], dprobs=o["dprobs"],
-                    combine=False)
+        M.grouped_mlp_bwd_routed(o["x_perm"], o["h"], o["dy_perm"], r["pair_of_row"],
+                                 inp["probs"].view(-1), r["offsets"], inp["W1"], inp["W2"], act,
+                                 dh=o["dh"], a_scaled=o["a_scaled"], ds_part=o["ds_part"],
+                                 dx_perm=o["dx_perm"], dW1=o["dW1"], dW2=o["dW2"], err=o["err"])
         n += M.last_launch_count()
-        M.grouped_mlp_bwd(o["x_perm"], o["h"], o["a"], o["dy_perm"], r["offsets"], inp["W1"],
-                          inp["W2"], act, dh=o["dh"], dx_perm=o["dx_perm"], dW1=o["dW1"],
-                          dW2=o["dW2"], err=o["err"])
+        M.router_grad_rows(o["ds_part"], r["row_of_pair"], T, k, dprobs=o["dprobs"])
         n += M.last_launch_count()
         M.unpermute(o["dx_perm"], r["row_of_pair"], T, k, out=o["dx"])
         n += M.last_launch_count()
@@ -383,8 +392,8 @@ def event_names(w):
         return KERNELS_FWD + KERNELS_BWD
     if w.mxfp8:
         return ["route", "permute", "mx_quantize_weights"] + KERNELS_FWD + ["combine"]
-    return (["route", "permute"] + KERNELS_FWD + ["combine", "permute_bwd", "router_grad"] +
-            KERNELS_BWD + ["unpermute_bwd"])
+    return (["route", "permute"] + KERNELS_FWD + ["combine", "permute_bwd"] +
+            KERNELS_BWD + ["router_grad_rows", "unpermute_bwd"])
 
 
 # ---------------------------------------------------------------- CPU oracle
@@ -674,7 +683,8 @@ def step_description(w):
     if w.mxfp8:
         return ("route + permute + W2 MXFP8 quantise + fwd (FC1 + MX epilogue, block-scaled FC2) "
                 "+ combine")
-    return "route + permute + fwd + combine + bwd (+ router grad)"
+    return ("route + permute + fwd + combine + bwd with the router gradient inside the expert "
+            "MLP (grouped_mlp_bwd_routed + router_grad_rows) + combine backward")
 
 
 def time_graph(step, steps, ws, flops):

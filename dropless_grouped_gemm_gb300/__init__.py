@@ -27,6 +27,7 @@ __all__ = [
     "permute", "unpermute", "grouped_mlp_fwd", "grouped_mlp_bwd", "MoeError",
     "FLAG_MXFP8", "MxFwd", "mx_quantize_weights", "mx_quantize", "mx_buffers",
     "MxBwd", "mx_quantize_weights_rowwise", "mx_bwd_workspace_size", "grouped_mlp_bwd_mx",
+    "grouped_mlp_bwd_routed", "router_grad_rows",
 ]
 
 ACT = {"swiglu": 0, "geglu": 1, "srelu": 2}
@@ -106,6 +107,11 @@ def lib():
         L.moe_grouped_mlp_bwd_mx.restype = i32
         L.moe_grouped_mlp_bwd_mx.argtypes = [vp, vp, vp, vp, i32, i32, i32, i32, i32, vp, vp, vp,
                                              vp, vp, vp, vp]
+        L.moe_grouped_mlp_bwd_routed.restype = i32
+        L.moe_grouped_mlp_bwd_routed.argtypes = [vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, vp,
+                                                 vp, i32, vp, vp, vp, vp, vp, vp, vp, vp]
+        L.moe_router_grad_rows.restype = i32
+        L.moe_router_grad_rows.argtypes = [vp, i32, vp, i32, i32, i32, vp, vp]
         L.moe_selftest_bounded_wait.restype = i32
         L.moe_selftest_bounded_wait.argtypes = [i32, vp, vp, vp]
         _LIB = L
@@ -423,3 +429,54 @@ def grouped_mlp_bwd_mx(x_perm, h_saved, dy_perm, offsets, mx: dict, act: str = "
                                       _stream(stream))
     _check(rc, "moe_grouped_mlp_bwd_mx")
     return dh, dx_perm, dW1, dW2, err
+
+
+def grouped_mlp_bwd_routed(x_perm, h_saved, do_perm, pair_of_row, probs, offsets, W1, W2,
+                           act: str = "swiglu", dh=None, a_scaled=None, ds_part=None,
+                           dx_perm=None, dW1=None, dW2=None, err=None, stream=None):
+    """Backward with the router gradient inside the expert MLP
+    (moe_grouped_mlp_bwd_routed).  do_perm is the gathered dO without the
+    router probability.  Returns (dh, a_scaled, ds_part, dx_perm, dW1, dW2, err)."""
+    for t, nm in ((x_perm, "x_perm"), (h_saved, "h_saved"), (do_perm, "do_perm"), (W1, "W1"),
+                  (W2, "W2")):
+        _need(t, torch.bfloat16, nm)
+    _need(pair_of_row, torch.int32, "pair_of_row", 1)
+    _need(probs, torch.float32, "probs")
+    _need(offsets, torch.int32, "offsets", 1)
+    M_cap, d = x_perm.shape
+    E, n, _ = W2.shape
+    n1 = n if act == "srelu" else 2 * n
+    dev = x_perm.device
+    bf = torch.bfloat16
+    if dh is None:
+        dh = torch.empty((M_cap, n1), dtype=bf, device=dev)
+    if a_scaled is None:
+        a_scaled = torch.empty((M_cap, n), dtype=bf, device=dev)
+    if ds_part is None:
+        ds_part = torch.empty((M_cap, (n + 127) // 128), dtype=torch.float32, device=dev)
+    if dx_perm is None:
+        dx_perm = torch.empty((M_cap, d), dtype=bf, device=dev)
+    if dW1 is None:
+        dW1 = torch.empty((E, d, n1), dtype=bf, device=dev)
+    if dW2 is None:
+        dW2 = torch.empty((E, n, d), dtype=bf, device=dev)
+    err = _err_word(err, dev)
+    rc = lib().moe_grouped_mlp_bwd_routed(
+        _ptr(x_perm), _ptr(h_saved), _ptr(do_perm), _ptr(pair_of_row), _ptr(probs), _ptr(offsets),
+        E, M_cap, d, n, _ptr(W1), _ptr(W2), ACT[act], _ptr(dh), _ptr(a_scaled), _ptr(ds_part),
+        _ptr(dx_perm), _ptr(dW1), _ptr(dW2), _ptr(err), _stream(stream))
+    _check(rc, "moe_grouped_mlp_bwd_routed")
+    return dh, a_scaled, ds_part, dx_perm, dW1, dW2, err
+
+
+def router_grad_rows(ds_part, row_of_pair, T: int, k: int, dprobs=None, stream=None):
+    """dprobs [T, k] from the routed backward's partials (moe_router_grad_rows)."""
+    _need(ds_part, torch.float32, "ds_part", 2)
+    _need(row_of_pair, torch.int32, "row_of_pair", 1)
+    M_cap, n_parts = ds_part.shape
+    if dprobs is None:
+        dprobs = torch.empty((T, k), dtype=torch.float32, device=ds_part.device)
+    rc = lib().moe_router_grad_rows(_ptr(ds_part), n_parts, _ptr(row_of_pair), T, k, M_cap,
+                                    _ptr(dprobs), _stream(stream))
+    _check(rc, "moe_router_grad_rows")
+    return dprobs

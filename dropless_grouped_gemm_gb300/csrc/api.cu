@@ -169,6 +169,66 @@ int check_mlp_sizes(int E, int M_cap, int d, int n) {
   return MOE_OK;
 }
 
+// The four backward GEMMs.  dy is FC2-dgrad's A operand and FC2-wgrad's B
+// operand, a_w FC2-wgrad's A operand.  Routed (probs != NULL): dy is the
+// unscaled gathered dO; FC2-dgrad applies each row's router probability in
+// its epilogue, which also writes A' (= a_w) and the dS partials.
+int bwd_gemms(const moe_bf16* x_perm, const moe_bf16* h_saved, const moe_bf16* a_w,
+              const moe_bf16* dy, const int32_t* offsets, int E, int M_cap, int d, int n,
+              const moe_bf16* W1, const moe_bf16* W2, int act, moe_bf16* dh, moe_bf16* dx_perm,
+              moe_bf16* dW1, moe_bf16* dW2, int32_t* err, cudaStream_t s, int sms,
+              const int32_t* pair_of_row, const float* probs, moe_bf16* a_scaled,
+              float* ds_part) {
+  const int n1 = (act == MOE_ACT_SRELU) ? n : 2 * n;
+  moe::GemmArgs probe{};
+  probe.M_cap = M_cap;
+  probe.E = E;
+  const bool skinny = moe::wgrad_skinny(probe);
+  // operand maps
+  CUtensorMap t_dy_k, t_w2_k, t_a_mn, t_dy_mn, t_dh_k, t_w1_k, t_x_mn, t_dh_mn, t_dw1, t_dw2;
+  if (!map_act(&t_dy_k, dy, M_cap, d, moe::kBM) ||           // FC2-dgrad A (K = d)
+      !map_w(&t_w2_k, W2, E, n, d, 128) ||                    // FC2-dgrad B rows = n (halves)
+      !map_act(&t_a_mn, a_w, M_cap, n, 64) ||                 // FC2-wgrad A (MN = n)
+      !map_act(&t_dy_mn, dy, M_cap, d, 64) ||                 // FC2-wgrad B (MN = d)
+      !map_act(&t_dh_k, dh, M_cap, n1, moe::kBM) ||           // FC1-dgrad A (K = n1)
+      !map_w(&t_w1_k, W1, E, d, n1, 128) ||                   // FC1-dgrad B rows = d (halves)
+      !map_act(&t_x_mn, x_perm, M_cap, d, 64) ||              // FC1-wgrad A (MN = d)
+      !map_act(&t_dh_mn, dh, M_cap, n1, 64) ||                // FC1-wgrad B (MN = n1)
+      !map_out3(&t_dw2, dW2, E, n, d, skinny) || !map_out3(&t_dw1, dW1, E, d, n1, skinny))
+    return MOE_E_CUDA;
+
+  // 1. dH = act'(H; dY W2^T)
+  moe::GemmArgs g{};
+  g.offsets = offsets; g.E = E; g.M_cap = M_cap; g.K = d; g.N = n;
+  g.out = dh; g.ldo = n1; g.aux = h_saved; g.ld_aux = n1; g.err = err;
+  if (probs) {
+    g.pair_of_row = pair_of_row; g.probs = probs; g.out3 = a_scaled; g.ldo3 = n;
+    g.ds_part = ds_part; g.ds_parts = (n + 127) / 128;
+  }
+  cudaError_t e = gemm(moe::GemmKind::kDgradAct, act, t_dy_k, t_w2_k, t_dy_k, g, sms, s);
+  if (e != cudaSuccess) return MOE_E_CUDA;
+  // 2. dW2_e = A_e^T dY_e
+  moe::GemmArgs gw2{};
+  gw2.offsets = offsets; gw2.E = E; gw2.M_cap = M_cap; gw2.N = d; gw2.R = n;
+  gw2.out = dW2; gw2.ldo = d; gw2.out_estride = static_cast<long long>(n) * d; gw2.err = err;
+  e = gemm(moe::GemmKind::kWgrad, 0, t_a_mn, t_dy_mn, t_dw2, gw2, sms, s);
+  if (e != cudaSuccess) return MOE_E_CUDA;
+  // 3. dX = dH W1^T
+  moe::GemmArgs gd{};
+  gd.offsets = offsets; gd.E = E; gd.M_cap = M_cap; gd.K = n1; gd.N = d;
+  gd.out = dx_perm; gd.ldo = d; gd.err = err;
+  e = gemm(moe::GemmKind::kDgrad, 0, t_dh_k, t_w1_k, t_dh_k, gd, sms, s);
+  if (e != cudaSuccess) return MOE_E_CUDA;
+  // 4. dW1_e = X_e^T dH_e
+  moe::GemmArgs gw1{};
+  gw1.offsets = offsets; gw1.E = E; gw1.M_cap = M_cap; gw1.N = n1; gw1.R = d;
+  gw1.out = dW1; gw1.ldo = n1; gw1.out_estride = static_cast<long long>(d) * n1; gw1.err = err;
+  e = gemm(moe::GemmKind::kWgrad, 0, t_x_mn, t_dh_mn, t_dw1, gw1, sms, s);
+  if (e != cudaSuccess) return MOE_E_CUDA;
+  g_last_launches = 4;
+  return MOE_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -411,49 +471,57 @@ int moe_grouped_mlp_bwd(const moe_bf16* x_perm, const moe_bf16* h_saved, const m
   const int sms = num_sms_current();
   if (sms <= 0) return MOE_E_CUDA;
 
-  moe::GemmArgs probe{};
-  probe.M_cap = M_cap;
-  probe.E = E;
-  const bool skinny = moe::wgrad_skinny(probe);
-  // operand maps
-  CUtensorMap t_dy_k, t_w2_k, t_a_mn, t_dy_mn, t_dh_k, t_w1_k, t_x_mn, t_dh_mn, t_dw1, t_dw2;
-  if (!map_act(&t_dy_k, dy_perm, M_cap, d, moe::kBM) ||      // FC2-dgrad A (K = d)
-      !map_w(&t_w2_k, W2, E, n, d, 128) ||                    // FC2-dgrad B rows = n (halves)
-      !map_act(&t_a_mn, a, M_cap, n, 64) ||                   // FC2-wgrad A (MN = n)
-      !map_act(&t_dy_mn, dy_perm, M_cap, d, 64) ||            // FC2-wgrad B (MN = d)
-      !map_act(&t_dh_k, dh, M_cap, n1, moe::kBM) ||           // FC1-dgrad A (K = n1)
-      !map_w(&t_w1_k, W1, E, d, n1, 128) ||                   // FC1-dgrad B rows = d (halves)
-      !map_act(&t_x_mn, x_perm, M_cap, d, 64) ||              // FC1-wgrad A (MN = d)
-      !map_act(&t_dh_mn, dh, M_cap, n1, 64) ||                // FC1-wgrad B (MN = n1)
-      !map_out3(&t_dw2, dW2, E, n, d, skinny) || !map_out3(&t_dw1, dW1, E, d, n1, skinny))
-    return MOE_E_CUDA;
+  return bwd_gemms(x_perm, h_saved, a, dy_perm, offsets, E, M_cap, d, n, W1, W2, act, dh, dx_perm,
+                   dW1, dW2, err, s, sms, nullptr, nullptr, nullptr, nullptr);
+}
 
-  // 1. dH = act'(H; dY W2^T)
-  moe::GemmArgs g{};
-  g.offsets = offsets; g.E = E; g.M_cap = M_cap; g.K = d; g.N = n;
-  g.out = dh; g.ldo = n1; g.aux = h_saved; g.ld_aux = n1; g.err = err;
-  cudaError_t e = gemm(moe::GemmKind::kDgradAct, act, t_dy_k, t_w2_k, t_dy_k, g, sms, s);
-  if (e != cudaSuccess) return MOE_E_CUDA;
-  // 2. dW2_e = A_e^T dY_e
-  moe::GemmArgs gw2{};
-  gw2.offsets = offsets; gw2.E = E; gw2.M_cap = M_cap; gw2.N = d; gw2.R = n;
-  gw2.out = dW2; gw2.ldo = d; gw2.out_estride = static_cast<long long>(n) * d; gw2.err = err;
-  e = gemm(moe::GemmKind::kWgrad, 0, t_a_mn, t_dy_mn, t_dw2, gw2, sms, s);
-  if (e != cudaSuccess) return MOE_E_CUDA;
-  // 3. dX = dH W1^T
-  moe::GemmArgs gd{};
-  gd.offsets = offsets; gd.E = E; gd.M_cap = M_cap; gd.K = n1; gd.N = d;
-  gd.out = dx_perm; gd.ldo = d; gd.err = err;
-  e = gemm(moe::GemmKind::kDgrad, 0, t_dh_k, t_w1_k, t_dh_k, gd, sms, s);
-  if (e != cudaSuccess) return MOE_E_CUDA;
-  // 4. dW1_e = X_e^T dH_e
-  moe::GemmArgs gw1{};
-  gw1.offsets = offsets; gw1.E = E; gw1.M_cap = M_cap; gw1.N = n1; gw1.R = d;
-  gw1.out = dW1; gw1.ldo = n1; gw1.out_estride = static_cast<long long>(d) * n1; gw1.err = err;
-  e = gemm(moe::GemmKind::kWgrad, 0, t_x_mn, t_dh_mn, t_dw1, gw1, sms, s);
-  if (e != cudaSuccess) return MOE_E_CUDA;
-  g_last_launches = 4;
-  return MOE_OK;
+int moe_grouped_mlp_bwd_routed(const moe_bf16* x_perm, const moe_bf16* h_saved,
+                               const moe_bf16* do_perm, const int32_t* pair_of_row,
+                               const float* probs, const int32_t* offsets, int E, int M_cap,
+                               int d, int n, const moe_bf16* W1, const moe_bf16* W2, int act,
+                               moe_bf16* dh, moe_bf16* a_scaled, float* ds_part,
+                               moe_bf16* dx_perm, moe_bf16* dW1, moe_bf16* dW2, int32_t* err,
+                               void* stream) {
+  g_last_launches = 0;
+  int rc = check_mlp_sizes(E, M_cap, d, n);
+  if (rc) return rc;
+  if (act < MOE_ACT_SWIGLU || act > MOE_ACT_SRELU) return MOE_E_ARG;
+  if (!offsets || !W1 || !W2 || !dW1 || !dW2 || !err) return MOE_E_NULL;
+  const int n1 = (act == MOE_ACT_SRELU) ? n : 2 * n;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (M_cap == 0) {
+    cudaError_t e = cudaMemsetAsync(dW1, 0, static_cast<size_t>(E) * d * n1 * 2, s);
+    if (e == cudaSuccess) e = cudaMemsetAsync(dW2, 0, static_cast<size_t>(E) * n * d * 2, s);
+    return cuda_rc(e);
+  }
+  if (!x_perm || !h_saved || !do_perm || !pair_of_row || !probs || !dh || !a_scaled || !ds_part ||
+      !dx_perm)
+    return MOE_E_NULL;
+  if (misaligned(x_perm) || misaligned(h_saved) || misaligned(do_perm) || misaligned(dh) ||
+      misaligned(a_scaled) || misaligned(dx_perm) || misaligned(dW1) || misaligned(dW2) ||
+      misaligned(W1) || misaligned(W2))
+    return MOE_E_ALIGN;
+  const int sms = num_sms_current();
+  if (sms <= 0) return MOE_E_CUDA;
+  return bwd_gemms(x_perm, h_saved, a_scaled, do_perm, offsets, E, M_cap, d, n, W1, W2, act, dh,
+                   dx_perm, dW1, dW2, err, s, sms, pair_of_row, probs, a_scaled, ds_part);
+}
+
+int moe_router_grad_rows(const float* ds_part, int n_parts, const int32_t* row_of_pair, int T,
+                         int k, int M_cap, float* dprobs, void* stream) {
+  g_last_launches = 0;
+  if (T < 0 || k < 1 || n_parts < 1 || M_cap < 0) return MOE_E_SIZE;
+  if (T == 0) return MOE_OK;
+  if (!ds_part || !row_of_pair || !dprobs) return MOE_E_NULL;
+  const int sms = num_sms_current();
+  if (sms <= 0) return MOE_E_CUDA;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  ev_begin(s);
+  const cudaError_t e = moe::launch_router_grad_rows(ds_part, n_parts, row_of_pair, T * k, M_cap,
+                                                     dprobs, sms, s);
+  ev_end(s);
+  g_last_launches = 1;
+  return cuda_rc(e);
 }
 
 int moe_mx_quantize_weights(const moe_bf16* W2, int E, int n, int d, uint8_t* w2_q,

@@ -246,6 +246,65 @@ __device__ __forceinline__ void epilogue_chunk(const GemmArgs& g, const Tile& tl
   }
 }
 
+// Routed FC2-dgrad epilogue ([Sonic] "역전파 계산 그래프 재작성하기": the dH
+// kernel also emits dS and A' = S*A): dA' columns col..col+31 of one row with
+// router probability p -> dH (same interleaving as H) and A' (bf16); returns
+// the chunk's part of <dA', A>, A = act(H) recomputed from the stored H.
+template <int ACT>
+__device__ __forceinline__ float dgrad_act_routed_chunk(const GemmArgs& g, long long grow, int col,
+                                                        float p, const uint32_t (&r)[32]) {
+  float ds = 0.f;
+  uint32_t ap[16];  // A' of the chunk's 32 columns, packed bf16 pairs
+  if constexpr (ACT == MOE_ACT_SRELU) {
+    const uint16_t* hp = g.aux + grow * g.ld_aux + col;
+    uint16_t* pd = g.out + grow * g.ldo + col;
+#pragma unroll
+    for (int v = 0; v < 4; ++v) {
+      const uint4 hv = *reinterpret_cast<const uint4*>(hp + 8 * v);
+      const uint32_t hw[4] = {hv.x, hv.y, hv.z, hv.w};
+      uint32_t o[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float h0 = fmaxf(bf16_lo(hw[i]), 0.f), h1 = fmaxf(bf16_hi(hw[i]), 0.f);
+        const float d0 = __uint_as_float(r[8 * v + 2 * i]), d1 = __uint_as_float(r[8 * v + 2 * i + 1]);
+        const float a0 = h0 * h0, a1 = h1 * h1;
+        ds += d0 * a0 + d1 * a1;
+        o[i] = pack_bf16x2(2.f * h0 * (p * d0), 2.f * h1 * (p * d1));
+        ap[4 * v + i] = pack_bf16x2(p * a0, p * a1);
+      }
+      st_global_v4(pd + 8 * v, o[0], o[1], o[2], o[3]);
+    }
+  } else {
+    const uint16_t* hp = g.aux + grow * g.ld_aux + 2 * col;
+    uint16_t* pd = g.out + grow * g.ldo + 2 * col;
+#pragma unroll
+    for (int v = 0; v < 8; ++v) {
+      const uint4 hv = *reinterpret_cast<const uint4*>(hp + 8 * v);
+      const uint32_t hw[4] = {hv.x, hv.y, hv.z, hv.w};  // (gate, up) pairs
+      uint32_t o[4];
+      float a[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float gg = bf16_lo(hw[i]), uu = bf16_hi(hw[i]);
+        const float dap = __uint_as_float(r[4 * v + i]);
+        float ph, dph;
+        gate_phi_dphi<ACT>(gg, ph, dph);
+        a[i] = ph * uu;
+        ds += dap * a[i];
+        const float da = p * dap;
+        o[i] = pack_bf16x2(da * uu * dph, da * ph);
+      }
+      ap[2 * v] = pack_bf16x2(p * a[0], p * a[1]);
+      ap[2 * v + 1] = pack_bf16x2(p * a[2], p * a[3]);
+      st_global_v4(pd + 8 * v, o[0], o[1], o[2], o[3]);
+    }
+  }
+  uint16_t* pa = g.out3 + grow * g.ldo3 + col;
+#pragma unroll
+  for (int v = 0; v < 4; ++v) st_global_v4(pa + 8 * v, ap[4 * v], ap[4 * v + 1], ap[4 * v + 2], ap[4 * v + 3]);
+  return ds;
+}
+
 // FC1 epilogue with MXFP8 output: one 32-value block of A per call (64
 // accumulator columns when gated, 32 for squared ReLU).  A is rounded to
 // bf16 first; the codes quantise those bf16 values.
@@ -637,6 +696,24 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 #pragma unroll
         for (int i = 0; i < 32; ++i) z[i] = 0;
         for (int c = wg * 4; c < wg * 4 + 4; ++c) epilogue_chunk<KIND, ACT>(g, tl, row_in_tile, c, z);
+      } else if (KIND == GemmKind::kDgradAct && g.probs != nullptr) {
+        // routed: this thread's row, the warpgroup's 128 columns
+        const bool vrow = row_in_tile < tl.rows;
+        const long long grow = tl.row0 + row_in_tile;
+        float p = 0.f, dsum = 0.f;
+        if (vrow) {
+          const int pr = g.pair_of_row[grow];
+          p = pr >= 0 ? g.probs[pr] : 0.f;
+        }
+        for (int c = wg * 4; c < wg * 4 + 4; ++c) {
+          uint32_t r[32];
+          tmem_ld32(tb + c * 32, r);
+          tmem_wait_ld();
+          const int col = tl.n0 + c * 32;
+          if (vrow && col < g.N) dsum += dgrad_act_routed_chunk<ACT>(g, grow, col, p, r);
+        }
+        const int half = tl.n0 + wg * 128;
+        if (vrow && half < g.N) g.ds_part[grow * g.ds_parts + half / 128] = dsum;
       } else {
         for (int c = wg * 4; c < wg * 4 + 4; ++c) {
           uint32_t r[32];

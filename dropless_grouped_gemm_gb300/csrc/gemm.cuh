@@ -39,6 +39,16 @@ struct GemmArgs {
   uint8_t* mx_qT;          // [n, M_cap] codes of A^T (32x1 blocks) or NULL
   uint8_t* mx_sT;          // [n, M_cap/32] scales of mx_qT
   int n_a;                 // columns of A (n)
+  // kDgradAct, routed (probs != nullptr): the accumulator is dA' = dO W2^T
+  // before the router probability p of the row's pair; the epilogue writes
+  // dH = act'(H; p dA'), A' = p act(H) and the partial <dA', act(H)> of each
+  // 128-column half tile
+  const int32_t* pair_of_row;  // [M_cap] row -> pair (-1: pad row)
+  const float* probs;          // [T*k] probability of each pair
+  uint16_t* out3;              // A' [M_cap, ldo3] bf16
+  long long ldo3;
+  float* ds_part;              // [M_cap, ds_parts] fp32
+  int ds_parts;
   // unit order inside an expert, set by launch_grouped_gemm: 0 = row pairs
   // outermost (a wave of CTAs sweeps every column tile of B), 1 = column
   // tiles outermost (a wave reuses each B column tile across all row pairs)

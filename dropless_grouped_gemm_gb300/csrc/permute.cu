@@ -117,6 +117,23 @@ __global__ void __launch_bounds__(kThreads)
   }
 }
 
+// dprobs[p] = sum of the row's partial <dA', A> (routed backward), summed in
+// a fixed order; 0 for pairs without a row
+__global__ void __launch_bounds__(kThreads)
+    router_grad_rows_kernel(const float* __restrict__ ds_part, int n_parts,
+                            const int32_t* __restrict__ row_of_pair, int P, int M_cap,
+                            float* __restrict__ dprobs) {
+  for (int p = blockIdx.x * kThreads + threadIdx.x; p < P; p += gridDim.x * kThreads) {
+    const int row = row_of_pair[p];
+    float s = 0.f;
+    if (row >= 0 && row < M_cap) {
+      const float* q = ds_part + static_cast<long long>(row) * n_parts;
+      for (int i = 0; i < n_parts; ++i) s += q[i];
+    }
+    dprobs[p] = s;
+  }
+}
+
 int grid_for(long long rows, int num_sms) {
   const long long want = (rows + kRowsPerBlock - 1) / kRowsPerBlock;
   const long long cap = 8LL * num_sms;
@@ -154,6 +171,16 @@ cudaError_t launch_unpermute(const uint16_t* src, const float* probs,
         T, k, d / 8, M_cap, dprobs);
     ++*launches;
   }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_router_grad_rows(const float* ds_part, int n_parts, const int32_t* row_of_pair,
+                                   int P, int M_cap, float* dprobs, int num_sms, cudaStream_t s) {
+  if (P <= 0) return cudaSuccess;
+  const long long want = (P + kThreads - 1) / kThreads;
+  const int grid = static_cast<int>(want < 4LL * num_sms ? want : 4LL * num_sms);
+  router_grad_rows_kernel<<<grid, kThreads, 0, s>>>(ds_part, n_parts, row_of_pair, P, M_cap,
+                                                    dprobs);
   return cudaGetLastError();
 }
 

@@ -36,4 +36,8 @@ cudaError_t launch_unpermute(const uint16_t* src, const float* probs,
                              const uint16_t* dO, float* dprobs, int num_sms, cudaStream_t s,
                              int* launches);
 
+// dprobs[p] from the routed backward's per-row partials ds_part [M_cap, n_parts]
+cudaError_t launch_router_grad_rows(const float* ds_part, int n_parts, const int32_t* row_of_pair,
+                                   int P, int M_cap, float* dprobs, int num_sms, cudaStream_t s);
+
 }  // namespace moe

@@ -326,6 +326,39 @@ int moe_grouped_mlp_bwd(const moe_bf16* x_perm, const moe_bf16* h_saved,
                         void* stream);
 
 /*
+ * moe_grouped_mlp_bwd_routed - backward with the router-score gradient
+ * taken inside the expert MLP ([Sonic] "역전파 계산 그래프 재작성하기":
+ * dS_{t,e} = <dO_t, Y_{e,t}> = <dO_t W2_e^T, A_e>, so Y is not needed; the
+ * dH kernel's epilogue also emits dS and A' = S*A).
+ *   do_perm [M_cap, d]: the gathered output gradient WITHOUT the router
+ *   probability (moe_permute with scale = NULL); pair_of_row [M_cap] and
+ *   probs [T*k] give each row's probability p (0 for pad rows).
+ *   FC2-dgrad computes dA' = dO W2^T; its epilogue writes dh = act'(H; p dA'),
+ *   a_scaled [M_cap, n] = p * act(H) (bf16) and ds_part [M_cap, ceil(n/128)]
+ *   (fp32 partial <dA', act(H)> of each 128-column half tile, caller-owned
+ *   scratch); FC2-wgrad then contracts a_scaled with do_perm.  dx_perm, dW1,
+ *   dW2 as in moe_grouped_mlp_bwd.  Four launches; finish with
+ *   moe_router_grad_rows.  Errors as moe_grouped_mlp_bwd.
+ */
+int moe_grouped_mlp_bwd_routed(const moe_bf16* x_perm, const moe_bf16* h_saved,
+                               const moe_bf16* do_perm, const int32_t* pair_of_row,
+                               const float* probs, const int32_t* offsets, int E,
+                               int M_cap, int d, int n, const moe_bf16* W1,
+                               const moe_bf16* W2, int act, moe_bf16* dh,
+                               moe_bf16* a_scaled, float* ds_part, moe_bf16* dx_perm,
+                               moe_bf16* dW1, moe_bf16* dW2, int32_t* err,
+                               void* stream);
+
+/*
+ * moe_router_grad_rows - dprobs [T*k] (fp32) of the routed backward:
+ * dprobs[p] = sum over the n_parts partials of ds_part's row row_of_pair[p]
+ * (fixed order, so reruns are bitwise identical); 0 for pairs without a
+ * row.  n_parts = ceil(n/128).  One launch.
+ */
+int moe_router_grad_rows(const float* ds_part, int n_parts, const int32_t* row_of_pair,
+                         int T, int k, int M_cap, float* dprobs, void* stream);
+
+/*
  * moe_mx_quantize_weights - MXFP8 copy of W2 for the block-scaled FC2
  * (blocks of 32 consecutive rows, FC2's reduction index, per column).
  *   W2 [E, n, d] bf16 -> w2_q [E, n, d] E4M3 codes, w2_s MMA-tiled scales
