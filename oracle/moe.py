@@ -20,6 +20,7 @@ __all__ = [
     "interleave_gate_up", "split_gate_up",
     "act_forward", "act_backward", "phi", "dphi",
     "grouped_mlp_fwd", "grouped_mlp_bwd", "grouped_mlp_bwd_routed",
+    "hadamard16", "amax", "amax_rht_transposed",
     "fc1_rows", "fc2_rows",
 ]
 
@@ -420,6 +421,49 @@ def grouped_mlp_bwd_routed(x_perm, H, dO_perm, row_prob, offsets, W1, W2, act: s
         dX[r0:r1] = _rb(dh @ W1[e].T, round_bf16)
         dW1[e] = x_perm[r0:r1].T @ dh
     return dH, dX, _rb(dW1, round_bf16), _rb(dW2, round_bf16), Ap, dS
+
+
+# ---------------------------------------------------------------------------
+# NVFP4 scaling statistics ([CuTe] "핵심 아이디어": the per-tensor amax of the
+# forward output and the amax of the transposed, Hadamard-rotated output in
+# the backward are separate memory passes unless fused)
+# ---------------------------------------------------------------------------
+
+def hadamard16() -> np.ndarray:
+    """16x16 Hadamard matrix of Sylvester's construction, H[i, j] =
+    (-1)^popcount(i & j), scaled by 1/4 so that it is orthonormal."""
+    i = np.arange(16)
+    parity = np.array([[bin(a & b).count("1") & 1 for b in i] for a in i])
+    return np.where(parity == 1, -1.0, 1.0) / 4.0
+
+
+def amax(t) -> float:
+    """Per-tensor absolute maximum."""
+    t = np.asarray(t, dtype=np.float64)
+    return float(np.abs(t).max()) if t.size else 0.0
+
+
+def amax_rht_transposed(G, offsets) -> float:
+    """Absolute maximum of the transposed copy of G [M, C] after the
+    16-point Hadamard rotation along its rows: per expert, the rows
+    [offsets[e], offsets[e+1]) are cut into 16-row blocks from the expert's
+    first row (the last block zero-padded), and each column of a block is
+    multiplied by hadamard16().  (Reading: the pages name the statistic;
+    the rotation is the orthonormal Sylvester one, without random signs.)"""
+    G = np.asarray(G, dtype=np.float64)
+    Hm = hadamard16()
+    best = 0.0
+    for e in range(len(offsets) - 1):
+        r0, r1 = int(offsets[e]), int(offsets[e + 1])
+        if r1 <= r0:
+            continue
+        rows = r1 - r0
+        nb = -(-rows // 16)
+        blk = np.zeros((nb * 16, G.shape[1]))
+        blk[:rows] = G[r0:r1]
+        rot = np.einsum("ij,bjc->bic", Hm, blk.reshape(nb, 16, G.shape[1]))
+        best = max(best, float(np.abs(rot).max()))
+    return best
 
 
 # sampled-row helpers for full-size parity checks (same arithmetic as above,

@@ -250,3 +250,38 @@ def test_routed_pad_rows_and_empty_expert():
     dH, _, dW1, dW2, Ap, dS = O.grouped_mlp_bwd_routed(x, H, dO, p, off, W1, W2, "swiglu")
     assert dS[3] == 0 and (Ap[3] == 0).all() and (dH[3] == 0).all()
     assert (dW1[1] == 0).all() and (dW2[1] == 0).all()
+
+
+def test_hadamard16_pins():
+    """Sylvester's recursion H_{2m} = [[H, H], [H, -H]] gives the same matrix;
+    it is orthonormal and symmetric."""
+    h = np.array([[1.0]])
+    for _ in range(4):
+        h = np.block([[h, h], [h, -h]])
+    assert np.array_equal(O.hadamard16(), h / 4.0)
+    assert np.allclose(O.hadamard16() @ O.hadamard16(), np.eye(16), atol=1e-15)
+
+
+def test_amax_rht_transposed_special_cases():
+    """One nonzero v in a block -> |v|/4; a constant block c -> 4|c| (all of
+    it in the first coefficient); Parseval: the rotated block keeps its sum of
+    squares; blocks start at each expert's first row, the last one padded."""
+    G = np.zeros((40, 3))
+    G[5, 0] = -8.0
+    assert O.amax_rht_transposed(G, [0, 40]) == 2.0
+    G = np.zeros((40, 2))
+    G[16:32, 1] = 0.5
+    assert O.amax_rht_transposed(G, [0, 40]) == 2.0
+    # an expert starting at row 3: its first block is rows 3..18, so a
+    # constant run on rows 3..18 rotates to 4c, while on rows 0..15 (crossing
+    # the block start) it would not
+    G = np.zeros((40, 1))
+    G[3:19, 0] = 1.0
+    assert O.amax_rht_transposed(G, [0, 3, 40]) == 4.0
+    assert O.amax_rht_transposed(G, [0, 40]) < 4.0
+    rng = np.random.default_rng(53)
+    blk = rng.standard_normal((16, 4))
+    rot = O.hadamard16() @ blk
+    assert np.allclose((rot ** 2).sum(0), (blk ** 2).sum(0))
+    assert np.isclose(O.amax_rht_transposed(blk, [0, 16]), np.abs(rot).max())
+    assert O.amax(np.array([[-3.0, 2.0]])) == 3.0 and O.amax(np.zeros((0, 4))) == 0.0
