@@ -88,7 +88,7 @@ def lib():
         L.moe_unpermute.argtypes = [vp, vp, vp, i32, i32, i32, i32, vp, vp, vp, vp]
         L.moe_grouped_mlp_fwd.restype = i32
         L.moe_grouped_mlp_fwd.argtypes = [vp, vp, i32, i32, i32, i32, vp, vp, i32, i32, vp, vp, vp,
-                                          vp, vp, vp]
+                                          vp, vp, vp, vp]
         L.moe_mx_quantize_weights.restype = i32
         L.moe_mx_quantize_weights.argtypes = [vp, i32, i32, i32, vp, vp, vp]
         L.moe_mx_quantize.restype = i32
@@ -99,7 +99,7 @@ def lib():
         L.moe_launch_events_used.argtypes = []
         L.moe_grouped_mlp_bwd.restype = i32
         L.moe_grouped_mlp_bwd.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, vp, vp, i32, i32,
-                                          vp, vp, vp, vp, vp, vp]
+                                          vp, vp, vp, vp, vp, vp, vp]
         L.moe_mx_quantize_weights_rowwise.restype = i32
         L.moe_mx_quantize_weights_rowwise.argtypes = [vp, i32, i32, vp, vp, vp]
         L.moe_mx_bwd_workspace_size.restype = sz
@@ -109,7 +109,7 @@ def lib():
                                              vp, vp, vp, vp]
         L.moe_grouped_mlp_bwd_routed.restype = i32
         L.moe_grouped_mlp_bwd_routed.argtypes = [vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, vp,
-                                                 vp, i32, vp, vp, vp, vp, vp, vp, vp, vp]
+                                                 vp, i32, vp, vp, vp, vp, vp, vp, vp, vp, vp]
         L.moe_router_grad_rows.restype = i32
         L.moe_router_grad_rows.argtypes = [vp, i32, vp, i32, i32, i32, vp, vp]
         L.moe_selftest_bounded_wait.restype = i32
@@ -253,11 +253,14 @@ def grouped_mlp_fwd(x_perm: torch.Tensor, offsets: torch.Tensor, W1: torch.Tenso
                     W2: torch.Tensor, act: str = "swiglu", save_h: bool = False,
                     h_saved: torch.Tensor | None = None, a: torch.Tensor | None = None,
                     y_perm: torch.Tensor | None = None, err: torch.Tensor | None = None,
-                    mx: dict | None = None, stream=None):
+                    mx: dict | None = None, amax: torch.Tensor | None = None, stream=None):
     """Grouped expert MLP forward (see moe_grouped_mlp_fwd).  With ``mx`` (a
     dict of uint8 device tensors w2_q, w2_s, a_q, a_s and optionally a_qT,
-    a_sT; see ``mx_buffers``) the MXFP8 path runs.  Returns
+    a_sT; see ``mx_buffers``) the MXFP8 path runs.  ``amax`` (a float32
+    device tensor of one element) is raised to max |A|.  Returns
     (h_saved or None, a, y_perm, err)."""
+    if amax is not None:
+        _need(amax, torch.float32, "amax")
     _need(x_perm, torch.bfloat16, "x_perm", 2)
     _need(offsets, torch.int32, "offsets", 1)
     _need(W1, torch.bfloat16, "W1", 3)
@@ -286,13 +289,13 @@ def grouped_mlp_fwd(x_perm: torch.Tensor, offsets: torch.Tensor, W1: torch.Tenso
     rc = lib().moe_grouped_mlp_fwd(_ptr(x_perm), _ptr(offsets), E, M_cap, d, n, _ptr(W1), _ptr(W2),
                                    ACT[act], flags, _ptr(h_saved) if save_h else None, _ptr(a),
                                    _ptr(y_perm), ctypes.byref(mxs) if mxs is not None else None,
-                                   _ptr(err), _stream(stream))
+                                   _ptr(amax), _ptr(err), _stream(stream))
     _check(rc, "moe_grouped_mlp_fwd")
     return (h_saved if save_h else None), a, y_perm, err
 
 
 def grouped_mlp_bwd(x_perm, h_saved, a, dy_perm, offsets, W1, W2, act: str = "swiglu",
-                    dh=None, dx_perm=None, dW1=None, dW2=None, err=None, stream=None):
+                    dh=None, dx_perm=None, dW1=None, dW2=None, err=None, amax=None, stream=None):
     """Grouped expert MLP backward (see moe_grouped_mlp_bwd).  Returns
     (dh, dx_perm, dW1, dW2, err)."""
     for t, nm in ((x_perm, "x_perm"), (h_saved, "h_saved"), (a, "a"), (dy_perm, "dy_perm"),
@@ -314,8 +317,8 @@ def grouped_mlp_bwd(x_perm, h_saved, a, dy_perm, offsets, W1, W2, act: str = "sw
     err = _err_word(err, dev)
     rc = lib().moe_grouped_mlp_bwd(_ptr(x_perm), _ptr(h_saved), _ptr(a), _ptr(dy_perm),
                                    _ptr(offsets), E, M_cap, d, n, _ptr(W1), _ptr(W2), ACT[act], 0,
-                                   _ptr(dh), _ptr(dx_perm), _ptr(dW1), _ptr(dW2), _ptr(err),
-                                   _stream(stream))
+                                   _ptr(dh), _ptr(dx_perm), _ptr(dW1), _ptr(dW2), _ptr(amax),
+                                   _ptr(err), _stream(stream))
     _check(rc, "moe_grouped_mlp_bwd")
     return dh, dx_perm, dW1, dW2, err
 
@@ -433,7 +436,7 @@ def grouped_mlp_bwd_mx(x_perm, h_saved, dy_perm, offsets, mx: dict, act: str = "
 
 def grouped_mlp_bwd_routed(x_perm, h_saved, do_perm, pair_of_row, probs, offsets, W1, W2,
                            act: str = "swiglu", dh=None, a_scaled=None, ds_part=None,
-                           dx_perm=None, dW1=None, dW2=None, err=None, stream=None):
+                           dx_perm=None, dW1=None, dW2=None, err=None, amax=None, stream=None):
     """Backward with the router gradient inside the expert MLP
     (moe_grouped_mlp_bwd_routed).  do_perm is the gathered dO without the
     router probability.  Returns (dh, a_scaled, ds_part, dx_perm, dW1, dW2, err)."""
@@ -464,7 +467,7 @@ def grouped_mlp_bwd_routed(x_perm, h_saved, do_perm, pair_of_row, probs, offsets
     rc = lib().moe_grouped_mlp_bwd_routed(
         _ptr(x_perm), _ptr(h_saved), _ptr(do_perm), _ptr(pair_of_row), _ptr(probs), _ptr(offsets),
         E, M_cap, d, n, _ptr(W1), _ptr(W2), ACT[act], _ptr(dh), _ptr(a_scaled), _ptr(ds_part),
-        _ptr(dx_perm), _ptr(dW1), _ptr(dW2), _ptr(err), _stream(stream))
+        _ptr(dx_perm), _ptr(dW1), _ptr(dW2), _ptr(amax), _ptr(err), _stream(stream))
     _check(rc, "moe_grouped_mlp_bwd_routed")
     return dh, a_scaled, ds_part, dx_perm, dW1, dW2, err
 

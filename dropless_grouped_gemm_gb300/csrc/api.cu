@@ -178,7 +178,7 @@ int bwd_gemms(const moe_bf16* x_perm, const moe_bf16* h_saved, const moe_bf16* a
               const moe_bf16* W1, const moe_bf16* W2, int act, moe_bf16* dh, moe_bf16* dx_perm,
               moe_bf16* dW1, moe_bf16* dW2, int32_t* err, cudaStream_t s, int sms,
               const int32_t* pair_of_row, const float* probs, moe_bf16* a_scaled,
-              float* ds_part) {
+              float* ds_part, float* amax_dh) {
   const int n1 = (act == MOE_ACT_SRELU) ? n : 2 * n;
   moe::GemmArgs probe{};
   probe.M_cap = M_cap;
@@ -200,7 +200,7 @@ int bwd_gemms(const moe_bf16* x_perm, const moe_bf16* h_saved, const moe_bf16* a
   // 1. dH = act'(H; dY W2^T)
   moe::GemmArgs g{};
   g.offsets = offsets; g.E = E; g.M_cap = M_cap; g.K = d; g.N = n;
-  g.out = dh; g.ldo = n1; g.aux = h_saved; g.ld_aux = n1; g.err = err;
+  g.out = dh; g.ldo = n1; g.aux = h_saved; g.ld_aux = n1; g.err = err; g.amax = amax_dh;
   if (probs) {
     g.pair_of_row = pair_of_row; g.probs = probs; g.out3 = a_scaled; g.ldo3 = n;
     g.ds_part = ds_part; g.ds_parts = (n + 127) / 128;
@@ -377,7 +377,7 @@ int moe_unpermute(const moe_bf16* src, const float* probs, const int32_t* row_of
 int moe_grouped_mlp_fwd(const moe_bf16* x_perm, const int32_t* offsets, int E, int M_cap, int d,
                         int n, const moe_bf16* W1, const moe_bf16* W2, int act, int flags,
                         moe_bf16* h_saved, moe_bf16* a, moe_bf16* y_perm, const moe_mx_fwd* mx,
-                        int32_t* err, void* stream) {
+                        float* amax_a, int32_t* err, void* stream) {
   g_last_launches = 0;
   int rc = check_mlp_sizes(E, M_cap, d, n);
   if (rc) return rc;
@@ -416,6 +416,7 @@ int moe_grouped_mlp_fwd(const moe_bf16* x_perm, const int32_t* offsets, int E, i
   moe::GemmArgs g1{};
   g1.offsets = offsets; g1.E = E; g1.M_cap = M_cap; g1.K = d; g1.N = n1; g1.R = 0;
   g1.out = a; g1.ldo = n; g1.out2 = save_h ? h_saved : nullptr; g1.ldo2 = n1; g1.err = err;
+  g1.amax = amax_a;
   if (use_mx) {
     g1.mx_q = mx->a_q; g1.mx_s = mx->a_s; g1.mx_qT = mx->a_qT;
     g1.mx_sT = mx->a_qT ? mx->a_sT : nullptr; g1.n_a = n;
@@ -449,7 +450,7 @@ int moe_grouped_mlp_bwd(const moe_bf16* x_perm, const moe_bf16* h_saved, const m
                         const moe_bf16* dy_perm, const int32_t* offsets, int E, int M_cap, int d,
                         int n, const moe_bf16* W1, const moe_bf16* W2, int act, int flags,
                         moe_bf16* dh, moe_bf16* dx_perm, moe_bf16* dW1, moe_bf16* dW2,
-                        int32_t* err, void* stream) {
+                        float* amax_dh, int32_t* err, void* stream) {
   g_last_launches = 0;
   int rc = check_mlp_sizes(E, M_cap, d, n);
   if (rc) return rc;
@@ -472,7 +473,7 @@ int moe_grouped_mlp_bwd(const moe_bf16* x_perm, const moe_bf16* h_saved, const m
   if (sms <= 0) return MOE_E_CUDA;
 
   return bwd_gemms(x_perm, h_saved, a, dy_perm, offsets, E, M_cap, d, n, W1, W2, act, dh, dx_perm,
-                   dW1, dW2, err, s, sms, nullptr, nullptr, nullptr, nullptr);
+                   dW1, dW2, err, s, sms, nullptr, nullptr, nullptr, nullptr, amax_dh);
 }
 
 int moe_grouped_mlp_bwd_routed(const moe_bf16* x_perm, const moe_bf16* h_saved,
@@ -480,8 +481,8 @@ int moe_grouped_mlp_bwd_routed(const moe_bf16* x_perm, const moe_bf16* h_saved,
                                const float* probs, const int32_t* offsets, int E, int M_cap,
                                int d, int n, const moe_bf16* W1, const moe_bf16* W2, int act,
                                moe_bf16* dh, moe_bf16* a_scaled, float* ds_part,
-                               moe_bf16* dx_perm, moe_bf16* dW1, moe_bf16* dW2, int32_t* err,
-                               void* stream) {
+                               moe_bf16* dx_perm, moe_bf16* dW1, moe_bf16* dW2, float* amax_dh,
+                               int32_t* err, void* stream) {
   g_last_launches = 0;
   int rc = check_mlp_sizes(E, M_cap, d, n);
   if (rc) return rc;
@@ -504,7 +505,8 @@ int moe_grouped_mlp_bwd_routed(const moe_bf16* x_perm, const moe_bf16* h_saved,
   const int sms = num_sms_current();
   if (sms <= 0) return MOE_E_CUDA;
   return bwd_gemms(x_perm, h_saved, a_scaled, do_perm, offsets, E, M_cap, d, n, W1, W2, act, dh,
-                   dx_perm, dW1, dW2, err, s, sms, pair_of_row, probs, a_scaled, ds_part);
+                   dx_perm, dW1, dW2, err, s, sms, pair_of_row, probs, a_scaled, ds_part,
+                   amax_dh);
 }
 
 int moe_router_grad_rows(const float* ds_part, int n_parts, const int32_t* row_of_pair, int T,

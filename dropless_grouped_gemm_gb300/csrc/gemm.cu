@@ -165,7 +165,7 @@ __device__ __forceinline__ void store_row32(uint16_t* p, const uint32_t (&r)[32]
 
 template <GemmKind KIND, int ACT>
 __device__ __forceinline__ void epilogue_chunk(const GemmArgs& g, const Tile& tl, int row_in_tile,
-                                               int c, const uint32_t (&r)[32]) {
+                                               int c, const uint32_t (&r)[32], float& amx) {
   const int col = tl.n0 + c * 32;  // first accumulator column of the chunk
   if (col >= g.N) return;
   if constexpr (KIND == GemmKind::kWgrad) {
@@ -185,6 +185,7 @@ __device__ __forceinline__ void epilogue_chunk(const GemmArgs& g, const Tile& tl
           const float h0 = fmaxf(__uint_as_float(r[2 * i]), 0.f);
           const float h1 = fmaxf(__uint_as_float(r[2 * i + 1]), 0.f);
           o[i] = pack_bf16x2(h0 * h0, h1 * h1);
+          amx = fmaxf(amx, fmaxf(bf16_lo(o[i]), bf16_hi(o[i])));
         }
         uint16_t* p = g.out + grow * g.ldo + col;
 #pragma unroll
@@ -196,49 +197,11 @@ __device__ __forceinline__ void epilogue_chunk(const GemmArgs& g, const Tile& tl
           const float a0 = gate_phi<ACT>(__uint_as_float(r[4 * i + 0])) * __uint_as_float(r[4 * i + 1]);
           const float a1 = gate_phi<ACT>(__uint_as_float(r[4 * i + 2])) * __uint_as_float(r[4 * i + 3]);
           o[i] = pack_bf16x2(a0, a1);
+          amx = fmaxf(amx, fmaxf(fabsf(bf16_lo(o[i])), fabsf(bf16_hi(o[i]))));
         }
         uint16_t* p = g.out + grow * g.ldo + col / 2;
         st_global_v4(p, o[0], o[1], o[2], o[3]);
         st_global_v4(p + 8, o[4], o[5], o[6], o[7]);
-      }
-    } else if constexpr (KIND == GemmKind::kDgradAct) {
-      if constexpr (ACT == MOE_ACT_SRELU) {
-        const uint16_t* hp = g.aux + grow * g.ld_aux + col;
-        uint16_t* p = g.out + grow * g.ldo + col;
-#pragma unroll
-        for (int v = 0; v < 4; ++v) {
-          const uint4 hv = *reinterpret_cast<const uint4*>(hp + 8 * v);
-          const uint32_t hw[4] = {hv.x, hv.y, hv.z, hv.w};
-          uint32_t o[4];
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const float d0 = __uint_as_float(r[8 * v + 2 * i]);
-            const float d1 = __uint_as_float(r[8 * v + 2 * i + 1]);
-            o[i] = pack_bf16x2(2.f * fmaxf(bf16_lo(hw[i]), 0.f) * d0,
-                               2.f * fmaxf(bf16_hi(hw[i]), 0.f) * d1);
-          }
-          st_global_v4(p + 8 * v, o[0], o[1], o[2], o[3]);
-        }
-      } else {
-        // dA columns j = col..col+31 -> H / dH columns 2j, 2j+1
-        const uint16_t* hp = g.aux + grow * g.ld_aux + 2 * col;
-        uint16_t* p = g.out + grow * g.ldo + 2 * col;
-#pragma unroll
-        for (int v = 0; v < 8; ++v) {
-          const uint4 hv = *reinterpret_cast<const uint4*>(hp + 8 * v);
-          const uint32_t hw[4] = {hv.x, hv.y, hv.z, hv.w};  // (g,u) pairs
-          uint32_t o[4];
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const float gg = bf16_lo(hw[i]);
-            const float uu = bf16_hi(hw[i]);
-            const float da = __uint_as_float(r[4 * v + i]);
-            float ph, dph;
-            gate_phi_dphi<ACT>(gg, ph, dph);
-            o[i] = pack_bf16x2(da * uu * dph, da * ph);
-          }
-          st_global_v4(p + 8 * v, o[0], o[1], o[2], o[3]);
-        }
       }
     } else {  // kFc2, kDgrad
       store_row32(g.out + grow * g.ldo + col, r);
@@ -246,62 +209,111 @@ __device__ __forceinline__ void epilogue_chunk(const GemmArgs& g, const Tile& tl
   }
 }
 
-// Routed FC2-dgrad epilogue ([Sonic] "역전파 계산 그래프 재작성하기": the dH
-// kernel also emits dS and A' = S*A): dA' columns col..col+31 of one row with
-// router probability p -> dH (same interleaving as H) and A' (bf16); returns
-// the chunk's part of <dA', A>, A = act(H) recomputed from the stored H.
+// FC2-dgrad + dActivation epilogue of one 32-column chunk of dA for the
+// thread's row (all 32 lanes of the warp call it together).
+//  * plain: r = dA; dH = act'(H; dA), same interleaving as H.
+//  * routed (g.probs; [Sonic] "역전파 계산 그래프 재작성하기": the dH kernel
+//    also emits dS and A' = S*A): r = dA' before the row's router
+//    probability p; dH = act'(H; p dA'), A' = p act(H) (act recomputed from
+//    the stored H); returns the chunk's part of <dA', act(H)>.
+//  * with g.amax ([CuTe] "핵심 아이디어": the amax of the transposed,
+//    Hadamard-rotated output is fused instead of a separate pass): each dH
+//    column of the warp's 32 rows is rotated in two 16-row blocks by a
+//    16-lane butterfly (H16 / 4) and its largest magnitude folded into amx.
+//    Rows past the tile's valid rows count as zero; tiles start on an
+//    expert's first row plus a multiple of 128, so the blocks run from each
+//    expert's first row.
 template <int ACT>
-__device__ __forceinline__ float dgrad_act_routed_chunk(const GemmArgs& g, long long grow, int col,
-                                                        float p, const uint32_t (&r)[32]) {
+__device__ __forceinline__ float dgrad_act_chunk(const GemmArgs& g, const Tile& tl, int row_in_tile,
+                                                 int col, float p, const uint32_t (&r)[32],
+                                                 float& amx) {
+  constexpr bool GATED = (ACT != MOE_ACT_SRELU);
+  constexpr int NV = GATED ? 64 : 32;  // dH values of the chunk
+  const bool valid = row_in_tile < tl.rows;
+  const bool routed = g.probs != nullptr;
+  const long long grow = tl.row0 + row_in_tile;
+  float dh[NV];
   float ds = 0.f;
-  uint32_t ap[16];  // A' of the chunk's 32 columns, packed bf16 pairs
-  if constexpr (ACT == MOE_ACT_SRELU) {
-    const uint16_t* hp = g.aux + grow * g.ld_aux + col;
-    uint16_t* pd = g.out + grow * g.ldo + col;
+  if (valid) {
+    uint32_t ap[16];  // routed: A' of the chunk's 32 dA columns, packed bf16 pairs
+    if constexpr (!GATED) {
+      const uint16_t* hp = g.aux + grow * g.ld_aux + col;
+      uint16_t* pd = g.out + grow * g.ldo + col;
 #pragma unroll
-    for (int v = 0; v < 4; ++v) {
-      const uint4 hv = *reinterpret_cast<const uint4*>(hp + 8 * v);
-      const uint32_t hw[4] = {hv.x, hv.y, hv.z, hv.w};
-      uint32_t o[4];
+      for (int v = 0; v < 4; ++v) {
+        const uint4 hv = *reinterpret_cast<const uint4*>(hp + 8 * v);
+        const uint32_t hw[4] = {hv.x, hv.y, hv.z, hv.w};
+        uint32_t o[4];
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const float h0 = fmaxf(bf16_lo(hw[i]), 0.f), h1 = fmaxf(bf16_hi(hw[i]), 0.f);
-        const float d0 = __uint_as_float(r[8 * v + 2 * i]), d1 = __uint_as_float(r[8 * v + 2 * i + 1]);
-        const float a0 = h0 * h0, a1 = h1 * h1;
-        ds += d0 * a0 + d1 * a1;
-        o[i] = pack_bf16x2(2.f * h0 * (p * d0), 2.f * h1 * (p * d1));
-        ap[4 * v + i] = pack_bf16x2(p * a0, p * a1);
+        for (int i = 0; i < 4; ++i) {
+          const float h0 = fmaxf(bf16_lo(hw[i]), 0.f), h1 = fmaxf(bf16_hi(hw[i]), 0.f);
+          float d0 = __uint_as_float(r[8 * v + 2 * i]), d1 = __uint_as_float(r[8 * v + 2 * i + 1]);
+          if (routed) {
+            const float a0 = h0 * h0, a1 = h1 * h1;
+            ds += d0 * a0 + d1 * a1;
+            ap[4 * v + i] = pack_bf16x2(p * a0, p * a1);
+            d0 *= p;
+            d1 *= p;
+          }
+          o[i] = pack_bf16x2(2.f * h0 * d0, 2.f * h1 * d1);
+          dh[8 * v + 2 * i] = bf16_lo(o[i]);
+          dh[8 * v + 2 * i + 1] = bf16_hi(o[i]);
+        }
+        st_global_v4(pd + 8 * v, o[0], o[1], o[2], o[3]);
       }
-      st_global_v4(pd + 8 * v, o[0], o[1], o[2], o[3]);
+    } else {
+      const uint16_t* hp = g.aux + grow * g.ld_aux + 2 * col;
+      uint16_t* pd = g.out + grow * g.ldo + 2 * col;
+#pragma unroll
+      for (int v = 0; v < 8; ++v) {
+        const uint4 hv = *reinterpret_cast<const uint4*>(hp + 8 * v);
+        const uint32_t hw[4] = {hv.x, hv.y, hv.z, hv.w};  // (gate, up) pairs
+        uint32_t o[4];
+        float a[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const float gg = bf16_lo(hw[i]), uu = bf16_hi(hw[i]);
+          float da = __uint_as_float(r[4 * v + i]);
+          float ph, dph;
+          gate_phi_dphi<ACT>(gg, ph, dph);
+          if (routed) {
+            a[i] = ph * uu;
+            ds += da * a[i];
+            da *= p;
+          }
+          o[i] = pack_bf16x2(da * uu * dph, da * ph);
+          dh[8 * v + 2 * i] = bf16_lo(o[i]);
+          dh[8 * v + 2 * i + 1] = bf16_hi(o[i]);
+        }
+        if (routed) {
+          ap[2 * v] = pack_bf16x2(p * a[0], p * a[1]);
+          ap[2 * v + 1] = pack_bf16x2(p * a[2], p * a[3]);
+        }
+        st_global_v4(pd + 8 * v, o[0], o[1], o[2], o[3]);
+      }
+    }
+    if (routed) {
+      uint16_t* pa = g.out3 + grow * g.ldo3 + col;
+#pragma unroll
+      for (int v = 0; v < 4; ++v) st_global_v4(pa + 8 * v, ap[4 * v], ap[4 * v + 1], ap[4 * v + 2], ap[4 * v + 3]);
     }
   } else {
-    const uint16_t* hp = g.aux + grow * g.ld_aux + 2 * col;
-    uint16_t* pd = g.out + grow * g.ldo + 2 * col;
 #pragma unroll
-    for (int v = 0; v < 8; ++v) {
-      const uint4 hv = *reinterpret_cast<const uint4*>(hp + 8 * v);
-      const uint32_t hw[4] = {hv.x, hv.y, hv.z, hv.w};  // (gate, up) pairs
-      uint32_t o[4];
-      float a[4];
+    for (int i = 0; i < NV; ++i) dh[i] = 0.f;
+  }
+  if (g.amax != nullptr) {
+    const int lane = threadIdx.x & 31;
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const float gg = bf16_lo(hw[i]), uu = bf16_hi(hw[i]);
-        const float dap = __uint_as_float(r[4 * v + i]);
-        float ph, dph;
-        gate_phi_dphi<ACT>(gg, ph, dph);
-        a[i] = ph * uu;
-        ds += dap * a[i];
-        const float da = p * dap;
-        o[i] = pack_bf16x2(da * uu * dph, da * ph);
+    for (int i = 0; i < NV; ++i) {
+      float x = dh[i];
+#pragma unroll
+      for (int sft = 1; sft < 16; sft <<= 1) {
+        const float o = __shfl_xor_sync(0xffffffffu, x, sft);
+        x = (lane & sft) ? (o - x) : (x + o);
       }
-      ap[2 * v] = pack_bf16x2(p * a[0], p * a[1]);
-      ap[2 * v + 1] = pack_bf16x2(p * a[2], p * a[3]);
-      st_global_v4(pd + 8 * v, o[0], o[1], o[2], o[3]);
+      amx = fmaxf(amx, 0.25f * fabsf(x));
     }
   }
-  uint16_t* pa = g.out3 + grow * g.ldo3 + col;
-#pragma unroll
-  for (int v = 0; v < 4; ++v) st_global_v4(pa + 8 * v, ap[4 * v], ap[4 * v + 1], ap[4 * v + 2], ap[4 * v + 3]);
   return ds;
 }
 
@@ -311,7 +323,7 @@ __device__ __forceinline__ float dgrad_act_routed_chunk(const GemmArgs& g, long 
 template <int ACT>
 __device__ __forceinline__ void fc1_mx_block(const GemmArgs& g, const Tile& tl, int row_in_tile,
                                              int lane, int q, int cb, const uint32_t (&r0)[32],
-                                             const uint32_t (&r1)[32]) {
+                                             const uint32_t (&r1)[32], float& amx) {
   constexpr bool GATED = (ACT != MOE_ACT_SRELU);
   const int acc_col = tl.n0 + cb * (GATED ? 64 : 32);
   if (acc_col >= g.N) return;                       // uniform across the CTA
@@ -343,6 +355,8 @@ __device__ __forceinline__ void fc1_mx_block(const GemmArgs& g, const Tile& tl, 
   uint32_t qw[8];
   const uint32_t sc = mx_quant32(a, qw);
   if (valid) {
+#pragma unroll
+    for (int i = 0; i < 32; ++i) amx = fmaxf(amx, fabsf(a[i]));
     uint16_t* pa = g.out + grow * g.ldo + acol;
 #pragma unroll
     for (int v = 0; v < 4; ++v) st_global_v4(pa + 8 * v, pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
@@ -619,6 +633,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const int row_in_tile = q * 32 + lane;
     int local = 0;
     uint32_t stg_slot = 0;
+    float amx = 0.f;                   // NVFP4 statistic of this thread's outputs
     for (int t = unit0; t < total_tiles; t += unit_step, ++local) {
       const Tile tl = decode_tile<KIND, CL>(g, s_off, s_ts, t, rank);
       const int buf = local & 1;
@@ -635,7 +650,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           tmem_ld32(tb + cb * STEP, r0);
           if constexpr (STEP == 64) tmem_ld32(tb + cb * STEP + 32, r1);
           tmem_wait_ld();
-          fc1_mx_block<ACT>(g, tl, row_in_tile, lane, q, cb, r0, r1);
+          fc1_mx_block<ACT>(g, tl, row_in_tile, lane, q, cb, r0, r1, amx);
         }
       } else if (KIND == GemmKind::kWgrad && tl.m0 + q * 32 + 32 <= g.R && tl.kblocks == 0) {
         // expert with no rows: its weight gradient is zero; store the zero box
@@ -695,13 +710,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         uint32_t z[32];
 #pragma unroll
         for (int i = 0; i < 32; ++i) z[i] = 0;
-        for (int c = wg * 4; c < wg * 4 + 4; ++c) epilogue_chunk<KIND, ACT>(g, tl, row_in_tile, c, z);
-      } else if (KIND == GemmKind::kDgradAct && g.probs != nullptr) {
-        // routed: this thread's row, the warpgroup's 128 columns
+        for (int c = wg * 4; c < wg * 4 + 4; ++c) epilogue_chunk<KIND, ACT>(g, tl, row_in_tile, c, z, amx);
+      } else if constexpr (KIND == GemmKind::kDgradAct) {
+        // this thread's row, the warpgroup's 128 columns (whole warps call
+        // dgrad_act_chunk: the amax butterflies span the warp's rows)
         const bool vrow = row_in_tile < tl.rows;
         const long long grow = tl.row0 + row_in_tile;
         float p = 0.f, dsum = 0.f;
-        if (vrow) {
+        if (g.probs != nullptr && vrow) {
           const int pr = g.pair_of_row[grow];
           p = pr >= 0 ? g.probs[pr] : 0.f;
         }
@@ -710,16 +726,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           tmem_ld32(tb + c * 32, r);
           tmem_wait_ld();
           const int col = tl.n0 + c * 32;
-          if (vrow && col < g.N) dsum += dgrad_act_routed_chunk<ACT>(g, grow, col, p, r);
+          if (col < g.N) dsum += dgrad_act_chunk<ACT>(g, tl, row_in_tile, col, p, r, amx);
         }
         const int half = tl.n0 + wg * 128;
-        if (vrow && half < g.N) g.ds_part[grow * g.ds_parts + half / 128] = dsum;
+        if (g.probs != nullptr && vrow && half < g.N) g.ds_part[grow * g.ds_parts + half / 128] = dsum;
       } else {
         for (int c = wg * 4; c < wg * 4 + 4; ++c) {
           uint32_t r[32];
           tmem_ld32(tb + c * 32, r);
           tmem_wait_ld();
-          epilogue_chunk<KIND, ACT>(g, tl, row_in_tile, c, r);
+          epilogue_chunk<KIND, ACT>(g, tl, row_in_tile, c, r, amx);
         }
       }
       tc_fence_before();
@@ -727,6 +743,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       if (lane == 0) mbar_arrive(&tempty_bar[buf]);
     }
     if (KIND == GemmKind::kWgrad && lane == 0) bulk_wait_all();  // staged stores done
+    if ((KIND == GemmKind::kFc1Act || KIND == GemmKind::kDgradAct) && g.amax != nullptr) {
+      // non-negative floats order like their bit patterns
+      const uint32_t m = __reduce_max_sync(0xffffffffu, __float_as_uint(amx));
+      if (lane == 0 && m != 0u) atomicMax(reinterpret_cast<unsigned int*>(g.amax), m);
+    }
     __syncwarp();
   }
 

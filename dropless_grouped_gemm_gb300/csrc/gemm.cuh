@@ -49,6 +49,10 @@ struct GemmArgs {
   long long ldo3;
   float* ds_part;              // [M_cap, ds_parts] fp32
   int ds_parts;
+  // optional NVFP4 statistic, raised with atomicMax (the caller sets the
+  // start value): kFc1Act max |A| of the bf16 A; kDgradAct max over 16-row
+  // blocks (from each expert's first row) of |H16 dH| / 4 per dH column
+  float* amax;
   // unit order inside an expert, set by launch_grouped_gemm: 0 = row pairs
   // outermost (a wave of CTAs sweeps every column tile of B), 1 = column
   // tiles outermost (a wave reuses each B column tile across all row pairs)

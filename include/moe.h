@@ -290,12 +290,19 @@ int moe_unpermute(const moe_bf16* src, const float* probs,
  * Requires n and d multiples of 128, M_cap a multiple of 32 and offsets
  * that are multiples of 32 (route with align = 32; otherwise
  * MOE_DEV_BAD_OFFSETS is set).
+ *
+ * amax_a (device float, or NULL): NVFP4's per-tensor statistic of the
+ * forward output ([CuTe] "핵심 아이디어 / 구조 / 동작 방식": computed in the
+ * GEMM instead of a separate memory pass).  The epilogue raises *amax_a to
+ * max |A| over the bf16 A it writes (atomic maximum; the caller sets the
+ * start value, e.g. 0).
  */
 int moe_grouped_mlp_fwd(const moe_bf16* x_perm, const int32_t* offsets,
                         int E, int M_cap, int d, int n, const moe_bf16* W1,
                         const moe_bf16* W2, int act, int flags,
                         moe_bf16* h_saved, moe_bf16* a, moe_bf16* y_perm,
-                        const moe_mx_fwd* mx, int32_t* err, void* stream);
+                        const moe_mx_fwd* mx, float* amax_a, int32_t* err,
+                        void* stream);
 
 /*
  * moe_grouped_mlp_bwd - backward of moe_grouped_mlp_fwd.
@@ -316,14 +323,22 @@ int moe_grouped_mlp_fwd(const moe_bf16* x_perm, const int32_t* offsets,
  *   x_perm [M_cap, d], h_saved [M_cap, n1], a [M_cap, n], dy_perm [M_cap, d]
  *   dh [M_cap, n1] (written), dx_perm [M_cap, d] (written),
  *   dW1 [E, d, n1] (written), dW2 [E, n, d] (written); all bf16.
+ *
+ * amax_dh (device float, or NULL): NVFP4's backward statistic, the amax of
+ * the transposed, Hadamard-rotated dH, taken in the dH epilogue.  Per
+ * expert, dH's rows are cut into 16-row blocks from the expert's first row
+ * (the last one zero-padded) and each column of a block is multiplied by
+ * the orthonormal 16x16 Hadamard matrix (Sylvester order, entries +-1/4);
+ * *amax_dh is raised to the largest magnitude (atomic maximum; the caller
+ * sets the start value).
  */
 int moe_grouped_mlp_bwd(const moe_bf16* x_perm, const moe_bf16* h_saved,
                         const moe_bf16* a, const moe_bf16* dy_perm,
                         const int32_t* offsets, int E, int M_cap, int d,
                         int n, const moe_bf16* W1, const moe_bf16* W2,
                         int act, int flags, moe_bf16* dh, moe_bf16* dx_perm,
-                        moe_bf16* dW1, moe_bf16* dW2, int32_t* err,
-                        void* stream);
+                        moe_bf16* dW1, moe_bf16* dW2, float* amax_dh,
+                        int32_t* err, void* stream);
 
 /*
  * moe_grouped_mlp_bwd_routed - backward with the router-score gradient
@@ -337,7 +352,7 @@ int moe_grouped_mlp_bwd(const moe_bf16* x_perm, const moe_bf16* h_saved,
  *   a_scaled [M_cap, n] = p * act(H) (bf16) and ds_part [M_cap, ceil(n/128)]
  *   (fp32 partial <dA', act(H)> of each 128-column half tile, caller-owned
  *   scratch); FC2-wgrad then contracts a_scaled with do_perm.  dx_perm, dW1,
- *   dW2 as in moe_grouped_mlp_bwd.  Four launches; finish with
+ *   dW2 and amax_dh as in moe_grouped_mlp_bwd.  Four launches; finish with
  *   moe_router_grad_rows.  Errors as moe_grouped_mlp_bwd.
  */
 int moe_grouped_mlp_bwd_routed(const moe_bf16* x_perm, const moe_bf16* h_saved,
@@ -346,8 +361,8 @@ int moe_grouped_mlp_bwd_routed(const moe_bf16* x_perm, const moe_bf16* h_saved,
                                int M_cap, int d, int n, const moe_bf16* W1,
                                const moe_bf16* W2, int act, moe_bf16* dh,
                                moe_bf16* a_scaled, float* ds_part, moe_bf16* dx_perm,
-                               moe_bf16* dW1, moe_bf16* dW2, int32_t* err,
-                               void* stream);
+                               moe_bf16* dW1, moe_bf16* dW2, float* amax_dh,
+                               int32_t* err, void* stream);
 
 /*
  * moe_router_grad_rows - dprobs [T*k] (fp32) of the routed backward:

@@ -39,13 +39,13 @@ def test_host_argument_errors(L):
     vp = ctypes.c_void_p
     # E = 0, k > E, bad align: rejected before anything touches the GPU
     assert L.moe_grouped_mlp_fwd(None, None, 0, 0, 64, 64, None, None, 0, 0, None, None, None,
-                                 None, None, None) == -3
+                                 None, None, None, None) == -3
     assert L.moe_grouped_mlp_fwd(None, None, 4, 128, 96, 64, None, None, 0, 0, None, None, None,
-                                 None, None, None) == -3    # d not a multiple of 64
+                                 None, None, None, None) == -3    # d not a multiple of 64
     assert L.moe_grouped_mlp_fwd(None, None, 4, 128, 64, 64, None, None, 7, 0, None, None, None,
-                                 None, None, None) == -4    # bad act
+                                 None, None, None, None) == -4    # bad act
     assert L.moe_grouped_mlp_fwd(None, None, 4, 128, 64, 64, None, None, 0, 2, None, None, None,
-                                 None, None, None) == -1    # MXFP8 without its buffers
+                                 None, None, None, None) == -1    # MXFP8 without its buffers
     assert L.moe_mx_quantize_weights(None, 4, 96, 128, None, None, None) == -3
     assert L.moe_mx_quantize(None, 64, 48, None, 2, None, None, None, None, None, None) == -3
     assert L.moe_route_offsets(None, 4, 3, 2, 1, 12, None, None, None, None, None, None, 0, None,
