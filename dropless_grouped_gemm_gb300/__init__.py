@@ -48,14 +48,16 @@ class MoeError(RuntimeError):
 class MxFwd(ctypes.Structure):
     """moe_mx_fwd: MXFP8 buffers of the forward (device pointers)."""
     _fields_ = [("w2_q", ctypes.c_void_p), ("w2_s", ctypes.c_void_p), ("a_q", ctypes.c_void_p),
-                ("a_s", ctypes.c_void_p), ("a_qT", ctypes.c_void_p), ("a_sT", ctypes.c_void_p)]
+                ("a_s", ctypes.c_void_p), ("a_qT", ctypes.c_void_p), ("a_sT", ctypes.c_void_p),
+                ("y_q", ctypes.c_void_p), ("y_s", ctypes.c_void_p)]
 
 
 class MxBwd(ctypes.Structure):
     """moe_mx_bwd: MXFP8 operands and workspace of the backward (device pointers)."""
     _fields_ = [("a_qT", ctypes.c_void_p), ("a_sT", ctypes.c_void_p), ("w2_q", ctypes.c_void_p),
                 ("w2_s", ctypes.c_void_p), ("w1_q", ctypes.c_void_p), ("w1_s", ctypes.c_void_p),
-                ("workspace", ctypes.c_void_p), ("ws_bytes", ctypes.c_size_t)]
+                ("workspace", ctypes.c_void_p), ("ws_bytes", ctypes.c_size_t),
+                ("dx_q", ctypes.c_void_p), ("dx_s", ctypes.c_void_p)]
 
 
 def lib_path() -> str:
@@ -281,10 +283,10 @@ def grouped_mlp_fwd(x_perm: torch.Tensor, offsets: torch.Tensor, W1: torch.Tenso
     flags = FLAG_SAVE_H if save_h else 0
     mxs = None
     if mx is not None:
-        for k_ in ("w2_q", "w2_s", "a_q", "a_s", "a_qT", "a_sT"):
+        names = ("w2_q", "w2_s", "a_q", "a_s", "a_qT", "a_sT", "y_q", "y_s")
+        for k_ in names:
             _need(mx.get(k_), torch.uint8, k_)
-        mxs = MxFwd(*[(mx[k_].data_ptr() if mx.get(k_) is not None else None)
-                      for k_ in ("w2_q", "w2_s", "a_q", "a_s", "a_qT", "a_sT")])
+        mxs = MxFwd(*[(mx[k_].data_ptr() if mx.get(k_) is not None else None) for k_ in names])
         flags |= FLAG_MXFP8
     rc = lib().moe_grouped_mlp_fwd(_ptr(x_perm), _ptr(offsets), E, M_cap, d, n, _ptr(W1), _ptr(W2),
                                    ACT[act], flags, _ptr(h_saved) if save_h else None, _ptr(a),
@@ -323,7 +325,8 @@ def grouped_mlp_bwd(x_perm, h_saved, a, dy_perm, offsets, W1, W2, act: str = "sw
     return dh, dx_perm, dW1, dW2, err
 
 
-def mx_buffers(E: int, n: int, d: int, M_cap: int, device, transposed: bool = True) -> dict:
+def mx_buffers(E: int, n: int, d: int, M_cap: int, device, transposed: bool = True,
+               quantize_y: bool = False) -> dict:
     """Allocate the uint8 buffers of moe_mx_fwd (sizes as moe.h states)."""
     u8 = torch.uint8
     b = {"w2_q": torch.empty((E, n, d), dtype=u8, device=device),
@@ -333,6 +336,9 @@ def mx_buffers(E: int, n: int, d: int, M_cap: int, device, transposed: bool = Tr
     if transposed:
         b["a_qT"] = torch.empty((n, M_cap), dtype=u8, device=device)
         b["a_sT"] = torch.empty((n, M_cap // 32), dtype=u8, device=device)
+    if quantize_y:
+        b["y_q"] = torch.empty((M_cap, d), dtype=u8, device=device)
+        b["y_s"] = torch.empty((M_cap, d // 32), dtype=u8, device=device)
     return b
 
 
@@ -423,9 +429,13 @@ def grouped_mlp_bwd_mx(x_perm, h_saved, dy_perm, offsets, mx: dict, act: str = "
     if workspace is None:
         workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=dev)
     _need(workspace, torch.uint8, "workspace")
+    for k_ in ("dx_q", "dx_s"):
+        _need(mx.get(k_), torch.uint8, k_)
     st = MxBwd(mx["a_qT"].data_ptr(), mx["a_sT"].data_ptr(), mx["w2_q"].data_ptr(),
                mx["w2_s"].data_ptr(), mx["w1_q"].data_ptr(), mx["w1_s"].data_ptr(),
-               workspace.data_ptr(), workspace.numel())
+               workspace.data_ptr(), workspace.numel(),
+               mx["dx_q"].data_ptr() if mx.get("dx_q") is not None else None,
+               mx["dx_s"].data_ptr() if mx.get("dx_s") is not None else None)
     rc = lib().moe_grouped_mlp_bwd_mx(_ptr(x_perm), _ptr(h_saved), _ptr(dy_perm), _ptr(offsets),
                                       E, M_cap, d, n, ACT[act], ctypes.byref(st), _ptr(dh),
                                       _ptr(dx_perm), _ptr(dW1), _ptr(dW2), _ptr(err),

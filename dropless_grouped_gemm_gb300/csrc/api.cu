@@ -387,8 +387,10 @@ int moe_grouped_mlp_fwd(const moe_bf16* x_perm, const int32_t* offsets, int E, i
   const bool save_h = flags & MOE_FLAG_SAVE_H;
   const bool use_mx = flags & MOE_FLAG_MXFP8;
   if (use_mx) {
-    if (!mx || !mx->w2_q || !mx->w2_s || !mx->a_q || !mx->a_s || (mx->a_qT && !mx->a_sT))
+    if (!mx || !mx->w2_q || !mx->w2_s || !mx->a_q || !mx->a_s || (mx->a_qT && !mx->a_sT) ||
+        (mx->y_q && !mx->y_s))
       return MOE_E_NULL;
+    if (misaligned(mx->y_q)) return MOE_E_ALIGN;
     if (n % 128 || d % 128 || M_cap % 32) return MOE_E_SIZE;
     if (misaligned(mx->w2_q) || misaligned(mx->w2_s) || misaligned(mx->a_q) ||
         misaligned(mx->a_s) || misaligned(mx->a_qT))
@@ -430,6 +432,7 @@ int moe_grouped_mlp_fwd(const moe_bf16* x_perm, const int32_t* offsets, int E, i
     moe::MxGemmArgs q{};
     q.offsets = offsets; q.E = E; q.M_cap = M_cap; q.K = n; q.N = d;
     q.a_s = mx->a_s; q.b_s = mx->w2_s; q.out = y_perm; q.ldo = d; q.err = err;
+    q.q_out = mx->y_q; q.s_out = mx->y_q ? mx->y_s : nullptr;
     ev_begin(s);
     e = moe::launch_mx_gemm(moe::MxKind::kFc2, 0, ta, tw2, ta, q, sms, s);
     ev_end(s);
@@ -583,8 +586,10 @@ int moe_grouped_mlp_bwd_mx(const moe_bf16* x_perm, const moe_bf16* h_saved,
     return cuda_rc(e);
   }
   if (!x_perm || !h_saved || !dy_perm || !dh || !dx_perm || !mx->a_qT || !mx->a_sT ||
-      !mx->w2_q || !mx->w2_s || !mx->w1_q || !mx->w1_s || !mx->workspace)
+      !mx->w2_q || !mx->w2_s || !mx->w1_q || !mx->w1_s || !mx->workspace ||
+      (mx->dx_q && !mx->dx_s))
     return MOE_E_NULL;
+  if (misaligned(mx->dx_q)) return MOE_E_ALIGN;
   if (misaligned(x_perm) || misaligned(h_saved) || misaligned(dy_perm) || misaligned(dh) ||
       misaligned(dx_perm) || misaligned(dW1) || misaligned(dW2) || misaligned(mx->a_qT) ||
       misaligned(mx->w2_q) || misaligned(mx->w2_s) || misaligned(mx->w1_q) ||
@@ -643,6 +648,7 @@ int moe_grouped_mlp_bwd_mx(const moe_bf16* x_perm, const moe_bf16* h_saved,
   moe::MxGemmArgs gd{};
   gd.offsets = offsets; gd.E = E; gd.M_cap = M_cap; gd.K = n1; gd.N = d;
   gd.a_s = ws.dh_s; gd.b_s = mx->w1_s; gd.out = dx_perm; gd.ldo = d; gd.err = err;
+  gd.q_out = mx->dx_q; gd.s_out = mx->dx_q ? mx->dx_s : nullptr;
   e = mx_gemm(moe::MxKind::kDgrad, 0, t_dh, t_w1, t_dh, gd, sms, s);
   if (e != cudaSuccess) return MOE_E_CUDA;
   // 8. dW1_e = X_e^T dH_e

@@ -382,6 +382,29 @@ __device__ __forceinline__ void mx_store_row32(uint16_t* p, const uint32_t (&v)[
         pack_bf16x2(__uint_as_float(v[8 * k + 6]), __uint_as_float(v[8 * k + 7])));
 }
 
+// GroupGemm + Quantize ([TE] "다음 단계: NVFP4, GEMM 융합 양자화, A2A 오버랩"):
+// 32 fp32 accumulator columns of one row -> 32 bf16 at p, and the row-wise
+// MXFP8 block of those bf16 values: 32 codes at q, the E8M0 scale at *s
+__device__ __forceinline__ void mx_store_quant_row32(uint16_t* p, uint8_t* q, uint8_t* s,
+                                                     const uint32_t (&v)[32]) {
+  uint32_t pk[16];
+  float f[32];
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    pk[i] = pack_bf16x2(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]));
+    f[2 * i] = bf16_lo(pk[i]);
+    f[2 * i + 1] = bf16_hi(pk[i]);
+  }
+#pragma unroll
+  for (int k = 0; k < 4; ++k)
+    *reinterpret_cast<uint4*>(p + 8 * k) = make_uint4(pk[4 * k], pk[4 * k + 1], pk[4 * k + 2], pk[4 * k + 3]);
+  uint32_t qw[8];
+  *s = static_cast<uint8_t>(mx_quant32(f, qw));
+  uint4* pq = reinterpret_cast<uint4*>(q);
+  pq[0] = make_uint4(qw[0], qw[1], qw[2], qw[3]);
+  pq[1] = make_uint4(qw[4], qw[5], qw[6], qw[7]);
+}
+
 // dA columns col..col+31 of one row -> dH (same interleaving as H)
 template <int ACT>
 __device__ __forceinline__ void mx_dact_row32(const MxGemmArgs& g, long long grow, int col,
@@ -426,7 +449,7 @@ __device__ __forceinline__ void mx_dact_row32(const MxGemmArgs& g, long long gro
 // owner and MMA issuer (tcgen05.mma ... block_scale; the scale chunks of a
 // stage go to TMEM with tcgen05.cp), warps 2-9 epilogue in two warpgroups,
 // one per 128-column half of the tile.
-template <MxKind KIND, int ACT>
+template <MxKind KIND, int ACT, bool QOUT>
 __global__ void __launch_bounds__(QTHREADS, 1)
     mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmC, const MxGemmArgs g) {
@@ -696,6 +719,10 @@ __global__ void __launch_bounds__(QTHREADS, 1)
 #pragma unroll
           for (int c = 0; c < 4; ++c) {
             if constexpr (KIND == MxKind::kDgradAct) mx_dact_row32<ACT>(g, grow, col0 + c * 32, v[c]);
+            else if (QOUT)
+              mx_store_quant_row32(g.out + grow * g.ldo + col0 + c * 32,
+                                   g.q_out + grow * g.N + col0 + c * 32,
+                                   g.s_out + grow * (g.N / 32) + (col0 + c * 32) / 32, v[c]);
             else mx_store_row32(g.out + grow * g.ldo + col0 + c * 32, v[c]);
           }
         }
@@ -713,10 +740,10 @@ __global__ void __launch_bounds__(QTHREADS, 1)
   }
 }
 
-template <MxKind KIND, int ACT>
+template <MxKind KIND, int ACT, bool QOUT = false>
 cudaError_t launch_mx_t(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tc,
                         const MxGemmArgs& g, int num_sms, cudaStream_t st) {
-  auto kern = mx_gemm_kernel<KIND, ACT>;
+  auto kern = mx_gemm_kernel<KIND, ACT, QOUT>;
   const size_t smem = mx_smem_bytes<KIND>(MOE_MAX_EXPERTS);
   static bool attr = false;  // per instantiation; the library drives one device
   if (!attr) {
@@ -779,8 +806,14 @@ cudaError_t launch_mx_gemm(MxKind kind, int act, const CUtensorMap& ta, const CU
                            const CUtensorMap& tc, const MxGemmArgs& g, int num_sms,
                            cudaStream_t st) {
   switch (kind) {
-    case MxKind::kFc2: return launch_mx_t<MxKind::kFc2, 0>(ta, tb, tc, g, num_sms, st);
-    case MxKind::kDgrad: return launch_mx_t<MxKind::kDgrad, 0>(ta, tb, tc, g, num_sms, st);
+    // the quantising epilogue (GroupGemm + Quantize) is its own instantiation,
+    // so that the plain one keeps its registers
+    case MxKind::kFc2:
+      return g.q_out ? launch_mx_t<MxKind::kFc2, 0, true>(ta, tb, tc, g, num_sms, st)
+                     : launch_mx_t<MxKind::kFc2, 0>(ta, tb, tc, g, num_sms, st);
+    case MxKind::kDgrad:
+      return g.q_out ? launch_mx_t<MxKind::kDgrad, 0, true>(ta, tb, tc, g, num_sms, st)
+                     : launch_mx_t<MxKind::kDgrad, 0>(ta, tb, tc, g, num_sms, st);
     case MxKind::kWgrad: return launch_mx_t<MxKind::kWgrad, 0>(ta, tb, tc, g, num_sms, st);
     case MxKind::kDgradAct:
       switch (act) {

@@ -45,6 +45,10 @@ struct MxGemmArgs {
   long long ldo;
   const uint16_t* aux;     // kDgradAct: H [M_cap, ld_aux]
   long long ld_aux;
+  // kFc2 / kDgrad, optional (q_out == nullptr: none): row-wise MXFP8 copy of
+  // the bf16 output - codes [M_cap, N], plain E8M0 scales [M_cap, N/32]
+  uint8_t* q_out;
+  uint8_t* s_out;
   int32_t* err;
 };
 

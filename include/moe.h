@@ -101,6 +101,9 @@ typedef struct moe_mx_fwd {
   uint8_t* a_qT;        /* [n, M_cap] codes of A^T, 32x1 blocks inside one expert,
                            or NULL (then a_sT is ignored)                          */
   uint8_t* a_sT;        /* [n, M_cap/32] E8M0 scales of a_qT                       */
+  uint8_t* y_q;         /* GroupGemm + Quantize: [M_cap, d] codes of the bf16 Y,
+                           row-wise 1x32 blocks, written by FC2's epilogue; or NULL */
+  uint8_t* y_s;         /* [M_cap, d/32] E8M0 scales of y_q                        */
 } moe_mx_fwd;
 
 /*
@@ -130,6 +133,9 @@ typedef struct moe_mx_bwd {
   const uint8_t* w1_s;  /* weight tiles, E*d*n1/32 bytes                           */
   void* workspace;      /* device scratch, 256-byte aligned, owned by the caller   */
   size_t ws_bytes;      /* >= moe_mx_bwd_workspace_size(M_cap, d, n, act)          */
+  uint8_t* dx_q;        /* GroupGemm + Quantize: [M_cap, d] codes of the bf16 dX,
+                           row-wise 1x32 blocks, written by FC1-dgrad; or NULL      */
+  uint8_t* dx_s;        /* [M_cap, d/32] E8M0 scales of dx_q                       */
 } moe_mx_bwd;
 
 /* Limits. */

@@ -172,3 +172,42 @@ def test_mx_requires_32_aligned_offsets():
     _, _, _, err = M.grouped_mlp_fwd(x2, cuda_i32(off), W1, W2, "swiglu", mx=buf)
     torch.cuda.synchronize()
     assert int(err.item()) & M.DEV_BAD_OFFSETS
+
+
+def test_group_gemm_quantize_outputs():
+    """GroupGemm + Quantize: FC2's epilogue (forward) and FC1-dgrad's (MXFP8
+    backward) also write the row-wise MXFP8 copy of the bf16 they store.
+    The codes and scales equal the OCP MX quantiser applied to that bf16
+    output, bit for bit, on every row inside an expert."""
+    M = _lib()
+    import dropless_grouped_gemm_gb300 as MM
+    E, d, n = 4, 256, 128
+    counts = [128, 0, 96, 64]
+    off = np.concatenate([[0], np.cumsum(counts)]).astype(np.int64)
+    M_cap = int(off[-1]) + 32
+    R = int(off[-1])
+    x = WL.normal((M_cap, d), (81, WL.X, 0), 1.0, "cuda")
+    W1 = WL.w1_interleaved(81, E, d, n, 0.05, "cuda")
+    W2 = WL.w2(81, E, n, d, 0.05, "cuda")
+    offs = cuda_i32(off)
+    bufs = MM.mx_buffers(E, n, d, M_cap, "cuda", quantize_y=True)
+    MM.mx_quantize_weights(W2, bufs["w2_q"], bufs["w2_s"])
+    h, a, y, err = MM.grouped_mlp_fwd(x, offs, W1, W2, "swiglu", save_h=True, mx=bufs)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    q, s = O.mx_quantize_rows(f64(y)[:R])
+    assert np.array_equal(bufs["y_q"][:R].cpu().numpy(), q)
+    assert np.array_equal(bufs["y_s"][:R].cpu().numpy(), s)
+    # backward: dX of FC1-dgrad
+    dy = WL.normal((M_cap, d), (81, WL.DY, 0), 1.0, "cuda")
+    w2q, w2s = MM.mx_quantize_weights_rowwise(W2)
+    w1q, w1s = MM.mx_quantize_weights_rowwise(W1)
+    ops = dict(a_qT=bufs["a_qT"], a_sT=bufs["a_sT"], w2_q=w2q, w2_s=w2s, w1_q=w1q, w1_s=w1s,
+               dx_q=torch.empty((M_cap, d), dtype=torch.uint8, device="cuda"),
+               dx_s=torch.empty((M_cap, d // 32), dtype=torch.uint8, device="cuda"))
+    _, dx, _, _, err = MM.grouped_mlp_bwd_mx(x, h, dy, offs, ops, "swiglu")
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    q, s = O.mx_quantize_rows(f64(dx)[:R])
+    assert np.array_equal(ops["dx_q"][:R].cpu().numpy(), q)
+    assert np.array_equal(ops["dx_s"][:R].cpu().numpy(), s)
