@@ -46,9 +46,8 @@ DEFAULT_WORKLOAD = "balanced_e8_m4096_k8192_n4096_swiglu"
 KERNELS_FWD = ["fc1_act", "fc2"]
 KERNELS_BWD = ["fc2_dgrad_dact", "fc2_wgrad", "fc1_dgrad", "fc1_wgrad"]
 # launch order of the MXFP8 backward (weight quantisers, then moe_grouped_mlp_bwd_mx)
-KERNELS_MX_BWD = ["mx_quantize_w2_rows", "mx_quantize_w1_rows", "mx_quantize_dy", "mx_quantize_x",
-                  "mx_retile_a", "fc2_dgrad_dact", "mx_quantize_dh", "fc2_wgrad", "fc1_dgrad",
-                  "fc1_wgrad"]
+KERNELS_MX_BWD = ["mx_quantize_w1_rows", "mx_quantize_dy", "mx_quantize_x", "mx_retile_a",
+                  "fc2_dgrad_dact", "mx_quantize_dh", "fc2_wgrad", "fc1_dgrad", "fc1_wgrad"]
 
 
 # ---------------------------------------------------------------- accounting
@@ -81,7 +80,8 @@ def kernel_work(w, M, E_ne):
         }
         if w.backward:
             work.update({
-                "mx_quantize_w2_rows": (0, E * n * d * 2 + mxb(E * n * d)),
+                # W2 read once, both MXFP8 copies written
+                "mx_quantize_weights2": (0, E * n * d * 2 + 2 * mxb(E * n * d)),
                 "mx_quantize_w1_rows": (0, E * d * n1 * 2 + mxb(E * d * n1)),
                 "mx_quantize_dy": (0, B * M * d + 2 * mxb(M * d)),
                 "mx_quantize_x": (0, B * M * d + mxb(M * d)),
@@ -271,18 +271,18 @@ def make_step(w, inp, o):
         """MXFP8 backward: weights quantised along their data-gradient
         reduction index, then the eight launches of grouped_mlp_bwd_mx."""
         mx, mb = o["mx"], o["mxb"]
-        M.mx_quantize_weights_rowwise(inp["W2"], mb["w2_q"], mb["w2_s"])
         M.mx_quantize_weights_rowwise(inp["W1"], mb["w1_q"], mb["w1_s"])
         ops = dict(a_qT=mx["a_qT"], a_sT=mx["a_sT"], w2_q=mb["w2_q"], w2_s=mb["w2_s"],
                    w1_q=mb["w1_q"], w1_s=mb["w1_s"])
         M.grouped_mlp_bwd_mx(x_perm, o["h"], dy_perm, offsets, ops, act, dh=o["dh"],
                              dx_perm=o["dx_perm"], dW1=o["dW1"], dW2=o["dW2"], err=o["err"],
                              workspace=mb["ws"])
-        return 2 + M.last_launch_count()
+        return 1 + M.last_launch_count()
 
     if w.routing == "identity" and w.mxfp8:
         def step_mx_id():
-            M.mx_quantize_weights(inp["W2"], o["mx"]["w2_q"], o["mx"]["w2_s"])
+            M.mx_quantize_weights2(inp["W2"], o["mx"]["w2_q"], o["mx"]["w2_s"], o["mxb"]["w2_q"],
+                                   o["mxb"]["w2_s"])
             n = M.last_launch_count()
             M.grouped_mlp_fwd(inp["x_perm"], inp["offsets"], inp["W1"], inp["W2"], act,
                               save_h=True, h_saved=o["h"], a=o["a"], y_perm=o["y_perm"],
@@ -313,7 +313,8 @@ def make_step(w, inp, o):
             n += M.last_launch_count()
             M.permute(inp["x"], r["pair_of_row"], k, out=o["x_perm"])
             n += M.last_launch_count()
-            M.mx_quantize_weights(inp["W2"], o["mx"]["w2_q"], o["mx"]["w2_s"])
+            M.mx_quantize_weights2(inp["W2"], o["mx"]["w2_q"], o["mx"]["w2_s"], o["mxb"]["w2_q"],
+                                   o["mxb"]["w2_s"])
             n += M.last_launch_count()
             M.grouped_mlp_fwd(o["x_perm"], r["offsets"], inp["W1"], inp["W2"], act, save_h=True,
                               h_saved=o["h"], a=o["a"], y_perm=o["y_perm"], err=o["err"],
@@ -385,8 +386,8 @@ def make_step(w, inp, o):
 def event_names(w):
     if w.mxfp8 and w.backward:
         if w.routing == "identity":
-            return ["mx_quantize_weights"] + KERNELS_FWD + KERNELS_MX_BWD
-        return (["route", "permute", "mx_quantize_weights"] + KERNELS_FWD +
+            return ["mx_quantize_weights2"] + KERNELS_FWD + KERNELS_MX_BWD
+        return (["route", "permute", "mx_quantize_weights2"] + KERNELS_FWD +
                 ["combine", "permute_bwd", "router_grad"] + KERNELS_MX_BWD + ["unpermute_bwd"])
     if w.routing == "identity":
         return KERNELS_FWD + KERNELS_BWD

@@ -27,7 +27,7 @@ __all__ = [
     "permute", "unpermute", "grouped_mlp_fwd", "grouped_mlp_bwd", "MoeError",
     "FLAG_MXFP8", "MxFwd", "mx_quantize_weights", "mx_quantize", "mx_buffers",
     "MxBwd", "mx_quantize_weights_rowwise", "mx_bwd_workspace_size", "grouped_mlp_bwd_mx",
-    "grouped_mlp_bwd_routed", "router_grad_rows",
+    "grouped_mlp_bwd_routed", "router_grad_rows", "mx_quantize_weights2",
 ]
 
 ACT = {"swiglu": 0, "geglu": 1, "srelu": 2}
@@ -102,6 +102,8 @@ def lib():
         L.moe_grouped_mlp_bwd.restype = i32
         L.moe_grouped_mlp_bwd.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, vp, vp, i32, i32,
                                           vp, vp, vp, vp, vp, vp, vp]
+        L.moe_mx_quantize_weights2.restype = i32
+        L.moe_mx_quantize_weights2.argtypes = [vp, i32, i32, i32, vp, vp, vp, vp, vp]
         L.moe_mx_quantize_weights_rowwise.restype = i32
         L.moe_mx_quantize_weights_rowwise.argtypes = [vp, i32, i32, vp, vp, vp]
         L.moe_mx_bwd_workspace_size.restype = sz
@@ -493,3 +495,28 @@ def router_grad_rows(ds_part, row_of_pair, T: int, k: int, dprobs=None, stream=N
                                     _ptr(dprobs), _stream(stream))
     _check(rc, "moe_router_grad_rows")
     return dprobs
+
+
+def mx_quantize_weights2(W2: torch.Tensor, w2_q=None, w2_s=None, w2_q_rows=None, w2_s_rows=None,
+                         stream=None):
+    """Both MXFP8 copies of W2 [E, n, d] from one read (moe_mx_quantize_weights2):
+    blocks along n (w2_q, w2_s; forward FC2) and along d (w2_q_rows,
+    w2_s_rows; backward FC2-dgrad).  Returns the four tensors."""
+    _need(W2, torch.bfloat16, "W2", 3)
+    E, n, d = W2.shape
+    u8 = torch.uint8
+    dev = W2.device
+    if w2_q is None:
+        w2_q = torch.empty((E, n, d), dtype=u8, device=dev)
+    if w2_s is None:
+        w2_s = torch.empty(E * (n // 32) * d, dtype=u8, device=dev)
+    if w2_q_rows is None:
+        w2_q_rows = torch.empty((E, n, d), dtype=u8, device=dev)
+    if w2_s_rows is None:
+        w2_s_rows = torch.empty(E * n * d // 32, dtype=u8, device=dev)
+    for t, nm in ((w2_q, "w2_q"), (w2_s, "w2_s"), (w2_q_rows, "w2_q_rows"), (w2_s_rows, "w2_s_rows")):
+        _need(t, u8, nm)
+    rc = lib().moe_mx_quantize_weights2(_ptr(W2), E, n, d, _ptr(w2_q), _ptr(w2_s), _ptr(w2_q_rows),
+                                        _ptr(w2_s_rows), _stream(stream))
+    _check(rc, "moe_mx_quantize_weights2")
+    return w2_q, w2_s, w2_q_rows, w2_s_rows

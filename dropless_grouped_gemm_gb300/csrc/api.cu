@@ -531,15 +531,23 @@ int moe_router_grad_rows(const float* ds_part, int n_parts, const int32_t* row_o
 
 int moe_mx_quantize_weights(const moe_bf16* W2, int E, int n, int d, uint8_t* w2_q,
                             uint8_t* w2_s, void* stream) {
+  return moe_mx_quantize_weights2(W2, E, n, d, w2_q, w2_s, nullptr, nullptr, stream);
+}
+
+int moe_mx_quantize_weights2(const moe_bf16* W2, int E, int n, int d, uint8_t* w2_q,
+                             uint8_t* w2_s, uint8_t* w2_q_rows, uint8_t* w2_s_rows,
+                             void* stream) {
   g_last_launches = 0;
   if (E < 1 || E > MOE_MAX_EXPERTS || n <= 0 || d <= 0 || n % 128 || d % 128) return MOE_E_SIZE;
-  if (!W2 || !w2_q || !w2_s) return MOE_E_NULL;
-  if (misaligned(W2) || misaligned(w2_q) || misaligned(w2_s)) return MOE_E_ALIGN;
+  if (!W2 || !w2_q || !w2_s || (w2_q_rows && !w2_s_rows)) return MOE_E_NULL;
+  if (misaligned(W2) || misaligned(w2_q) || misaligned(w2_s) || misaligned(w2_q_rows))
+    return MOE_E_ALIGN;
   const int sms = num_sms_current();
   if (sms <= 0) return MOE_E_CUDA;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   ev_begin(s);
-  const cudaError_t e = moe::launch_mx_quantize_weights(W2, E, n, d, w2_q, w2_s, sms, s);
+  const cudaError_t e = moe::launch_mx_quantize_weights(W2, E, n, d, w2_q, w2_s, w2_q_rows,
+                                                        w2_s_rows, sms, s);
   ev_end(s);
   g_last_launches = 1;
   return cuda_rc(e);

@@ -30,55 +30,91 @@ namespace moe {
 namespace {
 
 // ---------------------------------------------------------------- weights
-// one thread: 8 consecutive columns x one 32-row block of one expert
+// W2 [E, n, d] quantised for the forward FC2: blocks of 32 rows (FC2's
+// reduction index n) per column; with ROWS also for the backward FC2-dgrad:
+// blocks of 32 columns (its reduction index d) per row, so that MXFP8
+// training takes both copies from one read of W2.
+// A warp covers one 32-row block x 128 columns: lane = 16 * half + i holds
+// rows 16 * half .. +15 of columns 8 * i .. +7 (values kept as packed bf16
+// pairs).  A column's 32-row maximum combines the two halves (lanes 16
+// apart); a row's 32-column maximum combines four adjacent lanes.
+template <bool ROWS>
 __global__ void __launch_bounds__(256)
-    mx_quantize_weights_kernel(const uint4* __restrict__ w, int E, int n, int d,
-                               uint2* __restrict__ q, uint8_t* __restrict__ s) {
+    mx_quantize_w2_kernel(const uint4* __restrict__ w, int E, int n, int d,
+                          uint2* __restrict__ q, uint8_t* __restrict__ s,
+                          uint2* __restrict__ qr, uint8_t* __restrict__ sr) {
+  const int lane = threadIdx.x & 31;
+  const int half = lane >> 4;
   const int d8 = d / 8;
-  const long long total = static_cast<long long>(E) * (n / 32) * d8;
-  for (long long g = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; g < total;
-       g += static_cast<long long>(gridDim.x) * blockDim.x) {
-    const int c8 = static_cast<int>(g % d8);
-    const long long eb = g / d8;
+  const int cw = d / 128;                                  // warps per 32-row block
+  const long long nwarps = static_cast<long long>(E) * (n / 32) * cw;
+  for (long long wi = (blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x) / 32;
+       wi < nwarps; wi += static_cast<long long>(gridDim.x) * blockDim.x / 32) {
+    const int c8 = static_cast<int>(wi % cw) * 16 + (lane & 15);
+    const long long eb = wi / cw;
     const int b = static_cast<int>(eb % (n / 32));
     const int e = static_cast<int>(eb / (n / 32));
-    const long long row0 = static_cast<long long>(e) * n + 32LL * b;
-    float v[32][8];
+    const long long row0 = static_cast<long long>(e) * n + 32LL * b + 16 * half;
+    uint32_t x[16][4];
     float amax[8] = {0, 0, 0, 0, 0, 0, 0, 0};
 #pragma unroll
-    for (int i = 0; i < 32; ++i) {
-      const uint4 x = __ldg(w + (row0 + i) * d8 + c8);
-      const uint32_t xw[4] = {x.x, x.y, x.z, x.w};
+    for (int i = 0; i < 16; ++i) {
+      const uint4 v = __ldg(w + (row0 + i) * d8 + c8);
+      x[i][0] = v.x; x[i][1] = v.y; x[i][2] = v.z; x[i][3] = v.w;
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
-        v[i][2 * j] = bf16_lo(xw[j]);
-        v[i][2 * j + 1] = bf16_hi(xw[j]);
+        amax[2 * j] = fmaxf(amax[2 * j], fabsf(bf16_lo(x[i][j])));
+        amax[2 * j + 1] = fmaxf(amax[2 * j + 1], fabsf(bf16_hi(x[i][j])));
       }
-#pragma unroll
-      for (int j = 0; j < 8; ++j) amax[j] = fmaxf(amax[j], fabsf(v[i][j]));
     }
     uint32_t code[8];
     float inv[8];
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
+      amax[j] = fmaxf(amax[j], __shfl_xor_sync(0xffffffffu, amax[j], 16));
       code[j] = mx_scale_code(amax[j]);
       inv[j] = mx_inv_scale(code[j]);
     }
 #pragma unroll
-    for (int i = 0; i < 32; ++i) {
-      const uint32_t w0 = e4m3x2(v[i][0] * inv[0], v[i][1] * inv[1]) |
-                          (e4m3x2(v[i][2] * inv[2], v[i][3] * inv[3]) << 16);
-      const uint32_t w1 = e4m3x2(v[i][4] * inv[4], v[i][5] * inv[5]) |
-                          (e4m3x2(v[i][6] * inv[6], v[i][7] * inv[7]) << 16);
+    for (int i = 0; i < 16; ++i) {
+      const uint32_t w0 = e4m3x2(bf16_lo(x[i][0]) * inv[0], bf16_hi(x[i][0]) * inv[1]) |
+                          (e4m3x2(bf16_lo(x[i][1]) * inv[2], bf16_hi(x[i][1]) * inv[3]) << 16);
+      const uint32_t w1 = e4m3x2(bf16_lo(x[i][2]) * inv[4], bf16_hi(x[i][2]) * inv[5]) |
+                          (e4m3x2(bf16_lo(x[i][3]) * inv[6], bf16_hi(x[i][3]) * inv[7]) << 16);
       q[(row0 + i) * d8 + c8] = make_uint2(w0, w1);
     }
-    // scales: chunk (b/4, c/128) of expert e
-    uint8_t* se = s + static_cast<long long>(e) * (n / 32) * d;
+    if (half == 0) {   // scales: chunk (b/4, c/128) of expert e
+      uint8_t* se = s + static_cast<long long>(e) * (n / 32) * d;
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      const int c = c8 * 8 + j;
-      const long long chunk = static_cast<long long>(b / 4) * (d / 128) + c / 128;
-      se[chunk * 512 + mx_chunk_off(c & 127, b & 3)] = static_cast<uint8_t>(code[j]);
+      for (int j = 0; j < 8; ++j) {
+        const int c = c8 * 8 + j;
+        const long long chunk = static_cast<long long>(b / 4) * (d / 128) + c / 128;
+        se[chunk * 512 + mx_chunk_off(c & 127, b & 3)] = static_cast<uint8_t>(code[j]);
+      }
+    }
+    if constexpr (ROWS) {
+      const int c = c8 * 8;                     // first column of this lane
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        float m = 0.f;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) m = fmaxf(m, fmaxf(fabsf(bf16_lo(x[i][j])), fabsf(bf16_hi(x[i][j]))));
+        m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
+        m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
+        const uint32_t sc = mx_scale_code(m);
+        const float iv = mx_inv_scale(sc);
+        const uint32_t w0 = e4m3x2(bf16_lo(x[i][0]) * iv, bf16_hi(x[i][0]) * iv) |
+                            (e4m3x2(bf16_lo(x[i][1]) * iv, bf16_hi(x[i][1]) * iv) << 16);
+        const uint32_t w1 = e4m3x2(bf16_lo(x[i][2]) * iv, bf16_hi(x[i][2]) * iv) |
+                            (e4m3x2(bf16_lo(x[i][3]) * iv, bf16_hi(x[i][3]) * iv) << 16);
+        const long long r = row0 + i;
+        qr[r * d8 + c8] = make_uint2(w0, w1);
+        if ((lane & 3) == 0) {                  // weight tiles of W2 viewed as [E*n, d]
+          const long long chunk = (r / 128) * (d / 128) + c / 128;
+          sr[chunk * 512 + mx_chunk_off(static_cast<int>(r & 127), (c / 32) & 3)] =
+              static_cast<uint8_t>(sc);
+        }
+      }
     }
   }
 }
@@ -759,12 +795,19 @@ cudaError_t launch_mx_t(const CUtensorMap& ta, const CUtensorMap& tb, const CUte
 }  // namespace
 
 cudaError_t launch_mx_quantize_weights(const uint16_t* w2, int E, int n, int d, uint8_t* q,
-                                       uint8_t* s, int num_sms, cudaStream_t st) {
-  const long long threads = static_cast<long long>(E) * (n / 32) * (d / 8);
+                                       uint8_t* s, uint8_t* q_rows, uint8_t* s_rows, int num_sms,
+                                       cudaStream_t st) {
+  const long long threads = static_cast<long long>(E) * (n / 32) * (d / 128) * 32;
   const long long want = (threads + 255) / 256;
   const int blocks = static_cast<int>(want < 16LL * num_sms ? want : 16LL * num_sms);
-  mx_quantize_weights_kernel<<<blocks > 0 ? blocks : 1, 256, 0, st>>>(
-      reinterpret_cast<const uint4*>(w2), E, n, d, reinterpret_cast<uint2*>(q), s);
+  if (q_rows)
+    mx_quantize_w2_kernel<true><<<blocks > 0 ? blocks : 1, 256, 0, st>>>(
+        reinterpret_cast<const uint4*>(w2), E, n, d, reinterpret_cast<uint2*>(q), s,
+        reinterpret_cast<uint2*>(q_rows), s_rows);
+  else
+    mx_quantize_w2_kernel<false><<<blocks > 0 ? blocks : 1, 256, 0, st>>>(
+        reinterpret_cast<const uint4*>(w2), E, n, d, reinterpret_cast<uint2*>(q), s, nullptr,
+        nullptr);
   return cudaGetLastError();
 }
 

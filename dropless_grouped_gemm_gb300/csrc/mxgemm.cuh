@@ -52,8 +52,12 @@ struct MxGemmArgs {
   int32_t* err;
 };
 
+// W2 [E, n, d]: blocks of 32 rows per column (q, s: column tiles as in
+// moe.h); with q_rows also blocks of 32 columns per row (q_rows, s_rows in
+// weight tiles of W2 viewed as [E*n, d]) from the same read
 cudaError_t launch_mx_quantize_weights(const uint16_t* w2, int E, int n, int d, uint8_t* q,
-                                       uint8_t* s, int num_sms, cudaStream_t st);
+                                       uint8_t* s, uint8_t* q_rows, uint8_t* s_rows, int num_sms,
+                                       cudaStream_t st);
 // ragged activation: row-wise codes q / scales s (q may be null: transposed
 // copy only) and the transposed copy qT / sT (may be null).  tiled = false:
 // plain scales s [rows, cols/32], sT [cols, rows/32]; tiled = true: s in row

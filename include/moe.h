@@ -389,6 +389,18 @@ int moe_mx_quantize_weights(const moe_bf16* W2, int E, int n, int d,
                             uint8_t* w2_q, uint8_t* w2_s, void* stream);
 
 /*
+ * moe_mx_quantize_weights2 - both MXFP8 copies of W2 that MXFP8 training
+ * uses, from one read of W2: w2_q / w2_s as moe_mx_quantize_weights (blocks
+ * along n, for the forward FC2) and, if w2_q_rows != NULL, w2_q_rows
+ * [E, n, d] / w2_s_rows (blocks along d, weight tiles: the
+ * moe_mx_quantize_weights_rowwise layout with rows = E*n) for the
+ * backward's FC2-dgrad.  Same sizes and errors as moe_mx_quantize_weights.
+ */
+int moe_mx_quantize_weights2(const moe_bf16* W2, int E, int n, int d,
+                             uint8_t* w2_q, uint8_t* w2_s, uint8_t* w2_q_rows,
+                             uint8_t* w2_s_rows, void* stream);
+
+/*
  * moe_mx_quantize_weights_rowwise - MXFP8 copy of a weight for a data
  * gradient: W viewed as [rows, cols] bf16 (W2 [E, n, d] as rows = E*n,
  * cols = d; W1 [E, d, n1] as rows = E*d, cols = n1), blocks of 32 along

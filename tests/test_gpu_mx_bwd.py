@@ -51,6 +51,26 @@ def test_rowwise_weight_quantiser_bit_exact():
     assert np.array_equal(decode_weight_tiles(s, E * n, d), rs)
 
 
+def test_both_direction_weight_quantiser_bit_exact():
+    """moe_mx_quantize_weights2: the forward's copy (blocks along n) equals
+    moe_mx_quantize_weights' and the backward's (blocks along d) the
+    oracle's row-wise quantiser, both bit for bit, from one pass."""
+    M = _M()
+    E, n, d = 3, 256, 384
+    W2 = W.w2(22, E, n, d, 0.05, "cuda")
+    W2[1, 7, 64:96] = 0                                     # all-zero row block
+    W2[2, 0:32, 5] = torch.tensor(2.0 ** np.arange(-20, 12), dtype=torch.bfloat16)
+    q, s, qr, sr = M.mx_quantize_weights2(W2)
+    q1, s1 = M.mx_quantize_weights(W2)
+    torch.cuda.synchronize()
+    assert torch.equal(q, q1) and torch.equal(s, s1)
+    rq, rs = X.mx_quantize_rows(f64(W2).reshape(E * n, d))
+    assert np.array_equal(qr.cpu().numpy().reshape(E * n, d), rq)
+    assert np.array_equal(decode_weight_tiles(sr, E * n, d), rs)
+    cq, cs = X.mx_quantize_weights(f64(W2))
+    assert np.array_equal(q.cpu().numpy(), cq)
+
+
 def _layer(seed, counts, d, n, act, tail=64):
     off = np.concatenate([[0], np.cumsum(counts)]).astype(np.int64)
     assert (off % 32 == 0).all()
