@@ -765,13 +765,21 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 // Cluster size of the grouped GEMM launches: pairs of CTAs share B tiles
 // through TMA multicast.
 constexpr int kCluster = 2;
+constexpr int kMaxDevices = 64;
 
 template <GemmKind KIND, int ACT, bool MX = false, bool SKINNY = false>
 cudaError_t launch_t(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tc,
                      const GemmArgs& g, int num_sms, cudaStream_t s) {
   auto kern = grouped_gemm_kernel<KIND, ACT, MX, kCluster, SKINNY>;
   const size_t smem = smem_bytes<KIND, SKINNY>(MOE_MAX_EXPERTS);
-  static int grid = 0;  // per process; the library drives one device
+  // grid size and shared-memory attribute, set up once per device (a
+  // process may drive several devices, one at a time)
+  static int grid_of[kMaxDevices] = {0};
+  int dev = 0;
+  cudaError_t de = cudaGetDevice(&dev);
+  if (de != cudaSuccess) return de;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  int& grid = grid_of[dev];
   if (grid == 0) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));

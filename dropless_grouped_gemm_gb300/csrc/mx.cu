@@ -781,12 +781,17 @@ cudaError_t launch_mx_t(const CUtensorMap& ta, const CUtensorMap& tb, const CUte
                         const MxGemmArgs& g, int num_sms, cudaStream_t st) {
   auto kern = mx_gemm_kernel<KIND, ACT, QOUT>;
   const size_t smem = mx_smem_bytes<KIND>(MOE_MAX_EXPERTS);
-  static bool attr = false;  // per instantiation; the library drives one device
-  if (!attr) {
+  // shared-memory attribute, set once per device and instantiation
+  static bool attr_of[64] = {false};
+  int dev = 0;
+  const cudaError_t de = cudaGetDevice(&dev);
+  if (de != cudaSuccess) return de;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (!attr_of[dev]) {
     const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                static_cast<int>(smem));
     if (e != cudaSuccess) return e;
-    attr = true;
+    attr_of[dev] = true;
   }
   kern<<<num_sms, QTHREADS, smem, st>>>(ta, tb, tc, g);
   return cudaGetLastError();
