@@ -27,12 +27,13 @@ __all__ = [
     "permute", "unpermute", "grouped_mlp_fwd", "grouped_mlp_bwd", "MoeError",
     "FLAG_MXFP8", "MxFwd", "mx_quantize_weights", "mx_quantize", "mx_buffers",
     "MxBwd", "mx_quantize_weights_rowwise", "mx_bwd_workspace_size", "grouped_mlp_bwd_mx",
-    "grouped_mlp_bwd_routed", "router_grad_rows", "mx_quantize_weights2",
+    "grouped_mlp_bwd_routed", "router_grad_rows", "mx_quantize_weights2", "FLAG_ACCUMULATE_DW",
 ]
 
 ACT = {"swiglu": 0, "geglu": 1, "srelu": 2}
 FLAG_SAVE_H = 1
 FLAG_MXFP8 = 2
+FLAG_ACCUMULATE_DW = 4
 DEV_BAD_EXPERT, DEV_OVERFLOW, DEV_TIMEOUT, DEV_BAD_OFFSETS = 1, 2, 4, 8
 _RC = {-1: "MOE_E_NULL", -2: "MOE_E_ALIGN", -3: "MOE_E_SIZE", -4: "MOE_E_ARG",
        -5: "MOE_E_CUDA", -6: "MOE_E_WORKSPACE"}
@@ -109,11 +110,11 @@ def lib():
         L.moe_mx_bwd_workspace_size.restype = sz
         L.moe_mx_bwd_workspace_size.argtypes = [i32, i32, i32, i32]
         L.moe_grouped_mlp_bwd_mx.restype = i32
-        L.moe_grouped_mlp_bwd_mx.argtypes = [vp, vp, vp, vp, i32, i32, i32, i32, i32, vp, vp, vp,
-                                             vp, vp, vp, vp]
+        L.moe_grouped_mlp_bwd_mx.argtypes = [vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, vp, vp,
+                                             vp, vp, vp, vp, vp]
         L.moe_grouped_mlp_bwd_routed.restype = i32
         L.moe_grouped_mlp_bwd_routed.argtypes = [vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, vp,
-                                                 vp, i32, vp, vp, vp, vp, vp, vp, vp, vp, vp]
+                                                 vp, i32, i32, vp, vp, vp, vp, vp, vp, vp, vp, vp]
         L.moe_router_grad_rows.restype = i32
         L.moe_router_grad_rows.argtypes = [vp, i32, vp, i32, i32, i32, vp, vp]
         L.moe_selftest_bounded_wait.restype = i32
@@ -298,10 +299,21 @@ def grouped_mlp_fwd(x_perm: torch.Tensor, offsets: torch.Tensor, W1: torch.Tenso
     return (h_saved if save_h else None), a, y_perm, err
 
 
+def _bwd_flags(accumulate_dw: bool, dW1, dW2) -> int:
+    if not accumulate_dw:
+        return 0
+    if dW1 is None or dW2 is None:
+        raise ValueError("accumulate_dw needs the dW1 and dW2 to accumulate into")
+    return FLAG_ACCUMULATE_DW
+
+
 def grouped_mlp_bwd(x_perm, h_saved, a, dy_perm, offsets, W1, W2, act: str = "swiglu",
-                    dh=None, dx_perm=None, dW1=None, dW2=None, err=None, amax=None, stream=None):
+                    dh=None, dx_perm=None, dW1=None, dW2=None, err=None, amax=None, stream=None,
+                    accumulate_dw: bool = False):
     """Grouped expert MLP backward (see moe_grouped_mlp_bwd).  Returns
-    (dh, dx_perm, dW1, dW2, err)."""
+    (dh, dx_perm, dW1, dW2, err).  accumulate_dw: add this step's weight
+    gradients to the given dW1, dW2 (MOE_FLAG_ACCUMULATE_DW)."""
+    flags = _bwd_flags(accumulate_dw, dW1, dW2)
     for t, nm in ((x_perm, "x_perm"), (h_saved, "h_saved"), (a, "a"), (dy_perm, "dy_perm"),
                   (W1, "W1"), (W2, "W2")):
         _need(t, torch.bfloat16, nm)
@@ -320,7 +332,7 @@ def grouped_mlp_bwd(x_perm, h_saved, a, dy_perm, offsets, W1, W2, act: str = "sw
         dW2 = torch.empty((E, n, d), dtype=torch.bfloat16, device=dev)
     err = _err_word(err, dev)
     rc = lib().moe_grouped_mlp_bwd(_ptr(x_perm), _ptr(h_saved), _ptr(a), _ptr(dy_perm),
-                                   _ptr(offsets), E, M_cap, d, n, _ptr(W1), _ptr(W2), ACT[act], 0,
+                                   _ptr(offsets), E, M_cap, d, n, _ptr(W1), _ptr(W2), ACT[act], flags,
                                    _ptr(dh), _ptr(dx_perm), _ptr(dW1), _ptr(dW2), _ptr(amax),
                                    _ptr(err), _stream(stream))
     _check(rc, "moe_grouped_mlp_bwd")
@@ -403,11 +415,13 @@ def mx_bwd_workspace_size(M_cap: int, d: int, n: int, act: str = "swiglu") -> in
 
 def grouped_mlp_bwd_mx(x_perm, h_saved, dy_perm, offsets, mx: dict, act: str = "swiglu",
                        dh=None, dx_perm=None, dW1=None, dW2=None, err=None, workspace=None,
-                       stream=None):
+                       stream=None, accumulate_dw: bool = False):
     """MXFP8 grouped expert MLP backward (moe_grouped_mlp_bwd_mx).  ``mx``
     holds uint8 tensors a_qT, a_sT (the forward's transposed copy), w2_q, w2_s
     (W2 with blocks along d) and w1_q, w1_s (W1 with blocks along n1).
-    Returns (dh, dx_perm, dW1, dW2, err)."""
+    Returns (dh, dx_perm, dW1, dW2, err).  accumulate_dw as in
+    grouped_mlp_bwd."""
+    flags = _bwd_flags(accumulate_dw, dW1, dW2)
     for t, nm in ((x_perm, "x_perm"), (h_saved, "h_saved"), (dy_perm, "dy_perm")):
         _need(t, torch.bfloat16, nm)
     _need(offsets, torch.int32, "offsets", 1)
@@ -439,7 +453,7 @@ def grouped_mlp_bwd_mx(x_perm, h_saved, dy_perm, offsets, mx: dict, act: str = "
                mx["dx_q"].data_ptr() if mx.get("dx_q") is not None else None,
                mx["dx_s"].data_ptr() if mx.get("dx_s") is not None else None)
     rc = lib().moe_grouped_mlp_bwd_mx(_ptr(x_perm), _ptr(h_saved), _ptr(dy_perm), _ptr(offsets),
-                                      E, M_cap, d, n, ACT[act], ctypes.byref(st), _ptr(dh),
+                                      E, M_cap, d, n, ACT[act], flags, ctypes.byref(st), _ptr(dh),
                                       _ptr(dx_perm), _ptr(dW1), _ptr(dW2), _ptr(err),
                                       _stream(stream))
     _check(rc, "moe_grouped_mlp_bwd_mx")
@@ -448,10 +462,13 @@ def grouped_mlp_bwd_mx(x_perm, h_saved, dy_perm, offsets, mx: dict, act: str = "
 
 def grouped_mlp_bwd_routed(x_perm, h_saved, do_perm, pair_of_row, probs, offsets, W1, W2,
                            act: str = "swiglu", dh=None, a_scaled=None, ds_part=None,
-                           dx_perm=None, dW1=None, dW2=None, err=None, amax=None, stream=None):
+                           dx_perm=None, dW1=None, dW2=None, err=None, amax=None, stream=None,
+                           accumulate_dw: bool = False):
     """Backward with the router gradient inside the expert MLP
     (moe_grouped_mlp_bwd_routed).  do_perm is the gathered dO without the
-    router probability.  Returns (dh, a_scaled, ds_part, dx_perm, dW1, dW2, err)."""
+    router probability.  Returns (dh, a_scaled, ds_part, dx_perm, dW1, dW2,
+    err).  accumulate_dw as in grouped_mlp_bwd."""
+    flags = _bwd_flags(accumulate_dw, dW1, dW2)
     for t, nm in ((x_perm, "x_perm"), (h_saved, "h_saved"), (do_perm, "do_perm"), (W1, "W1"),
                   (W2, "W2")):
         _need(t, torch.bfloat16, nm)
@@ -478,7 +495,7 @@ def grouped_mlp_bwd_routed(x_perm, h_saved, do_perm, pair_of_row, probs, offsets
     err = _err_word(err, dev)
     rc = lib().moe_grouped_mlp_bwd_routed(
         _ptr(x_perm), _ptr(h_saved), _ptr(do_perm), _ptr(pair_of_row), _ptr(probs), _ptr(offsets),
-        E, M_cap, d, n, _ptr(W1), _ptr(W2), ACT[act], _ptr(dh), _ptr(a_scaled), _ptr(ds_part),
+        E, M_cap, d, n, _ptr(W1), _ptr(W2), ACT[act], flags, _ptr(dh), _ptr(a_scaled), _ptr(ds_part),
         _ptr(dx_perm), _ptr(dW1), _ptr(dW2), _ptr(amax), _ptr(err), _stream(stream))
     _check(rc, "moe_grouped_mlp_bwd_routed")
     return dh, a_scaled, ds_part, dx_perm, dW1, dW2, err

@@ -178,7 +178,7 @@ int bwd_gemms(const moe_bf16* x_perm, const moe_bf16* h_saved, const moe_bf16* a
               const moe_bf16* W1, const moe_bf16* W2, int act, moe_bf16* dh, moe_bf16* dx_perm,
               moe_bf16* dW1, moe_bf16* dW2, int32_t* err, cudaStream_t s, int sms,
               const int32_t* pair_of_row, const float* probs, moe_bf16* a_scaled,
-              float* ds_part, float* amax_dh) {
+              float* ds_part, float* amax_dh, bool accumulate) {
   const int n1 = (act == MOE_ACT_SRELU) ? n : 2 * n;
   moe::GemmArgs probe{};
   probe.M_cap = M_cap;
@@ -211,6 +211,7 @@ int bwd_gemms(const moe_bf16* x_perm, const moe_bf16* h_saved, const moe_bf16* a
   moe::GemmArgs gw2{};
   gw2.offsets = offsets; gw2.E = E; gw2.M_cap = M_cap; gw2.N = d; gw2.R = n;
   gw2.out = dW2; gw2.ldo = d; gw2.out_estride = static_cast<long long>(n) * d; gw2.err = err;
+  gw2.accumulate = accumulate;
   e = gemm(moe::GemmKind::kWgrad, 0, t_a_mn, t_dy_mn, t_dw2, gw2, sms, s);
   if (e != cudaSuccess) return MOE_E_CUDA;
   // 3. dX = dH W1^T
@@ -223,6 +224,7 @@ int bwd_gemms(const moe_bf16* x_perm, const moe_bf16* h_saved, const moe_bf16* a
   moe::GemmArgs gw1{};
   gw1.offsets = offsets; gw1.E = E; gw1.M_cap = M_cap; gw1.N = n1; gw1.R = d;
   gw1.out = dW1; gw1.ldo = n1; gw1.out_estride = static_cast<long long>(d) * n1; gw1.err = err;
+  gw1.accumulate = accumulate;
   e = gemm(moe::GemmKind::kWgrad, 0, t_x_mn, t_dh_mn, t_dw1, gw1, sms, s);
   if (e != cudaSuccess) return MOE_E_CUDA;
   g_last_launches = 4;
@@ -457,12 +459,16 @@ int moe_grouped_mlp_bwd(const moe_bf16* x_perm, const moe_bf16* h_saved, const m
   g_last_launches = 0;
   int rc = check_mlp_sizes(E, M_cap, d, n);
   if (rc) return rc;
-  if (act < MOE_ACT_SWIGLU || act > MOE_ACT_SRELU || flags != 0) return MOE_E_ARG;
+  if (act < MOE_ACT_SWIGLU || act > MOE_ACT_SRELU || (flags & ~MOE_FLAG_ACCUMULATE_DW))
+    return MOE_E_ARG;
+  const bool accumulate = flags & MOE_FLAG_ACCUMULATE_DW;
   if (!offsets || !W1 || !W2 || !dW1 || !dW2 || !err) return MOE_E_NULL;
   const int n1 = (act == MOE_ACT_SRELU) ? n : 2 * n;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (M_cap == 0) {
-    // no rows at all: the weight gradients are exactly zero
+    // no rows at all: the weight gradients are exactly zero (untouched
+    // when accumulating)
+    if (accumulate) return MOE_OK;
     cudaError_t e = cudaMemsetAsync(dW1, 0, static_cast<size_t>(E) * d * n1 * 2, s);
     if (e == cudaSuccess) e = cudaMemsetAsync(dW2, 0, static_cast<size_t>(E) * n * d * 2, s);
     return cuda_rc(e);
@@ -476,24 +482,27 @@ int moe_grouped_mlp_bwd(const moe_bf16* x_perm, const moe_bf16* h_saved, const m
   if (sms <= 0) return MOE_E_CUDA;
 
   return bwd_gemms(x_perm, h_saved, a, dy_perm, offsets, E, M_cap, d, n, W1, W2, act, dh, dx_perm,
-                   dW1, dW2, err, s, sms, nullptr, nullptr, nullptr, nullptr, amax_dh);
+                   dW1, dW2, err, s, sms, nullptr, nullptr, nullptr, nullptr, amax_dh, accumulate);
 }
 
 int moe_grouped_mlp_bwd_routed(const moe_bf16* x_perm, const moe_bf16* h_saved,
                                const moe_bf16* do_perm, const int32_t* pair_of_row,
                                const float* probs, const int32_t* offsets, int E, int M_cap,
                                int d, int n, const moe_bf16* W1, const moe_bf16* W2, int act,
-                               moe_bf16* dh, moe_bf16* a_scaled, float* ds_part,
+                               int flags, moe_bf16* dh, moe_bf16* a_scaled, float* ds_part,
                                moe_bf16* dx_perm, moe_bf16* dW1, moe_bf16* dW2, float* amax_dh,
                                int32_t* err, void* stream) {
   g_last_launches = 0;
   int rc = check_mlp_sizes(E, M_cap, d, n);
   if (rc) return rc;
-  if (act < MOE_ACT_SWIGLU || act > MOE_ACT_SRELU) return MOE_E_ARG;
+  if (act < MOE_ACT_SWIGLU || act > MOE_ACT_SRELU || (flags & ~MOE_FLAG_ACCUMULATE_DW))
+    return MOE_E_ARG;
+  const bool accumulate = flags & MOE_FLAG_ACCUMULATE_DW;
   if (!offsets || !W1 || !W2 || !dW1 || !dW2 || !err) return MOE_E_NULL;
   const int n1 = (act == MOE_ACT_SRELU) ? n : 2 * n;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (M_cap == 0) {
+    if (accumulate) return MOE_OK;
     cudaError_t e = cudaMemsetAsync(dW1, 0, static_cast<size_t>(E) * d * n1 * 2, s);
     if (e == cudaSuccess) e = cudaMemsetAsync(dW2, 0, static_cast<size_t>(E) * n * d * 2, s);
     return cuda_rc(e);
@@ -509,7 +518,7 @@ int moe_grouped_mlp_bwd_routed(const moe_bf16* x_perm, const moe_bf16* h_saved,
   if (sms <= 0) return MOE_E_CUDA;
   return bwd_gemms(x_perm, h_saved, a_scaled, do_perm, offsets, E, M_cap, d, n, W1, W2, act, dh,
                    dx_perm, dW1, dW2, err, s, sms, pair_of_row, probs, a_scaled, ds_part,
-                   amax_dh);
+                   amax_dh, accumulate);
 }
 
 int moe_router_grad_rows(const float* ds_part, int n_parts, const int32_t* row_of_pair, int T,
@@ -577,18 +586,21 @@ int moe_mx_quantize_weights_rowwise(const moe_bf16* W, int rows, int cols, uint8
 
 int moe_grouped_mlp_bwd_mx(const moe_bf16* x_perm, const moe_bf16* h_saved,
                            const moe_bf16* dy_perm, const int32_t* offsets, int E, int M_cap,
-                           int d, int n, int act, const moe_mx_bwd* mx, moe_bf16* dh,
-                           moe_bf16* dx_perm, moe_bf16* dW1, moe_bf16* dW2, int32_t* err,
-                           void* stream) {
+                           int d, int n, int act, int flags, const moe_mx_bwd* mx,
+                           moe_bf16* dh, moe_bf16* dx_perm, moe_bf16* dW1, moe_bf16* dW2,
+                           int32_t* err, void* stream) {
   g_last_launches = 0;
   int rc = check_mlp_sizes(E, M_cap, d, n);
   if (rc) return rc;
   if (d % 128 || n % 128 || M_cap % 32) return MOE_E_SIZE;
-  if (act < MOE_ACT_SWIGLU || act > MOE_ACT_SRELU) return MOE_E_ARG;
+  if (act < MOE_ACT_SWIGLU || act > MOE_ACT_SRELU || (flags & ~MOE_FLAG_ACCUMULATE_DW))
+    return MOE_E_ARG;
+  const bool accumulate = flags & MOE_FLAG_ACCUMULATE_DW;
   if (!offsets || !mx || !dW1 || !dW2 || !err) return MOE_E_NULL;
   const int n1 = (act == MOE_ACT_SRELU) ? n : 2 * n;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (M_cap == 0) {
+    if (accumulate) return MOE_OK;
     cudaError_t e = cudaMemsetAsync(dW1, 0, static_cast<size_t>(E) * d * n1 * 2, s);
     if (e == cudaSuccess) e = cudaMemsetAsync(dW2, 0, static_cast<size_t>(E) * n * d * 2, s);
     return cuda_rc(e);
@@ -650,6 +662,7 @@ int moe_grouped_mlp_bwd_mx(const moe_bf16* x_perm, const moe_bf16* h_saved,
   moe::MxGemmArgs gw2{};
   gw2.offsets = offsets; gw2.E = E; gw2.M_cap = M_cap; gw2.R = n; gw2.N = d;
   gw2.a_s = ws.a_sT; gw2.b_s = ws.dy_sT; gw2.err = err;
+  gw2.out = dW2; gw2.accumulate = accumulate;
   e = mx_gemm(moe::MxKind::kWgrad, 0, t_aT, t_dyT, t_dw2, gw2, sms, s);
   if (e != cudaSuccess) return MOE_E_CUDA;
   // 7. dX = dH W1^T
@@ -663,6 +676,7 @@ int moe_grouped_mlp_bwd_mx(const moe_bf16* x_perm, const moe_bf16* h_saved,
   moe::MxGemmArgs gw1{};
   gw1.offsets = offsets; gw1.E = E; gw1.M_cap = M_cap; gw1.R = d; gw1.N = n1;
   gw1.a_s = ws.x_sT; gw1.b_s = ws.dh_sT; gw1.err = err;
+  gw1.out = dW1; gw1.accumulate = accumulate;
   e = mx_gemm(moe::MxKind::kWgrad, 0, t_xT, t_dhT, t_dw1, gw1, sms, s);
   if (e != cudaSuccess) return MOE_E_CUDA;
   g_last_launches = 8;

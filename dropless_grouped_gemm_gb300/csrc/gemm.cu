@@ -172,7 +172,15 @@ __device__ __forceinline__ void epilogue_chunk(const GemmArgs& g, const Tile& tl
     const int orow = tl.m0 + row_in_tile;
     if (orow >= g.R) return;
     uint16_t* p = g.out + static_cast<long long>(tl.e) * g.out_estride + orow * g.ldo + col;
-    store_row32(p, r);
+    if (g.accumulate) {
+      uint32_t a[32];
+#pragma unroll
+      for (int i = 0; i < 32; ++i) a[i] = r[i];
+      add_bf16_row32(p, a);
+      store_row32(p, a);
+    } else {
+      store_row32(p, r);
+    }
   } else {
     if (row_in_tile >= tl.rows) return;
     const long long grow = tl.row0 + row_in_tile;
@@ -652,6 +660,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           tmem_wait_ld();
           fc1_mx_block<ACT>(g, tl, row_in_tile, lane, q, cb, r0, r1, amx);
         }
+      } else if (KIND == GemmKind::kWgrad && tl.kblocks == 0 && g.accumulate) {
+        // expert with no rows, accumulating: its weight gradient is untouched
       } else if (KIND == GemmKind::kWgrad && tl.m0 + q * 32 + 32 <= g.R && tl.kblocks == 0) {
         // expert with no rows: its weight gradient is zero; store the zero box
         if (lane == 0) {
@@ -674,6 +684,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           tmem_ld32(tb + c * BOXC, r0);
           if constexpr (BOXC == 64) tmem_ld32(tb + c * BOXC + 32, r1);
           tmem_wait_ld();
+          if (g.accumulate) {
+            const uint16_t* op = g.out + static_cast<long long>(tl.e) * g.out_estride +
+                                 static_cast<long long>(tl.m0 + q * 32 + lane) * g.ldo + col;
+            add_bf16_row32(op, r0);
+            if constexpr (BOXC == 64) add_bf16_row32(op + 32, r1);
+          }
           uint8_t* buf = staging + ((warp - 2) * C::nbuf + (stg_slot % C::nbuf)) * BOX;
           if (lane == 0) {                     // the box is free once its last store read it
             if constexpr (C::nbuf == 2) bulk_wait_read_1();

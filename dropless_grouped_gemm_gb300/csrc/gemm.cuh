@@ -57,6 +57,9 @@ struct GemmArgs {
   // outermost (a wave of CTAs sweeps every column tile of B), 1 = column
   // tiles outermost (a wave reuses each B column tile across all row pairs)
   int col_major;
+  // kWgrad: 1 = add the result to the bf16 values already in `out` (one
+  // rounding of old + new); experts with no rows leave theirs untouched
+  int accumulate;
 };
 
 // Launches the persistent grouped GEMM of `kind` (act: MOE_ACT_*) on `s`.

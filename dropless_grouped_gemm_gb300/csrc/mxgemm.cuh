@@ -50,6 +50,10 @@ struct MxGemmArgs {
   uint8_t* q_out;
   uint8_t* s_out;
   int32_t* err;
+  // kWgrad: 1 = add the result to the bf16 values already in `out` ([E, R,
+  // N], one rounding of old + new); experts with no rows leave theirs
+  // untouched
+  int accumulate;
 };
 
 // W2 [E, n, d]: blocks of 32 rows per column (q, s: column tiles as in

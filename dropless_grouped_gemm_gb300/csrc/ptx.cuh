@@ -248,6 +248,22 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 __device__ __forceinline__ float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t v) { return __uint_as_float(v & 0xFFFF0000u); }
 
+// accumulating weight gradients: adds the 32 bf16 values at p (16-byte
+// aligned) to 32 fp32 accumulator words, so that the store rounds old + new
+// once
+__device__ __forceinline__ void add_bf16_row32(const uint16_t* p, uint32_t (&r)[32]) {
+#pragma unroll
+  for (int v = 0; v < 4; ++v) {
+    const uint4 o = *reinterpret_cast<const uint4*>(p + 8 * v);
+    const uint32_t w[4] = {o.x, o.y, o.z, o.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      r[8 * v + 2 * i] = __float_as_uint(__uint_as_float(r[8 * v + 2 * i]) + bf16_lo(w[i]));
+      r[8 * v + 2 * i + 1] = __float_as_uint(__uint_as_float(r[8 * v + 2 * i + 1]) + bf16_hi(w[i]));
+    }
+  }
+}
+
 __device__ __forceinline__ void set_err(int32_t* err, int bits) {
   if (err) atomicOr(err, bits);
 }

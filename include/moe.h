@@ -71,6 +71,10 @@ typedef uint16_t moe_bf16;
 #define MOE_FLAG_SAVE_H 1      /* forward also stores H (needed by backward)   */
 #define MOE_FLAG_MXFP8 2       /* FC1 also emits MXFP8 A; FC2 is block-scaled
                                   MXFP8 (arguments in moe_mx_fwd)              */
+#define MOE_FLAG_ACCUMULATE_DW 4 /* backward: dW1, dW2 += this step's weight
+                                  gradients (gradient accumulation over
+                                  micro-batches); experts with no rows keep
+                                  their dW untouched                          */
 
 /*
  * MXFP8 data ([CuTe] "무엇을 해결하려는가" / "핵심 아이디어": an MXFP8 output
@@ -326,6 +330,14 @@ int moe_grouped_mlp_fwd(const moe_bf16* x_perm, const int32_t* offsets,
  *   dW1_e = X_e^T dH_e                      -> bf16
  * An expert with no rows gets dW1_e = dW2_e = 0.
  *
+ * flags: 0 or MOE_FLAG_ACCUMULATE_DW, gradient accumulation over
+ * micro-batches (the training configuration's gradient_accumulation_steps,
+ * [TE] "직접 재현하기: MaxText 컨테이너와 설정").  Accumulating, each weight
+ * gradient becomes bf16(dW_old + X_e^T dH_e) (the old bf16 value is added
+ * to the fp32 accumulator and the sum rounded once) and an expert with no
+ * rows leaves its dW1_e, dW2_e untouched; dh and dx_perm are written as
+ * usual.
+ *
  *   x_perm [M_cap, d], h_saved [M_cap, n1], a [M_cap, n], dy_perm [M_cap, d]
  *   dh [M_cap, n1] (written), dx_perm [M_cap, d] (written),
  *   dW1 [E, d, n1] (written), dW2 [E, n, d] (written); all bf16.
@@ -359,13 +371,14 @@ int moe_grouped_mlp_bwd(const moe_bf16* x_perm, const moe_bf16* h_saved,
  *   (fp32 partial <dA', act(H)> of each 128-column half tile, caller-owned
  *   scratch); FC2-wgrad then contracts a_scaled with do_perm.  dx_perm, dW1,
  *   dW2 and amax_dh as in moe_grouped_mlp_bwd.  Four launches; finish with
- *   moe_router_grad_rows.  Errors as moe_grouped_mlp_bwd.
+ *   moe_router_grad_rows.  flags: 0 or MOE_FLAG_ACCUMULATE_DW (as in
+ *   moe_grouped_mlp_bwd).  Errors as moe_grouped_mlp_bwd.
  */
 int moe_grouped_mlp_bwd_routed(const moe_bf16* x_perm, const moe_bf16* h_saved,
                                const moe_bf16* do_perm, const int32_t* pair_of_row,
                                const float* probs, const int32_t* offsets, int E,
                                int M_cap, int d, int n, const moe_bf16* W1,
-                               const moe_bf16* W2, int act, moe_bf16* dh,
+                               const moe_bf16* W2, int act, int flags, moe_bf16* dh,
                                moe_bf16* a_scaled, float* ds_part, moe_bf16* dx_perm,
                                moe_bf16* dW1, moe_bf16* dW2, float* amax_dh,
                                int32_t* err, void* stream);
@@ -426,14 +439,15 @@ size_t moe_mx_bwd_workspace_size(int M_cap, int d, int n, int act);
  *   dW2 [E, n, d] bf16 (zero for experts with no rows).  Eight launches:
  *   three quantisers (dY both ways, x transposed, A's scales re-tiled),
  *   FC2-dgrad + dAct, the dH quantiser, FC2-wgrad, FC1-dgrad, FC1-wgrad.
+ *   flags: 0 or MOE_FLAG_ACCUMULATE_DW (as in moe_grouped_mlp_bwd).
  *   Errors: as moe_grouped_mlp_bwd; MOE_E_WORKSPACE if mx->ws_bytes is too
  *   small; offsets that are not multiples of 32 raise MOE_DEV_BAD_OFFSETS.
  */
 int moe_grouped_mlp_bwd_mx(const moe_bf16* x_perm, const moe_bf16* h_saved,
                            const moe_bf16* dy_perm, const int32_t* offsets, int E,
-                           int M_cap, int d, int n, int act, const moe_mx_bwd* mx,
-                           moe_bf16* dh, moe_bf16* dx_perm, moe_bf16* dW1,
-                           moe_bf16* dW2, int32_t* err, void* stream);
+                           int M_cap, int d, int n, int act, int flags,
+                           const moe_mx_bwd* mx, moe_bf16* dh, moe_bf16* dx_perm,
+                           moe_bf16* dW1, moe_bf16* dW2, int32_t* err, void* stream);
 
 /*
  * moe_mx_quantize - group-aware MXFP8 quantisation of a ragged activation

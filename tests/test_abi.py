@@ -55,13 +55,31 @@ def test_host_argument_errors(L):
     assert L.moe_permute(None, None, None, 4, 1, 100, 4, None, None) == -3
     assert L.moe_unpermute(vp(16), None, vp(16), 2, 1, 64, 4, None, None, None, None) == -1
     # MXFP8 backward: sizes need multiples of 128 (d, n) and 32 (M_cap); mx required
-    assert L.moe_grouped_mlp_bwd_mx(None, None, None, vp(16), 4, 128, 192, 128, 0, None, None,
+    assert L.moe_grouped_mlp_bwd_mx(None, None, None, vp(16), 4, 128, 192, 128, 0, 0, None, None,
                                     None, vp(16), vp(16), vp(16), None) == -3
-    assert L.moe_grouped_mlp_bwd_mx(None, None, None, vp(16), 4, 100, 128, 128, 0, None, None,
+    assert L.moe_grouped_mlp_bwd_mx(None, None, None, vp(16), 4, 100, 128, 128, 0, 0, None, None,
                                     None, vp(16), vp(16), vp(16), None) == -3
-    assert L.moe_grouped_mlp_bwd_mx(None, None, None, vp(16), 4, 128, 128, 128, 0, None, None,
+    assert L.moe_grouped_mlp_bwd_mx(None, None, None, vp(16), 4, 128, 128, 128, 0, 0, None, None,
                                     None, vp(16), vp(16), vp(16), None) == -1
     assert L.moe_mx_quantize_weights_rowwise(vp(16), 100, 128, vp(16), vp(16), None) == -3
+
+
+def test_accumulate_flag_host_checks(L):
+    """MOE_FLAG_ACCUMULATE_DW is the only backward flag; an unknown bit is
+    refused.  With no rows at all an accumulating backward has nothing to
+    add and returns before any CUDA call (all pointers are dummies)."""
+    vp = ctypes.c_void_p
+    d = vp(256)
+    bwd = lambda flags, M_cap: L.moe_grouped_mlp_bwd(d, d, d, d, d, 2, M_cap, 128, 128, d, d, 0,
+                                                     flags, d, d, d, d, None, d, None)
+    routed = lambda flags, M_cap: L.moe_grouped_mlp_bwd_routed(
+        d, d, d, d, d, d, 2, M_cap, 128, 128, d, d, 0, flags, d, d, d, d, d, d, None, d, None)
+    mxb = lambda flags, M_cap: L.moe_grouped_mlp_bwd_mx(d, d, d, d, 2, M_cap, 128, 128, 0, flags,
+                                                         d, d, d, d, d, d, None)
+    for f in (bwd, routed, mxb):
+        assert f(8, 256) == -4
+        assert f(M.FLAG_ACCUMULATE_DW | 1, 256) == -4
+        assert f(M.FLAG_ACCUMULATE_DW, 0) == 0
 
 
 def test_mx_bwd_workspace_too_small(L):
@@ -71,7 +89,7 @@ def test_mx_bwd_workspace_too_small(L):
     need = M.mx_bwd_workspace_size(256, 128, 128, "swiglu")
     assert need >= 256 * (3 * 128 + 2 * 256)
     st = M.MxBwd(256, 256, 256, 256, 256, 256, 256, need - 1)
-    assert L.moe_grouped_mlp_bwd_mx(vp(256), vp(256), vp(256), vp(256), 2, 256, 128, 128, 0,
+    assert L.moe_grouped_mlp_bwd_mx(vp(256), vp(256), vp(256), vp(256), 2, 256, 128, 128, 0, 0,
                                     ctypes.byref(st), vp(256), vp(256), vp(256), vp(256),
                                     vp(256), None) == -6
 

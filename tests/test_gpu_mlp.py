@@ -97,6 +97,45 @@ def test_bwd(name, E, d, n, counts, act):
             assert float(dW1[e].abs().max()) == 0 and float(dW2[e].abs().max()) == 0
 
 
+ACC_CASES = [c for c in BWD_CASES
+             if c[0] in ("ragged_empty_one_row", "many_small_experts", "large_experts_ragged")]
+
+
+def _prior(shape, ref, key):
+    """A seeded earlier weight gradient with the RMS of this step's, so that
+    dropping or doubling either term fails the tolerance."""
+    rms = float(np.sqrt((ref ** 2).mean())) or 1.0
+    return W.normal(shape, key, rms, "cuda")
+
+
+@pytest.mark.parametrize("name,E,d,n,counts", ACC_CASES, ids=[c[0] for c in ACC_CASES])
+def test_bwd_accumulate_dw(name, E, d, n, counts):
+    """MOE_FLAG_ACCUMULATE_DW: dW1, dW2 become old + this step's gradient
+    (one bf16 rounding of the sum); experts with no rows keep their old
+    values bit for bit; dH and dX are unaffected."""
+    import dropless_grouped_gemm_gb300 as M
+    act = "swiglu"
+    off, x, W1, W2, dy = _case(E, d, n, counts, act, seed=13)
+    h, a, y = _fwd(off, x, W1, W2, act)
+    H, A, _ = O.grouped_mlp_fwd(f64(x), off, f64(W1), f64(W2), act)
+    dH, dX, dW1r, dW2r = O.grouped_mlp_bwd(f64(x), H, A, f64(dy), off, f64(W1), f64(W2), act)
+    old1 = _prior(dW1r.shape, dW1r, (13, W.X, 90))
+    old2 = _prior(dW2r.shape, dW2r, (13, W.X, 91))
+    dW1, dW2 = old1.clone(), old2.clone()
+    dh, dx, _, _, err = M.grouped_mlp_bwd(x, h, a, dy, cuda_i32(off), W1, W2, act, dW1=dW1,
+                                          dW2=dW2, accumulate_dw=True)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    R = int(off[-1])
+    assert_rms_close(f64(dh)[:R], dH[:R], f"{name} dH")
+    assert_rms_close(f64(dx)[:R], dX[:R], f"{name} dX")
+    assert_rms_close(f64(dW1), f64(old1) + dW1r, f"{name} dW1 accumulated")
+    assert_rms_close(f64(dW2), f64(old2) + dW2r, f"{name} dW2 accumulated")
+    for e in range(E):
+        if off[e + 1] == off[e]:
+            assert torch.equal(dW1[e], old1[e]) and torch.equal(dW2[e], old2[e])
+
+
 def test_aligned_zero_pad_rows():
     """With align > 1 the pad rows permute writes are zero; the GEMMs then
     produce zero rows there and the weight gradients ignore them."""

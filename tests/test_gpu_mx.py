@@ -125,11 +125,19 @@ def _check_blocks(gpu_a, ref_a, gpu_q, gpu_s, rows_axis):
     return int(same.sum()), same.size
 
 
+# (d, n, counts): the second shape gives an expert three 128-row blocks (the
+# second CTA of its last row pair has no rows) and an output width d that
+# ends in a single 128-column half
+FWD_SHAPES = [(256, 256, (96, 0, 160, 32)), (384, 256, (288, 0, 96, 64))]
+
+
+@pytest.mark.parametrize("shape", FWD_SHAPES, ids=["d256", "d384_rows288"])
 @pytest.mark.parametrize("act", ["swiglu", "geglu", "srelu"])
-def test_fused_fc1_mx_epilogue_and_block_scaled_fc2(act):
+def test_fused_fc1_mx_epilogue_and_block_scaled_fc2(act, shape):
     M = _lib()
-    E, d, n = 4, 256, 256
-    off, M_cap, x, W1, W2 = _mx_case(act, E, d, n)
+    E = 4
+    d, n, counts = shape
+    off, M_cap, x, W1, W2 = _mx_case(act, E, d, n, counts)
     buf = M.mx_buffers(E, n, d, M_cap, "cuda")
     M.mx_quantize_weights(W2, buf["w2_q"], buf["w2_s"])
     h, a, y, err = M.grouped_mlp_fwd(x, cuda_i32(off), W1, W2, act, save_h=True, mx=buf)

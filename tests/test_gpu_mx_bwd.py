@@ -87,14 +87,15 @@ def _layer(seed, counts, d, n, act, tail=64):
     return off, x, H, A, dy, W1, W2
 
 
-def _gpu_bwd(off, x, H, A, dy, W1, W2, act):
+def _gpu_bwd(off, x, H, A, dy, W1, W2, act, dW1=None, dW2=None, accumulate_dw=False):
     M = _M()
     offs = cuda_i32(off)
     _, _, aT, sT, e0 = M.mx_quantize(A, offs)          # the forward's transposed copy of A
     w2_q, w2_s = M.mx_quantize_weights_rowwise(W2)
     w1_q, w1_s = M.mx_quantize_weights_rowwise(W1)
     mx = dict(a_qT=aT, a_sT=sT, w2_q=w2_q, w2_s=w2_s, w1_q=w1_q, w1_s=w1_s)
-    dh, dx, dW1, dW2, err = M.grouped_mlp_bwd_mx(x, H, dy, offs, mx, act)
+    dh, dx, dW1, dW2, err = M.grouped_mlp_bwd_mx(x, H, dy, offs, mx, act, dW1=dW1, dW2=dW2,
+                                                  accumulate_dw=accumulate_dw)
     torch.cuda.synchronize()
     assert int(e0.item()) == 0 and int(err.item()) == 0
     assert M.last_launch_count() == 8
@@ -106,7 +107,27 @@ CASES = [
     ("tiles_ragged_empty", [160, 0, 96, 288], 256, 128),
     ("single_expert_long_k", [1024], 256, 128),
     ("many_small", [32 * ((i * 5) % 4) for i in range(40)], 128, 128),
+    # three 128-row blocks of d in the weight gradient and of an expert, and
+    # d = 384 ending in a single 128-column half
+    ("odd_row_blocks", [288, 32, 0, 416], 384, 128),
 ]
+
+
+def test_mx_bwd_accumulate_dw():
+    """MOE_FLAG_ACCUMULATE_DW on the MXFP8 backward: the block-scaled weight
+    gradients are added to the given ones (one bf16 rounding of the sum);
+    the empty expert's stay bit-identical."""
+    act = "swiglu"
+    counts = [160, 0, 96, 288]
+    off, x, H, A, dy, W1, W2 = _layer(33, counts, 256, 128, act)
+    ref = X.mx_grouped_mlp_bwd(f64(x), f64(H), f64(A), f64(dy), off, f64(W1), f64(W2), act)
+    old1 = W.normal(ref["dW1"].shape, (33, W.X, 90), float(np.sqrt((ref["dW1"] ** 2).mean())), "cuda")
+    old2 = W.normal(ref["dW2"].shape, (33, W.X, 91), float(np.sqrt((ref["dW2"] ** 2).mean())), "cuda")
+    dW1, dW2 = old1.clone(), old2.clone()
+    _gpu_bwd(off, x, H, A, dy, W1, W2, act, dW1=dW1, dW2=dW2, accumulate_dw=True)
+    assert_rms_close(f64(dW1), f64(old1) + ref["dW1"], "MX dW1 accumulated")
+    assert_rms_close(f64(dW2), f64(old2) + ref["dW2"], "MX dW2 accumulated")
+    assert torch.equal(dW1[1], old1[1]) and torch.equal(dW2[1], old2[1])
 
 
 @pytest.mark.parametrize("act", ["swiglu", "geglu", "srelu"])

@@ -72,6 +72,33 @@ def test_routed_backward_matches_oracle(name, E, T, k, d, n, align, act):
             assert float(dW1[e].abs().max()) == 0 and float(dW2[e].abs().max()) == 0
 
 
+def test_routed_backward_accumulate_dw():
+    """MOE_FLAG_ACCUMULATE_DW on the routed backward: the weight gradients
+    are added to the given ones; an empty expert's stay bit-identical."""
+    act = "swiglu"
+    M, idx, probs, r, ro, x, H, tok_dO, do_perm, W1, W2 = _setup(act, 6, 200, 1, 128, 128, 32, 62)
+    T, k = idx.shape
+    pt = torch.from_numpy(probs).cuda()
+    por = ro["pair_of_row"]
+    off = ro["offsets"]
+    row_prob = np.where(por >= 0, probs.reshape(-1)[np.maximum(por, 0)].astype(np.float64), 0.0)
+    _, _, dW1r, dW2r, _, _ = O.grouped_mlp_bwd_routed(f64(x), f64(H), O.permute(f64(tok_dO), por, k),
+                                                      row_prob, off, f64(W1), f64(W2), act)
+    old1 = W.normal(dW1r.shape, (62, W.X, 90), float(np.sqrt((dW1r ** 2).mean())), "cuda")
+    old2 = W.normal(dW2r.shape, (62, W.X, 91), float(np.sqrt((dW2r ** 2).mean())), "cuda")
+    dW1, dW2 = old1.clone(), old2.clone()
+    *_, err = M.grouped_mlp_bwd_routed(x, H, do_perm, r["pair_of_row"], pt.view(-1), r["offsets"],
+                                       W1, W2, act, dW1=dW1, dW2=dW2, accumulate_dw=True)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    assert_rms_close(f64(dW1), f64(old1) + dW1r, "routed dW1 accumulated")
+    assert_rms_close(f64(dW2), f64(old2) + dW2r, "routed dW2 accumulated")
+    empty = [e for e in range(len(off) - 1) if off[e + 1] == off[e]]
+    assert empty, "the case should hold an empty expert"
+    for e in empty:
+        assert torch.equal(dW1[e], old1[e]) and torch.equal(dW2[e], old2[e])
+
+
 def test_routed_router_gradient_equals_y_based():
     """The rewrite gives the router gradient of the plain path (<dO, Y> from
     the forward's Y) to within the tolerance, and reruns are bitwise equal."""
