@@ -28,6 +28,7 @@ __all__ = [
     "FLAG_MXFP8", "MxFwd", "mx_quantize_weights", "mx_quantize", "mx_buffers",
     "MxBwd", "mx_quantize_weights_rowwise", "mx_bwd_workspace_size", "grouped_mlp_bwd_mx",
     "grouped_mlp_bwd_routed", "router_grad_rows", "mx_quantize_weights2", "FLAG_ACCUMULATE_DW",
+    "grouped_gemm", "activation", "activation_bwd",
 ]
 
 ACT = {"swiglu": 0, "geglu": 1, "srelu": 2}
@@ -115,6 +116,12 @@ def lib():
         L.moe_grouped_mlp_bwd_routed.restype = i32
         L.moe_grouped_mlp_bwd_routed.argtypes = [vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, vp,
                                                  vp, i32, i32, vp, vp, vp, vp, vp, vp, vp, vp, vp]
+        L.moe_grouped_gemm.restype = i32
+        L.moe_grouped_gemm.argtypes = [vp, vp, i32, i32, i32, i32, vp, i32, vp, vp, vp]
+        L.moe_activation.restype = i32
+        L.moe_activation.argtypes = [vp, vp, i32, i32, i32, i32, vp, vp]
+        L.moe_activation_bwd.restype = i32
+        L.moe_activation_bwd.argtypes = [vp, vp, vp, i32, i32, i32, i32, vp, vp]
         L.moe_router_grad_rows.restype = i32
         L.moe_router_grad_rows.argtypes = [vp, i32, vp, i32, i32, i32, vp, vp]
         L.moe_selftest_bounded_wait.restype = i32
@@ -537,3 +544,53 @@ def mx_quantize_weights2(W2: torch.Tensor, w2_q=None, w2_s=None, w2_q_rows=None,
                                         _ptr(w2_s_rows), _stream(stream))
     _check(rc, "moe_mx_quantize_weights2")
     return w2_q, w2_s, w2_q_rows, w2_s_rows
+
+
+# ----------------------------------------------------------------- unfused pieces
+
+def grouped_gemm(a, offsets, B, b_layout: str = "kn", out=None, err=None, stream=None):
+    """Plain grouped GEMM (moe_grouped_gemm): out_e = a_e B_e with B [E, K, N]
+    ("kn"), or B stored [E, N, K] and out_e = a_e B_e^T ("nk").  Returns
+    (out, err)."""
+    _need(a, torch.bfloat16, "a", 2)
+    _need(B, torch.bfloat16, "B", 3)
+    _need(offsets, torch.int32, "offsets", 1)
+    layout = {"kn": 0, "nk": 1}[b_layout]
+    M_cap, K = a.shape
+    E = B.shape[0]
+    N = B.shape[2] if layout == 0 else B.shape[1]
+    if out is None:
+        out = torch.empty((M_cap, N), dtype=torch.bfloat16, device=a.device)
+    err = _err_word(err, a.device)
+    rc = lib().moe_grouped_gemm(_ptr(a), _ptr(offsets), E, M_cap, K, N, _ptr(B), layout, _ptr(out),
+                                _ptr(err), _stream(stream))
+    _check(rc, "moe_grouped_gemm")
+    return out, err
+
+
+def activation(h, offsets, act: str = "swiglu", a=None, stream=None):
+    """A = act(H) as its own memory pass (moe_activation)."""
+    _need(h, torch.bfloat16, "h", 2)
+    _need(offsets, torch.int32, "offsets", 1)
+    M_cap, n1 = h.shape
+    n = n1 if act == "srelu" else n1 // 2
+    if a is None:
+        a = torch.empty((M_cap, n), dtype=torch.bfloat16, device=h.device)
+    rc = lib().moe_activation(_ptr(h), _ptr(offsets), offsets.numel() - 1, M_cap, n, ACT[act],
+                              _ptr(a), _stream(stream))
+    _check(rc, "moe_activation")
+    return a
+
+
+def activation_bwd(h, da, offsets, act: str = "swiglu", dh=None, stream=None):
+    """dH = act'(H; dA) as its own memory pass (moe_activation_bwd)."""
+    _need(h, torch.bfloat16, "h", 2)
+    _need(da, torch.bfloat16, "da", 2)
+    _need(offsets, torch.int32, "offsets", 1)
+    M_cap, n = da.shape
+    if dh is None:
+        dh = torch.empty_like(h)
+    rc = lib().moe_activation_bwd(_ptr(h), _ptr(da), _ptr(offsets), offsets.numel() - 1, M_cap, n,
+                                  ACT[act], _ptr(dh), _stream(stream))
+    _check(rc, "moe_activation_bwd")
+    return dh

@@ -568,6 +568,77 @@ size_t moe_mx_bwd_workspace_size(int M_cap, int d, int n, int act) {
   return carve_mx_bwd(nullptr, M_cap, d, n1, n).bytes;
 }
 
+int moe_grouped_gemm(const moe_bf16* a, const int32_t* offsets, int E, int M_cap, int K, int N,
+                     const moe_bf16* B, int b_layout, moe_bf16* out, int32_t* err,
+                     void* stream) {
+  g_last_launches = 0;
+  int rc = check_mlp_sizes(E, M_cap, K, N);
+  if (rc) return rc;
+  if (b_layout != MOE_B_KN && b_layout != MOE_B_NK) return MOE_E_ARG;
+  if (!offsets || !B || !err) return MOE_E_NULL;
+  if (M_cap == 0) return MOE_OK;
+  if (!a || !out) return MOE_E_NULL;
+  if (misaligned(a) || misaligned(B) || misaligned(out)) return MOE_E_ALIGN;
+  const int sms = num_sms_current();
+  if (sms <= 0) return MOE_E_CUDA;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  // the FC2 contraction (B N-major) or the dgrad one (B K-major, rows = N)
+  CUtensorMap ta, tb;
+  if (!map_act(&ta, a, M_cap, K, moe::kBM)) return MOE_E_CUDA;
+  if (b_layout == MOE_B_KN ? !map_w(&tb, B, E, K, N, 64) : !map_w(&tb, B, E, N, K, 128))
+    return MOE_E_CUDA;
+  moe::GemmArgs g{};
+  g.offsets = offsets; g.E = E; g.M_cap = M_cap; g.K = K; g.N = N;
+  g.out = out; g.ldo = N; g.err = err;
+  const cudaError_t e = gemm(b_layout == MOE_B_KN ? moe::GemmKind::kFc2 : moe::GemmKind::kDgrad, 0,
+                             ta, tb, ta, g, sms, s);
+  if (e != cudaSuccess) return MOE_E_CUDA;
+  g_last_launches = 1;
+  return MOE_OK;
+}
+
+int moe_activation(const moe_bf16* h, const int32_t* offsets, int E, int M_cap, int n, int act,
+                   moe_bf16* a, void* stream) {
+  g_last_launches = 0;
+  int rc = check_mlp_sizes(E, M_cap, 64, n);
+  if (rc) return rc;
+  if (act < MOE_ACT_SWIGLU || act > MOE_ACT_SRELU) return MOE_E_ARG;
+  if (!offsets) return MOE_E_NULL;
+  if (M_cap == 0) return MOE_OK;
+  if (!h || !a) return MOE_E_NULL;
+  if (misaligned(h) || misaligned(a)) return MOE_E_ALIGN;
+  const int sms = num_sms_current();
+  if (sms <= 0) return MOE_E_CUDA;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  ev_begin(s);
+  const cudaError_t e = moe::launch_act_fwd(h, offsets, E, M_cap, n, act, a, sms, s);
+  ev_end(s);
+  if (e != cudaSuccess) return MOE_E_CUDA;
+  g_last_launches = 1;
+  return MOE_OK;
+}
+
+int moe_activation_bwd(const moe_bf16* h, const moe_bf16* da, const int32_t* offsets, int E,
+                       int M_cap, int n, int act, moe_bf16* dh, void* stream) {
+  g_last_launches = 0;
+  int rc = check_mlp_sizes(E, M_cap, 64, n);
+  if (rc) return rc;
+  if (act < MOE_ACT_SWIGLU || act > MOE_ACT_SRELU) return MOE_E_ARG;
+  if (!offsets) return MOE_E_NULL;
+  if (M_cap == 0) return MOE_OK;
+  if (!h || !da || !dh) return MOE_E_NULL;
+  if (misaligned(h) || misaligned(da) || misaligned(dh)) return MOE_E_ALIGN;
+  const int sms = num_sms_current();
+  if (sms <= 0) return MOE_E_CUDA;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  ev_begin(s);
+  const cudaError_t e = moe::launch_act_bwd(h, da, offsets, E, M_cap, n, act, dh, sms, s);
+  ev_end(s);
+  if (e != cudaSuccess) return MOE_E_CUDA;
+  g_last_launches = 1;
+  return MOE_OK;
+}
+
 int moe_mx_quantize_weights_rowwise(const moe_bf16* W, int rows, int cols, uint8_t* q,
                                     uint8_t* sc, void* stream) {
   g_last_launches = 0;

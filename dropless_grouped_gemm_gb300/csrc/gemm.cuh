@@ -77,6 +77,15 @@ cudaError_t launch_grouped_gemm(GemmKind kind, int act, const CUtensorMap& ta,
 constexpr int kSkinnyRows = 512;
 bool wgrad_skinny(const GemmArgs& g);
 
+// The activation and its derivative as separate memory passes (act.cu):
+// A = act(H) and dH = act'(H; dA) over the rows below offsets[E] (at most
+// rows_cap); H is [rows, n1], A / dA are [rows, n].
+cudaError_t launch_act_fwd(const uint16_t* h, const int32_t* offsets, int E, long long rows_cap,
+                           int n, int act, uint16_t* a, int num_sms, cudaStream_t st);
+cudaError_t launch_act_bwd(const uint16_t* h, const uint16_t* da, const int32_t* offsets, int E,
+                           long long rows_cap, int n, int act, uint16_t* dh, int num_sms,
+                           cudaStream_t st);
+
 // Box shapes (elements) the kernels expect for each operand's tensor map.
 constexpr int kBM = 128, kBN = 256, kBK = 64;
 

@@ -427,6 +427,47 @@ int moe_mx_quantize_weights_rowwise(const moe_bf16* W, int rows, int cols,
  * moe_mx_bwd_workspace_size - bytes of moe_mx_bwd.workspace for a layer
  * (0 for invalid sizes).  About M_cap * (3.4 d + 2.3 n1 + n/8).
  */
+/*
+ * The unfused pieces of the expert MLP: a plain grouped GEMM and the
+ * activation and its derivative as separate memory passes.  [CuTe]
+ * "무엇을 해결하려는가" names the cost they carry (the activation reads the
+ * FC1 output back and writes its result as its own memory pass) and
+ * "공개된 근거에서 확인되는 점" the comparison the fused path is measured
+ * against (grouped GEMM + activation kernels, unfused); the fused entry
+ * points above replace them.  Each is one launch; the library allocates
+ * nothing.
+ *
+ * moe_grouped_gemm - out_e = a_e B_e for the rows of each expert ([TE]
+ * "최적화 1: grouped GEMM": one launch over the experts' ragged groups, the
+ * counts read on the device).
+ *   a [M_cap, K] bf16, offsets [E+1] (device, non-decreasing, offsets[E] <=
+ *   M_cap), out [M_cap, N] bf16 (rows outside every expert not written).
+ *   b_layout MOE_B_KN: B [E, K, N]; MOE_B_NK: B stored as [E, N, K] and
+ *   out_e = a_e B_e^T.  K, N multiples of 64; pointers 16-byte aligned.
+ *   Errors as moe_grouped_mlp_fwd.
+ */
+#define MOE_B_KN 0
+#define MOE_B_NK 1
+int moe_grouped_gemm(const moe_bf16* a, const int32_t* offsets, int E, int M_cap, int K,
+                     int N, const moe_bf16* B, int b_layout, moe_bf16* out, int32_t* err,
+                     void* stream);
+
+/*
+ * moe_activation - A = act(H) from a stored bf16 H [M_cap, n1] (n1 = 2n
+ * gated, column 2j = gate_j, 2j+1 = up_j; n1 = n for MOE_ACT_SRELU) into
+ * A [M_cap, n], over the rows below offsets[E].  The arithmetic is the FC1
+ * epilogue's, applied to the bf16 H.
+ * moe_activation_bwd - dH = act'(H; dA) (gated: dg = dA u phi'(g), du =
+ * dA phi(g); SRELU: dh = 2 max(h, 0) dA) from bf16 H and dA [M_cap, n]
+ * into dh [M_cap, n1], over the rows below offsets[E].
+ *   n a multiple of 64; pointers 16-byte aligned.  Host errors as
+ *   moe_grouped_mlp_fwd.
+ */
+int moe_activation(const moe_bf16* h, const int32_t* offsets, int E, int M_cap, int n,
+                   int act, moe_bf16* a, void* stream);
+int moe_activation_bwd(const moe_bf16* h, const moe_bf16* da, const int32_t* offsets, int E,
+                       int M_cap, int n, int act, moe_bf16* dh, void* stream);
+
 size_t moe_mx_bwd_workspace_size(int M_cap, int d, int n, int act);
 
 /*

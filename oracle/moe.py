@@ -21,7 +21,7 @@ __all__ = [
     "act_forward", "act_backward", "phi", "dphi",
     "grouped_mlp_fwd", "grouped_mlp_bwd", "grouped_mlp_bwd_routed",
     "hadamard16", "amax", "amax_rht_transposed",
-    "fc1_rows", "fc2_rows",
+    "fc1_rows", "fc2_rows", "grouped_gemm",
 ]
 
 ERR_BAD_EXPERT = 1
@@ -337,6 +337,27 @@ def grouped_mlp_fwd(x_perm, offsets, W1, W2, act: str, round_bf16: bool = True):
         A[r0:r1] = a
         Y[r0:r1] = _rb(a @ W2[e], round_bf16)
     return H, A, Y
+
+
+def grouped_gemm(a, offsets, B, b_layout: str = "kn", round_bf16: bool = True):
+    """Plain grouped GEMM ([TE] "최적화 1: grouped GEMM": one call over the
+    experts' ragged row groups): out_e = A_e B_e for the rows of expert e,
+    with B [E, K, N] ("kn") or B stored transposed as [E, N, K] ("nk", then
+    out_e = A_e B_e^T).  Rows outside every expert are NaN (undefined); the
+    result is rounded to bf16 once."""
+    a = np.asarray(a, dtype=np.float64)
+    B = np.asarray(B, dtype=np.float64)
+    if b_layout == "nk":
+        B = np.swapaxes(B, 1, 2)
+    elif b_layout != "kn":
+        raise ValueError(b_layout)
+    E, N = B.shape[0], B.shape[2]
+    out = np.full((a.shape[0], N), np.nan)
+    for e in range(E):
+        r0, r1 = int(offsets[e]), int(offsets[e + 1])
+        if r1 > r0:
+            out[r0:r1] = _rb(a[r0:r1] @ B[e], round_bf16)
+    return out
 
 
 def grouped_mlp_bwd(x_perm, H, A, dY, offsets, W1, W2, act: str,

@@ -285,3 +285,33 @@ def test_amax_rht_transposed_special_cases():
     assert np.allclose((rot ** 2).sum(0), (blk ** 2).sum(0))
     assert np.isclose(O.amax_rht_transposed(blk, [0, 16]), np.abs(rot).max())
     assert O.amax(np.array([[-3.0, 2.0]])) == 3.0 and O.amax(np.zeros((0, 4))) == 0.0
+
+
+@pytest.mark.parametrize("layout", ["kn", "nk"])
+def test_grouped_gemm_brute_force(layout):
+    """The plain grouped GEMM against scalar loops on tiny ragged groups
+    (one of them empty; rows past the last expert stay undefined)."""
+    rng = np.random.default_rng(14)
+    rows = (2, 0, 3)
+    off = np.concatenate([[0], np.cumsum(rows)])
+    K, N = 5, 4
+    a = rng.standard_normal((int(off[-1]) + 1, K))
+    B = rng.standard_normal((3, K, N) if layout == "kn" else (3, N, K))
+    out = O.grouped_gemm(a, off, B, layout, round_bf16=False)
+    for e in range(3):
+        for r in range(off[e], off[e + 1]):
+            for c in range(N):
+                b = [B[e][i][c] if layout == "kn" else B[e][c][i] for i in range(K)]
+                assert abs(out[r][c] - sum(a[r][i] * b[i] for i in range(K))) < 1e-12
+    assert np.isnan(out[int(off[-1])]).all()
+
+
+def test_grouped_gemm_is_the_mlp_fc2():
+    """FC2 of the grouped MLP is the grouped GEMM of A with W2, and the
+    transposed layout of W2 gives the same result (bf16 rounding included)."""
+    rng = np.random.default_rng(15)
+    off, x, W1, W2 = _tiny("swiglu", rng)
+    H, A, Y = O.grouped_mlp_fwd(x, off, W1, W2, "swiglu")
+    R = int(off[-1])
+    assert np.array_equal(O.grouped_gemm(A, off, W2)[:R], Y[:R])
+    assert np.array_equal(O.grouped_gemm(A, off, np.swapaxes(W2, 1, 2).copy(), "nk")[:R], Y[:R])
