@@ -95,14 +95,17 @@ def kernel_work(w, M, E_ne):
         return work
     # routed workloads: the FC2-dgrad epilogue also writes A' (bf16) and the dS partials
     routed = w.routing != "identity"
+    # gathered operands read the token tensor itself (T rows), not its
+    # K-times larger permuted copy
+    tok = w.T * d if w.gather else M * d
     return {
-        "fc1_act": (2 * M * d * n1, B * (M * d + E_ne * d * n1 + M * n + M * n1)),
+        "fc1_act": (2 * M * d * n1, B * (tok + E_ne * d * n1 + M * n + M * n1)),
         "fc2": (2 * M * n * d, B * (M * n + E_ne * n * d + M * d)),
-        "fc2_dgrad_dact": (2 * M * d * n, B * (M * d + E_ne * n * d + 2 * M * n1) +
+        "fc2_dgrad_dact": (2 * M * d * n, B * (tok + E_ne * n * d + 2 * M * n1) +
                            ((B * M * n + 4 * M * ((n + 127) // 128)) if routed else 0)),
-        "fc2_wgrad": (2 * M * n * d, B * (M * n + M * d + E * n * d)),
+        "fc2_wgrad": (2 * M * n * d, B * (M * n + tok + E * n * d)),
         "fc1_dgrad": (2 * M * n1 * d, B * (M * n1 + E_ne * d * n1 + M * d)),
-        "fc1_wgrad": (2 * M * d * n1, B * (M * d + M * n1 + E * d * n1)),
+        "fc1_wgrad": (2 * M * d * n1, B * (tok + M * n1 + E * d * n1)),
     }
 
 
@@ -352,6 +355,34 @@ def make_step(w, inp, o):
             return n
         return step_mx
 
+    if w.gather:
+        def step_gather():
+            # the permutes fused into the GEMMs' loads ([Sonic] "Gather
+            # Fusion"): FC1, FC2-dgrad and both weight gradients read the
+            # token rows of x and dO through the routing map
+            n = 0
+            r = M.route_offsets(inp["topk_idx"], w.E, w.align, w.M_cap, out=o["route"],
+                                workspace=o["ws"])
+            n += M.last_launch_count()
+            M.grouped_mlp_fwd_gather(inp["x"], r["pair_of_row"], k, r["offsets"], inp["W1"],
+                                     inp["W2"], act, save_h=True, h_saved=o["h"], a=o["a"],
+                                     y_perm=o["y_perm"], err=o["err"])
+            n += M.last_launch_count()
+            M.unpermute(o["y_perm"], r["row_of_pair"], T, k, probs=inp["probs"], out=o["out"])
+            n += M.last_launch_count()
+            M.grouped_mlp_bwd_routed_gather(inp["x"], inp["dO"], r["pair_of_row"], k, o["h"],
+                                            inp["probs"].view(-1), r["offsets"], inp["W1"],
+                                            inp["W2"], act, dh=o["dh"], a_scaled=o["a_scaled"],
+                                            ds_part=o["ds_part"], dx_perm=o["dx_perm"],
+                                            dW1=o["dW1"], dW2=o["dW2"], err=o["err"])
+            n += M.last_launch_count()
+            M.router_grad_rows(o["ds_part"], r["row_of_pair"], T, k, dprobs=o["dprobs"])
+            n += M.last_launch_count()
+            M.unpermute(o["dx_perm"], r["row_of_pair"], T, k, out=o["dx"])
+            n += M.last_launch_count()
+            return n
+        return step_gather
+
     def step():
         n = 0
         r = M.route_offsets(inp["topk_idx"], w.E, w.align, w.M_cap, out=o["route"],
@@ -393,6 +424,9 @@ def event_names(w):
         return KERNELS_FWD + KERNELS_BWD
     if w.mxfp8:
         return ["route", "permute", "mx_quantize_weights"] + KERNELS_FWD + ["combine"]
+    if w.gather:
+        return (["route"] + KERNELS_FWD + ["combine"] + KERNELS_BWD +
+                ["router_grad_rows", "unpermute_bwd"])
     return (["route", "permute"] + KERNELS_FWD + ["combine", "permute_bwd"] +
             KERNELS_BWD + ["router_grad_rows", "unpermute_bwd"])
 
@@ -758,6 +792,11 @@ def step_description(w):
     if w.mxfp8:
         return ("route + permute + W2 MXFP8 quantise + fwd (FC1 + MX epilogue, block-scaled FC2) "
                 "+ combine")
+    if w.gather:
+        return ("route + fwd reading x through the routing map (grouped_mlp_fwd_gather) + "
+                "combine + bwd with the router gradient inside the expert MLP, reading x and dO "
+                "through the routing map (grouped_mlp_bwd_routed_gather + router_grad_rows) + "
+                "combine backward")
     return ("route + permute + fwd + combine + bwd with the router gradient inside the expert "
             "MLP (grouped_mlp_bwd_routed + router_grad_rows) + combine backward")
 

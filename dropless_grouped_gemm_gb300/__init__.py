@@ -28,7 +28,8 @@ __all__ = [
     "FLAG_MXFP8", "MxFwd", "mx_quantize_weights", "mx_quantize", "mx_buffers",
     "MxBwd", "mx_quantize_weights_rowwise", "mx_bwd_workspace_size", "grouped_mlp_bwd_mx",
     "grouped_mlp_bwd_routed", "router_grad_rows", "mx_quantize_weights2", "FLAG_ACCUMULATE_DW",
-    "grouped_gemm", "activation", "activation_bwd",
+    "grouped_gemm", "activation", "activation_bwd", "grouped_mlp_fwd_gather",
+    "grouped_mlp_bwd_routed_gather",
 ]
 
 ACT = {"swiglu": 0, "geglu": 1, "srelu": 2}
@@ -116,6 +117,13 @@ def lib():
         L.moe_grouped_mlp_bwd_routed.restype = i32
         L.moe_grouped_mlp_bwd_routed.argtypes = [vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, vp,
                                                  vp, i32, i32, vp, vp, vp, vp, vp, vp, vp, vp, vp]
+        L.moe_grouped_mlp_fwd_gather.restype = i32
+        L.moe_grouped_mlp_fwd_gather.argtypes = [vp, i32, i32, vp, vp, i32, i32, i32, i32, vp, vp,
+                                                 i32, i32, vp, vp, vp, vp, vp, vp]
+        L.moe_grouped_mlp_bwd_routed_gather.restype = i32
+        L.moe_grouped_mlp_bwd_routed_gather.argtypes = [vp, vp, i32, i32, vp, vp, vp, vp, i32, i32,
+                                                        i32, i32, vp, vp, i32, i32, vp, vp, vp, vp,
+                                                        vp, vp, vp, vp, vp]
         L.moe_grouped_gemm.restype = i32
         L.moe_grouped_gemm.argtypes = [vp, vp, i32, i32, i32, i32, vp, i32, vp, vp, vp]
         L.moe_activation.restype = i32
@@ -303,6 +311,44 @@ def grouped_mlp_fwd(x_perm: torch.Tensor, offsets: torch.Tensor, W1: torch.Tenso
                                    _ptr(y_perm), ctypes.byref(mxs) if mxs is not None else None,
                                    _ptr(amax), _ptr(err), _stream(stream))
     _check(rc, "moe_grouped_mlp_fwd")
+    return (h_saved if save_h else None), a, y_perm, err
+
+
+def grouped_mlp_fwd_gather(x: torch.Tensor, pair_of_row: torch.Tensor, k: int,
+                           offsets: torch.Tensor, W1: torch.Tensor, W2: torch.Tensor,
+                           act: str = "swiglu", save_h: bool = False, h_saved=None, a=None,
+                           y_perm=None, err=None, amax=None, stream=None):
+    """Grouped expert MLP forward reading the token rows of x [T, d] through
+    the routing map (moe_grouped_mlp_fwd_gather): no permuted copy of x.
+    Returns (h_saved or None, a, y_perm, err) like ``grouped_mlp_fwd``."""
+    if amax is not None:
+        _need(amax, torch.float32, "amax")
+    _need(x, torch.bfloat16, "x", 2)
+    _need(pair_of_row, torch.int32, "pair_of_row", 1)
+    _need(offsets, torch.int32, "offsets", 1)
+    _need(W1, torch.bfloat16, "W1", 3)
+    _need(W2, torch.bfloat16, "W2", 3)
+    T, d = x.shape
+    M_cap = pair_of_row.numel()
+    E, n, d2 = W2.shape
+    n1 = n if act == "srelu" else 2 * n
+    if d2 != d or tuple(W1.shape) != (E, d, n1) or offsets.numel() != E + 1:
+        raise MoeError("inconsistent shapes")
+    dev = x.device
+    if save_h and h_saved is None:
+        h_saved = torch.empty((M_cap, n1), dtype=torch.bfloat16, device=dev)
+    if a is None:
+        a = torch.empty((M_cap, n), dtype=torch.bfloat16, device=dev)
+    if y_perm is None:
+        y_perm = torch.empty((M_cap, d), dtype=torch.bfloat16, device=dev)
+    err = _err_word(err, dev)
+    if T == 0:      # the library reads nothing of x then, but needs an address
+        x = torch.zeros((1, d), dtype=torch.bfloat16, device=dev)
+    rc = lib().moe_grouped_mlp_fwd_gather(
+        _ptr(x), T, k, _ptr(pair_of_row), _ptr(offsets), E, M_cap, d, n, _ptr(W1), _ptr(W2),
+        ACT[act], FLAG_SAVE_H if save_h else 0, _ptr(h_saved) if save_h else None, _ptr(a),
+        _ptr(y_perm), _ptr(amax), _ptr(err), _stream(stream))
+    _check(rc, "moe_grouped_mlp_fwd_gather")
     return (h_saved if save_h else None), a, y_perm, err
 
 
@@ -505,6 +551,49 @@ def grouped_mlp_bwd_routed(x_perm, h_saved, do_perm, pair_of_row, probs, offsets
         E, M_cap, d, n, _ptr(W1), _ptr(W2), ACT[act], flags, _ptr(dh), _ptr(a_scaled), _ptr(ds_part),
         _ptr(dx_perm), _ptr(dW1), _ptr(dW2), _ptr(amax), _ptr(err), _stream(stream))
     _check(rc, "moe_grouped_mlp_bwd_routed")
+    return dh, a_scaled, ds_part, dx_perm, dW1, dW2, err
+
+
+def grouped_mlp_bwd_routed_gather(x, dO, pair_of_row, k: int, h_saved, probs, offsets, W1, W2,
+                                  act: str = "swiglu", dh=None, a_scaled=None, ds_part=None,
+                                  dx_perm=None, dW1=None, dW2=None, err=None, amax=None,
+                                  stream=None, accumulate_dw: bool = False):
+    """Routed backward reading x [T, d] and dO [T, d] through the routing map
+    (moe_grouped_mlp_bwd_routed_gather): no permuted copies.  Returns (dh,
+    a_scaled, ds_part, dx_perm, dW1, dW2, err) like
+    ``grouped_mlp_bwd_routed``."""
+    flags = _bwd_flags(accumulate_dw, dW1, dW2)
+    for t, nm in ((x, "x"), (dO, "dO"), (h_saved, "h_saved"), (W1, "W1"), (W2, "W2")):
+        _need(t, torch.bfloat16, nm)
+    _need(pair_of_row, torch.int32, "pair_of_row", 1)
+    _need(probs, torch.float32, "probs")
+    _need(offsets, torch.int32, "offsets", 1)
+    T, d = x.shape
+    M_cap = pair_of_row.numel()
+    E, n, _ = W2.shape
+    n1 = n if act == "srelu" else 2 * n
+    dev = x.device
+    bf = torch.bfloat16
+    if dh is None:
+        dh = torch.empty((M_cap, n1), dtype=bf, device=dev)
+    if a_scaled is None:
+        a_scaled = torch.empty((M_cap, n), dtype=bf, device=dev)
+    if ds_part is None:
+        ds_part = torch.empty((M_cap, (n + 127) // 128), dtype=torch.float32, device=dev)
+    if dx_perm is None:
+        dx_perm = torch.empty((M_cap, d), dtype=bf, device=dev)
+    if dW1 is None:
+        dW1 = torch.empty((E, d, n1), dtype=bf, device=dev)
+    if dW2 is None:
+        dW2 = torch.empty((E, n, d), dtype=bf, device=dev)
+    err = _err_word(err, dev)
+    if T == 0:      # nothing of x or dO is read then, but the maps need addresses
+        x = dO = torch.zeros((1, d), dtype=bf, device=dev)
+    rc = lib().moe_grouped_mlp_bwd_routed_gather(
+        _ptr(x), _ptr(dO), T, k, _ptr(h_saved), _ptr(pair_of_row), _ptr(probs), _ptr(offsets), E,
+        M_cap, d, n, _ptr(W1), _ptr(W2), ACT[act], flags, _ptr(dh), _ptr(a_scaled), _ptr(ds_part),
+        _ptr(dx_perm), _ptr(dW1), _ptr(dW2), _ptr(amax), _ptr(err), _stream(stream))
+    _check(rc, "moe_grouped_mlp_bwd_routed_gather")
     return dh, a_scaled, ds_part, dx_perm, dW1, dW2, err
 
 

@@ -172,13 +172,18 @@ int check_mlp_sizes(int E, int M_cap, int d, int n) {
 // The four backward GEMMs.  dy is FC2-dgrad's A operand and FC2-wgrad's B
 // operand, a_w FC2-wgrad's A operand.  Routed (probs != NULL): dy is the
 // unscaled gathered dO; FC2-dgrad applies each row's router probability in
-// its epilogue, which also writes A' (= a_w) and the dS partials.
+// its epilogue, which also writes A' (= a_w) and the dS partials.  With
+// x_tok / do_tok (routed only) the token tensors x [T, d] and dO [T, d]
+// replace x_perm and dy: the GEMMs read their rows through pair_of_row.
 int bwd_gemms(const moe_bf16* x_perm, const moe_bf16* h_saved, const moe_bf16* a_w,
               const moe_bf16* dy, const int32_t* offsets, int E, int M_cap, int d, int n,
               const moe_bf16* W1, const moe_bf16* W2, int act, moe_bf16* dh, moe_bf16* dx_perm,
               moe_bf16* dW1, moe_bf16* dW2, int32_t* err, cudaStream_t s, int sms,
               const int32_t* pair_of_row, const float* probs, moe_bf16* a_scaled,
-              float* ds_part, float* amax_dh, bool accumulate) {
+              float* ds_part, float* amax_dh, bool accumulate,
+              const moe_bf16* x_tok = nullptr, const moe_bf16* do_tok = nullptr, int T = 0,
+              int k = 1) {
+  const bool gather = x_tok != nullptr;
   const int n1 = (act == MOE_ACT_SRELU) ? n : 2 * n;
   moe::GemmArgs probe{};
   probe.M_cap = M_cap;
@@ -196,6 +201,13 @@ int bwd_gemms(const moe_bf16* x_perm, const moe_bf16* h_saved, const moe_bf16* a
       !map_act(&t_dh_mn, dh, M_cap, n1, 64) ||                // FC1-wgrad B (MN = n1)
       !map_out3(&t_dw2, dW2, E, n, d, skinny) || !map_out3(&t_dw1, dW1, E, d, n1, skinny))
     return MOE_E_CUDA;
+  // gathered: FC2-dgrad's A and FC2-wgrad's B are dO's rows, FC1-wgrad's A
+  // x's rows (the maps built above on the token tensors go unused)
+  auto set_gather = [&](moe::GemmArgs& ga, int operand, const moe_bf16* src) {
+    if (!gather) return;
+    ga.gather_pair = pair_of_row; ga.gather_k = k; ga.gather_T = T;
+    ga.gather_operand = operand; ga.gather_src = src; ga.gather_ld = d;
+  };
 
   // 1. dH = act'(H; dY W2^T)
   moe::GemmArgs g{};
@@ -205,6 +217,7 @@ int bwd_gemms(const moe_bf16* x_perm, const moe_bf16* h_saved, const moe_bf16* a
     g.pair_of_row = pair_of_row; g.probs = probs; g.out3 = a_scaled; g.ldo3 = n;
     g.ds_part = ds_part; g.ds_parts = (n + 127) / 128;
   }
+  set_gather(g, 0, do_tok);
   cudaError_t e = gemm(moe::GemmKind::kDgradAct, act, t_dy_k, t_w2_k, t_dy_k, g, sms, s);
   if (e != cudaSuccess) return MOE_E_CUDA;
   // 2. dW2_e = A_e^T dY_e
@@ -212,6 +225,7 @@ int bwd_gemms(const moe_bf16* x_perm, const moe_bf16* h_saved, const moe_bf16* a
   gw2.offsets = offsets; gw2.E = E; gw2.M_cap = M_cap; gw2.N = d; gw2.R = n;
   gw2.out = dW2; gw2.ldo = d; gw2.out_estride = static_cast<long long>(n) * d; gw2.err = err;
   gw2.accumulate = accumulate;
+  set_gather(gw2, 1, do_tok);
   e = gemm(moe::GemmKind::kWgrad, 0, t_a_mn, t_dy_mn, t_dw2, gw2, sms, s);
   if (e != cudaSuccess) return MOE_E_CUDA;
   // 3. dX = dH W1^T
@@ -225,6 +239,7 @@ int bwd_gemms(const moe_bf16* x_perm, const moe_bf16* h_saved, const moe_bf16* a
   gw1.offsets = offsets; gw1.E = E; gw1.M_cap = M_cap; gw1.N = n1; gw1.R = d;
   gw1.out = dW1; gw1.ldo = n1; gw1.out_estride = static_cast<long long>(d) * n1; gw1.err = err;
   gw1.accumulate = accumulate;
+  set_gather(gw1, 0, x_tok);
   e = gemm(moe::GemmKind::kWgrad, 0, t_x_mn, t_dh_mn, t_dw1, gw1, sms, s);
   if (e != cudaSuccess) return MOE_E_CUDA;
   g_last_launches = 4;
@@ -521,6 +536,46 @@ int moe_grouped_mlp_bwd_routed(const moe_bf16* x_perm, const moe_bf16* h_saved,
                    amax_dh, accumulate);
 }
 
+int moe_grouped_mlp_bwd_routed_gather(const moe_bf16* x, const moe_bf16* dO, int T, int k,
+                                      const moe_bf16* h_saved, const int32_t* pair_of_row,
+                                      const float* probs, const int32_t* offsets, int E,
+                                      int M_cap, int d, int n, const moe_bf16* W1,
+                                      const moe_bf16* W2, int act, int flags, moe_bf16* dh,
+                                      moe_bf16* a_scaled, float* ds_part, moe_bf16* dx_perm,
+                                      moe_bf16* dW1, moe_bf16* dW2, float* amax_dh, int32_t* err,
+                                      void* stream) {
+  g_last_launches = 0;
+  int rc = check_mlp_sizes(E, M_cap, d, n);
+  if (rc) return rc;
+  if (T < 0 || k < 1) return MOE_E_SIZE;
+  if (act < MOE_ACT_SWIGLU || act > MOE_ACT_SRELU || (flags & ~MOE_FLAG_ACCUMULATE_DW))
+    return MOE_E_ARG;
+  const bool accumulate = flags & MOE_FLAG_ACCUMULATE_DW;
+  if (!offsets || !W1 || !W2 || !dW1 || !dW2 || !err) return MOE_E_NULL;
+  const int n1 = (act == MOE_ACT_SRELU) ? n : 2 * n;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (M_cap == 0) {
+    if (accumulate) return MOE_OK;
+    cudaError_t e = cudaMemsetAsync(dW1, 0, static_cast<size_t>(E) * d * n1 * 2, s);
+    if (e == cudaSuccess) e = cudaMemsetAsync(dW2, 0, static_cast<size_t>(E) * n * d * 2, s);
+    return cuda_rc(e);
+  }
+  if (!x || !dO || !h_saved || !pair_of_row || !probs || !dh || !a_scaled || !ds_part ||
+      !dx_perm)
+    return MOE_E_NULL;
+  if (misaligned(x) || misaligned(dO) || misaligned(h_saved) || misaligned(dh) ||
+      misaligned(a_scaled) || misaligned(dx_perm) || misaligned(dW1) || misaligned(dW2) ||
+      misaligned(W1) || misaligned(W2))
+    return MOE_E_ALIGN;
+  const int sms = num_sms_current();
+  if (sms <= 0) return MOE_E_CUDA;
+  // x_perm / dy are not read in gather mode: the token tensors stand in for
+  // the map arguments that the gathered operands replace
+  return bwd_gemms(x, h_saved, a_scaled, dO, offsets, E, M_cap, d, n, W1, W2, act, dh, dx_perm,
+                   dW1, dW2, err, s, sms, pair_of_row, probs, a_scaled, ds_part, amax_dh,
+                   accumulate, x, dO, T, k);
+}
+
 int moe_router_grad_rows(const float* ds_part, int n_parts, const int32_t* row_of_pair, int T,
                          int k, int M_cap, float* dprobs, void* stream) {
   g_last_launches = 0;
@@ -566,6 +621,51 @@ size_t moe_mx_bwd_workspace_size(int M_cap, int d, int n, int act) {
   if (M_cap < 0 || d <= 0 || n <= 0 || act < MOE_ACT_SWIGLU || act > MOE_ACT_SRELU) return 0;
   const int n1 = (act == MOE_ACT_SRELU) ? n : 2 * n;
   return carve_mx_bwd(nullptr, M_cap, d, n1, n).bytes;
+}
+
+int moe_grouped_mlp_fwd_gather(const moe_bf16* x, int T, int k, const int32_t* pair_of_row,
+                               const int32_t* offsets, int E, int M_cap, int d, int n,
+                               const moe_bf16* W1, const moe_bf16* W2, int act, int flags,
+                               moe_bf16* h_saved, moe_bf16* a, moe_bf16* y_perm, float* amax_a,
+                               int32_t* err, void* stream) {
+  g_last_launches = 0;
+  int rc = check_mlp_sizes(E, M_cap, d, n);
+  if (rc) return rc;
+  if (T < 0 || k < 1) return MOE_E_SIZE;
+  if (act < MOE_ACT_SWIGLU || act > MOE_ACT_SRELU || (flags & ~MOE_FLAG_SAVE_H))
+    return MOE_E_ARG;
+  const bool save_h = flags & MOE_FLAG_SAVE_H;
+  if (!offsets || !W1 || !W2 || !err) return MOE_E_NULL;
+  if (M_cap == 0) return MOE_OK;
+  if (!x || !pair_of_row || !a || !y_perm || (save_h && !h_saved)) return MOE_E_NULL;
+  if (misaligned(x) || misaligned(W1) || misaligned(W2) || misaligned(a) || misaligned(y_perm) ||
+      (save_h && misaligned(h_saved)))
+    return MOE_E_ALIGN;
+  const int n1 = (act == MOE_ACT_SRELU) ? n : 2 * n;
+  const int sms = num_sms_current();
+  if (sms <= 0) return MOE_E_CUDA;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  CUtensorMap tw1, ta, tw2;
+  if (!map_w(&tw1, W1, E, d, n1, 64) || !map_act(&ta, a, M_cap, n, moe::kBM) ||
+      !map_w(&tw2, W2, E, n, d, 64))
+    return MOE_E_CUDA;
+  moe::GemmArgs g1{};
+  g1.offsets = offsets; g1.E = E; g1.M_cap = M_cap; g1.K = d; g1.N = n1; g1.R = 0;
+  g1.out = a; g1.ldo = n; g1.out2 = save_h ? h_saved : nullptr; g1.ldo2 = n1; g1.err = err;
+  g1.amax = amax_a;
+  // A's rows come from x through pair_of_row (copied by the kernel; the A
+  // map argument is unused)
+  g1.gather_pair = pair_of_row; g1.gather_k = k; g1.gather_T = T;
+  g1.gather_src = x; g1.gather_ld = d;
+  cudaError_t e = gemm(moe::GemmKind::kFc1Act, act, tw1, tw1, tw1, g1, sms, s);
+  if (e != cudaSuccess) return MOE_E_CUDA;
+  moe::GemmArgs g2{};
+  g2.offsets = offsets; g2.E = E; g2.M_cap = M_cap; g2.K = n; g2.N = d; g2.R = 0;
+  g2.out = y_perm; g2.ldo = d; g2.err = err;
+  e = gemm(moe::GemmKind::kFc2, 0, ta, tw2, ta, g2, sms, s);
+  if (e != cudaSuccess) return MOE_E_CUDA;
+  g_last_launches = 2;
+  return MOE_OK;
 }
 
 int moe_grouped_gemm(const moe_bf16* a, const int32_t* offsets, int E, int M_cap, int K, int N,

@@ -433,7 +433,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < NST; ++i) {
-      mbar_init(&full_bar[i], 1);
+      // gathered operands: lane 0's byte-count arrival plus one cp.async
+      // arrival per producer lane
+      mbar_init(&full_bar[i], g.gather_pair != nullptr ? 33 : 1);
       mbar_init(&empty_bar[i], CL);         // one commit from each CTA's MMA
     }
     for (int i = 0; i < 2; ++i) {
@@ -499,19 +501,144 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
   if (warp == 0) {
     // ---------------------------------------------------------- producer
-    if (lane == 0) {
-      int stage = 0;
-      uint32_t phase = 0;
-      uint32_t issued_parity[NST];
-      bool issued[NST];
-      for (int i = 0; i < NST; ++i) { issued[i] = false; issued_parity[i] = 0; }
-      bool ok = true;
+    // B: with a 2-CTA cluster each CTA fetches half of the shared B block
+    // and multicasts it into both CTAs' stage
+    auto load_b = [&](uint8_t* sb, uint64_t* fb, const Tile& tl, int kb) {
+      if constexpr (B_MN) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          if (tl.mc && (i >> 1) != rank) continue;
+          uint8_t* dst = sb + i * MN_BOX_BYTES;
+          const int kc = B_3D ? kb * BK : tl.krow0 + kb * BK;
+          if (CL == 2 && tl.mc) {
+            if constexpr (B_3D) tma_load_3d_mc(dst, &tmB, fb, tl.n0 + 64 * i, kc, tl.e, kPair);
+            else tma_load_2d_mc(dst, &tmB, fb, tl.n0 + 64 * i, kc, kPair);
+          } else {
+            if constexpr (B_3D) tma_load_3d(dst, &tmB, fb, tl.n0 + 64 * i, kc, tl.e);
+            else tma_load_2d(dst, &tmB, fb, tl.n0 + 64 * i, kc);
+          }
+        }
+      } else {
+        // K-major B: two 128-row halves
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          if (tl.mc && h != rank) continue;
+          uint8_t* dst = sb + h * (B_BYTES / 2);
+          if (CL == 2 && tl.mc) tma_load_3d_mc(dst, &tmB, fb, kb * BK, tl.n0 + 128 * h, tl.e, kPair);
+          else tma_load_3d(dst, &tmB, fb, kb * BK, tl.n0 + 128 * h, tl.e);
+        }
+      }
+    };
+    int stage = 0;
+    uint32_t phase = 0;
+    uint32_t issued_parity[NST];
+    bool issued[NST];
+    for (int i = 0; i < NST; ++i) { issued[i] = false; issued_parity[i] = 0; }
+    bool ok = true;
+    // token-tensor row of expert-major row r (gather_T, past the tensor, for
+    // a pad row or a row past the expert)
+    auto token_row = [&](long long r, bool valid) {
+      const int p = (valid && r < g.M_cap) ? g.gather_pair[r] : -1;
+      return p >= 0 ? p / g.gather_k : g.gather_T;
+    };
+    if (g.gather_pair != nullptr) {
+      // gathered operand (the permute fused into the load, [Sonic] "Gather
+      // Fusion"): the whole warp copies the token rows with 16-byte cp.async
+      // into the 128-byte-swizzled layout a TMA load would give (row r's
+      // chunk j at r*128 + (j ^ r%8)*16); one warp instruction moves four
+      // 128-byte rows.  Lane l copies chunk l%8 of row 4i + l/8 in its i-th
+      // copy; the token row indices it needs are held by lane (l & ~7) | i%8
+      // in slot i/8 (rr[m] = row 4(l%8 + 8m) + l/8).  Each lane's copies
+      // arrive on the full barrier (count 1 + 32); lane 0 waits, sets the
+      // byte count of the other operand and loads it with TMA.
+      const int ch = lane & 7, sub = lane >> 3;
+      auto copy_row = [&](uint8_t* box, int row, int tok, int col0) {
+        // zeros for a row past the tensor and for columns past its width
+        // (a weight gradient's column block may lie past d)
+        const bool ok_row = tok < g.gather_T && col0 + ch * 8 < g.gather_ld;
+        const uint16_t* src = g.gather_src + (ok_row ? static_cast<long long>(tok) * g.gather_ld + col0 + ch * 8 : 0);
+        cp_async16(box + row * 128 + ((ch ^ (row & 7)) * 16), src, ok_row ? 16u : 0u);
+      };
+      for (int t = unit0; t < total_tiles && ok; t += unit_step) {
+        const Tile tl = decode_tile<KIND, CL>(g, s_off, s_ts, t, rank);
+        int rr[4];
+        if constexpr (!A_MN) {
+          // K-major A: the tile's 128 rows, the same in every stage
+#pragma unroll
+          for (int m = 0; m < 4; ++m) {
+            const int i = 4 * (ch + 8 * m) + sub;
+            rr[m] = token_row(static_cast<long long>(tl.row0) + i, i < tl.rows);
+          }
+        }
+        for (int kb = 0; kb < tl.kblocks; ++kb) {
+          if constexpr (A_MN) {
+            // weight gradient: the block's 64 reduction rows (those past the
+            // expert read zeros)
+            const int kmax = (kb == tl.kblocks - 1) ? tl.klast : BK;
+#pragma unroll
+            for (int m = 0; m < 2; ++m) {
+              const int i = 4 * (ch + 8 * m) + sub;
+              rr[m] = token_row(static_cast<long long>(tl.krow0) + kb * BK + i, i < kmax);
+            }
+          }
+          if (lane == 0) ok = mbar_wait(&empty_bar[stage], phase ^ 1, abort_flag);
+          ok = __shfl_sync(0xffffffffu, ok, 0);
+          if (!ok) break;
+          uint8_t* sa = smem + stage * STAGE_BYTES;
+          uint8_t* sb = sa + A_BYTES;
+          uint64_t* fb = &full_bar[stage];
+          if constexpr (!A_MN) {
+            if (lane == 0) {
+              mbar_arrive_expect_tx(fb, B_BYTES);
+              load_b(sb, fb, tl, kb);
+            }
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+              copy_row(sa, 4 * i + sub, __shfl_sync(0xffffffffu, rr[i >> 3], (lane & ~7) | (i & 7)),
+                       kb * BK);
+          } else if (g.gather_operand == 0) {
+            // A = the token tensor transposed: two 64-column boxes of the
+            // block's 64 reduction rows
+            if (lane == 0) {
+              mbar_arrive_expect_tx(fb, B_BYTES);
+              load_b(sb, fb, tl, kb);
+            }
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+              const int box = i >> 4;
+              copy_row(sa + box * MN_BOX_BYTES, 4 * (i & 15) + sub,
+                       __shfl_sync(0xffffffffu, rr[(i & 15) >> 3], (lane & ~7) | (i & 7)),
+                       tl.m0 + 64 * box);
+            }
+          } else {
+            // B = the token tensor: four 64-column boxes; each CTA copies
+            // all of them itself (no multicast of gathered rows)
+            if (lane == 0) {
+              mbar_arrive_expect_tx(fb, A_BYTES);
+              const int kr = tl.krow0 + kb * BK;
+              tma_load_2d(sa, &tmA, fb, tl.m0, kr);
+              tma_load_2d(sa + MN_BOX_BYTES, &tmA, fb, tl.m0 + 64, kr);
+            }
+#pragma unroll
+            for (int i = 0; i < 64; ++i) {
+              const int box = i >> 4;
+              copy_row(sb + box * MN_BOX_BYTES, 4 * (i & 15) + sub,
+                       __shfl_sync(0xffffffffu, rr[(i & 15) >> 3], (lane & ~7) | (i & 7)),
+                       tl.n0 + 64 * box);
+            }
+          }
+          cp_async_arrive(fb);
+          issued[stage] = true;
+          issued_parity[stage] = phase;
+          if (++stage == NST) { stage = 0; phase ^= 1; }
+        }
+      }
+    } else if (lane == 0) {
       for (int t = unit0; t < total_tiles && ok; t += unit_step) {
         const Tile tl = decode_tile<KIND, CL>(g, s_off, s_ts, t, rank);
         for (int kb = 0; kb < tl.kblocks; ++kb) {
           if (!mbar_wait(&empty_bar[stage], phase ^ 1, abort_flag)) { ok = false; break; }
           uint8_t* sa = smem + stage * STAGE_BYTES;
-          uint8_t* sb = sa + A_BYTES;
           uint64_t* fb = &full_bar[stage];
           mbar_arrive_expect_tx(fb, STAGE_BYTES);
           if constexpr (A_MN) {
@@ -521,47 +648,23 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           } else {
             tma_load_2d(sa, &tmA, fb, kb * BK, tl.row0);
           }
-          // B: with a 2-CTA cluster each CTA fetches half of the shared B
-          // block and multicasts it into both CTAs' stage
-          if constexpr (B_MN) {
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              if (tl.mc && (i >> 1) != rank) continue;
-              uint8_t* dst = sb + i * MN_BOX_BYTES;
-              const int kc = B_3D ? kb * BK : tl.krow0 + kb * BK;
-              if (CL == 2 && tl.mc) {
-                if constexpr (B_3D) tma_load_3d_mc(dst, &tmB, fb, tl.n0 + 64 * i, kc, tl.e, kPair);
-                else tma_load_2d_mc(dst, &tmB, fb, tl.n0 + 64 * i, kc, kPair);
-              } else {
-                if constexpr (B_3D) tma_load_3d(dst, &tmB, fb, tl.n0 + 64 * i, kc, tl.e);
-                else tma_load_2d(dst, &tmB, fb, tl.n0 + 64 * i, kc);
-              }
-            }
-          } else {
-            // K-major B: two 128-row halves
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-              if (tl.mc && h != rank) continue;
-              uint8_t* dst = sb + h * (B_BYTES / 2);
-              if (CL == 2 && tl.mc) tma_load_3d_mc(dst, &tmB, fb, kb * BK, tl.n0 + 128 * h, tl.e, kPair);
-              else tma_load_3d(dst, &tmB, fb, kb * BK, tl.n0 + 128 * h, tl.e);
-            }
-          }
+          load_b(sa + A_BYTES, fb, tl, kb);
           issued[stage] = true;
           issued_parity[stage] = phase;
           if (++stage == NST) { stage = 0; phase ^= 1; }
         }
       }
-      if (!ok) {
-        // give up: wait (bounded) for our copies in flight before exiting
-        for (int i = 0; i < NST; ++i)
-          if (issued[i]) {
-            const uint32_t a = smem_u32(&full_bar[i]);
-            const uint64_t t0 = globaltimer_ns();
-            while (!mbar_try_wait(a, issued_parity[i]) && globaltimer_ns() - t0 < kWaitLimitNs) {}
-          }
-      }
     }
+    if (!ok && lane == 0) {
+      // give up: wait (bounded) for our copies in flight before exiting
+      for (int i = 0; i < NST; ++i)
+        if (issued[i]) {
+          const uint32_t a = smem_u32(&full_bar[i]);
+          const uint64_t t0 = globaltimer_ns();
+          while (!mbar_try_wait(a, issued_parity[i]) && globaltimer_ns() - t0 < kWaitLimitNs) {}
+        }
+    }
+    __syncwarp();
   } else if (warp == 1) {
     // ---------------------------------------------------------- MMA issuer
     int stage = 0;
@@ -582,6 +685,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         ok = __shfl_sync(0xffffffffu, ok, 0);
         if (!ok) break;
         tc_fence_after();
+        // rows gathered with cp.async were written through the generic proxy
+        if (g.gather_pair != nullptr && lane == 0) fence_proxy_async_smem();
         uint8_t* sa = smem + stage * STAGE_BYTES;
         uint8_t* sb = sa + A_BYTES;
         // In an expert's last reduction block only ceil(klast/16) MMAs touch

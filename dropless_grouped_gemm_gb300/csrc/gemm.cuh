@@ -60,6 +60,18 @@ struct GemmArgs {
   // kWgrad: 1 = add the result to the bf16 values already in `out` (one
   // rounding of old + new); experts with no rows leave theirs untouched
   int accumulate;
+  // gathered operand (the permute fused into the operand load): the
+  // operand's expert-major row r is row gather_pair[r] / gather_k of the
+  // token tensor gather_src [gather_T, gather_ld] (zeros for pad rows,
+  // gather_pair[r] < 0).  The ragged-row kinds gather their K-major A (tmA
+  // unused); kWgrad gathers the reduction rows of A (gather_operand 0, tmA
+  // unused) or of B (1, tmB unused).  NULL: no gather.
+  const int32_t* gather_pair;
+  int gather_k;
+  int gather_T;
+  int gather_operand;
+  const uint16_t* gather_src;
+  long long gather_ld;
 };
 
 // Launches the persistent grouped GEMM of `kind` (act: MOE_ACT_*) on `s`.

@@ -384,6 +384,28 @@ int moe_grouped_mlp_bwd_routed(const moe_bf16* x_perm, const moe_bf16* h_saved,
                                int32_t* err, void* stream);
 
 /*
+ * moe_grouped_mlp_bwd_routed_gather - moe_grouped_mlp_bwd_routed reading
+ * the token tensors directly ([Sonic] "Gather Fusion": the gathered rows
+ * are fetched again in the backward instead of being stored): FC2-dgrad's
+ * dO rows, FC2-wgrad's dO rows and FC1-wgrad's x rows come from x [T, d]
+ * and dO [T, d] through pair_of_row (token pair_of_row[r] / k; pad rows
+ * read zeros), so neither permuted copy exists.  The other arguments, the
+ * outputs (dh, a_scaled, ds_part, dx_perm in expert-major order; dW1, dW2)
+ * and flags are those of moe_grouped_mlp_bwd_routed, and equal its results
+ * on moe_permute(x), moe_permute(dO) bit for bit.  x and dO non-NULL and
+ * 16-byte aligned even when T = 0.  Four launches; finish with
+ * moe_router_grad_rows and moe_unpermute (dx).
+ */
+int moe_grouped_mlp_bwd_routed_gather(const moe_bf16* x, const moe_bf16* dO, int T, int k,
+                                      const moe_bf16* h_saved, const int32_t* pair_of_row,
+                                      const float* probs, const int32_t* offsets, int E,
+                                      int M_cap, int d, int n, const moe_bf16* W1,
+                                      const moe_bf16* W2, int act, int flags, moe_bf16* dh,
+                                      moe_bf16* a_scaled, float* ds_part, moe_bf16* dx_perm,
+                                      moe_bf16* dW1, moe_bf16* dW2, float* amax_dh,
+                                      int32_t* err, void* stream);
+
+/*
  * moe_router_grad_rows - dprobs [T*k] (fp32) of the routed backward:
  * dprobs[p] = sum over the n_parts partials of ds_part's row row_of_pair[p]
  * (fixed order, so reruns are bitwise identical); 0 for pairs without a
@@ -427,6 +449,25 @@ int moe_mx_quantize_weights_rowwise(const moe_bf16* W, int rows, int cols,
  * moe_mx_bwd_workspace_size - bytes of moe_mx_bwd.workspace for a layer
  * (0 for invalid sizes).  About M_cap * (3.4 d + 2.3 n1 + n/8).
  */
+/*
+ * moe_grouped_mlp_fwd_gather - moe_grouped_mlp_fwd with the permute fused
+ * into FC1's operand load ([Sonic] "Gather Fusion": the up-projection
+ * reads the routed rows itself, so the permuted copy of x, K times larger
+ * than x, is never written): row r of
+ * expert-major order is token pair_of_row[r] / k of x; pad rows
+ * (pair_of_row[r] < 0) read zeros.
+ *   x [T, d] bf16 (16-byte aligned, non-NULL even when T = 0: nothing is
+ *   then read from it); pair_of_row [M_cap] as written by
+ *   moe_route_offsets; the rest as moe_grouped_mlp_fwd.  flags: 0 or
+ *   MOE_FLAG_SAVE_H (no MXFP8).  H, A, y_perm equal moe_grouped_mlp_fwd's
+ *   on moe_permute(x) bit for bit.  Two launches.
+ */
+int moe_grouped_mlp_fwd_gather(const moe_bf16* x, int T, int k, const int32_t* pair_of_row,
+                               const int32_t* offsets, int E, int M_cap, int d, int n,
+                               const moe_bf16* W1, const moe_bf16* W2, int act, int flags,
+                               moe_bf16* h_saved, moe_bf16* a, moe_bf16* y_perm,
+                               float* amax_a, int32_t* err, void* stream);
+
 /*
  * The unfused pieces of the expert MLP: a plain grouped GEMM and the
  * activation and its derivative as separate memory passes.  [CuTe]

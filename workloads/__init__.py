@@ -247,6 +247,7 @@ class Workload:
     empty_expert: int | None = None
     align: int = 1
     mxfp8: bool = False
+    gather: bool = False     # GEMMs read token rows through the routing map
     x_std: float = 1.0
     w_std: float = 0.02
     dy_std: float = 1.0
@@ -276,6 +277,9 @@ WORKLOADS = {
                  notes="cuDNN-FE benchmark shape; counts fixed, equal"),
         Workload("zipf_t4096_d7168_e256_top8_n2048_swiglu", 2, 4096, 7168, 256, 8, 2048,
                  "swiglu", True, "logits", zipf_s=1.2),
+        # the same layer with the permutes fused into the GEMMs' loads
+        Workload("zipf_t4096_d7168_e256_top8_n2048_swiglu_gather", 2, 4096, 7168, 256, 8, 2048,
+                 "swiglu", True, "logits", zipf_s=1.2, gather=True),
         Workload("balanced_e8_m4096_k8192_n4096_geglu", 3, 8 * 4096, 8192, 8, 1, 2048,
                  "geglu", True, "identity"),
         Workload("balanced_e8_m4096_k8192_n2048_srelu", 5, 8 * 4096, 8192, 8, 1, 2048,
