@@ -394,7 +394,7 @@ __device__ __forceinline__ void fc1_mx_block(const GemmArgs& g, const Tile& tl, 
 }
 
 // ------------------------------------------------------------ the kernel
-template <GemmKind KIND, int ACT, bool MX, int CL, bool SKINNY>
+template <GemmKind KIND, int ACT, bool MX, int CL, bool SKINNY, bool GATHER>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                         const __grid_constant__ CUtensorMap tmB,
@@ -435,7 +435,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     for (int i = 0; i < NST; ++i) {
       // gathered operands: lane 0's byte-count arrival plus one cp.async
       // arrival per producer lane
-      mbar_init(&full_bar[i], g.gather_pair != nullptr ? 33 : 1);
+      mbar_init(&full_bar[i], GATHER ? 33 : 1);
       mbar_init(&empty_bar[i], CL);         // one commit from each CTA's MMA
     }
     for (int i = 0; i < 2; ++i) {
@@ -541,7 +541,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const int p = (valid && r < g.M_cap) ? g.gather_pair[r] : -1;
       return p >= 0 ? p / g.gather_k : g.gather_T;
     };
-    if (g.gather_pair != nullptr) {
+    if constexpr (GATHER) {
       // gathered operand (the permute fused into the load, [Sonic] "Gather
       // Fusion"): the whole warp copies the token rows with 16-byte cp.async
       // into the 128-byte-swizzled layout a TMA load would give (row r's
@@ -686,7 +686,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         if (!ok) break;
         tc_fence_after();
         // rows gathered with cp.async were written through the generic proxy
-        if (g.gather_pair != nullptr && lane == 0) fence_proxy_async_smem();
+        if (GATHER && lane == 0) fence_proxy_async_smem();
         uint8_t* sa = smem + stage * STAGE_BYTES;
         uint8_t* sb = sa + A_BYTES;
         // In an expert's last reduction block only ceil(klast/16) MMAs touch
@@ -888,10 +888,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 constexpr int kCluster = 2;
 constexpr int kMaxDevices = 64;
 
-template <GemmKind KIND, int ACT, bool MX = false, bool SKINNY = false>
+template <GemmKind KIND, int ACT, bool MX = false, bool SKINNY = false, bool GATHER = false>
 cudaError_t launch_t(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tc,
                      const GemmArgs& g, int num_sms, cudaStream_t s) {
-  auto kern = grouped_gemm_kernel<KIND, ACT, MX, kCluster, SKINNY>;
+  auto kern = grouped_gemm_kernel<KIND, ACT, MX, kCluster, SKINNY, GATHER>;
   const size_t smem = smem_bytes<KIND, SKINNY>(MOE_MAX_EXPERTS);
   // grid size and shared-memory attribute, set up once per device (a
   // process may drive several devices, one at a time)
@@ -961,6 +961,25 @@ cudaError_t launch_grouped_gemm(GemmKind kind, int act, const CUtensorMap& ta,
     const long long units_m = ((rows + BM - 1) / BM + kCluster - 1) / kCluster;
     const long long nt = (g.N + BN - 1) / BN;
     g.col_major = units_m <= nt ? 1 : 0;
+  }
+  if (g.gather_pair != nullptr) {
+    // the gathering producer is its own instantiation, so that the other
+    // kernels keep their code and registers
+    if (mx) return cudaErrorInvalidValue;
+    if (kind == GemmKind::kWgrad)
+      return wgrad_skinny(g) ? launch_t<GemmKind::kWgrad, 0, false, true, true>(ta, tb, tc, g, num_sms, s)
+                             : launch_t<GemmKind::kWgrad, 0, false, false, true>(ta, tb, tc, g, num_sms, s);
+#define MOE_GATHER_SWITCH(KIND)                                                                  \
+  switch (act) {                                                                                 \
+    case MOE_ACT_SWIGLU: return launch_t<KIND, MOE_ACT_SWIGLU, false, false, true>(ta, tb, tc, g, num_sms, s); \
+    case MOE_ACT_GEGLU: return launch_t<KIND, MOE_ACT_GEGLU, false, false, true>(ta, tb, tc, g, num_sms, s);   \
+    case MOE_ACT_SRELU: return launch_t<KIND, MOE_ACT_SRELU, false, false, true>(ta, tb, tc, g, num_sms, s);   \
+    default: return cudaErrorInvalidValue;                                                       \
+  }
+    if (kind == GemmKind::kFc1Act) MOE_GATHER_SWITCH(GemmKind::kFc1Act)
+    if (kind == GemmKind::kDgradAct) MOE_GATHER_SWITCH(GemmKind::kDgradAct)
+#undef MOE_GATHER_SWITCH
+    return cudaErrorInvalidValue;
   }
   if (mx) {
     if (kind != GemmKind::kFc1Act) return cudaErrorInvalidValue;
