@@ -554,7 +554,9 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(WL.WORKLOADS))
-    ap.add_argument("--e2e-steps", type=int, default=10)
+    ap.add_argument("--e2e-steps", type=int, default=30,
+                    help="steps of the pipelined end-to-end leg (its first input copy is not "
+                         "overlapped, so more steps approach the steady state)")
     ap.add_argument("--cpu-rows", type=int, default=512,
                     help="rows of the oracle's cpu_baseline sample")
     ap.add_argument("--ref-rows", type=int, default=64,
