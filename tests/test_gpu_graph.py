@@ -23,18 +23,29 @@ def _routing(seed, T, k, E):
     return idx, p / p.sum(1, keepdims=True)
 
 
-def test_layer_graph_capture_and_replay_with_new_routing():
+@pytest.mark.parametrize("wname", ["zipf_t4096_d7168_e256_top8_n2048_swiglu",
+                                   "zipf_t4096_d7168_e256_top8_n2048_swiglu_gather",
+                                   "zipf_t4096_d7168_e256_top8_n2048_mxfp8_train"],
+                         ids=["permuted", "gathered", "mxfp8_train"])
+def test_layer_graph_capture_and_replay_with_new_routing(wname):
+    """Each form of the layer step: with the permutes, with the GEMMs reading
+    token rows through the routing map, and the MXFP8 training step (weight
+    and activation quantisers, block-scaled GEMMs)."""
     import dropless_grouped_gemm_gb300 as M
     M.lib()
-    w = WL.scaled(WL.WORKLOADS["zipf_t4096_d7168_e256_top8_n2048_swiglu"], T=384, d=256, n=128,
-                  E=16, k=4)
+    # MXFP8 needs M_cap = T k + E (align - 1) to be a multiple of 32: E = 32
+    w = WL.scaled(WL.WORKLOADS[wname], T=384, d=256, n=128, E=32 if "mxfp8" in wname else 16, k=4)
     inp, o = BE.make_inputs(w, "cuda")
     step = BE.make_step(w, inp, o)
-    keys = ["x_perm", "h", "a", "y_perm", "out", "dprobs", "dh", "dx_perm", "dW1", "dW2", "dx"]
+    keys = ["h", "a", "y_perm", "out", "dprobs", "dh", "dx_perm", "dW1", "dW2", "dx"]
+    if not w.gather:
+        keys.append("x_perm")
 
     def snapshot():
         torch.cuda.synchronize()
-        return {k_: o[k_].clone() for k_ in keys}
+        snap = {k_: o[k_].clone() for k_ in keys}
+        snap["_rows"] = int(o["route"]["offsets"][-1].item())
+        return snap
 
     def set_routing(seed):
         idx, p = _routing(seed, w.T, w.k, w.E)
@@ -59,11 +70,12 @@ def test_layer_graph_capture_and_replay_with_new_routing():
     set_routing(2)
     g.replay()
     rep2 = snapshot()
-    R1 = int(o["route"]["offsets"][-1].item())
+    assert rep1["_rows"] == eager1["_rows"] and rep2["_rows"] == eager2["_rows"]
     for k_ in keys:
         a1, b1, a2, b2 = eager1[k_], rep1[k_], eager2[k_], rep2[k_]
         if a1.shape[0] == w.M_cap:     # rows past the used range are not written
-            a1, b1, a2, b2 = a1[:R1], b1[:R1], a2[:R1], b2[:R1]
+            r1, r2 = eager1["_rows"], eager2["_rows"]
+            a1, b1, a2, b2 = a1[:r1], b1[:r1], a2[:r2], b2[:r2]
         assert torch.equal(a1, b1), k_
         assert torch.equal(a2, b2), k_
     assert not torch.equal(eager1["out"], eager2["out"])
