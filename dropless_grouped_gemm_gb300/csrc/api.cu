@@ -862,7 +862,7 @@ int moe_mx_quantize(const moe_bf16* src, int rows, int cols, const int32_t* offs
     return MOE_E_SIZE;
   if (rows == 0) return MOE_OK;
   if (!src || !offsets || !q || !sc || !err || (qT && !sT)) return MOE_E_NULL;
-  if (misaligned(src) || misaligned(q)) return MOE_E_ALIGN;
+  if (misaligned(src) || misaligned(q) || misaligned(qT)) return MOE_E_ALIGN;
   const int sms = num_sms_current();
   if (sms <= 0) return MOE_E_CUDA;
   cudaStream_t s = static_cast<cudaStream_t>(stream);

@@ -83,10 +83,15 @@ def test_weight_quantiser_bit_exact():
     assert np.array_equal(decode_w2_scales(s, E, n, d), so)
 
 
-def test_group_aware_quantiser_bit_exact():
+# (rows, cols, offsets): the second shape has a partial 128-row tile and an
+# odd number of 32-column blocks
+QUANT_SHAPES = [(256, 256, [0, 64, 64, 192, 256 - 32]), (224, 96, [0, 64, 64, 160, 192])]
+
+
+@pytest.mark.parametrize("rows,cols,offs", QUANT_SHAPES, ids=["256x256", "224x96"])
+def test_group_aware_quantiser_bit_exact(rows, cols, offs):
     M = _lib()
-    rows, cols = 256, 256
-    offsets = np.array([0, 64, 64, 192, 256 - 32])       # empty expert; last 32 rows unused
+    offsets = np.array(offs)                             # empty expert; last 32 rows unused
     src = f64(WL.normal((rows, cols), (22, WL.X, 0), 1.0, "cuda"))
     src = _plant(src)
     src_t = torch.from_numpy(src).to(torch.bfloat16).cuda()
