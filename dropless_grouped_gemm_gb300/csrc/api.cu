@@ -604,7 +604,8 @@ int moe_mx_quantize_weights2(const moe_bf16* W2, int E, int n, int d, uint8_t* w
   g_last_launches = 0;
   if (E < 1 || E > MOE_MAX_EXPERTS || n <= 0 || d <= 0 || n % 128 || d % 128) return MOE_E_SIZE;
   if (!W2 || !w2_q || !w2_s || (w2_q_rows && !w2_s_rows)) return MOE_E_NULL;
-  if (misaligned(W2) || misaligned(w2_q) || misaligned(w2_s) || misaligned(w2_q_rows))
+  if (misaligned(W2) || misaligned(w2_q) || misaligned(w2_s) || misaligned(w2_q_rows) ||
+      misaligned(w2_s_rows))
     return MOE_E_ALIGN;
   const int sms = num_sms_current();
   if (sms <= 0) return MOE_E_CUDA;
