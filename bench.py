@@ -622,6 +622,8 @@ def main():
     M.lib().moe_set_launch_events(None, 0)
     barrier(ws)
     clocks = sampler.stop()
+    if int(o["err"].item()) != 0:   # a timed region with device errors measures nothing
+        raise SystemExit(f"device error bits {int(o['err'].item())} in the timed region")
     ms = t_start.elapsed_time(t_end) / args.steps
     ms = max_over_ranks(ms, ws)
 
