@@ -694,6 +694,8 @@ def main():
                          f"{'fwd (MXFP8 FC2)' if w.mxfp8 and not w.backward else 'fwd+bwd'}"
                          f"{' MXFP8' if w.mxfp8 and w.backward else ''} ({dt:.1f} s)"}
 
+    if int(o["err"].item()) != 0:   # graph, end-to-end and fusion legs share the error word
+        raise SystemExit(f"device error bits {int(o['err'].item())} after the graph / e2e legs")
     if rank == 0:
         line = {
             "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": ws,
