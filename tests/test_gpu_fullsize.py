@@ -20,6 +20,9 @@ pytestmark = [pytest.mark.gpu, pytest.mark.slow]
 
 C1 = "balanced_e8_m4096_k8192_n4096_swiglu"
 C2 = "zipf_t4096_d7168_e256_top8_n2048_swiglu"
+# the activation sweep on the same shape (GeGLU with tanh-approximated GELU;
+# squared ReLU, not gated, n = 2048)
+C3 = ["balanced_e8_m4096_k8192_n4096_geglu", "balanced_e8_m4096_k8192_n2048_srelu"]
 
 
 def test_generator_cpu_equals_gpu():
@@ -43,11 +46,11 @@ def _rows(shape_cols, key, std, rows):
     return f64(WL.normal_at(idx, key, std))
 
 
-@pytest.fixture(scope="module")
-def c1_run():
+@pytest.fixture(scope="module", params=[C1] + C3, ids=["swiglu", "geglu", "srelu"])
+def c1_run(request):
     import dropless_grouped_gemm_gb300 as M
     M.lib()
-    w = WL.WORKLOADS[C1]
+    w = WL.WORKLOADS[request.param]
     inp, o = BE.make_inputs(w, "cuda")
     step = BE.make_step(w, inp, o)
     assert step() == 6
@@ -71,11 +74,11 @@ def test_c1_rows_forward_backward(c1_run):
         H, A, Y = O.grouped_mlp_fwd(x, off, W1[None], W2[None], w.act)
         dH, dX, _, _ = O.grouped_mlp_bwd(x, H, A, dy, off, W1[None], W2[None], w.act)
         r = torch.as_tensor(rows).cuda()
-        assert_rms_close(f64(o["h"][r]), H, f"C1 e{e} H")
-        assert_rms_close(f64(o["a"][r]), A, f"C1 e{e} A")
-        assert_rms_close(f64(o["y_perm"][r]), Y, f"C1 e{e} Y")
-        assert_rms_close(f64(o["dh"][r]), dH, f"C1 e{e} dH")
-        assert_rms_close(f64(o["dx_perm"][r]), dX, f"C1 e{e} dX")
+        assert_rms_close(f64(o["h"][r]), H, f"{w.name} e{e} H")
+        assert_rms_close(f64(o["a"][r]), A, f"{w.name} e{e} A")
+        assert_rms_close(f64(o["y_perm"][r]), Y, f"{w.name} e{e} Y")
+        assert_rms_close(f64(o["dh"][r]), dH, f"{w.name} e{e} dH")
+        assert_rms_close(f64(o["dx_perm"][r]), dX, f"{w.name} e{e} dX")
 
 
 def test_c1_weight_gradient_entries(c1_run):
@@ -92,18 +95,19 @@ def test_c1_weight_gradient_entries(c1_run):
     js = np.sort(rng.choice(w.n, 16, replace=False))         # A / dA columns
     cs = np.sort(rng.choice(w.d, 16, replace=False))         # d columns
     ks = np.sort(rng.choice(w.d, 16, replace=False))
-    # H columns of the sampled gate/up pairs, A, dA, dH (rounding as stored)
-    hcols = np.stack([2 * js, 2 * js + 1], 1).reshape(-1)
+    # H columns of the sampled gate/up pairs (the column itself when not
+    # gated), A, dA, dH (rounding as stored)
+    hcols = np.stack([2 * js, 2 * js + 1], 1).reshape(-1) if w.gated else js
     h = O.bf16_round(x @ W1[:, hcols])
     a = O.bf16_round(O.act_forward(x @ W1[:, hcols], w.act))
     dA = dy @ W2[js, :].T
     dh = O.bf16_round(O.act_backward(h, dA, w.act))
     dW2_ref = O.bf16_round(a.T @ dy[:, cs])                    # [16, 16]
-    dW1_ref = O.bf16_round(x[:, ks].T @ dh)                    # [16, 32]
+    dW1_ref = O.bf16_round(x[:, ks].T @ dh)                    # [16, 32] (16 not gated)
     got2 = f64(o["dW2"][e][torch.as_tensor(js).cuda()][:, torch.as_tensor(cs).cuda()])
     got1 = f64(o["dW1"][e][torch.as_tensor(ks).cuda()][:, torch.as_tensor(hcols).cuda()])
-    assert_rms_close(got2, dW2_ref, "C1 dW2 entries")
-    assert_rms_close(got1, dW1_ref, "C1 dW1 entries")
+    assert_rms_close(got2, dW2_ref, f"{w.name} dW2 entries")
+    assert_rms_close(got1, dW1_ref, f"{w.name} dW1 entries")
 
 
 @pytest.fixture(scope="module")
