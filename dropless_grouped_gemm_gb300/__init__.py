@@ -29,7 +29,7 @@ __all__ = [
     "MxBwd", "mx_quantize_weights_rowwise", "mx_bwd_workspace_size", "grouped_mlp_bwd_mx",
     "grouped_mlp_bwd_routed", "router_grad_rows", "mx_quantize_weights2", "FLAG_ACCUMULATE_DW",
     "grouped_gemm", "activation", "activation_bwd", "grouped_mlp_fwd_gather",
-    "grouped_mlp_bwd_routed_gather",
+    "grouped_mlp_bwd_routed_gather", "route_logits",
 ]
 
 ACT = {"swiglu": 0, "geglu": 1, "srelu": 2}
@@ -82,6 +82,9 @@ def lib():
         L.moe_last_launch_count.argtypes = []
         L.moe_router_topk.restype = i32
         L.moe_router_topk.argtypes = [vp, i32, i32, i32, vp, vp, vp]
+        L.moe_route_logits.restype = i32
+        L.moe_route_logits.argtypes = [vp, i32, i32, i32, i32, i32, vp, vp, vp, vp, vp, vp, vp, vp,
+                                       sz, vp, vp]
         L.moe_route_workspace_size.restype = sz
         L.moe_route_workspace_size.argtypes = [i32, i32, i32]
         L.moe_route_offsets.restype = i32
@@ -223,6 +226,39 @@ def route_offsets(topk_idx: torch.Tensor, E: int, align: int = 1, M_cap: int | N
                                  _ptr(o["true_total"]), _ptr(workspace), workspace.numel(),
                                  _ptr(o["err"]), _stream(stream))
     _check(rc, "moe_route_offsets")
+    return o
+
+
+def route_logits(logits: torch.Tensor, k: int, align: int = 1, M_cap: int | None = None,
+                 err: torch.Tensor | None = None, out: dict | None = None,
+                 workspace: torch.Tensor | None = None, stream=None) -> dict:
+    """The router fused into the routing layout (see moe_route_logits):
+    from logits [T, E] float32 to the dict of route_offsets plus topk_idx
+    [T, k] and probs [T, k]."""
+    _need(logits, torch.float32, "logits", 2)
+    T, E = logits.shape
+    if M_cap is None:
+        M_cap = T * k + E * (align - 1)
+    dev = logits.device
+    o = out if out is not None else {
+        "topk_idx": torch.empty((T, k), dtype=torch.int32, device=dev),
+        "probs": torch.empty((T, k), dtype=torch.float32, device=dev),
+        "counts": torch.empty(E, dtype=torch.int32, device=dev),
+        "offsets": torch.empty(E + 1, dtype=torch.int32, device=dev),
+        "row_of_pair": torch.empty(T * k, dtype=torch.int32, device=dev),
+        "pair_of_row": torch.empty(M_cap, dtype=torch.int32, device=dev),
+        "true_total": torch.empty(1, dtype=torch.int32, device=dev),
+    }
+    o["err"] = _err_word(err if err is not None else o.get("err"), dev)
+    ws_bytes = route_workspace_size(T, k, E)
+    if workspace is None:
+        workspace = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=dev)
+    rc = lib().moe_route_logits(_ptr(logits), T, E, k, align, M_cap, _ptr(o["topk_idx"]),
+                                _ptr(o["probs"]), _ptr(o["counts"]), _ptr(o["offsets"]),
+                                _ptr(o["row_of_pair"]), _ptr(o["pair_of_row"]),
+                                _ptr(o["true_total"]), _ptr(workspace), workspace.numel(),
+                                _ptr(o["err"]), _stream(stream))
+    _check(rc, "moe_route_logits")
     return o
 
 

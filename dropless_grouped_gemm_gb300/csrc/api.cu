@@ -322,6 +322,34 @@ int moe_route_offsets(const int32_t* topk_idx, int T, int k, int E, int align, i
   return cuda_rc(e);
 }
 
+int moe_route_logits(const float* logits, int T, int E, int k, int align, int M_cap,
+                     int32_t* topk_idx, float* probs, int32_t* counts, int32_t* offsets,
+                     int32_t* row_of_pair, int32_t* pair_of_row, int32_t* true_total,
+                     void* workspace, size_t ws_bytes, int32_t* err, void* stream) {
+  g_last_launches = 0;
+  if (T < 0 || k < 1 || E < 1 || E > MOE_MAX_EXPERTS || k > E || align < 1 || align > 4096 ||
+      M_cap < 0)
+    return MOE_E_SIZE;
+  if (static_cast<long long>(T) * k + static_cast<long long>(E) * align >= (1LL << 31))
+    return MOE_E_SIZE;
+  if (!counts || !offsets || !true_total || !err) return MOE_E_NULL;
+  if (T > 0 && (!logits || !topk_idx || !probs || !row_of_pair)) return MOE_E_NULL;
+  if (M_cap > 0 && !pair_of_row) return MOE_E_NULL;
+  if (ws_bytes < moe::route_workspace_bytes(T, k, E)) return MOE_E_WORKSPACE;
+  if (!workspace) return MOE_E_NULL;
+  const int sms = num_sms_current();
+  if (sms <= 0) return MOE_E_CUDA;
+  int launches = 0;
+  ev_begin(static_cast<cudaStream_t>(stream));
+  const cudaError_t e = moe::launch_route_logits(logits, T, k, E, align, M_cap, topk_idx, probs,
+                                                 counts, offsets, row_of_pair, pair_of_row,
+                                                 true_total, workspace, err, sms,
+                                                 static_cast<cudaStream_t>(stream), &launches);
+  ev_end(static_cast<cudaStream_t>(stream));
+  g_last_launches = launches;
+  return cuda_rc(e);
+}
+
 int moe_route_offsets_noalloc(const int32_t* topk_idx, int T, int k, int E, int align, int M_cap,
                               int32_t* counts, int32_t* offsets, int32_t* row_of_pair,
                               int32_t* pair_of_row, int32_t* true_total, int32_t* err,

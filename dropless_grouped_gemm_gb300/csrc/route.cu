@@ -158,56 +158,104 @@ __global__ void __launch_bounds__(kThreads) route_rank(const int32_t* __restrict
   }
 }
 
-// Router: top-k experts of each token and the softmax of their logits.
-// One warp per token; lane l holds logits l, l+32, ... (E <= 1024).  Each of
-// the k rounds takes the warp-wide largest logit not yet chosen, ties going
-// to the lower expert index, so the choice is exact and deterministic.
+// Router: top-k experts of one token and the softmax of their logits, for
+// one warp.  Lane l holds logits l, l+32, ... (E <= 1024).  Each of the k
+// rounds takes the warp-wide largest logit not yet chosen, ties going to the
+// lower expert index, so the choice is exact and deterministic.  Round j
+// calls pick(j, expert, w) on every lane with the same values, w =
+// exp(logit - top) unnormalised; returns the sum of the k weights.
+template <class Pick>
+__device__ __forceinline__ float topk_warp(const float* __restrict__ row, int E, int k, int lane,
+                                           Pick pick) {
+  float v[32];
+#pragma unroll
+  for (int i = 0; i < 32; ++i) {
+    const int e = lane + 32 * i;
+    v[i] = (e < E) ? row[e] : -INFINITY;
+  }
+  uint32_t taken = 0;
+  float top = 0.f, sum = 0.f;
+  for (int j = 0; j < k; ++j) {
+    float bv = -INFINITY;
+    int bi = 0x7fffffff;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      const int e = lane + 32 * i;
+      if (e < E && !((taken >> i) & 1u) && (v[i] > bv || bi == 0x7fffffff)) {
+        bv = v[i];
+        bi = e;
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+      const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+      if (ov > bv || (ov == bv && oi < bi)) {
+        bv = ov;
+        bi = oi;
+      }
+    }
+    if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
+    if (j == 0) top = bv;
+    const float ex = expf(bv - top);
+    sum += ex;
+    pick(j, bi, ex);
+  }
+  return sum;
+}
+
+// One warp per token: topk_idx and the normalised probabilities.
 __global__ void __launch_bounds__(256) router_topk_kernel(const float* __restrict__ logits, int T,
                                                           int E, int k, int32_t* __restrict__ idx,
                                                           float* __restrict__ probs) {
   const int lane = threadIdx.x & 31;
   const int warps = gridDim.x * (blockDim.x >> 5);
   for (int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); t < T; t += warps) {
-    float v[32];
-    const float* row = logits + static_cast<long long>(t) * E;
-#pragma unroll
-    for (int i = 0; i < 32; ++i) {
-      const int e = lane + 32 * i;
-      v[i] = (e < E) ? row[e] : -INFINITY;
-    }
-    uint32_t taken = 0;
-    float top = 0.f, sum = 0.f;
-    for (int j = 0; j < k; ++j) {
-      float bv = -INFINITY;
-      int bi = 0x7fffffff;
-#pragma unroll
-      for (int i = 0; i < 32; ++i) {
-        const int e = lane + 32 * i;
-        if (e < E && !((taken >> i) & 1u) && (v[i] > bv || bi == 0x7fffffff)) {
-          bv = v[i];
-          bi = e;
-        }
-      }
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) {
-        const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-        const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-        if (ov > bv || (ov == bv && oi < bi)) {
-          bv = ov;
-          bi = oi;
-        }
-      }
-      if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
-      if (j == 0) top = bv;
-      const float ex = expf(bv - top);
-      sum += ex;
-      if (lane == 0) {
-        idx[static_cast<long long>(t) * k + j] = bi;
-        probs[static_cast<long long>(t) * k + j] = ex;   // normalised below
-      }
-    }
+    const long long p0 = static_cast<long long>(t) * k;
+    const float sum = topk_warp(logits + static_cast<long long>(t) * E, E, k, lane,
+                                [&](int j, int e, float w) {
+                                  if (lane == 0) {
+                                    idx[p0 + j] = e;
+                                    probs[p0 + j] = w;   // normalised below
+                                  }
+                                });
     __syncwarp();
-    for (int j = lane; j < k; j += 32) probs[static_cast<long long>(t) * k + j] /= sum;
+    for (int j = lane; j < k; j += 32) probs[p0 + j] /= sum;
+  }
+}
+
+// The router fused into the routing layout's first pass ([TE] "Transformer
+// Engine이 제공하는 세 가지 구성 요소": gate, top-k selection, dispatch and the
+// grouped FFN in one fused block): the same selection as router_topk_kernel,
+// and each chosen pair counted into its chunk's histogram ws[c][e] (c = pair
+// / kChunk; integer atomics, so the counts do not depend on their order; ws
+// is zeroed by route_fill).
+__global__ void __launch_bounds__(256) route_topk_hist(const float* __restrict__ logits, int T,
+                                                       int E, int k, int32_t* __restrict__ idx,
+                                                       float* __restrict__ probs,
+                                                       int32_t* __restrict__ ws) {
+  const int lane = threadIdx.x & 31;
+  const int warps = gridDim.x * (blockDim.x >> 5);
+  for (int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); t < T; t += warps) {
+    const long long p0 = static_cast<long long>(t) * k;
+    const float sum = topk_warp(logits + static_cast<long long>(t) * E, E, k, lane,
+                                [&](int j, int e, float w) {
+                                  if (lane == 0) {
+                                    idx[p0 + j] = e;
+                                    probs[p0 + j] = w;
+                                    atomicAdd(&ws[((p0 + j) / kChunk) * E + e], 1);
+                                  }
+                                });
+    __syncwarp();
+    for (int j = lane; j < k; j += 32) probs[p0 + j] /= sum;
+  }
+}
+
+// pair_of_row <- -1 and, for the fused router, the chunk histograms <- 0
+__global__ void route_fill2(int32_t* __restrict__ p, int n, int32_t* __restrict__ z, int nz) {
+  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n + nz; i += gridDim.x * blockDim.x) {
+    if (i < n) p[i] = -1;
+    else z[i - n] = 0;
   }
 }
 
@@ -219,6 +267,40 @@ cudaError_t launch_router_topk(const float* logits, int T, int E, int k, int32_t
   const long long want = (static_cast<long long>(T) + 7) / 8;
   const int blocks = static_cast<int>(want < 16LL * num_sms ? want : 16LL * num_sms);
   router_topk_kernel<<<blocks, 256, 0, s>>>(logits, T, E, k, idx, probs);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_route_logits(const float* logits, int T, int k, int E, int align, int M_cap,
+                               int32_t* topk_idx, float* probs, int32_t* counts,
+                               int32_t* offsets, int32_t* row_of_pair, int32_t* pair_of_row,
+                               int32_t* true_total, void* workspace, int32_t* err, int num_sms,
+                               cudaStream_t s, int* launches) {
+  const int P = T * k;
+  const int nchunks = (P + kChunk - 1) / kChunk;
+  int32_t* ws = static_cast<int32_t*>(workspace);
+  int32_t* demanded = ws + static_cast<long long>(nchunks) * E;
+  *launches = 0;
+  const long long nfill = static_cast<long long>(M_cap) + static_cast<long long>(nchunks) * E;
+  if (nfill > 0) {
+    const int blocks = static_cast<int>(min((nfill + 255) / 256, 4LL * num_sms));
+    route_fill2<<<blocks, 256, 0, s>>>(pair_of_row, M_cap, ws, nchunks * E);
+    ++*launches;
+  }
+  if (T > 0) {
+    const long long want = (static_cast<long long>(T) + 7) / 8;
+    const int blocks = static_cast<int>(want < 16LL * num_sms ? want : 16LL * num_sms);
+    route_topk_hist<<<blocks, 256, 0, s>>>(logits, T, E, k, topk_idx, probs, ws);
+    ++*launches;
+  }
+  route_scan<<<1, 1024, 0, s>>>(ws, nchunks, E, align, M_cap, counts, offsets, demanded,
+                                true_total, err);
+  ++*launches;
+  if (nchunks > 0) {
+    const size_t sm = static_cast<size_t>(E) * (1 + kWarps) * sizeof(int32_t);
+    route_rank<<<nchunks, kThreads, sm, s>>>(topk_idx, P, E, M_cap, ws, demanded, row_of_pair,
+                                             pair_of_row);
+    ++*launches;
+  }
   return cudaGetLastError();
 }
 

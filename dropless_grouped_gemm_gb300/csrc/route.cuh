@@ -26,6 +26,15 @@ cudaError_t launch_route(const int32_t* topk_idx, int T, int k, int E, int align
                          int32_t* pair_of_row, int32_t* true_total, void* workspace,
                          int32_t* err, int num_sms, cudaStream_t s, int* launches);
 
+// The router fused into the layout: top-k selection and softmax from the
+// logits [T, E] (writes topk_idx and probs) inside the layout's first pass,
+// then the same offsets and maps as launch_route.
+cudaError_t launch_route_logits(const float* logits, int T, int k, int E, int align, int M_cap,
+                                int32_t* topk_idx, float* probs, int32_t* counts,
+                                int32_t* offsets, int32_t* row_of_pair, int32_t* pair_of_row,
+                                int32_t* true_total, void* workspace, int32_t* err, int num_sms,
+                                cudaStream_t s, int* launches);
+
 cudaError_t launch_permute(const uint16_t* src, const float* scale, const int32_t* pair_of_row,
                            int T, int k, int d, int M_cap, uint16_t* dst, int num_sms,
                            cudaStream_t s);

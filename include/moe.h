@@ -204,6 +204,23 @@ int moe_route_offsets(const int32_t* topk_idx, int T, int k, int E, int align,
                       int32_t* err, void* stream);
 
 /*
+ * moe_route_logits - the router fused into the routing layout ([TE]
+ * "Transformer Engine이 제공하는 세 가지 구성 요소": gate, top-K selection,
+ * dispatch and the grouped FFN form one fused block).  The top-k selection
+ * and softmax of moe_router_topk run inside the layout's first pass, which
+ * also counts each chosen pair, so no separate router launch is needed.
+ *   logits [T, E] float32; writes topk_idx [T, k] and probs [T, k] (bit for
+ *   bit what moe_router_topk writes) and the outputs of moe_route_offsets
+ *   (counts, offsets, row_of_pair, pair_of_row, true_total), with the same
+ *   workspace (moe_route_workspace_size), alignment, overflow and error
+ *   rules.  Four launches (fill, fused select + count, scan, rank).
+ */
+int moe_route_logits(const float* logits, int T, int E, int k, int align, int M_cap,
+                     int32_t* topk_idx, float* probs, int32_t* counts, int32_t* offsets,
+                     int32_t* row_of_pair, int32_t* pair_of_row, int32_t* true_total,
+                     void* workspace, size_t ws_bytes, int32_t* err, void* stream);
+
+/*
  * moe_route_offsets_noalloc - moe_route_offsets for callers that cannot
  * allocate device memory.  The pages have no counterpart; this exists for
  * code that runs where cudaMalloc is off limits: inside a CUDA-graph

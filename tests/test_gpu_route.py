@@ -113,3 +113,36 @@ def test_router_then_layout_on_zipf_logits():
     ro = O.route_offsets(oi, w.E, 1)
     assert r["offsets"].cpu().numpy().tolist() == ro["offsets"].tolist()
     assert r["row_of_pair"].cpu().numpy().tolist() == ro["row_of_pair"].tolist()
+
+
+# T * k not a multiple of the 4,096-pair chunk, with tokens whose k pairs
+# straddle a chunk boundary (k = 3), an expert count above 1,024 / 2 and a
+# one-expert layer
+@pytest.mark.parametrize("T,E,k,align", [(4096, 256, 8, 1), (3000, 600, 3, 32), (700, 1, 1, 8),
+                                         (0, 16, 2, 1)])
+def test_fused_router_layout_equals_router_then_layout(T, E, k, align):
+    """moe_route_logits (top-k fused into the layout's first pass) writes the
+    router's topk_idx and probs and the layout's outputs bit for bit as the
+    separate router followed by moe_route_offsets, and matches the oracle."""
+    import dropless_grouped_gemm_gb300 as M
+    rng = np.random.default_rng(T + E + k)
+    lg = rng.standard_normal((T, E)).astype(np.float32)
+    if T > 2:
+        lg[0, :] = 0.25                               # all tied
+        lg[1, [0, E - 1]] = 9.0                       # tie at the top
+    lt = torch.from_numpy(lg).cuda()
+    fused = M.route_logits(lt, k, align)
+    if T > 0:
+        assert M.last_launch_count() == 4           # no separate router launch
+    idx, p = M.router_topk(lt, k)
+    sep = M.route_offsets(idx, E, align)
+    torch.cuda.synchronize()
+    assert int(fused["err"].item()) == 0
+    assert torch.equal(fused["topk_idx"], idx) and torch.equal(fused["probs"], p)
+    for k_ in ("counts", "offsets", "row_of_pair", "pair_of_row", "true_total"):
+        assert torch.equal(fused[k_], sep[k_]), k_
+    if T > 0:
+        oi, _ = O.router_topk(lg.astype(np.float64), k)
+        ro = O.route_offsets(oi, E, align)
+        assert fused["offsets"].cpu().numpy().tolist() == ro["offsets"].tolist()
+        assert fused["row_of_pair"].cpu().numpy().tolist() == ro["row_of_pair"].tolist()
