@@ -137,17 +137,23 @@ __global__ void __launch_bounds__(256)
                           (e4m3x2(bf16_lo(x[i][3]) * inv[6], bf16_hi(x[i][3]) * inv[7]) << 16);
       q[(row0 + i) * d8 + c8] = make_uint2(w0, w1);
     }
-    if (half == 0) {   // scales: chunk (b/4, c/128) of expert e
+    {   // column scales, chunk (b/4, c/128) of expert e: both halves hold the
+        // same codes, half 0 stores columns 8i..8i+3 and half 1 8i+4..8i+7
+        // (each store then touches the chunk's 4 lines once per warp)
       uint8_t* se = s + static_cast<long long>(e) * (n / 32) * d;
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const int c = c8 * 8 + j;
+      for (int jj = 0; jj < 4; ++jj) {
+        const int c = c8 * 8 + jj + 4 * half;
         const long long chunk = static_cast<long long>(b / 4) * (d / 128) + c / 128;
-        se[chunk * 512 + mx_chunk_off(c & 127, b & 3)] = static_cast<uint8_t>(code[j]);
+        se[chunk * 512 + mx_chunk_off(c & 127, b & 3)] =
+            static_cast<uint8_t>(half ? code[jj + 4] : code[jj]);
       }
     }
     {
       const int c = c8 * 8;                     // first column of this lane
+      // the 4 block scales of row 16 * half + l end in lane 16 * half + l
+      // (gathered by shuffles), stored as one 4-byte word per row
+      uint32_t my_row_sc = 0;
 #pragma unroll
       for (int i = 0; i < 16; ++i) {
         float m = 0.f;
@@ -163,12 +169,19 @@ __global__ void __launch_bounds__(256)
                             (e4m3x2(bf16_lo(x[i][3]) * iv, bf16_hi(x[i][3]) * iv) << 16);
         const long long r = row0 + i;
         qr[r * d8 + c8] = make_uint2(w0, w1);
-        if ((lane & 3) == 0) {                  // weight tiles of W2 viewed as [E*n, d]
-          const long long chunk = (r / 128) * (d / 128) + c / 128;
-          sr[chunk * 512 + mx_chunk_off(static_cast<int>(r & 127), (c / 32) & 3)] =
-              static_cast<uint8_t>(sc);
-        }
+        // lanes 16 * half + 4 cb hold this row's scale of column block cb
+        uint32_t packed = 0;
+#pragma unroll
+        for (int cb = 0; cb < 4; ++cb)
+          packed |= __shfl_sync(0xffffffffu, sc, (lane & 16) + 4 * cb) << (8 * cb);
+        if ((lane & 15) == i) my_row_sc = packed;
       }
+      // weight tiles of W2 viewed as [E*n, d]: row r's 4 bytes are
+      // contiguous in its chunk (the 4 column blocks of c / 128)
+      const long long r = row0 + (lane & 15);
+      const long long chunk = (r / 128) * (d / 128) + c / 128;
+      *reinterpret_cast<uint32_t*>(sr + chunk * 512 + mx_chunk_off(static_cast<int>(r & 127), 0)) =
+          my_row_sc;
     }
   }
 }
