@@ -286,34 +286,48 @@ __global__ void __launch_bounds__(256)
 
 // ---------------------------------------------------------------- row-wise weights
 // [rows, cols] with blocks of 32 along cols, scales in weight tiles (128-row
-// tiles from row 0); one thread per 32-value block
+// tiles from row 0).  A warp takes 32 consecutive blocks (2 KB, contiguous
+// since cols is a multiple of 128): in its k-th load lane l reads 16-byte
+// piece 32k + l, so each load instruction covers 512 contiguous bytes; lane
+// l then holds a quarter (8 values) of blocks 8k + l/4, and a block's
+// maximum takes two shuffles across its 4 lanes.
 __global__ void __launch_bounds__(256)
     mx_quantize_rows_w_kernel(const uint4* __restrict__ src, long long rows, int cols,
-                              uint4* __restrict__ q, uint8_t* __restrict__ s) {
+                              uint2* __restrict__ q, uint8_t* __restrict__ s) {
+  const int lane = threadIdx.x & 31;
   const int cb_n = cols / 32;
-  const long long total = rows * cb_n;
-  for (long long g = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; g < total;
-       g += static_cast<long long>(gridDim.x) * blockDim.x) {
-    const long long r = g / cb_n;
-    const int cb = static_cast<int>(g - r * cb_n);
-    const uint4* p = src + g * 4;                 // 32 bf16 = 4 x 16 bytes
-    float v[32];
+  const long long nwarps = rows * cb_n / 32;         // cols / 32 is a multiple of 4; see the launch
+  for (long long wi = (blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x) / 32;
+       wi < nwarps; wi += static_cast<long long>(gridDim.x) * blockDim.x / 32) {
+    const long long g0 = wi * 32;                    // first block of the warp
+    uint32_t x[4][4];
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
-      const uint4 x = __ldg(p + k);
-      const uint32_t xw[4] = {x.x, x.y, x.z, x.w};
+      const uint4 v = __ldg(src + g0 * 4 + 32 * k + lane);
+      x[k][0] = v.x; x[k][1] = v.y; x[k][2] = v.z; x[k][3] = v.w;
+    }
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        v[8 * k + 2 * j] = bf16_lo(xw[j]);
-        v[8 * k + 2 * j + 1] = bf16_hi(xw[j]);
+    for (int k = 0; k < 4; ++k) {
+      float m = 0.f;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) m = fmaxf(m, fmaxf(fabsf(bf16_lo(x[k][j])), fabsf(bf16_hi(x[k][j]))));
+      m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
+      m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
+      const uint32_t sc = mx_scale_code(m);
+      const float iv = mx_inv_scale(sc);
+      const uint32_t w0 = e4m3x2(bf16_lo(x[k][0]) * iv, bf16_hi(x[k][0]) * iv) |
+                          (e4m3x2(bf16_lo(x[k][1]) * iv, bf16_hi(x[k][1]) * iv) << 16);
+      const uint32_t w1 = e4m3x2(bf16_lo(x[k][2]) * iv, bf16_hi(x[k][2]) * iv) |
+                          (e4m3x2(bf16_lo(x[k][3]) * iv, bf16_hi(x[k][3]) * iv) << 16);
+      q[g0 * 4 + 32 * k + lane] = make_uint2(w0, w1);  // 8 codes: 256 contiguous bytes a warp
+      if ((lane & 3) == 0) {
+        const long long g = g0 + 8 * k + lane / 4;       // this block
+        const long long r = g / cb_n;
+        const int cb = static_cast<int>(g - r * cb_n);
+        const long long chunk = (r / 128) * (cols / 128) + cb / 4;
+        s[chunk * 512 + mx_chunk_off(static_cast<int>(r & 127), cb & 3)] = static_cast<uint8_t>(sc);
       }
     }
-    uint32_t qw[8];
-    const uint32_t sc = mx_quant32(v, qw);
-    q[2 * g] = make_uint4(qw[0], qw[1], qw[2], qw[3]);
-    q[2 * g + 1] = make_uint4(qw[4], qw[5], qw[6], qw[7]);
-    const long long chunk = (r / 128) * (cols / 128) + cb / 4;
-    s[chunk * 512 + mx_chunk_off(static_cast<int>(r & 127), cb & 3)] = static_cast<uint8_t>(sc);
   }
 }
 
@@ -981,11 +995,13 @@ cudaError_t launch_mx_quantize_act(const uint16_t* src, int rows, int cols, cons
 
 cudaError_t launch_mx_quantize_rows_w(const uint16_t* src, long long rows, int cols, uint8_t* q,
                                       uint8_t* s, int num_sms, cudaStream_t st) {
+  // one warp per 32 blocks (rows * cols / 32 is a multiple of 32: rows and
+  // cols are multiples of 128)
   const long long threads = rows * (cols / 32);
   const long long want = (threads + 255) / 256;
   const int blocks = static_cast<int>(want < 16LL * num_sms ? want : 16LL * num_sms);
   mx_quantize_rows_w_kernel<<<blocks > 0 ? blocks : 1, 256, 0, st>>>(
-      reinterpret_cast<const uint4*>(src), rows, cols, reinterpret_cast<uint4*>(q), s);
+      reinterpret_cast<const uint4*>(src), rows, cols, reinterpret_cast<uint2*>(q), s);
   return cudaGetLastError();
 }
 
