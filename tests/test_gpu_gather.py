@@ -124,3 +124,37 @@ def test_gather_full_size_zipf_layer_equals_permuted():
         assert torch.equal(o2[k_], o[k_]), k_
     del inp, o, o2
     torch.cuda.empty_cache()
+
+
+def test_gather_routed_backward_accumulates_like_permuted():
+    """MOE_FLAG_ACCUMULATE_DW on the gathered routed backward: the weight
+    gradients added to the given ones equal the permuted path's, bit for
+    bit, and the empty expert's stay untouched."""
+    import dropless_grouped_gemm_gb300 as M
+    E, T, k, d, n, align = 6, 500, 2, 128, 128, 32
+    act = "swiglu"
+    rng = np.random.default_rng(83)
+    idx = np.stack([rng.permutation(E)[:k] for _ in range(T)]).astype(np.int32)
+    idx[idx == E - 1] = E - 2                     # expert E-1 empty
+    probs = torch.from_numpy(rng.random((T, k)).astype(np.float32)).cuda().view(-1)
+    r = M.route_offsets(cuda_i32(idx), E, align)
+    M_cap = r["pair_of_row"].numel()
+    x = W.normal((T, d), (83, W.X, 0), 1.0, "cuda")
+    dO = W.normal((T, d), (83, W.DO, 0), 1.0, "cuda")
+    H = W.normal((M_cap, 2 * n), (83, W.X, 1), 1.0, "cuda")
+    W1 = W.w1_interleaved(83, E, d, n, 0.05, "cuda")
+    W2 = W.w2(83, E, n, d, 0.05, "cuda")
+    old1 = W.normal(tuple(W1.shape), (83, W.X, 90), 0.5, "cuda")
+    old2 = W.normal(tuple(W2.shape), (83, W.X, 91), 0.5, "cuda")
+    pr, off = r["pair_of_row"], r["offsets"]
+    xp, dop = M.permute(x, pr, k), M.permute(dO, pr, k)
+    a1, a2 = old1.clone(), old2.clone()
+    b1, b2 = old1.clone(), old2.clone()
+    M.grouped_mlp_bwd_routed(xp, H, dop, pr, probs, off, W1, W2, act, dW1=a1, dW2=a2,
+                             accumulate_dw=True)
+    M.grouped_mlp_bwd_routed_gather(x, dO, pr, k, H, probs, off, W1, W2, act, dW1=b1, dW2=b2,
+                                    accumulate_dw=True)
+    torch.cuda.synchronize()
+    assert torch.equal(a1, b1) and torch.equal(a2, b2)
+    assert torch.equal(b1[E - 1], old1[E - 1]) and torch.equal(b2[E - 1], old2[E - 1])
+    assert not torch.equal(b1[0], old1[0])
