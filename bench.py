@@ -63,8 +63,9 @@ def useful_flops(w, M):
 
 def kernel_work(w, M, E_ne):
     """Algorithmic FLOPs and bytes per launch of each grouped GEMM (bf16 =
-    2 B; weights of non-empty experts only; weight gradients of all
-    experts, written as zeros for empty ones)."""
+    2 B; weights of non-empty experts only, also in the weight quantisers,
+    which skip the empty experts; weight gradients of all experts, written
+    as zeros for empty ones)."""
     d, n, n1, E = w.d, w.n, w.n1, w.E
     B = 2
     if w.mxfp8:
@@ -73,7 +74,7 @@ def kernel_work(w, M, E_ne):
         # GEMMs stream E4M3 codes (1 B) plus one scale byte per 32 codes
         mxb = lambda elems: elems + elems // 32
         work = {
-            "mx_quantize_weights": (0, E * n * d * 2 + mxb(E * n * d)),
+            "mx_quantize_weights": (0, E_ne * n * d * 2 + mxb(E_ne * n * d)),
             "fc1_act": (2 * M * d * n1, B * (M * d + E_ne * d * n1 + M * n) + 2 * mxb(M * n) +
                         (B * M * n1 if w.backward else 0)),
             "fc2": (2 * M * n * d, mxb(M * n) + mxb(E_ne * n * d) + B * M * d),
@@ -81,8 +82,8 @@ def kernel_work(w, M, E_ne):
         if w.backward:
             work.update({
                 # W2 read once, both MXFP8 copies written
-                "mx_quantize_weights2": (0, E * n * d * 2 + 2 * mxb(E * n * d)),
-                "mx_quantize_w1_rows": (0, E * d * n1 * 2 + mxb(E * d * n1)),
+                "mx_quantize_weights2": (0, E_ne * n * d * 2 + 2 * mxb(E_ne * n * d)),
+                "mx_quantize_w1_rows": (0, E_ne * d * n1 * 2 + mxb(E_ne * d * n1)),
                 "mx_quantize_dy": (0, B * M * d + 2 * mxb(M * d)),
                 "mx_quantize_x": (0, B * M * d + mxb(M * d)),
                 "mx_retile_a": (0, 2 * (M * n // 32)),
@@ -274,7 +275,7 @@ def make_step(w, inp, o):
         """MXFP8 backward: weights quantised along their data-gradient
         reduction index, then the eight launches of grouped_mlp_bwd_mx."""
         mx, mb = o["mx"], o["mxb"]
-        M.mx_quantize_weights_rowwise(inp["W1"], mb["w1_q"], mb["w1_s"])
+        M.mx_quantize_weights_rowwise(inp["W1"], mb["w1_q"], mb["w1_s"], offsets=offsets)
         ops = dict(a_qT=mx["a_qT"], a_sT=mx["a_sT"], w2_q=mb["w2_q"], w2_s=mb["w2_s"],
                    w1_q=mb["w1_q"], w1_s=mb["w1_s"])
         M.grouped_mlp_bwd_mx(x_perm, o["h"], dy_perm, offsets, ops, act, dh=o["dh"],
@@ -285,7 +286,7 @@ def make_step(w, inp, o):
     if w.routing == "identity" and w.mxfp8:
         def step_mx_id():
             M.mx_quantize_weights2(inp["W2"], o["mx"]["w2_q"], o["mx"]["w2_s"], o["mxb"]["w2_q"],
-                                   o["mxb"]["w2_s"])
+                                   o["mxb"]["w2_s"], offsets=inp["offsets"])
             n = M.last_launch_count()
             M.grouped_mlp_fwd(inp["x_perm"], inp["offsets"], inp["W1"], inp["W2"], act,
                               save_h=True, h_saved=o["h"], a=o["a"], y_perm=o["y_perm"],
@@ -317,7 +318,7 @@ def make_step(w, inp, o):
             M.permute(inp["x"], r["pair_of_row"], k, out=o["x_perm"])
             n += M.last_launch_count()
             M.mx_quantize_weights2(inp["W2"], o["mx"]["w2_q"], o["mx"]["w2_s"], o["mxb"]["w2_q"],
-                                   o["mxb"]["w2_s"])
+                                   o["mxb"]["w2_s"], offsets=r["offsets"])
             n += M.last_launch_count()
             M.grouped_mlp_fwd(o["x_perm"], r["offsets"], inp["W1"], inp["W2"], act, save_h=True,
                               h_saved=o["h"], a=o["a"], y_perm=o["y_perm"], err=o["err"],
@@ -345,7 +346,7 @@ def make_step(w, inp, o):
             n += M.last_launch_count()
             M.permute(inp["x"], r["pair_of_row"], k, out=o["x_perm"])
             n += M.last_launch_count()
-            M.mx_quantize_weights(inp["W2"], o["mx"]["w2_q"], o["mx"]["w2_s"])
+            M.mx_quantize_weights(inp["W2"], o["mx"]["w2_q"], o["mx"]["w2_s"], offsets=r["offsets"])
             n += M.last_launch_count()
             M.grouped_mlp_fwd(o["x_perm"], r["offsets"], inp["W1"], inp["W2"], act, a=o["a"],
                               y_perm=o["y_perm"], err=o["err"], mx=o["mx"])

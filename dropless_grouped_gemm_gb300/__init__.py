@@ -98,7 +98,7 @@ def lib():
         L.moe_grouped_mlp_fwd.argtypes = [vp, vp, i32, i32, i32, i32, vp, vp, i32, i32, vp, vp, vp,
                                           vp, vp, vp, vp]
         L.moe_mx_quantize_weights.restype = i32
-        L.moe_mx_quantize_weights.argtypes = [vp, i32, i32, i32, vp, vp, vp]
+        L.moe_mx_quantize_weights.argtypes = [vp, i32, i32, i32, vp, vp, vp, vp]
         L.moe_mx_quantize.restype = i32
         L.moe_mx_quantize.argtypes = [vp, i32, i32, vp, i32, vp, vp, vp, vp, vp, vp]
         L.moe_set_launch_events.restype = i32
@@ -109,9 +109,9 @@ def lib():
         L.moe_grouped_mlp_bwd.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, vp, vp, i32, i32,
                                           vp, vp, vp, vp, vp, vp, vp]
         L.moe_mx_quantize_weights2.restype = i32
-        L.moe_mx_quantize_weights2.argtypes = [vp, i32, i32, i32, vp, vp, vp, vp, vp]
+        L.moe_mx_quantize_weights2.argtypes = [vp, i32, i32, i32, vp, vp, vp, vp, vp, vp]
         L.moe_mx_quantize_weights_rowwise.restype = i32
-        L.moe_mx_quantize_weights_rowwise.argtypes = [vp, i32, i32, vp, vp, vp]
+        L.moe_mx_quantize_weights_rowwise.argtypes = [vp, i32, i32, vp, i32, vp, vp, vp]
         L.moe_mx_bwd_workspace_size.restype = sz
         L.moe_mx_bwd_workspace_size.argtypes = [i32, i32, i32, i32]
         L.moe_grouped_mlp_bwd_mx.restype = i32
@@ -445,18 +445,31 @@ def mx_buffers(E: int, n: int, d: int, M_cap: int, device, transposed: bool = Tr
     return b
 
 
+def _offsets_arg(offsets, E):
+    if offsets is None:
+        return None
+    _need(offsets, torch.int32, "offsets", 1)
+    if offsets.numel() != E + 1:
+        raise ValueError(f"offsets has {offsets.numel()} entries, want E+1 = {E + 1}")
+    return offsets
+
+
 def mx_quantize_weights(W2: torch.Tensor, w2_q: torch.Tensor | None = None,
-                        w2_s: torch.Tensor | None = None, stream=None):
-    """MXFP8 codes and MMA-tiled scales of W2 [E, n, d] (moe_mx_quantize_weights)."""
+                        w2_s: torch.Tensor | None = None, stream=None, offsets=None):
+    """MXFP8 codes and MMA-tiled scales of W2 [E, n, d] (moe_mx_quantize_weights).
+    With the routing ``offsets``, experts without rows are skipped (left as
+    they were in w2_q / w2_s)."""
     _need(W2, torch.bfloat16, "W2", 3)
     E, n, d = W2.shape
+    offsets = _offsets_arg(offsets, E)
     if w2_q is None:
         w2_q = torch.empty((E, n, d), dtype=torch.uint8, device=W2.device)
     if w2_s is None:
         w2_s = torch.empty(E * (n // 32) * d, dtype=torch.uint8, device=W2.device)
     _need(w2_q, torch.uint8, "w2_q")
     _need(w2_s, torch.uint8, "w2_s")
-    rc = lib().moe_mx_quantize_weights(_ptr(W2), E, n, d, _ptr(w2_q), _ptr(w2_s), _stream(stream))
+    rc = lib().moe_mx_quantize_weights(_ptr(W2), E, n, d, _ptr(offsets), _ptr(w2_q), _ptr(w2_s),
+                                       _stream(stream))
     _check(rc, "moe_mx_quantize_weights")
     return w2_q, w2_s
 
@@ -481,19 +494,26 @@ def mx_quantize(src: torch.Tensor, offsets: torch.Tensor, transposed: bool = Tru
 
 
 def mx_quantize_weights_rowwise(W: torch.Tensor, q: torch.Tensor | None = None,
-                                s: torch.Tensor | None = None, stream=None):
+                                s: torch.Tensor | None = None, stream=None, offsets=None):
     """MXFP8 codes of a weight with blocks along its last axis and scales in
-    weight tiles (moe_mx_quantize_weights_rowwise); W is [E, R, K] or [R, K]."""
+    weight tiles (moe_mx_quantize_weights_rowwise); W is [E, R, K] or [R, K].
+    With the routing ``offsets`` (W then [E, R, K]), experts without rows
+    are skipped (left as they were in q / s)."""
     _need(W, torch.bfloat16, "W")
     K = W.shape[-1]
     rows = W.numel() // K
+    E = W.shape[0] if offsets is not None else 0
+    if offsets is not None and W.dim() != 3:
+        raise ValueError("offsets needs W as [E, R, K]")
+    offsets = _offsets_arg(offsets, E) if offsets is not None else None
     if q is None:
         q = torch.empty(tuple(W.shape), dtype=torch.uint8, device=W.device)
     if s is None:
         s = torch.empty(rows * K // 32, dtype=torch.uint8, device=W.device)
     _need(q, torch.uint8, "q")
     _need(s, torch.uint8, "s")
-    rc = lib().moe_mx_quantize_weights_rowwise(_ptr(W), rows, K, _ptr(q), _ptr(s), _stream(stream))
+    rc = lib().moe_mx_quantize_weights_rowwise(_ptr(W), rows, K, _ptr(offsets), E, _ptr(q), _ptr(s),
+                                               _stream(stream))
     _check(rc, "moe_mx_quantize_weights_rowwise")
     return q, s
 
@@ -647,12 +667,14 @@ def router_grad_rows(ds_part, row_of_pair, T: int, k: int, dprobs=None, stream=N
 
 
 def mx_quantize_weights2(W2: torch.Tensor, w2_q=None, w2_s=None, w2_q_rows=None, w2_s_rows=None,
-                         stream=None):
+                         stream=None, offsets=None):
     """Both MXFP8 copies of W2 [E, n, d] from one read (moe_mx_quantize_weights2):
     blocks along n (w2_q, w2_s; forward FC2) and along d (w2_q_rows,
-    w2_s_rows; backward FC2-dgrad).  Returns the four tensors."""
+    w2_s_rows; backward FC2-dgrad).  Returns the four tensors.  With the
+    routing ``offsets``, experts without rows are skipped."""
     _need(W2, torch.bfloat16, "W2", 3)
     E, n, d = W2.shape
+    offsets = _offsets_arg(offsets, E)
     u8 = torch.uint8
     dev = W2.device
     if w2_q is None:
@@ -665,8 +687,8 @@ def mx_quantize_weights2(W2: torch.Tensor, w2_q=None, w2_s=None, w2_q_rows=None,
         w2_s_rows = torch.empty(E * n * d // 32, dtype=u8, device=dev)
     for t, nm in ((w2_q, "w2_q"), (w2_s, "w2_s"), (w2_q_rows, "w2_q_rows"), (w2_s_rows, "w2_s_rows")):
         _need(t, u8, nm)
-    rc = lib().moe_mx_quantize_weights2(_ptr(W2), E, n, d, _ptr(w2_q), _ptr(w2_s), _ptr(w2_q_rows),
-                                        _ptr(w2_s_rows), _stream(stream))
+    rc = lib().moe_mx_quantize_weights2(_ptr(W2), E, n, d, _ptr(offsets), _ptr(w2_q), _ptr(w2_s),
+                                        _ptr(w2_q_rows), _ptr(w2_s_rows), _stream(stream))
     _check(rc, "moe_mx_quantize_weights2")
     return w2_q, w2_s, w2_q_rows, w2_s_rows
 

@@ -621,14 +621,14 @@ int moe_router_grad_rows(const float* ds_part, int n_parts, const int32_t* row_o
   return cuda_rc(e);
 }
 
-int moe_mx_quantize_weights(const moe_bf16* W2, int E, int n, int d, uint8_t* w2_q,
-                            uint8_t* w2_s, void* stream) {
-  return moe_mx_quantize_weights2(W2, E, n, d, w2_q, w2_s, nullptr, nullptr, stream);
+int moe_mx_quantize_weights(const moe_bf16* W2, int E, int n, int d, const int32_t* offsets,
+                            uint8_t* w2_q, uint8_t* w2_s, void* stream) {
+  return moe_mx_quantize_weights2(W2, E, n, d, offsets, w2_q, w2_s, nullptr, nullptr, stream);
 }
 
-int moe_mx_quantize_weights2(const moe_bf16* W2, int E, int n, int d, uint8_t* w2_q,
-                             uint8_t* w2_s, uint8_t* w2_q_rows, uint8_t* w2_s_rows,
-                             void* stream) {
+int moe_mx_quantize_weights2(const moe_bf16* W2, int E, int n, int d, const int32_t* offsets,
+                             uint8_t* w2_q, uint8_t* w2_s, uint8_t* w2_q_rows,
+                             uint8_t* w2_s_rows, void* stream) {
   g_last_launches = 0;
   if (E < 1 || E > MOE_MAX_EXPERTS || n <= 0 || d <= 0 || n % 128 || d % 128) return MOE_E_SIZE;
   if (!W2 || !w2_q || !w2_s || (w2_q_rows && !w2_s_rows)) return MOE_E_NULL;
@@ -639,8 +639,8 @@ int moe_mx_quantize_weights2(const moe_bf16* W2, int E, int n, int d, uint8_t* w
   if (sms <= 0) return MOE_E_CUDA;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   ev_begin(s);
-  const cudaError_t e = moe::launch_mx_quantize_weights(W2, E, n, d, w2_q, w2_s, w2_q_rows,
-                                                        w2_s_rows, sms, s);
+  const cudaError_t e = moe::launch_mx_quantize_weights(W2, E, n, d, offsets, w2_q, w2_s,
+                                                        w2_q_rows, w2_s_rows, sms, s);
   ev_end(s);
   g_last_launches = 1;
   return cuda_rc(e);
@@ -768,17 +768,21 @@ int moe_activation_bwd(const moe_bf16* h, const moe_bf16* da, const int32_t* off
   return MOE_OK;
 }
 
-int moe_mx_quantize_weights_rowwise(const moe_bf16* W, int rows, int cols, uint8_t* q,
-                                    uint8_t* sc, void* stream) {
+int moe_mx_quantize_weights_rowwise(const moe_bf16* W, int rows, int cols,
+                                    const int32_t* offsets, int E, uint8_t* q, uint8_t* sc,
+                                    void* stream) {
   g_last_launches = 0;
   if (rows <= 0 || cols <= 0 || rows % 128 || cols % 128) return MOE_E_SIZE;
+  if (offsets && (E < 1 || E > MOE_MAX_EXPERTS || rows % E || (rows / E) % 128))
+    return MOE_E_SIZE;
   if (!W || !q || !sc) return MOE_E_NULL;
   if (misaligned(W) || misaligned(q)) return MOE_E_ALIGN;
   const int sms = num_sms_current();
   if (sms <= 0) return MOE_E_CUDA;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   ev_begin(s);
-  const cudaError_t e = moe::launch_mx_quantize_rows_w(W, rows, cols, q, sc, sms, s);
+  const cudaError_t e = moe::launch_mx_quantize_rows_w(W, rows, cols, offsets,
+                                                       offsets ? rows / E : rows, q, sc, sms, s);
   ev_end(s);
   g_last_launches = 1;
   return cuda_rc(e);

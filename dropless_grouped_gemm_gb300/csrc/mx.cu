@@ -30,20 +30,51 @@ namespace moe {
 namespace {
 
 // ---------------------------------------------------------------- weights
+// With the routing offsets given, an expert that holds no rows is skipped:
+// no GEMM reads its weights (its row tiles do not exist), so its codes and
+// scales are left as they were.  Each block first lists the used experts in
+// order (one warp, 32 experts a ballot) and the grid-stride loop then runs
+// over the used experts' work alone, as densely as over all experts.
+// Without offsets the list is the identity over n_all experts.  Every
+// thread of the block must call it (one barrier).
+__device__ __forceinline__ int used_experts(const int32_t* __restrict__ offsets, int n_all,
+                                            int* s_list, int* s_count) {
+  if (offsets == nullptr) return n_all;
+  if (threadIdx.x < 32) {
+    const int lane = threadIdx.x;
+    int cnt = 0;
+    for (int base = 0; base < n_all; base += 32) {
+      const int e = base + lane;
+      const bool used = e < n_all && __ldg(offsets + e + 1) != __ldg(offsets + e);
+      const uint32_t m = __ballot_sync(0xffffffffu, used);
+      if (used) s_list[cnt + __popc(m & ((1u << lane) - 1u))] = e;
+      cnt += __popc(m);
+    }
+    if (lane == 0) *s_count = cnt;
+  }
+  __syncthreads();
+  return *s_count;
+}
+
 // W2 [E, n, d] quantised for the forward FC2 alone: blocks of 32 rows (FC2's
 // reduction index n) per column.  One thread: 8 consecutive columns x one
 // 32-row block of one expert (a warp reads 512 contiguous bytes per row).
 __global__ void __launch_bounds__(256)
     mx_quantize_weights_kernel(const uint4* __restrict__ w, int E, int n, int d,
-                               uint2* __restrict__ q, uint8_t* __restrict__ s) {
+                               const int32_t* __restrict__ offsets, uint2* __restrict__ q,
+                               uint8_t* __restrict__ s) {
+  __shared__ int s_list[MOE_MAX_EXPERTS];
+  __shared__ int s_count;
+  const int ne = used_experts(offsets, E, s_list, &s_count);
   const int d8 = d / 8;
-  const long long total = static_cast<long long>(E) * (n / 32) * d8;
+  const long long total = static_cast<long long>(ne) * (n / 32) * d8;
   for (long long g = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; g < total;
        g += static_cast<long long>(gridDim.x) * blockDim.x) {
     const int c8 = static_cast<int>(g % d8);
     const long long eb = g / d8;
     const int b = static_cast<int>(eb % (n / 32));
-    const int e = static_cast<int>(eb / (n / 32));
+    const int eu = static_cast<int>(eb / (n / 32));
+    const int e = offsets ? s_list[eu] : eu;
     const long long row0 = static_cast<long long>(e) * n + 32LL * b;
     float v[32][8];
     float amax[8] = {0, 0, 0, 0, 0, 0, 0, 0};
@@ -95,19 +126,24 @@ __global__ void __launch_bounds__(256)
 // apart); a row's 32-column maximum combines four adjacent lanes.
 __global__ void __launch_bounds__(256)
     mx_quantize_w2_kernel(const uint4* __restrict__ w, int E, int n, int d,
+                          const int32_t* __restrict__ offsets,
                           uint2* __restrict__ q, uint8_t* __restrict__ s,
                           uint2* __restrict__ qr, uint8_t* __restrict__ sr) {
   const int lane = threadIdx.x & 31;
   const int half = lane >> 4;
   const int d8 = d / 8;
+  __shared__ int s_list[MOE_MAX_EXPERTS];
+  __shared__ int s_count;
+  const int ne = used_experts(offsets, E, s_list, &s_count);
   const int cw = d / 128;                                  // warps per 32-row block
-  const long long nwarps = static_cast<long long>(E) * (n / 32) * cw;
+  const long long nwarps = static_cast<long long>(ne) * (n / 32) * cw;
   for (long long wi = (blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x) / 32;
        wi < nwarps; wi += static_cast<long long>(gridDim.x) * blockDim.x / 32) {
     const int c8 = static_cast<int>(wi % cw) * 16 + (lane & 15);
     const long long eb = wi / cw;
     const int b = static_cast<int>(eb % (n / 32));
-    const int e = static_cast<int>(eb / (n / 32));
+    const int eu = static_cast<int>(eb / (n / 32));
+    const int e = offsets ? s_list[eu] : eu;
     const long long row0 = static_cast<long long>(e) * n + 32LL * b + 16 * half;
     uint32_t x[16][4];
     float amax[8] = {0, 0, 0, 0, 0, 0, 0, 0};
@@ -291,15 +327,25 @@ __global__ void __launch_bounds__(256)
 // piece 32k + l, so each load instruction covers 512 contiguous bytes; lane
 // l then holds a quarter (8 values) of blocks 8k + l/4, and a block's
 // maximum takes two shuffles across its 4 lanes.
+// With offsets, rows_per_e (a multiple of 128) rows make one expert: an
+// expert then starts at a block index that is a multiple of 512, so a warp's
+// 32 blocks and a 128-row scale tile never straddle two experts.
 __global__ void __launch_bounds__(256)
     mx_quantize_rows_w_kernel(const uint4* __restrict__ src, long long rows, int cols,
+                              const int32_t* __restrict__ offsets, long long rows_per_e,
                               uint2* __restrict__ q, uint8_t* __restrict__ s) {
+  __shared__ int s_list[MOE_MAX_EXPERTS];
+  __shared__ int s_count;
   const int lane = threadIdx.x & 31;
   const int cb_n = cols / 32;
-  const long long nwarps = rows * cb_n / 32;         // cols / 32 is a multiple of 4; see the launch
+  const int ne = used_experts(offsets, static_cast<int>(rows / rows_per_e), s_list, &s_count);
+  const long long warps_e = rows_per_e * cb_n / 32;  // cols / 32 is a multiple of 4; see the launch
+  const long long nwarps = ne * warps_e;
   for (long long wi = (blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x) / 32;
        wi < nwarps; wi += static_cast<long long>(gridDim.x) * blockDim.x / 32) {
-    const long long g0 = wi * 32;                    // first block of the warp
+    const long long eu = wi / warps_e;
+    const long long e = offsets ? s_list[eu] : eu;
+    const long long g0 = (e * warps_e + (wi - eu * warps_e)) * 32;   // first block of the warp
     uint32_t x[4][4];
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
@@ -955,15 +1001,16 @@ cudaError_t launch_mx_t(const CUtensorMap& ta, const CUtensorMap& tb, const CUte
 
 }  // namespace
 
-cudaError_t launch_mx_quantize_weights(const uint16_t* w2, int E, int n, int d, uint8_t* q,
-                                       uint8_t* s, uint8_t* q_rows, uint8_t* s_rows, int num_sms,
+cudaError_t launch_mx_quantize_weights(const uint16_t* w2, int E, int n, int d,
+                                       const int32_t* offsets, uint8_t* q, uint8_t* s,
+                                       uint8_t* q_rows, uint8_t* s_rows, int num_sms,
                                        cudaStream_t st) {
   if (q_rows) {
     const long long threads = static_cast<long long>(E) * (n / 32) * (d / 128) * 32;
     const long long want = (threads + 255) / 256;
     const int blocks = static_cast<int>(want < 16LL * num_sms ? want : 16LL * num_sms);
     mx_quantize_w2_kernel<<<blocks > 0 ? blocks : 1, 256, 0, st>>>(
-        reinterpret_cast<const uint4*>(w2), E, n, d, reinterpret_cast<uint2*>(q), s,
+        reinterpret_cast<const uint4*>(w2), E, n, d, offsets, reinterpret_cast<uint2*>(q), s,
         reinterpret_cast<uint2*>(q_rows), s_rows);
   } else {
     // the forward alone: the one-direction kernel streams faster (measured
@@ -973,7 +1020,7 @@ cudaError_t launch_mx_quantize_weights(const uint16_t* w2, int E, int n, int d, 
     const long long want = (threads + 255) / 256;
     const int blocks = static_cast<int>(want < 16LL * num_sms ? want : 16LL * num_sms);
     mx_quantize_weights_kernel<<<blocks > 0 ? blocks : 1, 256, 0, st>>>(
-        reinterpret_cast<const uint4*>(w2), E, n, d, reinterpret_cast<uint2*>(q), s);
+        reinterpret_cast<const uint4*>(w2), E, n, d, offsets, reinterpret_cast<uint2*>(q), s);
   }
   return cudaGetLastError();
 }
@@ -993,7 +1040,8 @@ cudaError_t launch_mx_quantize_act(const uint16_t* src, int rows, int cols, cons
   return cudaGetLastError();
 }
 
-cudaError_t launch_mx_quantize_rows_w(const uint16_t* src, long long rows, int cols, uint8_t* q,
+cudaError_t launch_mx_quantize_rows_w(const uint16_t* src, long long rows, int cols,
+                                      const int32_t* offsets, long long rows_per_e, uint8_t* q,
                                       uint8_t* s, int num_sms, cudaStream_t st) {
   // one warp per 32 blocks (rows * cols / 32 is a multiple of 32: rows and
   // cols are multiples of 128)
@@ -1001,7 +1049,8 @@ cudaError_t launch_mx_quantize_rows_w(const uint16_t* src, long long rows, int c
   const long long want = (threads + 255) / 256;
   const int blocks = static_cast<int>(want < 16LL * num_sms ? want : 16LL * num_sms);
   mx_quantize_rows_w_kernel<<<blocks > 0 ? blocks : 1, 256, 0, st>>>(
-      reinterpret_cast<const uint4*>(src), rows, cols, reinterpret_cast<uint2*>(q), s);
+      reinterpret_cast<const uint4*>(src), rows, cols, offsets, rows_per_e,
+      reinterpret_cast<uint2*>(q), s);
   return cudaGetLastError();
 }
 

@@ -58,9 +58,11 @@ struct MxGemmArgs {
 
 // W2 [E, n, d]: blocks of 32 rows per column (q, s: column tiles as in
 // moe.h); with q_rows also blocks of 32 columns per row (q_rows, s_rows in
-// weight tiles of W2 viewed as [E*n, d]) from the same read
-cudaError_t launch_mx_quantize_weights(const uint16_t* w2, int E, int n, int d, uint8_t* q,
-                                       uint8_t* s, uint8_t* q_rows, uint8_t* s_rows, int num_sms,
+// weight tiles of W2 viewed as [E*n, d]) from the same read; offsets (may
+// be null): experts with no rows are skipped and left untouched
+cudaError_t launch_mx_quantize_weights(const uint16_t* w2, int E, int n, int d,
+                                       const int32_t* offsets, uint8_t* q, uint8_t* s,
+                                       uint8_t* q_rows, uint8_t* s_rows, int num_sms,
                                        cudaStream_t st);
 // ragged activation: row-wise codes q / scales s (q may be null: transposed
 // copy only) and the transposed copy qT / sT (may be null).  tiled = false:
@@ -69,8 +71,11 @@ cudaError_t launch_mx_quantize_weights(const uint16_t* w2, int E, int n, int d, 
 cudaError_t launch_mx_quantize_act(const uint16_t* src, int rows, int cols, const int32_t* offsets,
                                    int E, uint8_t* q, uint8_t* s, uint8_t* qT, uint8_t* sT,
                                    int32_t* err, bool tiled, int num_sms, cudaStream_t st);
-// [rows, cols] (rows a multiple of 128) with blocks along cols, weight tiles
-cudaError_t launch_mx_quantize_rows_w(const uint16_t* src, long long rows, int cols, uint8_t* q,
+// [rows, cols] (rows a multiple of 128) with blocks along cols, weight tiles;
+// offsets (may be null): expert e holds rows [e, e+1) * rows_per_e (a
+// multiple of 128) and is skipped, untouched, when it has no rows
+cudaError_t launch_mx_quantize_rows_w(const uint16_t* src, long long rows, int cols,
+                                      const int32_t* offsets, long long rows_per_e, uint8_t* q,
                                       uint8_t* s, int num_sms, cudaStream_t st);
 // plain transposed scales sT [cols, rows/32] -> K tiles
 cudaError_t launch_mx_retile_t(const uint8_t* sT, int rows, int cols, const int32_t* offsets,

@@ -436,9 +436,16 @@ int moe_router_grad_rows(const float* ds_part, int n_parts, const int32_t* row_o
  * (blocks of 32 consecutive rows, FC2's reduction index, per column).
  *   W2 [E, n, d] bf16 -> w2_q [E, n, d] E4M3 codes, w2_s MMA-tiled scales
  *   (E * (n/32) * d bytes).  n, d multiples of 128.
+ *   offsets: NULL, or the routing's device offsets [E+1]; then an expert
+ *   with no rows (offsets[e+1] == offsets[e]) is skipped and its codes and
+ *   scales are left as they were.  No GEMM of the layer reads an empty
+ *   expert's weights, so a step that quantises its weights after routing
+ *   ([TE] "Transformer Engine이 제공하는 세 가지 구성 요소": the per-step
+ *   MXFP8 cast of the expert weights) streams only the used experts.
  */
 int moe_mx_quantize_weights(const moe_bf16* W2, int E, int n, int d,
-                            uint8_t* w2_q, uint8_t* w2_s, void* stream);
+                            const int32_t* offsets, uint8_t* w2_q, uint8_t* w2_s,
+                            void* stream);
 
 /*
  * moe_mx_quantize_weights2 - both MXFP8 copies of W2 that MXFP8 training
@@ -446,11 +453,12 @@ int moe_mx_quantize_weights(const moe_bf16* W2, int E, int n, int d,
  * along n, for the forward FC2) and, if w2_q_rows != NULL, w2_q_rows
  * [E, n, d] / w2_s_rows (blocks along d, weight tiles: the
  * moe_mx_quantize_weights_rowwise layout with rows = E*n) for the
- * backward's FC2-dgrad.  Same sizes and errors as moe_mx_quantize_weights.
+ * backward's FC2-dgrad.  Same sizes, offsets and errors as
+ * moe_mx_quantize_weights.
  */
 int moe_mx_quantize_weights2(const moe_bf16* W2, int E, int n, int d,
-                             uint8_t* w2_q, uint8_t* w2_s, uint8_t* w2_q_rows,
-                             uint8_t* w2_s_rows, void* stream);
+                             const int32_t* offsets, uint8_t* w2_q, uint8_t* w2_s,
+                             uint8_t* w2_q_rows, uint8_t* w2_s_rows, void* stream);
 
 /*
  * moe_mx_quantize_weights_rowwise - MXFP8 copy of a weight for a data
@@ -458,9 +466,14 @@ int moe_mx_quantize_weights2(const moe_bf16* W2, int E, int n, int d,
  * cols = d; W1 [E, d, n1] as rows = E*d, cols = n1), blocks of 32 along
  * cols.  Writes q [rows, cols] codes and s in weight tiles (rows*cols/32
  * bytes).  rows, cols multiples of 128.
+ *   offsets: NULL (E ignored), or the routing's device offsets [E+1] with
+ *   rows = E * (rows per expert), rows per expert a multiple of 128
+ *   (else MOE_E_SIZE); experts with no rows are skipped and left as they
+ *   were, as in moe_mx_quantize_weights.
  */
 int moe_mx_quantize_weights_rowwise(const moe_bf16* W, int rows, int cols,
-                                    uint8_t* q, uint8_t* s, void* stream);
+                                    const int32_t* offsets, int E, uint8_t* q, uint8_t* s,
+                                    void* stream);
 
 /*
  * moe_mx_bwd_workspace_size - bytes of moe_mx_bwd.workspace for a layer

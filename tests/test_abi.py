@@ -46,7 +46,7 @@ def test_host_argument_errors(L):
                                  None, None, None, None) == -4    # bad act
     assert L.moe_grouped_mlp_fwd(None, None, 4, 128, 64, 64, None, None, 0, 2, None, None, None,
                                  None, None, None, None) == -1    # MXFP8 without its buffers
-    assert L.moe_mx_quantize_weights(None, 4, 96, 128, None, None, None) == -3
+    assert L.moe_mx_quantize_weights(None, 4, 96, 128, None, None, None, None) == -3
     assert L.moe_mx_quantize(None, 64, 48, None, 2, None, None, None, None, None, None) == -3
     assert L.moe_route_offsets(None, 4, 3, 2, 1, 12, None, None, None, None, None, None, 0, None,
                                None) == -3                  # k > E
@@ -61,7 +61,11 @@ def test_host_argument_errors(L):
                                     None, vp(16), vp(16), vp(16), None) == -3
     assert L.moe_grouped_mlp_bwd_mx(None, None, None, vp(16), 4, 128, 128, 128, 0, 0, None, None,
                                     None, vp(16), vp(16), vp(16), None) == -1
-    assert L.moe_mx_quantize_weights_rowwise(vp(16), 100, 128, vp(16), vp(16), None) == -3
+    assert L.moe_mx_quantize_weights_rowwise(vp(16), 100, 128, None, 0, vp(16), vp(16), None) == -3
+    # with routing offsets: rows must split into E experts of a multiple of 128 rows each
+    assert L.moe_mx_quantize_weights_rowwise(vp(16), 384, 128, vp(16), 2, vp(16), vp(16), None) == -3
+    assert L.moe_mx_quantize_weights_rowwise(vp(16), 384, 128, vp(16), 0, vp(16), vp(16), None) == -3
+    assert L.moe_mx_quantize_weights_rowwise(vp(16), 512, 128, None, 3, None, vp(16), None) == -1
 
 
 def test_accumulate_flag_host_checks(L):

@@ -71,6 +71,46 @@ def test_both_direction_weight_quantiser_bit_exact():
     assert np.array_equal(q.cpu().numpy(), cq)
 
 
+def test_weight_quantisers_skip_empty_experts():
+    """With the routing offsets, the three weight quantisers write the used
+    experts' codes and scales bit for bit as without them, and leave every
+    byte of an expert that has no rows as it was (sentinel 0xA5).  Per
+    expert, the codes are its [n, d] (or [d, n1]) slice and the scales a
+    contiguous run of n*d/32 bytes in both tile layouts.  Used and empty
+    experts alternate irregularly across more than 32 experts."""
+    M = _M()
+    E, n, d = 37, 256, 384                              # the used-expert list spans two ballots
+    counts = [32 * (1 + e % 2) if e % 3 == 0 or e == 33 else 0 for e in range(E)]
+    counts[36] = 0                                      # the last expert empty
+    offs = cuda_i32(np.concatenate([[0], np.cumsum(counts)]))
+    used = [e for e in range(E) if counts[e]]
+    W2 = W.w2(23, E, n, d, 0.05, "cuda")
+    W1 = W.w1_interleaved(23, E, d, n // 2, 0.05, "cuda")   # [E, d, n]: rows per expert d
+    fill = lambda t: torch.full_like(t, 0xA5)
+
+    def check(full, part, per_e):
+        for f, p in zip(full, part):
+            f, p = f.reshape(E, -1), p.reshape(E, -1)
+            assert f.shape[1] == per_e or f.shape[1] == per_e // 32
+            for e in range(E):
+                if counts[e]:
+                    assert torch.equal(p[e], f[e]), f"expert {e} differs"
+                else:
+                    assert bool((p[e] == 0xA5).all()), f"empty expert {e} written"
+
+    full2 = M.mx_quantize_weights2(W2)
+    part2 = M.mx_quantize_weights2(W2, *[fill(t) for t in full2], offsets=offs)
+    full1 = M.mx_quantize_weights(W2)
+    part1 = M.mx_quantize_weights(W2, *[fill(t) for t in full1], offsets=offs)
+    fullr = M.mx_quantize_weights_rowwise(W1)
+    partr = M.mx_quantize_weights_rowwise(W1, *[fill(t) for t in fullr], offsets=offs)
+    torch.cuda.synchronize()
+    check(full2, part2, n * d)
+    check(full1, part1, n * d)
+    check(fullr, partr, d * n)
+    assert used[:3] == [0, 3, 6] and 33 in used and 36 not in used
+
+
 def _layer(seed, counts, d, n, act, tail=64):
     off = np.concatenate([[0], np.cumsum(counts)]).astype(np.int64)
     assert (off % 32 == 0).all()
