@@ -11,3 +11,9 @@ if ROOT not in sys.path:
 def pytest_configure(config):
     config.addinivalue_line("markers", "gpu: needs a CUDA GPU (GB300, sm_103a)")
     config.addinivalue_line("markers", "slow: long-running (full-size workloads)")
+    # mutation test: plant one mistake in the oracle before the pin tests
+    # are collected (set only by test_oracle_mutants.py in a child process)
+    name = os.environ.get("ORACLE_MUTANT")
+    if name:
+        import _oracle_mutants
+        _oracle_mutants.apply(name)

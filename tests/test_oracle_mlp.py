@@ -252,6 +252,14 @@ def test_routed_pad_rows_and_empty_expert():
     assert (dW1[1] == 0).all() and (dW2[1] == 0).all()
 
 
+def test_amax_is_the_largest_magnitude():
+    """Per-tensor amax: the largest |value|, whichever its sign; 0 for an
+    empty or all-zero tensor."""
+    assert O.amax(np.array([[-3.0, 2.0], [0.5, -0.25]])) == 3.0
+    assert O.amax(np.array([1.5, -1.5])) == 1.5
+    assert O.amax(np.zeros((0, 4))) == 0.0 and O.amax(np.zeros(3)) == 0.0
+
+
 def test_hadamard16_pins():
     """Sylvester's recursion H_{2m} = [[H, H], [H, -H]] gives the same matrix;
     it is orthonormal and symmetric."""

@@ -125,6 +125,25 @@ def test_transpose_identity():
     assert (qT == qR).all() and (sT == sR).all()
 
 
+def test_weight_blocks_run_along_n():
+    """W2's blocks run along n (FC2's reduction index): expert e's codes and
+    scales equal the row-wise quantisation of W2[e]^T (rows of W2[e]^T are
+    columns of W2[e]).  An all-zero column block and a block holding a
+    single large value make blocks along d give different codes."""
+    rng = np.random.default_rng(22)
+    E, n, d = 2, 64, 96
+    W2 = O.bf16_round(rng.standard_normal((E, n, d)) * 0.05)
+    W2[0, 0:32, 3] = 0.0
+    W2[1, 40, 7] = 300.0
+    q, s = O.mx_quantize_weights(W2)
+    assert q.shape == (E, n, d) and s.shape == (E, n // 32, d)
+    for e in range(E):
+        qR, sR = O.mx_quantize_rows(W2[e].T)
+        assert (q[e].T == qR).all() and (s[e].T == sR).all()
+    # the zero block gets scale code 0; 300 = 1.17 * 2^8 gives exponent 8 - 8 = 0 (code 127)
+    assert s[0, 0, 3] == 0 and s[1, 1, 7] == 127
+
+
 def test_rowwise_dequant_error_bound():
     """Each dequantised element is within half an E4M3 spacing of the value
     (relative 2^-4 for normals) unless it saturates."""

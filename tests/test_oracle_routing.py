@@ -165,6 +165,22 @@ def test_permute_unpermute_identity():
     assert np.abs(back - x).max() < 1e-12
 
 
+def test_combine_weights_each_slot_by_its_own_probability():
+    """A worked case by hand: token 0 goes to experts (1, 0) with weights
+    (0.75, 0.25), token 1 to (0, 1) with (0.5, 0.5) reversed as (1, 0) with
+    (0.125, 0.875).  Expert rows hold distinct powers of two, so each output
+    names the rows and weights it used exactly."""
+    idx = np.array([[1, 0], [1, 0]])
+    r = O.route_offsets(idx, 2)
+    # rows: expert 0 = pairs (0,1), (1,1); expert 1 = pairs (0,0), (1,0)
+    assert r["row_of_pair"].tolist() == [2, 0, 3, 1]
+    y = np.array([[1.0, 0.0], [2.0, 0.0], [0.0, 4.0], [0.0, 8.0]])   # rows 0..3
+    p = np.array([[0.75, 0.25], [0.125, 0.875]])
+    out = O.unpermute(y, r["row_of_pair"], 2, 2, probs=p, round_bf16=False)
+    # token 0: 0.75 * row 2 + 0.25 * row 0;  token 1: 0.125 * row 3 + 0.875 * row 1
+    assert out.tolist() == [[0.25, 3.0], [1.75, 1.0]]
+
+
 def test_permute_scale_is_prob_times_row():
     rng = np.random.default_rng(2)
     T, k, E, d = 9, 2, 3, 8
