@@ -555,9 +555,10 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(WL.WORKLOADS))
-    ap.add_argument("--e2e-steps", type=int, default=30,
-                    help="steps of the pipelined end-to-end leg (its first input copy is not "
-                         "overlapped, so more steps approach the steady state)")
+    ap.add_argument("--e2e-steps", type=int, default=None,
+                    help="steps of the pipelined end-to-end leg (default: --steps, at least "
+                         "30; its first input copy is not overlapped, so more steps approach "
+                         "the steady state)")
     ap.add_argument("--cpu-rows", type=int, default=512,
                     help="rows of the oracle's cpu_baseline sample")
     ap.add_argument("--ref-rows", type=int, default=64,
@@ -680,7 +681,8 @@ def main():
     graph = time_graph(step, args.steps, ws, fwd_f + bwd_f)
 
     # end to end through the public API with host buffers
-    e2e = run_e2e(w, inp, o, step, args.e2e_steps, ws, fwd_f + bwd_f)
+    e2e_steps = args.e2e_steps if args.e2e_steps else max(args.steps, 30)
+    e2e = run_e2e(w, inp, o, step, e2e_steps, ws, fwd_f + bwd_f)
 
     # fused against unfused epilogues (outside the timed region)
     fusion = None
