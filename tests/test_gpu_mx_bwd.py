@@ -71,32 +71,33 @@ def test_both_direction_weight_quantiser_bit_exact():
     assert np.array_equal(q.cpu().numpy(), cq)
 
 
-def test_weight_quantisers_skip_empty_experts():
+@pytest.mark.parametrize("E,n,d", [(37, 256, 384), (1024, 128, 128)])
+def test_weight_quantisers_skip_empty_experts(E, n, d):
     """With the routing offsets, the three weight quantisers write the used
     experts' codes and scales bit for bit as without them, and leave every
     byte of an expert that has no rows as it was (sentinel 0xA5).  Per
     expert, the codes are its [n, d] (or [d, n1]) slice and the scales a
-    contiguous run of n*d/32 bytes in both tile layouts.  Used and empty
-    experts alternate irregularly across more than 32 experts."""
+    contiguous run of n*d/32 bytes in both tile layouts."""
     M = _M()
-    E, n, d = 37, 256, 384                              # the used-expert list spans two ballots
+    # used and empty experts alternate irregularly; the used-expert list
+    # spans two ballots (E = 37) or fills the library's limit (E = 1024)
     counts = [32 * (1 + e % 2) if e % 3 == 0 or e == 33 else 0 for e in range(E)]
-    counts[36] = 0                                      # the last expert empty
+    counts[E - 1] = 0                                   # the last expert empty
     offs = cuda_i32(np.concatenate([[0], np.cumsum(counts)]))
     used = [e for e in range(E) if counts[e]]
     W2 = W.w2(23, E, n, d, 0.05, "cuda")
     W1 = W.w1_interleaved(23, E, d, n // 2, 0.05, "cuda")   # [E, d, n]: rows per expert d
     fill = lambda t: torch.full_like(t, 0xA5)
 
+    ui = torch.tensor(used, device="cuda")
+    ei = torch.tensor([e for e in range(E) if not counts[e]], device="cuda")
+
     def check(full, part, per_e):
         for f, p in zip(full, part):
             f, p = f.reshape(E, -1), p.reshape(E, -1)
             assert f.shape[1] == per_e or f.shape[1] == per_e // 32
-            for e in range(E):
-                if counts[e]:
-                    assert torch.equal(p[e], f[e]), f"expert {e} differs"
-                else:
-                    assert bool((p[e] == 0xA5).all()), f"empty expert {e} written"
+            assert torch.equal(p[ui], f[ui]), "a used expert differs"
+            assert bool((p[ei] == 0xA5).all()), "an empty expert was written"
 
     full2 = M.mx_quantize_weights2(W2)
     part2 = M.mx_quantize_weights2(W2, *[fill(t) for t in full2], offsets=offs)
@@ -108,7 +109,7 @@ def test_weight_quantisers_skip_empty_experts():
     check(full2, part2, n * d)
     check(full1, part1, n * d)
     check(fullr, partr, d * n)
-    assert used[:3] == [0, 3, 6] and 33 in used and 36 not in used
+    assert used[:3] == [0, 3, 6] and 33 in used and E - 1 not in used
 
 
 def _layer(seed, counts, d, n, act, tail=64):
@@ -150,6 +151,8 @@ CASES = [
     # three 128-row blocks of d in the weight gradient and of an expert, and
     # d = 384 ending in a single 128-column half
     ("odd_row_blocks", [288, 32, 0, 416], 384, 128),
+    # the library's expert limit: 1024 experts, most of them empty
+    ("max_experts", [32 * (1 + (e % 3 == 0)) if e % 7 == 0 else 0 for e in range(1024)], 128, 128),
 ]
 
 
@@ -170,6 +173,27 @@ def test_mx_bwd_accumulate_dw():
     assert torch.equal(dW1[1], old1[1]) and torch.equal(dW2[1], old2[1])
 
 
+def _check_dw1(got, want, dh_gpu, dh_ref, off, name):
+    """dW1_e = x_e^T dH_e, from the transposed MXFP8 copies.  x is the
+    generator's on both sides, but dH is each side's own FC2-dgrad output:
+    where they differ by one bf16 step, the quantisers can emit a different
+    E4M3 code or block scale, and with experts of 32-64 rows one such flip
+    moves an entry by more than 2e-2 RMS.  So the element-wise tolerance
+    applies to the columns of dW1_e whose dH column agrees bit for bit on
+    every row of the expert, and all of dW1 meets the relative Frobenius
+    bound 2e-2 (the same rule as the full-size MXFP8 test)."""
+    bits_g, bits_r = O.bf16_bits(np.nan_to_num(dh_gpu)), O.bf16_bits(np.nan_to_num(dh_ref))
+    mask = np.zeros(got.shape, dtype=bool)
+    for e in range(len(off) - 1):
+        r0, r1 = int(off[e]), int(off[e + 1])
+        agree = (bits_g[r0:r1] == bits_r[r0:r1]).all(axis=0)
+        mask[e][:, agree] = True
+    assert mask.mean() >= 0.5, (name, "dH columns agreeing", mask.mean())
+    assert_rms_close(got[mask], want[mask], f"{name} dW1 on agreeing dH columns")
+    rel = np.linalg.norm(got - want) / np.linalg.norm(want)
+    assert rel <= 2e-2, (f"{name} dW1 relative error", rel)
+
+
 @pytest.mark.parametrize("act", ["swiglu", "geglu", "srelu"])
 @pytest.mark.parametrize("name,counts,d,n", CASES, ids=[c[0] for c in CASES])
 def test_mx_bwd_matches_oracle(name, counts, d, n, act):
@@ -180,7 +204,7 @@ def test_mx_bwd_matches_oracle(name, counts, d, n, act):
     assert_rms_close(f64(dh)[:R], ref["dH"][:R], f"{name}/{act} dH")
     assert_rms_close(f64(dx)[:R], ref["dX"][:R], f"{name}/{act} dX")
     assert_rms_close(f64(dW2), ref["dW2"], f"{name}/{act} dW2")
-    assert_rms_close(f64(dW1), ref["dW1"], f"{name}/{act} dW1")
+    _check_dw1(f64(dW1), ref["dW1"], f64(dh), ref["dH"], off, f"{name}/{act}")
     for e in range(len(counts)):
         if counts[e] == 0:
             assert float(dW1[e].abs().max()) == 0 and float(dW2[e].abs().max()) == 0
