@@ -26,7 +26,7 @@ __all__ = [
     "router_topk",
     "permute", "unpermute", "grouped_mlp_fwd", "grouped_mlp_bwd", "MoeError",
     "FLAG_MXFP8", "MxFwd", "mx_quantize_weights", "mx_quantize", "mx_buffers",
-    "MxBwd", "mx_quantize_weights_rowwise", "mx_bwd_workspace_size", "grouped_mlp_bwd_mx",
+    "MxBwd", "mx_quantize_weights_rowwise", "mx_quantize_tiled", "mx_bwd_workspace_size", "grouped_mlp_bwd_mx",
     "grouped_mlp_bwd_routed", "router_grad_rows", "mx_quantize_weights2", "FLAG_ACCUMULATE_DW",
     "grouped_gemm", "activation", "activation_bwd", "grouped_mlp_fwd_gather",
     "grouped_mlp_bwd_routed_gather", "route_logits",
@@ -110,6 +110,8 @@ def lib():
                                           vp, vp, vp, vp, vp, vp, vp]
         L.moe_mx_quantize_weights2.restype = i32
         L.moe_mx_quantize_weights2.argtypes = [vp, i32, i32, i32, vp, vp, vp, vp, vp, vp]
+        L.moe_mx_quantize_tiled.restype = i32
+        L.moe_mx_quantize_tiled.argtypes = [vp, i32, i32, vp, i32, vp, vp, vp, vp, vp, vp]
         L.moe_mx_quantize_weights_rowwise.restype = i32
         L.moe_mx_quantize_weights_rowwise.argtypes = [vp, i32, i32, vp, i32, vp, vp, vp]
         L.moe_mx_bwd_workspace_size.restype = sz
@@ -490,6 +492,31 @@ def mx_quantize(src: torch.Tensor, offsets: torch.Tensor, transposed: bool = Tru
     rc = lib().moe_mx_quantize(_ptr(src), rows, cols, _ptr(offsets), offsets.numel() - 1, _ptr(q),
                                _ptr(s), _ptr(qT), _ptr(sT), _ptr(err), _stream(stream))
     _check(rc, "moe_mx_quantize")
+    return q, s, qT, sT, err
+
+
+def mx_quantize_tiled(src: torch.Tensor, offsets: torch.Tensor, rowwise: bool = True,
+                      transposed: bool = True, err: torch.Tensor | None = None, stream=None):
+    """Group-aware MXFP8 quantisation with the scales in the block-scaled
+    GEMM's layouts (moe_mx_quantize_tiled).  Returns (q, s, qT, sT, err);
+    q/s are None unless ``rowwise``, qT/sT None unless ``transposed``; s and
+    sT are rows*cols/8 bytes each."""
+    _need(src, torch.bfloat16, "src", 2)
+    _need(offsets, torch.int32, "offsets", 1)
+    if not (rowwise or transposed):
+        raise ValueError("at least one copy")
+    rows, cols = src.shape
+    dev = src.device
+    u8 = torch.uint8
+    q = torch.empty((rows, cols), dtype=u8, device=dev) if rowwise else None
+    s = torch.empty(rows * cols // 8, dtype=u8, device=dev) if rowwise else None
+    qT = torch.empty((cols, rows), dtype=u8, device=dev) if transposed else None
+    sT = torch.empty(rows * cols // 8, dtype=u8, device=dev) if transposed else None
+    err = _err_word(err, dev)
+    rc = lib().moe_mx_quantize_tiled(_ptr(src), rows, cols, _ptr(offsets), offsets.numel() - 1,
+                                     _ptr(q), _ptr(s), _ptr(qT), _ptr(sT), _ptr(err),
+                                     _stream(stream))
+    _check(rc, "moe_mx_quantize_tiled")
     return q, s, qT, sT, err
 
 

@@ -907,4 +907,25 @@ int moe_mx_quantize(const moe_bf16* src, int rows, int cols, const int32_t* offs
   return cuda_rc(e);
 }
 
+int moe_mx_quantize_tiled(const moe_bf16* src, int rows, int cols, const int32_t* offsets,
+                          int E, uint8_t* q, uint8_t* sc, uint8_t* qT, uint8_t* sT,
+                          int32_t* err, void* stream) {
+  g_last_launches = 0;
+  if (E < 1 || E > MOE_MAX_EXPERTS || rows < 0 || cols <= 0 || rows % 32 || cols % 32)
+    return MOE_E_SIZE;
+  if (rows == 0) return MOE_OK;
+  if (cols % 128) return MOE_E_SIZE;
+  if (!src || !offsets || !err || (!q && !qT) || (q && !sc) || (qT && !sT)) return MOE_E_NULL;
+  if (misaligned(src) || misaligned(q) || misaligned(qT) || misaligned(sc)) return MOE_E_ALIGN;
+  const int sms = num_sms_current();
+  if (sms <= 0) return MOE_E_CUDA;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  ev_begin(s);
+  const cudaError_t e = moe::launch_mx_quantize_act(src, rows, cols, offsets, E, q, sc, qT, sT,
+                                                    err, true, sms, s);
+  ev_end(s);
+  g_last_launches = 1;
+  return cuda_rc(e);
+}
+
 }  // extern "C"

@@ -246,23 +246,19 @@ __device__ __forceinline__ int tile_start(const int* s_off, int E, int r32) {
   return oe + ((r32 - oe) & ~127);
 }
 
-// one warp: a 32-row block (inside one expert) x a 32-column block
-template <bool TILED>
+// Plain scale layouts (s [rows, cols/32], sT [cols, rows/32]), any width
+// that is a multiple of 32: one warp takes a 32-row block (inside one
+// expert) x a 32-column block, lane = row.
 __global__ void __launch_bounds__(256)
     mx_quantize_act_kernel(const uint4* __restrict__ src, int rows, int cols,
                            const int32_t* __restrict__ offsets, int E,
                            uint8_t* __restrict__ q, uint8_t* __restrict__ s,
                            uint8_t* __restrict__ qT, uint8_t* __restrict__ sT,
                            int32_t* __restrict__ err) {
-  __shared__ int s_off[MOE_MAX_EXPERTS + 1];
   const int lane = threadIdx.x & 31;
   const int cb_n = cols / 32;
   const long long nwarps = static_cast<long long>(rows / 32) * cb_n;
   const int used = min(max(offsets[E], 0), rows);
-  if (TILED) {
-    for (int e = threadIdx.x; e <= E; e += blockDim.x) s_off[e] = offsets[e];
-    __syncthreads();
-  }
   // a 32-row block must lie inside one expert: expert starts must be
   // multiples of 32 (reported, not repaired)
   if (blockIdx.x == 0)
@@ -286,19 +282,13 @@ __global__ void __launch_bounds__(256)
         v[8 * k + 2 * j + 1] = bf16_hi(xw[j]);
       }
     }
-    const int t0 = TILED ? tile_start(s_off, E, rb * 32) : 0;
     if (q) {
       uint32_t qw[8];
       const uint32_t sc = mx_quant32(v, qw);
       uint4* qo = reinterpret_cast<uint4*>(q + static_cast<long long>(r) * cols + cb * 32);
       qo[0] = make_uint4(qw[0], qw[1], qw[2], qw[3]);
       qo[1] = make_uint4(qw[4], qw[5], qw[6], qw[7]);
-      if (TILED) {
-        const long long chunk = static_cast<long long>(t0 / 32) * (cols / 128) + cb / 4;
-        s[chunk * 512 + mx_chunk_off(r - t0, cb & 3)] = static_cast<uint8_t>(sc);
-      } else {
-        s[static_cast<long long>(r) * cb_n + cb] = static_cast<uint8_t>(sc);
-      }
+      s[static_cast<long long>(r) * cb_n + cb] = static_cast<uint8_t>(sc);
     }
     if (qT) {
       uint32_t my_sc = 0;
@@ -310,12 +300,122 @@ __global__ void __launch_bounds__(256)
         if (lane == j) my_sc = scj;
       }
       const int c = cb * 32 + lane;
-      if (TILED) {
-        const long long chunk = static_cast<long long>(t0 / 32) * (cols / 128) + c / 128;
-        sT[chunk * 512 + mx_chunk_off(c & 127, (rb * 32 - t0) >> 5)] = static_cast<uint8_t>(my_sc);
-      } else {
-        sT[static_cast<long long>(c) * (rows / 32) + rb] = static_cast<uint8_t>(my_sc);
+      sT[static_cast<long long>(c) * (rows / 32) + rb] = static_cast<uint8_t>(my_sc);
+    }
+  }
+}
+
+// Tiled copies for widths that are multiples of 128 (the GEMMs' layouts):
+// one warp takes a 32-row block (inside one expert) x 128 columns, lane
+// 16 * half + i holding rows 16 * half .. +15 of columns 8 i .. 8 i + 7 as
+// packed bf16 pairs (the two-direction W2 quantiser's arrangement).  A
+// column's 32-row maximum combines the two halves (lanes 16 apart) and a
+// row's 32-column maximum four adjacent lanes.  The transposed codes of a
+// column then leave as one 16-byte store per lane (16 consecutive rows of
+// qT's row), the row-wise codes as one 8-byte store per row and lane, the
+// row scales as one 4-byte word per row (the four blocks of a 128-column
+// chunk are adjacent in its row tile), and the column scales as bytes split
+// across both halves, which hold the same codes.  The one-block-per-warp
+// kernel above spends most of its instructions on 32 single-byte stores
+// and 32 warp reductions per block for the transposed copy (848 warp
+// instructions per 32 x 32 block under ncu on a 8,192 x 8,192 dY).
+__global__ void __launch_bounds__(256)
+    mx_quantize_act_w_kernel(const uint4* __restrict__ src, int rows, int cols,
+                             const int32_t* __restrict__ offsets, int E,
+                             uint2* __restrict__ q, uint8_t* __restrict__ s,
+                             uint8_t* __restrict__ qT, uint8_t* __restrict__ sT,
+                             int32_t* __restrict__ err) {
+  __shared__ int s_off[MOE_MAX_EXPERTS + 1];
+  const int lane = threadIdx.x & 31;
+  const int half = lane >> 4;
+  const int li = lane & 15;
+  const int cw = cols / 128;
+  const int c8n = cols / 8;
+  const long long nwarps = static_cast<long long>(rows / 32) * cw;
+  const int used = min(max(offsets[E], 0), rows);
+  for (int e = threadIdx.x; e <= E; e += blockDim.x) s_off[e] = offsets[e];
+  __syncthreads();
+  // a 32-row block must lie inside one expert (reported, not repaired)
+  if (blockIdx.x == 0)
+    for (int e = threadIdx.x; e <= E; e += blockDim.x)
+      if (offsets[e] & 31) set_err(err, MOE_DEV_BAD_OFFSETS);
+  for (long long wi = (blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x) / 32;
+       wi < nwarps; wi += static_cast<long long>(gridDim.x) * blockDim.x / 32) {
+    const int rb = static_cast<int>(wi / cw);
+    const int cc = static_cast<int>(wi - static_cast<long long>(rb) * cw);
+    if (rb * 32 >= used) continue;       // rows past every expert: untouched
+    const int c8 = cc * 16 + li;
+    const int row0 = rb * 32 + 16 * half;
+    uint32_t x[16][4];
+#pragma unroll
+    for (int k = 0; k < 16; ++k) {
+      const uint4 v = __ldg(src + static_cast<long long>(row0 + k) * c8n + c8);
+      x[k][0] = v.x; x[k][1] = v.y; x[k][2] = v.z; x[k][3] = v.w;
+    }
+    const int t0 = tile_start(s_off, E, rb * 32);
+    const long long chunk = static_cast<long long>(t0 / 32) * cw + cc;
+    if (qT) {
+      float amax[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+#pragma unroll
+      for (int k = 0; k < 16; ++k)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          amax[2 * j] = fmaxf(amax[2 * j], fabsf(bf16_lo(x[k][j])));
+          amax[2 * j + 1] = fmaxf(amax[2 * j + 1], fabsf(bf16_hi(x[k][j])));
+        }
+      uint32_t code[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        amax[j] = fmaxf(amax[j], __shfl_xor_sync(0xffffffffu, amax[j], 16));
+        code[j] = mx_scale_code(amax[j]);
+        const float inv = mx_inv_scale(code[j]);
+        // column 8 li + j, rows row0 .. row0 + 15: 16 bytes of qT's row
+        auto val = [&](int k) {
+          return (j & 1) ? bf16_hi(x[k][j >> 1]) : bf16_lo(x[k][j >> 1]);
+        };
+        uint32_t w[4];
+#pragma unroll
+        for (int m = 0; m < 4; ++m)
+          w[m] = e4m3x2(val(4 * m) * inv, val(4 * m + 1) * inv) |
+                 (e4m3x2(val(4 * m + 2) * inv, val(4 * m + 3) * inv) << 16);
+        const long long c = static_cast<long long>(cc) * 128 + 8 * li + j;
+        *reinterpret_cast<uint4*>(qT + c * rows + row0) = make_uint4(w[0], w[1], w[2], w[3]);
       }
+      // column scales in the K tile of this row block: half 0 stores
+      // columns 8 li .. +3, half 1 8 li + 4 .. +7
+#pragma unroll
+      for (int jj = 0; jj < 4; ++jj) {
+        const int j = jj + 4 * half;
+        sT[chunk * 512 + mx_chunk_off(8 * li + j, (rb * 32 - t0) >> 5)] =
+            static_cast<uint8_t>(half ? code[jj + 4] : code[jj]);
+      }
+    }
+    if (q) {
+      // the 4 block scales of row 16 * half + l end in lane 16 * half + l
+      // (gathered by shuffles) and are stored as one word
+      uint32_t my_row_sc = 0;
+#pragma unroll
+      for (int k = 0; k < 16; ++k) {
+        float m = 0.f;
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          m = fmaxf(m, fmaxf(fabsf(bf16_lo(x[k][j])), fabsf(bf16_hi(x[k][j]))));
+        m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
+        m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
+        const uint32_t sc = mx_scale_code(m);
+        const float iv = mx_inv_scale(sc);
+        const uint32_t w0 = e4m3x2(bf16_lo(x[k][0]) * iv, bf16_hi(x[k][0]) * iv) |
+                            (e4m3x2(bf16_lo(x[k][1]) * iv, bf16_hi(x[k][1]) * iv) << 16);
+        const uint32_t w1 = e4m3x2(bf16_lo(x[k][2]) * iv, bf16_hi(x[k][2]) * iv) |
+                            (e4m3x2(bf16_lo(x[k][3]) * iv, bf16_hi(x[k][3]) * iv) << 16);
+        q[static_cast<long long>(row0 + k) * c8n + c8] = make_uint2(w0, w1);
+        uint32_t packed = 0;
+#pragma unroll
+        for (int cb = 0; cb < 4; ++cb)
+          packed |= __shfl_sync(0xffffffffu, sc, (lane & 16) + 4 * cb) << (8 * cb);
+        if (li == k) my_row_sc = packed;
+      }
+      *reinterpret_cast<uint32_t*>(s + chunk * 512 + mx_chunk_off(row0 + li - t0, 0)) = my_row_sc;
     }
   }
 }
@@ -1028,15 +1128,31 @@ cudaError_t launch_mx_quantize_weights(const uint16_t* w2, int E, int n, int d,
 cudaError_t launch_mx_quantize_act(const uint16_t* src, int rows, int cols, const int32_t* offsets,
                                    int E, uint8_t* q, uint8_t* s, uint8_t* qT, uint8_t* sT,
                                    int32_t* err, bool tiled, int num_sms, cudaStream_t st) {
+  if (tiled) {
+    if (cols % 128) return cudaErrorInvalidValue;   // the tiles cover 128-column groups
+    // as many blocks as the SMs hold at once: each loads the offsets once
+    static int per_sm = 0;
+    if (per_sm <= 0) {
+      int nb = 0;
+      if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, mx_quantize_act_w_kernel, 256, 0) !=
+              cudaSuccess || nb <= 0)
+        nb = 1;
+      per_sm = nb;
+    }
+    const long long warps = static_cast<long long>(rows / 32) * (cols / 128);
+    const long long want = (warps * 32 + 255) / 256;
+    const long long cap = static_cast<long long>(per_sm) * num_sms;
+    const int blocks = static_cast<int>(want < cap ? want : cap);
+    mx_quantize_act_w_kernel<<<blocks > 0 ? blocks : 1, 256, 0, st>>>(
+        reinterpret_cast<const uint4*>(src), rows, cols, offsets, E, reinterpret_cast<uint2*>(q), s,
+        qT, sT, err);
+    return cudaGetLastError();
+  }
   const long long warps = static_cast<long long>(rows / 32) * (cols / 32);
   const long long want = (warps * 32 + 255) / 256;
   const int blocks = static_cast<int>(want < 16LL * num_sms ? want : 16LL * num_sms);
-  if (tiled)
-    mx_quantize_act_kernel<true><<<blocks > 0 ? blocks : 1, 256, 0, st>>>(
-        reinterpret_cast<const uint4*>(src), rows, cols, offsets, E, q, s, qT, sT, err);
-  else
-    mx_quantize_act_kernel<false><<<blocks > 0 ? blocks : 1, 256, 0, st>>>(
-        reinterpret_cast<const uint4*>(src), rows, cols, offsets, E, q, s, qT, sT, err);
+  mx_quantize_act_kernel<<<blocks > 0 ? blocks : 1, 256, 0, st>>>(
+      reinterpret_cast<const uint4*>(src), rows, cols, offsets, E, q, s, qT, sT, err);
   return cudaGetLastError();
 }
 

@@ -575,6 +575,24 @@ int moe_mx_quantize(const moe_bf16* src, int rows, int cols,
                     uint8_t* qT, uint8_t* sT, int32_t* err, void* stream);
 
 /*
+ * moe_mx_quantize_tiled - moe_mx_quantize with the scales written in the
+ * layouts the block-scaled grouped GEMM reads, as moe_grouped_mlp_bwd_mx
+ * quantises its operands: s in row tiles (128-row tiles from offsets[e] +
+ * 128 i, 512-byte chunks of 128 rows x 4 blocks, chunk (t0/32)*(cols/128) +
+ * c/128 for the tile starting at row t0) and sT in reduction tiles (the
+ * same tiles along the transposed copy's columns: chunk (t0/32)*(cols/128)
+ * + c/128 holds columns c of the 128-column group x the tile's four 32-row
+ * blocks).  Both buffers are rows*cols/8 bytes.  q may be NULL when qT is
+ * given (transposed copy only), and qT NULL for the row-wise copy only.
+ * Codes are those of moe_mx_quantize.  cols must be a multiple of 128
+ * (MOE_E_SIZE otherwise), rows of 32; one warp covers 32 rows x 128
+ * columns.
+ */
+int moe_mx_quantize_tiled(const moe_bf16* src, int rows, int cols,
+                          const int32_t* offsets, int E, uint8_t* q, uint8_t* s,
+                          uint8_t* qT, uint8_t* sT, int32_t* err, void* stream);
+
+/*
  * Measurement hook (per host thread; no counterpart on the pages).
  * moe_set_launch_events(events, n): events points to n caller-created
  * cudaEvent_t handles (passed as void*).  From then on every grouped-GEMM

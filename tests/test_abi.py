@@ -48,6 +48,13 @@ def test_host_argument_errors(L):
                                  None, None, None, None) == -1    # MXFP8 without its buffers
     assert L.moe_mx_quantize_weights(None, 4, 96, 128, None, None, None, None) == -3
     assert L.moe_mx_quantize(None, 64, 48, None, 2, None, None, None, None, None, None) == -3
+    # tiled scales: widths in 128-column groups; at least one copy requested
+    assert L.moe_mx_quantize_tiled(vp(16), 64, 96, vp(16), 2, vp(16), vp(16), None, None, vp(16),
+                                   None) == -3
+    assert L.moe_mx_quantize_tiled(vp(16), 64, 128, vp(16), 2, None, None, None, None, vp(16),
+                                   None) == -1
+    assert L.moe_mx_quantize_tiled(vp(16), 64, 128, vp(16), 2, vp(16), None, None, None, vp(16),
+                                   None) == -1
     assert L.moe_route_offsets(None, 4, 3, 2, 1, 12, None, None, None, None, None, None, 0, None,
                                None) == -3                  # k > E
     assert L.moe_route_offsets(None, 4, 2, 8, 0, 12, None, None, None, None, None, None, 0, None,

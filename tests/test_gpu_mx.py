@@ -107,6 +107,69 @@ def test_group_aware_quantiser_bit_exact(rows, cols, offs):
     assert np.array_equal(sT.cpu().numpy()[:, :R // 32], sTo[:, :R // 32])
 
 
+def decode_k_tiles(sT, offsets, rows, cols):
+    """[cols, rows/32] column-block scales from the reduction-tile layout
+    (-1 outside every expert): the K step starting at row t0 of an expert
+    keeps column c's four 32-row blocks in chunk (t0/32)*(cols/128) + c/128,
+    at the chunk offset of row c % 128 and block (r - t0)/32."""
+    sT = sT.cpu().numpy()
+    out = -np.ones((cols, rows // 32), np.int64)
+    c = np.arange(cols)
+    cr = c % 128
+    for e in range(len(offsets) - 1):
+        for t0 in range(int(offsets[e]), int(offsets[e + 1]), 128):
+            for r32 in range(t0, min(t0 + 128, int(offsets[e + 1])), 32):
+                kb = (r32 - t0) // 32
+                off = ((t0 // 32) * (cols // 128) + c // 128) * 512 + (cr % 32) * 16 + (cr // 32) * 4 + kb
+                out[:, r32 // 32] = sT[off]
+    return out
+
+
+TILED_SHAPES = [(448, 256, [0, 64, 64, 288, 416]), (256, 384, [0, 128, 128, 224])]
+
+
+@pytest.mark.parametrize("rows,cols,offs", TILED_SHAPES, ids=["448x256", "256x384"])
+def test_tiled_quantiser_bit_exact(rows, cols, offs):
+    """moe_mx_quantize_tiled (the quantiser the MXFP8 backward runs on dY, x
+    and dH): codes and both tiled scale layouts equal the oracle's OCP MX
+    quantiser bit for bit on every row of an expert, with experts of 0, 64,
+    128 and 224 rows (tiles of 128 and a 96-row tail) and the planted edge
+    blocks; the row-only and transposed-only calls give the same bytes, and
+    rows past every expert stay untouched."""
+    M = _lib()
+    offsets = np.array(offs)
+    R = int(offsets[-1])
+    src = _plant(f64(WL.normal((rows, cols), (25, WL.X, 0), 1.0, "cuda")))
+    src[40, 128:160] = -0.0                                # a block of negative zeros
+    src_t = torch.from_numpy(src).to(torch.bfloat16).cuda()
+    offs_t = cuda_i32(offsets)
+    q, s, qT, sT, err = M.mx_quantize_tiled(src_t, offs_t)
+    q1, s1, _, _, e1 = M.mx_quantize_tiled(src_t, offs_t, transposed=False)
+    _, _, qT2, sT2, e2 = M.mx_quantize_tiled(src_t, offs_t, rowwise=False)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0 and int(e1.item()) == 0 and int(e2.item()) == 0
+    qo, so = O.mx_quantize_rows(src[:R])
+    assert np.array_equal(q.cpu().numpy()[:R], qo)
+    assert np.array_equal(decode_a_scales(s, offsets, rows, cols)[:R], so)
+    qTo, sTo = O.mx_quantize_cols(src, offsets, rows)
+    assert np.array_equal(qT.cpu().numpy()[:, :R], qTo[:, :R])
+    assert np.array_equal(decode_k_tiles(sT, offsets, rows, cols)[:, :R // 32], sTo[:, :R // 32])
+    assert torch.equal(q1[:R], q[:R]) and torch.equal(qT2[:, :R], qT[:, :R])
+    assert np.array_equal(decode_a_scales(s1, offsets, rows, cols)[:R], so)
+    assert np.array_equal(decode_k_tiles(sT2, offsets, rows, cols)[:, :R // 32], sTo[:, :R // 32])
+    # the plain-layout quantiser emits the same codes
+    qp, sp, qTp, sTp, ep = M.mx_quantize(src_t, offs_t)
+    torch.cuda.synchronize()
+    assert torch.equal(qp[:R], q[:R]) and torch.equal(qTp[:, :R], qT[:, :R])
+    # rows past every expert: untouched
+    sentinel = torch.full((rows, cols), 0x5A, dtype=torch.uint8, device="cuda")
+    M.lib().moe_mx_quantize_tiled(src_t.data_ptr(), rows, cols, offs_t.data_ptr(), len(offs) - 1,
+                                  sentinel.data_ptr(), s.data_ptr(), None, None, err.data_ptr(),
+                                  None)
+    torch.cuda.synchronize()
+    assert bool((sentinel[R:] == 0x5A).all()) and torch.equal(sentinel[:R], q[:R])
+
+
 def _mx_case(act, E=4, d=256, n=256, counts=(96, 0, 160, 32), seed=23):
     off = np.concatenate([[0], np.cumsum(counts)]).astype(np.int64)
     M_cap = int(off[-1]) + 32
