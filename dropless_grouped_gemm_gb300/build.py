@@ -18,7 +18,8 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libmoe.so")
-SOURCES = ["api.cu", "gemm.cu", "route.cu", "permute.cu", "mx.cu", "act.cu", "selftest.cu"]
+SOURCES = ["api.cu", "gemm.cu", "route.cu", "permute.cu", "mx.cu", "mx_quant.cu", "act.cu",
+           "selftest.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 
