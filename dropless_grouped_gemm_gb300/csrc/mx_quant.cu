@@ -130,15 +130,18 @@ __global__ void __launch_bounds__(256)
   __shared__ int s_list[MOE_MAX_EXPERTS];
   __shared__ int s_count;
   const int ne = used_experts(offsets, E, s_list, &s_count);
-  const int cw = d / 128;                                  // warps per 32-row block
-  const long long nwarps = static_cast<long long>(ne) * (n / 32) * cw;
-  for (long long wi = (blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x) / 32;
-       wi < nwarps; wi += static_cast<long long>(gridDim.x) * blockDim.x / 32) {
-    const int c8 = static_cast<int>(wi % cw) * 16 + (lane & 15);
-    const long long eb = wi / cw;
-    const int b = static_cast<int>(eb % (n / 32));
-    const int eu = static_cast<int>(eb / (n / 32));
-    const int e = offsets ? s_list[eu] : eu;
+  // 32-bit warp indices (the launch checks E * n * d < 2^40): two 32-bit
+  // divisions per iteration split one into expert, row block and column chunk
+  const uint32_t cw = static_cast<uint32_t>(d / 128);      // warps per 32-row block
+  const uint32_t nb = static_cast<uint32_t>(n / 32);       // row blocks of one expert
+  const uint32_t nwarps = static_cast<uint32_t>(ne) * nb * cw;
+  for (uint32_t wi = (blockIdx.x * blockDim.x + threadIdx.x) / 32; wi < nwarps;
+       wi += gridDim.x * blockDim.x / 32) {
+    const uint32_t eb = wi / cw;
+    const int c8 = static_cast<int>(wi - eb * cw) * 16 + (lane & 15);
+    const uint32_t eu = eb / nb;
+    const int b = static_cast<int>(eb - eu * nb);
+    const int e = offsets ? s_list[eu] : static_cast<int>(eu);
     const long long row0 = static_cast<long long>(e) * n + 32LL * b + 16 * half;
     uint32_t x[16][4];
     float amax[8] = {0, 0, 0, 0, 0, 0, 0, 0};
@@ -511,6 +514,7 @@ cudaError_t launch_mx_quantize_weights(const uint16_t* w2, int E, int n, int d,
                                        uint8_t* q_rows, uint8_t* s_rows, int num_sms,
                                        cudaStream_t st) {
   if (q_rows) {
+    if (static_cast<long long>(E) * n * d >= (1LL << 40)) return cudaErrorInvalidValue;
     const long long threads = static_cast<long long>(E) * (n / 32) * (d / 128) * 32;
     const long long want = (threads + 255) / 256;
     const int blocks = static_cast<int>(want < 16LL * num_sms ? want : 16LL * num_sms);
