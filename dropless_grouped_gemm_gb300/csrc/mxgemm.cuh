@@ -66,8 +66,9 @@ cudaError_t launch_mx_quantize_weights(const uint16_t* w2, int E, int n, int d,
                                        cudaStream_t st);
 // ragged activation: row-wise codes q / scales s (q may be null: transposed
 // copy only) and the transposed copy qT / sT (may be null).  tiled = false:
-// plain scales s [rows, cols/32], sT [cols, rows/32]; tiled = true: s in row
-// tiles, sT in K tiles.
+// plain scales s [rows, cols/32], sT [cols, rows/32]; tiled = true (cols a
+// multiple of 128, else cudaErrorInvalidValue): s in row tiles, sT in K
+// tiles.
 cudaError_t launch_mx_quantize_act(const uint16_t* src, int rows, int cols, const int32_t* offsets,
                                    int E, uint8_t* q, uint8_t* s, uint8_t* qT, uint8_t* sT,
                                    int32_t* err, bool tiled, int num_sms, cudaStream_t st);
