@@ -170,6 +170,19 @@ def test_tiled_quantiser_bit_exact(rows, cols, offs):
     assert bool((sentinel[R:] == 0x5A).all()) and torch.equal(sentinel[:R], q[:R])
 
 
+def test_tiled_quantiser_reports_unaligned_offsets():
+    """A 32-row block must lie inside one expert: offsets that are not
+    multiples of 32 raise MOE_DEV_BAD_OFFSETS in the error word (reported,
+    not repaired), and aligned offsets leave it clear."""
+    M = _lib()
+    src = WL.normal((256, 128), (26, WL.X, 0), 1.0, "cuda")
+    _, _, _, _, bad = M.mx_quantize_tiled(src, cuda_i32(np.array([0, 96, 150, 224])))
+    _, _, _, _, good = M.mx_quantize_tiled(src, cuda_i32(np.array([0, 96, 160, 224])))
+    torch.cuda.synchronize()
+    assert int(bad.item()) & M.DEV_BAD_OFFSETS
+    assert int(good.item()) == 0
+
+
 def _mx_case(act, E=4, d=256, n=256, counts=(96, 0, 160, 32), seed=23):
     off = np.concatenate([[0], np.cumsum(counts)]).astype(np.int64)
     M_cap = int(off[-1]) + 32
