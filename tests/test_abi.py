@@ -108,3 +108,25 @@ def test_mx_bwd_workspace_too_small(L):
 def test_workspace_size_host_only(L):
     assert M.route_workspace_size(4096, 8, 256) >= 8 * 256 * 4
     assert M.route_workspace_size(0, 1, 4) == 4 * 4
+
+
+def test_header_compiles_as_c(tmp_path):
+    """include/moe.h is a C ABI: it compiles as strict C99 (no C++ types or
+    defaults leak into it), with every warning an error."""
+    import shutil
+    import subprocess
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    src = tmp_path / "use_moe.c"
+    src.write_text('#include "moe.h"\n'
+                   "int main(void) {\n"
+                   "  moe_mx_bwd b;\n"
+                   "  (void)b;\n"
+                   "  return moe_version() != 0 ? 0 : 1;\n"
+                   "}\n")
+    r = subprocess.run([cc, "-std=c99", "-Wall", "-Wextra", "-pedantic", "-Werror",
+                        "-I", os.path.join(root, "include"), "-c", str(src),
+                        "-o", str(tmp_path / "use_moe.o")], capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
