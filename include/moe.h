@@ -222,7 +222,10 @@ int moe_route_logits(const float* logits, int T, int E, int k, int align, int M_
 
 /*
  * moe_route_offsets_noalloc - moe_route_offsets for callers that cannot
- * allocate device memory.  The pages have no counterpart; this exists for
+ * allocate device memory.  It computes the same routing layout ([TE] "MoE
+ * 학습이 밀집 모델보다 어려운 이유: 래그드 텐서": per-expert counts and the
+ * ragged, expert-major row layout kept on the device).  The pages have no
+ * allocation-free variant; this exists for
  * code that runs where cudaMalloc is off limits: inside a CUDA-graph
  * capture that must not grow a memory pool, under an allocator-free
  * runtime, or in a plugin whose host framework owns every allocation and
@@ -423,7 +426,9 @@ int moe_grouped_mlp_bwd_routed_gather(const moe_bf16* x, const moe_bf16* dO, int
                                       int32_t* err, void* stream);
 
 /*
- * moe_router_grad_rows - dprobs [T*k] (fp32) of the routed backward:
+ * moe_router_grad_rows - dprobs [T*k] (fp32) of the routed backward
+ * ([Sonic] "역전파 계산 그래프 재작성하기": dS = <dO W2^T, A>, whose partial sums
+ * the FC2-dgrad epilogue leaves per 128-column half tile):
  * dprobs[p] = sum over the n_parts partials of ds_part's row row_of_pair[p]
  * (fixed order, so reruns are bitwise identical); 0 for pairs without a
  * row.  n_parts = ceil(n/128).  One launch.
@@ -449,7 +454,9 @@ int moe_mx_quantize_weights(const moe_bf16* W2, int E, int n, int d,
 
 /*
  * moe_mx_quantize_weights2 - both MXFP8 copies of W2 that MXFP8 training
- * uses, from one read of W2: w2_q / w2_s as moe_mx_quantize_weights (blocks
+ * uses ([TE] "Transformer Engine이 제공하는 세 가지 구성 요소": the MXFP8 cast
+ * of the expert weights), from one read of W2: w2_q / w2_s as
+ * moe_mx_quantize_weights (blocks
  * along n, for the forward FC2) and, if w2_q_rows != NULL, w2_q_rows
  * [E, n, d] / w2_s_rows (blocks along d, weight tiles: the
  * moe_mx_quantize_weights_rowwise layout with rows = E*n) for the
@@ -462,7 +469,9 @@ int moe_mx_quantize_weights2(const moe_bf16* W2, int E, int n, int d,
 
 /*
  * moe_mx_quantize_weights_rowwise - MXFP8 copy of a weight for a data
- * gradient: W viewed as [rows, cols] bf16 (W2 [E, n, d] as rows = E*n,
+ * gradient ([TE] "Transformer Engine이 제공하는 세 가지 구성 요소": the MXFP8
+ * cast of the expert weights; here with blocks along the data gradient's
+ * reduction index): W viewed as [rows, cols] bf16 (W2 [E, n, d] as rows = E*n,
  * cols = d; W1 [E, d, n1] as rows = E*d, cols = n1), blocks of 32 along
  * cols.  Writes q [rows, cols] codes and s in weight tiles (rows*cols/32
  * bytes).  rows, cols multiples of 128.
@@ -543,7 +552,10 @@ size_t moe_mx_bwd_workspace_size(int M_cap, int d, int n, int act);
 
 /*
  * moe_grouped_mlp_bwd_mx - MXFP8 backward of the grouped expert MLP (same
- * results as moe_grouped_mlp_bwd up to MXFP8's rounding of the operands).
+ * results as moe_grouped_mlp_bwd up to MXFP8's rounding of the operands;
+ * [TE] "다음 단계: NVFP4, GEMM 융합 양자화, A2A 오버랩": GroupGemm +
+ * dActivation + Quantize/Transpose; [CuTe] "무엇을 해결하려는가": the
+ * transposed low-precision copy that the weight gradients read).
  *   x_perm [M_cap, d], h_saved [M_cap, n1], dy_perm [M_cap, d] bf16;
  *   offsets [E+1] multiples of 32 (route with align = 32); d, n multiples
  *   of 128, M_cap a multiple of 32.  Outputs dh [M_cap, n1], dx_perm
@@ -575,8 +587,10 @@ int moe_mx_quantize(const moe_bf16* src, int rows, int cols,
                     uint8_t* qT, uint8_t* sT, int32_t* err, void* stream);
 
 /*
- * moe_mx_quantize_tiled - moe_mx_quantize with the scales written in the
- * layouts the block-scaled grouped GEMM reads, as moe_grouped_mlp_bwd_mx
+ * moe_mx_quantize_tiled - moe_mx_quantize (the same group-aware
+ * quantisation, [TE] "Transformer Engine이 제공하는 세 가지 구성 요소") with
+ * the scales written in the layouts the block-scaled grouped GEMM reads, as
+ * moe_grouped_mlp_bwd_mx
  * quantises its operands: s in row tiles (128-row tiles from offsets[e] +
  * 128 i, 512-byte chunks of 128 rows x 4 blocks, chunk (t0/32)*(cols/128) +
  * c/128 for the tile starting at row t0) and sT in reduction tiles (the
