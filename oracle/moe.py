@@ -39,7 +39,9 @@ def bf16_round(v) -> np.ndarray:
     For |v| in [2^(e-1), 2^e) the bf16 spacing is 2^(e-8); below the smallest
     normal (2^-126) the spacing is fixed at 2^-133.  Division and
     multiplication by powers of two are exact, so ``rint`` (ties to even) does
-    the rounding."""
+    the rounding.
+    Storage format of every activation and weight ([CuTe] "무엇을 해결하려는가": BF16 activation outputs;
+    "공개된 근거에서 확인되는 점": the benchmark shape is BF16)."""
     v = np.asarray(v, dtype=np.float64)
     out = np.zeros_like(v)
     nz = v != 0
@@ -54,12 +56,14 @@ def bf16_round(v) -> np.ndarray:
 
 
 def bf16_bits(v) -> np.ndarray:
-    """bf16 bit patterns (uint16) of float64 values (rounded first)."""
+    """bf16 bit patterns (uint16) of float64 values (rounded first).
+    Used for bit-exact comparisons ([CuTe] "무엇을 해결하려는가")."""
     q = bf16_round(v).astype(np.float32)  # exact: q is representable
     return (q.view(np.uint32) >> 16).astype(np.uint16)
 
 
 def bf16_from_bits(b) -> np.ndarray:
+    """Values of BF16 bit patterns ([CuTe] "무엇을 해결하려는가")."""
     b = np.asarray(b, dtype=np.uint16)
     return (b.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
 
@@ -75,7 +79,8 @@ def router_topk(logits, k: int):
     """For each token, the k largest logits (ties: lower expert index first,
     in decreasing logit order) and the softmax of those k logits.
 
-    Returns (topk_idx int64 [T, k], probs float64 [T, k])."""
+    Returns (topk_idx int64 [T, k], probs float64 [T, k]).
+    Follows [TE] "Transformer Engine이 제공하는 세 가지 구성 요소" (gate, top-K selection, then dispatch)."""
     logits = np.asarray(logits, dtype=np.float64)
     T, E = logits.shape
     idx = np.zeros((T, k), dtype=np.int64)
@@ -124,6 +129,7 @@ def route_offsets(topk_idx, E: int, align: int = 1, M_cap: int | None = None):
     * ``true_total`` rows demanded before any truncation;
     * ``err`` ERR_BAD_EXPERT if an id is outside [-1, E), ERR_OVERFLOW if
       ``true_total > M_cap`` (rows at or past M_cap are dropped).
+    Follows [TE] "MoE 학습이 밀집 모델보다 어려운 이유: 래그드 텐서" and ""드롭리스"의 실제 경계: 래그드 버퍼 계수와 오버플로 검사".
     """
     idx = np.asarray(topk_idx, dtype=np.int64)
     T, k = idx.shape if idx.ndim == 2 else (0, 1)
@@ -228,7 +234,8 @@ def router_grad(dO, y_perm, row_of_pair, T: int, k: int):
 
 def interleave_gate_up(w_gate, w_up):
     """[..., d, n] gate and up -> [..., d, 2n] with column 2j = gate_j,
-    column 2j+1 = up_j."""
+    column 2j+1 = up_j.
+    Follows [CuTe] "핵심 아이디어 / 구조 / 동작 방식" (gate and up columns interleaved)."""
     w_gate = np.asarray(w_gate)
     w_up = np.asarray(w_up)
     out = np.empty(w_gate.shape[:-1] + (2 * w_gate.shape[-1],), dtype=w_gate.dtype)
@@ -238,6 +245,7 @@ def interleave_gate_up(w_gate, w_up):
 
 
 def split_gate_up(w1):
+    """Inverse of interleave_gate_up ([CuTe] "핵심 아이디어 / 구조 / 동작 방식")."""
     w1 = np.asarray(w1)
     return w1[..., 0::2], w1[..., 1::2]
 
@@ -254,7 +262,8 @@ _A = 0.044715
 
 def phi(g, act: str):
     """Gate nonlinearity: SiLU (Swish-1) for SwiGLU, tanh-approximated GELU
-    (Hendrycks & Gimpel) for GeGLU."""
+    (Hendrycks & Gimpel) for GeGLU.
+    Follows [CuTe] "핵심 아이디어 / 구조 / 동작 방식" (Swish on the gate side)."""
     g = np.asarray(g, dtype=np.float64)
     if act == "swiglu":
         return g / (1.0 + np.exp(-g))
@@ -264,7 +273,8 @@ def phi(g, act: str):
 
 
 def dphi(g, act: str):
-    """Analytic derivative of ``phi``."""
+    """Analytic derivative of ``phi``, needed by the dActivation epilogue
+    ([CuTe] "무엇을 해결하려는가": the backward GroupGemm + dActivation)."""
     g = np.asarray(g, dtype=np.float64)
     if act == "swiglu":
         s = 1.0 / (1.0 + np.exp(-g))
@@ -278,7 +288,8 @@ def dphi(g, act: str):
 
 def act_forward(h, act: str):
     """A = act(H).  Gated: H columns (2j, 2j+1) = (gate, up), A_j = phi(g) u.
-    Squared ReLU: A = max(H, 0)^2."""
+    Squared ReLU: A = max(H, 0)^2.
+    Follows [CuTe] "무엇을 해결하려는가" (SwiGLU, GeGLU, sReLU) and "핵심 아이디어 / 구조 / 동작 방식"."""
     h = np.asarray(h, dtype=np.float64)
     if act == "srelu":
         return np.maximum(h, 0.0) ** 2
@@ -288,7 +299,9 @@ def act_forward(h, act: str):
 
 def act_backward(h, dA, act: str):
     """dH from dA and H (chain rule of ``act_forward``).  Gated:
-    dg = dA u phi'(g), du = dA phi(g), written back interleaved."""
+    dg = dA u phi'(g), du = dA phi(g), written back interleaved.
+    Follows [CuTe] "무엇을 해결하려는가" (GroupGemm + dActivation) and [Sonic] "역전파 계산 그래프 재작성하기" (the dH
+    kernel reloads H)."""
     h = np.asarray(h, dtype=np.float64)
     dA = np.asarray(dA, dtype=np.float64)
     if act == "srelu":
@@ -307,6 +320,7 @@ def act_backward(h, dA, act: str):
 # ---------------------------------------------------------------------------
 
 def _rb(v, on):
+    """Rounding to BF16 where a BF16 implementation stores a tensor ([CuTe] "무엇을 해결하려는가")."""
     return bf16_round(v) if on else np.asarray(v, dtype=np.float64)
 
 
@@ -317,7 +331,8 @@ def grouped_mlp_fwd(x_perm, offsets, W1, W2, act: str, round_bf16: bool = True):
     Rounding points mirror what a bf16 implementation stores: H (saved for
     backward) and A are rounded to bf16, A is computed from the unrounded H,
     FC2 reads the rounded A, Y is rounded.  Rows outside every expert are
-    NaN (undefined)."""
+    NaN (undefined).
+    Follows [TE] "최적화 1: grouped GEMM, 전문가마다 다른 토큰 수를 커널 하나로" and [CuTe] "핵심 아이디어 / 구조 / 동작 방식"."""
     x_perm = np.asarray(x_perm, dtype=np.float64)
     W1 = np.asarray(W1, dtype=np.float64)
     W2 = np.asarray(W2, dtype=np.float64)
@@ -366,7 +381,9 @@ def grouped_mlp_bwd(x_perm, H, A, dY, offsets, W1, W2, act: str,
     dA_e = dY_e W2_e^T, dH_e = act'(H_e; dA_e), dW2_e = A_e^T dY_e,
     dX_e = dH_e W1_e^T, dW1_e = X_e^T dH_e.  An expert with no rows gets
     dW1_e = dW2_e = 0.  dH is rounded to bf16 before it feeds dX and dW1
-    (a bf16 implementation stores it)."""
+    (a bf16 implementation stores it).
+    Follows [CuTe] "무엇을 해결하려는가" (GroupGemm + dActivation) and [TE] "최적화 1: grouped GEMM, 전문가마다 다른
+    토큰 수를 커널 하나로"."""
     x_perm = np.asarray(x_perm, dtype=np.float64)
     H = np.asarray(H, dtype=np.float64)
     A = np.asarray(A, dtype=np.float64)
@@ -452,14 +469,17 @@ def grouped_mlp_bwd_routed(x_perm, H, dO_perm, row_prob, offsets, W1, W2, act: s
 
 def hadamard16() -> np.ndarray:
     """16x16 Hadamard matrix of Sylvester's construction, H[i, j] =
-    (-1)^popcount(i & j), scaled by 1/4 so that it is orthonormal."""
+    (-1)^popcount(i & j), scaled by 1/4 so that it is orthonormal.  The
+    rotation of the backward's NVFP4 statistic ([CuTe] "핵심 아이디어 / 구조 /
+    동작 방식": amax of the transposed, Hadamard-rotated output)."""
     i = np.arange(16)
     parity = np.array([[bin(a & b).count("1") & 1 for b in i] for a in i])
     return np.where(parity == 1, -1.0, 1.0) / 4.0
 
 
 def amax(t) -> float:
-    """Per-tensor absolute maximum."""
+    """Per-tensor absolute maximum.
+    Follows [CuTe] "핵심 아이디어 / 구조 / 동작 방식" (the forward output's per-tensor amax)."""
     t = np.asarray(t, dtype=np.float64)
     return float(np.abs(t).max()) if t.size else 0.0
 
@@ -470,7 +490,8 @@ def amax_rht_transposed(G, offsets) -> float:
     [offsets[e], offsets[e+1]) are cut into 16-row blocks from the expert's
     first row (the last block zero-padded), and each column of a block is
     multiplied by hadamard16().  (Reading: the pages name the statistic;
-    the rotation is the orthonormal Sylvester one, without random signs.)"""
+    the rotation is the orthonormal Sylvester one, without random signs.)
+    Follows [CuTe] "핵심 아이디어 / 구조 / 동작 방식"."""
     G = np.asarray(G, dtype=np.float64)
     Hm = hadamard16()
     best = 0.0
@@ -492,7 +513,8 @@ def amax_rht_transposed(G, offsets) -> float:
 
 def fc1_rows(x_rows, W1_e, act: str, cols=None):
     """(H, A) of the given rows of one expert; ``cols`` selects A columns
-    (and the matching H column pairs when gated)."""
+    (and the matching H column pairs when gated).
+    The arithmetic of grouped_mlp_fwd on selected rows ([CuTe] "핵심 아이디어 / 구조 / 동작 방식")."""
     x_rows = np.asarray(x_rows, dtype=np.float64)
     W1_e = np.asarray(W1_e, dtype=np.float64)
     h = x_rows @ W1_e
@@ -503,4 +525,6 @@ def fc1_rows(x_rows, W1_e, act: str, cols=None):
 
 
 def fc2_rows(a_rows, W2_e):
+    """The arithmetic of grouped_mlp_fwd's down-projection on selected rows ([TE] "최적화 1: grouped
+    GEMM, 전문가마다 다른 토큰 수를 커널 하나로")."""
     return bf16_round(np.asarray(a_rows, np.float64) @ np.asarray(W2_e, np.float64))

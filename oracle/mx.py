@@ -29,7 +29,8 @@ E4M3_MAX = 448.0
 
 
 def e4m3_decode_table() -> np.ndarray:
-    """Value of each of the 256 codes (NaN for the two NaN codes)."""
+    """Value of each of the 256 codes (NaN for the two NaN codes).
+    E4M3 element format of MXFP8 ([TE] "Transformer Engine이 제공하는 세 가지 구성 요소"; OCP MX v1.0)."""
     vals = np.empty(256, dtype=np.float64)
     for c in range(256):
         s = -1.0 if c & 0x80 else 1.0
@@ -51,6 +52,7 @@ _POS_VALS = _DEC[:0x7F]
 
 
 def e4m3_decode(codes) -> np.ndarray:
+    """Decodes E4M3 codes ([TE] "Transformer Engine이 제공하는 세 가지 구성 요소"; OCP MX v1.0)."""
     return _DEC[np.asarray(codes, dtype=np.uint8)]
 
 
@@ -58,7 +60,8 @@ def e4m3_encode_bruteforce(v) -> np.ndarray:
     """Brute-force nearest finite E4M3 code, ties to the even code (even
     mantissa), magnitudes above 448 saturate to 448; the sign bit is kept
     (so -0 and negative values that round to zero give 0x80).  This is the
-    definition; ``e4m3_encode`` computes the same function faster."""
+    definition; ``e4m3_encode`` computes the same function faster.
+    MXFP8 element rounding ([CuTe] "핵심 아이디어 / 구조 / 동작 방식": the MXFP8 output; OCP MX v1.0)."""
     v = np.asarray(v, dtype=np.float64)
     # saturate first: beyond 448 every magnitude maps to 448 (measuring
     # distances from huge values would also lose the codes' spacing)
@@ -78,7 +81,8 @@ def e4m3_encode_bruteforce(v) -> np.ndarray:
 def e4m3_encode(v) -> np.ndarray:
     """Same function as ``e4m3_encode_bruteforce`` (nearest finite code,
     ties to even, saturating, sign kept), found by bisection in the sorted
-    table of the 127 non-negative finite values instead of a full scan."""
+    table of the 127 non-negative finite values instead of a full scan.
+    MXFP8 element rounding ([CuTe] "핵심 아이디어 / 구조 / 동작 방식"; OCP MX v1.0)."""
     v = np.asarray(v, dtype=np.float64)
     a = np.minimum(np.abs(v).reshape(-1), E4M3_MAX)
     hi = np.clip(np.searchsorted(_POS_VALS, a, side="left"), 0, 0x7E)   # first value >= a
@@ -94,7 +98,9 @@ def e4m3_encode(v) -> np.ndarray:
 
 def e8m0_exponent(amax) -> np.ndarray:
     """Shared-scale exponent e = clamp(floor(log2 amax) - 8, -127, 127);
-    amax = 0 gives -127.  floor(log2) is read exactly from frexp."""
+    amax = 0 gives -127.  floor(log2) is read exactly from frexp.
+    The E8M0 shared scale of an MXFP8 block ([TE] "Transformer Engine이 제공하는 세 가지 구성 요소"; OCP MX
+    v1.0)."""
     amax = np.asarray(amax, dtype=np.float64)
     _, ex = np.frexp(amax)          # amax = m 2^ex, m in [0.5, 1)
     e = (ex - 1) - 8
@@ -104,7 +110,8 @@ def e8m0_exponent(amax) -> np.ndarray:
 
 def mx_quantize_blocks(blocks):
     """``blocks`` [..., 32] float64 -> (codes uint8 [..., 32], scale codes
-    uint8 [...]) where the scale code is e + 127."""
+    uint8 [...]) where the scale code is e + 127.
+    One MXFP8 block ([CuTe] "핵심 아이디어 / 구조 / 동작 방식": the MXFP8 output; OCP MX v1.0)."""
     blocks = np.asarray(blocks, dtype=np.float64)
     amax = np.abs(blocks).max(axis=-1)
     e = e8m0_exponent(amax)
@@ -114,7 +121,8 @@ def mx_quantize_blocks(blocks):
 
 def mx_quantize_rows(A):
     """Row-wise MX: blocks of 32 consecutive columns of each row.
-    A [M, n] (n % 32 == 0) -> codes [M, n], scales [M, n/32]."""
+    A [M, n] (n % 32 == 0) -> codes [M, n], scales [M, n/32].
+    Follows [CuTe] "핵심 아이디어 / 구조 / 동작 방식" (the MXFP8 output)."""
     A = np.asarray(A, dtype=np.float64)
     M, n = A.shape
     q, s = mx_quantize_blocks(A.reshape(M, n // 32, 32))
@@ -128,7 +136,9 @@ def mx_quantize_cols(A, offsets, M_cap=None):
     range starts on a block boundary and no block crosses two experts).
 
     Returns (codes_T uint8 [n, M_cap], scales_T uint8 [n, M_cap/32]); rows
-    outside every expert are left 0."""
+    outside every expert are left 0.
+    Follows [CuTe] "핵심 아이디어 / 구조 / 동작 방식" (the transposed output) and [TE] "Transformer Engine이
+    제공하는 세 가지 구성 요소" (group-aware quantisation)."""
     A = np.asarray(A, dtype=np.float64)
     M = A.shape[0] if M_cap is None else M_cap
     n = A.shape[1]
@@ -148,7 +158,9 @@ def mx_quantize_cols(A, offsets, M_cap=None):
 
 def mx_quantize_weights(W2):
     """W2 [E, n, d]: blocks of 32 consecutive rows (FC2's reduction index)
-    for each column.  Returns codes [E, n, d] and scales [E, n/32, d]."""
+    for each column.  Returns codes [E, n, d] and scales [E, n/32, d].
+    Follows [TE] "Transformer Engine이 제공하는 세 가지 구성 요소" (MXFP8 expert weights for the MXFP8 grouped
+    GEMM)."""
     W2 = np.asarray(W2, dtype=np.float64)
     E, n, d = W2.shape
     blk = W2.reshape(E, n // 32, 32, d).transpose(0, 1, 3, 2)   # [E, n/32, d, 32]
@@ -158,7 +170,8 @@ def mx_quantize_weights(W2):
 
 def mx_dequantize(codes, scale_codes, axis_block: int):
     """Decode codes with their block scales; ``axis_block`` is the axis of
-    ``codes`` along which 32 consecutive elements share a scale."""
+    ``codes`` along which 32 consecutive elements share a scale.
+    Inverse of the MX block rule ([TE] "Transformer Engine이 제공하는 세 가지 구성 요소"; OCP MX v1.0)."""
     v = e4m3_decode(codes)
     s = np.ldexp(1.0, scale_codes.astype(np.int64) - 127)
     s = np.repeat(s, 32, axis=axis_block)
@@ -168,7 +181,8 @@ def mx_dequantize(codes, scale_codes, axis_block: int):
 def mx_fc2(A_q, A_s, W2_q, W2_s, offsets):
     """MXFP8 down-projection Y_e = sum over 32-blocks b of
     (s_A s_W) * sum_{i in b} qA qW, float64; Y rounded to bf16 by the caller.
-    Products of dequantised values are exact in float64."""
+    Products of dequantised values are exact in float64.
+    Follows [TE] "Transformer Engine이 제공하는 세 가지 구성 요소" (the MXFP8 grouped GEMM)."""
     from .moe import bf16_round
     A = mx_dequantize(A_q, A_s, axis_block=1)
     M = A.shape[0]
@@ -204,7 +218,8 @@ def mx_dgrad(G_q, G_s, W_q, W_s, offsets):
 
     G_q [M, K] codes with row-wise scales G_s [M, K/32]; W_q [E, N, K] codes
     with scales W_s [E, N, K/32] (blocks along K, the last axis).  Returns
-    float64 [M, N], unrounded; rows outside every expert are NaN."""
+    float64 [M, N], unrounded; rows outside every expert are NaN.
+    Follows [TE] "다음 단계: NVFP4, GEMM 융합 양자화, A2A 오버랩" (the backward grouped GEMMs in MXFP8)."""
     G = mx_dequantize(G_q, G_s, axis_block=1)
     E, N, K = W_q.shape
     out = np.full((G.shape[0], N), np.nan)
@@ -221,7 +236,9 @@ def mx_wgrad(P_qT, P_sT, Q_qT, Q_sT, offsets):
     """Block-scaled weight gradient dW_e = P_e^T Q_e, summed over the rows of
     expert e, from the transposed copies: P_qT [p, M] with scales P_sT
     [p, M/32] (blocks of 32 rows inside one expert), Q_qT [q, M], Q_sT.
-    Returns float64 [E, p, q], unrounded; an expert with no rows gets 0."""
+    Returns float64 [E, p, q], unrounded; an expert with no rows gets 0.
+    Follows [CuTe] "무엇을 해결하려는가" (the transposed low-precision copy) and [TE] "다음 단계: NVFP4, GEMM 융합
+    양자화, A2A 오버랩"."""
     P = mx_dequantize(P_qT, P_sT, axis_block=1)              # [p, M]
     Q = mx_dequantize(Q_qT, Q_sT, axis_block=1)              # [q, M]
     E = len(offsets) - 1
@@ -248,7 +265,9 @@ def mx_grouped_mlp_bwd(x_perm, H, A, dY, offsets, W1, W2, act: str):
       6. dX = deq(dH) deq(W1_e)^T;
       7. x -> transposed copy;  dW1_e = deq(x^T) deq(dH^T).
     Returns a dict with dH, dX, dW1, dW2 (bf16-rounded float64) and the
-    quantised intermediates (codes, scales) of steps 1, 2, 5 and 7."""
+    quantised intermediates (codes, scales) of steps 1, 2, 5 and 7.
+    Follows [TE] "다음 단계: NVFP4, GEMM 융합 양자화, A2A 오버랩" (GroupGemm + dActivation +
+    Quantize/Transpose) and [CuTe] "무엇을 해결하려는가"."""
     from .moe import act_backward, bf16_round
     x_perm = np.asarray(x_perm, dtype=np.float64)
     H = np.asarray(H, dtype=np.float64)
