@@ -1,5 +1,7 @@
 // api.cu - the extern "C" entry points of libmoe (declared in include/moe.h):
 // host-side argument checks, TMA tensor-map encoding, launch sequencing.
+// What each entry point computes, and the passage of the pages that defines
+// it, is stated at its declaration in include/moe.h.
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>

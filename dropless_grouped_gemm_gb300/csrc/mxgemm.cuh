@@ -1,4 +1,5 @@
-// mxgemm.cuh - host-side interface of the MXFP8 kernels (mx.cu).
+// mxgemm.cuh - host-side interface of the MXFP8 kernels: the block-scaled
+// grouped GEMM (mx.cu) and the quantisers (mx_quant.cu).
 //
 // Scale layouts read by the block-scaled GEMM.  All are made of 512-byte
 // chunks in the order tcgen05.cp moves them into TMEM (128 operand rows x 4
