@@ -22,7 +22,8 @@ import torch
 
 __all__ = [
     "ACT", "FLAG_SAVE_H", "DEV_BAD_EXPERT", "DEV_OVERFLOW", "DEV_TIMEOUT", "DEV_BAD_OFFSETS",
-    "lib", "lib_path", "version", "last_launch_count", "route_workspace_size", "route_offsets",
+    "lib", "lib_path", "version", "last_launch_count", "route_workspace_size", "workspace_size",
+    "route_offsets",
     "router_topk",
     "permute", "unpermute", "grouped_mlp_fwd", "grouped_mlp_bwd", "MoeError",
     "FLAG_MXFP8", "MxFwd", "mx_quantize_weights", "mx_quantize", "mx_buffers",
@@ -116,6 +117,8 @@ def lib():
         L.moe_mx_quantize_weights_rowwise.argtypes = [vp, i32, i32, vp, i32, vp, vp, vp]
         L.moe_mx_bwd_workspace_size.restype = sz
         L.moe_mx_bwd_workspace_size.argtypes = [i32, i32, i32, i32]
+        L.moe_workspace_size.restype = sz
+        L.moe_workspace_size.argtypes = [i32, i32, i32, i32, i32, i32, i32, i32]
         L.moe_grouped_mlp_bwd_mx.restype = i32
         L.moe_grouped_mlp_bwd_mx.argtypes = [vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, vp, vp,
                                              vp, vp, vp, vp, vp]
@@ -199,6 +202,14 @@ def router_topk(logits: torch.Tensor, k: int, stream=None):
 
 def route_workspace_size(T: int, k: int, E: int) -> int:
     return int(lib().moe_route_workspace_size(T, k, E))
+
+
+def workspace_size(T: int, k: int, E: int, M_cap: int, d: int, n: int, act: str = "swiglu",
+                   mxfp8: bool = False) -> int:
+    """Device scratch for one layer's calls (moe_workspace_size): the routing
+    layout's and, with ``mxfp8``, the MXFP8 backward's, one buffer for both."""
+    return int(lib().moe_workspace_size(T, k, E, M_cap, d, n, ACT[act],
+                                        FLAG_MXFP8 if mxfp8 else 0))
 
 
 def route_offsets(topk_idx: torch.Tensor, E: int, align: int = 1, M_cap: int | None = None,

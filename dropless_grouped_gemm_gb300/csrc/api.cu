@@ -654,6 +654,12 @@ size_t moe_mx_bwd_workspace_size(int M_cap, int d, int n, int act) {
   return carve_mx_bwd(nullptr, M_cap, d, n1, n).bytes;
 }
 
+size_t moe_workspace_size(int T, int k, int E, int M_cap, int d, int n, int act, int flags) {
+  const size_t r = moe_route_workspace_size(T, k, E);
+  const size_t m = (flags & MOE_FLAG_MXFP8) ? moe_mx_bwd_workspace_size(M_cap, d, n, act) : 0;
+  return r > m ? r : m;
+}
+
 int moe_grouped_mlp_fwd_gather(const moe_bf16* x, int T, int k, const int32_t* pair_of_row,
                                const int32_t* offsets, int E, int M_cap, int d, int n,
                                const moe_bf16* W1, const moe_bf16* W2, int act, int flags,

@@ -551,6 +551,16 @@ int moe_activation_bwd(const moe_bf16* h, const moe_bf16* da, const int32_t* off
 size_t moe_mx_bwd_workspace_size(int M_cap, int d, int n, int act);
 
 /*
+ * moe_workspace_size - device scratch for one layer's calls: the larger of
+ * moe_route_workspace_size(T, k, E) and, when flags has MOE_FLAG_MXFP8,
+ * moe_mx_bwd_workspace_size(M_cap, d, n, act).  One buffer of this size
+ * serves both, since the routing layout and the MXFP8 backward use it at
+ * different points of the step on the same stream; the other entry points
+ * need no scratch.  Host-only, no CUDA call; 0 when every part is invalid.
+ */
+size_t moe_workspace_size(int T, int k, int E, int M_cap, int d, int n, int act, int flags);
+
+/*
  * moe_grouped_mlp_bwd_mx - MXFP8 backward of the grouped expert MLP (same
  * results as moe_grouped_mlp_bwd up to MXFP8's rounding of the operands;
  * [TE] "다음 단계: NVFP4, GEMM 융합 양자화, A2A 오버랩": GroupGemm +

@@ -130,3 +130,16 @@ def test_header_compiles_as_c(tmp_path):
                         "-I", os.path.join(root, "include"), "-c", str(src),
                         "-o", str(tmp_path / "use_moe.o")], capture_output=True, text=True)
     assert r.returncode == 0, r.stderr
+
+
+def test_layer_workspace_size_is_the_larger_part(L):
+    """moe_workspace_size: the routing layout's scratch, or the MXFP8
+    backward's when that is larger and requested; host-only."""
+    T, k, E, M_cap, d, n = 4096, 8, 256, 32768 + 256 * 31, 7168, 2048
+    r = L.moe_route_workspace_size(T, k, E)
+    m = L.moe_mx_bwd_workspace_size(M_cap, d, n, 0)
+    assert r > 0 and m > r
+    assert L.moe_workspace_size(T, k, E, M_cap, d, n, 0, 0) == r
+    assert L.moe_workspace_size(T, k, E, M_cap, d, n, 0, M.FLAG_MXFP8) == m
+    assert M.workspace_size(T, k, E, M_cap, d, n, "swiglu", mxfp8=True) == m
+    assert L.moe_workspace_size(0, 0, 0, 0, 0, 0, 0, M.FLAG_MXFP8) == 0
