@@ -19,9 +19,13 @@ combine, and their backward with the router-score gradient.
 Inputs are seeded and synthetic (``workloads``), resident in HBM before the
 timed region, and larger than L2 (no flush needed).  Timing: W warm-up
 steps, then K steps between CUDA events on the launching stream, bracketed
-by a barrier and a synchronize, max over ranks.  Under torchrun each rank
-runs an independent replica (the path does not shard; there is no
-collective in the data path).
+by a synchronize on both sides.
+
+The path runs on one GPU.  Its grouped GEMMs load shared weight tiles with
+cluster-multicast TMA, which is kept to single-GPU processes: with
+WORLD_SIZE > 1 (torchrun) or --gpus > 1 the bench prints one
+``{"unavailable": ...}`` line and exits with status 2, before any CUDA or
+process-group call.
 """
 from __future__ import annotations
 
@@ -483,39 +487,51 @@ def cpu_cores():
     return os.cpu_count()
 
 
+# ---------------------------------------------------------------- roofline
+SUSTAINED_AFTER_S = 2.0
+
+
+def roofline(kernel, flops, nbytes, t_s, peaks, fp8, region_s):
+    """Roofline record of one kernel: achieved = algorithmic FLOPs (or
+    bytes) per launch / its average live duration.  The tensor peak is the
+    measured burst bf16 rate when the timed region is shorter than
+    SUSTAINED_AFTER_S (the GPU has not settled at its power cap yet), the
+    sustained rate otherwise; the other one is reported beside it.  FP8
+    peaks are 2x the bf16 figure (the nominal dense ratio, not a
+    measurement)."""
+    mult = 2.0 if fp8 else 1.0
+    burst = peaks["bf16_tflops"] * mult
+    sust = peaks["bf16_tflops_sustained"] * mult
+    use_sust = region_s >= SUSTAINED_AFTER_S
+    tpeak = sust if use_sust else burst
+    tag = "bf16_tflops_sustained" if use_sust else "bf16_tflops"
+    if flops / (tpeak * 1e12) >= nbytes / (peaks["hbm_gbs"] * 1e9):
+        ach = flops / t_s / 1e12
+        return {"kernel": kernel, "bound": "tensor", "achieved": round(ach, 1),
+                "peak": round(tpeak, 1), "unit": "TFLOP/s",
+                "peak_kind": (f"2 x {tag} (fp8 nominal ratio, {peaks['source']})" if fp8 else
+                              f"{tag} ({peaks['source']})"),
+                "frac": round(ach / tpeak, 4),
+                "frac_burst": round(ach / burst, 4), "frac_sustained": round(ach / sust, 4),
+                "algorithmic_per_launch": flops}
+    ach = nbytes / t_s / 1e9
+    return {"kernel": kernel, "bound": "hbm", "achieved": round(ach, 1),
+            "peak": peaks["hbm_gbs"], "unit": "GB/s", "peak_kind": f"hbm_gbs ({peaks['source']})",
+            "frac": round(ach / peaks["hbm_gbs"], 4), "algorithmic_per_launch": nbytes}
+
+
 # ---------------------------------------------------------------- main
-def dist_setup(gpus):
-    import torch
-    ws = int(os.environ.get("WORLD_SIZE", "1"))
-    rank = int(os.environ.get("RANK", "0"))
-    lrank = int(os.environ.get("LOCAL_RANK", "0"))
-    if ws > 1:
-        import torch.distributed as dist
-        torch.cuda.set_device(lrank)
-        dist.init_process_group("nccl", device_id=torch.device("cuda", lrank))
-    return ws, rank, lrank
+SINGLE_GPU_ONLY = ("single-GPU path: the grouped GEMMs use cluster-multicast TMA loads, which "
+                   "run only in single-GPU processes; run one process per GPU as independent "
+                   "replicas")
 
 
-def barrier(ws):
-    if ws > 1:
-        import torch.distributed as dist
-        dist.barrier()
-
-
-def max_over_ranks(v, ws, device="cuda"):
-    """Max of a per-rank scalar over all ranks (the job's time is the
-    slowest replica's)."""
-    if ws == 1:
-        return v
-    import torch
-    import torch.distributed as dist
-    t = torch.tensor([v], dtype=torch.float64, device=device)
-    dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    return float(t.item())
+def world_size():
+    return int(os.environ.get("WORLD_SIZE", "1"))
 
 
 def run_reference(args, w):
-    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    ws = world_size()
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return 0
@@ -573,14 +589,19 @@ def main():
     if args.impl == "reference":
         return run_reference(args, w)
 
+    if world_size() > 1 or args.gpus > 1:
+        if int(os.environ.get("RANK", "0")) == 0:
+            print(json.dumps({"unavailable": SINGLE_GPU_ONLY, "n_gpus": max(world_size(),
+                                                                              args.gpus)}),
+                  flush=True)
+        return 2
+
     import torch
-    ws, rank, lrank = dist_setup(args.gpus)
-    dev = f"cuda:{lrank}"
+    lrank = 0
+    dev = "cuda:0"
     torch.cuda.set_device(lrank)
-    if rank == 0:
-        from dropless_grouped_gemm_gb300 import build as B
-        B.build()
-    barrier(ws)
+    from dropless_grouped_gemm_gb300 import build as B
+    B.build()
     import dropless_grouped_gemm_gb300 as M
     M.lib()
 
@@ -610,7 +631,6 @@ def main():
     sampler = ClockSampler(gpu_id)
     time.sleep(0.3)
     launches = 0
-    barrier(ws)
     torch.cuda.synchronize()
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
@@ -622,18 +642,16 @@ def main():
     torch.cuda.synchronize()
     used = M.lib().moe_launch_events_used()
     M.lib().moe_set_launch_events(None, 0)
-    barrier(ws)
     clocks = sampler.stop()
     if int(o["err"].item()) != 0:   # a timed region with device errors measures nothing
         raise SystemExit(f"device error bits {int(o['err'].item())} in the timed region")
     ms = t_start.elapsed_time(t_end) / args.steps
-    ms = max_over_ranks(ms, ws)
 
     Mrows = inp["M"]
     fwd_f, bwd_f = useful_flops(w, Mrows)
-    per_rank_tf = (fwd_f + bwd_f) / (ms * 1e-3) / 1e12
-    value = per_rank_tf * ws
+    value = (fwd_f + bwd_f) / (ms * 1e-3) / 1e12
     peaks = load_peaks()
+    region_s = ms * args.steps * 1e-3
 
     # per-kernel durations
     dur = {nm: [] for nm in names}
@@ -659,30 +677,16 @@ def main():
     fl, by = work[dom]
     t_dom = kern[dom]["ms"] * 1e-3
     fp8 = w.mxfp8 and (dom == "fc2" or (w.backward and dom in KERNELS_BWD))
-    tpeak = peaks["bf16_tflops_sustained"] * (2.0 if fp8 else 1.0)   # dense fp8 = 2x bf16 (nominal ratio)
-    tensor_time = fl / (tpeak * 1e12)
-    hbm_time = by / (peaks["hbm_gbs"] * 1e9)
-    if tensor_time >= hbm_time:
-        roof = {"kernel": dom, "bound": "tensor", "achieved": round(fl / t_dom / 1e12, 1),
-                "peak": tpeak, "unit": "TFLOP/s",
-                "peak_kind": (f"2 x bf16_tflops_sustained (fp8, {peaks['source']})" if fp8 else
-                              f"bf16_tflops_sustained ({peaks['source']})")}
-        algo = fl
-    else:
-        roof = {"kernel": dom, "bound": "hbm", "achieved": round(by / t_dom / 1e9, 1),
-                "peak": peaks["hbm_gbs"], "unit": "GB/s", "peak_kind": f"hbm_gbs ({peaks['source']})"}
-        algo = by
-    roof["frac"] = round(roof["achieved"] / roof["peak"], 4)
-    roof["algorithmic_per_launch"] = algo
+    roof = roofline(dom, fl, by, t_dom, peaks, fp8, region_s)
     roof["traffic"] = ncu_traffic(dom, w)
 
     # the same step captured once as a CUDA graph and replayed (the pages'
     # benchmark times graph replays); the whole path is capturable
-    graph = time_graph(step, args.steps, ws, fwd_f + bwd_f)
+    graph = time_graph(step, max(args.steps, 20), fwd_f + bwd_f)
 
     # end to end through the public API with host buffers
     e2e_steps = args.e2e_steps if args.e2e_steps else max(args.steps, 30)
-    e2e = run_e2e(w, inp, o, step, e2e_steps, ws, fwd_f + bwd_f)
+    e2e = run_e2e(w, inp, o, step, e2e_steps, fwd_f + bwd_f)
 
     # fused against unfused epilogues (outside the timed region)
     fusion = None
@@ -690,7 +694,7 @@ def main():
         fusion = fusion_control(w, inp, o)
 
     cpu = None
-    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+    if not args.no_cpu_baseline:
         v, dt = time_oracle(w, args.cpu_rows)
         cpu = {"value": v, "unit": "TFLOP/s", "cores": cpu_cores(), "kind": "oracle",
                "sample": f"{args.cpu_rows} rows of expert 0, float64 "
@@ -699,28 +703,24 @@ def main():
 
     if int(o["err"].item()) != 0:   # graph, end-to-end and fusion legs share the error word
         raise SystemExit(f"device error bits {int(o['err'].item())} after the graph / e2e legs")
-    if rank == 0:
-        line = {
-            "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": ws,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 4),
-            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-            "dtype": "e4m3/e8m0 block-scaled (FC1 bf16)" if w.mxfp8 else "bf16",
-            "data": "synthetic",
-            "pct_of_bf16_peak": round(100 * per_rank_tf / peaks["bf16_tflops"], 2),
-            "config": {"workload": w.name, "E": w.E, "T": w.T, "top_k": w.k, "d": w.d, "n": w.n,
-                       "act": w.act, "rows": Mrows, "nonempty_experts": inp["E_ne"],
-                       "step": step_description(w),
-                       "l2": "inputs larger than L2 (no flush)", "parallelism": "replicas"},
-            "roofline": roof, "kernels": kern, "graph": graph, "cpu_baseline": cpu, "e2e": e2e,
-            "clocks": clocks, "gpu_launches": launches,
-        }
-        if fusion is not None:
-            line["fusion_control"] = fusion
-        print(json.dumps(line), flush=True)
-    barrier(ws)
-    if ws > 1:
-        import torch.distributed as dist
-        dist.destroy_process_group()
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "e4m3/e8m0 block-scaled (FC1 bf16)" if w.mxfp8 else "bf16",
+        "data": "synthetic",
+        "pct_of_bf16_peak": round(100 * value / peaks["bf16_tflops"], 2),
+        "config": {"workload": w.name, "E": w.E, "T": w.T, "top_k": w.k, "d": w.d, "n": w.n,
+                   "act": w.act, "rows": Mrows, "nonempty_experts": inp["E_ne"],
+                   "step": step_description(w),
+                   "l2": "inputs larger than L2 (no flush)", "parallelism": "none (1 GPU)",
+                   "timed_region_s": round(region_s, 3)},
+        "roofline": roof, "kernels": kern, "graph": graph, "cpu_baseline": cpu, "e2e": e2e,
+        "clocks": clocks, "gpu_launches": launches,
+    }
+    if fusion is not None:
+        line["fusion_control"] = fusion
+    print(json.dumps(line), flush=True)
     return 0
 
 
@@ -810,9 +810,10 @@ def step_description(w):
             "MLP (grouped_mlp_bwd_routed + router_grad_rows) + combine backward")
 
 
-def time_graph(step, steps, ws, flops):
-    """One step captured as a CUDA graph, replayed `steps` times between
-    CUDA events."""
+def time_graph(step, replays, flops):
+    """One step captured as a CUDA graph and replayed: each of ``replays``
+    (at least 20) replays timed by its own pair of CUDA events; the median
+    replay is reported (the pages time graph replays)."""
     import torch
     cur = torch.cuda.current_stream()
     side = torch.cuda.Stream()
@@ -825,43 +826,48 @@ def time_graph(step, steps, ws, flops):
     for _ in range(2):
         g.replay()
     torch.cuda.synchronize()
-    barrier(ws)
-    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    s.record()
-    for _ in range(steps):
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(replays)]
+    for s, e in evs:
+        s.record()
         g.replay()
-    e.record()
+        e.record()
     torch.cuda.synchronize()
-    ms = max_over_ranks(s.elapsed_time(e) / steps, ws)
+    t = sorted(s.elapsed_time(e) for s, e in evs)
+    ms = statistics.median(t)
     del g
-    return {"ms_per_step": round(ms, 4), "value": round(flops / (ms * 1e-3) / 1e12 * ws, 2),
-            "unit": "TFLOP/s"}
+    return {"ms_per_step": round(ms, 4), "value": round(flops / (ms * 1e-3) / 1e12, 2),
+            "unit": "TFLOP/s", "replays": replays, "statistic": "median",
+            "min_ms": round(t[0], 4), "max_ms": round(t[-1], 4)}
 
 
-def run_e2e(w, inp, o, step, steps, ws, flops):
+def run_e2e(w, inp, o, step, steps, flops):
     """Same metric through the public API from pinned host buffers.  Every
-    step copies its inputs host->device and reads its result back to the
+    step copies its inputs host->device and reads its results back to the
     host, as an input pipeline would: the inputs of step i+1 are copied on
-    one stream while step i computes, and step i's result is read back on
-    another, with two device input sets and two result buffers.  The timed
-    region runs from the first input copy to the last result read."""
+    one stream while step i computes, and step i's results are read back on
+    another, with two device input sets and two result sets.  A training
+    step's results are the input gradient and both weight gradients; a
+    forward step's is the layer output.  The timed region runs from the
+    first input copy to the last result read."""
     import torch
     if w.routing == "identity":
         names_in = ["x_perm", "dy_perm", "offsets"]
-        out_name = "dx_perm"
+        out_names = ["dx_perm", "dW1", "dW2"]
     elif w.mxfp8 and not w.backward:
         names_in = ["x", "topk_idx", "probs"]
-        out_name = "out"
+        out_names = ["out"]
     else:
         names_in = ["x", "dO", "topk_idx", "probs"]
-        out_name = "dx"
+        out_names = ["dx", "dW1", "dW2", "dprobs"]
     host = {nm: torch.empty(inp[nm].shape, dtype=inp[nm].dtype, pin_memory=True)
             for nm in names_in}
     for nm in names_in:
         host[nm].copy_(inp[nm])
-    out_host = torch.empty(o[out_name].shape, dtype=o[out_name].dtype, pin_memory=True)
+    out_host = {nm: torch.empty(o[nm].shape, dtype=o[nm].dtype, pin_memory=True)
+                for nm in out_names}
     h2d = sum(host[nm].numel() * host[nm].element_size() for nm in names_in)
-    d2h = out_host.numel() * out_host.element_size()
+    d2h = sum(t.numel() * t.element_size() for t in out_host.values())
     # two input sets / result buffers; weights and intermediates shared
     sets, outs, steps_fn = [], [], []
     for i in range(2):
@@ -871,7 +877,8 @@ def run_e2e(w, inp, o, step, steps, ws, flops):
                 ins[nm] = torch.empty_like(inp[nm])
         oo = dict(o)
         if i == 1:
-            oo[out_name] = torch.empty_like(o[out_name])
+            for nm in out_names:
+                oo[nm] = torch.empty_like(o[nm])
         sets.append(ins)
         outs.append(oo)
         steps_fn.append(make_step(w, ins, oo))
@@ -903,12 +910,12 @@ def run_e2e(w, inp, o, step, steps, ws, flops):
             freed[k].record(comp)
             with torch.cuda.stream(down):
                 down.wait_event(freed[k])
-                out_host.copy_(outs[k][out_name], non_blocking=True)
+                for nm in out_names:
+                    out_host[nm].copy_(outs[k][nm], non_blocking=True)
                 read[k].record(down)
 
     run(2)
     torch.cuda.synchronize()
-    barrier(ws)
     s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     s.record(up)
     run(steps)
@@ -916,10 +923,11 @@ def run_e2e(w, inp, o, step, steps, ws, flops):
     down.wait_stream(up)
     e.record(down)
     torch.cuda.synchronize()
-    ms = max_over_ranks(s.elapsed_time(e) / steps, ws)
-    return {"value": round(flops / (ms * 1e-3) / 1e12 * ws, 2), "unit": "TFLOP/s",
+    ms = s.elapsed_time(e) / steps
+    return {"value": round(flops / (ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
             "ms_per_step": round(ms, 4), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-            "pipelined": "inputs of step i+1 copied during step i; two input sets"}
+            "read_back": out_names,
+            "pipelined": "inputs of step i+1 copied during step i; two input and result sets"}
 
 
 if __name__ == "__main__":

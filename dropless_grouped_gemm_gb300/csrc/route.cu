@@ -16,7 +16,9 @@
 //   3. route_rank:  chunk c again, in pair order: stable rank of each pair
 //                   among the pairs of its expert -> row_of_pair, pair_of_row
 // pair_of_row is first filled with -1 (route_fill).
+#include <cuda.h>
 #include <cuda_runtime.h>
+#include <cudaTypedefs.h>
 
 #include <mutex>
 
@@ -346,28 +348,68 @@ cudaError_t launch_route(const int32_t* topk_idx, int T, int k, int E, int align
 // the library's own device image.  Every GPU that loads libmoe holds it
 // (kRouteScratchWords * 4 bytes) until the process exits.  Host code must not
 // pass the array's name to a kernel (on the host it is only a stand-in);
-// the device address comes from cudaGetSymbolAddress, looked up once per
-// device with that device current.
+// the device address comes from cudaGetSymbolAddress, with the device
+// current.  The address belongs to the module as loaded in one CUDA context,
+// so it is cached per context: keyed by the context's unique ID
+// (cuCtxGetId), which a context created later - e.g. the primary context
+// that follows cudaDeviceReset - never reuses.
 static __device__ __align__(256) int32_t g_route_scratch[kRouteScratchWords];
 
 namespace {
 std::mutex g_scratch_mu;
-void* g_scratch_ptr[64] = {nullptr};
+struct ScratchEntry {
+  unsigned long long ctx_id;
+  void* ptr;
+};
+constexpr int kScratchCache = 64;
+ScratchEntry g_scratch_cache[kScratchCache] = {};
+int g_scratch_next = 0;
+
+// unique ID of the calling thread's current context (0 if none or unknown)
+unsigned long long current_context_id() {
+  static PFN_cuCtxGetCurrent_v4000 get_cur = nullptr;
+  static PFN_cuCtxGetId_v12000 get_id = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 4000, cudaEnableDefault, &q) ==
+            cudaSuccess && q == cudaDriverEntryPointSuccess)
+      get_cur = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(p);
+    p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess && q == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<PFN_cuCtxGetId_v12000>(p);
+  });
+  if (!get_cur || !get_id) return 0;
+  CUcontext ctx = nullptr;
+  if (get_cur(&ctx) != CUDA_SUCCESS || ctx == nullptr) return 0;
+  unsigned long long id = 0;
+  if (get_id(ctx, &id) != CUDA_SUCCESS) return 0;
+  return id;
+}
 }  // namespace
 
 cudaError_t route_scratch_address(void** out) {
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   std::lock_guard<std::mutex> lock(g_scratch_mu);
-  if (g_scratch_ptr[dev] == nullptr) {
-    void* p = nullptr;
-    e = cudaGetSymbolAddress(&p, g_route_scratch);
-    if (e != cudaSuccess) return e;
-    g_scratch_ptr[dev] = p;
+  unsigned long long id = current_context_id();
+  if (id != 0)
+    for (const ScratchEntry& c : g_scratch_cache)
+      if (c.ctx_id == id) {
+        *out = c.ptr;
+        return cudaSuccess;
+      }
+  // first call in this context (the lookup also brings up the device's
+  // primary context when no context is current yet)
+  void* p = nullptr;
+  const cudaError_t e = cudaGetSymbolAddress(&p, g_route_scratch);
+  if (e != cudaSuccess) return e;
+  id = current_context_id();
+  if (id != 0) {
+    g_scratch_cache[g_scratch_next] = {id, p};
+    g_scratch_next = (g_scratch_next + 1) % kScratchCache;
   }
-  *out = g_scratch_ptr[dev];
+  *out = p;
   return cudaSuccess;
 }
 

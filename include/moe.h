@@ -222,24 +222,24 @@ int moe_route_logits(const float* logits, int T, int E, int k, int align, int M_
 
 /*
  * moe_route_offsets_noalloc - moe_route_offsets for callers that cannot
- * allocate device memory.  It computes the same routing layout ([TE] "MoE
- * 학습이 밀집 모델보다 어려운 이유: 래그드 텐서": per-expert counts and the
- * ragged, expert-major row layout kept on the device).  The pages have no
- * allocation-free variant; this exists for
- * code that runs where cudaMalloc is off limits: inside a CUDA-graph
- * capture that must not grow a memory pool, under an allocator-free
- * runtime, or in a plugin whose host framework owns every allocation and
- * offers no scratch.  Same arguments and results as moe_route_offsets,
- * minus the workspace: the scratch is a fixed 1 MiB array inside the
- * library's device image (every GPU that loads the library holds it until
- * the process exits).
+ * allocate device memory.  The paper has no counterpart: this entry point
+ * exists only for code that runs where cudaMalloc is off limits - inside a
+ * CUDA-graph capture that must not grow a memory pool, under an
+ * allocator-free runtime, or in a plugin whose host framework owns every
+ * allocation and offers no scratch.  Same arguments and results as
+ * moe_route_offsets, minus the workspace: the scratch is a fixed 1 MiB array
+ * inside the library's device image (every GPU that loads the library holds
+ * it until the process exits).
  *   - Limit: moe_route_workspace_size(T, k, E) =
  *     (ceil(T*k / 4096) + 1) * E * 4 bytes must be <= 1 MiB (E = 1024:
  *     T*k <= 1,044,480 pairs; E = 256: T*k <= 4,190,208); larger sizes
  *     return MOE_E_WORKSPACE and enqueue nothing.
- *   - The first call on each device looks the array's device address up
- *     (cudaGetSymbolAddress, with that device current) and caches it; make
- *     that first call before any stream capture.
+ *   - The array's device address is looked up (cudaGetSymbolAddress, with
+ *     the device current) on the first call in each CUDA context and cached
+ *     under that context's unique ID.  A new context - a non-primary one,
+ *     or the primary context that follows cudaDeviceReset - gets its own
+ *     lookup on its first call.  Make that first call before any stream
+ *     capture.
  *   - No cudaMalloc, cudaFree or allocating library call is made.  Nothing
  *     in the scratch needs to start at zero (each call writes every word it
  *     reads), but all calls share it: calls whose kernels can overlap on the

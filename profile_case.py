@@ -1,6 +1,6 @@
 """Run one seeded case of the path a fixed number of times (for profilers).
 
-    python -m dropless_grouped_gemm_gb300.profile_case --workload NAME
+    python profile_case.py --workload NAME
         [--rows-per-expert R | --tokens T] [--what fwd|bwd|step] [--reps N]
 
 Inputs come from the ``workloads`` generator; shapes other than the row /
@@ -14,7 +14,7 @@ import argparse
 import os
 import sys
 
-ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+ROOT = os.path.dirname(os.path.abspath(__file__))
 if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
