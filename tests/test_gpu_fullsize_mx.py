@@ -7,9 +7,14 @@ The GPU runs one step of the bench's MXFP8 training workload.  The oracle
   * sampled rows of a hot expert, a small one and the smallest: A and the
     block-scaled FC2 output Y; dH (block-scaled FC2-dgrad + dAct) and dX
     (block-scaled FC1-dgrad);
-  * the whole MXFP8 weight gradients of a small expert (element-wise on the
-    columns whose quantised operand both sides derive from bit-identical
-    bf16 values, in aggregate on all), and zeros for experts with no rows.
+  * the fused FC1 epilogue's MXFP8 codes and scales (row-wise and the
+    group-aware transposed copy) of a hot, a median and the smallest
+    expert, bit for bit against the OCP MX quantiser applied to the GPU's
+    own bf16 A, on every block;
+  * the whole MXFP8 weight gradients of a small expert: element-wise
+    against the oracle's block-scaled weight gradient of the GPU's own bf16
+    operands (stage-wise), and in aggregate against the oracle's
+    independent chain from x; zeros for experts with no rows.
 Rows of an expert include its pad rows (zeros) up to the 32-row boundary:
 the group-aware blocks of the weight gradients see them."""
 import numpy as np
@@ -21,6 +26,7 @@ import oracle as O
 from oracle import mx as X
 import workloads as WL
 from _helpers import assert_rms_close, f64
+from test_gpu_mx import decode_a_scales
 
 pytestmark = [pytest.mark.gpu, pytest.mark.slow]
 
@@ -103,20 +109,46 @@ def test_mx_rows_forward_and_data_gradients(run):
         assert_rms_close(f64(o["dx_perm"][r]), dX, f"MX e{e} dX")
 
 
-def _agree_cols(gpu, ref):
-    """Columns whose bf16 values agree bit for bit on every row."""
-    return np.where((O.bf16_bits(gpu) == O.bf16_bits(ref)).all(axis=0))[0]
+def test_mx_fc1_codes_and_scales_bit_exact(run):
+    """The FC1 epilogue's E4M3 codes and E8M0 scales of A, row-wise (1x32
+    along n, MMA-tiled scales) and transposed (32x1 along the rows of one
+    expert), equal the OCP MX quantiser applied to the GPU's own bf16 A on
+    every block of three experts: the largest, a median one and the
+    smallest (pad rows up to the 32-row boundary included)."""
+    w, o, ro, probs = run
+    counts, off = ro["counts"], ro["offsets"]
+    mx = o["mx"]
+    n, Mc = w.n, w.M_cap
+    nonempty = [int(e) for e in np.argsort(counts) if counts[e] > 0]
+    gs_all = decode_a_scales(mx["a_s"], off, Mc, n)
+    for e in [int(np.argmax(counts)), nonempty[len(nonempty) // 2], nonempty[0]]:
+        r0, r1 = int(off[e]), int(off[e + 1])
+        assert r0 % 32 == 0 and r1 % 32 == 0 and r1 > r0
+        ga = f64(o["a"][r0:r1])
+        qo, so = X.mx_quantize_rows(ga)
+        gq = mx["a_q"][r0:r1].cpu().numpy()
+        assert np.array_equal(gq, qo), (e, "row-wise codes",
+                                        int((gq != qo).sum()), "of", qo.size)
+        assert np.array_equal(gs_all[r0:r1], so), (e, "row-wise scales")
+        qTo, sTo = X.mx_quantize_cols(ga, np.array([0, r1 - r0]))
+        gqT = mx["a_qT"][:, r0:r1].cpu().numpy()
+        gsT = mx["a_sT"][:, r0 // 32:r1 // 32].cpu().numpy()
+        assert np.array_equal(gqT, qTo), (e, "transposed codes",
+                                          int((gqT != qTo).sum()), "of", qTo.size)
+        assert np.array_equal(gsT, sTo), (e, "transposed scales")
 
 
 def test_mx_weight_gradients_small_expert_and_empty(run):
-    """Whole dW1/dW2 of a small expert.  Each side quantises the operands it
-    computed itself (A from its FC1, dH from its FC2-dgrad, dY from the
-    scaled permute); a one-step bf16
-    difference can flip an E4M3 code or a block scale, and with a few dozen
-    rows a flip shows in the sum.  So the element-wise tolerance applies on
-    the columns whose bf16 operand agrees bit for bit on both sides (the
-    quantisers then produce the same codes), and every entry must meet the
-    aggregate bound: relative Frobenius error <= 2e-2."""
+    """Whole dW1/dW2 of a small expert, two ways.
+      * Stage-wise, element-wise: the oracle's block-scaled weight gradient
+        (group-aware transposed copies, exact products, fp64 sums) of the
+        GPU's own bf16 operands - A from its FC1, dY from its scaled
+        permute, dH from its FC2-dgrad, x from the generator - against every
+        entry of the GPU's dW within the bf16 tolerance.
+      * The independent chain: the oracle's MXFP8 backward from x, where
+        each side quantises operands it computed itself (a one-step bf16
+        difference can flip an E4M3 code, which shows in a sum over a few
+        dozen rows): relative Frobenius error <= 2e-2 over the whole dW."""
     w, o, ro, probs = run
     counts, off = ro["counts"], ro["offsets"]
     e = int([e for e in np.argsort(counts) if counts[e] > 40][0])   # two 32-row blocks or more
@@ -131,18 +163,12 @@ def test_mx_weight_gradients_small_expert_and_empty(run):
     for name, got, want in (("dW2", got2, ref["dW2"][0]), ("dW1", got1, ref["dW1"][0])):
         rel = np.linalg.norm(got - want) / np.linalg.norm(want)
         assert rel <= 2e-2, (f"MX {name}[{e}] relative error", rel)
-    # dW2 = A^T dY: rows of dW2 follow A's columns, columns follow dY's (the
-    # scaled permute rounds an fp32 product, the oracle an exact one: they
-    # may differ by one step at a few elements)
-    ia = _agree_cols(f64(o["a"][r]), A)
-    jd = _agree_cols(f64(o["dy_perm"][r]), dy)
-    assert len(ia) >= A.shape[1] // 2 and len(jd) >= dy.shape[1] // 2, (len(ia), len(jd))
-    assert_rms_close(got2[np.ix_(ia, jd)], ref["dW2"][0][np.ix_(ia, jd)],
-                     f"MX dW2[{e}] on {len(ia)} x {len(jd)} agreeing rows x columns")
-    # dW1 = x^T dH: columns of dW1 follow dH's columns (x is the generator's on both sides)
-    jh = _agree_cols(f64(o["dh"][r]), ref["dH"][:len(rows)])
-    assert len(jh) >= ref["dH"].shape[1] // 2, len(jh)
-    assert_rms_close(got1[:, jh], ref["dW1"][0][:, jh], f"MX dW1[{e}] on {len(jh)} agreeing columns")
+    # stage-wise: the oracle's block-scaled wgrad on the GPU's own operands
+    ga, gdy, gdh = f64(o["a"][r]), f64(o["dy_perm"][r]), f64(o["dh"][r])
+    want2 = X.mx_wgrad(*X.mx_quantize_cols(ga, o1), *X.mx_quantize_cols(gdy, o1), o1)[0]
+    want1 = X.mx_wgrad(*X.mx_quantize_cols(x, o1), *X.mx_quantize_cols(gdh, o1), o1)[0]
+    assert_rms_close(got2, want2, f"MX dW2[{e}] from the GPU's own A, dY")
+    assert_rms_close(got1, want1, f"MX dW1[{e}] from the GPU's own dH")
     for e in [int(e) for e in range(w.E) if counts[e] == 0][:3]:
         assert float(o["dW1"][e].abs().max()) == 0.0
         assert float(o["dW2"][e].abs().max()) == 0.0

@@ -3,12 +3,10 @@
 * The weight quantiser and the standalone group-aware quantiser run on
   generator inputs (plus planted edge blocks): codes and scales must be
   bit-exact.
-* The fused FC1 epilogue quantises its own bf16 A.  The oracle computes A
-  independently (float64, rounded to bf16 once); the two agree except for
-  one-step rounding differences.  Where a 32-value block of A agrees bit for
-  bit, the quantisation decision is taken on the same input by both sides,
-  so codes and scale must be bit-exact there; the test requires most blocks
-  to qualify and checks the rest through the tolerance on the decoded values.
+* The fused FC1 epilogue quantises its own bf16 A.  Its codes and scales,
+  row-wise and transposed, must equal the OCP MX quantiser applied to that
+  bf16 A bit for bit on every block.  Separately, A itself is compared with
+  the oracle's independently computed A within the bf16 tolerance.
 * The block-scaled FC2 output is compared with the oracle's MX FC2 on the
   oracle's own quantised A and W2, within the bf16 tolerance."""
 import numpy as np
@@ -193,17 +191,17 @@ def _mx_case(act, E=4, d=256, n=256, counts=(96, 0, 160, 32), seed=23):
     return off, M_cap, x, W1, W2
 
 
-def _check_blocks(gpu_a, ref_a, gpu_q, gpu_s, rows_axis):
-    """Bit-exact codes/scales on blocks whose bf16 input agrees.  Blocks are
-    32 consecutive entries along the last axis; returns the compared count."""
+def _check_blocks(gpu_a, gpu_q, gpu_s, what):
+    """Codes and scales bit-exact on every block against the OCP MX
+    quantiser applied to the GPU's own bf16 A (the quantiser's input is the
+    bf16-rounded A).  Blocks are 32 consecutive entries along the last
+    axis."""
     ga = gpu_a.reshape(gpu_a.shape[0], -1, 32)
-    ra = ref_a.reshape(ref_a.shape[0], -1, 32)
-    same = (ga == ra).all(axis=2)
     qo, so = O.mx_quantize_blocks(ga)
     gq = gpu_q.reshape(gpu_q.shape[0], -1, 32)
-    assert np.array_equal(gq[same], qo[same]), rows_axis
-    assert np.array_equal(gpu_s[same], so[same]), rows_axis
-    return int(same.sum()), same.size
+    bad = ~((gq == qo).all(axis=2) & (gpu_s == so))
+    assert not bad.any(), (what, "blocks differing", int(bad.sum()), "of", bad.size,
+                           "first at", tuple(int(v) for v in np.argwhere(bad)[0]))
 
 
 # (d, n, counts): the second shape gives an expert three 128-row blocks (the
@@ -230,13 +228,12 @@ def test_fused_fc1_mx_epilogue_and_block_scaled_fc2(act, shape):
     assert_rms_close(ga, A[:R], f"{act} A (bf16)")
     # row-wise codes / scales (MMA-tiled scales decoded)
     gs = decode_a_scales(buf["a_s"], off, M_cap, n)[:R]
-    done, total = _check_blocks(ga, A[:R], buf["a_q"].cpu().numpy()[:R], gs, "rows")
-    assert done >= 0.5 * total, (done, total)
-    # transposed copy: column blocks of 32 rows inside each expert
+    _check_blocks(ga, buf["a_q"].cpu().numpy()[:R], gs, "rows")
+    # transposed copy: column blocks of 32 rows inside each expert (offsets
+    # are multiples of 32, so the blocks of A^T's rows never cross experts)
     gT = buf["a_qT"].cpu().numpy()[:, :R]
     gsT = buf["a_sT"].cpu().numpy()[:, :R // 32]
-    done_t, total_t = _check_blocks(ga.T.copy(), A[:R].T.copy(), gT, gsT, "cols")
-    assert done_t >= 0.3 * total_t, (done_t, total_t)
+    _check_blocks(ga.T.copy(), gT, gsT, "cols")
     # decoded codes everywhere within the MX error of the oracle's A
     deq = O.mx_dequantize(buf["a_q"].cpu().numpy()[:R], gs.astype(np.uint8), axis_block=1)
     assert np.linalg.norm(deq - A[:R]) <= 0.05 * np.linalg.norm(A[:R])

@@ -7,8 +7,9 @@ vs the oracle's MXFP8 backward.
   on the same bf16 inputs, within the bf16 tolerance.  Both sides quantise
   dY, x, A and the weights identically (the quantisers are bit-exact); dH is
   quantised from each side's own bf16 dH, which may differ by one bf16 step
-  at a few elements, so dX and dW1 can differ by one E4M3 step there - far
-  inside the tolerance.
+  at a few elements, so dX and dW1 can differ by one E4M3 step there.  dW1
+  and dW2 are also compared element-wise with the oracle's block-scaled
+  weight gradient of the GPU's own bf16 operands (stage-wise).
 * Expert sizes cover several 128-row tiles, ragged last reduction steps
   (32/64/96 rows), empty experts and many small experts."""
 import numpy as np
@@ -173,25 +174,17 @@ def test_mx_bwd_accumulate_dw():
     assert torch.equal(dW1[1], old1[1]) and torch.equal(dW2[1], old2[1])
 
 
-def _check_dw1(got, want, dh_gpu, dh_ref, off, name):
-    """dW1_e = x_e^T dH_e, from the transposed MXFP8 copies.  x is the
-    generator's on both sides, but dH is each side's own FC2-dgrad output:
-    where they differ by one bf16 step, the quantisers can emit a different
-    E4M3 code or block scale, and with experts of 32-64 rows one such flip
-    moves an entry by more than 2e-2 RMS.  So the element-wise tolerance
-    applies to the columns of dW1_e whose dH column agrees bit for bit on
-    every row of the expert, and all of dW1 meets the relative Frobenius
-    bound 2e-2 (the same rule as the full-size MXFP8 test)."""
-    bits_g, bits_r = O.bf16_bits(np.nan_to_num(dh_gpu)), O.bf16_bits(np.nan_to_num(dh_ref))
-    mask = np.zeros(got.shape, dtype=bool)
-    for e in range(len(off) - 1):
-        r0, r1 = int(off[e]), int(off[e + 1])
-        agree = (bits_g[r0:r1] == bits_r[r0:r1]).all(axis=0)
-        mask[e][:, agree] = True
-    assert mask.mean() >= 0.5, (name, "dH columns agreeing", mask.mean())
-    assert_rms_close(got[mask], want[mask], f"{name} dW1 on agreeing dH columns")
-    rel = np.linalg.norm(got - want) / np.linalg.norm(want)
-    assert rel <= 2e-2, (f"{name} dW1 relative error", rel)
+def _stagewise_wgrads(x, dh_gpu, a, dy, off, R):
+    """The oracle's block-scaled weight gradients of the GPU's own bf16
+    operands: dW1 = x^T dH from the GPU's dH, dW2 = A^T dY (A, dY and x are
+    the generator's on both sides).  Rows past the experts are zeroed (they
+    are outside every block)."""
+    M = x.shape[0]
+    dh0 = np.zeros_like(dh_gpu)
+    dh0[:R] = dh_gpu[:R]
+    dW1 = X.mx_wgrad(*X.mx_quantize_cols(x, off, M), *X.mx_quantize_cols(dh0, off, M), off)
+    dW2 = X.mx_wgrad(*X.mx_quantize_cols(a, off, M), *X.mx_quantize_cols(dy, off, M), off)
+    return dW1, dW2
 
 
 @pytest.mark.parametrize("act", ["swiglu", "geglu", "srelu"])
@@ -204,7 +197,15 @@ def test_mx_bwd_matches_oracle(name, counts, d, n, act):
     assert_rms_close(f64(dh)[:R], ref["dH"][:R], f"{name}/{act} dH")
     assert_rms_close(f64(dx)[:R], ref["dX"][:R], f"{name}/{act} dX")
     assert_rms_close(f64(dW2), ref["dW2"], f"{name}/{act} dW2")
-    _check_dw1(f64(dW1), ref["dW1"], f64(dh), ref["dH"], off, f"{name}/{act}")
+    # dW1: element-wise against the oracle's block-scaled wgrad of the GPU's
+    # own dH (stage-wise); against the independent chain, whose dH may
+    # differ by one bf16 step at a few elements and so flip an E4M3 code in
+    # a 32-row block, in aggregate
+    s1, s2 = _stagewise_wgrads(f64(x), f64(dh), f64(A), f64(dy), off, R)
+    assert_rms_close(f64(dW1), s1, f"{name}/{act} dW1 (stage-wise)")
+    assert_rms_close(f64(dW2), s2, f"{name}/{act} dW2 (stage-wise)")
+    rel = np.linalg.norm(f64(dW1) - ref["dW1"]) / np.linalg.norm(ref["dW1"])
+    assert rel <= 2e-2, (f"{name}/{act} dW1 relative error vs the independent chain", rel)
     for e in range(len(counts)):
         if counts[e] == 0:
             assert float(dW1[e].abs().max()) == 0 and float(dW2[e].abs().max()) == 0
