@@ -171,13 +171,17 @@ def route_offsets(topk_idx, E: int, align: int = 1, M_cap: int | None = None):
                 pair_of_row=pair_of_row, true_total=true_total, err=err)
 
 
-def permute(x, pair_of_row, k: int, scale=None, round_bf16: bool = True):
+def permute(x, pair_of_row, k: int, scale=None, round_bf16: bool = True,
+            round_out: bool = True):
     """Expert-major gather ([TE] "최적화 2: NCCL EP": dispatch = permute the
     token rows; [Sonic] "Gather Fusion": gather collects each expert's rows).
 
     ``x_perm[r] = x[pair_of_row[r] // k]`` (optionally times
     ``scale[pair_of_row[r]]``, the backward use with router probabilities);
-    rows with ``pair_of_row[r] == -1`` are zero."""
+    rows with ``pair_of_row[r] == -1`` are zero.  The scaled product is
+    rounded to bf16 where it is stored; ``round_out=False`` returns it
+    before that rounding (the exact value a stored result is compared
+    with)."""
     x = np.asarray(x, dtype=np.float64)
     d = x.shape[1]
     M_cap = len(pair_of_row)
@@ -190,14 +194,17 @@ def permute(x, pair_of_row, k: int, scale=None, round_bf16: bool = True):
         if scale is not None:
             row = np.float64(np.asarray(scale).reshape(-1)[p]) * row
         out[r] = row
-    return bf16_round(out) if (round_bf16 and scale is not None) else out
+    return bf16_round(out) if (round_bf16 and round_out and scale is not None) else out
 
 
-def unpermute(y_perm, row_of_pair, T: int, k: int, probs=None, round_bf16=True):
+def unpermute(y_perm, row_of_pair, T: int, k: int, probs=None, round_bf16=True,
+              round_out: bool = True):
     """Combine ([TE] "최적화 2: NCCL EP": results return to token order and the
     per-expert outputs are accumulated per token; [Sonic] "scatter" +
     "expert aggregation").  ``out[t] = sum_j probs[t,j] * y_perm[row(t,j)]``,
-    with weight 1 when ``probs`` is None; skipped pairs contribute 0."""
+    with weight 1 when ``probs`` is None; skipped pairs contribute 0.  The
+    sum is rounded to bf16 where it is stored; ``round_out=False`` returns it
+    before that rounding."""
     y_perm = np.asarray(y_perm, dtype=np.float64)
     d = y_perm.shape[1] if y_perm.ndim == 2 else 0
     out = np.zeros((T, d), dtype=np.float64)
@@ -208,7 +215,7 @@ def unpermute(y_perm, row_of_pair, T: int, k: int, probs=None, round_bf16=True):
                 continue
             w = 1.0 if probs is None else float(np.asarray(probs)[t, j])
             out[t] += w * y_perm[r]
-    return bf16_round(out) if round_bf16 else out
+    return bf16_round(out) if (round_bf16 and round_out) else out
 
 
 def router_grad(dO, y_perm, row_of_pair, T: int, k: int):
@@ -324,14 +331,18 @@ def _rb(v, on):
     return bf16_round(v) if on else np.asarray(v, dtype=np.float64)
 
 
-def grouped_mlp_fwd(x_perm, offsets, W1, W2, act: str, round_bf16: bool = True):
+def grouped_mlp_fwd(x_perm, offsets, W1, W2, act: str, round_bf16: bool = True,
+                    round_out: bool = True):
     """Per expert e with rows R_e = [offsets[e], offsets[e+1]):
     H_e = X_e W1_e, A_e = act(H_e), Y_e = A_e W2_e.
 
     Rounding points mirror what a bf16 implementation stores: H (saved for
     backward) and A are rounded to bf16, A is computed from the unrounded H,
     FC2 reads the rounded A, Y is rounded.  Rows outside every expert are
-    NaN (undefined).
+    NaN (undefined).  With ``round_out=False`` the returned H, A and Y are
+    the values just before their storage rounding, while every step still
+    consumes the rounded values (a stored bf16 result is then compared with
+    the exact value it rounds).
     Follows [TE] "최적화 1: grouped GEMM, 전문가마다 다른 토큰 수를 커널 하나로" and [CuTe] "핵심 아이디어 / 구조 / 동작 방식"."""
     x_perm = np.asarray(x_perm, dtype=np.float64)
     W1 = np.asarray(W1, dtype=np.float64)
@@ -347,19 +358,21 @@ def grouped_mlp_fwd(x_perm, offsets, W1, W2, act: str, round_bf16: bool = True):
         if r1 <= r0:
             continue
         h = x_perm[r0:r1] @ W1[e]
-        a = _rb(act_forward(h, act), round_bf16)
-        H[r0:r1] = _rb(h, round_bf16)
-        A[r0:r1] = a
-        Y[r0:r1] = _rb(a @ W2[e], round_bf16)
+        a_exact = act_forward(h, act)
+        a = _rb(a_exact, round_bf16)
+        H[r0:r1] = _rb(h, round_bf16 and round_out)
+        A[r0:r1] = a if round_out else a_exact
+        Y[r0:r1] = _rb(a @ W2[e], round_bf16 and round_out)
     return H, A, Y
 
 
-def grouped_gemm(a, offsets, B, b_layout: str = "kn", round_bf16: bool = True):
+def grouped_gemm(a, offsets, B, b_layout: str = "kn", round_bf16: bool = True,
+                 round_out: bool = True):
     """Plain grouped GEMM ([TE] "최적화 1: grouped GEMM": one call over the
     experts' ragged row groups): out_e = A_e B_e for the rows of expert e,
     with B [E, K, N] ("kn") or B stored transposed as [E, N, K] ("nk", then
     out_e = A_e B_e^T).  Rows outside every expert are NaN (undefined); the
-    result is rounded to bf16 once."""
+    result is rounded to bf16 once (not with ``round_out=False``)."""
     a = np.asarray(a, dtype=np.float64)
     B = np.asarray(B, dtype=np.float64)
     if b_layout == "nk":
@@ -371,17 +384,19 @@ def grouped_gemm(a, offsets, B, b_layout: str = "kn", round_bf16: bool = True):
     for e in range(E):
         r0, r1 = int(offsets[e]), int(offsets[e + 1])
         if r1 > r0:
-            out[r0:r1] = _rb(a[r0:r1] @ B[e], round_bf16)
+            out[r0:r1] = _rb(a[r0:r1] @ B[e], round_bf16 and round_out)
     return out
 
 
 def grouped_mlp_bwd(x_perm, H, A, dY, offsets, W1, W2, act: str,
-                    round_bf16: bool = True):
+                    round_bf16: bool = True, round_out: bool = True):
     """Backward of ``grouped_mlp_fwd`` per expert:
     dA_e = dY_e W2_e^T, dH_e = act'(H_e; dA_e), dW2_e = A_e^T dY_e,
     dX_e = dH_e W1_e^T, dW1_e = X_e^T dH_e.  An expert with no rows gets
     dW1_e = dW2_e = 0.  dH is rounded to bf16 before it feeds dX and dW1
-    (a bf16 implementation stores it).
+    (a bf16 implementation stores it).  With ``round_out=False`` the returned
+    dH, dX, dW1, dW2 are the values just before their storage rounding;
+    dX and dW1 are still computed from the rounded dH.
     Follows [CuTe] "무엇을 해결하려는가" (GroupGemm + dActivation) and [TE] "최적화 1: grouped GEMM, 전문가마다 다른
     토큰 수를 커널 하나로"."""
     x_perm = np.asarray(x_perm, dtype=np.float64)
@@ -402,16 +417,18 @@ def grouped_mlp_bwd(x_perm, H, A, dY, offsets, W1, W2, act: str,
         if r1 <= r0:
             continue
         dA = dY[r0:r1] @ W2[e].T
-        dh = _rb(act_backward(H[r0:r1], dA, act), round_bf16)
-        dH[r0:r1] = dh
+        dh_exact = act_backward(H[r0:r1], dA, act)
+        dh = _rb(dh_exact, round_bf16)
+        dH[r0:r1] = dh if round_out else dh_exact
         dW2[e] = A[r0:r1].T @ dY[r0:r1]
-        dX[r0:r1] = _rb(dh @ W1[e].T, round_bf16)
+        dX[r0:r1] = _rb(dh @ W1[e].T, round_bf16 and round_out)
         dW1[e] = x_perm[r0:r1].T @ dh
-    return dH, dX, _rb(dW1, round_bf16), _rb(dW2, round_bf16)
+    ro = round_bf16 and round_out
+    return dH, dX, _rb(dW1, ro), _rb(dW2, ro)
 
 
 def grouped_mlp_bwd_routed(x_perm, H, dO_perm, row_prob, offsets, W1, W2, act: str,
-                           round_bf16: bool = True):
+                           round_bf16: bool = True, round_out: bool = True):
     """Backward with the router gradient taken inside the expert MLP
     ([Sonic] "역전파 계산 그래프 재작성하기": dS_{t,e} = <dO_t, Y_{e,t}> =
     <dO_t W2_e^T, A_e>, so Y need not be kept; A is recomputed from H, and
@@ -427,7 +444,9 @@ def grouped_mlp_bwd_routed(x_perm, H, dO_perm, row_prob, offsets, W1, W2, act: s
       A'   = p_r A_r                          (rounded to bf16)
       dW2_e = A'_e^T dO_e,  dX_e = dH_e W1_e^T,  dW1_e = X_e^T dH_e.
     Returns dH, dX, dW1, dW2, A', dS (float64 [M], NaN outside every
-    expert)."""
+    expert).  With ``round_out=False`` the returned dH, dX, dW1, dW2 and A'
+    are the values just before their storage rounding; later steps still
+    consume the rounded dH and A'."""
     x_perm = np.asarray(x_perm, dtype=np.float64)
     H = np.asarray(H, dtype=np.float64)
     dO = np.asarray(dO_perm, dtype=np.float64)
@@ -451,14 +470,16 @@ def grouped_mlp_bwd_routed(x_perm, H, dO_perm, row_prob, offsets, W1, W2, act: s
         dAp = dO[r0:r1] @ W2[e].T
         A = act_forward(H[r0:r1], act)
         dS[r0:r1] = (dAp * A).sum(axis=1)
-        dh = _rb(act_backward(H[r0:r1], pr * dAp, act), round_bf16)
-        dH[r0:r1] = dh
+        dh_exact = act_backward(H[r0:r1], pr * dAp, act)
+        dh = _rb(dh_exact, round_bf16)
+        dH[r0:r1] = dh if round_out else dh_exact
         ap = _rb(pr * A, round_bf16)
-        Ap[r0:r1] = ap
+        Ap[r0:r1] = ap if round_out else pr * A
         dW2[e] = ap.T @ dO[r0:r1]
-        dX[r0:r1] = _rb(dh @ W1[e].T, round_bf16)
+        dX[r0:r1] = _rb(dh @ W1[e].T, round_bf16 and round_out)
         dW1[e] = x_perm[r0:r1].T @ dh
-    return dH, dX, _rb(dW1, round_bf16), _rb(dW2, round_bf16), Ap, dS
+    ro = round_bf16 and round_out
+    return dH, dX, _rb(dW1, ro), _rb(dW2, ro), Ap, dS
 
 
 # ---------------------------------------------------------------------------
@@ -511,7 +532,7 @@ def amax_rht_transposed(G, offsets) -> float:
 # sampled-row helpers for full-size parity checks (same arithmetic as above,
 # restricted to selected rows of one expert and selected output columns)
 
-def fc1_rows(x_rows, W1_e, act: str, cols=None):
+def fc1_rows(x_rows, W1_e, act: str, cols=None, round_out: bool = True):
     """(H, A) of the given rows of one expert; ``cols`` selects A columns
     (and the matching H column pairs when gated).
     The arithmetic of grouped_mlp_fwd on selected rows ([CuTe] "핵심 아이디어 / 구조 / 동작 방식")."""
@@ -521,10 +542,11 @@ def fc1_rows(x_rows, W1_e, act: str, cols=None):
     a = act_forward(h, act)
     if cols is not None:
         a = a[:, cols]
-    return bf16_round(h), bf16_round(a)
+    return (bf16_round(h), bf16_round(a)) if round_out else (h, a)
 
 
-def fc2_rows(a_rows, W2_e):
+def fc2_rows(a_rows, W2_e, round_out: bool = True):
     """The arithmetic of grouped_mlp_fwd's down-projection on selected rows ([TE] "최적화 1: grouped
     GEMM, 전문가마다 다른 토큰 수를 커널 하나로")."""
-    return bf16_round(np.asarray(a_rows, np.float64) @ np.asarray(W2_e, np.float64))
+    y = np.asarray(a_rows, np.float64) @ np.asarray(W2_e, np.float64)
+    return bf16_round(y) if round_out else y

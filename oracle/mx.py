@@ -250,7 +250,7 @@ def mx_wgrad(P_qT, P_sT, Q_qT, Q_sT, offsets):
     return dW
 
 
-def mx_grouped_mlp_bwd(x_perm, H, A, dY, offsets, W1, W2, act: str):
+def mx_grouped_mlp_bwd(x_perm, H, A, dY, offsets, W1, W2, act: str, round_out: bool = True):
     """MXFP8 backward of the grouped expert MLP (see the reading above).
 
     Inputs are the bf16 values of x_perm [M, d], H [M, n1], A [M, n],
@@ -264,8 +264,10 @@ def mx_grouped_mlp_bwd(x_perm, H, A, dY, offsets, W1, W2, act: str):
       5. dH -> row-wise blocks (along n1) and the transposed copy;
       6. dX = deq(dH) deq(W1_e)^T;
       7. x -> transposed copy;  dW1_e = deq(x^T) deq(dH^T).
-    Returns a dict with dH, dX, dW1, dW2 (bf16-rounded float64) and the
-    quantised intermediates (codes, scales) of steps 1, 2, 5 and 7.
+    Returns a dict with dH, dX, dW1, dW2 (bf16-rounded float64; with
+    ``round_out=False`` the values just before that rounding, while steps 5-7
+    still quantise the rounded dH) and the quantised intermediates (codes,
+    scales) of steps 1, 2, 5 and 7.
     Follows [TE] "다음 단계: NVFP4, GEMM 융합 양자화, A2A 오버랩" (GroupGemm + dActivation +
     Quantize/Transpose) and [CuTe] "무엇을 해결하려는가"."""
     from .moe import act_backward, bf16_round
@@ -286,20 +288,23 @@ def mx_grouped_mlp_bwd(x_perm, H, A, dY, offsets, W1, W2, act: str):
     w1_q, w1_s = w1_q.reshape(E, d, n1), w1_s.reshape(E, d, n1 // 32)
     dA = mx_dgrad(dy_q, dy_s, w2_q, w2_s, offsets)
     dH = np.full((M, n1), np.nan)
+    dH_exact = np.full((M, n1), np.nan)
     for e in range(E):
         r0, r1 = int(offsets[e]), int(offsets[e + 1])
         if r1 > r0:
-            dH[r0:r1] = bf16_round(act_backward(H[r0:r1], dA[r0:r1], act))
+            dH_exact[r0:r1] = act_backward(H[r0:r1], dA[r0:r1], act)
+            dH[r0:r1] = bf16_round(dH_exact[r0:r1])
+    rnd = bf16_round if round_out else (lambda v: v)
     a_qT, a_sT = mx_quantize_cols(A, offsets, M)
-    dW2 = bf16_round(mx_wgrad(a_qT, a_sT, dy_qT, dy_sT, offsets))
+    dW2 = rnd(mx_wgrad(a_qT, a_sT, dy_qT, dy_sT, offsets))
     used = int(offsets[-1])
     dH0 = np.where(np.isnan(dH), 0.0, dH)
     dh_q, dh_s = mx_quantize_rows(dH0)
     dh_qT, dh_sT = mx_quantize_cols(dH0, offsets, M)
-    dX = bf16_round(mx_dgrad(dh_q, dh_s, w1_q, w1_s, offsets))
+    dX = rnd(mx_dgrad(dh_q, dh_s, w1_q, w1_s, offsets))
     x_qT, x_sT = mx_quantize_cols(x_perm, offsets, M)
-    dW1 = bf16_round(mx_wgrad(x_qT, x_sT, dh_qT, dh_sT, offsets))
-    return {"dH": dH, "dX": dX, "dW1": dW1, "dW2": dW2,
+    dW1 = rnd(mx_wgrad(x_qT, x_sT, dh_qT, dh_sT, offsets))
+    return {"dH": dH if round_out else dH_exact, "dX": dX, "dW1": dW1, "dW2": dW2,
             "dy_q": dy_q[:used], "dy_s": dy_s[:used], "dy_qT": dy_qT, "dy_sT": dy_sT,
             "w2_q": w2_q, "w2_s": w2_s, "w1_q": w1_q, "w1_s": w1_s,
             "dh_q": dh_q[:used], "dh_s": dh_s[:used], "dh_qT": dh_qT, "dh_sT": dh_sT,

@@ -63,20 +63,21 @@ MUTANTS = {
     "dsrelu_drops_2": ("moe", "act_backward", "2.0 * np.maximum(h, 0.0) * dA",
                        "np.maximum(h, 0.0) * dA"),
     # ---- grouped MLP
-    "fwd_fc2_wrong_expert": ("moe", "grouped_mlp_fwd", "_rb(a @ W2[e], round_bf16)",
-                             "_rb(a @ W2[0], round_bf16)"),
+    "fwd_fc2_wrong_expert": ("moe", "grouped_mlp_fwd", "_rb(a @ W2[e], round_bf16 and round_out)",
+                             "_rb(a @ W2[0], round_bf16 and round_out)"),
     "fwd_drops_last_row_of_expert0": ("moe", "grouped_mlp_fwd",
                                       "r0, r1 = int(offsets[e]), int(offsets[e + 1])",
                                       "r0, r1 = int(offsets[e]), int(offsets[e + 1]) - (e == 0)"),
     "fwd_a_from_rounded_h_not_fc2_input": ("moe", "grouped_mlp_fwd",
-                                           "Y[r0:r1] = _rb(a @ W2[e], round_bf16)",
-                                           "Y[r0:r1] = _rb(act_forward(h, act) @ W2[e], round_bf16)"),
+                                           "Y[r0:r1] = _rb(a @ W2[e], round_bf16 and round_out)",
+                                           "Y[r0:r1] = _rb(act_forward(h, act) @ W2[e], "
+                                           "round_bf16 and round_out)"),
     "gemm_nk_not_transposed": ("moe", "grouped_gemm", "B = np.swapaxes(B, 1, 2)",
                                "B = B.reshape(B.shape[0], B.shape[2], B.shape[1])"),
     "bwd_dh_sign": ("moe", "grouped_mlp_bwd", "act_backward(H[r0:r1], dA, act)",
                     "act_backward(H[r0:r1], -dA, act)"),
-    "bwd_dx_wrong_expert": ("moe", "grouped_mlp_bwd", "_rb(dh @ W1[e].T, round_bf16)",
-                            "_rb(dh @ W1[e - 1].T, round_bf16)"),
+    "bwd_dx_wrong_expert": ("moe", "grouped_mlp_bwd", "_rb(dh @ W1[e].T, round_bf16 and round_out)",
+                            "_rb(dh @ W1[e - 1].T, round_bf16 and round_out)"),
     "bwd_dw2_transposed_product": ("moe", "grouped_mlp_bwd", "dW2[e] = A[r0:r1].T @ dY[r0:r1]",
                                    "dW2[e] = (dY[r0:r1].T @ A[r0:r1]).reshape(dW2[e].shape)"),
     "bwd_dw1_rows_shifted": ("moe", "grouped_mlp_bwd", "dW1[e] = x_perm[r0:r1].T @ dh",

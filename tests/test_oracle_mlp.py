@@ -323,3 +323,64 @@ def test_grouped_gemm_is_the_mlp_fc2():
     R = int(off[-1])
     assert np.array_equal(O.grouped_gemm(A, off, W2)[:R], Y[:R])
     assert np.array_equal(O.grouped_gemm(A, off, np.swapaxes(W2, 1, 2).copy(), "nk")[:R], Y[:R])
+
+
+@pytest.mark.parametrize("act", ACTS)
+def test_round_out_changes_only_the_final_rounding(act):
+    """round_out=False returns each stored result just before its bf16
+    rounding, with every step still fed the rounded values: rounding the
+    unrounded outputs gives the default outputs bit for bit, and they lie
+    within half a bf16 step (2^-8 relative) of them.  Also for the scaled
+    permute, the combine, the plain grouped GEMM, the sampled-row helpers
+    and the MXFP8 backward."""
+    from oracle import mx as X
+    rng = np.random.default_rng(7)
+    off, x, W1, W2 = _tiny(act, rng, rows=(64, 0, 32, 96), d=64, n=32)
+    x, W1, W2 = O.bf16_round(x), O.bf16_round(W1), O.bf16_round(W2)
+    M = int(off[-1])
+    dY = O.bf16_round(rng.standard_normal((M, x.shape[1])))
+    p = rng.uniform(0.1, 1.0, M)
+
+    def same(u, r):
+        u, r = np.asarray(u), np.asarray(r)
+        fin = np.isfinite(r)
+        assert np.array_equal(np.isfinite(u), fin)
+        assert np.array_equal(O.bf16_round(u[fin]), r[fin])
+        assert (np.abs(u[fin] - r[fin]) <= 2.0 ** -8 * np.abs(u[fin]) + 1e-300).all()
+        return not np.array_equal(u[fin], r[fin])
+
+    changed = []
+    fr, fu = O.grouped_mlp_fwd(x, off, W1, W2, act), O.grouped_mlp_fwd(x, off, W1, W2, act,
+                                                                       round_out=False)
+    changed += [same(u, r) for u, r in zip(fu, fr)]
+    H, A, _ = fr
+    br = O.grouped_mlp_bwd(x, H, A, dY, off, W1, W2, act)
+    bu = O.grouped_mlp_bwd(x, H, A, dY, off, W1, W2, act, round_out=False)
+    changed += [same(u, r) for u, r in zip(bu, br)]
+    rr = O.grouped_mlp_bwd_routed(x, H, dY, p, off, W1, W2, act)
+    ru = O.grouped_mlp_bwd_routed(x, H, dY, p, off, W1, W2, act, round_out=False)
+    changed += [same(u, r) for u, r in zip(ru[:5], rr[:5])]
+    assert np.array_equal(ru[5], rr[5], equal_nan=True)          # dS is float32-stored: unrounded
+    changed.append(same(O.grouped_gemm(A, off, W2, round_out=False), O.grouped_gemm(A, off, W2)))
+    h1, a1 = O.fc1_rows(x[:5], W1[0], act, round_out=False)
+    h0, a0 = O.fc1_rows(x[:5], W1[0], act)
+    changed += [same(h1, h0), same(a1, a0)]
+    changed.append(same(O.fc2_rows(a0, W2[0], round_out=False), O.fc2_rows(a0, W2[0])))
+    T, k = 40, 2
+    pair_of_row = np.concatenate([rng.permutation(T * k), -np.ones(8, np.int64)])
+    row_of_pair = np.argsort(pair_of_row[:T * k])
+    sc = rng.uniform(0.1, 1.0, T * k)
+    xt = O.bf16_round(rng.standard_normal((T, 16)))
+    changed.append(same(O.permute(xt, pair_of_row, k, scale=sc, round_out=False),
+                        O.permute(xt, pair_of_row, k, scale=sc)))
+    yp = O.bf16_round(rng.standard_normal((len(pair_of_row), 16)))
+    pr = sc.reshape(T, k)
+    changed.append(same(O.unpermute(yp, row_of_pair, T, k, probs=pr, round_out=False),
+                        O.unpermute(yp, row_of_pair, T, k, probs=pr)))
+    mr = X.mx_grouped_mlp_bwd(x, H, A, dY, off, W1, W2, act)
+    mu = X.mx_grouped_mlp_bwd(x, H, A, dY, off, W1, W2, act, round_out=False)
+    for key in ("dH", "dX", "dW1", "dW2"):
+        changed.append(same(mu[key], mr[key]))
+    for key in ("dh_q", "dh_s", "dh_qT", "dh_sT"):            # fed the rounded dH either way
+        assert np.array_equal(mu[key], mr[key])
+    assert all(changed), changed
