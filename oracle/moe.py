@@ -21,7 +21,7 @@ __all__ = [
     "act_forward", "act_backward", "phi", "dphi",
     "grouped_mlp_fwd", "grouped_mlp_bwd", "grouped_mlp_bwd_routed",
     "hadamard16", "amax", "amax_rht_transposed",
-    "fc1_rows", "fc2_rows", "grouped_gemm",
+    "fc1_rows", "fc2_rows", "grouped_gemm", "grouped_wgrad",
 ]
 
 ERR_BAD_EXPERT = 1
@@ -386,6 +386,24 @@ def grouped_gemm(a, offsets, B, b_layout: str = "kn", round_bf16: bool = True,
         if r1 > r0:
             out[r0:r1] = _rb(a[r0:r1] @ B[e], round_bf16 and round_out)
     return out
+
+
+def grouped_wgrad(P, Q, offsets, round_out: bool = True):
+    """Weight gradient of a grouped GEMM ([TE] "최적화 1: grouped GEMM": the
+    experts' ragged row groups): dW_e = P_e^T Q_e, the sum over the rows
+    of expert e, P [M, p], Q [M, q] -> [E, p, q]; an expert with no rows
+    gets 0.  The same product as grouped_mlp_bwd's dW1 (P = X, Q = dH) and
+    dW2 (P = A, Q = dY), for checking one weight-gradient GEMM on given
+    operands.  Rounded to bf16 once (not with ``round_out=False``)."""
+    P = np.asarray(P, dtype=np.float64)
+    Q = np.asarray(Q, dtype=np.float64)
+    E = len(offsets) - 1
+    dW = np.zeros((E, P.shape[1], Q.shape[1]))
+    for e in range(E):
+        r0, r1 = int(offsets[e]), int(offsets[e + 1])
+        if r1 > r0:
+            dW[e] = P[r0:r1].T @ Q[r0:r1]
+    return bf16_round(dW) if round_out else dW
 
 
 def grouped_mlp_bwd(x_perm, H, A, dY, offsets, W1, W2, act: str,

@@ -72,6 +72,10 @@ MUTANTS = {
                                            "Y[r0:r1] = _rb(a @ W2[e], round_bf16 and round_out)",
                                            "Y[r0:r1] = _rb(act_forward(h, act) @ W2[e], "
                                            "round_bf16 and round_out)"),
+    "wgrad_operands_swapped": ("moe", "grouped_wgrad", "dW[e] = P[r0:r1].T @ Q[r0:r1]",
+                               "dW[e] = (Q[r0:r1].T @ P[r0:r1]).reshape(dW[e].shape)"),
+    "wgrad_drops_first_row": ("moe", "grouped_wgrad", "dW[e] = P[r0:r1].T @ Q[r0:r1]",
+                              "dW[e] = P[r0 + 1:r1].T @ Q[r0 + 1:r1]"),
     "gemm_nk_not_transposed": ("moe", "grouped_gemm", "B = np.swapaxes(B, 1, 2)",
                                "B = B.reshape(B.shape[0], B.shape[2], B.shape[1])"),
     "bwd_dh_sign": ("moe", "grouped_mlp_bwd", "act_backward(H[r0:r1], dA, act)",

@@ -37,5 +37,5 @@ def test_bounded_wait_times_out_and_context_survives():
     _, _, y, e2 = M.grouped_mlp_fwd(x, cuda_i32(off), W1, W2, "swiglu")
     torch.cuda.synchronize()
     assert int(e2.item()) == 0
-    _, _, Y = O.grouped_mlp_fwd(f64(x), off, f64(W1), f64(W2), "swiglu")
+    _, _, Y = O.grouped_mlp_fwd(f64(x), off, f64(W1), f64(W2), "swiglu", round_out=False)
     assert_rms_close(f64(y)[:200], Y[:200], "Y after the timeout test")

@@ -46,6 +46,18 @@ def _token_rows(cols, key, std, toks):
     return f64(WL.normal_at(idx, key, std))
 
 
+def dy_exact(w, ro, probs, rows):
+    """p * dO of the given rows before the bf16 rounding (pad rows zero)."""
+    pairs = ro["pair_of_row"][rows]
+    real = pairs >= 0
+    out = np.zeros((len(rows), w.d))
+    if real.any():
+        dO = _token_rows(w.d, (w.cfg_id, WL.DO, 0), w.dy_std, pairs[real] // w.k)
+        out[real] = O.permute(dO, np.arange(int(real.sum())), 1,
+                              scale=probs.reshape(-1)[pairs[real]], round_out=False)
+    return out
+
+
 def _expert_inputs(w, ro, probs, rows):
     """x_perm and dy_perm rows (pad rows zero), from the generator."""
     pairs = ro["pair_of_row"][rows]
@@ -88,21 +100,26 @@ def test_mx_rows_forward_and_data_gradients(run):
         rows = rr if len(rr) <= 6 else np.sort(rng.choice(rr, 6, replace=False))
         x, dy = _expert_inputs(w, ro, probs, rows)
         o1 = np.array([0, len(rows)])
-        H, A, _ = O.grouped_mlp_fwd(x, o1, W1[None], W2[None], w.act)
-        # forward: Y from row-wise MX A and W2 with blocks along n
-        qa, sa = X.mx_quantize_rows(A)
+        _, A, _ = O.grouped_mlp_fwd(x, o1, W1[None], W2[None], w.act, round_out=False)
+        r = torch.as_tensor(rows).cuda()
+        # each block-scaled GEMM on its own inputs, the GPU's stored bf16
+        # operands: FC2 from A (row-wise MX, W2 with blocks along n); FC2-dgrad
+        # + dAct from dY and H (dY and W2 with blocks along d); FC1-dgrad from
+        # dH (dH and W1 with blocks along n1)
+        ga, gh = f64(o["a"][r]), f64(o["h"][r])
+        gdy, gdh = f64(o["dy_perm"][r]), f64(o["dh"][r])
+        qa, sa = X.mx_quantize_rows(ga)
         qw, sw = X.mx_quantize_weights(W2[None])
         Y = X.mx_fc2(qa, sa, qw, sw, o1)
-        # backward data gradients: dY and W2 with blocks along d; dH and W1
-        # with blocks along n1
-        dyq, dys = X.mx_quantize_rows(dy)
+        dyq, dys = X.mx_quantize_rows(gdy)
         w2q, w2s = X.mx_quantize_rows(W2)
         dA = X.mx_dgrad(dyq, dys, w2q[None], w2s[None], o1)
-        dH = O.bf16_round(O.act_backward(H, dA, w.act))
-        dhq, dhs = X.mx_quantize_rows(dH)
+        dH = O.act_backward(gh, dA, w.act)
+        dhq, dhs = X.mx_quantize_rows(gdh)
         w1q, w1s = X.mx_quantize_rows(W1)
-        dX = O.bf16_round(X.mx_dgrad(dhq, dhs, w1q[None], w1s[None], o1))
-        r = torch.as_tensor(rows).cuda()
+        dX = X.mx_dgrad(dhq, dhs, w1q[None], w1s[None], o1)
+        # the scaled permute's dY against the generator's dO times the probability
+        assert_rms_close(gdy, dy_exact(w, ro, probs, rows), f"MX e{e} dY")
         assert_rms_close(f64(o["a"][r]), A, f"MX e{e} A")
         assert_rms_close(f64(o["y_perm"][r]), Y, f"MX e{e} Y")
         assert_rms_close(f64(o["dh"][r]), dH, f"MX e{e} dH")

@@ -1,8 +1,12 @@
 """GPU grouped expert MLP (moe_grouped_mlp_fwd / _bwd) vs the oracle.
 
 Sizes span several 128x256 tiles, ragged tails, empty experts and a
-one-row expert; every output tensor must satisfy
-max|err| <= 2e-2 * RMS(oracle)."""
+one-row expert.  Every output tensor must satisfy
+max(|err| - 2^-8 |ref|) <= 2e-2 * RMS(ref), ref being the oracle's exact
+value before the storage rounding.  The backward is checked stage by
+stage, each GEMM on its own inputs: dH and dW2 from the GPU forward's
+stored bf16 H and A, dX and dW1 from the GPU's stored bf16 dH (the forward
+and dH are themselves checked against the oracle)."""
 import numpy as np
 import pytest
 import torch
@@ -34,6 +38,18 @@ def _case(E, d, n, counts, act, seed, tail=5, align=1):
     return off, x, W1, W2, dy
 
 
+def _bwd_refs(x, h, a, dy, dh, off, W1, W2, act):
+    """Unrounded oracle references of the backward's four outputs, stage by
+    stage: dH = act'(H; dY W2^T) and dW2 = A^T dY from the GPU's H and A;
+    dX = dH W1^T (FC1-dgrad) and dW1 = X^T dH from the GPU's dH."""
+    dH, _, _, dW2 = O.grouped_mlp_bwd(f64(x), f64(h), f64(a), f64(dy), off, f64(W1), f64(W2),
+                                      act, round_out=False)
+    gdh = f64(dh)
+    dX = O.grouped_gemm(gdh, off, f64(W1), "nk", round_out=False)
+    dW1 = O.grouped_wgrad(f64(x), gdh, off, round_out=False)
+    return dH, dX, dW1, dW2
+
+
 def _fwd(off, x, W1, W2, act, save_h=True):
     import dropless_grouped_gemm_gb300 as M
     h, a, y, err = M.grouped_mlp_fwd(x, cuda_i32(off), W1, W2, act, save_h=save_h)
@@ -58,7 +74,7 @@ FWD_CASES = [
 def test_fwd(name, E, d, n, counts, act):
     off, x, W1, W2, _ = _case(E, d, n, counts, act, seed=11)
     h, a, y = _fwd(off, x, W1, W2, act)
-    H, A, Y = O.grouped_mlp_fwd(f64(x), off, f64(W1), f64(W2), act)
+    H, A, Y = O.grouped_mlp_fwd(f64(x), off, f64(W1), f64(W2), act, round_out=False)
     R = int(off[-1])
     assert_rms_close(f64(h)[:R], H[:R], f"{name}/{act} H")
     assert_rms_close(f64(a)[:R], A[:R], f"{name}/{act} A")
@@ -85,8 +101,7 @@ def test_bwd(name, E, d, n, counts, act):
     dh, dx, dW1, dW2, err = M.grouped_mlp_bwd(x, h, a, dy, cuda_i32(off), W1, W2, act)
     torch.cuda.synchronize()
     assert int(err.item()) == 0
-    H, A, _ = O.grouped_mlp_fwd(f64(x), off, f64(W1), f64(W2), act)
-    dH, dX, dW1r, dW2r = O.grouped_mlp_bwd(f64(x), H, A, f64(dy), off, f64(W1), f64(W2), act)
+    dH, dX, dW1r, dW2r = _bwd_refs(x, h, a, dy, dh, off, W1, W2, act)
     R = int(off[-1])
     assert_rms_close(f64(dh)[:R], dH[:R], f"{name}/{act} dH")
     assert_rms_close(f64(dx)[:R], dX[:R], f"{name}/{act} dX")
@@ -117,8 +132,8 @@ def test_bwd_accumulate_dw(name, E, d, n, counts):
     act = "swiglu"
     off, x, W1, W2, dy = _case(E, d, n, counts, act, seed=13)
     h, a, y = _fwd(off, x, W1, W2, act)
-    H, A, _ = O.grouped_mlp_fwd(f64(x), off, f64(W1), f64(W2), act)
-    dH, dX, dW1r, dW2r = O.grouped_mlp_bwd(f64(x), H, A, f64(dy), off, f64(W1), f64(W2), act)
+    _, _, dW1r, dW2r = O.grouped_mlp_bwd(f64(x), f64(h), f64(a), f64(dy), off, f64(W1),
+                                           f64(W2), act, round_out=False)
     old1 = _prior(dW1r.shape, dW1r, (13, W.X, 90))
     old2 = _prior(dW2r.shape, dW2r, (13, W.X, 91))
     dW1, dW2 = old1.clone(), old2.clone()
@@ -126,6 +141,7 @@ def test_bwd_accumulate_dw(name, E, d, n, counts):
                                           dW2=dW2, accumulate_dw=True)
     torch.cuda.synchronize()
     assert int(err.item()) == 0
+    dH, dX, dW1r, dW2r = _bwd_refs(x, h, a, dy, dh, off, W1, W2, act)
     R = int(off[-1])
     assert_rms_close(f64(dh)[:R], dH[:R], f"{name} dH")
     assert_rms_close(f64(dx)[:R], dX[:R], f"{name} dX")
@@ -153,7 +169,7 @@ def test_aligned_zero_pad_rows():
     ro = O.route_offsets(idx, E, align)
     off = ro["offsets"]
     H, A, Y = O.grouped_mlp_fwd(O.permute(f64(tok), ro["pair_of_row"], k), off, f64(W1), f64(W2),
-                                "swiglu")
+                                "swiglu", round_out=False)
     R = int(off[-1])
     assert_rms_close(f64(y)[:R], Y[:R], "Y")
     pad = ro["pair_of_row"][:R] < 0
@@ -205,10 +221,11 @@ def test_maximum_experts():
     dh, dx, dW1, dW2, err = M.grouped_mlp_bwd(x, h, a, dy, cuda_i32(off), W1, W2, "swiglu")
     torch.cuda.synchronize()
     assert int(err.item()) == 0
-    H, A, Y = O.grouped_mlp_fwd(f64(x), off, f64(W1), f64(W2), "swiglu")
-    dH, dX, dW1r, dW2r = O.grouped_mlp_bwd(f64(x), H, A, f64(dy), off, f64(W1), f64(W2), "swiglu")
+    H, A, Y = O.grouped_mlp_fwd(f64(x), off, f64(W1), f64(W2), "swiglu", round_out=False)
+    dH, dX, dW1r, dW2r = _bwd_refs(x, h, a, dy, dh, off, W1, W2, "swiglu")
     R = int(off[-1])
     assert_rms_close(f64(y)[:R], Y[:R], "E=1024 Y")
+    assert_rms_close(f64(dh)[:R], dH[:R], "E=1024 dH")
     assert_rms_close(f64(dx)[:R], dX[:R], "E=1024 dX")
     assert_rms_close(f64(dW1), dW1r, "E=1024 dW1")
     assert_rms_close(f64(dW2), dW2r, "E=1024 dW2")

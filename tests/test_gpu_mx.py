@@ -223,7 +223,7 @@ def test_fused_fc1_mx_epilogue_and_block_scaled_fc2(act, shape):
     torch.cuda.synchronize()
     assert int(err.item()) == 0
     R = int(off[-1])
-    H, A, _ = O.grouped_mlp_fwd(f64(x), off, f64(W1), f64(W2), act)
+    H, A, _ = O.grouped_mlp_fwd(f64(x), off, f64(W1), f64(W2), act, round_out=False)
     ga = f64(a)[:R]
     assert_rms_close(ga, A[:R], f"{act} A (bf16)")
     # row-wise codes / scales (MMA-tiled scales decoded)
@@ -267,7 +267,7 @@ def test_mx_forward_max_experts_with_skipped_weights():
     torch.cuda.synchronize()
     assert int(err.item()) == 0
     R = int(off[-1])
-    _, A, _ = O.grouped_mlp_fwd(f64(x), off, f64(W1), f64(W2), act)
+    _, A, _ = O.grouped_mlp_fwd(f64(x), off, f64(W1), f64(W2), act, round_out=False)
     assert_rms_close(f64(a)[:R], A[:R], "E=1024 A (bf16)")
     qa, sa = O.mx_quantize_rows(f64(a)[:R])            # FC2's input: the GPU's bf16 A
     qw, sw = O.mx_quantize_weights(f64(W2))

@@ -56,8 +56,13 @@ def test_routed_backward_matches_oracle(name, E, T, k, d, n, align, act):
     row_prob = np.where(por >= 0, probs.reshape(-1)[np.maximum(por, 0)].astype(np.float64), 0.0)
     off = ro["offsets"]
     dO_perm = O.permute(f64(tok_dO), por, k)
-    dH, dX, dW1r, dW2r, Ap, dS = O.grouped_mlp_bwd_routed(f64(x), f64(H), dO_perm, row_prob, off,
-                                                          f64(W1), f64(W2), act)
+    dH, _, _, _, Ap, dS = O.grouped_mlp_bwd_routed(f64(x), f64(H), dO_perm, row_prob, off,
+                                                   f64(W1), f64(W2), act, round_out=False)
+    # the three GEMMs after FC2-dgrad, each on its own inputs: dX = dH W1^T
+    # and dW1 = X^T dH from the GPU's dH, dW2 = A'^T dO from the GPU's A'
+    dX = O.grouped_gemm(f64(dh), off, f64(W1), "nk", round_out=False)
+    dW1r = O.grouped_wgrad(f64(x), f64(dh), off, round_out=False)
+    dW2r = O.grouped_wgrad(f64(ap), dO_perm, off, round_out=False)
     R = int(off[-1])
     assert_rms_close(f64(dh)[:R], dH[:R], f"{name}/{act} dH")
     assert_rms_close(f64(ap)[:R], Ap[:R], f"{name}/{act} A'")
@@ -83,14 +88,19 @@ def test_routed_backward_accumulate_dw():
     off = ro["offsets"]
     row_prob = np.where(por >= 0, probs.reshape(-1)[np.maximum(por, 0)].astype(np.float64), 0.0)
     _, _, dW1r, dW2r, _, _ = O.grouped_mlp_bwd_routed(f64(x), f64(H), O.permute(f64(tok_dO), por, k),
-                                                      row_prob, off, f64(W1), f64(W2), act)
+                                                      row_prob, off, f64(W1), f64(W2), act,
+                                                      round_out=False)
     old1 = W.normal(dW1r.shape, (62, W.X, 90), float(np.sqrt((dW1r ** 2).mean())), "cuda")
     old2 = W.normal(dW2r.shape, (62, W.X, 91), float(np.sqrt((dW2r ** 2).mean())), "cuda")
     dW1, dW2 = old1.clone(), old2.clone()
-    *_, err = M.grouped_mlp_bwd_routed(x, H, do_perm, r["pair_of_row"], pt.view(-1), r["offsets"],
-                                       W1, W2, act, dW1=dW1, dW2=dW2, accumulate_dw=True)
+    dh, ap, *_, err = M.grouped_mlp_bwd_routed(x, H, do_perm, r["pair_of_row"], pt.view(-1),
+                                               r["offsets"], W1, W2, act, dW1=dW1, dW2=dW2,
+                                               accumulate_dw=True)
     torch.cuda.synchronize()
     assert int(err.item()) == 0
+    # each weight gradient on its own inputs (the GPU's dH and A')
+    dW1r = O.grouped_wgrad(f64(x), f64(dh), off, round_out=False)
+    dW2r = O.grouped_wgrad(f64(ap), O.permute(f64(tok_dO), por, k), off, round_out=False)
     assert_rms_close(f64(dW1), f64(old1) + dW1r, "routed dW1 accumulated")
     assert_rms_close(f64(dW2), f64(old2) + dW2r, "routed dW2 accumulated")
     empty = [e for e in range(len(off) - 1) if off[e + 1] == off[e]]

@@ -33,7 +33,7 @@ def test_grouped_gemm_matches_oracle(layout, K, N):
     out, err = M.grouped_gemm(a, cuda_i32(off), B, layout, out=sentinel)
     torch.cuda.synchronize()
     assert int(err.item()) == 0 and M.last_launch_count() == 1
-    ref = O.grouped_gemm(f64(a), off, f64(B), layout)
+    ref = O.grouped_gemm(f64(a), off, f64(B), layout, round_out=False)
     assert_rms_close(f64(out)[:R], ref[:R], f"grouped_gemm {layout} K={K} N={N}")
     assert (f64(out)[R:] == 7.0).all()          # rows outside every expert untouched
 
@@ -53,8 +53,8 @@ def test_activation_passes_match_oracle(act):
     M.activation(h, offs, act, a=a)
     M.activation_bwd(h, da, offs, act, dh=dh)
     torch.cuda.synchronize()
-    assert_rms_close(f64(a)[:R], O.bf16_round(O.act_forward(f64(h)[:R], act)), f"{act} A")
-    assert_rms_close(f64(dh)[:R], O.bf16_round(O.act_backward(f64(h)[:R], f64(da)[:R], act)),
+    assert_rms_close(f64(a)[:R], O.act_forward(f64(h)[:R], act), f"{act} A")
+    assert_rms_close(f64(dh)[:R], O.act_backward(f64(h)[:R], f64(da)[:R], act),
                      f"{act} dH")
     assert (f64(a)[R:] == 7.0).all() and (f64(dh)[R:] == 7.0).all()
 

@@ -325,6 +325,39 @@ def test_grouped_gemm_is_the_mlp_fc2():
     assert np.array_equal(O.grouped_gemm(A, off, np.swapaxes(W2, 1, 2).copy(), "nk")[:R], Y[:R])
 
 
+def test_grouped_wgrad_brute_force():
+    """dW_e = P_e^T Q_e against scalar loops over the rows of each expert
+    (an empty expert gives exact zeros; rows past the last expert are not
+    read)."""
+    rng = np.random.default_rng(16)
+    rows = (3, 0, 2)
+    off = np.concatenate([[0], np.cumsum(rows)])
+    P = rng.standard_normal((int(off[-1]) + 2, 4))
+    Q = rng.standard_normal((int(off[-1]) + 2, 3))
+    P[-2:] = np.nan
+    dW = O.grouped_wgrad(P, Q, off, round_out=False)
+    assert dW.shape == (3, 4, 3)
+    for e in range(3):
+        for i in range(4):
+            for j in range(3):
+                want = sum(P[r][i] * Q[r][j] for r in range(off[e], off[e + 1]))
+                assert abs(dW[e][i][j] - want) < 1e-12
+    assert (dW[1] == 0).all()
+
+
+@pytest.mark.parametrize("act", ACTS)
+def test_grouped_wgrad_is_the_mlp_weight_gradients(act):
+    """grouped_mlp_bwd's dW1 is grouped_wgrad(X, dH) and its dW2 is
+    grouped_wgrad(A, dY), bit for bit (bf16 rounding included)."""
+    rng = np.random.default_rng(17)
+    off, x, W1, W2 = _tiny(act, rng)
+    H, A, _ = O.grouped_mlp_fwd(x, off, W1, W2, act)
+    dY = rng.standard_normal((int(off[-1]), W2.shape[2]))
+    dH, _, dW1, dW2 = O.grouped_mlp_bwd(x, H, A, dY, off, W1, W2, act)
+    assert np.array_equal(O.grouped_wgrad(x, dH, off), dW1)
+    assert np.array_equal(O.grouped_wgrad(A, dY, off), dW2)
+
+
 @pytest.mark.parametrize("act", ACTS)
 def test_round_out_changes_only_the_final_rounding(act):
     """round_out=False returns each stored result just before its bf16
@@ -362,6 +395,8 @@ def test_round_out_changes_only_the_final_rounding(act):
     changed += [same(u, r) for u, r in zip(ru[:5], rr[:5])]
     assert np.array_equal(ru[5], rr[5], equal_nan=True)          # dS is float32-stored: unrounded
     changed.append(same(O.grouped_gemm(A, off, W2, round_out=False), O.grouped_gemm(A, off, W2)))
+    changed.append(same(O.grouped_wgrad(x, br[0], off, round_out=False),
+                        O.grouped_wgrad(x, br[0], off)))
     h1, a1 = O.fc1_rows(x[:5], W1[0], act, round_out=False)
     h0, a0 = O.fc1_rows(x[:5], W1[0], act)
     changed += [same(h1, h0), same(a1, a0)]
