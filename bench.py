@@ -49,9 +49,10 @@ METRIC = "grouped MoE MLP fwd+bwd useful TFLOP/s and % of GB300 dense BF16/FP8 p
 DEFAULT_WORKLOAD = "balanced_e8_m4096_k8192_n4096_swiglu"
 KERNELS_FWD = ["fc1_act", "fc2"]
 KERNELS_BWD = ["fc2_dgrad_dact", "fc2_wgrad", "fc1_dgrad", "fc1_wgrad"]
-# launch order of the MXFP8 backward (weight quantisers, then moe_grouped_mlp_bwd_mx)
+# launch order of the MXFP8 backward (weight quantiser, then moe_grouped_mlp_bwd_mx,
+# whose FC2-dgrad epilogue also quantises dH both ways)
 KERNELS_MX_BWD = ["mx_quantize_w1_rows", "mx_quantize_dy", "mx_quantize_x", "mx_retile_a",
-                  "fc2_dgrad_dact", "mx_quantize_dh", "fc2_wgrad", "fc1_dgrad", "fc1_wgrad"]
+                  "fc2_dgrad_dact", "fc2_wgrad", "fc1_dgrad", "fc1_wgrad"]
 
 
 # ---------------------------------------------------------------- accounting
@@ -91,8 +92,9 @@ def kernel_work(w, M, E_ne):
                 "mx_quantize_dy": (0, B * M * d + 2 * mxb(M * d)),
                 "mx_quantize_x": (0, B * M * d + mxb(M * d)),
                 "mx_retile_a": (0, 2 * (M * n // 32)),
-                "fc2_dgrad_dact": (2 * M * d * n, mxb(M * d) + mxb(E_ne * n * d) + 2 * B * M * n1),
-                "mx_quantize_dh": (0, B * M * n1 + 2 * mxb(M * n1)),
+                # reads dY codes, W2 codes, H; writes dH (bf16) and its two MXFP8 copies
+                "fc2_dgrad_dact": (2 * M * d * n, mxb(M * d) + mxb(E_ne * n * d) + 2 * B * M * n1 +
+                                   2 * mxb(M * n1)),
                 "fc2_wgrad": (2 * M * n * d, mxb(M * n) + mxb(M * d) + B * E * n * d),
                 "fc1_dgrad": (2 * M * n1 * d, mxb(M * n1) + mxb(E_ne * d * n1) + B * M * d),
                 "fc1_wgrad": (2 * M * d * n1, mxb(M * d) + mxb(M * n1) + B * E * d * n1),
@@ -692,6 +694,8 @@ def main():
     fusion = None
     if w.routing == "identity" and not w.mxfp8 and w.backward and not args.no_fusion_control:
         fusion = fusion_control(w, inp, o)
+    if w.mxfp8 and w.backward and not args.no_fusion_control:
+        fusion = mx_fusion_control(w, inp, o)
 
     cpu = None
     if not args.no_cpu_baseline:
@@ -787,6 +791,62 @@ def fusion_control(w, inp, o, reps=20):
             "reps": reps,
             "what": "same GEMM kernels; unfused = GEMM storing H (dA) + separate "
                     "activation (derivative) pass"}
+
+
+def mx_fusion_control(w, inp, o, reps=20):
+    """GroupGemm + dActivation + Quantize/Transpose against its unfused
+    control: the MXFP8 backward with dH quantised in FC2-dgrad's epilogue
+    (7 launches) and with FC2-dgrad storing dH alone and a separate tiled
+    quantiser pass (8 launches), interleaved over ``reps`` rounds on the
+    step's own operands, each launch timed by its own events; the results
+    of the two are identical (tested)."""
+    import ctypes
+    import torch
+    import dropless_grouped_gemm_gb300 as M
+    if w.routing == "identity":
+        x, dy, off = inp["x_perm"], inp["dy_perm"], inp["offsets"]
+    else:
+        x, dy, off = o["x_perm"], o["dy_perm"], o["route"]["offsets"]
+    mx, mb = o["mx"], o["mxb"]
+    ops = dict(a_qT=mx["a_qT"], a_sT=mx["a_sT"], w2_q=mb["w2_q"], w2_s=mb["w2_s"],
+               w1_q=mb["w1_q"], w1_s=mb["w1_s"])
+
+    def call(sep):
+        M.grouped_mlp_bwd_mx(x, o["h"], dy, off, ops, w.act, dh=o["dh"], dx_perm=o["dx_perm"],
+                             dW1=o["dW1"], dW2=o["dW2"], err=o["err"], workspace=mb["ws"],
+                             separate_dh_quant=sep)
+    per = 15
+    stream = torch.cuda.current_stream()
+    for _ in range(2):
+        call(False)
+        call(True)
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(2 * per * reps)]
+    for e in evs:
+        e.record(stream)
+    torch.cuda.synchronize()
+    handles = (ctypes.c_void_p * len(evs))(*[e.cuda_event for e in evs])
+    M.lib().moe_set_launch_events(handles, len(evs))
+    for _ in range(reps):
+        call(False)
+        call(True)
+    torch.cuda.synchronize()
+    used = M.lib().moe_launch_events_used()
+    M.lib().moe_set_launch_events(None, 0)
+    if used != len(evs) or int(o["err"].item()) != 0:
+        return None
+    t = [[evs[2 * (r * per + i)].elapsed_time(evs[2 * (r * per + i) + 1]) for r in range(reps)]
+         for i in range(per)]
+    avg = [sum(v) / len(v) for v in t]
+    fused = avg[3]                       # FC2-dgrad + dAct + Quantize/Transpose
+    unf_gemm, unf_q = avg[7 + 3], avg[7 + 4]
+    return {"bwd_dh": {"fused_ms": round(fused, 4), "unfused_ms": round(unf_gemm + unf_q, 4),
+                       "gemm_ms": round(unf_gemm, 4), "quantize_ms": round(unf_q, 4),
+                       "speedup": round((unf_gemm + unf_q) / fused, 3)},
+            "fused_backward_ms": round(sum(avg[:7]), 4),
+            "unfused_backward_ms": round(sum(avg[7:]), 4),
+            "reps": reps,
+            "what": "MXFP8 backward: FC2-dgrad + dAct with dH's MXFP8 copies written by its "
+                    "epilogue, against FC2-dgrad + dAct storing dH and a separate tiled quantiser"}
 
 
 def step_description(w):

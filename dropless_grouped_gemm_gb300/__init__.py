@@ -30,13 +30,15 @@ __all__ = [
     "MxBwd", "mx_quantize_weights_rowwise", "mx_quantize_tiled", "mx_bwd_workspace_size", "grouped_mlp_bwd_mx",
     "grouped_mlp_bwd_routed", "router_grad_rows", "mx_quantize_weights2", "FLAG_ACCUMULATE_DW",
     "grouped_gemm", "activation", "activation_bwd", "grouped_mlp_fwd_gather",
-    "grouped_mlp_bwd_routed_gather", "route_logits",
+    "grouped_mlp_bwd_routed_gather", "route_logits", "FLAG_MX_SEPARATE_DH_QUANT",
+    "mx_bwd_workspace_layout",
 ]
 
 ACT = {"swiglu": 0, "geglu": 1, "srelu": 2}
 FLAG_SAVE_H = 1
 FLAG_MXFP8 = 2
 FLAG_ACCUMULATE_DW = 4
+FLAG_MX_SEPARATE_DH_QUANT = 8
 DEV_BAD_EXPERT, DEV_OVERFLOW, DEV_TIMEOUT, DEV_BAD_OFFSETS = 1, 2, 4, 8
 _RC = {-1: "MOE_E_NULL", -2: "MOE_E_ALIGN", -3: "MOE_E_SIZE", -4: "MOE_E_ARG",
        -5: "MOE_E_CUDA", -6: "MOE_E_WORKSPACE"}
@@ -117,6 +119,8 @@ def lib():
         L.moe_mx_quantize_weights_rowwise.argtypes = [vp, i32, i32, vp, i32, vp, vp, vp]
         L.moe_mx_bwd_workspace_size.restype = sz
         L.moe_mx_bwd_workspace_size.argtypes = [i32, i32, i32, i32]
+        L.moe_mx_bwd_workspace_layout.restype = sz
+        L.moe_mx_bwd_workspace_layout.argtypes = [i32, i32, i32, i32, vp]
         L.moe_workspace_size.restype = sz
         L.moe_workspace_size.argtypes = [i32, i32, i32, i32, i32, i32, i32, i32]
         L.moe_grouped_mlp_bwd_mx.restype = i32
@@ -560,15 +564,34 @@ def mx_bwd_workspace_size(M_cap: int, d: int, n: int, act: str = "swiglu") -> in
     return int(lib().moe_mx_bwd_workspace_size(M_cap, d, n, ACT[act]))
 
 
+MX_BWD_SECTIONS = ("dy_q", "dy_s", "dy_qT", "dy_sT", "x_qT", "x_sT", "a_sT", "dh_q", "dh_s",
+                   "dh_qT", "dh_sT")
+
+
+def mx_bwd_workspace_layout(M_cap: int, d: int, n: int, act: str = "swiglu") -> dict:
+    """Byte offsets of the MXFP8 backward's quantised operands inside its
+    workspace (moe_mx_bwd_workspace_layout), by section name, plus "bytes"."""
+    offs = (ctypes.c_size_t * len(MX_BWD_SECTIONS))()
+    total = int(lib().moe_mx_bwd_workspace_layout(M_cap, d, n, ACT[act], offs))
+    if total == 0:
+        raise MoeError("moe_mx_bwd_workspace_layout: invalid sizes")
+    out = {nm: int(offs[i]) for i, nm in enumerate(MX_BWD_SECTIONS)}
+    out["bytes"] = total
+    return out
+
+
 def grouped_mlp_bwd_mx(x_perm, h_saved, dy_perm, offsets, mx: dict, act: str = "swiglu",
                        dh=None, dx_perm=None, dW1=None, dW2=None, err=None, workspace=None,
-                       stream=None, accumulate_dw: bool = False):
+                       stream=None, accumulate_dw: bool = False, separate_dh_quant: bool = False):
     """MXFP8 grouped expert MLP backward (moe_grouped_mlp_bwd_mx).  ``mx``
     holds uint8 tensors a_qT, a_sT (the forward's transposed copy), w2_q, w2_s
     (W2 with blocks along d) and w1_q, w1_s (W1 with blocks along n1).
     Returns (dh, dx_perm, dW1, dW2, err).  accumulate_dw as in
-    grouped_mlp_bwd."""
+    grouped_mlp_bwd; separate_dh_quant selects the unfused control (dH
+    quantised in its own pass, MOE_FLAG_MX_SEPARATE_DH_QUANT)."""
     flags = _bwd_flags(accumulate_dw, dW1, dW2)
+    if separate_dh_quant:
+        flags |= FLAG_MX_SEPARATE_DH_QUANT
     for t, nm in ((x_perm, "x_perm"), (h_saved, "h_saved"), (dy_perm, "dy_perm")):
         _need(t, torch.bfloat16, nm)
     _need(offsets, torch.int32, "offsets", 1)

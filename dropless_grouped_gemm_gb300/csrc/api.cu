@@ -654,6 +654,19 @@ size_t moe_mx_bwd_workspace_size(int M_cap, int d, int n, int act) {
   return carve_mx_bwd(nullptr, M_cap, d, n1, n).bytes;
 }
 
+size_t moe_mx_bwd_workspace_layout(int M_cap, int d, int n, int act, size_t* offs) {
+  if (!offs || M_cap < 0 || d <= 0 || n <= 0 || act < MOE_ACT_SWIGLU || act > MOE_ACT_SRELU)
+    return 0;
+  const int n1 = (act == MOE_ACT_SRELU) ? n : 2 * n;
+  // a base far from zero, so that every section's address stays positive
+  uint8_t* const base = reinterpret_cast<uint8_t*>(static_cast<uintptr_t>(1) << 40);
+  const MxBwdWs w = carve_mx_bwd(base, M_cap, d, n1, n);
+  const uint8_t* sec[11] = {w.dy_q, w.dy_s, w.dy_qT, w.dy_sT, w.x_qT, w.x_sT,
+                            w.a_sT, w.dh_q, w.dh_s, w.dh_qT, w.dh_sT};
+  for (int i = 0; i < 11; ++i) offs[i] = static_cast<size_t>(sec[i] - base);
+  return w.bytes;
+}
+
 size_t moe_workspace_size(int T, int k, int E, int M_cap, int d, int n, int act, int flags) {
   const size_t r = moe_route_workspace_size(T, k, E);
   const size_t m = (flags & MOE_FLAG_MXFP8) ? moe_mx_bwd_workspace_size(M_cap, d, n, act) : 0;
@@ -805,9 +818,11 @@ int moe_grouped_mlp_bwd_mx(const moe_bf16* x_perm, const moe_bf16* h_saved,
   int rc = check_mlp_sizes(E, M_cap, d, n);
   if (rc) return rc;
   if (d % 128 || n % 128 || M_cap % 32) return MOE_E_SIZE;
-  if (act < MOE_ACT_SWIGLU || act > MOE_ACT_SRELU || (flags & ~MOE_FLAG_ACCUMULATE_DW))
+  if (act < MOE_ACT_SWIGLU || act > MOE_ACT_SRELU ||
+      (flags & ~(MOE_FLAG_ACCUMULATE_DW | MOE_FLAG_MX_SEPARATE_DH_QUANT)))
     return MOE_E_ARG;
   const bool accumulate = flags & MOE_FLAG_ACCUMULATE_DW;
+  const bool fuse_dh = !(flags & MOE_FLAG_MX_SEPARATE_DH_QUANT);
   if (!offsets || !mx || !dW1 || !dW2 || !err) return MOE_E_NULL;
   const int n1 = (act == MOE_ACT_SRELU) ? n : 2 * n;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -861,14 +876,17 @@ int moe_grouped_mlp_bwd_mx(const moe_bf16* x_perm, const moe_bf16* h_saved,
     ev_end(s);
   }
   if (e != cudaSuccess) return MOE_E_CUDA;
-  // 4. dH = act'(H; dY W2^T)
+  // 4. dH = act'(H; dY W2^T); fused: with dH's MXFP8 copies both ways
   moe::MxGemmArgs g{};
   g.offsets = offsets; g.E = E; g.M_cap = M_cap; g.K = d; g.N = n;
   g.a_s = ws.dy_s; g.b_s = mx->w2_s; g.out = dh; g.ldo = n1; g.aux = h_saved; g.ld_aux = n1;
   g.err = err;
+  if (fuse_dh) {
+    g.dh_q = ws.dh_q; g.dh_s = ws.dh_s; g.dh_qT = ws.dh_qT; g.dh_sT = ws.dh_sT; g.n1 = n1;
+  }
   e = mx_gemm(moe::MxKind::kDgradAct, act, t_dy, t_w2, t_dy, g, sms, s);
-  // 5. dH both ways
-  if (e == cudaSuccess) e = quant(dh, n1, ws.dh_q, ws.dh_s, ws.dh_qT, ws.dh_sT);
+  // 5. unfused control: dH both ways in a separate pass
+  if (e == cudaSuccess && !fuse_dh) e = quant(dh, n1, ws.dh_q, ws.dh_s, ws.dh_qT, ws.dh_sT);
   if (e != cudaSuccess) return MOE_E_CUDA;
   // 6. dW2_e = A_e^T dY_e
   moe::MxGemmArgs gw2{};
@@ -891,7 +909,7 @@ int moe_grouped_mlp_bwd_mx(const moe_bf16* x_perm, const moe_bf16* h_saved,
   gw1.out = dW1; gw1.accumulate = accumulate;
   e = mx_gemm(moe::MxKind::kWgrad, 0, t_xT, t_dhT, t_dw1, gw1, sms, s);
   if (e != cudaSuccess) return MOE_E_CUDA;
-  g_last_launches = 8;
+  g_last_launches = fuse_dh ? 7 : 8;
   return MOE_OK;
 }
 

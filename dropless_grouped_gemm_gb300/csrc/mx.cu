@@ -35,6 +35,10 @@ constexpr int QTMEM_COLS = 512;
 constexpr int QSF_TMEM = QBN;                     // scale columns after the accumulator
 constexpr int QSF_COLS = 12;                      // a stage's three chunks, 4 columns each
 constexpr int QBOX_BYTES = 32 * 64 * 2;           // staged output box: 32 rows x 64 bf16
+// The quantising FC2-dgrad epilogue parks the second half of each
+// warpgroup's 128 accumulator columns here (after the scale columns) so
+// that only 64 of them occupy registers once the accumulator is released
+constexpr int QSTASH_TMEM = 320;
 
 // TMEM holds one 256-column accumulator (the scale columns leave no room
 // for a second); the epilogue moves it to registers and releases it at once,
@@ -253,6 +257,69 @@ __device__ __forceinline__ void mx_dact_row32(const MxGemmArgs& g, long long gro
       *reinterpret_cast<uint4*>(p + 8 * v) = make_uint4(o[0], o[1], o[2], o[3]);
     }
   }
+}
+
+// GroupGemm + dActivation + Quantize/Transpose ([TE] "다음 단계: NVFP4, GEMM
+// 융합 양자화, A2A 오버랩"; [CuTe] "무엇을 해결하려는가": the low-precision
+// output and its transposed copy come from the epilogue, so the bf16
+// intermediate is not read again).  One 32-column block of dH for the
+// thread's row (16 dA columns when gated, 32 for squared ReLU); the whole
+// warp calls it together, its 32 lanes being 32 consecutive rows of one
+// expert (a column block of the transposed copy).  Stores the bf16 dH, the
+// row-wise codes and scale (row tile of the 128-row tile starting at
+// tl_row0) and the transposed codes and scales (K tile of the same rows,
+// block q of it).
+template <int ACT>
+__device__ __forceinline__ void mx_dact_quant_block(const MxGemmArgs& g, int tl_row0, int q,
+                                                    int lane, int hc, const uint32_t* r) {
+  const int rt = q * 32 + lane;
+  const long long grow = static_cast<long long>(tl_row0) + rt;
+  const uint16_t* hp = g.aux + grow * g.ld_aux + hc;
+  uint32_t pk[16];
+  float f[32];
+#pragma unroll
+  for (int v = 0; v < 4; ++v) {
+    const uint4 hv = *reinterpret_cast<const uint4*>(hp + 8 * v);
+    const uint32_t hw[4] = {hv.x, hv.y, hv.z, hv.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      if constexpr (ACT == MOE_ACT_SRELU) {
+        pk[4 * v + i] = pack_bf16x2(2.f * fmaxf(bf16_lo(hw[i]), 0.f) * __uint_as_float(r[8 * v + 2 * i]),
+                                    2.f * fmaxf(bf16_hi(hw[i]), 0.f) * __uint_as_float(r[8 * v + 2 * i + 1]));
+      } else {
+        const float gg = bf16_lo(hw[i]), uu = bf16_hi(hw[i]);  // (gate, up) pair
+        const float da = __uint_as_float(r[4 * v + i]);
+        float ph, dph;
+        gate_phi_dphi<ACT>(gg, ph, dph);
+        pk[4 * v + i] = pack_bf16x2(da * uu * dph, da * ph);
+      }
+      f[8 * v + 2 * i] = bf16_lo(pk[4 * v + i]);
+      f[8 * v + 2 * i + 1] = bf16_hi(pk[4 * v + i]);
+    }
+  }
+  uint16_t* p = g.out + grow * g.ldo + hc;
+#pragma unroll
+  for (int v = 0; v < 4; ++v)
+    *reinterpret_cast<uint4*>(p + 8 * v) = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+  // both scale layouts put this 128-row tile's chunk of column group hc / 128 at
+  const long long chunk = static_cast<long long>(tl_row0 / 32) * (g.n1 / 128) + hc / 128;
+  // row-wise block
+  uint32_t qw[8];
+  const uint32_t sc = mx_quant32(f, qw);
+  uint4* pq = reinterpret_cast<uint4*>(g.dh_q + grow * g.n1 + hc);
+  pq[0] = make_uint4(qw[0], qw[1], qw[2], qw[3]);
+  pq[1] = make_uint4(qw[4], qw[5], qw[6], qw[7]);
+  g.dh_s[chunk * 512 + mx_chunk_off(rt, (hc >> 5) & 3)] = static_cast<uint8_t>(sc);
+  // transposed copy: column hc + j over the warp's 32 rows is one block
+  uint32_t my_sc = 0;
+#pragma unroll
+  for (int j = 0; j < 32; ++j) {
+    uint32_t code;
+    const uint32_t scj = mx_quant_lanes(f[j], code);
+    g.dh_qT[static_cast<long long>(hc + j) * g.M_cap + grow] = static_cast<uint8_t>(code);
+    if (lane == j) my_sc = scj;
+  }
+  g.dh_sT[chunk * 512 + mx_chunk_off((hc + lane) & 127, q)] = static_cast<uint8_t>(my_sc);
 }
 
 // Persistent warp-specialised block-scaled grouped GEMM in 2-CTA clusters:
@@ -496,6 +563,50 @@ __global__ void __launch_bounds__(QTHREADS, 1)
       const bool zero = W && tl.kblocks == 0;
       // accumulating weight gradients leave an empty expert's untouched
       const bool mine = wg < tl.nh && !tl.ghost && !(zero && g.accumulate);
+      if constexpr (KIND == MxKind::kDgradAct && QOUT) {
+        // GroupGemm + dActivation + Quantize/Transpose: columns 64..127 of
+        // the warpgroup's half go to the TMEM stash, 0..63 to registers;
+        // then the accumulator is released and the dH blocks are produced
+        const uint32_t lanes = static_cast<uint32_t>(q * 32) << 16;
+        const uint32_t tb = tmem_base + lanes + wg * QHN;
+        const uint32_t st = tmem_base + lanes + QSTASH_TMEM + wg * 64;
+        uint32_t v0[32], v1[32];
+        if (mine) {
+          tmem_ld32(tb + 64, v0);
+          tmem_wait_ld();
+          tmem_st32(st, v0);
+          tmem_ld32(tb + 96, v0);
+          tmem_wait_ld();
+          tmem_st32(st + 32, v0);
+          tmem_ld32(tb, v0);
+          tmem_ld32(tb + 32, v1);
+          tmem_wait_ld();
+          tmem_wait_st();
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(tempty_bar);
+        // offsets are multiples of 32: a warp's 32 rows are all valid or none
+        if (!mine || q * 32 >= tl.rows) continue;
+        constexpr int BLK = (ACT == MOE_ACT_SRELU) ? 32 : 16;   // dA columns per dH block
+        const int col0 = tl.n0 + wg * QHN;
+#pragma unroll 1
+        for (int c = 0; c < 4; ++c) {
+          if (c == 2) {
+            tmem_ld32(st, v0);
+            tmem_ld32(st + 32, v1);
+            tmem_wait_ld();
+          }
+          const uint32_t* src = (c & 1) ? v1 : v0;
+#pragma unroll
+          for (int b = 0; b < 32 / BLK; ++b) {
+            const int dcol = col0 + 32 * c + b * BLK;          // first dA column
+            mx_dact_quant_block<ACT>(g, tl.row0, q, lane, (ACT == MOE_ACT_SRELU) ? dcol : 2 * dcol,
+                                     src + b * BLK);
+          }
+        }
+        continue;
+      }
       uint32_t v[4][32];
       if (mine && !zero) {
         const uint32_t tb = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + wg * QHN;
@@ -632,6 +743,16 @@ cudaError_t launch_mx_gemm(MxKind kind, int act, const CUtensorMap& ta, const CU
                      : launch_mx_t<MxKind::kDgrad, 0>(ta, tb, tc, g, num_sms, st);
     case MxKind::kWgrad: return launch_mx_t<MxKind::kWgrad, 0>(ta, tb, tc, g, num_sms, st);
     case MxKind::kDgradAct:
+      if (g.dh_q != nullptr) {
+        // GroupGemm + dActivation + Quantize/Transpose
+        if (!g.dh_s || !g.dh_qT || !g.dh_sT || g.n1 <= 0 || g.n1 % 128) return cudaErrorInvalidValue;
+        switch (act) {
+          case MOE_ACT_SWIGLU: return launch_mx_t<MxKind::kDgradAct, MOE_ACT_SWIGLU, true>(ta, tb, tc, g, num_sms, st);
+          case MOE_ACT_GEGLU: return launch_mx_t<MxKind::kDgradAct, MOE_ACT_GEGLU, true>(ta, tb, tc, g, num_sms, st);
+          case MOE_ACT_SRELU: return launch_mx_t<MxKind::kDgradAct, MOE_ACT_SRELU, true>(ta, tb, tc, g, num_sms, st);
+          default: return cudaErrorInvalidValue;
+        }
+      }
       switch (act) {
         case MOE_ACT_SWIGLU: return launch_mx_t<MxKind::kDgradAct, MOE_ACT_SWIGLU>(ta, tb, tc, g, num_sms, st);
         case MOE_ACT_GEGLU: return launch_mx_t<MxKind::kDgradAct, MOE_ACT_GEGLU>(ta, tb, tc, g, num_sms, st);

@@ -51,6 +51,17 @@ struct MxGemmArgs {
   uint8_t* q_out;
   uint8_t* s_out;
   int32_t* err;
+  // kDgradAct, optional (dh_q == nullptr: none): GroupGemm + dActivation +
+  // Quantize/Transpose - the epilogue also writes the MXFP8 copies of the
+  // bf16 dH it stores, as the tiled activation quantiser would: row-wise
+  // codes dh_q [M_cap, n1] with scales dh_s in row tiles (FC1-dgrad's A),
+  // and the transposed copy dh_qT [n1, M_cap] with scales dh_sT in K tiles
+  // (FC1-wgrad's B)
+  uint8_t* dh_q;
+  uint8_t* dh_s;
+  uint8_t* dh_qT;
+  uint8_t* dh_sT;
+  int n1;
   // kWgrad: 1 = add the result to the bf16 values already in `out` ([E, R,
   // N], one rounding of old + new); experts with no rows leave theirs
   // untouched

@@ -75,6 +75,10 @@ typedef uint16_t moe_bf16;
                                   gradients (gradient accumulation over
                                   micro-batches); experts with no rows keep
                                   their dW untouched                          */
+#define MOE_FLAG_MX_SEPARATE_DH_QUANT 8 /* MXFP8 backward: quantise dH in its
+                                  own pass after FC2-dgrad instead of in
+                                  FC2-dgrad's epilogue (the unfused control;
+                                  identical results)                          */
 
 /*
  * MXFP8 data ([CuTe] "무엇을 해결하려는가" / "핵심 아이디어": an MXFP8 output
@@ -551,6 +555,19 @@ int moe_activation_bwd(const moe_bf16* h, const moe_bf16* da, const int32_t* off
 size_t moe_mx_bwd_workspace_size(int M_cap, int d, int n, int act);
 
 /*
+ * moe_mx_bwd_workspace_layout - where moe_grouped_mlp_bwd_mx keeps its
+ * quantised operands inside mx->workspace, for callers that reuse them
+ * (e.g. dH's MXFP8 copies) or check them.  Writes 11 byte offsets, in this
+ * order: dY codes [M_cap, d] and scales (row tiles), dY^T codes [d, M_cap]
+ * and scales (K tiles), x^T codes [d, M_cap] and scales (K tiles), A^T
+ * scales re-tiled (K tiles), dH codes [M_cap, n1] and scales (row tiles),
+ * dH^T codes [n1, M_cap] and scales (K tiles).  Valid after the call on the
+ * stream has completed.  Host-only; returns the workspace size, 0 (and
+ * writes nothing) on invalid sizes or a NULL offs.
+ */
+size_t moe_mx_bwd_workspace_layout(int M_cap, int d, int n, int act, size_t* offs);
+
+/*
  * moe_workspace_size - device scratch for one layer's calls: the larger of
  * moe_route_workspace_size(T, k, E) and, when flags has MOE_FLAG_MXFP8,
  * moe_mx_bwd_workspace_size(M_cap, d, n, act).  One buffer of this size
@@ -570,10 +587,17 @@ size_t moe_workspace_size(int T, int k, int E, int M_cap, int d, int n, int act,
  *   offsets [E+1] multiples of 32 (route with align = 32); d, n multiples
  *   of 128, M_cap a multiple of 32.  Outputs dh [M_cap, n1], dx_perm
  *   [M_cap, d] (rows outside every expert untouched), dW1 [E, d, n1],
- *   dW2 [E, n, d] bf16 (zero for experts with no rows).  Eight launches:
+ *   dW2 [E, n, d] bf16 (zero for experts with no rows).  Seven launches:
  *   three quantisers (dY both ways, x transposed, A's scales re-tiled),
- *   FC2-dgrad + dAct, the dH quantiser, FC2-wgrad, FC1-dgrad, FC1-wgrad.
- *   flags: 0 or MOE_FLAG_ACCUMULATE_DW (as in moe_grouped_mlp_bwd).
+ *   FC2-dgrad + dAct + Quantize/Transpose (the epilogue writes the bf16 dH
+ *   and both MXFP8 copies of it that FC1-dgrad and FC1-wgrad read, as the
+ *   standalone tiled quantiser would, bit for bit), FC2-wgrad, FC1-dgrad,
+ *   FC1-wgrad.  With MOE_FLAG_MX_SEPARATE_DH_QUANT, eight: FC2-dgrad + dAct
+ *   stores dH alone and a separate pass quantises it.
+ *   flags: MOE_FLAG_ACCUMULATE_DW (as in moe_grouped_mlp_bwd),
+ *   MOE_FLAG_MX_SEPARATE_DH_QUANT, or both.
+ *   The quantised operands live in mx->workspace at the offsets
+ *   moe_mx_bwd_workspace_layout gives.
  *   Errors: as moe_grouped_mlp_bwd; MOE_E_WORKSPACE if mx->ws_bytes is too
  *   small; offsets that are not multiples of 32 raise MOE_DEV_BAD_OFFSETS.
  */

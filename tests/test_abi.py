@@ -76,7 +76,8 @@ def test_host_argument_errors(L):
 
 
 def test_accumulate_flag_host_checks(L):
-    """MOE_FLAG_ACCUMULATE_DW is the only backward flag; an unknown bit is
+    """MOE_FLAG_ACCUMULATE_DW is the backward flag (and, for the MXFP8
+    backward alone, MOE_FLAG_MX_SEPARATE_DH_QUANT); an unknown bit is
     refused.  With no rows at all an accumulating backward has nothing to
     add and returns before any CUDA call (all pointers are dummies)."""
     vp = ctypes.c_void_p
@@ -88,9 +89,12 @@ def test_accumulate_flag_host_checks(L):
     mxb = lambda flags, M_cap: L.moe_grouped_mlp_bwd_mx(d, d, d, d, 2, M_cap, 128, 128, 0, flags,
                                                          d, d, d, d, d, d, None)
     for f in (bwd, routed, mxb):
-        assert f(8, 256) == -4
+        assert f(16, 256) == -4
         assert f(M.FLAG_ACCUMULATE_DW | 1, 256) == -4
         assert f(M.FLAG_ACCUMULATE_DW, 0) == 0
+    for f in (bwd, routed):
+        assert f(M.FLAG_MX_SEPARATE_DH_QUANT, 256) == -4
+    assert mxb(M.FLAG_ACCUMULATE_DW | M.FLAG_MX_SEPARATE_DH_QUANT, 0) == 0
 
 
 def test_mx_bwd_workspace_too_small(L):
@@ -143,3 +147,24 @@ def test_layer_workspace_size_is_the_larger_part(L):
     assert L.moe_workspace_size(T, k, E, M_cap, d, n, 0, M.FLAG_MXFP8) == m
     assert M.workspace_size(T, k, E, M_cap, d, n, "swiglu", mxfp8=True) == m
     assert L.moe_workspace_size(0, 0, 0, 0, 0, 0, 0, M.FLAG_MXFP8) == 0
+
+
+def test_mx_bwd_workspace_layout(L):
+    """moe_mx_bwd_workspace_layout: 11 sections, 256-byte aligned, in the
+    documented order, sized as the documented shapes, ending within the
+    workspace size; invalid sizes give 0; host-only."""
+    M_cap, d, n = 1024, 256, 128
+    for act, n1 in (("swiglu", 2 * n), ("srelu", n)):
+        lay = M.mx_bwd_workspace_layout(M_cap, d, n, act)
+        sizes = {"dy_q": M_cap * d, "dy_s": M_cap * d // 8, "dy_qT": M_cap * d,
+                 "dy_sT": M_cap * d // 8, "x_qT": M_cap * d, "x_sT": M_cap * d // 8,
+                 "a_sT": M_cap * n // 8, "dh_q": M_cap * n1, "dh_s": M_cap * n1 // 8,
+                 "dh_qT": M_cap * n1, "dh_sT": M_cap * n1 // 8}
+        names = list(M.MX_BWD_SECTIONS)
+        assert lay["bytes"] == M.mx_bwd_workspace_size(M_cap, d, n, act)
+        for a, b in zip(names, names[1:]):
+            assert lay[a] % 256 == 0 and lay[b] >= lay[a] + sizes[a], (a, b)
+        assert lay[names[0]] == 0 and lay[names[-1]] + sizes[names[-1]] <= lay["bytes"]
+    offs = (ctypes.c_size_t * 11)()
+    assert L.moe_mx_bwd_workspace_layout(64, 0, 128, 0, offs) == 0
+    assert L.moe_mx_bwd_workspace_layout(64, 128, 128, 0, None) == 0

@@ -129,7 +129,8 @@ def _layer(seed, counts, d, n, act, tail=64):
     return off, x, H, A, dy, W1, W2
 
 
-def _gpu_bwd(off, x, H, A, dy, W1, W2, act, dW1=None, dW2=None, accumulate_dw=False):
+def _gpu_bwd(off, x, H, A, dy, W1, W2, act, dW1=None, dW2=None, accumulate_dw=False,
+             separate_dh_quant=False, workspace=None):
     M = _M()
     offs = cuda_i32(off)
     _, _, aT, sT, e0 = M.mx_quantize(A, offs)          # the forward's transposed copy of A
@@ -137,10 +138,12 @@ def _gpu_bwd(off, x, H, A, dy, W1, W2, act, dW1=None, dW2=None, accumulate_dw=Fa
     w1_q, w1_s = M.mx_quantize_weights_rowwise(W1)
     mx = dict(a_qT=aT, a_sT=sT, w2_q=w2_q, w2_s=w2_s, w1_q=w1_q, w1_s=w1_s)
     dh, dx, dW1, dW2, err = M.grouped_mlp_bwd_mx(x, H, dy, offs, mx, act, dW1=dW1, dW2=dW2,
-                                                  accumulate_dw=accumulate_dw)
+                                                  accumulate_dw=accumulate_dw,
+                                                  separate_dh_quant=separate_dh_quant,
+                                                  workspace=workspace)
     torch.cuda.synchronize()
     assert int(e0.item()) == 0 and int(err.item()) == 0
-    assert M.last_launch_count() == 8
+    assert M.last_launch_count() == (8 if separate_dh_quant else 7)
     return dh, dx, dW1, dW2
 
 
@@ -246,3 +249,55 @@ def test_mx_bwd_deterministic():
         if p.shape[0] == x.shape[0]:
             p, q = p[:R], q[:R]
         assert torch.equal(p, q)
+
+
+def _dh_sections(ws, lay, M_cap, n1):
+    """dH's MXFP8 copies from the backward's workspace: row-wise codes [M,
+    n1] and row-tile scales, transposed codes [n1, M] and K-tile scales."""
+    sec = lambda nm, nbytes: ws[lay[nm]:lay[nm] + nbytes]
+    return (sec("dh_q", M_cap * n1).view(M_cap, n1), sec("dh_s", M_cap * n1 // 8),
+            sec("dh_qT", M_cap * n1).view(n1, M_cap), sec("dh_sT", M_cap * n1 // 8))
+
+
+FUSE_CASES = [c for c in CASES if c[0] in ("tiles_ragged_empty", "odd_row_blocks", "many_small")]
+
+
+@pytest.mark.parametrize("act", ["swiglu", "geglu", "srelu"])
+@pytest.mark.parametrize("name,counts,d,n", FUSE_CASES, ids=[c[0] for c in FUSE_CASES])
+def test_fused_dact_quantize_transpose(name, counts, d, n, act):
+    """GroupGemm + dActivation + Quantize/Transpose: FC2-dgrad's epilogue
+    writes dH's row-wise MXFP8 codes (row-tile scales) and its group-aware
+    transposed copy (K-tile scales).  On every row and column block inside
+    the experts they equal, bit for bit, (a) the separate tiled quantiser
+    run on the same bf16 dH (the unfused control) and (b) the OCP MX
+    quantiser of the oracle applied to the GPU's own bf16 dH; and every
+    output of the backward equals the unfused control's bit for bit."""
+    from test_gpu_mx import decode_a_scales, decode_k_tiles
+    M = _M()
+    off, x, H, A, dy, W1, W2 = _layer(35, counts, d, n, act)
+    M_cap = x.shape[0]
+    n1 = H.shape[1]
+    R = int(off[-1])
+    lay = M.mx_bwd_workspace_layout(M_cap, d, n, act)
+    wf = torch.full((lay["bytes"],), 0x5A, dtype=torch.uint8, device="cuda")
+    wu = torch.full((lay["bytes"],), 0xA5, dtype=torch.uint8, device="cuda")
+    fused = _gpu_bwd(off, x, H, A, dy, W1, W2, act, workspace=wf)
+    unfused = _gpu_bwd(off, x, H, A, dy, W1, W2, act, separate_dh_quant=True, workspace=wu)
+    for nm, a, b in zip(("dh", "dx", "dW1", "dW2"), fused, unfused):
+        if a.shape[0] == M_cap:
+            a, b = a[:R], b[:R]
+        assert torch.equal(a, b), nm
+    fq, fs, fqT, fsT = _dh_sections(wf, lay, M_cap, n1)
+    uq, us, uqT, usT = _dh_sections(wu, lay, M_cap, n1)
+    assert torch.equal(fq[:R], uq[:R]) and torch.equal(fqT[:, :R], uqT[:, :R])
+    gs_f = decode_a_scales(fs, off, M_cap, n1)[:R]
+    gsT_f = decode_k_tiles(fsT, off, M_cap, n1)[:, :R // 32]
+    assert np.array_equal(gs_f, decode_a_scales(us, off, M_cap, n1)[:R])
+    assert np.array_equal(gsT_f, decode_k_tiles(usT, off, M_cap, n1)[:, :R // 32])
+    gdh = f64(fused[0])[:R]
+    qo, so = X.mx_quantize_rows(gdh)
+    assert np.array_equal(fq[:R].cpu().numpy(), qo)
+    assert np.array_equal(gs_f, so)
+    qTo, sTo = X.mx_quantize_cols(gdh, off)
+    assert np.array_equal(fqT[:, :R].cpu().numpy(), qTo[:, :R])
+    assert np.array_equal(gsT_f, sTo[:, :R // 32])
