@@ -31,7 +31,7 @@ __all__ = [
     "grouped_mlp_bwd_routed", "router_grad_rows", "mx_quantize_weights2", "FLAG_ACCUMULATE_DW",
     "grouped_gemm", "activation", "activation_bwd", "grouped_mlp_fwd_gather",
     "grouped_mlp_bwd_routed_gather", "route_logits", "FLAG_MX_SEPARATE_DH_QUANT",
-    "mx_bwd_workspace_layout",
+    "mx_bwd_workspace_layout", "set_pair_mma",
 ]
 
 ACT = {"swiglu": 0, "geglu": 1, "srelu": 2}
@@ -119,6 +119,8 @@ def lib():
         L.moe_mx_quantize_weights_rowwise.argtypes = [vp, i32, i32, vp, i32, vp, vp, vp]
         L.moe_mx_bwd_workspace_size.restype = sz
         L.moe_mx_bwd_workspace_size.argtypes = [i32, i32, i32, i32]
+        L.moe_set_pair_mma.restype = i32
+        L.moe_set_pair_mma.argtypes = [i32]
         L.moe_mx_bwd_workspace_layout.restype = sz
         L.moe_mx_bwd_workspace_layout.argtypes = [i32, i32, i32, i32, vp]
         L.moe_workspace_size.restype = sz
@@ -562,6 +564,17 @@ def mx_quantize_weights_rowwise(W: torch.Tensor, q: torch.Tensor | None = None,
 
 def mx_bwd_workspace_size(M_cap: int, d: int, n: int, act: str = "swiglu") -> int:
     return int(lib().moe_mx_bwd_workspace_size(M_cap, d, n, ACT[act]))
+
+
+PAIR_NEVER, PAIR_AUTO, PAIR_ALWAYS = 0, 1, 2
+
+
+def set_pair_mma(mode: int) -> int:
+    """moe_set_pair_mma: 0 never, 1 automatic (default), 2 always pair the
+    two CTAs of a cluster with 2-SM MMAs; returns the previous mode."""
+    rc = int(lib().moe_set_pair_mma(int(mode)))
+    _check(rc if rc < 0 else 0, "moe_set_pair_mma")
+    return rc
 
 
 MX_BWD_SECTIONS = ("dy_q", "dy_s", "dy_qT", "dy_sT", "x_qT", "x_sT", "a_sT", "dh_q", "dh_s",

@@ -654,6 +654,11 @@ size_t moe_mx_bwd_workspace_size(int M_cap, int d, int n, int act) {
   return carve_mx_bwd(nullptr, M_cap, d, n1, n).bytes;
 }
 
+int moe_set_pair_mma(int mode) {
+  const int prev = moe::set_pair_mode(mode);
+  return prev < 0 ? MOE_E_ARG : prev;
+}
+
 size_t moe_mx_bwd_workspace_layout(int M_cap, int d, int n, int act, size_t* offs) {
   if (!offs || M_cap < 0 || d <= 0 || n <= 0 || act < MOE_ACT_SWIGLU || act > MOE_ACT_SRELU)
     return 0;

@@ -17,7 +17,15 @@
 //              derivative math, stores to global
 // Two 256-column fp32 accumulators in TMEM let tile i+1's MMAs overlap
 // tile i's epilogue.
+//
+// Pair mode (the ragged-row kinds on experts of 256 rows or more): the two
+// CTAs of a cluster compute a 256 x 256 tile with 2-SM MMAs
+// (tcgen05.mma.cta_group::2, issued by the first CTA): each CTA loads its
+// own 128 rows of A and one 128-column half of B into 32 KB stages, six of
+// them, and holds its 128 rows of the accumulator in its own TMEM.
 #include <cuda_runtime.h>
+
+#include <atomic>
 
 #include "act.cuh"
 #include "gemm.cuh"
@@ -36,6 +44,11 @@ constexpr int MN_BOX_BYTES = 64 * BK * 2;  // one 64(MN) x 64(K) box: 8 KB
 constexpr int NUM_THREADS = 320;
 constexpr int EPI_WARPS = 8;
 constexpr int TMEM_COLS = 2 * BN;
+// pair mode: each CTA's stage holds its 128 rows of A and one 128-column
+// half of B
+constexpr int PAIR_B_BYTES = (BN / 2) * BK * 2;        // 16 KB
+constexpr int PAIR_STAGE_BYTES = A_BYTES + PAIR_B_BYTES;  // 32 KB
+constexpr int PAIR_STAGES = 6;
 
 // Weight-gradient kernels stage their output in shared memory and write it
 // with TMA stores.  Two configurations:
@@ -46,20 +59,21 @@ constexpr int TMEM_COLS = 2 * BN;
 //  * large experts (long reductions, tensor-bound): four stages and one
 //    32 x 32 box per warp (64-byte swizzle).
 // Each also keeps one box of zeros for experts with no rows.
-template <GemmKind KIND, bool SKINNY>
+template <GemmKind KIND, bool SKINNY, bool PAIR = false>
 struct Cfg {
   static constexpr bool W = (KIND == GemmKind::kWgrad);
-  static constexpr int stages = (W && SKINNY) ? 3 : STAGES;
+  static constexpr int stages = PAIR ? ((W && SKINNY) ? 4 : PAIR_STAGES) : (W && SKINNY) ? 3 : STAGES;
+  static constexpr int stage_bytes = PAIR ? PAIR_STAGE_BYTES : STAGE_BYTES;
   static constexpr int box_cols = SKINNY ? 64 : 32;
   static constexpr int box_bytes = 32 * box_cols * 2;
   static constexpr int nbuf = SKINNY ? 2 : 1;
   static constexpr int stg_bytes = W ? (nbuf * EPI_WARPS + 1) * box_bytes : 0;
 };
-template <GemmKind KIND, bool SKINNY>
+template <GemmKind KIND, bool SKINNY, bool PAIR = false>
 constexpr size_t smem_bytes(int E) {
-  return 1024 /*align slack*/ + static_cast<size_t>(Cfg<KIND, SKINNY>::stages) * STAGE_BYTES +
-         Cfg<KIND, SKINNY>::stg_bytes + (2 * Cfg<KIND, SKINNY>::stages + 5) * 8 /*barriers*/ +
-         16 + 2 * (E + 1) * 4 /*scheduler*/;
+  using C = Cfg<KIND, SKINNY, PAIR>;
+  return 1024 /*align slack*/ + static_cast<size_t>(C::stages) * C::stage_bytes + C::stg_bytes +
+         (2 * C::stages + 5) * 8 /*barriers*/ + 16 + 2 * (E + 1) * 4 /*scheduler*/;
 }
 
 // ------------------------------------------------------------ scheduling
@@ -86,15 +100,16 @@ __device__ __forceinline__ int row_blocks(const GemmArgs& g, const int* s_off, i
   return (KIND == GemmKind::kWgrad) ? (g.R + BM - 1) / BM
                                     : (s_off[e + 1] - s_off[e] + BM - 1) / BM;
 }
-template <GemmKind KIND, int CL>
+template <GemmKind KIND, int CL, bool PAIR = false>
 __device__ __forceinline__ int tiles_of_expert(const GemmArgs& g, const int* s_off, int e) {
   const int nt = (g.N + BN - 1) / BN;
   const int mt = row_blocks<KIND>(g, s_off, e);
+  if (PAIR) return ((mt + 1) / 2) * nt;   // 256-row units, also for one row block
   if (CL == 2 && mt == 1) return (nt + 1) / 2;
   return ((mt + CL - 1) / CL) * nt;
 }
 
-template <GemmKind KIND, int CL>
+template <GemmKind KIND, int CL, bool PAIR = false>
 __device__ __forceinline__ Tile decode_tile(const GemmArgs& g, const int* s_off,
                                             const int* s_ts, int t, int rank) {
   // expert e with s_ts[e] <= t < s_ts[e+1]
@@ -109,7 +124,7 @@ __device__ __forceinline__ Tile decode_tile(const GemmArgs& g, const int* s_off,
   const int local = t - s_ts[lo];
   const int nt = (g.N + BN - 1) / BN;
   int mi;
-  if (CL == 2 && row_blocks<KIND>(g, s_off, lo) == 1) {
+  if (!PAIR && CL == 2 && row_blocks<KIND>(g, s_off, lo) == 1) {
     tl.mc = false;
     mi = 0;
     tl.n0 = (2 * local + rank) * BN;
@@ -125,7 +140,7 @@ __device__ __forceinline__ Tile decode_tile(const GemmArgs& g, const int* s_off,
     }
     tl.n0 = ni * BN;
     mi = CL * pm + rank;
-    tl.mc = (CL == 2);
+    tl.mc = !PAIR && (CL == 2);
   }
   if constexpr (KIND == GemmKind::kWgrad) {
     tl.m0 = mi * BM;
@@ -394,7 +409,7 @@ __device__ __forceinline__ void fc1_mx_block(const GemmArgs& g, const Tile& tl, 
 }
 
 // ------------------------------------------------------------ the kernel
-template <GemmKind KIND, int ACT, bool MX, int CL, bool SKINNY, bool GATHER>
+template <GemmKind KIND, int ACT, bool MX, int CL, bool SKINNY, bool GATHER, bool PAIR>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                         const __grid_constant__ CUtensorMap tmB,
@@ -403,16 +418,19 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   constexpr bool B_MN = (KIND == GemmKind::kFc1Act || KIND == GemmKind::kFc2 ||
                          KIND == GemmKind::kWgrad);
   constexpr bool B_3D = (KIND != GemmKind::kWgrad);
-  constexpr uint32_t IDESC = idesc_bf16(BM, BN, A_MN, B_MN);
+  static_assert(!PAIR || (CL == 2 && !GATHER), "pair mode: TMA operands in 2-CTA clusters");
+  // pair mode: one M = 256 MMA over both CTAs' rows
+  constexpr uint32_t IDESC = idesc_bf16(PAIR ? 2 * BM : BM, BN, A_MN, B_MN);
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
-  using C = Cfg<KIND, SKINNY>;
+  using C = Cfg<KIND, SKINNY, PAIR>;
   constexpr int NST = C::stages;
+  constexpr int SBYTES = C::stage_bytes;
   constexpr int BOX = C::box_bytes;
   constexpr int BOXC = C::box_cols;
-  uint8_t* staging = smem + NST * STAGE_BYTES;            // C::nbuf boxes per epilogue warp
+  uint8_t* staging = smem + NST * SBYTES;                 // C::nbuf boxes per epilogue warp
   uint8_t* zero_box = staging + C::nbuf * EPI_WARPS * BOX;  // 32 x BOXC bf16 zeros
   uint64_t* full_bar = reinterpret_cast<uint64_t*>(staging + C::stg_bytes);
   uint64_t* empty_bar = full_bar + NST;
@@ -434,13 +452,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   if (threadIdx.x == 0) {
     for (int i = 0; i < NST; ++i) {
       // gathered operands: lane 0's byte-count arrival plus one cp.async
-      // arrival per producer lane
+      // arrival per producer lane.  Pair mode: the first CTA's full barrier
+      // takes both CTAs' bytes; one commit (multicast) frees a stage in both
       mbar_init(&full_bar[i], GATHER ? 33 : 1);
-      mbar_init(&empty_bar[i], CL);         // one commit from each CTA's MMA
+      mbar_init(&empty_bar[i], PAIR ? 1 : CL);  // one commit from each CTA's MMA
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&tfull_bar[i], 1);
-      mbar_init(&tempty_bar[i], EPI_WARPS);
+      // pair mode: the first CTA's MMA waits for both CTAs' epilogue warps
+      mbar_init(&tempty_bar[i], PAIR ? 2 * EPI_WARPS : EPI_WARPS);
     }
     mbar_init(drain_bar, 1);
     *abort_flag = 0;
@@ -454,7 +474,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       reinterpret_cast<uint4*>(zero_box)[i] = make_uint4(0, 0, 0, 0);
     fence_proxy_async_smem();
   }
-  if (warp == 1) tmem_alloc(tmem_slot, TMEM_COLS);
+  if (warp == 1) {
+    if constexpr (PAIR) tmem_alloc_pair(tmem_slot, TMEM_COLS);
+    else tmem_alloc(tmem_slot, TMEM_COLS);
+  }
   if (warp == 2) {
     // offsets -> smem, made safe: non-decreasing and within [0, M_cap]
     bool bad = false;
@@ -479,7 +502,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     int carry = 0;
     for (int base = 0; base < g.E; base += 32) {
       const int e = base + lane;
-      const int t = (e < g.E) ? tiles_of_expert<KIND, CL>(g, s_off, e) : 0;
+      const int t = (e < g.E) ? tiles_of_expert<KIND, CL, PAIR>(g, s_off, e) : 0;
       int v = t;
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
@@ -560,7 +583,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         cp_async16(box + row * 128 + ((ch ^ (row & 7)) * 16), src, ok_row ? 16u : 0u);
       };
       for (int t = unit0; t < total_tiles && ok; t += unit_step) {
-        const Tile tl = decode_tile<KIND, CL>(g, s_off, s_ts, t, rank);
+        const Tile tl = decode_tile<KIND, CL, PAIR>(g, s_off, s_ts, t, rank);
         int rr[4];
         if constexpr (!A_MN) {
           // K-major A: the tile's 128 rows, the same in every stage
@@ -584,7 +607,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           if (lane == 0) ok = mbar_wait(&empty_bar[stage], phase ^ 1, abort_flag);
           ok = __shfl_sync(0xffffffffu, ok, 0);
           if (!ok) break;
-          uint8_t* sa = smem + stage * STAGE_BYTES;
+          uint8_t* sa = smem + stage * SBYTES;
           uint8_t* sb = sa + A_BYTES;
           uint64_t* fb = &full_bar[stage];
           if constexpr (!A_MN) {
@@ -633,12 +656,48 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           if (++stage == NST) { stage = 0; phase ^= 1; }
         }
       }
-    } else if (lane == 0) {
+    } else if (PAIR && lane == 0) {
+      // pair mode: this CTA's 128 rows of A and its 128-column half of B;
+      // the bytes of both CTAs count on the first CTA's full barrier
+      const uint32_t full0 = mapa_shared(smem_u32(&full_bar[0]), 0);
       for (int t = unit0; t < total_tiles && ok; t += unit_step) {
-        const Tile tl = decode_tile<KIND, CL>(g, s_off, s_ts, t, rank);
+        const Tile tl = decode_tile<KIND, CL, PAIR>(g, s_off, s_ts, t, rank);
         for (int kb = 0; kb < tl.kblocks; ++kb) {
           if (!mbar_wait(&empty_bar[stage], phase ^ 1, abort_flag)) { ok = false; break; }
-          uint8_t* sa = smem + stage * STAGE_BYTES;
+          uint8_t* sa = smem + stage * SBYTES;
+          uint8_t* sb = sa + A_BYTES;
+          const uint32_t fb = full0 + stage * 8;
+          if (rank == 0) mbar_arrive_expect_tx(&full_bar[stage], 2 * SBYTES);
+          if constexpr (A_MN) {
+            // weight gradient: this CTA's 128 output rows of the activation^T
+            const int kr = tl.krow0 + kb * BK;
+            tma_load_2d_pair(sa, &tmA, fb, tl.m0, kr);
+            tma_load_2d_pair(sa + MN_BOX_BYTES, &tmA, fb, tl.m0 + 64, kr);
+          } else {
+            tma_load_2d_pair(sa, &tmA, fb, kb * BK, tl.row0);
+          }
+          const int nh = tl.n0 + (BN / 2) * rank;   // this CTA's half of the tile's columns
+          if constexpr (B_MN) {
+            const int kc = B_3D ? kb * BK : tl.krow0 + kb * BK;
+#pragma unroll
+            for (int i = 0; i < 2; ++i) {
+              if constexpr (B_3D) tma_load_3d_pair(sb + i * MN_BOX_BYTES, &tmB, fb, nh + 64 * i, kc, tl.e);
+              else tma_load_2d_pair(sb + i * MN_BOX_BYTES, &tmB, fb, nh + 64 * i, kc);
+            }
+          } else {
+            tma_load_3d_pair(sb, &tmB, fb, kb * BK, nh, tl.e);
+          }
+          issued[stage] = true;
+          issued_parity[stage] = phase;
+          if (++stage == NST) { stage = 0; phase ^= 1; }
+        }
+      }
+    } else if (lane == 0) {
+      for (int t = unit0; t < total_tiles && ok; t += unit_step) {
+        const Tile tl = decode_tile<KIND, CL, PAIR>(g, s_off, s_ts, t, rank);
+        for (int kb = 0; kb < tl.kblocks; ++kb) {
+          if (!mbar_wait(&empty_bar[stage], phase ^ 1, abort_flag)) { ok = false; break; }
+          uint8_t* sa = smem + stage * SBYTES;
           uint64_t* fb = &full_bar[stage];
           mbar_arrive_expect_tx(fb, STAGE_BYTES);
           if constexpr (A_MN) {
@@ -656,26 +715,36 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       }
     }
     if (!ok && lane == 0) {
-      // give up: wait (bounded) for our copies in flight before exiting
-      for (int i = 0; i < NST; ++i)
-        if (issued[i]) {
-          const uint32_t a = smem_u32(&full_bar[i]);
-          const uint64_t t0 = globaltimer_ns();
-          while (!mbar_try_wait(a, issued_parity[i]) && globaltimer_ns() - t0 < kWaitLimitNs) {}
-        }
+      // give up: wait (bounded) for our copies in flight before exiting (in
+      // pair mode the first CTA's full barriers count both CTAs' copies; the
+      // second CTA waits a fixed 1 ms, far longer than a copy takes)
+      if (PAIR && rank != 0) {
+        const uint64_t t0 = globaltimer_ns();
+        while (globaltimer_ns() - t0 < 1000000ull) {}
+      } else {
+        for (int i = 0; i < NST; ++i)
+          if (issued[i]) {
+            const uint32_t a = smem_u32(&full_bar[i]);
+            const uint64_t t0 = globaltimer_ns();
+            while (!mbar_try_wait(a, issued_parity[i]) && globaltimer_ns() - t0 < kWaitLimitNs) {}
+          }
+      }
     }
     __syncwarp();
-  } else if (warp == 1) {
+  } else if (warp == 1 && (!PAIR || rank == 0)) {
     // ---------------------------------------------------------- MMA issuer
+    // (pair mode: the first CTA's warp issues for both CTAs)
     int stage = 0;
     uint32_t phase = 0;
     int local = 0;
     bool ok = true;
     for (int t = unit0; t < total_tiles && ok; t += unit_step, ++local) {
-      const Tile tl = decode_tile<KIND, CL>(g, s_off, s_ts, t, rank);
+      const Tile tl = decode_tile<KIND, CL, PAIR>(g, s_off, s_ts, t, rank);
       const int buf = local & 1;
       const uint32_t aph = (local >> 1) & 1;
-      if (lane == 0) ok = mbar_wait(&tempty_bar[buf], aph ^ 1, abort_flag);
+      if (lane == 0)
+        ok = PAIR ? mbar_wait_cluster(&tempty_bar[buf], aph ^ 1, abort_flag)
+                  : mbar_wait(&tempty_bar[buf], aph ^ 1, abort_flag);
       ok = __shfl_sync(0xffffffffu, ok, 0);
       if (!ok) break;
       tc_fence_after();
@@ -687,7 +756,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         tc_fence_after();
         // rows gathered with cp.async were written through the generic proxy
         if (GATHER && lane == 0) fence_proxy_async_smem();
-        uint8_t* sa = smem + stage * STAGE_BYTES;
+        uint8_t* sa = smem + stage * SBYTES;
         uint8_t* sb = sa + A_BYTES;
         // In an expert's last reduction block only ceil(klast/16) MMAs touch
         // its rows; the rows after klast up to that 16-row boundary belong to
@@ -698,7 +767,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           if (kb == tl.kblocks - 1 && tl.klast < BK) {
             kk_n = (tl.klast + UK - 1) / UK;
             const int zr = kk_n * UK - tl.klast;
-            const int units = 6 * zr * 8;  // 16-byte units
+            // boxes of 64 rows x 128 bytes: 2 of A and 4 of B (pair mode: 2
+            // of B in each CTA, the second CTA's written through the cluster)
+            constexpr int NBOX = PAIR ? 4 : 6;
+            const int units = NBOX * zr * 8;  // 16-byte units
             for (int u = lane; u < units; u += 32) {
               const int box = u / (zr * 8);
               const int rem = u - box * (zr * 8);
@@ -707,8 +779,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
               uint8_t* p = (box < 2 ? sa + box * MN_BOX_BYTES : sb + (box - 2) * MN_BOX_BYTES) +
                            row * 128 + ch * 16;
               *reinterpret_cast<uint4*>(p) = make_uint4(0, 0, 0, 0);
+              if constexpr (PAIR) st_cluster_zero16(mapa_shared(smem_u32(p), 1));
             }
-            fence_proxy_async_smem();
+            if constexpr (PAIR) {
+              fence_proxy_async_cluster();
+              fence_acq_rel_cluster();
+            } else {
+              fence_proxy_async_smem();
+            }
           }
         }
         __syncwarp();
@@ -719,36 +797,46 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                                      : sdesc_sw128(a0 + kk * 32, 16, 1024);
             const uint64_t bd = B_MN ? sdesc_sw128(b0 + kk * 2048, MN_BOX_BYTES, 1024)
                                      : sdesc_sw128(b0 + kk * 32, 16, 1024);
-            umma_bf16(d_tmem, ad, bd, IDESC, (kb > 0 || kk > 0) ? 1u : 0u);
+            if constexpr (PAIR) umma_bf16_pair(d_tmem, ad, bd, IDESC, (kb > 0 || kk > 0) ? 1u : 0u);
+            else umma_bf16(d_tmem, ad, bd, IDESC, (kb > 0 || kk > 0) ? 1u : 0u);
           }
-          if constexpr (CL == 2) umma_commit_mc(&empty_bar[stage], kPair);  // frees it in both CTAs
+          if constexpr (PAIR) umma_commit_pair_mc(&empty_bar[stage]);      // frees it in both CTAs
+          else if constexpr (CL == 2) umma_commit_mc(&empty_bar[stage], kPair);
           else umma_commit(&empty_bar[stage]);
         }
         __syncwarp();
         if (++stage == NST) { stage = 0; phase ^= 1; }
       }
       if (!ok) break;
-      if (lane == 0) umma_commit(&tfull_bar[buf]);
+      if (lane == 0) {
+        if constexpr (PAIR) umma_commit_pair_mc(&tfull_bar[buf]);   // both CTAs' epilogues
+        else umma_commit(&tfull_bar[buf]);
+      }
       __syncwarp();
     }
     if (!ok && lane == 0) {
       // give up: let every MMA already issued finish before TMEM is freed
-      umma_commit(drain_bar);
+      if constexpr (PAIR) umma_commit_pair(drain_bar);
+      else umma_commit(drain_bar);
       const uint32_t a = smem_u32(drain_bar);
       const uint64_t t0 = globaltimer_ns();
       while (!mbar_try_wait(a, 0) && globaltimer_ns() - t0 < kWaitLimitNs) {}
     }
     __syncwarp();
+  } else if (warp == 1) {
+    // pair mode, second CTA: its MMA warp has nothing to issue
   } else {
     // ---------------------------------------------------------- epilogue
     const int q = warp & 3;            // TMEM lane quadrant of this warp
+    // pair mode: the first CTA's MMA warp waits for this CTA's epilogue too
+    const uint32_t tempty0 = PAIR ? mapa_shared(smem_u32(&tempty_bar[0]), 0) : 0u;
     const int wg = (warp - 2) >> 2;    // warpgroup: columns [wg*128, wg*128+128) of the tile
     const int row_in_tile = q * 32 + lane;
     int local = 0;
     uint32_t stg_slot = 0;
     float amx = 0.f;                   // NVFP4 statistic of this thread's outputs
     for (int t = unit0; t < total_tiles; t += unit_step, ++local) {
-      const Tile tl = decode_tile<KIND, CL>(g, s_off, s_ts, t, rank);
+      const Tile tl = decode_tile<KIND, CL, PAIR>(g, s_off, s_ts, t, rank);
       const int buf = local & 1;
       const uint32_t aph = (local >> 1) & 1;
       bool ok = true;
@@ -861,7 +949,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&tempty_bar[buf]);
+      if (lane == 0) {
+        if (PAIR && rank != 0) mbar_arrive_cluster(tempty0 + buf * 8);
+        else mbar_arrive(&tempty_bar[buf]);
+      }
     }
     if (KIND == GemmKind::kWgrad && lane == 0) bulk_wait_all();  // staged stores done
     if ((KIND == GemmKind::kFc1Act || KIND == GemmKind::kDgradAct) && g.amax != nullptr) {
@@ -879,7 +970,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   if (*abort_flag && threadIdx.x == 0) set_err(g.err, MOE_DEV_TIMEOUT);
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem_base, TMEM_COLS);
+    if constexpr (PAIR) tmem_dealloc_pair(tmem_base, TMEM_COLS);
+    else tmem_dealloc(tmem_base, TMEM_COLS);
   }
 }
 
@@ -888,11 +980,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 constexpr int kCluster = 2;
 constexpr int kMaxDevices = 64;
 
-template <GemmKind KIND, int ACT, bool MX = false, bool SKINNY = false, bool GATHER = false>
+template <GemmKind KIND, int ACT, bool MX = false, bool SKINNY = false, bool GATHER = false,
+          bool PAIR = false>
 cudaError_t launch_t(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tc,
                      const GemmArgs& g, int num_sms, cudaStream_t s) {
-  auto kern = grouped_gemm_kernel<KIND, ACT, MX, kCluster, SKINNY, GATHER>;
-  const size_t smem = smem_bytes<KIND, SKINNY>(MOE_MAX_EXPERTS);
+  auto kern = grouped_gemm_kernel<KIND, ACT, MX, kCluster, SKINNY, GATHER, PAIR>;
+  const size_t smem = smem_bytes<KIND, SKINNY, PAIR>(MOE_MAX_EXPERTS);
   // grid size and shared-memory attribute, set up once per device (a
   // process may drive several devices, one at a time)
   static int grid_of[kMaxDevices] = {0};
@@ -937,7 +1030,36 @@ cudaError_t launch_t(const CUtensorMap& ta, const CUtensorMap& tb, const CUtenso
   return cudaLaunchKernelEx(&cfg, kern, ta, tb, tc, g);
 }
 
+// ragged-row kind in pair mode or not, per activation
+template <GemmKind KIND, bool MX, bool PAIR>
+cudaError_t launch_act(int act, const CUtensorMap& ta, const CUtensorMap& tb,
+                       const CUtensorMap& tc, const GemmArgs& g, int num_sms, cudaStream_t s) {
+  switch (act) {
+    case MOE_ACT_SWIGLU: return launch_t<KIND, MOE_ACT_SWIGLU, MX, false, false, PAIR>(ta, tb, tc, g, num_sms, s);
+    case MOE_ACT_GEGLU: return launch_t<KIND, MOE_ACT_GEGLU, MX, false, false, PAIR>(ta, tb, tc, g, num_sms, s);
+    case MOE_ACT_SRELU: return launch_t<KIND, MOE_ACT_SRELU, MX, false, false, PAIR>(ta, tb, tc, g, num_sms, s);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+std::atomic<int> g_pair_mode{kPairAuto};
+
 }  // namespace
+
+int set_pair_mode(int mode) {
+  if (mode < kPairNever || mode > kPairAlways) return -1;
+  return g_pair_mode.exchange(mode);
+}
+
+bool use_pair(GemmKind kind, const GemmArgs& g) {
+  if (g.gather_pair != nullptr) return false;
+  const int m = g_pair_mode.load();
+  if (m == kPairNever) return false;
+  if (m == kPairAlways) return true;
+  // experts of 256 rows or more on average: a 256-row unit rarely idles a
+  // CTA, and the halved stages let six of them cover the load latency
+  return static_cast<long long>(g.M_cap) >= static_cast<long long>(kPairRows) * g.E;
+}
 
 bool wgrad_skinny(const GemmArgs& g) {
   return static_cast<long long>(g.M_cap) < static_cast<long long>(kSkinnyRows) * g.E;
@@ -983,11 +1105,16 @@ cudaError_t launch_grouped_gemm(GemmKind kind, int act, const CUtensorMap& ta,
   }
   if (mx) {
     if (kind != GemmKind::kFc1Act) return cudaErrorInvalidValue;
-    switch (act) {
-      case MOE_ACT_SWIGLU: return launch_t<GemmKind::kFc1Act, MOE_ACT_SWIGLU, true>(ta, tb, tc, g, num_sms, s);
-      case MOE_ACT_GEGLU: return launch_t<GemmKind::kFc1Act, MOE_ACT_GEGLU, true>(ta, tb, tc, g, num_sms, s);
-      case MOE_ACT_SRELU: return launch_t<GemmKind::kFc1Act, MOE_ACT_SRELU, true>(ta, tb, tc, g, num_sms, s);
-      default: return cudaErrorInvalidValue;
+    return use_pair(kind, g) ? launch_act<GemmKind::kFc1Act, true, true>(act, ta, tb, tc, g, num_sms, s)
+                             : launch_act<GemmKind::kFc1Act, true, false>(act, ta, tb, tc, g, num_sms, s);
+  }
+  if (use_pair(kind, g)) {
+    switch (kind) {
+      case GemmKind::kFc1Act: return launch_act<GemmKind::kFc1Act, false, true>(act, ta, tb, tc, g, num_sms, s);
+      case GemmKind::kDgradAct: return launch_act<GemmKind::kDgradAct, false, true>(act, ta, tb, tc, g, num_sms, s);
+      case GemmKind::kFc2: return launch_t<GemmKind::kFc2, 0, false, false, false, true>(ta, tb, tc, g, num_sms, s);
+      case GemmKind::kDgrad: return launch_t<GemmKind::kDgrad, 0, false, false, false, true>(ta, tb, tc, g, num_sms, s);
+      default: break;   // kWgrad: below
     }
   }
 #define MOE_ACT_SWITCH(KIND)                                                         \
@@ -1003,6 +1130,10 @@ cudaError_t launch_grouped_gemm(GemmKind kind, int act, const CUtensorMap& ta,
     case GemmKind::kFc2: return launch_t<GemmKind::kFc2, 0>(ta, tb, tc, g, num_sms, s);
     case GemmKind::kDgrad: return launch_t<GemmKind::kDgrad, 0>(ta, tb, tc, g, num_sms, s);
     case GemmKind::kWgrad:
+      if (use_pair(kind, g))
+        return wgrad_skinny(g)
+                   ? launch_t<GemmKind::kWgrad, 0, false, true, false, true>(ta, tb, tc, g, num_sms, s)
+                   : launch_t<GemmKind::kWgrad, 0, false, false, false, true>(ta, tb, tc, g, num_sms, s);
       return wgrad_skinny(g) ? launch_t<GemmKind::kWgrad, 0, false, true>(ta, tb, tc, g, num_sms, s)
                              : launch_t<GemmKind::kWgrad, 0, false, false>(ta, tb, tc, g, num_sms, s);
   }

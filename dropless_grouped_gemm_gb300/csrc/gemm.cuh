@@ -89,6 +89,16 @@ cudaError_t launch_grouped_gemm(GemmKind kind, int act, const CUtensorMap& ta,
 constexpr int kSkinnyRows = 512;
 bool wgrad_skinny(const GemmArgs& g);
 
+// Pair mode (2-SM MMAs over 256-row units) for the ragged-row kinds:
+// kPairAuto uses it when the average rows per expert (M_cap / E, known on
+// the host) reach kPairRows; kPairNever / kPairAlways force the choice (for
+// measurement and tests).  set_pair_mode returns the previous mode, or -1
+// for an unknown one.
+constexpr int kPairNever = 0, kPairAuto = 1, kPairAlways = 2;
+constexpr int kPairRows = 256;
+int set_pair_mode(int mode);
+bool use_pair(GemmKind kind, const GemmArgs& g);
+
 // The activation and its derivative as separate memory passes (act.cu):
 // A = act(H) and dH = act'(H; dA) over the rows below offsets[E] (at most
 // rows_cap); H is [rows, n1], A / dA are [rows, n].

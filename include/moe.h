@@ -568,6 +568,21 @@ size_t moe_mx_bwd_workspace_size(int M_cap, int d, int n, int act);
 size_t moe_mx_bwd_workspace_layout(int M_cap, int d, int n, int act, size_t* offs);
 
 /*
+ * moe_set_pair_mma - how the grouped GEMMs of the ragged-row kinds (FC1,
+ * FC2, FC2-dgrad, FC1-dgrad) pair the two CTAs of a cluster, process-wide:
+ *   0  never: each CTA computes its own 128 x 256 tiles (1-SM MMAs; the two
+ *      CTAs share B tiles through TMA multicast);
+ *   1  automatic (the default): 2-SM MMAs over 256 x 256 tiles (each CTA
+ *      loads 128 rows of A and half of B; tcgen05.mma.cta_group::2) when the
+ *      average rows per expert, M_cap / E, reach 256, else as 0;
+ *   2  always 2-SM.
+ * Results are identical across modes; the choice is for speed (and for
+ * measuring one against the other).  Returns the previous mode, or
+ * MOE_E_ARG for an unknown one.  Host-only; affects launches made after it.
+ */
+int moe_set_pair_mma(int mode);
+
+/*
  * moe_workspace_size - device scratch for one layer's calls: the larger of
  * moe_route_workspace_size(T, k, E) and, when flags has MOE_FLAG_MXFP8,
  * moe_mx_bwd_workspace_size(M_cap, d, n, act).  One buffer of this size
