@@ -31,7 +31,9 @@ def main():
     ap.add_argument("--rows-per-expert", type=int, default=None)
     ap.add_argument("--tokens", type=int, default=None)
     ap.add_argument("--experts", type=int, default=None,
-                    help="fewer experts (routed workloads), for captures that must stay small")
+                    help="fewer experts, for captures that must stay small (routed workloads: "
+                         "the same tokens over fewer experts; identity-routed ones: the first "
+                         "E experts with their rows, every launch's work scaled by E / E_full)")
     ap.add_argument("--what", choices=["fwd", "bwd", "step"], default="step")
     ap.add_argument("--reps", type=int, default=3)
     a = ap.parse_args()
@@ -44,6 +46,8 @@ def main():
         w = WL.scaled(w, T=a.tokens)
     if a.experts is not None and w.routing != "identity":
         w = WL.scaled(w, E=a.experts, k=min(w.k, a.experts))
+    if a.experts is not None and w.routing == "identity":
+        w = WL.scaled(w, E=a.experts, T=a.experts * (w.T // w.E))
     inp, o = BE.make_inputs(w, "cuda")
     step = BE.make_step(w, inp, o)
     if a.what == "step":
