@@ -479,6 +479,9 @@ int moe_grouped_mlp_fwd(const moe_bf16* x_perm, const int32_t* offsets, int E, i
     moe::MxGemmArgs q{};
     q.offsets = offsets; q.E = E; q.M_cap = M_cap; q.K = n; q.N = d;
     q.a_s = mx->a_s; q.b_s = mx->w2_s; q.out = y_perm; q.ldo = d; q.err = err;
+    // scale sizes: A's row tiles, W2's column tiles (for the pair mode's TMA)
+    q.a_s_bytes = static_cast<long long>(M_cap) * n / 8;
+    q.b_s_bytes = static_cast<long long>(E) * n * d / 32;
     q.q_out = mx->y_q; q.s_out = mx->y_q ? mx->y_s : nullptr;
     ev_begin(s);
     e = moe::launch_mx_gemm(moe::MxKind::kFc2, 0, ta, tw2, ta, q, sms, s);
@@ -886,6 +889,8 @@ int moe_grouped_mlp_bwd_mx(const moe_bf16* x_perm, const moe_bf16* h_saved,
   g.offsets = offsets; g.E = E; g.M_cap = M_cap; g.K = d; g.N = n;
   g.a_s = ws.dy_s; g.b_s = mx->w2_s; g.out = dh; g.ldo = n1; g.aux = h_saved; g.ld_aux = n1;
   g.err = err;
+  g.a_s_bytes = static_cast<long long>(M_cap) * d / 8;
+  g.b_s_bytes = static_cast<long long>(E) * n * d / 32;
   if (fuse_dh) {
     g.dh_q = ws.dh_q; g.dh_s = ws.dh_s; g.dh_qT = ws.dh_qT; g.dh_sT = ws.dh_sT; g.n1 = n1;
   }
@@ -897,6 +902,8 @@ int moe_grouped_mlp_bwd_mx(const moe_bf16* x_perm, const moe_bf16* h_saved,
   moe::MxGemmArgs gw2{};
   gw2.offsets = offsets; gw2.E = E; gw2.M_cap = M_cap; gw2.R = n; gw2.N = d;
   gw2.a_s = ws.a_sT; gw2.b_s = ws.dy_sT; gw2.err = err;
+  gw2.a_s_bytes = static_cast<long long>(M_cap) * n / 8;
+  gw2.b_s_bytes = static_cast<long long>(M_cap) * d / 8;
   gw2.out = dW2; gw2.accumulate = accumulate;
   e = mx_gemm(moe::MxKind::kWgrad, 0, t_aT, t_dyT, t_dw2, gw2, sms, s);
   if (e != cudaSuccess) return MOE_E_CUDA;
@@ -904,6 +911,8 @@ int moe_grouped_mlp_bwd_mx(const moe_bf16* x_perm, const moe_bf16* h_saved,
   moe::MxGemmArgs gd{};
   gd.offsets = offsets; gd.E = E; gd.M_cap = M_cap; gd.K = n1; gd.N = d;
   gd.a_s = ws.dh_s; gd.b_s = mx->w1_s; gd.out = dx_perm; gd.ldo = d; gd.err = err;
+  gd.a_s_bytes = static_cast<long long>(M_cap) * n1 / 8;
+  gd.b_s_bytes = static_cast<long long>(E) * d * n1 / 32;
   gd.q_out = mx->dx_q; gd.s_out = mx->dx_q ? mx->dx_s : nullptr;
   e = mx_gemm(moe::MxKind::kDgrad, 0, t_dh, t_w1, t_dh, gd, sms, s);
   if (e != cudaSuccess) return MOE_E_CUDA;
@@ -911,6 +920,8 @@ int moe_grouped_mlp_bwd_mx(const moe_bf16* x_perm, const moe_bf16* h_saved,
   moe::MxGemmArgs gw1{};
   gw1.offsets = offsets; gw1.E = E; gw1.M_cap = M_cap; gw1.R = d; gw1.N = n1;
   gw1.a_s = ws.x_sT; gw1.b_s = ws.dh_sT; gw1.err = err;
+  gw1.a_s_bytes = static_cast<long long>(M_cap) * d / 8;
+  gw1.b_s_bytes = static_cast<long long>(M_cap) * n1 / 8;
   gw1.out = dW1; gw1.accumulate = accumulate;
   e = mx_gemm(moe::MxKind::kWgrad, 0, t_xT, t_dhT, t_dw1, gw1, sms, s);
   if (e != cudaSuccess) return MOE_E_CUDA;

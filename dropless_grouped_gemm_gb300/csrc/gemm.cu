@@ -1046,6 +1046,8 @@ std::atomic<int> g_pair_mode{kPairAuto};
 
 }  // namespace
 
+int pair_mode() { return g_pair_mode.load(); }
+
 int set_pair_mode(int mode) {
   if (mode < kPairNever || mode > kPairAlways) return -1;
   return g_pair_mode.exchange(mode);

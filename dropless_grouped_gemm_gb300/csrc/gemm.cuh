@@ -97,6 +97,7 @@ bool wgrad_skinny(const GemmArgs& g);
 constexpr int kPairNever = 0, kPairAuto = 1, kPairAlways = 2;
 constexpr int kPairRows = 256;
 int set_pair_mode(int mode);
+int pair_mode();
 bool use_pair(GemmKind kind, const GemmArgs& g);
 
 // The activation and its derivative as separate memory passes (act.cu):

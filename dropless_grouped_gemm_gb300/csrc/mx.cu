@@ -6,9 +6,14 @@
 // epilogue.  [TE] "Transformer Engine이 제공하는 세 가지 구성 요소": an MXFP8
 // grouped GEMM; [TE] "다음 단계: NVFP4, GEMM 융합 양자화, A2A 오버랩": the
 // backward's GroupGemm + dActivation + Quantize/Transpose.
+#include <cuda.h>
 #include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <mutex>
 
 #include "act.cuh"
+#include "gemm.cuh"
 #include "mx.cuh"
 #include "mxgemm.cuh"
 #include "ptx.cuh"
@@ -39,6 +44,12 @@ constexpr int QBOX_BYTES = 32 * 64 * 2;           // staged output box: 32 rows 
 // warpgroup's 128 accumulator columns here (after the scale columns) so
 // that only 64 of them occupy registers once the accumulator is released
 constexpr int QSTASH_TMEM = 320;
+// Pair mode (2-SM MMAs, M = 256 over the CTA pair, N = 256): each CTA's stage
+// holds its 128 rows of A, its 128-column half of B and three scale chunks
+// (its A rows' and both B halves'), all loaded by TMA onto the first CTA's
+// full barrier
+constexpr int QP_SF_OFF = QA_BYTES + QBH_BYTES;    // 32 KB
+constexpr int QP_STAGE_BYTES = QP_SF_OFF + 2048;   // 34 KB
 
 // TMEM holds one 256-column accumulator (the scale columns leave no room
 // for a second); the epilogue moves it to registers and releases it at once,
@@ -46,16 +57,18 @@ constexpr int QSTASH_TMEM = 320;
 // gradient stages its output for TMA stores (one box per epilogue warp plus
 // a box of zeros for experts with no rows) and keeps three stages; the other
 // kinds keep four.
-template <MxKind KIND>
+template <MxKind KIND, bool PAIR = false>
 struct QCfg {
   static constexpr bool W = (KIND == MxKind::kWgrad);
-  static constexpr int stages = W ? 3 : 4;
+  static constexpr int stages = PAIR ? (W ? 5 : 6) : (W ? 3 : 4);
+  static constexpr int stage_bytes = PAIR ? QP_STAGE_BYTES : QSTAGE_BYTES;
   static constexpr int stg_bytes = W ? (QEPI_WARPS + 1) * QBOX_BYTES : 0;
 };
-template <MxKind KIND>
+template <MxKind KIND, bool PAIR = false>
 constexpr size_t mx_smem_bytes(int E) {
-  return 1024 + static_cast<size_t>(QCfg<KIND>::stages) * QSTAGE_BYTES + QCfg<KIND>::stg_bytes +
-         (2 * QCfg<KIND>::stages + 4) * 8 + 16 + 2 * (E + 1) * 4;
+  using C = QCfg<KIND, PAIR>;
+  return 1024 + static_cast<size_t>(C::stages) * C::stage_bytes + C::stg_bytes +
+         (2 * C::stages + 4) * 8 + 16 + 2 * (E + 1) * 4;
 }
 
 // Instruction descriptor, kind::mxf8f6f4 block-scaled: A/B E4M3 (format 0),
@@ -132,15 +145,15 @@ __device__ __forceinline__ int mx_row_blocks(const MxGemmArgs& g, const int* s_o
   return (KIND == MxKind::kWgrad) ? g.R / QBM : (s_off[e + 1] - s_off[e] + QBM - 1) / QBM;
 }
 
-template <MxKind KIND>
+template <MxKind KIND, bool PAIR = false>
 __device__ __forceinline__ int mx_tiles_of_expert(const MxGemmArgs& g, const int* s_off, int e) {
   const int nt = (g.N + QBN - 1) / QBN;
   const int mt = mx_row_blocks<KIND>(g, s_off, e);
-  if (mt == 1) return (nt + 1) / 2;
-  return ((mt + 1) / 2) * nt;
+  if (!PAIR && mt == 1) return (nt + 1) / 2;
+  return ((mt + 1) / 2) * nt;   // pair mode: 256-row units, also for one row block
 }
 
-template <MxKind KIND>
+template <MxKind KIND, bool PAIR = false>
 __device__ __forceinline__ QTile mx_decode(const MxGemmArgs& g, const int* s_off, const int* s_ts,
                                            int t, int rank) {
   int lo = 0, hi = g.E - 1;
@@ -155,13 +168,13 @@ __device__ __forceinline__ QTile mx_decode(const MxGemmArgs& g, const int* s_off
   QTile tl;
   tl.e = lo;
   int mi;
-  if (mt == 1) {
+  if (!PAIR && mt == 1) {
     tl.mc = false;
     mi = 0;
     tl.n0 = (2 * local + rank) * QBN;
   } else {
     const int pm = local / nt;
-    tl.mc = true;
+    tl.mc = !PAIR;
     mi = 2 * pm + rank;
     tl.n0 = (local - pm * nt) * QBN;
   }
@@ -328,20 +341,24 @@ __device__ __forceinline__ void mx_dact_quant_block(const MxGemmArgs& g, int tl_
 // issuer (tcgen05.mma ... block_scale; the scale chunks of a stage go to TMEM
 // with tcgen05.cp; its commit frees the stage in both CTAs), warps 2-9
 // epilogue in two warpgroups, one per 128-column half of the tile.
-template <MxKind KIND, int ACT, bool QOUT>
+template <MxKind KIND, int ACT, bool QOUT, bool PAIR>
 __global__ void __launch_bounds__(QTHREADS, 1)
     mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                   const __grid_constant__ CUtensorMap tmC, const MxGemmArgs g) {
+                   const __grid_constant__ CUtensorMap tmC,
+                   const __grid_constant__ CUtensorMap tmSA,
+                   const __grid_constant__ CUtensorMap tmSB, const MxGemmArgs g) {
   constexpr bool W = (KIND == MxKind::kWgrad);
   constexpr bool B_MN = (KIND == MxKind::kFc2);
-  constexpr uint32_t IDESC = idesc_mx(QBM, QHN, false, B_MN);
-  constexpr int NST = QCfg<KIND>::stages;
+  // pair mode: one M = 256, N = 256 MMA per 32 of K over both CTAs
+  constexpr uint32_t IDESC = PAIR ? idesc_mx(2 * QBM, QBN, false, B_MN) : idesc_mx(QBM, QHN, false, B_MN);
+  constexpr int NST = QCfg<KIND, PAIR>::stages;
+  constexpr int SBYTES = QCfg<KIND, PAIR>::stage_bytes;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
-  uint8_t* staging = smem + NST * QSTAGE_BYTES;               // one box per epilogue warp
+  uint8_t* staging = smem + NST * SBYTES;                     // one box per epilogue warp
   uint8_t* zero_box = staging + QEPI_WARPS * QBOX_BYTES;
-  uint64_t* full_bar = reinterpret_cast<uint64_t*>(staging + QCfg<KIND>::stg_bytes);
+  uint64_t* full_bar = reinterpret_cast<uint64_t*>(staging + QCfg<KIND, PAIR>::stg_bytes);
   uint64_t* empty_bar = full_bar + NST;
   uint64_t* tfull_bar = empty_bar + NST;
   uint64_t* tempty_bar = tfull_bar + 1;
@@ -358,23 +375,33 @@ __global__ void __launch_bounds__(QTHREADS, 1)
   if (threadIdx.x == 0) {
     for (int i = 0; i < NST; ++i) {
       mbar_init(&full_bar[i], 1);
-      mbar_init(&empty_bar[i], QCL);  // one commit from each CTA's MMA warp
+      // one commit from each CTA's MMA warp; pair mode: the first CTA's
+      // commit, multicast to both
+      mbar_init(&empty_bar[i], PAIR ? 1 : QCL);
     }
     mbar_init(tfull_bar, 1);
-    mbar_init(tempty_bar, QEPI_WARPS);
+    // pair mode: the first CTA's MMA waits for both CTAs' epilogue warps
+    mbar_init(tempty_bar, PAIR ? 2 * QEPI_WARPS : QEPI_WARPS);
     mbar_init(drain_bar, 1);
     *abort_flag = 0;
     fence_mbar_init();
     prefetch_tmap(&tmA);
     prefetch_tmap(&tmB);
     if (W) prefetch_tmap(&tmC);
+    if (PAIR) {
+      prefetch_tmap(&tmSA);
+      prefetch_tmap(&tmSB);
+    }
   }
   if (W && warp >= 2) {  // epilogue threads clear the zero box
     for (int i = threadIdx.x - 64; i < QBOX_BYTES / 16; i += 32 * QEPI_WARPS)
       reinterpret_cast<uint4*>(zero_box)[i] = make_uint4(0, 0, 0, 0);
     fence_proxy_async_smem();
   }
-  if (warp == 1) tmem_alloc(tmem_slot, QTMEM_COLS);
+  if (warp == 1) {
+    if constexpr (PAIR) tmem_alloc_pair(tmem_slot, QTMEM_COLS);
+    else tmem_alloc(tmem_slot, QTMEM_COLS);
+  }
   if (warp == 2) {
     // offsets: non-decreasing multiples of 32 within [0, M_cap]
     bool bad = false;
@@ -396,7 +423,7 @@ __global__ void __launch_bounds__(QTHREADS, 1)
     int carry = 0;
     for (int base = 0; base < g.E; base += 32) {
       const int e = base + lane;
-      const int t = (e < g.E) ? mx_tiles_of_expert<KIND>(g, s_off, e) : 0;
+      const int t = (e < g.E) ? mx_tiles_of_expert<KIND, PAIR>(g, s_off, e) : 0;
       int v = t;
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
@@ -414,7 +441,62 @@ __global__ void __launch_bounds__(QTHREADS, 1)
   const uint32_t tmem_base = *tmem_slot;
   const int total = s_ts[g.E];
 
-  if (warp == 0) {
+  if (warp == 0 && PAIR) {
+    // ---------------------------------------------------------- producer (pair)
+    // this CTA's 128 rows of A, its 128-column half of B and three scale
+    // chunks; every byte counts on the first CTA's full barrier
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      const long long kc_n = g.K / QBK, nq = g.N / QHN, rq = g.R / QBM;
+      const uint32_t full0 = mapa_shared(smem_u32(&full_bar[0]), 0);
+      for (int t = unit0; t < total && ok; t += unit_step) {
+        const QTile tl = mx_decode<KIND, PAIR>(g, s_off, s_ts, t, rank);
+        for (int kb = 0; kb < tl.kblocks; ++kb) {
+          if (!mbar_wait(&empty_bar[stage], phase ^ 1, abort_flag)) { ok = false; break; }
+          uint8_t* sa = smem + stage * SBYTES;
+          uint8_t* sb = sa + QA_BYTES;
+          uint8_t* ssf = sa + QP_SF_OFF;
+          const uint32_t fb = full0 + stage * 8;
+          if (rank == 0) mbar_arrive_expect_tx(&full_bar[stage], 2 * (QA_BYTES + QBH_BYTES + 3 * 512));
+          const int nh = tl.n0 + rank * QHN;   // this CTA's half of B
+          long long ca, cb0, cstep;           // scale chunks: A, B half 0, half 1 - half 0
+          if constexpr (W) {
+            const int kc = tl.k0 + kb * QBK;
+            tma_load_2d_pair(sa, &tmA, fb, kc, tl.m0);
+            tma_load_2d_pair(sb, &tmB, fb, kc, nh);
+            ca = static_cast<long long>(kc / 32) * rq + tl.m0 / QBM;
+            cb0 = static_cast<long long>(kc / 32) * nq + tl.n0 / QHN;
+            cstep = 1;
+          } else {
+            tma_load_2d_pair(sa, &tmA, fb, kb * QBK, tl.row0);
+            ca = static_cast<long long>(tl.row0 / 32) * kc_n + kb;
+            if constexpr (B_MN) {
+              tma_load_3d_pair(sb, &tmB, fb, nh, kb * QBK, tl.e);
+              cb0 = (static_cast<long long>(tl.e) * kc_n + kb) * nq + tl.n0 / QHN;
+              cstep = 1;
+            } else {
+              tma_load_2d_pair(sb, &tmB, fb, kb * QBK, tl.e * g.N + nh);
+              cb0 = ((static_cast<long long>(tl.e) * g.N + tl.n0) / QHN) * kc_n + kb;
+              cstep = kc_n;
+            }
+          }
+          // chunks past a buffer read as zeros (rows or columns that are not stored)
+          tma_load_2d_pair(ssf, &tmSA, fb, 0, static_cast<int>(2 * ca));
+          tma_load_2d_pair(ssf + 512, &tmSB, fb, 0, static_cast<int>(2 * cb0));
+          tma_load_2d_pair(ssf + 1024, &tmSB, fb, 0, static_cast<int>(2 * (cb0 + cstep)));
+          if (++stage == NST) { stage = 0; phase ^= 1; }
+        }
+      }
+      if (!ok) {
+        // give up: the first CTA's full barriers count both CTAs' copies,
+        // which this CTA cannot wait on; 1 ms is far longer than a copy takes
+        const uint64_t t0 = globaltimer_ns();
+        while (globaltimer_ns() - t0 < 1000000ull) {}
+      }
+    }
+  } else if (warp == 0) {
     // ---------------------------------------------------------- producer
     if (lane == 0) {
       int stage = 0;
@@ -425,10 +507,10 @@ __global__ void __launch_bounds__(QTHREADS, 1)
       bool ok = true;
       const long long kc_n = g.K / QBK, nq = g.N / QHN, rq = g.R / QBM;
       for (int t = unit0; t < total && ok; t += unit_step) {
-        const QTile tl = mx_decode<KIND>(g, s_off, s_ts, t, rank);
+        const QTile tl = mx_decode<KIND, PAIR>(g, s_off, s_ts, t, rank);
         for (int kb = 0; kb < tl.kblocks; ++kb) {
           if (!mbar_wait(&empty_bar[stage], phase ^ 1, abort_flag)) { ok = false; break; }
-          uint8_t* sa = smem + stage * QSTAGE_BYTES;
+          uint8_t* sa = smem + stage * SBYTES;
           uint8_t* sb = sa + QA_BYTES;
           uint8_t* ssf = sa + QSF_OFF;
           uint64_t* fb = &full_bar[stage];
@@ -489,6 +571,61 @@ __global__ void __launch_bounds__(QTHREADS, 1)
           }
       }
     }
+  } else if (warp == 1 && PAIR) {
+    // ---------------------------------------------------------- MMA issuer (pair)
+    // the first CTA's warp copies both CTAs' scale chunks into their TMEM and
+    // issues the M = 256 MMAs; the second CTA's MMA warp has nothing to do
+    if (rank == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      int local = 0;
+      bool ok = true;
+      for (int t = unit0; t < total && ok; t += unit_step, ++local) {
+        const QTile tl = mx_decode<KIND, PAIR>(g, s_off, s_ts, t, rank);
+        if (lane == 0) ok = mbar_wait_cluster(tempty_bar, (local & 1) ^ 1, abort_flag);
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (!ok) break;
+        tc_fence_after();
+        for (int kb = 0; kb < tl.kblocks; ++kb) {
+          if (lane == 0) ok = mbar_wait(&full_bar[stage], phase, abort_flag);
+          ok = __shfl_sync(0xffffffffu, ok, 0);
+          if (!ok) break;
+          tc_fence_after();
+          if (lane == 0) {
+            uint8_t* sa = smem + stage * SBYTES;
+            uint8_t* sb = sa + QA_BYTES;
+            uint8_t* ssf = sa + QP_SF_OFF;
+            const uint32_t sf_t = tmem_base + QSF_TMEM + stage * QSF_COLS;
+            // A rows' scales, then both B halves' in consecutive columns
+            tmem_cp_sf_pair(sf_t, sdesc_sf(smem_u32(ssf)));
+            tmem_cp_sf_pair(sf_t + 4, sdesc_sf(smem_u32(ssf + 512)));
+            tmem_cp_sf_pair(sf_t + 8, sdesc_sf(smem_u32(ssf + 1024)));
+            const uint32_t a0 = smem_u32(sa), b0 = smem_u32(sb);
+            const int kk_n = (W && kb == tl.kblocks - 1) ? tl.klast / 32 : QBK / 32;
+            for (int kk = 0; kk < kk_n; ++kk) {
+              const uint64_t ad = sdesc_sw128(a0 + kk * 32, 16, 1024);
+              const uint64_t bd = B_MN ? sdesc_sw128(b0 + kk * 4096, QBH_BYTES, 1024)
+                                       : sdesc_sw128(b0 + kk * 32, 16, 1024);
+              const uint32_t id = IDESC | (static_cast<uint32_t>(kk) << 29) | (static_cast<uint32_t>(kk) << 4);
+              umma_mx_pair(tmem_base, ad, bd, id, sf_t, sf_t + 4, (kb > 0 || kk > 0) ? 1u : 0u);
+            }
+            umma_commit_pair_mc(&empty_bar[stage]);   // frees the stage in both CTAs
+          }
+          __syncwarp();
+          if (++stage == NST) { stage = 0; phase ^= 1; }
+        }
+        if (!ok) break;
+        if (lane == 0) umma_commit_pair_mc(tfull_bar);   // both CTAs' epilogues
+        __syncwarp();
+      }
+      if (!ok && lane == 0) {
+        umma_commit_pair(drain_bar);
+        const uint32_t a = smem_u32(drain_bar);
+        const uint64_t t0 = globaltimer_ns();
+        while (!mbar_try_wait(a, 0) && globaltimer_ns() - t0 < kWaitLimitNs) {}
+      }
+      __syncwarp();
+    }
   } else if (warp == 1) {
     // ---------------------------------------------------------- MMA issuer
     int stage = 0;
@@ -496,7 +633,7 @@ __global__ void __launch_bounds__(QTHREADS, 1)
     int local = 0;
     bool ok = true;
     for (int t = unit0; t < total && ok; t += unit_step, ++local) {
-      const QTile tl = mx_decode<KIND>(g, s_off, s_ts, t, rank);
+      const QTile tl = mx_decode<KIND, PAIR>(g, s_off, s_ts, t, rank);
       // the accumulator is free once the epilogue has read the previous tile
       if (lane == 0) ok = mbar_wait(tempty_bar, (local & 1) ^ 1, abort_flag);
       ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -508,7 +645,7 @@ __global__ void __launch_bounds__(QTHREADS, 1)
         if (!ok) break;
         tc_fence_after();
         if (lane == 0 && !tl.ghost) {
-          uint8_t* sa = smem + stage * QSTAGE_BYTES;
+          uint8_t* sa = smem + stage * SBYTES;
           uint8_t* sb = sa + QA_BYTES;
           uint8_t* ssf = sa + QSF_OFF;
           const uint32_t sf_t = tmem_base + QSF_TMEM + stage * QSF_COLS;
@@ -553,9 +690,15 @@ __global__ void __launch_bounds__(QTHREADS, 1)
     const int wg = (warp - 2) >> 2;      // 128-column half of the tile
     const int r = q * 32 + lane;
     uint8_t* my_box = staging + (warp - 2) * QBOX_BYTES;
+    // pair mode: the first CTA's MMA warp waits for this CTA's epilogue too
+    const uint32_t tempty0 = PAIR ? mapa_shared(smem_u32(tempty_bar), 0) : 0u;
+    auto release = [&]() {
+      if (PAIR && rank != 0) mbar_arrive_cluster(tempty0);
+      else mbar_arrive(tempty_bar);
+    };
     int local = 0;
     for (int t = unit0; t < total; t += unit_step, ++local) {
-      const QTile tl = mx_decode<KIND>(g, s_off, s_ts, t, rank);
+      const QTile tl = mx_decode<KIND, PAIR>(g, s_off, s_ts, t, rank);
       bool ok = true;
       if (lane == 0) ok = mbar_wait(tfull_bar, local & 1, abort_flag);
       if (!__shfl_sync(0xffffffffu, ok, 0)) break;
@@ -585,7 +728,7 @@ __global__ void __launch_bounds__(QTHREADS, 1)
         }
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(tempty_bar);
+        if (lane == 0) release();
         // offsets are multiples of 32: a warp's 32 rows are all valid or none
         if (!mine || q * 32 >= tl.rows) continue;
         constexpr int BLK = (ACT == MOE_ACT_SRELU) ? 32 : 16;   // dA columns per dH block
@@ -617,7 +760,7 @@ __global__ void __launch_bounds__(QTHREADS, 1)
       // release the accumulator: the next tile's MMAs may start
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(tempty_bar);
+      if (lane == 0) release();
       if (!mine) continue;
       const int col0 = tl.n0 + wg * QHN;
       if constexpr (W) {
@@ -685,15 +828,46 @@ __global__ void __launch_bounds__(QTHREADS, 1)
   if (*abort_flag && threadIdx.x == 0) set_err(g.err, MOE_DEV_TIMEOUT);
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem_base, QTMEM_COLS);
+    if constexpr (PAIR) tmem_dealloc_pair(tmem_base, QTMEM_COLS);
+    else tmem_dealloc(tmem_base, QTMEM_COLS);
   }
 }
 
-template <MxKind KIND, int ACT, bool QOUT = false>
+// 2-D u8 map over a scale buffer seen as rows of 256 bytes; a box of two
+// rows is one 512-byte chunk (pair mode loads the chunks with TMA)
+PFN_cuTensorMapEncodeTiled_v12000 mx_encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+bool map_scale_chunks(CUtensorMap* m, const uint8_t* base, long long bytes) {
+  auto fn = mx_encode_fn();
+  if (!fn || base == nullptr || bytes < 512 || bytes % 256) return false;
+  cuuint64_t gdim[2] = {256, static_cast<cuuint64_t>(bytes / 256)};
+  cuuint64_t gstride[1] = {256};
+  cuuint32_t bdim[2] = {256, 2}, estr[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(base), gdim, gstride, bdim,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <MxKind KIND, int ACT, bool QOUT = false, bool PAIR = false>
 cudaError_t launch_mx_t(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tc,
                         const MxGemmArgs& g, int num_sms, cudaStream_t st) {
-  auto kern = mx_gemm_kernel<KIND, ACT, QOUT>;
-  const size_t smem = mx_smem_bytes<KIND>(MOE_MAX_EXPERTS);
+  auto kern = mx_gemm_kernel<KIND, ACT, QOUT, PAIR>;
+  const size_t smem = mx_smem_bytes<KIND, PAIR>(MOE_MAX_EXPERTS);
+  CUtensorMap tsa = ta, tsb = ta;   // any valid maps when not in pair mode
+  if (PAIR && (!map_scale_chunks(&tsa, g.a_s, g.a_s_bytes) ||
+               !map_scale_chunks(&tsb, g.b_s, g.b_s_bytes)))
+    return cudaErrorInvalidValue;
   // grid size and shared-memory attribute, set up once per device and
   // instantiation
   static int grid_of[64] = {0};
@@ -724,7 +898,24 @@ cudaError_t launch_mx_t(const CUtensorMap& ta, const CUtensorMap& tb, const CUte
     grid = QCL * ((clusters > 0 && clusters < most) ? clusters : most);
   }
   cfg.gridDim = dim3(grid);
-  return cudaLaunchKernelEx(&cfg, kern, ta, tb, tc, g);
+  return cudaLaunchKernelEx(&cfg, kern, ta, tb, tc, tsa, tsb, g);
+}
+
+// pair mode for this launch: as the bf16 GEMM's (moe_set_pair_mma), and only
+// with the scale buffers' sizes known
+bool mx_use_pair(const MxGemmArgs& g) {
+  if (g.a_s_bytes <= 0 || g.b_s_bytes <= 0) return false;
+  const int m = pair_mode();
+  if (m == kPairNever) return false;
+  if (m == kPairAlways) return true;
+  return static_cast<long long>(g.M_cap) >= static_cast<long long>(kPairRows) * g.E;
+}
+
+template <MxKind KIND, int ACT, bool QOUT = false>
+cudaError_t launch_mx(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tc,
+                      const MxGemmArgs& g, int num_sms, cudaStream_t st) {
+  return mx_use_pair(g) ? launch_mx_t<KIND, ACT, QOUT, true>(ta, tb, tc, g, num_sms, st)
+                        : launch_mx_t<KIND, ACT, QOUT, false>(ta, tb, tc, g, num_sms, st);
 }
 
 }  // namespace
@@ -736,27 +927,27 @@ cudaError_t launch_mx_gemm(MxKind kind, int act, const CUtensorMap& ta, const CU
     // the quantising epilogue (GroupGemm + Quantize) is its own instantiation,
     // so that the plain one keeps its registers
     case MxKind::kFc2:
-      return g.q_out ? launch_mx_t<MxKind::kFc2, 0, true>(ta, tb, tc, g, num_sms, st)
-                     : launch_mx_t<MxKind::kFc2, 0>(ta, tb, tc, g, num_sms, st);
+      return g.q_out ? launch_mx<MxKind::kFc2, 0, true>(ta, tb, tc, g, num_sms, st)
+                     : launch_mx<MxKind::kFc2, 0>(ta, tb, tc, g, num_sms, st);
     case MxKind::kDgrad:
-      return g.q_out ? launch_mx_t<MxKind::kDgrad, 0, true>(ta, tb, tc, g, num_sms, st)
-                     : launch_mx_t<MxKind::kDgrad, 0>(ta, tb, tc, g, num_sms, st);
-    case MxKind::kWgrad: return launch_mx_t<MxKind::kWgrad, 0>(ta, tb, tc, g, num_sms, st);
+      return g.q_out ? launch_mx<MxKind::kDgrad, 0, true>(ta, tb, tc, g, num_sms, st)
+                     : launch_mx<MxKind::kDgrad, 0>(ta, tb, tc, g, num_sms, st);
+    case MxKind::kWgrad: return launch_mx<MxKind::kWgrad, 0>(ta, tb, tc, g, num_sms, st);
     case MxKind::kDgradAct:
       if (g.dh_q != nullptr) {
         // GroupGemm + dActivation + Quantize/Transpose
         if (!g.dh_s || !g.dh_qT || !g.dh_sT || g.n1 <= 0 || g.n1 % 128) return cudaErrorInvalidValue;
         switch (act) {
-          case MOE_ACT_SWIGLU: return launch_mx_t<MxKind::kDgradAct, MOE_ACT_SWIGLU, true>(ta, tb, tc, g, num_sms, st);
-          case MOE_ACT_GEGLU: return launch_mx_t<MxKind::kDgradAct, MOE_ACT_GEGLU, true>(ta, tb, tc, g, num_sms, st);
-          case MOE_ACT_SRELU: return launch_mx_t<MxKind::kDgradAct, MOE_ACT_SRELU, true>(ta, tb, tc, g, num_sms, st);
+          case MOE_ACT_SWIGLU: return launch_mx<MxKind::kDgradAct, MOE_ACT_SWIGLU, true>(ta, tb, tc, g, num_sms, st);
+          case MOE_ACT_GEGLU: return launch_mx<MxKind::kDgradAct, MOE_ACT_GEGLU, true>(ta, tb, tc, g, num_sms, st);
+          case MOE_ACT_SRELU: return launch_mx<MxKind::kDgradAct, MOE_ACT_SRELU, true>(ta, tb, tc, g, num_sms, st);
           default: return cudaErrorInvalidValue;
         }
       }
       switch (act) {
-        case MOE_ACT_SWIGLU: return launch_mx_t<MxKind::kDgradAct, MOE_ACT_SWIGLU>(ta, tb, tc, g, num_sms, st);
-        case MOE_ACT_GEGLU: return launch_mx_t<MxKind::kDgradAct, MOE_ACT_GEGLU>(ta, tb, tc, g, num_sms, st);
-        case MOE_ACT_SRELU: return launch_mx_t<MxKind::kDgradAct, MOE_ACT_SRELU>(ta, tb, tc, g, num_sms, st);
+        case MOE_ACT_SWIGLU: return launch_mx<MxKind::kDgradAct, MOE_ACT_SWIGLU>(ta, tb, tc, g, num_sms, st);
+        case MOE_ACT_GEGLU: return launch_mx<MxKind::kDgradAct, MOE_ACT_GEGLU>(ta, tb, tc, g, num_sms, st);
+        case MOE_ACT_SRELU: return launch_mx<MxKind::kDgradAct, MOE_ACT_SRELU>(ta, tb, tc, g, num_sms, st);
         default: return cudaErrorInvalidValue;
       }
   }

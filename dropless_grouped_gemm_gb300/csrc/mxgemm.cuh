@@ -42,6 +42,8 @@ struct MxGemmArgs {
   int R;                   // kWgrad: output rows per expert (multiple of 128)
   const uint8_t* a_s;      // A scales
   const uint8_t* b_s;      // B scales
+  long long a_s_bytes;     // sizes of the two scale buffers (pair mode loads their
+  long long b_s_bytes;     // chunks with TMA; 0: pair mode is not used)
   uint16_t* out;           // ragged-row kinds: [M_cap, ldo] bf16
   long long ldo;
   const uint16_t* aux;     // kDgradAct: H [M_cap, ld_aux]

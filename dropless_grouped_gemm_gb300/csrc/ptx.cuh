@@ -308,6 +308,27 @@ __device__ __forceinline__ void umma_bf16_pair(uint32_t d_tmem, uint64_t a_desc,
       "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
+// block-scaled 2-SM MMA (E4M3 x E4M3, E8M0 scales per 32 of K), issued by
+// the pair's first CTA; each CTA's scale columns hold its own A rows' scales
+// and the B scales of every output column
+__device__ __forceinline__ void umma_mx_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                             uint32_t idesc, uint32_t sfa, uint32_t sfb,
+                                             uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::mxf8f6f4.block_scale.scale_vec::1X "
+      "[%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa), "r"(sfb), "r"(accumulate)
+      : "memory");
+}
+// shared memory -> TMEM copy of a 512-byte scale chunk in both CTAs of the
+// pair (each from its own shared memory at the descriptor's address into its
+// own TMEM at taddr), issued by the pair's first CTA
+__device__ __forceinline__ void tmem_cp_sf_pair(uint32_t taddr, uint64_t sdesc) {
+  asm volatile("tcgen05.cp.cta_group::2.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc)
+               : "memory");
+}
 // arrive once on the barrier at this offset in both CTAs of the pair when
 // the pair's earlier MMAs have completed
 __device__ __forceinline__ void umma_commit_pair_mc(uint64_t* bar) {

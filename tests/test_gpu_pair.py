@@ -147,3 +147,43 @@ def test_pair_mxfp8_fc1_codes_equal_single():
     from test_gpu_mx import decode_a_scales
     assert np.array_equal(decode_a_scales(b0["a_s"], off, M_cap, n)[:R],
                           decode_a_scales(b1["a_s"], off, M_cap, n)[:R])
+
+
+MX_CASES = [
+    # name, counts (multiples of 32), d, n
+    ("mx_one_unit", [256], 256, 128),
+    ("mx_odd_row_blocks", [384, 0, 96], 384, 128),
+    ("mx_ragged_k", [160, 0, 96, 288], 256, 128),
+]
+
+
+@pytest.mark.parametrize("act", ["swiglu", "srelu"])
+@pytest.mark.parametrize("name,counts,d,n", MX_CASES, ids=[c[0] for c in MX_CASES])
+def test_mx_pair_equals_single(name, counts, d, n, act):
+    """The block-scaled GEMMs in pair mode (M = 256 MMAs over the CTA pair;
+    each CTA's TMEM gets its own A rows' scales and both B halves' scales,
+    loaded by TMA) give the single-CTA kernels' outputs bit for bit: the
+    forward's block-scaled FC2, and the MXFP8 backward's FC2-dgrad + dAct +
+    quantisation, both weight gradients and FC1-dgrad."""
+    import dropless_grouped_gemm_gb300 as M
+    from test_gpu_mx_bwd import _gpu_bwd, _layer
+    off, x, H, A, dy, W1, W2 = _layer(44, counts, d, n, act)
+    E = len(counts)
+    R = int(off[-1])
+    M_cap = x.shape[0]
+    outs = []
+    for mode in (0, 2):
+        M.set_pair_mma(mode)
+        buf = M.mx_buffers(E, n, d, M_cap, "cuda")
+        M.mx_quantize_weights(W2, buf["w2_q"], buf["w2_s"])
+        Wf = (W.w1_plain(44, E, d, n, 0.05, "cuda") if act == "srelu" else
+              W.w1_interleaved(44, E, d, n, 0.05, "cuda"))
+        h, a, y, err = M.grouped_mlp_fwd(x, cuda_i32(off), Wf, W2, act, save_h=True, mx=buf)
+        torch.cuda.synchronize()
+        assert int(err.item()) == 0
+        outs.append((y[:R].clone(),) + tuple(t.clone() for t in
+                                              _gpu_bwd(off, x, H, A, dy, W1, W2, act)))
+    for nm, p, q in zip(("Y", "dH", "dX", "dW1", "dW2"), outs[1], outs[0]):
+        if p.shape[0] == M_cap:
+            p, q = p[:R], q[:R]
+        assert torch.equal(p, q), f"{name}/{act} {nm}: MXFP8 pair mode differs from single-CTA tiles"
