@@ -41,9 +41,10 @@ constexpr int QSF_TMEM = QBN;                     // scale columns after the acc
 constexpr int QSF_COLS = 12;                      // a stage's three chunks, 4 columns each
 constexpr int QBOX_BYTES = 32 * 64 * 2;           // staged output box: 32 rows x 64 bf16
 // The quantising FC2-dgrad epilogue parks the second half of each
-// warpgroup's 128 accumulator columns here (after the scale columns) so
-// that only 64 of them occupy registers once the accumulator is released
-constexpr int QSTASH_TMEM = 320;
+// warpgroup's 128 accumulator columns here (after the scale columns of up
+// to six stages, 256..327) so that only 64 of them occupy registers once the
+// accumulator is released: columns 384..511
+constexpr int QSTASH_TMEM = 384;
 // Pair mode (2-SM MMAs, M = 256 over the CTA pair, N = 256): each CTA's stage
 // holds its 128 rows of A, its 128-column half of B and three scale chunks
 // (its A rows' and both B halves'), all loaded by TMA onto the first CTA's
@@ -63,6 +64,10 @@ struct QCfg {
   static constexpr int stages = PAIR ? (W ? 5 : 6) : (W ? 3 : 4);
   static constexpr int stage_bytes = PAIR ? QP_STAGE_BYTES : QSTAGE_BYTES;
   static constexpr int stg_bytes = W ? (QEPI_WARPS + 1) * QBOX_BYTES : 0;
+  // TMEM: accumulator, then each stage's scale columns, then the stash
+  static_assert(QSF_TMEM + stages * QSF_COLS <= QSTASH_TMEM &&
+                    QSTASH_TMEM + 2 * 64 <= QTMEM_COLS,
+                "TMEM columns of the scales and the stash overlap");
 };
 template <MxKind KIND, bool PAIR = false>
 constexpr size_t mx_smem_bytes(int E) {
@@ -901,21 +906,26 @@ cudaError_t launch_mx_t(const CUtensorMap& ta, const CUtensorMap& tb, const CUte
   return cudaLaunchKernelEx(&cfg, kern, ta, tb, tc, tsa, tsb, g);
 }
 
-// pair mode for this launch: as the bf16 GEMM's (moe_set_pair_mma), and only
-// with the scale buffers' sizes known
-bool mx_use_pair(const MxGemmArgs& g) {
+// pair mode for this launch (moe_set_pair_mma), only with the scale buffers'
+// sizes known.  Automatic: always for the ragged-row kinds, whose 34 KB
+// stages beat the single-CTA tiles' 50 KB even on a layer of one-row-block
+// experts (Zipf MXFP8 training layer, 128 rows per expert on average: FC2
+// 1.03 -> 0.86 ms, FC2-dgrad 1.01 -> 0.85, FC1-dgrad 1.84 -> 1.45); the
+// weight gradients from 256 rows per expert on average, as the bf16 GEMM
+// (on that layer they measured 1.84 / 3.64 ms single against 1.87 / 3.71).
+bool mx_use_pair(MxKind kind, const MxGemmArgs& g) {
   if (g.a_s_bytes <= 0 || g.b_s_bytes <= 0) return false;
   const int m = pair_mode();
   if (m == kPairNever) return false;
-  if (m == kPairAlways) return true;
+  if (m == kPairAlways || kind != MxKind::kWgrad) return true;
   return static_cast<long long>(g.M_cap) >= static_cast<long long>(kPairRows) * g.E;
 }
 
 template <MxKind KIND, int ACT, bool QOUT = false>
 cudaError_t launch_mx(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tc,
                       const MxGemmArgs& g, int num_sms, cudaStream_t st) {
-  return mx_use_pair(g) ? launch_mx_t<KIND, ACT, QOUT, true>(ta, tb, tc, g, num_sms, st)
-                        : launch_mx_t<KIND, ACT, QOUT, false>(ta, tb, tc, g, num_sms, st);
+  return mx_use_pair(KIND, g) ? launch_mx_t<KIND, ACT, QOUT, true>(ta, tb, tc, g, num_sms, st)
+                              : launch_mx_t<KIND, ACT, QOUT, false>(ta, tb, tc, g, num_sms, st);
 }
 
 }  // namespace

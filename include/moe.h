@@ -568,13 +568,14 @@ size_t moe_mx_bwd_workspace_size(int M_cap, int d, int n, int act);
 size_t moe_mx_bwd_workspace_layout(int M_cap, int d, int n, int act, size_t* offs);
 
 /*
- * moe_set_pair_mma - how the grouped GEMMs of the ragged-row kinds (FC1,
- * FC2, FC2-dgrad, FC1-dgrad) pair the two CTAs of a cluster, process-wide:
+ * moe_set_pair_mma - how the grouped GEMMs (bf16 and block-scaled MXFP8)
+ * pair the two CTAs of a cluster, process-wide:
  *   0  never: each CTA computes its own 128 x 256 tiles (1-SM MMAs; the two
  *      CTAs share B tiles through TMA multicast);
  *   1  automatic (the default): 2-SM MMAs over 256 x 256 tiles (each CTA
  *      loads 128 rows of A and half of B; tcgen05.mma.cta_group::2) when the
- *      average rows per expert, M_cap / E, reach 256, else as 0;
+ *      average rows per expert, M_cap / E, reach 256, else as 0; the
+ *      block-scaled MXFP8 GEMMs other than the weight gradients always;
  *   2  always 2-SM.
  * Results are identical across modes; the choice is for speed (and for
  * measuring one against the other).  Returns the previous mode, or

@@ -189,3 +189,90 @@ def test_mx_weight_gradients_small_expert_and_empty(run):
     for e in [int(e) for e in range(w.E) if counts[e] == 0][:3]:
         assert float(o["dW1"][e].abs().max()) == 0.0
         assert float(o["dW2"][e].abs().max()) == 0.0
+
+
+BAL = "balanced_e8_m4096_k8192_n4096_mxfp8_train"
+
+
+@pytest.fixture(scope="module")
+def bal_run():
+    import dropless_grouped_gemm_gb300 as M
+    M.lib()
+    w = WL.WORKLOADS[BAL]
+    inp, o = BE.make_inputs(w, "cuda")
+    step = BE.make_step(w, inp, o)
+    step()
+    torch.cuda.synchronize()
+    assert int(o["err"].item()) == 0
+    yield w, inp, o
+    del inp, o
+    torch.cuda.empty_cache()
+
+
+def _bal_rows(w, key, std, rows):
+    idx = (torch.as_tensor(rows, dtype=torch.int64)[:, None] * w.d +
+           torch.arange(w.d, dtype=torch.int64)[None, :]).cuda()
+    return f64(WL.normal_at(idx, key, std))
+
+
+def test_mx_balanced_rows_each_gemm_on_its_inputs(bal_run):
+    """The balanced MXFP8 training step (E=8 x 4096 rows, d=8192, 2n=4096;
+    pair mode, six-stage reductions of 64 steps): sampled rows of experts 0
+    and 5.  A against the oracle from x; each block-scaled GEMM on the
+    GPU's own stored operands, quantised by the oracle: Y (FC2 from A), dH
+    (FC2-dgrad + dAct from dY and H), dX (FC1-dgrad from dH); the fused
+    FC1 epilogue's codes of A and FC2-dgrad's bf16 dH round trip."""
+    w, inp, o = bal_run
+    m = w.T // w.E
+    rng = np.random.default_rng(7)
+    for e in (0, 5):
+        W1, W2 = _expert_weights(w, e)
+        rows = e * m + np.sort(rng.choice(m, 4, replace=False))
+        x = _bal_rows(w, (w.cfg_id, WL.X, 0), w.x_std, rows)
+        o1 = np.array([0, len(rows)])
+        _, A, _ = O.grouped_mlp_fwd(x, o1, W1[None], W2[None], w.act, round_out=False)
+        r = torch.as_tensor(rows).cuda()
+        ga, gh, gdh = f64(o["a"][r]), f64(o["h"][r]), f64(o["dh"][r])
+        gdy = f64(inp["dy_perm"][r])
+        qa, sa = X.mx_quantize_rows(ga)
+        qw, sw = X.mx_quantize_weights(W2[None])
+        Y = X.mx_fc2(qa, sa, qw, sw, o1)
+        dyq, dys = X.mx_quantize_rows(gdy)
+        w2q, w2s = X.mx_quantize_rows(W2)
+        dH = O.act_backward(gh, X.mx_dgrad(dyq, dys, w2q[None], w2s[None], o1), w.act)
+        dhq, dhs = X.mx_quantize_rows(gdh)
+        w1q, w1s = X.mx_quantize_rows(W1)
+        dX = X.mx_dgrad(dhq, dhs, w1q[None], w1s[None], o1)
+        assert_rms_close(ga, A, f"balanced MX e{e} A")
+        assert_rms_close(f64(o["y_perm"][r]), Y, f"balanced MX e{e} Y")
+        assert_rms_close(gdh, dH, f"balanced MX e{e} dH")
+        assert_rms_close(f64(o["dx_perm"][r]), dX, f"balanced MX e{e} dX")
+        assert np.array_equal(o["mx"]["a_q"][r].cpu().numpy(), qa)
+
+
+def test_mx_balanced_weight_gradient_entries(bal_run):
+    """dW1[e][k, c] = sum over the expert's 4096 rows of deq(x^T)[k] deq(dH^T)[c]
+    and dW2[e][j, c] = sum deq(A^T)[j] deq(dY^T)[c], for sampled (k | j, c),
+    from the GPU's own bf16 dH and A and the generator's x and dY, each
+    column quantised in 32-row blocks of the expert by the oracle."""
+    w, inp, o = bal_run
+    m = w.T // w.E
+    e = 3
+    rows = np.arange(e * m, (e + 1) * m)
+    r = torch.as_tensor(rows).cuda()
+    rng = np.random.default_rng(8)
+    ks = np.sort(rng.choice(w.d, 16, replace=False))
+    cs = np.sort(rng.choice(w.n1, 16, replace=False))
+    js = np.sort(rng.choice(w.n, 16, replace=False))
+    cd = np.sort(rng.choice(w.d, 16, replace=False))
+    o1 = np.array([0, m])
+    x = f64(inp["x_perm"][r][:, torch.as_tensor(ks).cuda()])
+    gdh = f64(o["dh"][r][:, torch.as_tensor(cs).cuda()])
+    ga = f64(o["a"][r][:, torch.as_tensor(js).cuda()])
+    gdy = f64(inp["dy_perm"][r][:, torch.as_tensor(cd).cuda()])
+    want1 = X.mx_wgrad(*X.mx_quantize_cols(x, o1), *X.mx_quantize_cols(gdh, o1), o1)[0]
+    want2 = X.mx_wgrad(*X.mx_quantize_cols(ga, o1), *X.mx_quantize_cols(gdy, o1), o1)[0]
+    got1 = f64(o["dW1"][e][torch.as_tensor(ks).cuda()][:, torch.as_tensor(cs).cuda()])
+    got2 = f64(o["dW2"][e][torch.as_tensor(js).cuda()][:, torch.as_tensor(cd).cuda()])
+    assert_rms_close(got1, want1, "balanced MX dW1 entries")
+    assert_rms_close(got2, want2, "balanced MX dW2 entries")

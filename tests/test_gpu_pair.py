@@ -154,6 +154,10 @@ MX_CASES = [
     ("mx_one_unit", [256], 256, 128),
     ("mx_odd_row_blocks", [384, 0, 96], 384, 128),
     ("mx_ragged_k", [160, 0, 96, 288], 256, 128),
+    # reductions of 8 stages (K = 1024) over several units: every one of the
+    # six stages' scale columns is live while an epilogue parks accumulator
+    # columns in TMEM (the two must not share columns)
+    ("mx_long_k", [512, 512, 256], 1024, 256),
 ]
 
 
