@@ -362,6 +362,23 @@ def make_step(w, inp, o):
             return n
         return step_mx
 
+    if not w.backward:
+        def step_fwd():
+            # forward-only layer: routing layout, permute, expert MLP, combine
+            n = 0
+            r = M.route_offsets(inp["topk_idx"], w.E, w.align, w.M_cap, out=o["route"],
+                                workspace=o["ws"])
+            n += M.last_launch_count()
+            M.permute(inp["x"], r["pair_of_row"], k, out=o["x_perm"])
+            n += M.last_launch_count()
+            M.grouped_mlp_fwd(o["x_perm"], r["offsets"], inp["W1"], inp["W2"], act, a=o["a"],
+                              y_perm=o["y_perm"], err=o["err"])
+            n += M.last_launch_count()
+            M.unpermute(o["y_perm"], r["row_of_pair"], T, k, probs=inp["probs"], out=o["out"])
+            n += M.last_launch_count()
+            return n
+        return step_fwd
+
     if w.gather:
         def step_gather():
             # the permutes fused into the GEMMs' loads ([Sonic] "Gather
@@ -431,6 +448,8 @@ def event_names(w):
         return KERNELS_FWD + KERNELS_BWD
     if w.mxfp8:
         return ["route", "permute", "mx_quantize_weights"] + KERNELS_FWD + ["combine"]
+    if not w.backward:
+        return ["route", "permute"] + KERNELS_FWD + ["combine"]
     if w.gather:
         return (["route"] + KERNELS_FWD + ["combine"] + KERNELS_BWD +
                 ["router_grad_rows", "unpermute_bwd"])
@@ -467,7 +486,7 @@ def oracle_step(w, x, dy, W1, W2, off):
         O.mx_fc2(qa, sa, qw, sw, off)
         if w.backward:
             OX.mx_grouped_mlp_bwd(x, H, A, dy, off, W1, W2, w.act)
-    else:
+    elif w.backward:
         O.grouped_mlp_bwd(x, H, A, dy, off, W1, W2, w.act)
 
 
@@ -552,7 +571,7 @@ def run_reference(args, w):
     fwd, bwd = useful_flops(w, rows)
     v = (fwd + bwd) / dt / 1e12
     sample = (f"{rows} rows of expert 0 ({w.d}x{w.n1} W1, {w.n}x{w.d} W2), oracle float64 "
-              f"{'fwd (MXFP8 FC2)' if w.mxfp8 and not w.backward else 'fwd+bwd'}"
+              f"{('fwd (MXFP8 FC2)' if w.mxfp8 else 'fwd') if not w.backward else 'fwd+bwd'}"
               f"{' MXFP8' if w.mxfp8 and w.backward else ''} per step")
     line = {"impl": "reference", "metric": METRIC, "value": v, "unit": "TFLOP/s",
             "n_gpus": ws, "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3,
@@ -702,7 +721,7 @@ def main():
         v, dt = time_oracle(w, args.cpu_rows)
         cpu = {"value": v, "unit": "TFLOP/s", "cores": cpu_cores(), "kind": "oracle",
                "sample": f"{args.cpu_rows} rows of expert 0, float64 "
-                         f"{'fwd (MXFP8 FC2)' if w.mxfp8 and not w.backward else 'fwd+bwd'}"
+                         f"{('fwd (MXFP8 FC2)' if w.mxfp8 else 'fwd') if not w.backward else 'fwd+bwd'}"
                          f"{' MXFP8' if w.mxfp8 and w.backward else ''} ({dt:.1f} s)"}
 
     if int(o["err"].item()) != 0:   # graph, end-to-end and fusion legs share the error word
@@ -861,6 +880,8 @@ def step_description(w):
     if w.mxfp8:
         return ("route + permute + W2 MXFP8 quantise + fwd (FC1 + MX epilogue, block-scaled FC2) "
                 "+ combine")
+    if not w.backward:
+        return "route + permute + fwd + combine"
     if w.gather:
         return ("route + fwd reading x through the routing map (grouped_mlp_fwd_gather) + "
                 "combine + bwd with the router gradient inside the expert MLP, reading x and dO "
@@ -914,7 +935,7 @@ def run_e2e(w, inp, o, step, steps, flops):
     if w.routing == "identity":
         names_in = ["x_perm", "dy_perm", "offsets"]
         out_names = ["dx_perm", "dW1", "dW2"]
-    elif w.mxfp8 and not w.backward:
+    elif not w.backward:
         names_in = ["x", "topk_idx", "probs"]
         out_names = ["out"]
     else:
