@@ -162,6 +162,14 @@ bool map_out3(CUtensorMap* m, const void* p, int E, int rows, int cols, bool wid
                   wide ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B);
 }
 
+// [rows, cols] bf16 output written by staged TMA stores of FC2 / FC1-dgrad:
+// box 32 cols x 32 rows, 64-byte swizzle
+bool map_out2(CUtensorMap* m, const void* p, int rows, int cols) {
+  const uint64_t dims[2] = {static_cast<uint64_t>(cols), static_cast<uint64_t>(rows)};
+  const uint32_t box[2] = {32, 32};
+  return make_map(m, p, 2, dims, box, false, CU_TENSOR_MAP_SWIZZLE_64B);
+}
+
 int cuda_rc(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_E_CUDA; }
 
 int check_mlp_sizes(int E, int M_cap, int d, int n) {
@@ -234,7 +242,10 @@ int bwd_gemms(const moe_bf16* x_perm, const moe_bf16* h_saved, const moe_bf16* a
   moe::GemmArgs gd{};
   gd.offsets = offsets; gd.E = E; gd.M_cap = M_cap; gd.K = n1; gd.N = d;
   gd.out = dx_perm; gd.ldo = d; gd.err = err;
-  e = gemm(moe::GemmKind::kDgrad, 0, t_dh_k, t_w1_k, t_dh_k, gd, sms, s);
+  CUtensorMap t_dx;
+  if (!map_out2(&t_dx, dx_perm, M_cap, d)) return MOE_E_CUDA;
+  gd.tma_out = 1;
+  e = gemm(moe::GemmKind::kDgrad, 0, t_dh_k, t_w1_k, t_dx, gd, sms, s);
   if (e != cudaSuccess) return MOE_E_CUDA;
   // 4. dW1_e = X_e^T dH_e
   moe::GemmArgs gw1{};
@@ -493,7 +504,10 @@ int moe_grouped_mlp_fwd(const moe_bf16* x_perm, const int32_t* offsets, int E, i
   moe::GemmArgs g2{};
   g2.offsets = offsets; g2.E = E; g2.M_cap = M_cap; g2.K = n; g2.N = d; g2.R = 0;
   g2.out = y_perm; g2.ldo = d; g2.err = err;
-  e = gemm(moe::GemmKind::kFc2, 0, ta, tw2, ta, g2, sms, s);
+  CUtensorMap ty;
+  if (!map_out2(&ty, y_perm, M_cap, d)) return MOE_E_CUDA;
+  g2.tma_out = 1;
+  e = gemm(moe::GemmKind::kFc2, 0, ta, tw2, ty, g2, sms, s);
   if (e != cudaSuccess) return MOE_E_CUDA;
   g_last_launches = 2;
   return MOE_OK;
@@ -720,7 +734,10 @@ int moe_grouped_mlp_fwd_gather(const moe_bf16* x, int T, int k, const int32_t* p
   moe::GemmArgs g2{};
   g2.offsets = offsets; g2.E = E; g2.M_cap = M_cap; g2.K = n; g2.N = d; g2.R = 0;
   g2.out = y_perm; g2.ldo = d; g2.err = err;
-  e = gemm(moe::GemmKind::kFc2, 0, ta, tw2, ta, g2, sms, s);
+  CUtensorMap ty;
+  if (!map_out2(&ty, y_perm, M_cap, d)) return MOE_E_CUDA;
+  g2.tma_out = 1;
+  e = gemm(moe::GemmKind::kFc2, 0, ta, tw2, ty, g2, sms, s);
   if (e != cudaSuccess) return MOE_E_CUDA;
   g_last_launches = 2;
   return MOE_OK;
@@ -748,8 +765,11 @@ int moe_grouped_gemm(const moe_bf16* a, const int32_t* offsets, int E, int M_cap
   moe::GemmArgs g{};
   g.offsets = offsets; g.E = E; g.M_cap = M_cap; g.K = K; g.N = N;
   g.out = out; g.ldo = N; g.err = err;
+  CUtensorMap to;
+  if (!map_out2(&to, out, M_cap, N)) return MOE_E_CUDA;
+  g.tma_out = 1;
   const cudaError_t e = gemm(b_layout == MOE_B_KN ? moe::GemmKind::kFc2 : moe::GemmKind::kDgrad, 0,
-                             ta, tb, ta, g, sms, s);
+                             ta, tb, to, g, sms, s);
   if (e != cudaSuccess) return MOE_E_CUDA;
   g_last_launches = 1;
   return MOE_OK;

@@ -64,10 +64,15 @@ struct Cfg {
   static constexpr bool W = (KIND == GemmKind::kWgrad);
   static constexpr int stages = PAIR ? ((W && SKINNY) ? 4 : PAIR_STAGES) : (W && SKINNY) ? 3 : STAGES;
   static constexpr int stage_bytes = PAIR ? PAIR_STAGE_BYTES : STAGE_BYTES;
+  // FC2 and FC1-dgrad store their bf16 output through one staged 32 x 32
+  // box per epilogue warp (their reductions are short enough that plain
+  // stores left the epilogue longer than the next tile's MMAs)
+  static constexpr bool STO = (KIND == GemmKind::kFc2 || KIND == GemmKind::kDgrad);
   static constexpr int box_cols = SKINNY ? 64 : 32;
   static constexpr int box_bytes = 32 * box_cols * 2;
   static constexpr int nbuf = SKINNY ? 2 : 1;
-  static constexpr int stg_bytes = W ? (nbuf * EPI_WARPS + 1) * box_bytes : 0;
+  static constexpr int stg_bytes =
+      W ? (nbuf * EPI_WARPS + 1) * box_bytes : (STO ? EPI_WARPS * box_bytes : 0);
 };
 template <GemmKind KIND, bool SKINNY, bool PAIR = false>
 constexpr size_t smem_bytes(int E) {
@@ -939,6 +944,35 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
         const int half = tl.n0 + wg * 128;
         if (g.probs != nullptr && vrow && half < g.N) g.ds_part[grow * g.ds_parts + half / 128] = dsum;
+      } else if (C::STO && g.tma_out && q * 32 + 32 <= tl.rows) {
+        // the warp's 32 rows all lie in the expert: stage each 32 x 32 chunk
+        // (64-byte swizzle: 16-byte chunk j of row r at j ^ ((r / 2) % 4))
+        // and write it with a TMA store
+        uint8_t* box = staging + (warp - 2) * BOX;
+        for (int c = wg * 4; c < wg * 4 + 4; ++c) {
+          const int col = tl.n0 + c * 32;
+          if (col >= g.N) break;
+          uint32_t r[32];
+          tmem_ld32(tb + c * 32, r);
+          tmem_wait_ld();
+          if (lane == 0) bulk_wait_read_0();       // the box's previous store has read it
+          __syncwarp();
+          uint8_t* row = box + lane * 64;
+          const int sw = (lane >> 1) & 3;
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+            *reinterpret_cast<uint4*>(row + ((j ^ sw) * 16)) = make_uint4(
+                pack_bf16x2(__uint_as_float(r[8 * j + 0]), __uint_as_float(r[8 * j + 1])),
+                pack_bf16x2(__uint_as_float(r[8 * j + 2]), __uint_as_float(r[8 * j + 3])),
+                pack_bf16x2(__uint_as_float(r[8 * j + 4]), __uint_as_float(r[8 * j + 5])),
+                pack_bf16x2(__uint_as_float(r[8 * j + 6]), __uint_as_float(r[8 * j + 7])));
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            tma_store_2d(&tmC, box, col, tl.row0 + q * 32);
+            bulk_commit();
+          }
+        }
       } else {
         for (int c = wg * 4; c < wg * 4 + 4; ++c) {
           uint32_t r[32];
@@ -954,7 +988,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         else mbar_arrive(&tempty_bar[buf]);
       }
     }
-    if (KIND == GemmKind::kWgrad && lane == 0) bulk_wait_all();  // staged stores done
+    if ((KIND == GemmKind::kWgrad || C::STO) && lane == 0) bulk_wait_all();  // staged stores done
     if ((KIND == GemmKind::kFc1Act || KIND == GemmKind::kDgradAct) && g.amax != nullptr) {
       // non-negative floats order like their bit patterns
       const uint32_t m = __reduce_max_sync(0xffffffffu, __float_as_uint(amx));

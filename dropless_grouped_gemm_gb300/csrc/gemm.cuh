@@ -60,6 +60,11 @@ struct GemmArgs {
   // kWgrad: 1 = add the result to the bf16 values already in `out` (one
   // rounding of old + new); experts with no rows leave theirs untouched
   int accumulate;
+  // kFc2 / kDgrad: 1 = tmC maps `out` as [M_cap, N] bf16 (ldo == N), box 32
+  // columns x 32 rows with 64-byte swizzle, and the epilogue writes whole
+  // 32-row groups of a tile with staged TMA stores (a ragged last group of
+  // an expert with plain stores); 0 = plain stores throughout
+  int tma_out;
   // gathered operand (the permute fused into the operand load): the
   // operand's expert-major row r is row gather_pair[r] / gather_k of the
   // token tensor gather_src [gather_T, gather_ld] (zeros for pad rows,
