@@ -494,8 +494,11 @@ int moe_grouped_mlp_fwd(const moe_bf16* x_perm, const int32_t* offsets, int E, i
     q.a_s_bytes = static_cast<long long>(M_cap) * n / 8;
     q.b_s_bytes = static_cast<long long>(E) * n * d / 32;
     q.q_out = mx->y_q; q.s_out = mx->y_q ? mx->y_s : nullptr;
+    CUtensorMap ty;
+    if (!map_out2(&ty, y_perm, M_cap, d)) return MOE_E_CUDA;
+    q.tma_out = 1;
     ev_begin(s);
-    e = moe::launch_mx_gemm(moe::MxKind::kFc2, 0, ta, tw2, ta, q, sms, s);
+    e = moe::launch_mx_gemm(moe::MxKind::kFc2, 0, ta, tw2, ty, q, sms, s);
     ev_end(s);
     if (e != cudaSuccess) return MOE_E_CUDA;
     g_last_launches = 2;
@@ -934,7 +937,10 @@ int moe_grouped_mlp_bwd_mx(const moe_bf16* x_perm, const moe_bf16* h_saved,
   gd.a_s_bytes = static_cast<long long>(M_cap) * n1 / 8;
   gd.b_s_bytes = static_cast<long long>(E) * d * n1 / 32;
   gd.q_out = mx->dx_q; gd.s_out = mx->dx_q ? mx->dx_s : nullptr;
-  e = mx_gemm(moe::MxKind::kDgrad, 0, t_dh, t_w1, t_dh, gd, sms, s);
+  CUtensorMap t_dx;
+  if (!map_out2(&t_dx, dx_perm, M_cap, d)) return MOE_E_CUDA;
+  gd.tma_out = 1;
+  e = mx_gemm(moe::MxKind::kDgrad, 0, t_dh, t_w1, t_dx, gd, sms, s);
   if (e != cudaSuccess) return MOE_E_CUDA;
   // 8. dW1_e = X_e^T dH_e
   moe::MxGemmArgs gw1{};

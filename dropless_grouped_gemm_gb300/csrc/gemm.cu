@@ -1019,6 +1019,8 @@ template <GemmKind KIND, int ACT, bool MX = false, bool SKINNY = false, bool GAT
 cudaError_t launch_t(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tc,
                      const GemmArgs& g, int num_sms, cudaStream_t s) {
   auto kern = grouped_gemm_kernel<KIND, ACT, MX, kCluster, SKINNY, GATHER, PAIR>;
+  static_assert(smem_bytes<KIND, SKINNY, PAIR>(MOE_MAX_EXPERTS) <= 227 * 1024,
+                "dynamic shared memory above the 227 KB a CTA may have");
   const size_t smem = smem_bytes<KIND, SKINNY, PAIR>(MOE_MAX_EXPERTS);
   // grid size and shared-memory attribute, set up once per device (a
   // process may drive several devices, one at a time)

@@ -45,12 +45,13 @@ constexpr int QBOX_BYTES = 32 * 64 * 2;           // staged output box: 32 rows 
 // to six stages, 256..327) so that only 64 of them occupy registers once the
 // accumulator is released: columns 384..511
 constexpr int QSTASH_TMEM = 384;
-// Pair mode (2-SM MMAs, M = 256 over the CTA pair, N = 256): each CTA's stage
-// holds its 128 rows of A, its 128-column half of B and three scale chunks
-// (its A rows' and both B halves'), all loaded by TMA onto the first CTA's
-// full barrier
-constexpr int QP_SF_OFF = QA_BYTES + QBH_BYTES;    // 32 KB
-constexpr int QP_STAGE_BYTES = QP_SF_OFF + 2048;   // 34 KB
+// Pair mode (2-SM MMAs, M = 256 over the CTA pair, N = 256): each CTA's
+// 32 KB stage holds its 128 rows of A and its 128-column half of B; the
+// stage's three scale chunks (its A rows' and both B halves') sit in a
+// separate region after the stages, 1.5 KB per stage; all of it is loaded
+// by TMA onto the first CTA's full barrier
+constexpr int QP_STAGE_BYTES = QA_BYTES + QBH_BYTES;   // 32 KB
+constexpr int QP_SF_BYTES = 3 * 512;
 
 // TMEM holds one 256-column accumulator (the scale columns leave no room
 // for a second); the epilogue moves it to registers and releases it at once,
@@ -61,9 +62,15 @@ constexpr int QP_STAGE_BYTES = QP_SF_OFF + 2048;   // 34 KB
 template <MxKind KIND, bool PAIR = false>
 struct QCfg {
   static constexpr bool W = (KIND == MxKind::kWgrad);
+  // FC2 and FC1-dgrad store their bf16 output through one staged 32 x 32
+  // box (2 KB) per epilogue warp
+  static constexpr bool STO = (KIND == MxKind::kFc2 || KIND == MxKind::kDgrad);
   static constexpr int stages = PAIR ? (W ? 5 : 6) : (W ? 3 : 4);
   static constexpr int stage_bytes = PAIR ? QP_STAGE_BYTES : QSTAGE_BYTES;
-  static constexpr int stg_bytes = W ? (QEPI_WARPS + 1) * QBOX_BYTES : 0;
+  // rounded up so that the staging boxes after it stay 1024-byte aligned
+  static constexpr int sf_bytes = PAIR ? (stages * QP_SF_BYTES + 1023) / 1024 * 1024 : 0;
+  static constexpr int stg_bytes =
+      W ? (QEPI_WARPS + 1) * QBOX_BYTES : (STO ? QEPI_WARPS * 32 * 32 * 2 : 0);
   // TMEM: accumulator, then each stage's scale columns, then the stash
   static_assert(QSF_TMEM + stages * QSF_COLS <= QSTASH_TMEM &&
                     QSTASH_TMEM + 2 * 64 <= QTMEM_COLS,
@@ -72,7 +79,7 @@ struct QCfg {
 template <MxKind KIND, bool PAIR = false>
 constexpr size_t mx_smem_bytes(int E) {
   using C = QCfg<KIND, PAIR>;
-  return 1024 + static_cast<size_t>(C::stages) * C::stage_bytes + C::stg_bytes +
+  return 1024 + static_cast<size_t>(C::stages) * C::stage_bytes + C::sf_bytes + C::stg_bytes +
          (2 * C::stages + 4) * 8 + 16 + 2 * (E + 1) * 4;
 }
 
@@ -361,7 +368,8 @@ __global__ void __launch_bounds__(QTHREADS, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
-  uint8_t* staging = smem + NST * SBYTES;                     // one box per epilogue warp
+  uint8_t* sf_region = smem + NST * SBYTES;                   // pair mode: scale chunks
+  uint8_t* staging = sf_region + QCfg<KIND, PAIR>::sf_bytes;   // one box per epilogue warp
   uint8_t* zero_box = staging + QEPI_WARPS * QBOX_BYTES;
   uint64_t* full_bar = reinterpret_cast<uint64_t*>(staging + QCfg<KIND, PAIR>::stg_bytes);
   uint64_t* empty_bar = full_bar + NST;
@@ -462,7 +470,7 @@ __global__ void __launch_bounds__(QTHREADS, 1)
           if (!mbar_wait(&empty_bar[stage], phase ^ 1, abort_flag)) { ok = false; break; }
           uint8_t* sa = smem + stage * SBYTES;
           uint8_t* sb = sa + QA_BYTES;
-          uint8_t* ssf = sa + QP_SF_OFF;
+          uint8_t* ssf = sf_region + stage * QP_SF_BYTES;
           const uint32_t fb = full0 + stage * 8;
           if (rank == 0) mbar_arrive_expect_tx(&full_bar[stage], 2 * (QA_BYTES + QBH_BYTES + 3 * 512));
           const int nh = tl.n0 + rank * QHN;   // this CTA's half of B
@@ -599,7 +607,7 @@ __global__ void __launch_bounds__(QTHREADS, 1)
           if (lane == 0) {
             uint8_t* sa = smem + stage * SBYTES;
             uint8_t* sb = sa + QA_BYTES;
-            uint8_t* ssf = sa + QP_SF_OFF;
+            uint8_t* ssf = sf_region + stage * QP_SF_BYTES;
             const uint32_t sf_t = tmem_base + QSF_TMEM + stage * QSF_COLS;
             // A rows' scales, then both B halves' in consecutive columns
             tmem_cp_sf_pair(sf_t, sdesc_sf(smem_u32(ssf)));
@@ -809,6 +817,31 @@ __global__ void __launch_bounds__(QTHREADS, 1)
             }
           }
         }
+      } else if (QCfg<KIND, PAIR>::STO && !QOUT && g.tma_out && q * 32 + 32 <= tl.rows) {
+        // the warp's 32 rows all lie in the expert: stage each 32 x 32 chunk
+        // (64-byte swizzle: 16-byte chunk j of row r at j ^ ((r / 2) % 4))
+        // and write it with a TMA store
+        uint8_t* box = staging + (warp - 2) * (32 * 32 * 2);
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          if (lane == 0) bulk_wait_read_0();       // the box's previous store has read it
+          __syncwarp();
+          uint8_t* row = box + lane * 64;
+          const int sw = (lane >> 1) & 3;
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+            *reinterpret_cast<uint4*>(row + ((j ^ sw) * 16)) = make_uint4(
+                pack_bf16x2(__uint_as_float(v[c][8 * j + 0]), __uint_as_float(v[c][8 * j + 1])),
+                pack_bf16x2(__uint_as_float(v[c][8 * j + 2]), __uint_as_float(v[c][8 * j + 3])),
+                pack_bf16x2(__uint_as_float(v[c][8 * j + 4]), __uint_as_float(v[c][8 * j + 5])),
+                pack_bf16x2(__uint_as_float(v[c][8 * j + 6]), __uint_as_float(v[c][8 * j + 7])));
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            tma_store_2d(&tmC, box, col0 + c * 32, tl.row0 + q * 32);
+            bulk_commit();
+          }
+        }
       } else {
         if (r < tl.rows) {
           const long long grow = tl.row0 + r;
@@ -824,7 +857,7 @@ __global__ void __launch_bounds__(QTHREADS, 1)
         }
       }
     }
-    if (W && lane == 0) bulk_wait_all();  // staged stores done before the CTA exits
+    if ((W || QCfg<KIND, PAIR>::STO) && lane == 0) bulk_wait_all();  // staged stores done before the CTA exits
     __syncwarp();
   }
   tc_fence_before();
@@ -868,6 +901,8 @@ template <MxKind KIND, int ACT, bool QOUT = false, bool PAIR = false>
 cudaError_t launch_mx_t(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tc,
                         const MxGemmArgs& g, int num_sms, cudaStream_t st) {
   auto kern = mx_gemm_kernel<KIND, ACT, QOUT, PAIR>;
+  static_assert(mx_smem_bytes<KIND, PAIR>(MOE_MAX_EXPERTS) <= 227 * 1024,
+                "dynamic shared memory above the 227 KB a CTA may have");
   const size_t smem = mx_smem_bytes<KIND, PAIR>(MOE_MAX_EXPERTS);
   CUtensorMap tsa = ta, tsb = ta;   // any valid maps when not in pair mode
   if (PAIR && (!map_scale_chunks(&tsa, g.a_s, g.a_s_bytes) ||

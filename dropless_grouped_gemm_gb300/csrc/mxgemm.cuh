@@ -53,6 +53,11 @@ struct MxGemmArgs {
   uint8_t* q_out;
   uint8_t* s_out;
   int32_t* err;
+  // kFc2 / kDgrad without q_out: 1 = tmC maps `out` as [M_cap, N] bf16
+  // (ldo == N), box 32 columns x 32 rows with 64-byte swizzle, and the
+  // epilogue writes whole 32-row groups with staged TMA stores; 0 = plain
+  // stores
+  int tma_out;
   // kDgradAct, optional (dh_q == nullptr: none): GroupGemm + dActivation +
   // Quantize/Transpose - the epilogue also writes the MXFP8 copies of the
   // bf16 dH it stores, as the tiled activation quantiser would: row-wise
