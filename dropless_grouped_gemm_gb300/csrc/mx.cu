@@ -65,12 +65,15 @@ struct QCfg {
   // FC2 and FC1-dgrad store their bf16 output through one staged 32 x 32
   // box (2 KB) per epilogue warp
   static constexpr bool STO = (KIND == MxKind::kFc2 || KIND == MxKind::kDgrad);
+  // the quantising FC2-dgrad epilogue transposes dH through one 2 KB box
+  // per epilogue warp
+  static constexpr bool TBOX = STO || KIND == MxKind::kDgradAct;
   static constexpr int stages = PAIR ? (W ? 5 : 6) : (W ? 3 : 4);
   static constexpr int stage_bytes = PAIR ? QP_STAGE_BYTES : QSTAGE_BYTES;
   // rounded up so that the staging boxes after it stay 1024-byte aligned
   static constexpr int sf_bytes = PAIR ? (stages * QP_SF_BYTES + 1023) / 1024 * 1024 : 0;
   static constexpr int stg_bytes =
-      W ? (QEPI_WARPS + 1) * QBOX_BYTES : (STO ? QEPI_WARPS * 32 * 32 * 2 : 0);
+      W ? (QEPI_WARPS + 1) * QBOX_BYTES : (TBOX ? QEPI_WARPS * 32 * 32 * 2 : 0);
   // TMEM: accumulator, then each stage's scale columns, then the stash
   static_assert(QSF_TMEM + stages * QSF_COLS <= QSTASH_TMEM &&
                     QSTASH_TMEM + 2 * 64 <= QTMEM_COLS,
@@ -293,10 +296,15 @@ __device__ __forceinline__ void mx_dact_row32(const MxGemmArgs& g, long long gro
 // expert (a column block of the transposed copy).  Stores the bf16 dH, the
 // row-wise codes and scale (row tile of the 128-row tile starting at
 // tl_row0) and the transposed codes and scales (K tile of the same rows,
-// block q of it).
+// block q of it).  The transposed copy goes through the warp's 2 KB box in
+// shared memory: row r's 16-byte chunk j sits at chunk (j + r/2) % 4 of the
+// row, so that both the row writes (8 lanes per 128-byte phase) and the
+// column reads (one 64-byte row per load) are free of bank conflicts; lane
+// c then quantises column c's 32 values as one block.
 template <int ACT>
 __device__ __forceinline__ void mx_dact_quant_block(const MxGemmArgs& g, int tl_row0, int q,
-                                                    int lane, int hc, const uint32_t* r) {
+                                                    int lane, int hc, const uint32_t* r,
+                                                    uint8_t* box) {
   const int rt = q * 32 + lane;
   const long long grow = static_cast<long long>(tl_row0) + rt;
   const uint16_t* hp = g.aux + grow * g.ld_aux + hc;
@@ -335,16 +343,29 @@ __device__ __forceinline__ void mx_dact_quant_block(const MxGemmArgs& g, int tl_
   pq[0] = make_uint4(qw[0], qw[1], qw[2], qw[3]);
   pq[1] = make_uint4(qw[4], qw[5], qw[6], qw[7]);
   g.dh_s[chunk * 512 + mx_chunk_off(rt, (hc >> 5) & 3)] = static_cast<uint8_t>(sc);
-  // transposed copy: column hc + j over the warp's 32 rows is one block
-  uint32_t my_sc = 0;
+  // transposed copy: column hc + c over the warp's 32 rows is one block
+  uint8_t* myrow = box + lane * 64;
 #pragma unroll
-  for (int j = 0; j < 32; ++j) {
-    uint32_t code;
-    const uint32_t scj = mx_quant_lanes(f[j], code);
-    g.dh_qT[static_cast<long long>(hc + j) * g.M_cap + grow] = static_cast<uint8_t>(code);
-    if (lane == j) my_sc = scj;
+  for (int j = 0; j < 4; ++j)
+    *reinterpret_cast<uint4*>(myrow + (((j + (lane >> 1)) & 3) * 16)) =
+        make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
+  __syncwarp();
+  float col[32];
+  const int cj = lane >> 3, ce = (lane & 7) * 2;   // this lane's column: chunk, byte in it
+#pragma unroll
+  for (int rr = 0; rr < 32; ++rr) {
+    const uint16_t b = *reinterpret_cast<const uint16_t*>(
+        box + rr * 64 + (((cj + (rr >> 1)) & 3) * 16) + ce);
+    col[rr] = __uint_as_float(static_cast<uint32_t>(b) << 16);
   }
-  g.dh_sT[chunk * 512 + mx_chunk_off((hc + lane) & 127, q)] = static_cast<uint8_t>(my_sc);
+  __syncwarp();   // the box is free for the next block
+  uint32_t cq[8];
+  const uint32_t csc = mx_quant32(col, cq);
+  uint4* pt = reinterpret_cast<uint4*>(g.dh_qT + static_cast<long long>(hc + lane) * g.M_cap +
+                                       (grow - lane));
+  pt[0] = make_uint4(cq[0], cq[1], cq[2], cq[3]);
+  pt[1] = make_uint4(cq[4], cq[5], cq[6], cq[7]);
+  g.dh_sT[chunk * 512 + mx_chunk_off((hc + lane) & 127, q)] = static_cast<uint8_t>(csc);
 }
 
 // Persistent warp-specialised block-scaled grouped GEMM in 2-CTA clusters:
@@ -758,7 +779,7 @@ __global__ void __launch_bounds__(QTHREADS, 1)
           for (int b = 0; b < 32 / BLK; ++b) {
             const int dcol = col0 + 32 * c + b * BLK;          // first dA column
             mx_dact_quant_block<ACT>(g, tl.row0, q, lane, (ACT == MOE_ACT_SRELU) ? dcol : 2 * dcol,
-                                     src + b * BLK);
+                                     src + b * BLK, staging + (warp - 2) * (32 * 32 * 2));
           }
         }
         continue;
