@@ -774,23 +774,28 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             const int zr = kk_n * UK - tl.klast;
             // boxes of 64 rows x 128 bytes: 2 of A and 4 of B (pair mode: 2
             // of B in each CTA, the second CTA's written through the cluster)
+            // Lane l clears 16-byte chunk l % 8 of rows klast + l / 8, +4, ...
+            // in every box (a whole 128-byte row, so the swizzle does not
+            // matter); no division on this per-tile path, which bounds the
+            // rate of skinny experts' tiles.
             constexpr int NBOX = PAIR ? 4 : 6;
-            const int units = NBOX * zr * 8;  // 16-byte units
-            for (int u = lane; u < units; u += 32) {
-              const int box = u / (zr * 8);
-              const int rem = u - box * (zr * 8);
-              const int row = tl.klast + rem / 8;
-              const int ch = rem & 7;
-              uint8_t* p = (box < 2 ? sa + box * MN_BOX_BYTES : sb + (box - 2) * MN_BOX_BYTES) +
-                           row * 128 + ch * 16;
-              *reinterpret_cast<uint4*>(p) = make_uint4(0, 0, 0, 0);
-              if constexpr (PAIR) st_cluster_zero16(mapa_shared(smem_u32(p), 1));
-            }
-            if constexpr (PAIR) {
-              fence_proxy_async_cluster();
-              fence_acq_rel_cluster();
-            } else {
-              fence_proxy_async_smem();
+            if (zr > 0) {
+              const int ch = lane & 7;
+              for (int row = tl.klast + (lane >> 3); row < kk_n * UK; row += 4) {
+#pragma unroll
+                for (int box = 0; box < NBOX; ++box) {
+                  uint8_t* p = (box < 2 ? sa + box * MN_BOX_BYTES : sb + (box - 2) * MN_BOX_BYTES) +
+                               row * 128 + ch * 16;
+                  *reinterpret_cast<uint4*>(p) = make_uint4(0, 0, 0, 0);
+                  if constexpr (PAIR) st_cluster_zero16(mapa_shared(smem_u32(p), 1));
+                }
+              }
+              if constexpr (PAIR) {
+                fence_proxy_async_cluster();
+                fence_acq_rel_cluster();
+              } else {
+                fence_proxy_async_smem();
+              }
             }
           }
         }
