@@ -49,6 +49,8 @@ constexpr int TMEM_COLS = 2 * BN;
 constexpr int PAIR_B_BYTES = (BN / 2) * BK * 2;        // 16 KB
 constexpr int PAIR_STAGE_BYTES = A_BYTES + PAIR_B_BYTES;  // 32 KB
 constexpr int PAIR_STAGES = 6;
+// row pairs per column sweep in FC1's grouped unit order
+constexpr int kRowGroup = 8;
 
 // Weight-gradient kernels stage their output in shared memory and write it
 // with TMA stores.  Two configurations:
@@ -135,7 +137,15 @@ __device__ __forceinline__ Tile decode_tile(const GemmArgs& g, const int* s_off,
     tl.n0 = (2 * local + rank) * BN;
   } else {
     int pm, ni;
-    if (g.col_major) {
+    if (g.col_major == 2) {
+      // groups of kRowGroup row pairs, each group swept column-major
+      const int np = (row_blocks<KIND>(g, s_off, lo) + CL - 1) / CL;
+      const int grp = local / (kRowGroup * nt);
+      const int idx = local - grp * (kRowGroup * nt);
+      const int gg = min(kRowGroup, np - grp * kRowGroup);
+      ni = idx / gg;
+      pm = grp * kRowGroup + (idx - ni * gg);
+    } else if (g.col_major) {
       const int np = (row_blocks<KIND>(g, s_off, lo) + CL - 1) / CL;
       ni = local / np;
       pm = local - ni * np;
@@ -802,13 +812,20 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         __syncwarp();
         if (lane == 0) {
           const uint32_t a0 = smem_u32(sa), b0 = smem_u32(sb);
-          for (int kk = 0; kk < kk_n; ++kk) {
+          auto mma = [&](int kk) {
             const uint64_t ad = A_MN ? sdesc_sw128(a0 + kk * 2048, MN_BOX_BYTES, 1024)
                                      : sdesc_sw128(a0 + kk * 32, 16, 1024);
             const uint64_t bd = B_MN ? sdesc_sw128(b0 + kk * 2048, MN_BOX_BYTES, 1024)
                                      : sdesc_sw128(b0 + kk * 32, 16, 1024);
             if constexpr (PAIR) umma_bf16_pair(d_tmem, ad, bd, IDESC, (kb > 0 || kk > 0) ? 1u : 0u);
             else umma_bf16(d_tmem, ad, bd, IDESC, (kb > 0 || kk > 0) ? 1u : 0u);
+          };
+          if (kk_n == BK / UK) {
+            // a whole block: the four MMAs issued back to back
+#pragma unroll
+            for (int kk = 0; kk < BK / UK; ++kk) mma(kk);
+          } else {
+            for (int kk = 0; kk < kk_n; ++kk) mma(kk);
           }
           if constexpr (PAIR) umma_commit_pair_mc(&empty_bar[stage]);      // frees it in both CTAs
           else if constexpr (CL == 2) umma_commit_mc(&empty_bar[stage], kPair);
@@ -1126,6 +1143,12 @@ cudaError_t launch_grouped_gemm(GemmKind kind, int act, const CUtensorMap& ta,
     const long long units_m = ((rows + BM - 1) / BM + kCluster - 1) / kCluster;
     const long long nt = (g.N + BN - 1) / BN;
     g.col_major = units_m <= nt ? 1 : 0;
+    // FC1 reads x over K = d (64 MB per expert on the balanced layer), more
+    // than an L2 half keeps between two column sweeps: sweeping kRowGroup
+    // row pairs at a time re-reads less of it (ncu, two balanced experts:
+    // DRAM reads 678 -> 580 MB per launch; groups of 4 read 704 MB), at the
+    // same speed
+    if (kind == GemmKind::kFc1Act && units_m > kRowGroup) g.col_major = 2;
   }
   if (g.gather_pair != nullptr) {
     // the gathering producer is its own instantiation, so that the other

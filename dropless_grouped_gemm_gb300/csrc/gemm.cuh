@@ -55,7 +55,8 @@ struct GemmArgs {
   float* amax;
   // unit order inside an expert, set by launch_grouped_gemm: 0 = row pairs
   // outermost (a wave of CTAs sweeps every column tile of B), 1 = column
-  // tiles outermost (a wave reuses each B column tile across all row pairs)
+  // tiles outermost (a wave reuses each B column tile across all row pairs),
+  // 2 = groups of row pairs, each swept with column tiles outermost
   int col_major;
   // kWgrad: 1 = add the result to the bf16 values already in `out` (one
   // rounding of old + new); experts with no rows leave theirs untouched
