@@ -764,48 +764,49 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       if (!ok) break;
       tc_fence_after();
       const uint32_t d_tmem = tmem_base + buf * BN;
-      for (int kb = 0; kb < tl.kblocks; ++kb) {
+      // One reduction block.  TAIL: an expert's ragged last block of a
+      // weight gradient.  Its own instantiation keeps the tail's clearing
+      // and fences out of the whole blocks' path: with them in the same
+      // loop body, even untaken, the weight gradients' MMAs ran 12% slower.
+      auto kblock = [&](int kb, auto tail_c) -> bool {
+        constexpr bool TAIL = decltype(tail_c)::value;
         if (lane == 0) ok = mbar_wait(&full_bar[stage], phase, abort_flag);
         ok = __shfl_sync(0xffffffffu, ok, 0);
-        if (!ok) break;
+        if (!ok) return false;
         tc_fence_after();
         // rows gathered with cp.async were written through the generic proxy
         if (GATHER && lane == 0) fence_proxy_async_smem();
         uint8_t* sa = smem + stage * SBYTES;
         uint8_t* sb = sa + A_BYTES;
-        // In an expert's last reduction block only ceil(klast/16) MMAs touch
-        // its rows; the rows after klast up to that 16-row boundary belong to
-        // the next expert and are zeroed in all six 64x64 boxes (2 of A, 4 of
-        // B) before the MMAs read them.
         int kk_n = BK / UK;
-        if constexpr (KIND == GemmKind::kWgrad) {
-          if (kb == tl.kblocks - 1 && tl.klast < BK) {
-            kk_n = (tl.klast + UK - 1) / UK;
-            const int zr = kk_n * UK - tl.klast;
-            // boxes of 64 rows x 128 bytes: 2 of A and 4 of B (pair mode: 2
-            // of B in each CTA, the second CTA's written through the cluster)
-            // Lane l clears 16-byte chunk l % 8 of rows klast + l / 8, +4, ...
-            // in every box (a whole 128-byte row, so the swizzle does not
-            // matter); no division on this per-tile path, which bounds the
-            // rate of skinny experts' tiles.
-            constexpr int NBOX = PAIR ? 4 : 6;
-            if (zr > 0) {
-              const int ch = lane & 7;
-              for (int row = tl.klast + (lane >> 3); row < kk_n * UK; row += 4) {
+        if constexpr (TAIL) {
+          // Only ceil(klast/16) MMAs touch the expert's rows; the rows after
+          // klast up to that 16-row boundary belong to the next expert and
+          // are cleared in all six 64x64 boxes (2 of A, 4 of B; pair mode: 2
+          // of B in each CTA, the second CTA's written through the cluster)
+          // before the MMAs read them.  Lane l clears 16-byte chunk l % 8 of
+          // rows klast + l / 8, +4, ... in every box (a whole 128-byte row,
+          // so the swizzle does not matter), with no division on this
+          // per-tile path, which bounds the rate of skinny experts' tiles.
+          kk_n = (tl.klast + UK - 1) / UK;
+          const int zr = kk_n * UK - tl.klast;
+          constexpr int NBOX = PAIR ? 4 : 6;
+          if (zr > 0) {
+            const int ch = lane & 7;
+            for (int row = tl.klast + (lane >> 3); row < kk_n * UK; row += 4) {
 #pragma unroll
-                for (int box = 0; box < NBOX; ++box) {
-                  uint8_t* p = (box < 2 ? sa + box * MN_BOX_BYTES : sb + (box - 2) * MN_BOX_BYTES) +
-                               row * 128 + ch * 16;
-                  *reinterpret_cast<uint4*>(p) = make_uint4(0, 0, 0, 0);
-                  if constexpr (PAIR) st_cluster_zero16(mapa_shared(smem_u32(p), 1));
-                }
+              for (int box = 0; box < NBOX; ++box) {
+                uint8_t* p = (box < 2 ? sa + box * MN_BOX_BYTES : sb + (box - 2) * MN_BOX_BYTES) +
+                             row * 128 + ch * 16;
+                *reinterpret_cast<uint4*>(p) = make_uint4(0, 0, 0, 0);
+                if constexpr (PAIR) st_cluster_zero16(mapa_shared(smem_u32(p), 1));
               }
-              if constexpr (PAIR) {
-                fence_proxy_async_cluster();
-                fence_acq_rel_cluster();
-              } else {
-                fence_proxy_async_smem();
-              }
+            }
+            if constexpr (PAIR) {
+              fence_proxy_async_cluster();
+              fence_acq_rel_cluster();
+            } else {
+              fence_proxy_async_smem();
             }
           }
         }
@@ -820,12 +821,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             if constexpr (PAIR) umma_bf16_pair(d_tmem, ad, bd, IDESC, (kb > 0 || kk > 0) ? 1u : 0u);
             else umma_bf16(d_tmem, ad, bd, IDESC, (kb > 0 || kk > 0) ? 1u : 0u);
           };
-          if (kk_n == BK / UK) {
-            // a whole block: the four MMAs issued back to back
+          if constexpr (TAIL) {
+            for (int kk = 0; kk < kk_n; ++kk) mma(kk);
+          } else {
 #pragma unroll
             for (int kk = 0; kk < BK / UK; ++kk) mma(kk);
-          } else {
-            for (int kk = 0; kk < kk_n; ++kk) mma(kk);
           }
           if constexpr (PAIR) umma_commit_pair_mc(&empty_bar[stage]);      // frees it in both CTAs
           else if constexpr (CL == 2) umma_commit_mc(&empty_bar[stage], kPair);
@@ -833,7 +833,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
         __syncwarp();
         if (++stage == NST) { stage = 0; phase ^= 1; }
-      }
+        return true;
+      };
+      const bool ragged = KIND == GemmKind::kWgrad && tl.kblocks > 0 && tl.klast < BK;
+      const int whole = ragged ? tl.kblocks - 1 : tl.kblocks;
+      for (int kb = 0; kb < whole; ++kb)
+        if (!kblock(kb, BoolC<false>{})) break;
+      if constexpr (KIND == GemmKind::kWgrad)
+        if (ok && ragged) kblock(tl.kblocks - 1, BoolC<true>{});
       if (!ok) break;
       if (lane == 0) {
         if constexpr (PAIR) umma_commit_pair_mc(&tfull_bar[buf]);   // both CTAs' epilogues

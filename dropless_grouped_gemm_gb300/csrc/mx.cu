@@ -673,10 +673,16 @@ __global__ void __launch_bounds__(QTHREADS, 1)
       ok = __shfl_sync(0xffffffffu, ok, 0);
       if (!ok) break;
       tc_fence_after();
-      for (int kb = 0; kb < tl.kblocks; ++kb) {
+      // One reduction step.  GEN: the generic form (an expert's last step of
+      // a weight gradient, which holds klast of its rows, or a tile with one
+      // 128-column half inside N); otherwise four K = 32 MMAs per half,
+      // unrolled (a runtime MMA count in the same loop body slowed the
+      // whole steps' issue).
+      auto kstep = [&](int kb, auto gen_c) -> bool {
+        constexpr bool GEN = decltype(gen_c)::value;
         if (lane == 0) ok = mbar_wait(&full_bar[stage], phase, abort_flag);
         ok = __shfl_sync(0xffffffffu, ok, 0);
-        if (!ok) break;
+        if (!ok) return false;
         tc_fence_after();
         if (lane == 0 && !tl.ghost) {
           uint8_t* sa = smem + stage * SBYTES;
@@ -684,21 +690,31 @@ __global__ void __launch_bounds__(QTHREADS, 1)
           uint8_t* ssf = sa + QSF_OFF;
           const uint32_t sf_t = tmem_base + QSF_TMEM + stage * QSF_COLS;
           tmem_cp_sf(sf_t, sdesc_sf(smem_u32(ssf)));
-          for (int h = 0; h < tl.nh; ++h)
-            tmem_cp_sf(sf_t + 4 * (1 + h), sdesc_sf(smem_u32(ssf + 512 * (1 + h))));
           const uint32_t a0 = smem_u32(sa), b0 = smem_u32(sb);
-          // an expert's last reduction step of a weight gradient holds
-          // klast (a multiple of 32) of its rows: one MMA per 32 of them
-          const int kk_n = (W && kb == tl.kblocks - 1) ? tl.klast / 32 : QBK / 32;
-          for (int kk = 0; kk < kk_n; ++kk) {
+          auto mma = [&](int kk, int h) {
             const uint64_t ad = sdesc_sw128(a0 + kk * 32, 16, 1024);
             const uint32_t id = IDESC | (static_cast<uint32_t>(kk) << 29) | (static_cast<uint32_t>(kk) << 4);
-            for (int h = 0; h < tl.nh; ++h) {
-              const uint32_t bh = b0 + h * QBH_BYTES;
-              const uint64_t bd = B_MN ? sdesc_sw128(bh + kk * 4096, QBH_BYTES, 1024)
-                                       : sdesc_sw128(bh + kk * 32, 16, 1024);
-              umma_mx(tmem_base + h * QHN, ad, bd, id, sf_t, sf_t + 4 * (1 + h),
-                      (kb > 0 || kk > 0) ? 1u : 0u);
+            const uint32_t bh = b0 + h * QBH_BYTES;
+            const uint64_t bd = B_MN ? sdesc_sw128(bh + kk * 4096, QBH_BYTES, 1024)
+                                     : sdesc_sw128(bh + kk * 32, 16, 1024);
+            umma_mx(tmem_base + h * QHN, ad, bd, id, sf_t, sf_t + 4 * (1 + h),
+                    (kb > 0 || kk > 0) ? 1u : 0u);
+          };
+          if constexpr (GEN) {
+            for (int h = 0; h < tl.nh; ++h)
+              tmem_cp_sf(sf_t + 4 * (1 + h), sdesc_sf(smem_u32(ssf + 512 * (1 + h))));
+            // an expert's last reduction step of a weight gradient holds
+            // klast (a multiple of 32) of its rows: one MMA per 32 of them
+            const int kk_n = (W && kb == tl.kblocks - 1) ? tl.klast / 32 : QBK / 32;
+            for (int kk = 0; kk < kk_n; ++kk)
+              for (int h = 0; h < tl.nh; ++h) mma(kk, h);
+          } else {
+            tmem_cp_sf(sf_t + 4, sdesc_sf(smem_u32(ssf + 512)));
+            tmem_cp_sf(sf_t + 8, sdesc_sf(smem_u32(ssf + 1024)));
+#pragma unroll
+            for (int kk = 0; kk < QBK / 32; ++kk) {
+              mma(kk, 0);
+              mma(kk, 1);
             }
           }
         }
@@ -706,7 +722,18 @@ __global__ void __launch_bounds__(QTHREADS, 1)
         if (lane == 0) umma_commit_mc(&empty_bar[stage], kQPair);
         __syncwarp();
         if (++stage == NST) { stage = 0; phase ^= 1; }
+        return true;
+      };
+      const bool short_last = W && tl.kblocks > 0 && tl.klast < QBK;
+      const int whole = short_last ? tl.kblocks - 1 : tl.kblocks;
+      if (tl.nh == 2) {
+        for (int kb = 0; kb < whole; ++kb)
+          if (!kstep(kb, BoolC<false>{})) break;
+      } else {
+        for (int kb = 0; kb < whole; ++kb)
+          if (!kstep(kb, BoolC<true>{})) break;
       }
+      if (ok && short_last) kstep(tl.kblocks - 1, BoolC<true>{});
       if (!ok) break;
       if (lane == 0) umma_commit(tfull_bar);
       __syncwarp();

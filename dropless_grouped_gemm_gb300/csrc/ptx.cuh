@@ -10,6 +10,13 @@
 
 namespace moe {
 
+// compile-time flag for generic lambdas that are instantiated twice (e.g. a
+// loop body with and without its rare case)
+template <bool B>
+struct BoolC {
+  static constexpr bool value = B;
+};
+
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
