@@ -635,13 +635,20 @@ __global__ void __launch_bounds__(QTHREADS, 1)
             tmem_cp_sf_pair(sf_t + 4, sdesc_sf(smem_u32(ssf + 512)));
             tmem_cp_sf_pair(sf_t + 8, sdesc_sf(smem_u32(ssf + 1024)));
             const uint32_t a0 = smem_u32(sa), b0 = smem_u32(sb);
-            const int kk_n = (W && kb == tl.kblocks - 1) ? tl.klast / 32 : QBK / 32;
-            for (int kk = 0; kk < kk_n; ++kk) {
+            auto mma = [&](int kk) {
               const uint64_t ad = sdesc_sw128(a0 + kk * 32, 16, 1024);
               const uint64_t bd = B_MN ? sdesc_sw128(b0 + kk * 4096, QBH_BYTES, 1024)
                                        : sdesc_sw128(b0 + kk * 32, 16, 1024);
               const uint32_t id = IDESC | (static_cast<uint32_t>(kk) << 29) | (static_cast<uint32_t>(kk) << 4);
               umma_mx_pair(tmem_base, ad, bd, id, sf_t, sf_t + 4, (kb > 0 || kk > 0) ? 1u : 0u);
+            };
+            if (W && kb == tl.kblocks - 1 && tl.klast < QBK) {
+              // an expert's last reduction step of a weight gradient: one MMA
+              // per 32 of its klast rows
+              for (int kk = 0; kk < tl.klast / 32; ++kk) mma(kk);
+            } else {
+#pragma unroll
+              for (int kk = 0; kk < QBK / 32; ++kk) mma(kk);
             }
             umma_commit_pair_mc(&empty_bar[stage]);   // frees the stage in both CTAs
           }
