@@ -481,9 +481,16 @@ int moe_grouped_mlp_fwd(const moe_bf16* x_perm, const int32_t* offsets, int E, i
     g1.mx_q = mx->a_q; g1.mx_s = mx->a_s; g1.mx_qT = mx->a_qT;
     g1.mx_sT = mx->a_qT ? mx->a_sT : nullptr; g1.n_a = n;
   }
+  // bf16 FC1: H and A leave through staged TMA stores
+  CUtensorMap th = tx, tao = tx;
+  if (!use_mx) {
+    if ((save_h && !map_out2(&th, h_saved, M_cap, n1)) || !map_out2(&tao, a, M_cap, n))
+      return MOE_E_CUDA;
+    g1.tma_out = 1;
+  }
   ev_begin(s);
-  cudaError_t e = moe::launch_grouped_gemm(moe::GemmKind::kFc1Act, act, tx, tw1, tx, g1, sms, s,
-                                           use_mx);
+  cudaError_t e = moe::launch_grouped_gemm(moe::GemmKind::kFc1Act, act, tx, tw1, th, g1, sms, s,
+                                           use_mx, &tao);
   ev_end(s);
   if (e != cudaSuccess) return MOE_E_CUDA;
   if (use_mx) {
@@ -732,7 +739,15 @@ int moe_grouped_mlp_fwd_gather(const moe_bf16* x, int T, int k, const int32_t* p
   // map argument is unused)
   g1.gather_pair = pair_of_row; g1.gather_k = k; g1.gather_T = T;
   g1.gather_src = x; g1.gather_ld = d;
-  cudaError_t e = gemm(moe::GemmKind::kFc1Act, act, tw1, tw1, tw1, g1, sms, s);
+  // H and A leave through staged TMA stores
+  CUtensorMap th = tw1, tao;
+  if ((save_h && !map_out2(&th, h_saved, M_cap, n1)) || !map_out2(&tao, a, M_cap, n))
+    return MOE_E_CUDA;
+  g1.tma_out = 1;
+  ev_begin(s);
+  cudaError_t e = moe::launch_grouped_gemm(moe::GemmKind::kFc1Act, act, tw1, tw1, th, g1, sms, s,
+                                           false, &tao);
+  ev_end(s);
   if (e != cudaSuccess) return MOE_E_CUDA;
   moe::GemmArgs g2{};
   g2.offsets = offsets; g2.E = E; g2.M_cap = M_cap; g2.K = n; g2.N = d; g2.R = 0;

@@ -69,7 +69,8 @@ struct Cfg {
   // FC2 and FC1-dgrad store their bf16 output through one staged 32 x 32
   // box per epilogue warp (their reductions are short enough that plain
   // stores left the epilogue longer than the next tile's MMAs)
-  static constexpr bool STO = (KIND == GemmKind::kFc2 || KIND == GemmKind::kDgrad);
+  static constexpr bool STO =
+      (KIND == GemmKind::kFc2 || KIND == GemmKind::kDgrad || KIND == GemmKind::kFc1Act);
   static constexpr int box_cols = SKINNY ? 64 : 32;
   static constexpr int box_bytes = 32 * box_cols * 2;
   static constexpr int nbuf = SKINNY ? 2 : 1;
@@ -428,7 +429,8 @@ template <GemmKind KIND, int ACT, bool MX, int CL, bool SKINNY, bool GATHER, boo
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                         const __grid_constant__ CUtensorMap tmB,
-                        const __grid_constant__ CUtensorMap tmC, const GemmArgs g) {
+                        const __grid_constant__ CUtensorMap tmC,
+                        const __grid_constant__ CUtensorMap tmD, const GemmArgs g) {
   constexpr bool A_MN = (KIND == GemmKind::kWgrad);
   constexpr bool B_MN = (KIND == GemmKind::kFc1Act || KIND == GemmKind::kFc2 ||
                          KIND == GemmKind::kWgrad);
@@ -482,7 +484,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     fence_mbar_init();
     prefetch_tmap(&tmA);
     prefetch_tmap(&tmB);
-    if (KIND == GemmKind::kWgrad) prefetch_tmap(&tmC);
+    if (KIND == GemmKind::kWgrad || (C::STO && g.tma_out)) prefetch_tmap(&tmC);
+    if (KIND == GemmKind::kFc1Act && !MX && g.tma_out) prefetch_tmap(&tmD);
   }
   if (KIND == GemmKind::kWgrad && warp >= 2) {  // epilogue threads clear the zero box
     for (int i = threadIdx.x - 64; i < BOX / 16; i += 32 * EPI_WARPS)
@@ -973,7 +976,67 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
         const int half = tl.n0 + wg * 128;
         if (g.probs != nullptr && vrow && half < g.N) g.ds_part[grow * g.ds_parts + half / 128] = dsum;
-      } else if (C::STO && g.tma_out && q * 32 + 32 <= tl.rows) {
+      } else if (KIND == GemmKind::kFc1Act && g.tma_out && q * 32 + 32 <= tl.rows) {
+        // FC1, the warp's 32 rows all in the expert: H (when saved) and A go
+        // through the warp's 32 x 32 box (64-byte swizzle) and TMA stores.
+        // Gated: a chunk of 32 accumulator columns gives 16 columns of A,
+        // so A's box takes two chunks.
+        uint8_t* box = staging + (warp - 2) * BOX;
+        uint8_t* srow = box + lane * 64;
+        const int sw = (lane >> 1) & 3;
+        const int grow0 = tl.row0 + q * 32;
+        auto put = [&](const uint32_t* v, const CUtensorMap* m, int x) {
+          if (lane == 0) bulk_wait_read_0();     // the box's previous store has read it
+          __syncwarp();
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+            *reinterpret_cast<uint4*>(srow + ((j ^ sw) * 16)) =
+                make_uint4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            tma_store_2d(m, box, x, grow0);
+            bulk_commit();
+          }
+        };
+        uint32_t av[16];
+#pragma unroll
+        for (int cc = 0; cc < 4; ++cc) {
+          const int c = wg * 4 + cc;     // cc's parity is c's: static indices into av
+          const int col = tl.n0 + c * 32;
+          if (col >= g.N) break;
+          uint32_t r[32];
+          tmem_ld32(tb + c * 32, r);
+          tmem_wait_ld();
+          if (g.out2) {
+            uint32_t hv[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+              hv[i] = pack_bf16x2(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1]));
+            put(hv, &tmC, col);
+          }
+          if constexpr (ACT == MOE_ACT_SRELU) {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              const float h0 = fmaxf(__uint_as_float(r[2 * i]), 0.f);
+              const float h1 = fmaxf(__uint_as_float(r[2 * i + 1]), 0.f);
+              av[i] = pack_bf16x2(h0 * h0, h1 * h1);
+              amx = fmaxf(amx, fmaxf(bf16_lo(av[i]), bf16_hi(av[i])));
+            }
+            put(av, &tmD, col);
+          } else {
+            const int h = (cc & 1) * 8;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              const float a0 = gate_phi<ACT>(__uint_as_float(r[4 * i + 0])) * __uint_as_float(r[4 * i + 1]);
+              const float a1 = gate_phi<ACT>(__uint_as_float(r[4 * i + 2])) * __uint_as_float(r[4 * i + 3]);
+              av[h + i] = pack_bf16x2(a0, a1);
+              amx = fmaxf(amx, fmaxf(fabsf(bf16_lo(av[h + i])), fabsf(bf16_hi(av[h + i]))));
+            }
+            if (cc & 1) put(av, &tmD, (col - 32) / 2);
+          }
+        }
+      } else if (C::STO && KIND != GemmKind::kFc1Act && g.tma_out && q * 32 + 32 <= tl.rows) {
         // the warp's 32 rows all lie in the expert: stage each 32 x 32 chunk
         // (64-byte swizzle: 16-byte chunk j of row r at j ^ ((r / 2) % 4))
         // and write it with a TMA store
@@ -1046,7 +1109,7 @@ constexpr int kMaxDevices = 64;
 template <GemmKind KIND, int ACT, bool MX = false, bool SKINNY = false, bool GATHER = false,
           bool PAIR = false>
 cudaError_t launch_t(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tc,
-                     const GemmArgs& g, int num_sms, cudaStream_t s) {
+                     const CUtensorMap& td, const GemmArgs& g, int num_sms, cudaStream_t s) {
   auto kern = grouped_gemm_kernel<KIND, ACT, MX, kCluster, SKINNY, GATHER, PAIR>;
   static_assert(smem_bytes<KIND, SKINNY, PAIR>(MOE_MAX_EXPERTS) <= 227 * 1024,
                 "dynamic shared memory above the 227 KB a CTA may have");
@@ -1092,17 +1155,18 @@ cudaError_t launch_t(const CUtensorMap& ta, const CUtensorMap& tb, const CUtenso
   at[0].val.clusterDim.z = 1;
   cfg.attrs = at;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kern, ta, tb, tc, g);
+  return cudaLaunchKernelEx(&cfg, kern, ta, tb, tc, td, g);
 }
 
 // ragged-row kind in pair mode or not, per activation
 template <GemmKind KIND, bool MX, bool PAIR>
 cudaError_t launch_act(int act, const CUtensorMap& ta, const CUtensorMap& tb,
-                       const CUtensorMap& tc, const GemmArgs& g, int num_sms, cudaStream_t s) {
+                       const CUtensorMap& tc, const CUtensorMap& td, const GemmArgs& g,
+                       int num_sms, cudaStream_t s) {
   switch (act) {
-    case MOE_ACT_SWIGLU: return launch_t<KIND, MOE_ACT_SWIGLU, MX, false, false, PAIR>(ta, tb, tc, g, num_sms, s);
-    case MOE_ACT_GEGLU: return launch_t<KIND, MOE_ACT_GEGLU, MX, false, false, PAIR>(ta, tb, tc, g, num_sms, s);
-    case MOE_ACT_SRELU: return launch_t<KIND, MOE_ACT_SRELU, MX, false, false, PAIR>(ta, tb, tc, g, num_sms, s);
+    case MOE_ACT_SWIGLU: return launch_t<KIND, MOE_ACT_SWIGLU, MX, false, false, PAIR>(ta, tb, tc, td, g, num_sms, s);
+    case MOE_ACT_GEGLU: return launch_t<KIND, MOE_ACT_GEGLU, MX, false, false, PAIR>(ta, tb, tc, td, g, num_sms, s);
+    case MOE_ACT_SRELU: return launch_t<KIND, MOE_ACT_SRELU, MX, false, false, PAIR>(ta, tb, tc, td, g, num_sms, s);
     default: return cudaErrorInvalidValue;
   }
 }
@@ -1134,7 +1198,8 @@ bool wgrad_skinny(const GemmArgs& g) {
 
 cudaError_t launch_grouped_gemm(GemmKind kind, int act, const CUtensorMap& ta,
                                 const CUtensorMap& tb, const CUtensorMap& tc, const GemmArgs& g_in,
-                                int num_sms, cudaStream_t s, bool mx) {
+                                int num_sms, cudaStream_t s, bool mx, const CUtensorMap* td_in) {
+  const CUtensorMap& td = td_in ? *td_in : tc;
   // Unit order: when an expert has no more row-pair units than column
   // tiles, sweep column tiles outermost, so that a wave of clusters reuses
   // each B column tile across the expert's row pairs while the A block stays
@@ -1162,13 +1227,13 @@ cudaError_t launch_grouped_gemm(GemmKind kind, int act, const CUtensorMap& ta,
     // kernels keep their code and registers
     if (mx) return cudaErrorInvalidValue;
     if (kind == GemmKind::kWgrad)
-      return wgrad_skinny(g) ? launch_t<GemmKind::kWgrad, 0, false, true, true>(ta, tb, tc, g, num_sms, s)
-                             : launch_t<GemmKind::kWgrad, 0, false, false, true>(ta, tb, tc, g, num_sms, s);
+      return wgrad_skinny(g) ? launch_t<GemmKind::kWgrad, 0, false, true, true>(ta, tb, tc, td, g, num_sms, s)
+                             : launch_t<GemmKind::kWgrad, 0, false, false, true>(ta, tb, tc, td, g, num_sms, s);
 #define MOE_GATHER_SWITCH(KIND)                                                                  \
   switch (act) {                                                                                 \
-    case MOE_ACT_SWIGLU: return launch_t<KIND, MOE_ACT_SWIGLU, false, false, true>(ta, tb, tc, g, num_sms, s); \
-    case MOE_ACT_GEGLU: return launch_t<KIND, MOE_ACT_GEGLU, false, false, true>(ta, tb, tc, g, num_sms, s);   \
-    case MOE_ACT_SRELU: return launch_t<KIND, MOE_ACT_SRELU, false, false, true>(ta, tb, tc, g, num_sms, s);   \
+    case MOE_ACT_SWIGLU: return launch_t<KIND, MOE_ACT_SWIGLU, false, false, true>(ta, tb, tc, td, g, num_sms, s); \
+    case MOE_ACT_GEGLU: return launch_t<KIND, MOE_ACT_GEGLU, false, false, true>(ta, tb, tc, td, g, num_sms, s);   \
+    case MOE_ACT_SRELU: return launch_t<KIND, MOE_ACT_SRELU, false, false, true>(ta, tb, tc, td, g, num_sms, s);   \
     default: return cudaErrorInvalidValue;                                                       \
   }
     if (kind == GemmKind::kFc1Act) MOE_GATHER_SWITCH(GemmKind::kFc1Act)
@@ -1178,37 +1243,37 @@ cudaError_t launch_grouped_gemm(GemmKind kind, int act, const CUtensorMap& ta,
   }
   if (mx) {
     if (kind != GemmKind::kFc1Act) return cudaErrorInvalidValue;
-    return use_pair(kind, g) ? launch_act<GemmKind::kFc1Act, true, true>(act, ta, tb, tc, g, num_sms, s)
-                             : launch_act<GemmKind::kFc1Act, true, false>(act, ta, tb, tc, g, num_sms, s);
+    return use_pair(kind, g) ? launch_act<GemmKind::kFc1Act, true, true>(act, ta, tb, tc, td, g, num_sms, s)
+                             : launch_act<GemmKind::kFc1Act, true, false>(act, ta, tb, tc, td, g, num_sms, s);
   }
   if (use_pair(kind, g)) {
     switch (kind) {
-      case GemmKind::kFc1Act: return launch_act<GemmKind::kFc1Act, false, true>(act, ta, tb, tc, g, num_sms, s);
-      case GemmKind::kDgradAct: return launch_act<GemmKind::kDgradAct, false, true>(act, ta, tb, tc, g, num_sms, s);
-      case GemmKind::kFc2: return launch_t<GemmKind::kFc2, 0, false, false, false, true>(ta, tb, tc, g, num_sms, s);
-      case GemmKind::kDgrad: return launch_t<GemmKind::kDgrad, 0, false, false, false, true>(ta, tb, tc, g, num_sms, s);
+      case GemmKind::kFc1Act: return launch_act<GemmKind::kFc1Act, false, true>(act, ta, tb, tc, td, g, num_sms, s);
+      case GemmKind::kDgradAct: return launch_act<GemmKind::kDgradAct, false, true>(act, ta, tb, tc, td, g, num_sms, s);
+      case GemmKind::kFc2: return launch_t<GemmKind::kFc2, 0, false, false, false, true>(ta, tb, tc, td, g, num_sms, s);
+      case GemmKind::kDgrad: return launch_t<GemmKind::kDgrad, 0, false, false, false, true>(ta, tb, tc, td, g, num_sms, s);
       default: break;   // kWgrad: below
     }
   }
 #define MOE_ACT_SWITCH(KIND)                                                         \
   switch (act) {                                                                     \
-    case MOE_ACT_SWIGLU: return launch_t<KIND, MOE_ACT_SWIGLU>(ta, tb, tc, g, num_sms, s); \
-    case MOE_ACT_GEGLU: return launch_t<KIND, MOE_ACT_GEGLU>(ta, tb, tc, g, num_sms, s);   \
-    case MOE_ACT_SRELU: return launch_t<KIND, MOE_ACT_SRELU>(ta, tb, tc, g, num_sms, s);   \
+    case MOE_ACT_SWIGLU: return launch_t<KIND, MOE_ACT_SWIGLU>(ta, tb, tc, td, g, num_sms, s); \
+    case MOE_ACT_GEGLU: return launch_t<KIND, MOE_ACT_GEGLU>(ta, tb, tc, td, g, num_sms, s);   \
+    case MOE_ACT_SRELU: return launch_t<KIND, MOE_ACT_SRELU>(ta, tb, tc, td, g, num_sms, s);   \
     default: return cudaErrorInvalidValue;                                           \
   }
   switch (kind) {
     case GemmKind::kFc1Act: MOE_ACT_SWITCH(GemmKind::kFc1Act)
     case GemmKind::kDgradAct: MOE_ACT_SWITCH(GemmKind::kDgradAct)
-    case GemmKind::kFc2: return launch_t<GemmKind::kFc2, 0>(ta, tb, tc, g, num_sms, s);
-    case GemmKind::kDgrad: return launch_t<GemmKind::kDgrad, 0>(ta, tb, tc, g, num_sms, s);
+    case GemmKind::kFc2: return launch_t<GemmKind::kFc2, 0>(ta, tb, tc, td, g, num_sms, s);
+    case GemmKind::kDgrad: return launch_t<GemmKind::kDgrad, 0>(ta, tb, tc, td, g, num_sms, s);
     case GemmKind::kWgrad:
       if (use_pair(kind, g))
         return wgrad_skinny(g)
-                   ? launch_t<GemmKind::kWgrad, 0, false, true, false, true>(ta, tb, tc, g, num_sms, s)
-                   : launch_t<GemmKind::kWgrad, 0, false, false, false, true>(ta, tb, tc, g, num_sms, s);
-      return wgrad_skinny(g) ? launch_t<GemmKind::kWgrad, 0, false, true>(ta, tb, tc, g, num_sms, s)
-                             : launch_t<GemmKind::kWgrad, 0, false, false>(ta, tb, tc, g, num_sms, s);
+                   ? launch_t<GemmKind::kWgrad, 0, false, true, false, true>(ta, tb, tc, td, g, num_sms, s)
+                   : launch_t<GemmKind::kWgrad, 0, false, false, false, true>(ta, tb, tc, td, g, num_sms, s);
+      return wgrad_skinny(g) ? launch_t<GemmKind::kWgrad, 0, false, true>(ta, tb, tc, td, g, num_sms, s)
+                             : launch_t<GemmKind::kWgrad, 0, false, false>(ta, tb, tc, td, g, num_sms, s);
   }
 #undef MOE_ACT_SWITCH
   return cudaErrorInvalidValue;

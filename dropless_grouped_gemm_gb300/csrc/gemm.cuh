@@ -64,7 +64,8 @@ struct GemmArgs {
   // kFc2 / kDgrad: 1 = tmC maps `out` as [M_cap, N] bf16 (ldo == N), box 32
   // columns x 32 rows with 64-byte swizzle, and the epilogue writes whole
   // 32-row groups of a tile with staged TMA stores (a ragged last group of
-  // an expert with plain stores); 0 = plain stores throughout
+  // an expert with plain stores); 0 = plain stores throughout.  kFc1Act
+  // (bf16 outputs): the same for H (out2, tmC) and A (out, tmD)
   int tma_out;
   // gathered operand (the permute fused into the operand load): the
   // operand's expert-major row r is row gather_pair[r] / gather_k of the
@@ -82,11 +83,14 @@ struct GemmArgs {
 
 // Launches the persistent grouped GEMM of `kind` (act: MOE_ACT_*) on `s`.
 // tc: the output's tensor map for kWgrad ([E, R, N] bf16, see wgrad_skinny
-// for its box); unused (any valid map) for the other kinds.
+// for its box), and with tma_out for kFc2 / kDgrad (out) and kFc1Act (H,
+// out2); td: with tma_out, kFc1Act's A (out).  Both [rows, cols] maps of
+// tma_out have 32 x 32 boxes with 64-byte swizzle.  Unused maps may be any
+// valid map (td defaults to tc).
 cudaError_t launch_grouped_gemm(GemmKind kind, int act, const CUtensorMap& ta,
                                 const CUtensorMap& tb, const CUtensorMap& tc,
                                 const GemmArgs& args, int num_sms, cudaStream_t s,
-                                bool mx = false);
+                                bool mx = false, const CUtensorMap* td = nullptr);
 
 // Weight gradients use the skinny-expert configuration when the average
 // rows per expert (M_cap / E, known on the host without reading counts) is
