@@ -37,9 +37,10 @@ void ev_end(cudaStream_t s) {
   }
 }
 cudaError_t gemm(moe::GemmKind kind, int act, const CUtensorMap& ta, const CUtensorMap& tb,
-                 const CUtensorMap& tc, const moe::GemmArgs& g, int sms, cudaStream_t s) {
+                 const CUtensorMap& tc, const moe::GemmArgs& g, int sms, cudaStream_t s,
+                 const CUtensorMap* td = nullptr) {
   ev_begin(s);
-  const cudaError_t e = moe::launch_grouped_gemm(kind, act, ta, tb, tc, g, sms, s);
+  const cudaError_t e = moe::launch_grouped_gemm(kind, act, ta, tb, tc, g, sms, s, false, td);
   ev_end(s);
   return e;
 }
@@ -228,7 +229,12 @@ int bwd_gemms(const moe_bf16* x_perm, const moe_bf16* h_saved, const moe_bf16* a
     g.ds_part = ds_part; g.ds_parts = (n + 127) / 128;
   }
   set_gather(g, 0, do_tok);
-  cudaError_t e = gemm(moe::GemmKind::kDgradAct, act, t_dy_k, t_w2_k, t_dy_k, g, sms, s);
+  // dH (and A') leave through staged TMA stores
+  CUtensorMap t_dh_o, t_as_o = t_dy_k;
+  if (!map_out2(&t_dh_o, dh, M_cap, n1) || (probs && !map_out2(&t_as_o, a_scaled, M_cap, n)))
+    return MOE_E_CUDA;
+  g.tma_out = 1;
+  cudaError_t e = gemm(moe::GemmKind::kDgradAct, act, t_dy_k, t_w2_k, t_dh_o, g, sms, s, &t_as_o);
   if (e != cudaSuccess) return MOE_E_CUDA;
   // 2. dW2_e = A_e^T dY_e
   moe::GemmArgs gw2{};

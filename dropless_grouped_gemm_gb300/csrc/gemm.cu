@@ -69,8 +69,8 @@ struct Cfg {
   // FC2 and FC1-dgrad store their bf16 output through one staged 32 x 32
   // box per epilogue warp (their reductions are short enough that plain
   // stores left the epilogue longer than the next tile's MMAs)
-  static constexpr bool STO =
-      (KIND == GemmKind::kFc2 || KIND == GemmKind::kDgrad || KIND == GemmKind::kFc1Act);
+  static constexpr bool STO = (KIND == GemmKind::kFc2 || KIND == GemmKind::kDgrad ||
+                               KIND == GemmKind::kFc1Act || KIND == GemmKind::kDgradAct);
   static constexpr int box_cols = SKINNY ? 64 : 32;
   static constexpr int box_bytes = 32 * box_cols * 2;
   static constexpr int nbuf = SKINNY ? 2 : 1;
@@ -262,19 +262,49 @@ __device__ __forceinline__ void epilogue_chunk(const GemmArgs& g, const Tile& tl
 //    Rows past the tile's valid rows count as zero; tiles start on an
 //    expert's first row plus a multiple of 128, so the blocks run from each
 //    expert's first row.
+// 16 packed bf16 pairs of each lane's row into the warp's 32 x 32 box
+// (64-byte swizzle: 16-byte chunk j of row r at j ^ ((r / 2) % 4)) and one
+// TMA store of the box at (x, y); the box is reused once its previous store
+// has read it.  Whole warps call it.
+__device__ __forceinline__ void put_box32(uint8_t* box, const uint32_t* v, const CUtensorMap* m,
+                                          int x, int y) {
+  const int lane = threadIdx.x & 31;
+  if (lane == 0) bulk_wait_read_0();
+  __syncwarp();
+  uint8_t* row = box + lane * 64;
+  const int sw = (lane >> 1) & 3;
+#pragma unroll
+  for (int j = 0; j < 4; ++j)
+    *reinterpret_cast<uint4*>(row + ((j ^ sw) * 16)) =
+        make_uint4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+  fence_proxy_async_smem();
+  __syncwarp();
+  if (lane == 0) {
+    tma_store_2d(m, box, x, y);
+    bulk_commit();
+  }
+}
+
+// box != nullptr: the warp's 32 rows all lie in the expert, and dH (tdh,
+// [M_cap, ldo]) and A' (ta, [M_cap, ldo3]) leave through the warp's box and
+// TMA stores instead of per-thread stores
 template <int ACT>
 __device__ __forceinline__ float dgrad_act_chunk(const GemmArgs& g, const Tile& tl, int row_in_tile,
                                                  int col, float p, const uint32_t (&r)[32],
-                                                 float& amx) {
+                                                 float& amx, uint8_t* box = nullptr,
+                                                 const CUtensorMap* tdh = nullptr,
+                                                 const CUtensorMap* ta = nullptr) {
   constexpr bool GATED = (ACT != MOE_ACT_SRELU);
   constexpr int NV = GATED ? 64 : 32;  // dH values of the chunk
   const bool valid = row_in_tile < tl.rows;
   const bool routed = g.probs != nullptr;
   const long long grow = tl.row0 + row_in_tile;
+  const int y0 = tl.row0 + (row_in_tile & ~31);   // the warp's first row (staged stores)
   float dh[NV];
   float ds = 0.f;
   if (valid) {
     uint32_t ap[16];  // routed: A' of the chunk's 32 dA columns, packed bf16 pairs
+    uint32_t ob[16];  // staged: the box being filled
     if constexpr (!GATED) {
       const uint16_t* hp = g.aux + grow * g.ld_aux + col;
       uint16_t* pd = g.out + grow * g.ldo + col;
@@ -298,7 +328,13 @@ __device__ __forceinline__ float dgrad_act_chunk(const GemmArgs& g, const Tile& 
           dh[8 * v + 2 * i] = bf16_lo(o[i]);
           dh[8 * v + 2 * i + 1] = bf16_hi(o[i]);
         }
-        st_global_v4(pd + 8 * v, o[0], o[1], o[2], o[3]);
+        if (box) {
+#pragma unroll
+          for (int i = 0; i < 4; ++i) ob[4 * v + i] = o[i];
+          if (v == 3) put_box32(box, ob, tdh, col, y0);
+        } else {
+          st_global_v4(pd + 8 * v, o[0], o[1], o[2], o[3]);
+        }
       }
     } else {
       const uint16_t* hp = g.aux + grow * g.ld_aux + 2 * col;
@@ -328,13 +364,23 @@ __device__ __forceinline__ float dgrad_act_chunk(const GemmArgs& g, const Tile& 
           ap[2 * v] = pack_bf16x2(p * a[0], p * a[1]);
           ap[2 * v + 1] = pack_bf16x2(p * a[2], p * a[3]);
         }
-        st_global_v4(pd + 8 * v, o[0], o[1], o[2], o[3]);
+        if (box) {
+#pragma unroll
+          for (int i = 0; i < 4; ++i) ob[4 * (v & 3) + i] = o[i];
+          if ((v & 3) == 3) put_box32(box, ob, tdh, 2 * col + 32 * (v >> 2), y0);
+        } else {
+          st_global_v4(pd + 8 * v, o[0], o[1], o[2], o[3]);
+        }
       }
     }
     if (routed) {
-      uint16_t* pa = g.out3 + grow * g.ldo3 + col;
+      if (box) {
+        put_box32(box, ap, ta, col, y0);
+      } else {
+        uint16_t* pa = g.out3 + grow * g.ldo3 + col;
 #pragma unroll
-      for (int v = 0; v < 4; ++v) st_global_v4(pa + 8 * v, ap[4 * v], ap[4 * v + 1], ap[4 * v + 2], ap[4 * v + 3]);
+        for (int v = 0; v < 4; ++v) st_global_v4(pa + 8 * v, ap[4 * v], ap[4 * v + 1], ap[4 * v + 2], ap[4 * v + 3]);
+      }
     }
   } else {
 #pragma unroll
@@ -485,7 +531,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     prefetch_tmap(&tmA);
     prefetch_tmap(&tmB);
     if (KIND == GemmKind::kWgrad || (C::STO && g.tma_out)) prefetch_tmap(&tmC);
-    if (KIND == GemmKind::kFc1Act && !MX && g.tma_out) prefetch_tmap(&tmD);
+    if ((KIND == GemmKind::kFc1Act && !MX) || KIND == GemmKind::kDgradAct)
+      if (g.tma_out) prefetch_tmap(&tmD);
   }
   if (KIND == GemmKind::kWgrad && warp >= 2) {  // epilogue threads clear the zero box
     for (int i = threadIdx.x - 64; i < BOX / 16; i += 32 * EPI_WARPS)
@@ -967,12 +1014,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           const int pr = g.pair_of_row[grow];
           p = pr >= 0 ? g.probs[pr] : 0.f;
         }
+        // the warp's 32 rows all in the expert: staged TMA stores of dH (and A')
+        uint8_t* box = (g.tma_out && q * 32 + 32 <= tl.rows) ? staging + (warp - 2) * BOX : nullptr;
         for (int c = wg * 4; c < wg * 4 + 4; ++c) {
           uint32_t r[32];
           tmem_ld32(tb + c * 32, r);
           tmem_wait_ld();
           const int col = tl.n0 + c * 32;
-          if (col < g.N) dsum += dgrad_act_chunk<ACT>(g, tl, row_in_tile, col, p, r, amx);
+          if (col < g.N) dsum += dgrad_act_chunk<ACT>(g, tl, row_in_tile, col, p, r, amx, box, &tmC, &tmD);
         }
         const int half = tl.n0 + wg * 128;
         if (g.probs != nullptr && vrow && half < g.N) g.ds_part[grow * g.ds_parts + half / 128] = dsum;
