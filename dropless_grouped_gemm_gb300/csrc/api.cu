@@ -487,13 +487,12 @@ int moe_grouped_mlp_fwd(const moe_bf16* x_perm, const int32_t* offsets, int E, i
     g1.mx_q = mx->a_q; g1.mx_s = mx->a_s; g1.mx_qT = mx->a_qT;
     g1.mx_sT = mx->a_qT ? mx->a_sT : nullptr; g1.n_a = n;
   }
-  // bf16 FC1: H and A leave through staged TMA stores
+  // H and A leave through staged TMA stores (with MXFP8 outputs, the
+  // transposed copy goes through the same staging box)
   CUtensorMap th = tx, tao = tx;
-  if (!use_mx) {
-    if ((save_h && !map_out2(&th, h_saved, M_cap, n1)) || !map_out2(&tao, a, M_cap, n))
-      return MOE_E_CUDA;
-    g1.tma_out = 1;
-  }
+  if ((save_h && !map_out2(&th, h_saved, M_cap, n1)) || !map_out2(&tao, a, M_cap, n))
+    return MOE_E_CUDA;
+  g1.tma_out = 1;
   ev_begin(s);
   cudaError_t e = moe::launch_grouped_gemm(moe::GemmKind::kFc1Act, act, tx, tw1, th, g1, sms, s,
                                            use_mx, &tao);

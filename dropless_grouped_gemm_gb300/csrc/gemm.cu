@@ -408,7 +408,10 @@ __device__ __forceinline__ float dgrad_act_chunk(const GemmArgs& g, const Tile& 
 template <int ACT>
 __device__ __forceinline__ void fc1_mx_block(const GemmArgs& g, const Tile& tl, int row_in_tile,
                                              int lane, int q, int cb, const uint32_t (&r0)[32],
-                                             const uint32_t (&r1)[32], float& amx) {
+                                             const uint32_t (&r1)[32], float& amx,
+                                             uint8_t* box = nullptr,
+                                             const CUtensorMap* th = nullptr,
+                                             const CUtensorMap* ta = nullptr) {
   constexpr bool GATED = (ACT != MOE_ACT_SRELU);
   const int acc_col = tl.n0 + cb * (GATED ? 64 : 32);
   if (acc_col >= g.N) return;                       // uniform across the CTA
@@ -439,6 +442,59 @@ __device__ __forceinline__ void fc1_mx_block(const GemmArgs& g, const Tile& tl, 
   const int b = acol / 32;
   uint32_t qw[8];
   const uint32_t sc = mx_quant32(a, qw);
+  if (box != nullptr) {
+    // the warp's 32 rows all lie in the expert (MXFP8 experts are whole
+    // 32-row blocks): H and A through the warp's box and TMA stores; the
+    // transposed copy through the same box, rows written with a skew (row
+    // r's 16-byte chunk j at (j + r/2) % 4, no bank conflicts either way)
+    // so that lane c reads column c and quantises it as one 32 x 1 block
+    const int y0 = tl.row0 + q * 32;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) amx = fmaxf(amx, fabsf(a[i]));
+    if (g.out2) {
+      uint32_t hv[16];
+#pragma unroll
+      for (int i = 0; i < 16; ++i) hv[i] = pack_bf16x2(__uint_as_float(r0[2 * i]), __uint_as_float(r0[2 * i + 1]));
+      put_box32(box, hv, th, acc_col, y0);
+      if constexpr (GATED) {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) hv[i] = pack_bf16x2(__uint_as_float(r1[2 * i]), __uint_as_float(r1[2 * i + 1]));
+        put_box32(box, hv, th, acc_col + 32, y0);
+      }
+    }
+    put_box32(box, pk, ta, acol, y0);
+    uint4* pq = reinterpret_cast<uint4*>(g.mx_q + grow * g.n_a + acol);
+    pq[0] = make_uint4(qw[0], qw[1], qw[2], qw[3]);
+    pq[1] = make_uint4(qw[4], qw[5], qw[6], qw[7]);
+    const long long chunk = static_cast<long long>(tl.row0 / 32) * (g.n_a / 128) + b / 4;
+    g.mx_s[chunk * 512 + mx_chunk_off(row_in_tile, b & 3)] = static_cast<uint8_t>(sc);
+    if (g.mx_qT != nullptr) {
+      if (lane == 0) bulk_wait_read_0();   // A's store has read the box
+      __syncwarp();
+      uint8_t* myrow = box + lane * 64;
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        *reinterpret_cast<uint4*>(myrow + (((j + (lane >> 1)) & 3) * 16)) =
+            make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
+      __syncwarp();
+      float col[32];
+      const int cj = lane >> 3, ce = (lane & 7) * 2;
+#pragma unroll
+      for (int rr = 0; rr < 32; ++rr) {
+        const uint16_t bv =
+            *reinterpret_cast<const uint16_t*>(box + rr * 64 + (((cj + (rr >> 1)) & 3) * 16) + ce);
+        col[rr] = __uint_as_float(static_cast<uint32_t>(bv) << 16);
+      }
+      __syncwarp();
+      uint32_t cq[8];
+      const uint32_t csc = mx_quant32(col, cq);
+      uint4* pt = reinterpret_cast<uint4*>(g.mx_qT + static_cast<long long>(acol + lane) * g.M_cap + y0);
+      pt[0] = make_uint4(cq[0], cq[1], cq[2], cq[3]);
+      pt[1] = make_uint4(cq[4], cq[5], cq[6], cq[7]);
+      g.mx_sT[static_cast<long long>(acol + lane) * (g.M_cap / 32) + y0 / 32] = static_cast<uint8_t>(csc);
+    }
+    return;
+  }
   if (valid) {
 #pragma unroll
     for (int i = 0; i < 32; ++i) amx = fmaxf(amx, fabsf(a[i]));
@@ -531,7 +587,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     prefetch_tmap(&tmA);
     prefetch_tmap(&tmB);
     if (KIND == GemmKind::kWgrad || (C::STO && g.tma_out)) prefetch_tmap(&tmC);
-    if ((KIND == GemmKind::kFc1Act && !MX) || KIND == GemmKind::kDgradAct)
+    if (KIND == GemmKind::kFc1Act || KIND == GemmKind::kDgradAct)
       if (g.tma_out) prefetch_tmap(&tmD);
   }
   if (KIND == GemmKind::kWgrad && warp >= 2) {  // epilogue threads clear the zero box
@@ -930,12 +986,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const uint32_t tb = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + buf * BN;
       if constexpr (KIND == GemmKind::kFc1Act && MX) {
         constexpr int STEP = (ACT == MOE_ACT_SRELU) ? 32 : 64;
+        // the warp's 32 rows in the expert: staged stores and transpose
+        uint8_t* mbox = (g.tma_out && q * 32 < tl.rows) ? staging + (warp - 2) * BOX : nullptr;
         for (int cb = wg * (BN / STEP / 2); cb < (wg + 1) * (BN / STEP / 2); ++cb) {
           uint32_t r0[32], r1[32];
           tmem_ld32(tb + cb * STEP, r0);
           if constexpr (STEP == 64) tmem_ld32(tb + cb * STEP + 32, r1);
           tmem_wait_ld();
-          fc1_mx_block<ACT>(g, tl, row_in_tile, lane, q, cb, r0, r1, amx);
+          fc1_mx_block<ACT>(g, tl, row_in_tile, lane, q, cb, r0, r1, amx, mbox, &tmC, &tmD);
         }
       } else if (KIND == GemmKind::kWgrad && tl.kblocks == 0 && g.accumulate) {
         // expert with no rows, accumulating: its weight gradient is untouched
