@@ -934,10 +934,14 @@ int moe_grouped_mlp_bwd_mx(const moe_bf16* x_perm, const moe_bf16* h_saved,
   g.err = err;
   g.a_s_bytes = static_cast<long long>(M_cap) * d / 8;
   g.b_s_bytes = static_cast<long long>(E) * n * d / 32;
+  CUtensorMap t_dh_o = t_dy;
   if (fuse_dh) {
     g.dh_q = ws.dh_q; g.dh_s = ws.dh_s; g.dh_qT = ws.dh_qT; g.dh_sT = ws.dh_sT; g.n1 = n1;
+    // the fused epilogue stages dH's bf16 blocks and writes them with TMA stores
+    if (!map_out2(&t_dh_o, dh, M_cap, n1)) return MOE_E_CUDA;
+    g.tma_out = 1;
   }
-  e = mx_gemm(moe::MxKind::kDgradAct, act, t_dy, t_w2, t_dy, g, sms, s);
+  e = mx_gemm(moe::MxKind::kDgradAct, act, t_dy, t_w2, t_dh_o, g, sms, s);
   // 5. unfused control: dH both ways in a separate pass
   if (e == cudaSuccess && !fuse_dh) e = quant(dh, n1, ws.dh_q, ws.dh_s, ws.dh_qT, ws.dh_sT);
   if (e != cudaSuccess) return MOE_E_CUDA;

@@ -304,7 +304,7 @@ __device__ __forceinline__ void mx_dact_row32(const MxGemmArgs& g, long long gro
 template <int ACT>
 __device__ __forceinline__ void mx_dact_quant_block(const MxGemmArgs& g, int tl_row0, int q,
                                                     int lane, int hc, const uint32_t* r,
-                                                    uint8_t* box) {
+                                                    uint8_t* box, const CUtensorMap* tdh) {
   const int rt = q * 32 + lane;
   const long long grow = static_cast<long long>(tl_row0) + rt;
   const uint16_t* hp = g.aux + grow * g.ld_aux + hc;
@@ -330,10 +330,12 @@ __device__ __forceinline__ void mx_dact_quant_block(const MxGemmArgs& g, int tl_
       f[8 * v + 2 * i + 1] = bf16_hi(pk[4 * v + i]);
     }
   }
-  uint16_t* p = g.out + grow * g.ldo + hc;
+  if (tdh == nullptr) {
+    uint16_t* p = g.out + grow * g.ldo + hc;
 #pragma unroll
-  for (int v = 0; v < 4; ++v)
-    *reinterpret_cast<uint4*>(p + 8 * v) = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+    for (int v = 0; v < 4; ++v)
+      *reinterpret_cast<uint4*>(p + 8 * v) = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+  }
   // both scale layouts put this 128-row tile's chunk of column group hc / 128 at
   const long long chunk = static_cast<long long>(tl_row0 / 32) * (g.n1 / 128) + hc / 128;
   // row-wise block
@@ -344,6 +346,10 @@ __device__ __forceinline__ void mx_dact_quant_block(const MxGemmArgs& g, int tl_
   pq[1] = make_uint4(qw[4], qw[5], qw[6], qw[7]);
   g.dh_s[chunk * 512 + mx_chunk_off(rt, (hc >> 5) & 3)] = static_cast<uint8_t>(sc);
   // transposed copy: column hc + c over the warp's 32 rows is one block
+  if (tdh != nullptr) {   // the box's previous use was a TMA store: wait until it has read it
+    if (lane == 0) bulk_wait_read_0();
+    __syncwarp();
+  }
   uint8_t* myrow = box + lane * 64;
 #pragma unroll
   for (int j = 0; j < 4; ++j)
@@ -358,7 +364,21 @@ __device__ __forceinline__ void mx_dact_quant_block(const MxGemmArgs& g, int tl_
         box + rr * 64 + (((cj + (rr >> 1)) & 3) * 16) + ce);
     col[rr] = __uint_as_float(static_cast<uint32_t>(b) << 16);
   }
-  __syncwarp();   // the box is free for the next block
+  __syncwarp();   // the box is free for dH's staged store or the next block
+  if (tdh != nullptr) {
+    // dH's 32 x 32 block: 64-byte swizzle (chunk j of row r at j ^ ((r/2) % 4)), TMA store
+    const int sw = (lane >> 1) & 3;
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      *reinterpret_cast<uint4*>(myrow + ((j ^ sw) * 16)) =
+          make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) {
+      tma_store_2d(tdh, box, hc, tl_row0 + q * 32);
+      bulk_commit();
+    }
+  }
   uint32_t cq[8];
   const uint32_t csc = mx_quant32(col, cq);
   uint4* pt = reinterpret_cast<uint4*>(g.dh_qT + static_cast<long long>(hc + lane) * g.M_cap +
@@ -421,7 +441,7 @@ __global__ void __launch_bounds__(QTHREADS, 1)
     fence_mbar_init();
     prefetch_tmap(&tmA);
     prefetch_tmap(&tmB);
-    if (W) prefetch_tmap(&tmC);
+    if (W || (g.tma_out && (QCfg<KIND, PAIR>::STO || KIND == MxKind::kDgradAct))) prefetch_tmap(&tmC);
     if (PAIR) {
       prefetch_tmap(&tmSA);
       prefetch_tmap(&tmSB);
@@ -813,7 +833,8 @@ __global__ void __launch_bounds__(QTHREADS, 1)
           for (int b = 0; b < 32 / BLK; ++b) {
             const int dcol = col0 + 32 * c + b * BLK;          // first dA column
             mx_dact_quant_block<ACT>(g, tl.row0, q, lane, (ACT == MOE_ACT_SRELU) ? dcol : 2 * dcol,
-                                     src + b * BLK, staging + (warp - 2) * (32 * 32 * 2));
+                                     src + b * BLK, staging + (warp - 2) * (32 * 32 * 2),
+                                     g.tma_out ? &tmC : nullptr);
           }
         }
         continue;
@@ -912,7 +933,7 @@ __global__ void __launch_bounds__(QTHREADS, 1)
         }
       }
     }
-    if ((W || QCfg<KIND, PAIR>::STO) && lane == 0) bulk_wait_all();  // staged stores done before the CTA exits
+    if ((W || QCfg<KIND, PAIR>::TBOX) && lane == 0) bulk_wait_all();  // staged stores done before the CTA exits
     __syncwarp();
   }
   tc_fence_before();
