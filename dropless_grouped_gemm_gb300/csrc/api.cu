@@ -22,6 +22,9 @@ cudaError_t launch_bounded_wait_selftest(int limit_us, int32_t* err, int32_t* wa
 namespace {
 
 thread_local int g_last_launches = 0;
+// kernels beyond one that launch_grouped_gemm made for a call (a skinny
+// layer's GEMM splits its hot experts into a launch of their own)
+thread_local int g_split_extra = 0;
 thread_local cudaEvent_t const* g_events = nullptr;
 thread_local int g_events_n = 0;
 thread_local int g_events_used = 0;
@@ -40,7 +43,10 @@ cudaError_t gemm(moe::GemmKind kind, int act, const CUtensorMap& ta, const CUten
                  const CUtensorMap& tc, const moe::GemmArgs& g, int sms, cudaStream_t s,
                  const CUtensorMap* td = nullptr) {
   ev_begin(s);
-  const cudaError_t e = moe::launch_grouped_gemm(kind, act, ta, tb, tc, g, sms, s, false, td);
+  int launched = 1;
+  const cudaError_t e =
+      moe::launch_grouped_gemm(kind, act, ta, tb, tc, g, sms, s, false, td, &launched);
+  g_split_extra += launched - 1;
   ev_end(s);
   return e;
 }
@@ -242,7 +248,11 @@ int bwd_gemms(const moe_bf16* x_perm, const moe_bf16* h_saved, const moe_bf16* a
   gw2.out = dW2; gw2.ldo = d; gw2.out_estride = static_cast<long long>(n) * d; gw2.err = err;
   gw2.accumulate = accumulate;
   set_gather(gw2, 1, do_tok);
-  e = gemm(moe::GemmKind::kWgrad, 0, t_a_mn, t_dy_mn, t_dw2, gw2, sms, s);
+  // a skinny layer's hot experts run with the large-expert staging: its box
+  CUtensorMap t_dw2_l, t_dw1_l;
+  if (skinny && (!map_out3(&t_dw2_l, dW2, E, n, d, false) || !map_out3(&t_dw1_l, dW1, E, d, n1, false)))
+    return MOE_E_CUDA;
+  e = gemm(moe::GemmKind::kWgrad, 0, t_a_mn, t_dy_mn, t_dw2, gw2, sms, s, skinny ? &t_dw2_l : nullptr);
   if (e != cudaSuccess) return MOE_E_CUDA;
   // 3. dX = dH W1^T
   moe::GemmArgs gd{};
@@ -259,9 +269,9 @@ int bwd_gemms(const moe_bf16* x_perm, const moe_bf16* h_saved, const moe_bf16* a
   gw1.out = dW1; gw1.ldo = n1; gw1.out_estride = static_cast<long long>(d) * n1; gw1.err = err;
   gw1.accumulate = accumulate;
   set_gather(gw1, 0, x_tok);
-  e = gemm(moe::GemmKind::kWgrad, 0, t_x_mn, t_dh_mn, t_dw1, gw1, sms, s);
+  e = gemm(moe::GemmKind::kWgrad, 0, t_x_mn, t_dh_mn, t_dw1, gw1, sms, s, skinny ? &t_dw1_l : nullptr);
   if (e != cudaSuccess) return MOE_E_CUDA;
-  g_last_launches = 4;
+  g_last_launches = 4 + g_split_extra;
   return MOE_OK;
 }
 
@@ -275,11 +285,12 @@ int moe_last_launch_count(void) { return g_last_launches; }
 
 int moe_selftest_bounded_wait(int limit_us, int32_t* err, int32_t* waited_us, void* stream) {
   g_last_launches = 0;
+  g_split_extra = 0;
   if (limit_us < 1 || limit_us > 1000000) return MOE_E_SIZE;
   if (!err || !waited_us) return MOE_E_NULL;
   const cudaError_t e = moe::launch_bounded_wait_selftest(limit_us, err, waited_us,
                                                           static_cast<cudaStream_t>(stream));
-  g_last_launches = 1;
+  g_last_launches = 1 + g_split_extra;
   return cuda_rc(e);
 }
 
@@ -296,6 +307,7 @@ int moe_launch_events_used(void) { return g_events_used; }
 int moe_router_topk(const float* logits, int T, int E, int k, int32_t* topk_idx, float* probs,
                     void* stream) {
   g_last_launches = 0;
+  g_split_extra = 0;
   if (T < 0 || E < 1 || E > MOE_MAX_EXPERTS || k < 1 || k > E) return MOE_E_SIZE;
   if (T == 0) return MOE_OK;
   if (!logits || !topk_idx || !probs) return MOE_E_NULL;
@@ -305,7 +317,7 @@ int moe_router_topk(const float* logits, int T, int E, int k, int32_t* topk_idx,
   ev_begin(s);
   const cudaError_t e = moe::launch_router_topk(logits, T, E, k, topk_idx, probs, sms, s);
   ev_end(s);
-  g_last_launches = 1;
+  g_last_launches = 1 + g_split_extra;
   return cuda_rc(e);
 }
 
@@ -319,6 +331,7 @@ int moe_route_offsets(const int32_t* topk_idx, int T, int k, int E, int align, i
                       int32_t* pair_of_row, int32_t* true_total, void* workspace,
                       size_t ws_bytes, int32_t* err, void* stream) {
   g_last_launches = 0;
+  g_split_extra = 0;
   if (T < 0 || k < 1 || E < 1 || E > MOE_MAX_EXPERTS || k > E || align < 1 || align > 4096 ||
       M_cap < 0)
     return MOE_E_SIZE;
@@ -337,7 +350,7 @@ int moe_route_offsets(const int32_t* topk_idx, int T, int k, int E, int align, i
                                           row_of_pair, pair_of_row, true_total, workspace, err,
                                           sms, static_cast<cudaStream_t>(stream), &launches);
   ev_end(static_cast<cudaStream_t>(stream));
-  g_last_launches = launches;
+  g_last_launches = launches + g_split_extra;
   return cuda_rc(e);
 }
 
@@ -346,6 +359,7 @@ int moe_route_logits(const float* logits, int T, int E, int k, int align, int M_
                      int32_t* row_of_pair, int32_t* pair_of_row, int32_t* true_total,
                      void* workspace, size_t ws_bytes, int32_t* err, void* stream) {
   g_last_launches = 0;
+  g_split_extra = 0;
   if (T < 0 || k < 1 || E < 1 || E > MOE_MAX_EXPERTS || k > E || align < 1 || align > 4096 ||
       M_cap < 0)
     return MOE_E_SIZE;
@@ -365,7 +379,7 @@ int moe_route_logits(const float* logits, int T, int E, int k, int align, int M_
                                                  true_total, workspace, err, sms,
                                                  static_cast<cudaStream_t>(stream), &launches);
   ev_end(static_cast<cudaStream_t>(stream));
-  g_last_launches = launches;
+  g_last_launches = launches + g_split_extra;
   return cuda_rc(e);
 }
 
@@ -374,6 +388,7 @@ int moe_route_offsets_noalloc(const int32_t* topk_idx, int T, int k, int E, int 
                               int32_t* pair_of_row, int32_t* true_total, int32_t* err,
                               void* stream) {
   g_last_launches = 0;
+  g_split_extra = 0;
   if (T < 0 || k < 1 || E < 1 || E > MOE_MAX_EXPERTS || k > E || align < 1 || align > 4096 ||
       M_cap < 0)
     return MOE_E_SIZE;
@@ -395,13 +410,14 @@ int moe_route_offsets_noalloc(const int32_t* topk_idx, int T, int k, int E, int 
                                           row_of_pair, pair_of_row, true_total, scratch, err,
                                           sms, static_cast<cudaStream_t>(stream), &launches);
   ev_end(static_cast<cudaStream_t>(stream));
-  g_last_launches = launches;
+  g_last_launches = launches + g_split_extra;
   return cuda_rc(e);
 }
 
 int moe_permute(const moe_bf16* src, const float* scale, const int32_t* pair_of_row, int T, int k,
                 int d, int M_cap, moe_bf16* dst, void* stream) {
   g_last_launches = 0;
+  g_split_extra = 0;
   if (T < 0 || k < 1 || d <= 0 || d % 64 || M_cap < 0) return MOE_E_SIZE;
   if (M_cap == 0) return MOE_OK;
   if (!pair_of_row || !dst || (T > 0 && !src)) return MOE_E_NULL;
@@ -412,7 +428,7 @@ int moe_permute(const moe_bf16* src, const float* scale, const int32_t* pair_of_
   const cudaError_t e = moe::launch_permute(src, scale, pair_of_row, T, k, d, M_cap, dst, sms,
                                             static_cast<cudaStream_t>(stream));
   ev_end(static_cast<cudaStream_t>(stream));
-  g_last_launches = 1;
+  g_last_launches = 1 + g_split_extra;
   return cuda_rc(e);
 }
 
@@ -420,6 +436,7 @@ int moe_unpermute(const moe_bf16* src, const float* probs, const int32_t* row_of
                   int k, int d, int M_cap, moe_bf16* dst, const moe_bf16* dO, float* dprobs,
                   void* stream) {
   g_last_launches = 0;
+  g_split_extra = 0;
   if (T < 0 || k < 1 || d <= 0 || d % 64 || M_cap < 0) return MOE_E_SIZE;
   if (T == 0) return MOE_OK;
   if (!src || !row_of_pair) return MOE_E_NULL;
@@ -434,7 +451,7 @@ int moe_unpermute(const moe_bf16* src, const float* probs, const int32_t* row_of
                                               dprobs, sms, static_cast<cudaStream_t>(stream),
                                               &launches);
   ev_end(static_cast<cudaStream_t>(stream));
-  g_last_launches = launches;
+  g_last_launches = launches + g_split_extra;
   return cuda_rc(e);
 }
 
@@ -443,6 +460,7 @@ int moe_grouped_mlp_fwd(const moe_bf16* x_perm, const int32_t* offsets, int E, i
                         moe_bf16* h_saved, moe_bf16* a, moe_bf16* y_perm, const moe_mx_fwd* mx,
                         float* amax_a, int32_t* err, void* stream) {
   g_last_launches = 0;
+  g_split_extra = 0;
   int rc = check_mlp_sizes(E, M_cap, d, n);
   if (rc) return rc;
   if (act < MOE_ACT_SWIGLU || act > MOE_ACT_SRELU ||
@@ -494,8 +512,10 @@ int moe_grouped_mlp_fwd(const moe_bf16* x_perm, const int32_t* offsets, int E, i
     return MOE_E_CUDA;
   g1.tma_out = 1;
   ev_begin(s);
+  int launched = 1;
   cudaError_t e = moe::launch_grouped_gemm(moe::GemmKind::kFc1Act, act, tx, tw1, th, g1, sms, s,
-                                           use_mx, &tao);
+                                           use_mx, &tao, &launched);
+  g_split_extra += launched - 1;
   ev_end(s);
   if (e != cudaSuccess) return MOE_E_CUDA;
   if (use_mx) {
@@ -513,7 +533,7 @@ int moe_grouped_mlp_fwd(const moe_bf16* x_perm, const int32_t* offsets, int E, i
     e = moe::launch_mx_gemm(moe::MxKind::kFc2, 0, ta, tw2, ty, q, sms, s);
     ev_end(s);
     if (e != cudaSuccess) return MOE_E_CUDA;
-    g_last_launches = 2;
+    g_last_launches = 2 + g_split_extra;
     return MOE_OK;
   }
   moe::GemmArgs g2{};
@@ -524,7 +544,7 @@ int moe_grouped_mlp_fwd(const moe_bf16* x_perm, const int32_t* offsets, int E, i
   g2.tma_out = 1;
   e = gemm(moe::GemmKind::kFc2, 0, ta, tw2, ty, g2, sms, s);
   if (e != cudaSuccess) return MOE_E_CUDA;
-  g_last_launches = 2;
+  g_last_launches = 2 + g_split_extra;
   return MOE_OK;
 }
 
@@ -534,6 +554,7 @@ int moe_grouped_mlp_bwd(const moe_bf16* x_perm, const moe_bf16* h_saved, const m
                         moe_bf16* dh, moe_bf16* dx_perm, moe_bf16* dW1, moe_bf16* dW2,
                         float* amax_dh, int32_t* err, void* stream) {
   g_last_launches = 0;
+  g_split_extra = 0;
   int rc = check_mlp_sizes(E, M_cap, d, n);
   if (rc) return rc;
   if (act < MOE_ACT_SWIGLU || act > MOE_ACT_SRELU || (flags & ~MOE_FLAG_ACCUMULATE_DW))
@@ -570,6 +591,7 @@ int moe_grouped_mlp_bwd_routed(const moe_bf16* x_perm, const moe_bf16* h_saved,
                                moe_bf16* dx_perm, moe_bf16* dW1, moe_bf16* dW2, float* amax_dh,
                                int32_t* err, void* stream) {
   g_last_launches = 0;
+  g_split_extra = 0;
   int rc = check_mlp_sizes(E, M_cap, d, n);
   if (rc) return rc;
   if (act < MOE_ACT_SWIGLU || act > MOE_ACT_SRELU || (flags & ~MOE_FLAG_ACCUMULATE_DW))
@@ -607,6 +629,7 @@ int moe_grouped_mlp_bwd_routed_gather(const moe_bf16* x, const moe_bf16* dO, int
                                       moe_bf16* dW1, moe_bf16* dW2, float* amax_dh, int32_t* err,
                                       void* stream) {
   g_last_launches = 0;
+  g_split_extra = 0;
   int rc = check_mlp_sizes(E, M_cap, d, n);
   if (rc) return rc;
   if (T < 0 || k < 1) return MOE_E_SIZE;
@@ -641,6 +664,7 @@ int moe_grouped_mlp_bwd_routed_gather(const moe_bf16* x, const moe_bf16* dO, int
 int moe_router_grad_rows(const float* ds_part, int n_parts, const int32_t* row_of_pair, int T,
                          int k, int M_cap, float* dprobs, void* stream) {
   g_last_launches = 0;
+  g_split_extra = 0;
   if (T < 0 || k < 1 || n_parts < 1 || M_cap < 0) return MOE_E_SIZE;
   if (T == 0) return MOE_OK;
   if (!ds_part || !row_of_pair || !dprobs) return MOE_E_NULL;
@@ -651,7 +675,7 @@ int moe_router_grad_rows(const float* ds_part, int n_parts, const int32_t* row_o
   const cudaError_t e = moe::launch_router_grad_rows(ds_part, n_parts, row_of_pair, T * k, M_cap,
                                                      dprobs, sms, s);
   ev_end(s);
-  g_last_launches = 1;
+  g_last_launches = 1 + g_split_extra;
   return cuda_rc(e);
 }
 
@@ -664,6 +688,7 @@ int moe_mx_quantize_weights2(const moe_bf16* W2, int E, int n, int d, const int3
                              uint8_t* w2_q, uint8_t* w2_s, uint8_t* w2_q_rows,
                              uint8_t* w2_s_rows, void* stream) {
   g_last_launches = 0;
+  g_split_extra = 0;
   if (E < 1 || E > MOE_MAX_EXPERTS || n <= 0 || d <= 0 || n % 128 || d % 128) return MOE_E_SIZE;
   if (!W2 || !w2_q || !w2_s || (w2_q_rows && !w2_s_rows)) return MOE_E_NULL;
   if (misaligned(W2) || misaligned(w2_q) || misaligned(w2_s) || misaligned(w2_q_rows) ||
@@ -676,7 +701,7 @@ int moe_mx_quantize_weights2(const moe_bf16* W2, int E, int n, int d, const int3
   const cudaError_t e = moe::launch_mx_quantize_weights(W2, E, n, d, offsets, w2_q, w2_s,
                                                         w2_q_rows, w2_s_rows, sms, s);
   ev_end(s);
-  g_last_launches = 1;
+  g_last_launches = 1 + g_split_extra;
   return cuda_rc(e);
 }
 
@@ -716,6 +741,7 @@ int moe_grouped_mlp_fwd_gather(const moe_bf16* x, int T, int k, const int32_t* p
                                moe_bf16* h_saved, moe_bf16* a, moe_bf16* y_perm, float* amax_a,
                                int32_t* err, void* stream) {
   g_last_launches = 0;
+  g_split_extra = 0;
   int rc = check_mlp_sizes(E, M_cap, d, n);
   if (rc) return rc;
   if (T < 0 || k < 1) return MOE_E_SIZE;
@@ -750,8 +776,10 @@ int moe_grouped_mlp_fwd_gather(const moe_bf16* x, int T, int k, const int32_t* p
     return MOE_E_CUDA;
   g1.tma_out = 1;
   ev_begin(s);
+  int launched = 1;
   cudaError_t e = moe::launch_grouped_gemm(moe::GemmKind::kFc1Act, act, tw1, tw1, th, g1, sms, s,
-                                           false, &tao);
+                                           false, &tao, &launched);
+  g_split_extra += launched - 1;
   ev_end(s);
   if (e != cudaSuccess) return MOE_E_CUDA;
   moe::GemmArgs g2{};
@@ -762,7 +790,7 @@ int moe_grouped_mlp_fwd_gather(const moe_bf16* x, int T, int k, const int32_t* p
   g2.tma_out = 1;
   e = gemm(moe::GemmKind::kFc2, 0, ta, tw2, ty, g2, sms, s);
   if (e != cudaSuccess) return MOE_E_CUDA;
-  g_last_launches = 2;
+  g_last_launches = 2 + g_split_extra;
   return MOE_OK;
 }
 
@@ -770,6 +798,7 @@ int moe_grouped_gemm(const moe_bf16* a, const int32_t* offsets, int E, int M_cap
                      const moe_bf16* B, int b_layout, moe_bf16* out, int32_t* err,
                      void* stream) {
   g_last_launches = 0;
+  g_split_extra = 0;
   int rc = check_mlp_sizes(E, M_cap, K, N);
   if (rc) return rc;
   if (b_layout != MOE_B_KN && b_layout != MOE_B_NK) return MOE_E_ARG;
@@ -794,13 +823,14 @@ int moe_grouped_gemm(const moe_bf16* a, const int32_t* offsets, int E, int M_cap
   const cudaError_t e = gemm(b_layout == MOE_B_KN ? moe::GemmKind::kFc2 : moe::GemmKind::kDgrad, 0,
                              ta, tb, to, g, sms, s);
   if (e != cudaSuccess) return MOE_E_CUDA;
-  g_last_launches = 1;
+  g_last_launches = 1 + g_split_extra;
   return MOE_OK;
 }
 
 int moe_activation(const moe_bf16* h, const int32_t* offsets, int E, int M_cap, int n, int act,
                    moe_bf16* a, void* stream) {
   g_last_launches = 0;
+  g_split_extra = 0;
   int rc = check_mlp_sizes(E, M_cap, 64, n);
   if (rc) return rc;
   if (act < MOE_ACT_SWIGLU || act > MOE_ACT_SRELU) return MOE_E_ARG;
@@ -815,13 +845,14 @@ int moe_activation(const moe_bf16* h, const int32_t* offsets, int E, int M_cap, 
   const cudaError_t e = moe::launch_act_fwd(h, offsets, E, M_cap, n, act, a, sms, s);
   ev_end(s);
   if (e != cudaSuccess) return MOE_E_CUDA;
-  g_last_launches = 1;
+  g_last_launches = 1 + g_split_extra;
   return MOE_OK;
 }
 
 int moe_activation_bwd(const moe_bf16* h, const moe_bf16* da, const int32_t* offsets, int E,
                        int M_cap, int n, int act, moe_bf16* dh, void* stream) {
   g_last_launches = 0;
+  g_split_extra = 0;
   int rc = check_mlp_sizes(E, M_cap, 64, n);
   if (rc) return rc;
   if (act < MOE_ACT_SWIGLU || act > MOE_ACT_SRELU) return MOE_E_ARG;
@@ -836,7 +867,7 @@ int moe_activation_bwd(const moe_bf16* h, const moe_bf16* da, const int32_t* off
   const cudaError_t e = moe::launch_act_bwd(h, da, offsets, E, M_cap, n, act, dh, sms, s);
   ev_end(s);
   if (e != cudaSuccess) return MOE_E_CUDA;
-  g_last_launches = 1;
+  g_last_launches = 1 + g_split_extra;
   return MOE_OK;
 }
 
@@ -844,6 +875,7 @@ int moe_mx_quantize_weights_rowwise(const moe_bf16* W, int rows, int cols,
                                     const int32_t* offsets, int E, uint8_t* q, uint8_t* sc,
                                     void* stream) {
   g_last_launches = 0;
+  g_split_extra = 0;
   if (rows <= 0 || cols <= 0 || rows % 128 || cols % 128) return MOE_E_SIZE;
   if (offsets && (E < 1 || E > MOE_MAX_EXPERTS || rows % E || (rows / E) % 128))
     return MOE_E_SIZE;
@@ -856,7 +888,7 @@ int moe_mx_quantize_weights_rowwise(const moe_bf16* W, int rows, int cols,
   const cudaError_t e = moe::launch_mx_quantize_rows_w(W, rows, cols, offsets,
                                                        offsets ? rows / E : rows, q, sc, sms, s);
   ev_end(s);
-  g_last_launches = 1;
+  g_last_launches = 1 + g_split_extra;
   return cuda_rc(e);
 }
 
@@ -866,6 +898,7 @@ int moe_grouped_mlp_bwd_mx(const moe_bf16* x_perm, const moe_bf16* h_saved,
                            moe_bf16* dh, moe_bf16* dx_perm, moe_bf16* dW1, moe_bf16* dW2,
                            int32_t* err, void* stream) {
   g_last_launches = 0;
+  g_split_extra = 0;
   int rc = check_mlp_sizes(E, M_cap, d, n);
   if (rc) return rc;
   if (d % 128 || n % 128 || M_cap % 32) return MOE_E_SIZE;
@@ -975,7 +1008,7 @@ int moe_grouped_mlp_bwd_mx(const moe_bf16* x_perm, const moe_bf16* h_saved,
   gw1.out = dW1; gw1.accumulate = accumulate;
   e = mx_gemm(moe::MxKind::kWgrad, 0, t_xT, t_dhT, t_dw1, gw1, sms, s);
   if (e != cudaSuccess) return MOE_E_CUDA;
-  g_last_launches = fuse_dh ? 7 : 8;
+  g_last_launches = (fuse_dh ? 7 : 8) + g_split_extra;
   return MOE_OK;
 }
 
@@ -983,6 +1016,7 @@ int moe_mx_quantize(const moe_bf16* src, int rows, int cols, const int32_t* offs
                     uint8_t* q, uint8_t* sc, uint8_t* qT, uint8_t* sT, int32_t* err,
                     void* stream) {
   g_last_launches = 0;
+  g_split_extra = 0;
   if (E < 1 || E > MOE_MAX_EXPERTS || rows < 0 || cols <= 0 || rows % 32 || cols % 32)
     return MOE_E_SIZE;
   if (rows == 0) return MOE_OK;
@@ -995,7 +1029,7 @@ int moe_mx_quantize(const moe_bf16* src, int rows, int cols, const int32_t* offs
   const cudaError_t e = moe::launch_mx_quantize_act(src, rows, cols, offsets, E, q, sc, qT, sT,
                                                     err, false, sms, s);
   ev_end(s);
-  g_last_launches = 1;
+  g_last_launches = 1 + g_split_extra;
   return cuda_rc(e);
 }
 
@@ -1003,6 +1037,7 @@ int moe_mx_quantize_tiled(const moe_bf16* src, int rows, int cols, const int32_t
                           int E, uint8_t* q, uint8_t* sc, uint8_t* qT, uint8_t* sT,
                           int32_t* err, void* stream) {
   g_last_launches = 0;
+  g_split_extra = 0;
   if (E < 1 || E > MOE_MAX_EXPERTS || rows < 0 || cols <= 0 || rows % 32 || cols % 32)
     return MOE_E_SIZE;
   if (rows == 0) return MOE_OK;
@@ -1016,7 +1051,7 @@ int moe_mx_quantize_tiled(const moe_bf16* src, int rows, int cols, const int32_t
   const cudaError_t e = moe::launch_mx_quantize_act(src, rows, cols, offsets, E, q, sc, qT, sT,
                                                     err, true, sms, s);
   ev_end(s);
-  g_last_launches = 1;
+  g_last_launches = 1 + g_split_extra;
   return cuda_rc(e);
 }
 

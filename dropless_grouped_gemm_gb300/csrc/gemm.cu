@@ -623,7 +623,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     int carry = 0;
     for (int base = 0; base < g.E; base += 32) {
       const int e = base + lane;
-      const int t = (e < g.E) ? tiles_of_expert<KIND, CL, PAIR>(g, s_off, e) : 0;
+      const int rows_e = (e < g.E) ? s_off[e + 1] - s_off[e] : 0;
+      const bool owned = rows_e >= g.row_min && (g.row_max == 0 || rows_e < g.row_max);
+      const int t = (e < g.E && owned) ? tiles_of_expert<KIND, CL, PAIR>(g, s_off, e) : 0;
       int v = t;
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
@@ -1303,10 +1305,12 @@ bool wgrad_skinny(const GemmArgs& g) {
   return static_cast<long long>(g.M_cap) < static_cast<long long>(kSkinnyRows) * g.E;
 }
 
-cudaError_t launch_grouped_gemm(GemmKind kind, int act, const CUtensorMap& ta,
-                                const CUtensorMap& tb, const CUtensorMap& tc, const GemmArgs& g_in,
-                                int num_sms, cudaStream_t s, bool mx, const CUtensorMap* td_in) {
-  const CUtensorMap& td = td_in ? *td_in : tc;
+namespace {
+// one launch in the given configuration (pair: 2-SM MMAs; skinny: the
+// weight gradient's skinny-expert configuration, whose output box tc has)
+cudaError_t launch_cfg(GemmKind kind, int act, const CUtensorMap& ta, const CUtensorMap& tb,
+                       const CUtensorMap& tc, const CUtensorMap& td, const GemmArgs& g_in,
+                       int num_sms, cudaStream_t s, bool mx, bool pair, bool skinny) {
   // Unit order: when an expert has no more row-pair units than column
   // tiles, sweep column tiles outermost, so that a wave of clusters reuses
   // each B column tile across the expert's row pairs while the A block stays
@@ -1334,7 +1338,7 @@ cudaError_t launch_grouped_gemm(GemmKind kind, int act, const CUtensorMap& ta,
     // kernels keep their code and registers
     if (mx) return cudaErrorInvalidValue;
     if (kind == GemmKind::kWgrad)
-      return wgrad_skinny(g) ? launch_t<GemmKind::kWgrad, 0, false, true, true>(ta, tb, tc, td, g, num_sms, s)
+      return skinny ? launch_t<GemmKind::kWgrad, 0, false, true, true>(ta, tb, tc, td, g, num_sms, s)
                              : launch_t<GemmKind::kWgrad, 0, false, false, true>(ta, tb, tc, td, g, num_sms, s);
 #define MOE_GATHER_SWITCH(KIND)                                                                  \
   switch (act) {                                                                                 \
@@ -1350,10 +1354,10 @@ cudaError_t launch_grouped_gemm(GemmKind kind, int act, const CUtensorMap& ta,
   }
   if (mx) {
     if (kind != GemmKind::kFc1Act) return cudaErrorInvalidValue;
-    return use_pair(kind, g) ? launch_act<GemmKind::kFc1Act, true, true>(act, ta, tb, tc, td, g, num_sms, s)
+    return pair ? launch_act<GemmKind::kFc1Act, true, true>(act, ta, tb, tc, td, g, num_sms, s)
                              : launch_act<GemmKind::kFc1Act, true, false>(act, ta, tb, tc, td, g, num_sms, s);
   }
-  if (use_pair(kind, g)) {
+  if (pair) {
     switch (kind) {
       case GemmKind::kFc1Act: return launch_act<GemmKind::kFc1Act, false, true>(act, ta, tb, tc, td, g, num_sms, s);
       case GemmKind::kDgradAct: return launch_act<GemmKind::kDgradAct, false, true>(act, ta, tb, tc, td, g, num_sms, s);
@@ -1375,15 +1379,43 @@ cudaError_t launch_grouped_gemm(GemmKind kind, int act, const CUtensorMap& ta,
     case GemmKind::kFc2: return launch_t<GemmKind::kFc2, 0>(ta, tb, tc, td, g, num_sms, s);
     case GemmKind::kDgrad: return launch_t<GemmKind::kDgrad, 0>(ta, tb, tc, td, g, num_sms, s);
     case GemmKind::kWgrad:
-      if (use_pair(kind, g))
-        return wgrad_skinny(g)
+      if (pair)
+        return skinny
                    ? launch_t<GemmKind::kWgrad, 0, false, true, false, true>(ta, tb, tc, td, g, num_sms, s)
                    : launch_t<GemmKind::kWgrad, 0, false, false, false, true>(ta, tb, tc, td, g, num_sms, s);
-      return wgrad_skinny(g) ? launch_t<GemmKind::kWgrad, 0, false, true>(ta, tb, tc, td, g, num_sms, s)
+      return skinny ? launch_t<GemmKind::kWgrad, 0, false, true>(ta, tb, tc, td, g, num_sms, s)
                              : launch_t<GemmKind::kWgrad, 0, false, false>(ta, tb, tc, td, g, num_sms, s);
   }
 #undef MOE_ACT_SWITCH
   return cudaErrorInvalidValue;
+}
+}  // namespace
+
+cudaError_t launch_grouped_gemm(GemmKind kind, int act, const CUtensorMap& ta,
+                                const CUtensorMap& tb, const CUtensorMap& tc, const GemmArgs& g,
+                                int num_sms, cudaStream_t s, bool mx, const CUtensorMap* td_in,
+                                int* launched) {
+  const CUtensorMap& td = td_in ? *td_in : tc;
+  if (launched) *launched = 1;
+  if (g.gather_pair == nullptr && g.row_min == 0 && g.row_max == 0 && g.E > 1 &&
+      g_pair_mode.load() == kPairAuto && !use_pair(kind, g)) {
+    // A skinny layer's experts of kPairRows rows or more (hot experts of a
+    // fine-grained layer) run first with the pair configuration, the rest
+    // after them with the single-CTA one.  The two launches write disjoint
+    // experts; experts with no rows belong to the second.
+    GemmArgs gh = g;
+    gh.row_min = kPairRows;
+    GemmArgs gl = g;
+    gl.row_max = kPairRows;
+    const bool wl = (kind == GemmKind::kWgrad);
+    cudaError_t e = launch_cfg(kind, act, ta, tb, (wl && td_in) ? *td_in : tc, td, gh, num_sms, s,
+                               mx, true, wl && !td_in && wgrad_skinny(g));
+    if (e != cudaSuccess) return e;
+    if (launched) *launched = 2;
+    return launch_cfg(kind, act, ta, tb, tc, td, gl, num_sms, s, mx, false, wgrad_skinny(g));
+  }
+  return launch_cfg(kind, act, ta, tb, tc, td, g, num_sms, s, mx, use_pair(kind, g),
+                    wgrad_skinny(g));
 }
 
 }  // namespace moe

@@ -58,6 +58,11 @@ struct GemmArgs {
   // tiles outermost (a wave reuses each B column tile across all row pairs),
   // 2 = groups of row pairs, each swept with column tiles outermost
   int col_major;
+  // experts whose rows (weight gradients: reduction rows) lie outside
+  // [row_min, row_max) own no units in this launch (row_max 0: no bound);
+  // set by launch_grouped_gemm when it splits a launch
+  int row_min;
+  int row_max;
   // kWgrad: 1 = add the result to the bf16 values already in `out` (one
   // rounding of old + new); experts with no rows leave theirs untouched
   int accumulate;
@@ -84,13 +89,22 @@ struct GemmArgs {
 // Launches the persistent grouped GEMM of `kind` (act: MOE_ACT_*) on `s`.
 // tc: the output's tensor map for kWgrad ([E, R, N] bf16, see wgrad_skinny
 // for its box), and with tma_out for kFc2 / kDgrad (out) and kFc1Act (H,
-// out2); td: with tma_out, kFc1Act's A (out).  Both [rows, cols] maps of
-// tma_out have 32 x 32 boxes with 64-byte swizzle.  Unused maps may be any
-// valid map (td defaults to tc).
+// out2); td: with tma_out, kFc1Act's A (out) and kDgradAct's A' (out3);
+// for kWgrad of a skinny layer, optionally the output map with the
+// large-expert box (32 columns).  The [rows, cols] maps of tma_out have
+// 32 x 32 boxes with 64-byte swizzle.  Unused maps may be any valid map (td
+// defaults to tc).
+// A layer whose experts average fewer than kPairRows rows runs the
+// single-CTA configuration (weight gradients: the skinny one, see
+// wgrad_skinny); in automatic pair mode its experts that do reach kPairRows
+// rows run first, in a launch of their own with the pair configuration
+// (weight gradients: the large-expert one when td is given).  *launched:
+// the number of kernels launched (1 or 2).
 cudaError_t launch_grouped_gemm(GemmKind kind, int act, const CUtensorMap& ta,
                                 const CUtensorMap& tb, const CUtensorMap& tc,
                                 const GemmArgs& args, int num_sms, cudaStream_t s,
-                                bool mx = false, const CUtensorMap* td = nullptr);
+                                bool mx = false, const CUtensorMap* td = nullptr,
+                                int* launched = nullptr);
 
 // Weight gradients use the skinny-expert configuration when the average
 // rows per expert (M_cap / E, known on the host without reading counts) is

@@ -22,6 +22,12 @@ CASES = [
 ]
 
 
+def _split(M_cap, E):
+    """Extra launch of a non-gathered GEMM whose experts average fewer than
+    256 rows: those of 256 rows or more run first, with 2-SM tiles."""
+    return int(E > 1 and M_cap < 256 * E)
+
+
 @pytest.mark.parametrize("act", ["swiglu", "srelu"])
 @pytest.mark.parametrize("name,E,T,k,d,n,align", CASES, ids=[c[0] for c in CASES])
 def test_gather_forward_equals_permuted(name, E, T, k, d, n, align, act):
@@ -40,7 +46,10 @@ def test_gather_forward_equals_permuted(name, E, T, k, d, n, align, act):
     h1, a1, y1, e1 = M.grouped_mlp_fwd_gather(x, r["pair_of_row"], k, r["offsets"], W1, W2, act,
                                               save_h=True)
     torch.cuda.synchronize()
-    assert int(e0.item()) == 0 and int(e1.item()) == 0 and M.last_launch_count() == 2
+    # FC2 reads the permuted A: on a layer below 256 rows per expert its hot
+    # experts get a launch of their own (_split)
+    assert int(e0.item()) == 0 and int(e1.item()) == 0
+    assert M.last_launch_count() == 2 + _split(xp.shape[0], E)
     ro = O.route_offsets(idx, E, align)
     off = ro["offsets"]
     R = int(off[-1])
@@ -78,7 +87,8 @@ def test_gather_routed_backward_equals_permuted(name, E, T, k, d, n, align, act)
     ref = M.grouped_mlp_bwd_routed(xp, H, dop, pr, probs.view(-1), off, W1, W2, act)
     got = M.grouped_mlp_bwd_routed_gather(x, dO, pr, k, H, probs.view(-1), off, W1, W2, act)
     torch.cuda.synchronize()
-    assert int(ref[-1].item()) == 0 and int(got[-1].item()) == 0 and M.last_launch_count() == 4
+    assert int(ref[-1].item()) == 0 and int(got[-1].item()) == 0
+    assert M.last_launch_count() == 4 + _split(M_cap, E)     # FC1-dgrad reads dH, not gathered
     ro = O.route_offsets(idx, E, align)
     R = int(ro["offsets"][-1])
     for nm, i in (("dh", 0), ("a_scaled", 1), ("ds_part", 2), ("dx_perm", 3)):
@@ -120,7 +130,9 @@ def test_gather_full_size_zipf_layer_equals_permuted():
     n2 = BE.make_step(wg, inp, o2)()
     torch.cuda.synchronize()
     assert int(o["err"].item()) == 0 and int(o2["err"].item()) == 0
-    assert n2 == n1 - 2                       # the two permutes are gone
+    # the two permutes are gone; each of the six GEMMs splits its hot experts
+    # into a launch of their own on this layer, except the four gathered ones
+    assert n2 == n1 - 2 - 4 * _split(base.M_cap, base.E)
     R = int(o["route"]["offsets"][-1].item())
     for k_ in ("h", "a", "y_perm", "dh", "a_scaled", "ds_part", "dx_perm"):
         assert torch.equal(o2[k_][:R], o[k_][:R]), k_

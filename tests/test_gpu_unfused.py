@@ -32,7 +32,10 @@ def test_grouped_gemm_matches_oracle(layout, K, N):
     sentinel = torch.full((M_cap, N), 7.0, dtype=torch.bfloat16, device="cuda")
     out, err = M.grouped_gemm(a, cuda_i32(off), B, layout, out=sentinel)
     torch.cuda.synchronize()
-    assert int(err.item()) == 0 and M.last_launch_count() == 1
+    # experts below 256 rows on average: those of 256 rows or more (found on
+    # the device) run first, in a launch of their own with 2-SM tiles
+    split = M_cap < 256 * E and E > 1
+    assert int(err.item()) == 0 and M.last_launch_count() == (2 if split else 1)
     ref = O.grouped_gemm(f64(a), off, f64(B), layout, round_out=False)
     assert_rms_close(f64(out)[:R], ref[:R], f"grouped_gemm {layout} K={K} N={N}")
     assert (f64(out)[R:] == 7.0).all()          # rows outside every expert untouched
