@@ -54,7 +54,9 @@ cudaError_t gemm(moe::GemmKind kind, int act, const CUtensorMap& ta, const CUten
 cudaError_t mx_gemm(moe::MxKind kind, int act, const CUtensorMap& ta, const CUtensorMap& tb,
                     const CUtensorMap& tc, const moe::MxGemmArgs& g, int sms, cudaStream_t s) {
   ev_begin(s);
-  const cudaError_t e = moe::launch_mx_gemm(kind, act, ta, tb, tc, g, sms, s);
+  int launched = 1;
+  const cudaError_t e = moe::launch_mx_gemm(kind, act, ta, tb, tc, g, sms, s, &launched);
+  g_split_extra += launched - 1;
   ev_end(s);
   return e;
 }

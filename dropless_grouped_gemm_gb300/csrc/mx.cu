@@ -477,7 +477,9 @@ __global__ void __launch_bounds__(QTHREADS, 1)
     int carry = 0;
     for (int base = 0; base < g.E; base += 32) {
       const int e = base + lane;
-      const int t = (e < g.E) ? mx_tiles_of_expert<KIND, PAIR>(g, s_off, e) : 0;
+      const int rows_e = (e < g.E) ? s_off[e + 1] - s_off[e] : 0;
+      const bool owned = rows_e >= g.row_min && (g.row_max == 0 || rows_e < g.row_max);
+      const int t = (e < g.E && owned) ? mx_tiles_of_expert<KIND, PAIR>(g, s_off, e) : 0;
       int v = t;
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
@@ -1043,7 +1045,23 @@ cudaError_t launch_mx(const CUtensorMap& ta, const CUtensorMap& tb, const CUtens
 
 cudaError_t launch_mx_gemm(MxKind kind, int act, const CUtensorMap& ta, const CUtensorMap& tb,
                            const CUtensorMap& tc, const MxGemmArgs& g, int num_sms,
-                           cudaStream_t st) {
+                           cudaStream_t st, int* launched) {
+  if (launched) *launched = 1;
+  if (kind == MxKind::kWgrad && g.row_min == 0 && g.row_max == 0 && g.E > 1 &&
+      pair_mode() == kPairAuto && g.a_s_bytes > 0 && g.b_s_bytes > 0 &&
+      !mx_use_pair(kind, g)) {
+    // hot experts (kPairRows reduction rows or more) with 2-SM tiles, then
+    // the rest single-CTA; the two launches write disjoint experts, experts
+    // with no rows belong to the second
+    MxGemmArgs gh = g;
+    gh.row_min = kPairRows;
+    MxGemmArgs gl = g;
+    gl.row_max = kPairRows;
+    cudaError_t e = launch_mx_t<MxKind::kWgrad, 0, false, true>(ta, tb, tc, gh, num_sms, st);
+    if (e != cudaSuccess) return e;
+    if (launched) *launched = 2;
+    return launch_mx_t<MxKind::kWgrad, 0, false, false>(ta, tb, tc, gl, num_sms, st);
+  }
   switch (kind) {
     // the quantising epilogue (GroupGemm + Quantize) is its own instantiation,
     // so that the plain one keeps its registers

@@ -58,6 +58,12 @@ struct MxGemmArgs {
   // epilogue writes whole 32-row groups with staged TMA stores; 0 = plain
   // stores
   int tma_out;
+  // kWgrad: experts whose reduction rows lie outside [row_min, row_max) own
+  // no units in this launch (row_max 0: no bound); set by launch_mx_gemm
+  // when it splits a launch
+  int row_min;
+  int row_max;
+  // also: the tma_out staged stores of kDgradAct's bf16 dH when dh_q is set
   // kDgradAct, optional (dh_q == nullptr: none): GroupGemm + dActivation +
   // Quantize/Transpose - the epilogue also writes the MXFP8 copies of the
   // bf16 dH it stores, as the tiled activation quantiser would: row-wise
@@ -101,8 +107,11 @@ cudaError_t launch_mx_quantize_rows_w(const uint16_t* src, long long rows, int c
 cudaError_t launch_mx_retile_t(const uint8_t* sT, int rows, int cols, const int32_t* offsets,
                                int E, uint8_t* out, int num_sms, cudaStream_t st);
 // tc: output map of kWgrad ([E, R, N] bf16, box 64 x 32, 128-byte swizzle)
+// A weight gradient of a layer below kPairRows rows per expert runs its
+// experts of kPairRows reduction rows or more first, in a launch of their
+// own with 2-SM tiles (automatic pair mode); *launched: kernels launched.
 cudaError_t launch_mx_gemm(MxKind kind, int act, const CUtensorMap& ta, const CUtensorMap& tb,
                            const CUtensorMap& tc, const MxGemmArgs& g, int num_sms,
-                           cudaStream_t st);
+                           cudaStream_t st, int* launched = nullptr);
 
 }  // namespace moe

@@ -143,7 +143,14 @@ def _gpu_bwd(off, x, H, A, dy, W1, W2, act, dW1=None, dW2=None, accumulate_dw=Fa
                                                   workspace=workspace)
     torch.cuda.synchronize()
     assert int(e0.item()) == 0 and int(err.item()) == 0
-    assert M.last_launch_count() == (8 if separate_dh_quant else 7)
+    # in automatic pair mode each weight gradient of a layer below 256 rows
+    # per expert runs its experts of 256 rows or more in a launch of their
+    # own (2-SM tiles)
+    M_cap, E = x.shape[0], W2.shape[0]
+    mode = M.set_pair_mma(M.PAIR_AUTO)
+    M.set_pair_mma(mode)
+    split = int(mode == M.PAIR_AUTO and E > 1 and M_cap < 256 * E)
+    assert M.last_launch_count() == (8 if separate_dh_quant else 7) + 2 * split
     return dh, dx, dW1, dW2
 
 
