@@ -574,8 +574,11 @@ size_t moe_mx_bwd_workspace_layout(int M_cap, int d, int n, int act, size_t* off
  *      CTAs share B tiles through TMA multicast);
  *   1  automatic (the default): 2-SM MMAs over 256 x 256 tiles (each CTA
  *      loads 128 rows of A and half of B; tcgen05.mma.cta_group::2) when the
- *      average rows per expert, M_cap / E, reach 256, else as 0; the
- *      block-scaled MXFP8 GEMMs other than the weight gradients always;
+ *      average rows per expert, M_cap / E, reach 256; the block-scaled
+ *      MXFP8 GEMMs other than the weight gradients always.  Below that
+ *      average (E > 1) a GEMM makes two launches: the experts of 256 rows
+ *      or more (weight gradients: reduction rows), found on the device,
+ *      with 2-SM tiles, then the others as in mode 0;
  *   2  always 2-SM.
  * Results are identical across modes; the choice is for speed (and for
  * measuring one against the other).  Returns the previous mode, or
@@ -686,7 +689,9 @@ int moe_selftest_bounded_wait(int limit_us, int32_t* err, int32_t* waited_us,
 const char* moe_version(void);
 
 /* Number of kernel launches the last successful call on this host thread
- * enqueued (for launch accounting; 0 before any call). */
+ * enqueued (for launch accounting; 0 before any call).  It includes the
+ * second launch of each GEMM that automatic pair mode splits by expert
+ * size (moe_set_pair_mma). */
 int moe_last_launch_count(void);
 
 #ifdef __cplusplus
