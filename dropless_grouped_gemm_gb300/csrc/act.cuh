@@ -3,7 +3,8 @@
 //   SwiGLU: phi(g) = g * sigmoid(g) (Swish on the gate side, times the up
 //           projection) - [CuTe] "핵심 아이디어 / 구조 / 동작 방식".
 //   GeGLU:  phi(g) = 0.5 g (1 + tanh(sqrt(2/pi) (g + 0.044715 g^3))), the
-//           tanh approximation of GELU (Hendrycks & Gimpel).
+//           tanh approximation of GELU (Hendrycks & Gimpel), evaluated as
+//           g sigmoid(2 sqrt(2/pi) (g + 0.044715 g^3)), the same function.
 #pragma once
 
 #include "ptx.cuh"
@@ -19,8 +20,10 @@ __device__ __forceinline__ float gate_phi(float g) {
   if constexpr (ACT == MOE_ACT_SWIGLU) {
     return g * sigmoidf_(g);
   } else {
+    // 1 + tanh(z) = 2 sigmoid(2z): no tanh, and no cancellation for
+    // negative gates, where 1 + tanh(z) is small
     const float z = kGeluC * (g + kGeluA * g * g * g);
-    return 0.5f * g * (1.0f + tanhf(z));
+    return g * sigmoidf_(2.0f * z);
   }
 }
 // phi and phi' together
@@ -31,10 +34,12 @@ __device__ __forceinline__ void gate_phi_dphi(float g, float& ph, float& dph) {
     ph = g * s;
     dph = s * (1.0f + g * (1.0f - s));
   } else {
+    // with s = sigmoid(2z): 1 + tanh z = 2s and 1 - tanh^2 z = 4 s (1 - s), so
+    // phi = g s and phi' = s + 2 g s (1 - s) z'(g), z' = c (1 + 3 a g^2)
     const float z = kGeluC * (g + kGeluA * g * g * g);
-    const float th = tanhf(z);
-    ph = 0.5f * g * (1.0f + th);
-    dph = 0.5f * (1.0f + th) + 0.5f * g * (1.0f - th * th) * kGeluC * (1.0f + 3.0f * kGeluA * g * g);
+    const float s = sigmoidf_(2.0f * z);
+    ph = g * s;
+    dph = s + 2.0f * g * s * (1.0f - s) * kGeluC * (1.0f + 3.0f * kGeluA * g * g);
   }
 }
 
