@@ -9,7 +9,9 @@ reductions zero the rows past an expert's last 16-row boundary in both
 CTAs' shared memory (the second CTA's through the cluster).  The first case is the smallest one (one expert
 of 256 rows, one 256 x 256 output tile), then ragged shapes: an odd number
 of 128-row blocks (the second CTA of the last unit has no rows), one-row and
-empty experts, an output width that ends in half a tile, 64 experts."""
+empty experts, an output width that ends in half a tile, 64 experts.  On a
+skinny layer the automatic mode's split launches (hot experts with 2-SM
+tiles, the rest single-CTA) give the single-CTA outputs bit for bit too."""
 import numpy as np
 import pytest
 import torch
@@ -191,3 +193,49 @@ def test_mx_pair_equals_single(name, counts, d, n, act):
         if p.shape[0] == M_cap:
             p, q = p[:R], q[:R]
         assert torch.equal(p, q), f"{name}/{act} {nm}: MXFP8 pair mode differs from single-CTA tiles"
+
+
+# A skinny layer (below 256 rows per expert on average) with a few hot
+# experts: in automatic mode each GEMM runs its experts of 256 rows or more
+# (weight gradients: reduction rows) in a launch of their own with 2-SM
+# tiles, then the rest single-CTA.
+SPLIT_COUNTS = [600, 0, 40, 300, 1, 0, 5, 270]
+
+
+@pytest.mark.parametrize("act", ["swiglu", "srelu"])
+def test_split_by_expert_size_equals_single(act):
+    """Automatic mode on a skinny layer (the split launches) against
+    single-CTA tiles throughout: all seven outputs bit for bit, and two
+    kernels per GEMM."""
+    import dropless_grouped_gemm_gb300 as M
+    E, d, n = len(SPLIT_COUNTS), 256, 128
+    off, x, W1, W2, dy = _case(E, d, n, SPLIT_COUNTS, act, seed=45)
+    assert x.shape[0] < 256 * E and max(SPLIT_COUNTS) >= 256
+    single = _run(off, x, W1, W2, dy, act, 0)
+    split = _run(off, x, W1, W2, dy, act, 1)
+    assert M.last_launch_count() == 2 * 4           # the backward's four GEMMs, split
+    R = int(off[-1])
+    for nm, p, q in zip(("H", "A", "Y", "dH", "dX", "dW1", "dW2"), split, single):
+        if p.shape[0] == x.shape[0]:
+            p, q = p[:R], q[:R]
+        assert torch.equal(p, q), f"{act} {nm}: split launches differ from single-CTA tiles"
+
+
+def test_mx_split_weight_gradients_equal_single():
+    """The MXFP8 backward on a skinny layer: in automatic mode the block-
+    scaled weight gradients split by expert size (and the other GEMMs run
+    2-SM); against single-CTA tiles throughout, every output bit for bit."""
+    import dropless_grouped_gemm_gb300 as M
+    from test_gpu_mx_bwd import _gpu_bwd, _layer
+    counts = [608, 0, 64, 320, 32, 0, 0, 288]
+    off, x, H, A, dy, W1, W2 = _layer(46, counts, 256, 128, "swiglu")
+    assert x.shape[0] < 256 * len(counts)
+    R = int(off[-1])
+    outs = []
+    for mode in (0, 1):
+        M.set_pair_mma(mode)
+        outs.append(tuple(t.clone() for t in _gpu_bwd(off, x, H, A, dy, W1, W2, "swiglu")))
+    for nm, p, q in zip(("dH", "dX", "dW1", "dW2"), outs[1], outs[0]):
+        if p.shape[0] == x.shape[0]:
+            p, q = p[:R], q[:R]
+        assert torch.equal(p, q), f"MXFP8 {nm}: split launches differ from single-CTA tiles"
