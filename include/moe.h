@@ -394,7 +394,8 @@ int moe_grouped_mlp_bwd(const moe_bf16* x_perm, const moe_bf16* h_saved,
  *   a_scaled [M_cap, n] = p * act(H) (bf16) and ds_part [M_cap, ceil(n/128)]
  *   (fp32 partial <dA', act(H)> of each 128-column half tile, caller-owned
  *   scratch); FC2-wgrad then contracts a_scaled with do_perm.  dx_perm, dW1,
- *   dW2 and amax_dh as in moe_grouped_mlp_bwd.  Four launches; finish with
+ *   dW2 and amax_dh as in moe_grouped_mlp_bwd.  Four GEMMs (each one or two
+ *   launches, moe_set_pair_mma); finish with
  *   moe_router_grad_rows.  flags: 0 or MOE_FLAG_ACCUMULATE_DW (as in
  *   moe_grouped_mlp_bwd).  Errors as moe_grouped_mlp_bwd.
  */
@@ -417,7 +418,8 @@ int moe_grouped_mlp_bwd_routed(const moe_bf16* x_perm, const moe_bf16* h_saved,
  * outputs (dh, a_scaled, ds_part, dx_perm in expert-major order; dW1, dW2)
  * and flags are those of moe_grouped_mlp_bwd_routed, and equal its results
  * on moe_permute(x), moe_permute(dO) bit for bit.  x and dO non-NULL and
- * 16-byte aligned even when T = 0.  Four launches; finish with
+ * 16-byte aligned even when T = 0.  Four GEMMs (the non-gathered ones may
+ *   take two launches, moe_set_pair_mma); finish with
  * moe_router_grad_rows and moe_unpermute (dx).
  */
 int moe_grouped_mlp_bwd_routed_gather(const moe_bf16* x, const moe_bf16* dO, int T, int k,
@@ -503,7 +505,8 @@ int moe_mx_quantize_weights_rowwise(const moe_bf16* W, int rows, int cols,
  *   then read from it); pair_of_row [M_cap] as written by
  *   moe_route_offsets; the rest as moe_grouped_mlp_fwd.  flags: 0 or
  *   MOE_FLAG_SAVE_H (no MXFP8).  H, A, y_perm equal moe_grouped_mlp_fwd's
- *   on moe_permute(x) bit for bit.  Two launches.
+ *   on moe_permute(x) bit for bit.  Two GEMMs (FC2 may take two launches,
+ *   moe_set_pair_mma).
  */
 int moe_grouped_mlp_fwd_gather(const moe_bf16* x, int T, int k, const int32_t* pair_of_row,
                                const int32_t* offsets, int E, int M_cap, int d, int n,
@@ -612,7 +615,9 @@ size_t moe_workspace_size(int T, int k, int E, int M_cap, int d, int n, int act,
  *   and both MXFP8 copies of it that FC1-dgrad and FC1-wgrad read, as the
  *   standalone tiled quantiser would, bit for bit), FC2-wgrad, FC1-dgrad,
  *   FC1-wgrad.  With MOE_FLAG_MX_SEPARATE_DH_QUANT, eight: FC2-dgrad + dAct
- *   stores dH alone and a separate pass quantises it.
+ *   stores dH alone and a separate pass quantises it.  In automatic pair
+ *   mode each weight gradient of a layer below 256 rows per expert takes
+ *   two launches (moe_set_pair_mma).
  *   flags: MOE_FLAG_ACCUMULATE_DW (as in moe_grouped_mlp_bwd),
  *   MOE_FLAG_MX_SEPARATE_DH_QUANT, or both.
  *   The quantised operands live in mx->workspace at the offsets
