@@ -3,7 +3,8 @@ NaN; afterwards every row inside an expert is finite and equal, bit for bit,
 to the run on unpoisoned buffers (nothing read an output before writing
 it), and every row outside all experts is still NaN (nothing wrote there).
 Expert sizes 0, 1, 127, 128, 129 and 255 rows straddle the 128-row tiles
-(multiples of 32 on the MXFP8 path)."""
+(multiples of 32 on the MXFP8 path); a second layer adds hot experts of 300
+and 600 rows, which run in the 2-SM launch of the split GEMMs."""
 import numpy as np
 import pytest
 import torch
@@ -38,10 +39,17 @@ def _layer(counts, d, n, act, tail, seed):
     return off, E, R, M_cap, n1, x, dy, W1, W2
 
 
+# the second layer has hot experts (300 and 600 rows, ragged 32-row ends):
+# on this skinny layer they run in the GEMMs' 2-SM launch, the rest in the
+# single-CTA one
+BF16_COUNTS = {"small": [127, 0, 1, 129, 128, 255], "hot": [300, 0, 1, 129, 600, 255]}
+
+
+@pytest.mark.parametrize("layer", sorted(BF16_COUNTS))
 @pytest.mark.parametrize("act", ["swiglu", "srelu"])
-def test_bf16_layer_writes_exactly_the_expert_rows(act):
+def test_bf16_layer_writes_exactly_the_expert_rows(act, layer):
     import dropless_grouped_gemm_gb300 as M
-    off, E, R, M_cap, n1, x, dy, W1, W2 = _layer([127, 0, 1, 129, 128, 255], 256, 128, act, 37, 91)
+    off, E, R, M_cap, n1, x, dy, W1, W2 = _layer(BF16_COUNTS[layer], 256, 128, act, 37, 91)
     d, n = x.shape[1], W2.shape[1]
     offs = cuda_i32(off)
 
@@ -65,13 +73,18 @@ def test_bf16_layer_writes_exactly_the_expert_rows(act):
     assert float(w_p["dW1"][1].float().abs().max()) == 0.0
 
 
-def test_routed_backward_writes_exactly_the_expert_rows():
+@pytest.mark.parametrize("hot", [False, True], ids=["spread", "hot"])
+def test_routed_backward_writes_exactly_the_expert_rows(hot):
     import dropless_grouped_gemm_gb300 as M
     act = "swiglu"
     E, T, k = 6, 300, 2
     rng = np.random.default_rng(92)
     idx = np.stack([rng.permutation(E)[:k] for _ in range(T)]).astype(np.int32)
     idx[idx == E - 1] = 0                    # expert E-1 empty
+    if hot:
+        # expert 0 takes every token (300 rows: the GEMMs' 2-SM launch)
+        idx[:, 0] = 0
+        idx[:, 1] = rng.integers(1, E - 1, T)
     probs = torch.from_numpy(rng.random((T, k)).astype(np.float32)).cuda().view(-1)
     r = M.route_offsets(cuda_i32(idx), E, 8)             # pad rows inside the experts
     M_cap = r["pair_of_row"].numel()
@@ -99,10 +112,11 @@ def test_routed_backward_writes_exactly_the_expert_rows():
         _check(k_, p[k_], z[k_], R)
 
 
-def test_mxfp8_layer_writes_exactly_the_expert_rows():
+@pytest.mark.parametrize("counts", [[96, 0, 32, 160, 128, 224], [320, 0, 32, 160, 608, 224]],
+                         ids=["small", "hot"])
+def test_mxfp8_layer_writes_exactly_the_expert_rows(counts):
     import dropless_grouped_gemm_gb300 as M
     act = "swiglu"
-    counts = [96, 0, 32, 160, 128, 224]
     off, E, R, M_cap, n1, x, dy, W1, W2 = _layer(counts, 256, 128, act, 64, 93)
     d, n = x.shape[1], W2.shape[1]
     offs = cuda_i32(off)
