@@ -927,7 +927,8 @@ def run_e2e(w, inp, o, step, steps, flops):
     step copies its inputs host->device and reads its results back to the
     host, as an input pipeline would: the inputs of step i+1 are copied on
     one stream while step i computes, and step i's results are read back on
-    another, with two device input sets and two result sets.  A training
+    another, with three device input sets and three result sets (with two,
+    step i+1 waited for step i-1's results to be read back).  A training
     step's results are the input gradient and both weight gradients; a
     forward step's is the layer output.  The timed region runs from the
     first input copy to the last result read."""
@@ -949,15 +950,16 @@ def run_e2e(w, inp, o, step, steps, flops):
                 for nm in out_names}
     h2d = sum(host[nm].numel() * host[nm].element_size() for nm in names_in)
     d2h = sum(t.numel() * t.element_size() for t in out_host.values())
-    # two input sets / result buffers; weights and intermediates shared
+    # NSET input sets / result buffers; weights and intermediates shared
+    NSET = 3
     sets, outs, steps_fn = [], [], []
-    for i in range(2):
+    for i in range(NSET):
         ins = dict(inp)
-        if i == 1:
+        if i > 0:
             for nm in names_in:
                 ins[nm] = torch.empty_like(inp[nm])
         oo = dict(o)
-        if i == 1:
+        if i > 0:
             for nm in out_names:
                 oo[nm] = torch.empty_like(o[nm])
         sets.append(ins)
@@ -965,14 +967,14 @@ def run_e2e(w, inp, o, step, steps, flops):
         steps_fn.append(make_step(w, ins, oo))
     comp = torch.cuda.current_stream()
     up, down = torch.cuda.Stream(), torch.cuda.Stream()
-    ready = [torch.cuda.Event() for _ in range(2)]
-    freed = [torch.cuda.Event() for _ in range(2)]   # compute done with the set / result
-    read = [torch.cuda.Event() for _ in range(2)]    # result copied out
+    ready = [torch.cuda.Event() for _ in range(NSET)]
+    freed = [torch.cuda.Event() for _ in range(NSET)]   # compute done with the set / result
+    read = [torch.cuda.Event() for _ in range(NSET)]    # result copied out
 
     def h2d_copy(i):
-        k = i % 2
+        k = i % NSET
         with torch.cuda.stream(up):
-            if i >= 2:
+            if i >= NSET:
                 up.wait_event(freed[k])
             for nm in names_in:
                 sets[k][nm].copy_(host[nm], non_blocking=True)
@@ -981,11 +983,11 @@ def run_e2e(w, inp, o, step, steps, flops):
     def run(n):
         h2d_copy(0)
         for i in range(n):
-            k = i % 2
+            k = i % NSET
             if i + 1 < n:
                 h2d_copy(i + 1)
             comp.wait_event(ready[k])
-            if i >= 2:
+            if i >= NSET:
                 comp.wait_event(read[k])            # result buffer k copied out
             steps_fn[k]()
             freed[k].record(comp)
@@ -995,7 +997,7 @@ def run_e2e(w, inp, o, step, steps, flops):
                     out_host[nm].copy_(outs[k][nm], non_blocking=True)
                 read[k].record(down)
 
-    run(2)
+    run(NSET)
     torch.cuda.synchronize()
     s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     s.record(up)
@@ -1008,7 +1010,7 @@ def run_e2e(w, inp, o, step, steps, flops):
     return {"value": round(flops / (ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
             "ms_per_step": round(ms, 4), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
             "read_back": out_names,
-            "pipelined": "inputs of step i+1 copied during step i; two input and result sets"}
+            "pipelined": "inputs of step i+1 copied during step i; three input and result sets"}
 
 
 if __name__ == "__main__":
