@@ -601,6 +601,9 @@ def main():
     ap.add_argument("--ref-rows", type=int, default=64,
                     help="rows per step of the --impl reference sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-next-rows", action="store_true",
+                    help="skip the timings of the rows built after the hot path (NVFP4 "
+                         "statistics, GroupGemm + Quantize, device router)")
     ap.add_argument("--no-fusion-control", action="store_true",
                     help="skip the fused-against-unfused epilogue comparison")
     args = ap.parse_args()
@@ -715,6 +718,7 @@ def main():
         fusion = fusion_control(w, inp, o)
     if w.mxfp8 and w.backward and not args.no_fusion_control:
         fusion = mx_fusion_control(w, inp, o)
+    extra = None if args.no_next_rows else next_rows(w, inp, o, peaks)
 
     cpu = None
     if not args.no_cpu_baseline:
@@ -743,6 +747,8 @@ def main():
     }
     if fusion is not None:
         line["fusion_control"] = fusion
+    if extra is not None:
+        line["next_rows"] = extra
     print(json.dumps(line), flush=True)
     return 0
 
@@ -866,6 +872,160 @@ def mx_fusion_control(w, inp, o, reps=20):
             "reps": reps,
             "what": "MXFP8 backward: FC2-dgrad + dAct with dH's MXFP8 copies written by its "
                     "epilogue, against FC2-dgrad + dAct storing dH and a separate tiled quantiser"}
+
+
+def _launch_rounds(round_, per, reps):
+    """Average duration (ms) of each of the ``per`` library launches (or
+    calls) that ``round_`` makes, from the events the library records
+    around them, over ``reps`` rounds after two untimed ones; None when the
+    events do not add up or the error word is set."""
+    import ctypes
+    import torch
+    import dropless_grouped_gemm_gb300 as M
+    stream = torch.cuda.current_stream()
+    for _ in range(2):
+        round_()
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(2 * per * reps)]
+    for e in evs:
+        e.record(stream)
+    torch.cuda.synchronize()
+    handles = (ctypes.c_void_p * len(evs))(*[e.cuda_event for e in evs])
+    M.lib().moe_set_launch_events(handles, len(evs))
+    for _ in range(reps):
+        round_()
+    torch.cuda.synchronize()
+    used = M.lib().moe_launch_events_used()
+    M.lib().moe_set_launch_events(None, 0)
+    if used != len(evs):
+        return None
+    t = [[evs[2 * (r * per + i)].elapsed_time(evs[2 * (r * per + i) + 1]) for r in range(reps)]
+         for i in range(per)]
+    return [sum(v) / len(v) for v in t]
+
+
+def next_rows(w, inp, o, peaks, reps=20):
+    """The rows built after the hot path, timed on the step's own operands
+    outside the timed region, each launch between its own events:
+    - bf16 training layers (identity routing): the NVFP4 statistics fused
+      into the epilogues ([TE] "다음 단계: NVFP4, GEMM 융합 양자화, A2A 오버랩"):
+      FC1 raising max|A| and FC2-dgrad raising the amax of the transposed
+      16-point Hadamard-rotated dH, against the same launches without them;
+    - MXFP8 training layers (identity routing): GroupGemm + Quantize, the
+      block-scaled FC2 and FC1-dgrad also writing the MXFP8 copy of their
+      bf16 output, against the same launches without it;
+    - routed layers: the device router (top-k and softmax of the logits),
+      the routing layout from its indices, and the router fused into the
+      layout's first pass, from the workload's logits; the fused and the
+      separate results are compared for identity."""
+    import torch
+    import dropless_grouped_gemm_gb300 as M
+    act = w.act
+    dev = o["err"].device
+    if w.routing == "identity" and w.backward and not w.mxfp8:
+        x, dy, off, W1, W2 = inp["x_perm"], inp["dy_perm"], inp["offsets"], inp["W1"], inp["W2"]
+        amax_a = torch.zeros(1, dtype=torch.float32, device=dev)
+        amax_dh = torch.zeros(1, dtype=torch.float32, device=dev)
+
+        def round_():
+            for am in (None, amax_a):                                           # 2 + 2
+                M.grouped_mlp_fwd(x, off, W1, W2, act, save_h=True, h_saved=o["h"], a=o["a"],
+                                  y_perm=o["y_perm"], err=o["err"], amax=am)
+            for am in (None, amax_dh):                                          # 4 + 4
+                M.grouped_mlp_bwd(x, o["h"], o["a"], dy, off, W1, W2, act, dh=o["dh"],
+                                  dx_perm=o["dx_perm"], dW1=o["dW1"], dW2=o["dW2"], err=o["err"],
+                                  amax=am)
+        avg = _launch_rounds(round_, 12, reps)
+        if avg is None or int(o["err"].item()) != 0:
+            return None
+        fc1, fc1_s, dg, dg_s = avg[0], avg[2], avg[4], avg[8]
+        return {"nvfp4_statistics": {
+            "fc1_ms": round(fc1, 4), "fc1_with_amax_a_ms": round(fc1_s, 4),
+            "fc1_overhead": round(fc1_s / fc1 - 1, 4),
+            "fc2_dgrad_dact_ms": round(dg, 4), "fc2_dgrad_dact_with_amax_dh_ms": round(dg_s, 4),
+            "fc2_dgrad_dact_overhead": round(dg_s / dg - 1, 4),
+            "amax_a": float(amax_a.item()), "amax_dh": float(amax_dh.item()),
+            "what": "max|A| in FC1's epilogue; amax of the transposed 16-point Hadamard-rotated "
+                    "dH in FC2-dgrad's epilogue (one atomic maximum per warp)"},
+            "reps": reps}
+    if w.routing == "identity" and w.backward and w.mxfp8:
+        x, dy, off, W1, W2 = inp["x_perm"], inp["dy_perm"], inp["offsets"], inp["W1"], inp["W2"]
+        Mc, d = w.M_cap, w.d
+        u8 = torch.uint8
+        mx, mb = o["mx"], o["mxb"]
+        mxq = dict(mx, y_q=torch.empty((Mc, d), dtype=u8, device=dev),
+                   y_s=torch.empty((Mc, d // 32), dtype=u8, device=dev))
+        ops = dict(a_qT=mx["a_qT"], a_sT=mx["a_sT"], w2_q=mb["w2_q"], w2_s=mb["w2_s"],
+                   w1_q=mb["w1_q"], w1_s=mb["w1_s"])
+        opsq = dict(ops, dx_q=torch.empty((Mc, d), dtype=u8, device=dev),
+                    dx_s=torch.empty((Mc, d // 32), dtype=u8, device=dev))
+
+        def round_():
+            for m_ in (mx, mxq):                                                # 2 + 2
+                M.grouped_mlp_fwd(x, off, W1, W2, act, save_h=True, h_saved=o["h"], a=o["a"],
+                                  y_perm=o["y_perm"], err=o["err"], mx=m_)
+            for p_ in (ops, opsq):                                              # 7 + 7
+                M.grouped_mlp_bwd_mx(x, o["h"], dy, off, p_, act, dh=o["dh"],
+                                     dx_perm=o["dx_perm"], dW1=o["dW1"], dW2=o["dW2"],
+                                     err=o["err"], workspace=mb["ws"])
+        avg = _launch_rounds(round_, 18, reps)
+        if avg is None or int(o["err"].item()) != 0:
+            return None
+        fc2, fc2_q, dgr, dgr_q = avg[1], avg[3], avg[4 + 5], avg[11 + 5]
+        return {"group_gemm_quantize": {
+            "fc2_ms": round(fc2, 4), "fc2_with_y_mxfp8_ms": round(fc2_q, 4),
+            "fc2_overhead": round(fc2_q / fc2 - 1, 4),
+            "fc1_dgrad_ms": round(dgr, 4), "fc1_dgrad_with_dx_mxfp8_ms": round(dgr_q, 4),
+            "fc1_dgrad_overhead": round(dgr_q / dgr - 1, 4),
+            "what": "block-scaled FC2 (FC1-dgrad) writing Y (dX) as bf16 and as row-wise "
+                    "E4M3 codes with E8M0 scales from the same epilogue"},
+            "reps": reps}
+    if w.routing != "identity":
+        T, k, E = w.T, w.k, w.E
+        lg = torch.from_numpy(WL.logits(w.cfg_id, T, E, w.zipf_s, w.empty_expert)).to(dev)
+        ws = o["ws"]
+
+        def lay():
+            return {nm: torch.empty_like(v) for nm, v in o["route"].items() if nm != "err"}
+        out_sep, out_fused = lay(), lay()
+        out_fused["topk_idx"] = torch.empty((T, k), dtype=torch.int32, device=dev)
+        out_fused["probs"] = torch.empty((T, k), dtype=torch.float32, device=dev)
+        calls = {
+            "router_topk": lambda: M.router_topk(lg, k),
+            "route_offsets": lambda: M.route_offsets(inp["topk_idx"], E, w.align, w.M_cap,
+                                                     err=o["err"], out=out_sep, workspace=ws),
+            "router_then_layout": lambda: M.route_offsets(M.router_topk(lg, k)[0], E, w.align,
+                                                          w.M_cap, err=o["err"], out=out_sep,
+                                                          workspace=ws),
+            "route_logits_fused": lambda: M.route_logits(lg, k, w.align, w.M_cap, err=o["err"],
+                                                         out=out_fused, workspace=ws),
+        }
+        # each captured as a CUDA graph and replayed: GPU time, without the
+        # host's cost of issuing the calls
+        ms = {nm: time_graph(f, reps, 0.0)["ms_per_step"] for nm, f in calls.items()}
+        idx, probs = M.router_topk(lg, k)
+        sep = M.route_offsets(idx, E, w.align, w.M_cap, workspace=ws)
+        fused = M.route_logits(lg, k, w.align, w.M_cap, workspace=ws)
+        torch.cuda.synchronize()
+        same = all(torch.equal(fused[nm], sep[nm]) for nm in
+                   ("counts", "offsets", "row_of_pair", "pair_of_row")) and \
+            torch.equal(fused["topk_idx"], idx) and torch.equal(fused["probs"], probs) and \
+            torch.equal(idx, inp["topk_idx"])
+        lg_bytes = T * E * 4
+        return {"router": {
+            "router_topk_ms": ms["router_topk"],
+            "route_offsets_ms": ms["route_offsets"],
+            "router_then_layout_ms": ms["router_then_layout"],
+            "route_logits_fused_ms": ms["route_logits_fused"],
+            "fused_speedup": round(ms["router_then_layout"] / ms["route_logits_fused"], 3),
+            "router_logits_gbs": round(lg_bytes / ms["router_topk"] / 1e6, 1),
+            "router_frac_of_hbm": round(lg_bytes / ms["router_topk"] / 1e6 / peaks["hbm_gbs"], 4),
+            "identical": bool(same),
+            "what": "T x E float32 logits -> top-k indices and softmax weights (router_topk); "
+                    "the routing layout from given indices (route_offsets); the two in sequence; "
+                    "the router fused into the layout's first pass (route_logits); each call "
+                    "captured as a CUDA graph, median of the replays"},
+            "reps": reps}
+    return None
 
 
 def step_description(w):

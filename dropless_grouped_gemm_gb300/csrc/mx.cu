@@ -225,27 +225,23 @@ __device__ __forceinline__ void mx_store_row32(uint16_t* p, const uint32_t (&v)[
         pack_bf16x2(__uint_as_float(v[8 * k + 6]), __uint_as_float(v[8 * k + 7])));
 }
 
-// GroupGemm + Quantize ([TE] "다음 단계: NVFP4, GEMM 융합 양자화, A2A 오버랩"):
-// 32 fp32 accumulator columns of one row -> 32 bf16 at p, and the row-wise
-// MXFP8 block of those bf16 values: 32 codes at q, the E8M0 scale at *s
-__device__ __forceinline__ void mx_store_quant_row32(uint16_t* p, uint8_t* q, uint8_t* s,
-                                                     const uint32_t (&v)[32]) {
-  uint32_t pk[16];
-  float f[32];
+// mx_quant32 from 32 bf16 values packed in pairs (element 2i in the low
+// half of p[i]), so that no float copy of the block stays live
+__device__ __forceinline__ uint32_t mx_quant32_bf16(const uint32_t (&p)[16], uint32_t (&q)[8]) {
+  auto lo16 = [](uint32_t x) { return __uint_as_float(x << 16); };
+  auto hi16 = [](uint32_t x) { return __uint_as_float(x & 0xFFFF0000u); };
+  float amax = 0.f;
 #pragma unroll
-  for (int i = 0; i < 16; ++i) {
-    pk[i] = pack_bf16x2(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]));
-    f[2 * i] = bf16_lo(pk[i]);
-    f[2 * i + 1] = bf16_hi(pk[i]);
+  for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fmaxf(fabsf(lo16(p[i])), fabsf(hi16(p[i]))));
+  const uint32_t code = mx_scale_code(amax);
+  const float inv = mx_inv_scale(code);
+#pragma unroll
+  for (int w = 0; w < 8; ++w) {
+    const uint32_t lo = e4m3x2(lo16(p[2 * w]) * inv, hi16(p[2 * w]) * inv);
+    const uint32_t hi = e4m3x2(lo16(p[2 * w + 1]) * inv, hi16(p[2 * w + 1]) * inv);
+    q[w] = lo | (hi << 16);
   }
-#pragma unroll
-  for (int k = 0; k < 4; ++k)
-    *reinterpret_cast<uint4*>(p + 8 * k) = make_uint4(pk[4 * k], pk[4 * k + 1], pk[4 * k + 2], pk[4 * k + 3]);
-  uint32_t qw[8];
-  *s = static_cast<uint8_t>(mx_quant32(f, qw));
-  uint4* pq = reinterpret_cast<uint4*>(q);
-  pq[0] = make_uint4(qw[0], qw[1], qw[2], qw[3]);
-  pq[1] = make_uint4(qw[4], qw[5], qw[6], qw[7]);
+  return code;
 }
 
 // dA columns col..col+31 of one row -> dH (same interleaving as H)
@@ -841,6 +837,78 @@ __global__ void __launch_bounds__(QTHREADS, 1)
         }
         continue;
       }
+      if constexpr (QOUT && KIND != MxKind::kDgradAct) {
+        // GroupGemm + Quantize ([TE] "다음 단계: NVFP4, GEMM 융합 양자화, A2A
+        // 오버랩"): the bf16 output and its row-wise MXFP8 copy.  The
+        // accumulator is read one 32-column chunk at a time and rounded to
+        // bf16 at once (half the registers of the fp32 values), then
+        // released.  Each chunk leaves as a staged TMA store of the bf16
+        // values (64-byte swizzle, as below) and, from the thread that owns
+        // the row, its 32 E4M3 codes quantised from those bf16 values; the
+        // four E8M0 scales of the thread's 128 columns leave as one word.
+        uint32_t pk4[4][16];
+        if (mine) {
+          const uint32_t tb = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + wg * QHN;
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            uint32_t t32[32];
+            tmem_ld32(tb + c * 32, t32);
+            tmem_wait_ld();
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+              pk4[c][i] = pack_bf16x2(__uint_as_float(t32[2 * i]), __uint_as_float(t32[2 * i + 1]));
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) release();
+        // offsets are multiples of 32: a warp's 32 rows are all valid or none
+        if (!mine || q * 32 >= tl.rows) continue;
+        const int col0 = tl.n0 + wg * QHN;
+        const long long grow = tl.row0 + r;
+        const bool staged = g.tma_out && q * 32 + 32 <= tl.rows;
+        uint8_t* box = staging + (warp - 2) * (32 * 32 * 2);
+        uint32_t s4 = 0;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          if (staged) {
+            if (lane == 0) bulk_wait_read_0();     // the box's previous store has read it
+            __syncwarp();
+            uint8_t* row = box + lane * 64;
+            const int sw = (lane >> 1) & 3;
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+              *reinterpret_cast<uint4*>(row + ((j ^ sw) * 16)) =
+                  make_uint4(pk4[c][4 * j], pk4[c][4 * j + 1], pk4[c][4 * j + 2], pk4[c][4 * j + 3]);
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+              tma_store_2d(&tmC, box, col0 + c * 32, tl.row0 + q * 32);
+              bulk_commit();
+            }
+          } else {
+            uint4* p = reinterpret_cast<uint4*>(g.out + grow * g.ldo + col0 + c * 32);
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+              p[k] = make_uint4(pk4[c][4 * k], pk4[c][4 * k + 1], pk4[c][4 * k + 2], pk4[c][4 * k + 3]);
+          }
+          uint32_t qw[8];
+          s4 |= mx_quant32_bf16(pk4[c], qw) << (8 * c);
+          uint4* pq = reinterpret_cast<uint4*>(g.q_out + grow * g.N + col0 + c * 32);
+          pq[0] = make_uint4(qw[0], qw[1], qw[2], qw[3]);
+          pq[1] = make_uint4(qw[4], qw[5], qw[6], qw[7]);
+        }
+        // N and col0 are multiples of 128: the word is 4-byte aligned when
+        // the scale buffer is
+        uint8_t* sp = g.s_out + grow * (g.N / 32) + col0 / 32;
+        if ((reinterpret_cast<uintptr_t>(sp) & 3) == 0) {
+          *reinterpret_cast<uint32_t*>(sp) = s4;
+        } else {
+#pragma unroll
+          for (int c = 0; c < 4; ++c) sp[c] = static_cast<uint8_t>(s4 >> (8 * c));
+        }
+        continue;
+      }
       uint32_t v[4][32];
       if (mine && !zero) {
         const uint32_t tb = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + wg * QHN;
@@ -895,7 +963,7 @@ __global__ void __launch_bounds__(QTHREADS, 1)
             }
           }
         }
-      } else if (QCfg<KIND, PAIR>::STO && !QOUT && g.tma_out && q * 32 + 32 <= tl.rows) {
+      } else if (QCfg<KIND, PAIR>::STO && g.tma_out && q * 32 + 32 <= tl.rows) {
         // the warp's 32 rows all lie in the expert: stage each 32 x 32 chunk
         // (64-byte swizzle: 16-byte chunk j of row r at j ^ ((r / 2) % 4))
         // and write it with a TMA store
@@ -926,10 +994,6 @@ __global__ void __launch_bounds__(QTHREADS, 1)
 #pragma unroll
           for (int c = 0; c < 4; ++c) {
             if constexpr (KIND == MxKind::kDgradAct) mx_dact_row32<ACT>(g, grow, col0 + c * 32, v[c]);
-            else if (QOUT)
-              mx_store_quant_row32(g.out + grow * g.ldo + col0 + c * 32,
-                                   g.q_out + grow * g.N + col0 + c * 32,
-                                   g.s_out + grow * (g.N / 32) + (col0 + c * 32) / 32, v[c]);
             else mx_store_row32(g.out + grow * g.ldo + col0 + c * 32, v[c]);
           }
         }

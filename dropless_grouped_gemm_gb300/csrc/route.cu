@@ -21,6 +21,7 @@
 #include <cudaTypedefs.h>
 
 #include <mutex>
+#include <type_traits>
 
 #include "ptx.cuh"
 #include "route.cuh"
@@ -161,17 +162,19 @@ __global__ void __launch_bounds__(kThreads) route_rank(const int32_t* __restrict
 }
 
 // Router: top-k experts of one token and the softmax of their logits, for
-// one warp.  Lane l holds logits l, l+32, ... (E <= 1024).  Each of the k
+// one warp.  Lane l holds logits l, l+32, ..., NV of them (32 * NV >= E; the
+// launchers take the smallest power of two, so that each round scans only
+// the slots that can hold a logit).  Each of the k
 // rounds takes the warp-wide largest logit not yet chosen, ties going to the
 // lower expert index, so the choice is exact and deterministic.  Round j
 // calls pick(j, expert, w) on every lane with the same values, w =
 // exp(logit - top) unnormalised; returns the sum of the k weights.
-template <class Pick>
+template <int NV, class Pick>
 __device__ __forceinline__ float topk_warp(const float* __restrict__ row, int E, int k, int lane,
                                            Pick pick) {
-  float v[32];
+  float v[NV];
 #pragma unroll
-  for (int i = 0; i < 32; ++i) {
+  for (int i = 0; i < NV; ++i) {
     const int e = lane + 32 * i;
     v[i] = (e < E) ? row[e] : -INFINITY;
   }
@@ -181,7 +184,7 @@ __device__ __forceinline__ float topk_warp(const float* __restrict__ row, int E,
     float bv = -INFINITY;
     int bi = 0x7fffffff;
 #pragma unroll
-    for (int i = 0; i < 32; ++i) {
+    for (int i = 0; i < NV; ++i) {
       const int e = lane + 32 * i;
       if (e < E && !((taken >> i) & 1u) && (v[i] > bv || bi == 0x7fffffff)) {
         bv = v[i];
@@ -207,6 +210,7 @@ __device__ __forceinline__ float topk_warp(const float* __restrict__ row, int E,
 }
 
 // One warp per token: topk_idx and the normalised probabilities.
+template <int NV>
 __global__ void __launch_bounds__(256) router_topk_kernel(const float* __restrict__ logits, int T,
                                                           int E, int k, int32_t* __restrict__ idx,
                                                           float* __restrict__ probs) {
@@ -214,7 +218,7 @@ __global__ void __launch_bounds__(256) router_topk_kernel(const float* __restric
   const int warps = gridDim.x * (blockDim.x >> 5);
   for (int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); t < T; t += warps) {
     const long long p0 = static_cast<long long>(t) * k;
-    const float sum = topk_warp(logits + static_cast<long long>(t) * E, E, k, lane,
+    const float sum = topk_warp<NV>(logits + static_cast<long long>(t) * E, E, k, lane,
                                 [&](int j, int e, float w) {
                                   if (lane == 0) {
                                     idx[p0 + j] = e;
@@ -230,26 +234,44 @@ __global__ void __launch_bounds__(256) router_topk_kernel(const float* __restric
 // Engine이 제공하는 세 가지 구성 요소": gate, top-k selection, dispatch and the
 // grouped FFN in one fused block): the same selection as router_topk_kernel,
 // and each chosen pair counted into its chunk's histogram ws[c][e] (c = pair
-// / kChunk; integer atomics, so the counts do not depend on their order; ws
-// is zeroed by route_fill).
+// / kChunk; ws is zeroed by route_fill2).  A block takes kTopkTokens
+// consecutive tokens, one per warp, whose pairs lie in at most `rows`
+// consecutive chunks (2 while kTopkTokens * k <= kChunk, 3 up to k = 1024):
+// it counts them in shared memory and adds each non-zero count to ws with
+// one atomic (a skewed router sends most tokens to a few experts, whose
+// counters would otherwise take one global atomic per pair).  The counts
+// are integer sums, so they do not depend on the order of the additions.
+constexpr int kTopkTokens = 8;
+template <int NV>
 __global__ void __launch_bounds__(256) route_topk_hist(const float* __restrict__ logits, int T,
                                                        int E, int k, int32_t* __restrict__ idx,
                                                        float* __restrict__ probs,
-                                                       int32_t* __restrict__ ws) {
+                                                       int32_t* __restrict__ ws, int rows) {
+  extern __shared__ int32_t hist[];   // [rows][E]: the block's first chunk and the next ones
   const int lane = threadIdx.x & 31;
-  const int warps = gridDim.x * (blockDim.x >> 5);
-  for (int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); t < T; t += warps) {
+  const int t0 = blockIdx.x * kTopkTokens;
+  const long long c0 = static_cast<long long>(t0) * k / kChunk;
+  for (int i = threadIdx.x; i < rows * E; i += blockDim.x) hist[i] = 0;
+  __syncthreads();
+  const int t = t0 + (threadIdx.x >> 5);
+  if (t < T) {
     const long long p0 = static_cast<long long>(t) * k;
-    const float sum = topk_warp(logits + static_cast<long long>(t) * E, E, k, lane,
+    const float sum = topk_warp<NV>(logits + static_cast<long long>(t) * E, E, k, lane,
                                 [&](int j, int e, float w) {
                                   if (lane == 0) {
                                     idx[p0 + j] = e;
                                     probs[p0 + j] = w;
-                                    atomicAdd(&ws[((p0 + j) / kChunk) * E + e], 1);
+                                    atomicAdd(&hist[((p0 + j) / kChunk - c0) * E + e], 1);
                                   }
                                 });
     __syncwarp();
     for (int j = lane; j < k; j += 32) probs[p0 + j] /= sum;
+  }
+  __syncthreads();
+  // rows past the last chunk stay zero and are skipped
+  for (int i = threadIdx.x; i < rows * E; i += blockDim.x) {
+    const int v = hist[i];
+    if (v != 0) atomicAdd(&ws[c0 * E + i], v);
   }
 }
 
@@ -261,6 +283,17 @@ __global__ void route_fill2(int32_t* __restrict__ p, int n, int32_t* __restrict_
   }
 }
 
+// logit slots per lane: the smallest power of two with 32 slots >= E
+template <class F>
+cudaError_t with_slots(int E, F&& f) {
+  if (E <= 32) return f(std::integral_constant<int, 1>{});
+  if (E <= 64) return f(std::integral_constant<int, 2>{});
+  if (E <= 128) return f(std::integral_constant<int, 4>{});
+  if (E <= 256) return f(std::integral_constant<int, 8>{});
+  if (E <= 512) return f(std::integral_constant<int, 16>{});
+  return f(std::integral_constant<int, 32>{});
+}
+
 }  // namespace
 
 cudaError_t launch_router_topk(const float* logits, int T, int E, int k, int32_t* idx,
@@ -268,8 +301,10 @@ cudaError_t launch_router_topk(const float* logits, int T, int E, int k, int32_t
   if (T <= 0) return cudaSuccess;
   const long long want = (static_cast<long long>(T) + 7) / 8;
   const int blocks = static_cast<int>(want < 16LL * num_sms ? want : 16LL * num_sms);
-  router_topk_kernel<<<blocks, 256, 0, s>>>(logits, T, E, k, idx, probs);
-  return cudaGetLastError();
+  return with_slots(E, [&](auto nv) {
+    router_topk_kernel<decltype(nv)::value><<<blocks, 256, 0, s>>>(logits, T, E, k, idx, probs);
+    return cudaGetLastError();
+  });
 }
 
 cudaError_t launch_route_logits(const float* logits, int T, int k, int E, int align, int M_cap,
@@ -289,9 +324,17 @@ cudaError_t launch_route_logits(const float* logits, int T, int k, int E, int al
     ++*launches;
   }
   if (T > 0) {
-    const long long want = (static_cast<long long>(T) + 7) / 8;
-    const int blocks = static_cast<int>(want < 16LL * num_sms ? want : 16LL * num_sms);
-    route_topk_hist<<<blocks, 256, 0, s>>>(logits, T, E, k, topk_idx, probs, ws);
+    // the kTopkTokens * k pairs of a block's tokens touch at most `rows`
+    // chunks (k <= E <= 1024: at most 12 KB of counters)
+    const int rows = (kTopkTokens * k - 1) / kChunk + 2;
+    const int blocks = (T + kTopkTokens - 1) / kTopkTokens;
+    const cudaError_t e = with_slots(E, [&](auto nv) {
+      route_topk_hist<decltype(nv)::value>
+          <<<blocks, 32 * kTopkTokens, static_cast<size_t>(rows) * E * sizeof(int32_t), s>>>(
+              logits, T, E, k, topk_idx, probs, ws, rows);
+      return cudaGetLastError();
+    });
+    if (e != cudaSuccess) return e;
     ++*launches;
   }
   route_scan<<<1, 1024, 0, s>>>(ws, nchunks, E, align, M_cap, counts, offsets, demanded,
