@@ -84,7 +84,8 @@ def test_deterministic():
         assert torch.equal(a[k_], b[k_])
 
 
-@pytest.mark.parametrize("T,E,k", [(4096, 256, 8), (300, 1024, 4), (64, 5, 5), (1000, 3, 1)])
+@pytest.mark.parametrize("T,E,k", [(4096, 256, 8), (300, 1024, 4), (64, 5, 5), (1000, 3, 1),
+                                   (500, 64, 6), (500, 128, 4), (300, 512, 16)])
 def test_router_topk(T, E, k):
     """Device top-k: the chosen experts match the oracle exactly (ties to the
     lower index); the softmax weights within float32 rounding."""
@@ -116,10 +117,13 @@ def test_router_then_layout_on_zipf_logits():
 
 
 # T * k not a multiple of the 4,096-pair chunk, with tokens whose k pairs
-# straddle a chunk boundary (k = 3), an expert count above 1,024 / 2 and a
-# one-expert layer
+# straddle a chunk boundary (k = 3), an expert count above 1,024 / 2, a
+# one-expert layer, every per-lane slot count of the router (E up to 32,
+# 64, 128, 256, 512, 1,024) and k > 512, where a block's eight tokens span
+# three chunks
 @pytest.mark.parametrize("T,E,k,align", [(4096, 256, 8, 1), (3000, 600, 3, 32), (700, 1, 1, 8),
-                                         (0, 16, 2, 1)])
+                                         (0, 16, 2, 1), (2000, 64, 6, 1), (1500, 128, 4, 4),
+                                         (1200, 512, 16, 1), (40, 700, 600, 1)])
 def test_fused_router_layout_equals_router_then_layout(T, E, k, align):
     """moe_route_logits (top-k fused into the layout's first pass) writes the
     router's topk_idx and probs and the layout's outputs bit for bit as the
