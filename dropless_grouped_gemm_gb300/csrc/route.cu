@@ -169,6 +169,17 @@ __global__ void __launch_bounds__(kThreads) route_rank(const int32_t* __restrict
 // lower expert index, so the choice is exact and deterministic.  Round j
 // calls pick(j, expert, w) on every lane with the same values, w =
 // exp(logit - top) unnormalised; returns the sum of the k weights.
+// float -> 32-bit key whose unsigned order is the order of the floats (no
+// NaN; -0 is keyed as +0, so that the two compare equal as floats do)
+__device__ __forceinline__ uint32_t order_key(float f) {
+  uint32_t b = __float_as_uint(f);
+  if (b == 0x80000000u) b = 0u;
+  return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+__device__ __forceinline__ float key_value(uint32_t k) {
+  return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
+}
+
 template <int NV, class Pick>
 __device__ __forceinline__ float topk_warp(const float* __restrict__ row, int E, int k, int lane,
                                            Pick pick) {
@@ -191,15 +202,14 @@ __device__ __forceinline__ float topk_warp(const float* __restrict__ row, int E,
         bi = e;
       }
     }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-      const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-      if (ov > bv || (ov == bv && oi < bi)) {
-        bv = ov;
-        bi = oi;
-      }
-    }
+    // warp argmax in two reductions: the largest key, then the lowest
+    // expert index among the lanes that hold it (0 marks a lane with no
+    // candidate; every real key is above it)
+    const uint32_t kv = (bi == 0x7fffffff) ? 0u : order_key(bv);
+    const uint32_t km = __reduce_max_sync(0xffffffffu, kv);
+    bi = static_cast<int>(__reduce_min_sync(
+        0xffffffffu, (kv == km && bi != 0x7fffffff) ? static_cast<uint32_t>(bi) : 0xffffffffu));
+    bv = key_value(km);
     if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
     if (j == 0) top = bv;
     const float ex = expf(bv - top);
