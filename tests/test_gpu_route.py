@@ -102,6 +102,27 @@ def test_router_topk(T, E, k):
     assert np.abs(p.cpu().numpy() - op).max() < 1e-6
 
 
+def test_router_signed_zero_ties():
+    """+0.0 and -0.0 logits compare equal, as floats do: a tie between them
+    goes to the lower expert index, as in the oracle's stable sort."""
+    import dropless_grouped_gemm_gb300 as M
+    E, k = 40, 3
+    lg = np.full((6, E), -1.0, dtype=np.float32)
+    lg[0, [7, 3]] = [-0.0, 0.0]          # tie at the top, -0 at the higher index
+    lg[1, [3, 7]] = [-0.0, 0.0]          # -0 at the lower index
+    lg[2, [1, 33, 38]] = [0.0, -0.0, 0.0]
+    lg[3, :] = -0.0                      # all tied
+    lg[4, :] = 0.0
+    lg[4, 20:] = -0.0
+    lg[5, [0, 39]] = [-np.inf, 0.0]
+    idx, p = M.router_topk(torch.from_numpy(lg).cuda(), k)
+    oi, op = O.router_topk(lg.astype(np.float64), k)
+    assert idx.cpu().numpy().tolist() == oi.tolist()
+    assert np.abs(p.cpu().numpy() - op).max() < 1e-6
+    fused = M.route_logits(torch.from_numpy(lg).cuda(), k, 1)
+    assert torch.equal(fused["topk_idx"], idx) and torch.equal(fused["probs"], p)
+
+
 def test_router_then_layout_on_zipf_logits():
     """Router on the Zipf layer's logits, then the routing layout: equal to
     the oracle's router followed by the oracle's layout."""
