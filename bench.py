@@ -778,7 +778,6 @@ def fusion_control(w, inp, o, reps=20):
     graph replay); their unfused baseline also uses other GEMM kernels, so
     only the fusion itself is compared here.  Each launch is timed with its
     own events, interleaved over ``reps`` rounds."""
-    import ctypes
     import torch
     import dropless_grouped_gemm_gb300 as M
     act, Mc = w.act, w.M_cap
@@ -799,26 +798,9 @@ def fusion_control(w, inp, o, reps=20):
                           dx_perm=o["dx_perm"], dW1=o["dW1"], dW2=o["dW2"], err=o["err"])  # 4
         M.grouped_gemm(dy, off, W2, "nk", out=da_u, err=o["err"])                 # 1
         M.activation_bwd(o["h"], da_u, off, act, dh=dh_u)                        # 1
-    per = 10
-    stream = torch.cuda.current_stream()
-    for _ in range(2):
-        round_()
-    evs = [torch.cuda.Event(enable_timing=True) for _ in range(2 * per * reps)]
-    for e in evs:
-        e.record(stream)
-    torch.cuda.synchronize()
-    handles = (ctypes.c_void_p * len(evs))(*[e.cuda_event for e in evs])
-    M.lib().moe_set_launch_events(handles, len(evs))
-    for _ in range(reps):
-        round_()
-    torch.cuda.synchronize()
-    used = M.lib().moe_launch_events_used()
-    M.lib().moe_set_launch_events(None, 0)
-    if used != len(evs) or int(o["err"].item()) != 0:
+    avg = _launch_rounds(round_, 10, reps)
+    if avg is None or int(o["err"].item()) != 0:
         return None
-    t = [[evs[2 * (r * per + i)].elapsed_time(evs[2 * (r * per + i) + 1]) for r in range(reps)]
-         for i in range(per)]
-    avg = [sum(v) / len(v) for v in t]
     fused_f, unf_f = avg[0], avg[2] + avg[3]
     fused_b, unf_b = avg[4], avg[8] + avg[9]
     return {"fwd": {"fused_ms": round(fused_f, 4), "unfused_ms": round(unf_f, 4),
@@ -839,8 +821,6 @@ def mx_fusion_control(w, inp, o, reps=20):
     quantiser pass (8 launches), interleaved over ``reps`` rounds on the
     step's own operands, each launch timed by its own events; the results
     of the two are identical (tested)."""
-    import ctypes
-    import torch
     import dropless_grouped_gemm_gb300 as M
     if w.routing == "identity":
         x, dy, off = inp["x_perm"], inp["dy_perm"], inp["offsets"]
@@ -854,28 +834,12 @@ def mx_fusion_control(w, inp, o, reps=20):
         M.grouped_mlp_bwd_mx(x, o["h"], dy, off, ops, w.act, dh=o["dh"], dx_perm=o["dx_perm"],
                              dW1=o["dW1"], dW2=o["dW2"], err=o["err"], workspace=mb["ws"],
                              separate_dh_quant=sep)
-    per = 15
-    stream = torch.cuda.current_stream()
-    for _ in range(2):
+    def round_():
         call(False)
         call(True)
-    evs = [torch.cuda.Event(enable_timing=True) for _ in range(2 * per * reps)]
-    for e in evs:
-        e.record(stream)
-    torch.cuda.synchronize()
-    handles = (ctypes.c_void_p * len(evs))(*[e.cuda_event for e in evs])
-    M.lib().moe_set_launch_events(handles, len(evs))
-    for _ in range(reps):
-        call(False)
-        call(True)
-    torch.cuda.synchronize()
-    used = M.lib().moe_launch_events_used()
-    M.lib().moe_set_launch_events(None, 0)
-    if used != len(evs) or int(o["err"].item()) != 0:
+    avg = _launch_rounds(round_, 15, reps)
+    if avg is None or int(o["err"].item()) != 0:
         return None
-    t = [[evs[2 * (r * per + i)].elapsed_time(evs[2 * (r * per + i) + 1]) for r in range(reps)]
-         for i in range(per)]
-    avg = [sum(v) / len(v) for v in t]
     fused = avg[3]                       # FC2-dgrad + dAct + Quantize/Transpose
     unf_gemm, unf_q = avg[7 + 3], avg[7 + 4]
     return {"bwd_dh": {"fused_ms": round(fused, 4), "unfused_ms": round(unf_gemm + unf_q, 4),
