@@ -289,15 +289,29 @@ def test_mx_requires_32_aligned_offsets():
     assert int(err.item()) & M.DEV_BAD_OFFSETS
 
 
-def test_group_gemm_quantize_outputs():
+# both tile configurations of the quantising epilogue (2-SM tiles, the
+# automatic choice for FC2 and FC1-dgrad, and single-CTA tiles forced), on a
+# layer with d = 256 and one with d = 384, whose second 256-column tile has
+# one 128-column half past N
+@pytest.mark.parametrize("pair_mode", [1, 0])
+@pytest.mark.parametrize("E,d,n,counts", [(4, 256, 128, [128, 0, 96, 64]),
+                                          (4, 384, 128, [512, 0, 288, 256])])
+def test_group_gemm_quantize_outputs(E, d, n, counts, pair_mode):
     """GroupGemm + Quantize: FC2's epilogue (forward) and FC1-dgrad's (MXFP8
     backward) also write the row-wise MXFP8 copy of the bf16 they store.
     The codes and scales equal the OCP MX quantiser applied to that bf16
     output, bit for bit, on every row inside an expert."""
+    import dropless_grouped_gemm_gb300 as MM
+    prev = MM.set_pair_mma(pair_mode)
+    try:
+        _group_gemm_quantize(E, d, n, counts)
+    finally:
+        MM.set_pair_mma(prev)
+
+
+def _group_gemm_quantize(E, d, n, counts):
     M = _lib()
     import dropless_grouped_gemm_gb300 as MM
-    E, d, n = 4, 256, 128
-    counts = [128, 0, 96, 64]
     off = np.concatenate([[0], np.cumsum(counts)]).astype(np.int64)
     M_cap = int(off[-1]) + 32
     R = int(off[-1])
