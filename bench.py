@@ -321,7 +321,7 @@ def make_step(w, inp, o):
             r = M.route_offsets(inp["topk_idx"], w.E, w.align, w.M_cap, out=o["route"],
                                 workspace=o["ws"])
             n += M.last_launch_count()
-            M.permute(inp["x"], r["pair_of_row"], k, out=o["x_perm"])
+            M.permute(inp["x"], r["pair_of_row"], k, out=o["x_perm"], row_of_pair=r["row_of_pair"])
             n += M.last_launch_count()
             M.mx_quantize_weights2(inp["W2"], o["mx"]["w2_q"], o["mx"]["w2_s"], o["mxb"]["w2_q"],
                                    o["mxb"]["w2_s"], offsets=r["offsets"])
@@ -333,7 +333,7 @@ def make_step(w, inp, o):
             M.unpermute(o["y_perm"], r["row_of_pair"], T, k, probs=inp["probs"], out=o["out"])
             n += M.last_launch_count()
             M.permute(inp["dO"], r["pair_of_row"], k, scale=inp["probs"].view(-1),
-                      out=o["dy_perm"])
+                      out=o["dy_perm"], row_of_pair=r["row_of_pair"])
             n += M.last_launch_count()
             M.unpermute(o["y_perm"], r["row_of_pair"], T, k, dO=inp["dO"], dprobs=o["dprobs"],
                         combine=False)
@@ -350,7 +350,7 @@ def make_step(w, inp, o):
             r = M.route_offsets(inp["topk_idx"], w.E, w.align, w.M_cap, out=o["route"],
                                 workspace=o["ws"])
             n += M.last_launch_count()
-            M.permute(inp["x"], r["pair_of_row"], k, out=o["x_perm"])
+            M.permute(inp["x"], r["pair_of_row"], k, out=o["x_perm"], row_of_pair=r["row_of_pair"])
             n += M.last_launch_count()
             M.mx_quantize_weights(inp["W2"], o["mx"]["w2_q"], o["mx"]["w2_s"], offsets=r["offsets"])
             n += M.last_launch_count()
@@ -369,7 +369,7 @@ def make_step(w, inp, o):
             r = M.route_offsets(inp["topk_idx"], w.E, w.align, w.M_cap, out=o["route"],
                                 workspace=o["ws"])
             n += M.last_launch_count()
-            M.permute(inp["x"], r["pair_of_row"], k, out=o["x_perm"])
+            M.permute(inp["x"], r["pair_of_row"], k, out=o["x_perm"], row_of_pair=r["row_of_pair"])
             n += M.last_launch_count()
             M.grouped_mlp_fwd(o["x_perm"], r["offsets"], inp["W1"], inp["W2"], act, a=o["a"],
                               y_perm=o["y_perm"], err=o["err"])
@@ -412,7 +412,7 @@ def make_step(w, inp, o):
         r = M.route_offsets(inp["topk_idx"], w.E, w.align, w.M_cap, out=o["route"],
                             workspace=o["ws"])
         n += M.last_launch_count()
-        M.permute(inp["x"], r["pair_of_row"], k, out=o["x_perm"])
+        M.permute(inp["x"], r["pair_of_row"], k, out=o["x_perm"], row_of_pair=r["row_of_pair"])
         n += M.last_launch_count()
         M.grouped_mlp_fwd(o["x_perm"], r["offsets"], inp["W1"], inp["W2"], act, save_h=True,
                           h_saved=o["h"], a=o["a"], y_perm=o["y_perm"], err=o["err"])
@@ -423,7 +423,7 @@ def make_step(w, inp, o):
         # backward with the router gradient inside the expert MLP ([Sonic]
         # rewrite): dO gathered without the probability; FC2-dgrad applies it
         # and emits dS partials and A' = S*A; FC2-wgrad contracts A' with dO
-        M.permute(inp["dO"], r["pair_of_row"], k, out=o["dy_perm"])
+        M.permute(inp["dO"], r["pair_of_row"], k, out=o["dy_perm"], row_of_pair=r["row_of_pair"])
         n += M.last_launch_count()
         M.grouped_mlp_bwd_routed(o["x_perm"], o["h"], o["dy_perm"], r["pair_of_row"],
                                  inp["probs"].view(-1), r["offsets"], inp["W1"], inp["W2"], act,

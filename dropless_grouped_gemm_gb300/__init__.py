@@ -8,7 +8,7 @@ fails, an exception is raised.
 Functions mirror the C ABI in ``include/moe.h``:
 
     route_offsets      -> moe_route_offsets
-    permute            -> moe_permute
+    permute            -> moe_permute (moe_permute_tokens with row_of_pair)
     unpermute          -> moe_unpermute
     grouped_mlp_fwd    -> moe_grouped_mlp_fwd
     grouped_mlp_bwd    -> moe_grouped_mlp_bwd
@@ -95,6 +95,8 @@ def lib():
                                         vp, vp]
         L.moe_permute.restype = i32
         L.moe_permute.argtypes = [vp, vp, vp, i32, i32, i32, i32, vp, vp]
+        L.moe_permute_tokens.restype = i32
+        L.moe_permute_tokens.argtypes = [vp, vp, vp, vp, i32, i32, i32, i32, vp, vp]
         L.moe_unpermute.restype = i32
         L.moe_unpermute.argtypes = [vp, vp, vp, i32, i32, i32, i32, vp, vp, vp, vp]
         L.moe_grouped_mlp_fwd.restype = i32
@@ -282,16 +284,27 @@ def route_logits(logits: torch.Tensor, k: int, align: int = 1, M_cap: int | None
 
 
 def permute(src: torch.Tensor, pair_of_row: torch.Tensor, k: int, scale: torch.Tensor | None = None,
-            out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
-    """Expert-major gather (see moe_permute)."""
+            out: torch.Tensor | None = None, stream=None,
+            row_of_pair: torch.Tensor | None = None) -> torch.Tensor:
+    """Expert-major gather (see moe_permute).  With ``row_of_pair`` (the
+    routing layout's inverse map) the copy runs in token order
+    (moe_permute_tokens), reading each token row once."""
     _need(src, torch.bfloat16, "src", 2)
     _need(pair_of_row, torch.int32, "pair_of_row")
+    _need(row_of_pair, torch.int32, "row_of_pair")
     _need(scale, torch.float32, "scale")
     T, d = src.shape
     M_cap = pair_of_row.numel()
     if out is None:
         out = torch.empty((M_cap, d), dtype=torch.bfloat16, device=src.device)
     _need(out, torch.bfloat16, "out", 2)
+    if row_of_pair is not None:
+        if row_of_pair.numel() != T * k:
+            raise MoeError("row_of_pair must hold T*k entries")
+        rc = lib().moe_permute_tokens(_ptr(src), _ptr(scale), _ptr(row_of_pair), _ptr(pair_of_row),
+                                      T, k, d, M_cap, _ptr(out), _stream(stream))
+        _check(rc, "moe_permute_tokens")
+        return out
     rc = lib().moe_permute(_ptr(src), _ptr(scale), _ptr(pair_of_row), T, k, d, M_cap, _ptr(out),
                            _stream(stream))
     _check(rc, "moe_permute")

@@ -434,6 +434,27 @@ int moe_permute(const moe_bf16* src, const float* scale, const int32_t* pair_of_
   return cuda_rc(e);
 }
 
+int moe_permute_tokens(const moe_bf16* src, const float* scale, const int32_t* row_of_pair,
+                       const int32_t* pair_of_row, int T, int k, int d, int M_cap, moe_bf16* dst,
+                       void* stream) {
+  g_last_launches = 0;
+  g_split_extra = 0;
+  if (T < 0 || k < 1 || d <= 0 || d % 64 || M_cap < 0) return MOE_E_SIZE;
+  if (static_cast<long long>(T) * k >= (1LL << 31)) return MOE_E_SIZE;
+  if (M_cap == 0) return MOE_OK;
+  if (!pair_of_row || !dst || (T > 0 && (!src || !row_of_pair))) return MOE_E_NULL;
+  if (misaligned(src) || misaligned(dst)) return MOE_E_ALIGN;
+  const int sms = num_sms_current();
+  if (sms <= 0) return MOE_E_CUDA;
+  ev_begin(static_cast<cudaStream_t>(stream));
+  const cudaError_t e = moe::launch_permute_tokens(src, scale, row_of_pair, pair_of_row, T, k, d,
+                                                   M_cap, dst, sms,
+                                                   static_cast<cudaStream_t>(stream));
+  ev_end(static_cast<cudaStream_t>(stream));
+  g_last_launches = 1 + g_split_extra;
+  return cuda_rc(e);
+}
+
 int moe_unpermute(const moe_bf16* src, const float* probs, const int32_t* row_of_pair, int T,
                   int k, int d, int M_cap, moe_bf16* dst, const moe_bf16* dO, float* dprobs,
                   void* stream) {

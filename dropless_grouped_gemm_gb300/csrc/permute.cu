@@ -69,6 +69,67 @@ __global__ void __launch_bounds__(kThreads)
   }
 }
 
+// The same permuted copy in token order, from both maps: one warp per token
+// reads the token's row once, 2 KB at a time, and writes it to each of its k
+// rows (row_of_pair), scaled per pair when scale is given; a pair whose row
+// lies outside [0, M_cap), or is not mapped back to it by pair_of_row, writes
+// nothing.  The row-order kernel above reads each token row once per pair
+// from whichever SM takes the destination row, and on the two-die GB300 most
+// of those reads miss the reading die's L2 (3.7x the token tensor from DRAM
+// on the Zipf layer).  Work items after the T tokens are groups of 32 rows:
+// a row that no valid pair maps to (pair_of_row outside [0, P)) is zeroed.
+__global__ void __launch_bounds__(kThreads)
+    permute_tokens_kernel(const uint4* __restrict__ src, const float* __restrict__ scale,
+                          const int32_t* __restrict__ row_of_pair,
+                          const int32_t* __restrict__ pair_of_row, int T, int k, int dv,
+                          int M_cap, uint4* __restrict__ dst) {
+  const int lane = threadIdx.x & 31;
+  const long long P = static_cast<long long>(T) * k;
+  const int nseg = (dv + kSeg - 1) / kSeg;
+  const long long tok_items = static_cast<long long>(T) * nseg;
+  const long long groups = (M_cap + 31) / 32;
+  const long long items = tok_items + groups;
+  for (long long it = static_cast<long long>(blockIdx.x) * kRowsPerBlock + (threadIdx.x >> 5);
+       it < items; it += static_cast<long long>(gridDim.x) * kRowsPerBlock) {
+    if (it < tok_items) {
+      const int t = static_cast<int>(it / nseg);
+      const uint4* in = src + static_cast<long long>(t) * dv;
+      {
+        const int v0 = static_cast<int>(it - static_cast<long long>(t) * nseg) * kSeg;
+        uint4 x[kSeg / 32];
+#pragma unroll
+        for (int i = 0; i < kSeg / 32; ++i) {
+          const int v = v0 + lane + 32 * i;
+          x[i] = (v < dv) ? __ldg(in + v) : make_uint4(0, 0, 0, 0);
+        }
+        for (int j = 0; j < k; ++j) {
+          const long long p = static_cast<long long>(t) * k + j;
+          const int r = row_of_pair[p];
+          if (r < 0 || r >= M_cap || pair_of_row[r] != p) continue;
+          uint4* out = dst + static_cast<long long>(r) * dv;
+          const float sc = scale ? scale[p] : 1.0f;
+#pragma unroll
+          for (int i = 0; i < kSeg / 32; ++i) {
+            const int v = v0 + lane + 32 * i;
+            if (v < dv) __stcs(out + v, scale ? scale_bf16x8(x[i], sc) : x[i]);
+          }
+        }
+      }
+    } else {
+      const int r0 = static_cast<int>(it - tok_items) * 32;
+      const int r = r0 + lane;
+      const int p = (r < M_cap) ? pair_of_row[r] : 0;
+      unsigned pad = __ballot_sync(0xffffffffu, r < M_cap && (p < 0 || p >= P));
+      while (pad) {
+        const int b = __ffs(pad) - 1;
+        pad &= pad - 1;
+        uint4* out = dst + static_cast<long long>(r0 + b) * dv;
+        for (int v = lane; v < dv; v += 32) __stcs(out + v, make_uint4(0, 0, 0, 0));
+      }
+    }
+  }
+}
+
 // dst[t] = sum_j w_tj src[row(t,j)] (fp32, j ascending).  Work item:
 // segment sg of token t; the rows of up to kSlots slots are loaded together
 // before they are added in slot order, so their latencies overlap.
@@ -192,7 +253,8 @@ int grid_for(const void* kernel, int* per_sm, long long items, int num_sms) {
   return static_cast<int>(want < cap ? (want > 0 ? want : 1) : cap);
 }
 
-int g_permute_per_sm = 0, g_combine_per_sm = 0, g_router_grad_per_sm = 0;
+int g_permute_per_sm = 0, g_permute_tokens_per_sm = 0, g_combine_per_sm = 0,
+    g_router_grad_per_sm = 0;
 
 }  // namespace
 
@@ -204,6 +266,21 @@ cudaError_t launch_permute(const uint16_t* src, const float* scale, const int32_
                             M_cap, num_sms),
                    kThreads, 0, s>>>(
       reinterpret_cast<const uint4*>(src), scale, pair_of_row, T * k, k, d / 8, M_cap,
+      reinterpret_cast<uint4*>(dst));
+  return cudaGetLastError();
+}
+
+cudaError_t launch_permute_tokens(const uint16_t* src, const float* scale,
+                                  const int32_t* row_of_pair, const int32_t* pair_of_row, int T,
+                                  int k, int d, int M_cap, uint16_t* dst, int num_sms,
+                                  cudaStream_t s) {
+  if (M_cap <= 0) return cudaSuccess;
+  const long long items =
+      static_cast<long long>(T) * ((d / 8 + kSeg - 1) / kSeg) + (M_cap + 31) / 32;
+  permute_tokens_kernel<<<grid_for(reinterpret_cast<const void*>(permute_tokens_kernel),
+                                   &g_permute_tokens_per_sm, items, num_sms),
+                          kThreads, 0, s>>>(
+      reinterpret_cast<const uint4*>(src), scale, row_of_pair, pair_of_row, T, k, d / 8, M_cap,
       reinterpret_cast<uint4*>(dst));
   return cudaGetLastError();
 }

@@ -39,6 +39,13 @@ cudaError_t launch_permute(const uint16_t* src, const float* scale, const int32_
                            int T, int k, int d, int M_cap, uint16_t* dst, int num_sms,
                            cudaStream_t s);
 
+// the same copy in token order from both (mutually inverse) maps, pad rows
+// zeroed
+cudaError_t launch_permute_tokens(const uint16_t* src, const float* scale,
+                                  const int32_t* row_of_pair, const int32_t* pair_of_row, int T,
+                                  int k, int d, int M_cap, uint16_t* dst, int num_sms,
+                                  cudaStream_t s);
+
 cudaError_t launch_unpermute(const uint16_t* src, const float* probs,
                              const int32_t* row_of_pair, int T, int k, int d, int M_cap,
                              uint16_t* dst,

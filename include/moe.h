@@ -272,6 +272,28 @@ int moe_permute(const moe_bf16* src, const float* scale,
                 moe_bf16* dst, void* stream);
 
 /*
+ * moe_permute_tokens - the same expert-major copy as moe_permute, walked in
+ * token order ([TE] "최적화 2: NCCL EP"): each token row is read once and
+ * written to each of its k rows, which moe_permute does by reading the token
+ * row once per pair.  It takes both maps that moe_route_offsets writes.
+ *
+ *   src [T, d] bf16, dst [M_cap, d] bf16, scale [T*k] float32 or NULL,
+ *   row_of_pair [T*k], pair_of_row [M_cap].
+ *   For each pair p = t*k + j with r = row_of_pair[p] in [0, M_cap) and
+ *   pair_of_row[r] == p:  dst[r] = src[t] (scale == NULL) or
+ *   bf16_rn(scale[p] * src[t]).  dst[r] = 0 for every row r whose
+ *   pair_of_row[r] lies outside [0, T*k).
+ *   With the inverse pair of maps of moe_route_offsets this writes exactly
+ *   what moe_permute writes, bit for bit; a row that pair_of_row assigns to
+ *   a pair whose row_of_pair entry points elsewhere is left unwritten.
+ *   Errors as moe_permute; row_of_pair may be NULL only when T == 0.
+ */
+int moe_permute_tokens(const moe_bf16* src, const float* scale,
+                       const int32_t* row_of_pair, const int32_t* pair_of_row,
+                       int T, int k, int d, int M_cap, moe_bf16* dst,
+                       void* stream);
+
+/*
  * moe_unpermute - combine ([TE] "최적화 2: NCCL EP": results return to token
  * order and each token accumulates its experts' outputs) and, optionally,
  * the router-score gradient ([Sonic] "역전파 계산 그래프 재작성하기":

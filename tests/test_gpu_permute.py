@@ -30,6 +30,36 @@ def test_permute_exact(T, k, E, d, align):
     assert np.array_equal(f64(xp), ref)           # bit-exact copy, zero pad rows
 
 
+# token-order permute (moe_permute_tokens): the same output as the row-order
+# kernel, bit for bit, from the routing layout's two maps - plain and scaled,
+# with pad rows (align), with pairs dropped by a too-small M_cap (their rows
+# -1, the rows past M_cap never written), k = 1, and T = 0 (pad rows only)
+@pytest.mark.parametrize("T,k,E,d,align,cap_cut,scaled", [
+    (512, 2, 4, 128, 1, 0, False), (300, 8, 64, 7168, 32, 0, False),
+    (300, 8, 64, 7168, 32, 0, True), (77, 1, 3, 64, 8, 0, False),
+    (400, 4, 16, 256, 1, 100, False), (400, 4, 16, 256, 16, 100, True),
+    (0, 2, 4, 128, 8, 0, False)])
+def test_permute_tokens_equals_row_order(T, k, E, d, align, cap_cut, scaled):
+    import dropless_grouped_gemm_gb300 as M
+    rng = np.random.default_rng(T + k + E + align)
+    idx = (np.stack([rng.permutation(E)[:k] for _ in range(T)]).astype(np.int32)
+           if T > 0 else np.zeros((0, k), np.int32))
+    M_cap = T * k - cap_cut if cap_cut else T * k + E * (align - 1)
+    r = M.route_offsets(cuda_i32(idx).reshape(T, k), E, align, M_cap)
+    x = W.normal((max(T, 1), d), (7, W.X, 0), 1.0, "cuda")[:T]
+    sc = torch.from_numpy(rng.random(T * k).astype(np.float32)).cuda() if scaled else None
+    a = torch.full((M_cap, d), float("nan"), dtype=torch.bfloat16, device="cuda")
+    b = torch.full((M_cap, d), float("nan"), dtype=torch.bfloat16, device="cuda")
+    M.permute(x, r["pair_of_row"], k, scale=sc, out=a)
+    M.permute(x, r["pair_of_row"], k, scale=sc, out=b, row_of_pair=r["row_of_pair"])
+    torch.cuda.synchronize()
+    assert int(r["err"].item()) == (M.DEV_OVERFLOW if cap_cut else 0)
+    assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+    if T > 0 and not scaled and not cap_cut:
+        ref = O.permute(f64(x), r["pair_of_row"].cpu().numpy(), k)
+        assert np.array_equal(f64(b), ref)
+
+
 def test_permute_scaled():
     import dropless_grouped_gemm_gb300 as M
     T, k, E, d = 257, 4, 16, 512
