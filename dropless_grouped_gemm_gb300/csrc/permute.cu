@@ -69,15 +69,18 @@ __global__ void __launch_bounds__(kThreads)
   }
 }
 
-// The same permuted copy in token order, from both maps: one warp per token
-// reads the token's row once, 2 KB at a time, and writes it to each of its k
+// The same permuted copy in token order, from both maps: a warp reads a
+// 2 KB segment of a token's row once and writes it to each of the token's k
 // rows (row_of_pair), scaled per pair when scale is given; a pair whose row
 // lies outside [0, M_cap), or is not mapped back to it by pair_of_row, writes
 // nothing.  The row-order kernel above reads each token row once per pair
 // from whichever SM takes the destination row, and on the two-die GB300 most
 // of those reads miss the reading die's L2 (3.7x the token tensor from DRAM
-// on the Zipf layer).  Work items after the T tokens are groups of 32 rows:
-// a row that no valid pair maps to (pair_of_row outside [0, P)) is zeroed.
+// on the Zipf layer).  The token work items are 2 KB segments of a row; the
+// items after them are the M_cap rows, one each: a row that no valid pair
+// maps to (pair_of_row outside [0, P)) is zeroed.  (Groups of 32 rows put a
+// run of pad rows on one warp: 151 against 137 us for the row-order kernel
+// on a layer with 7,936 pad rows.)
 __global__ void __launch_bounds__(kThreads)
     permute_tokens_kernel(const uint4* __restrict__ src, const float* __restrict__ scale,
                           const int32_t* __restrict__ row_of_pair,
@@ -87,8 +90,7 @@ __global__ void __launch_bounds__(kThreads)
   const long long P = static_cast<long long>(T) * k;
   const int nseg = (dv + kSeg - 1) / kSeg;
   const long long tok_items = static_cast<long long>(T) * nseg;
-  const long long groups = (M_cap + 31) / 32;
-  const long long items = tok_items + groups;
+  const long long items = tok_items + M_cap;
   for (long long it = static_cast<long long>(blockIdx.x) * kRowsPerBlock + (threadIdx.x >> 5);
        it < items; it += static_cast<long long>(gridDim.x) * kRowsPerBlock) {
     if (it < tok_items) {
@@ -116,14 +118,10 @@ __global__ void __launch_bounds__(kThreads)
         }
       }
     } else {
-      const int r0 = static_cast<int>(it - tok_items) * 32;
-      const int r = r0 + lane;
-      const int p = (r < M_cap) ? pair_of_row[r] : 0;
-      unsigned pad = __ballot_sync(0xffffffffu, r < M_cap && (p < 0 || p >= P));
-      while (pad) {
-        const int b = __ffs(pad) - 1;
-        pad &= pad - 1;
-        uint4* out = dst + static_cast<long long>(r0 + b) * dv;
+      const int r = static_cast<int>(it - tok_items);
+      const int p = pair_of_row[r];
+      if (p < 0 || p >= P) {
+        uint4* out = dst + static_cast<long long>(r) * dv;
         for (int v = lane; v < dv; v += 32) __stcs(out + v, make_uint4(0, 0, 0, 0));
       }
     }
@@ -275,8 +273,7 @@ cudaError_t launch_permute_tokens(const uint16_t* src, const float* scale,
                                   int k, int d, int M_cap, uint16_t* dst, int num_sms,
                                   cudaStream_t s) {
   if (M_cap <= 0) return cudaSuccess;
-  const long long items =
-      static_cast<long long>(T) * ((d / 8 + kSeg - 1) / kSeg) + (M_cap + 31) / 32;
+  const long long items = static_cast<long long>(T) * ((d / 8 + kSeg - 1) / kSeg) + M_cap;
   permute_tokens_kernel<<<grid_for(reinterpret_cast<const void*>(permute_tokens_kernel),
                                    &g_permute_tokens_per_sm, items, num_sms),
                           kThreads, 0, s>>>(
