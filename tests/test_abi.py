@@ -60,6 +60,13 @@ def test_host_argument_errors(L):
     assert L.moe_route_offsets(None, 4, 2, 8, 0, 12, None, None, None, None, None, None, 0, None,
                                None) == -3                  # align 0
     assert L.moe_permute(None, None, None, 4, 1, 100, 4, None, None) == -3
+    # token-order permute: same size rules; both maps (row_of_pair only when T > 0)
+    assert L.moe_permute_tokens(None, None, None, None, 4, 1, 100, 4, None, None) == -3
+    assert L.moe_permute_tokens(vp(16), None, None, vp(16), 4, 1, 64, 4, vp(16), None) == -1
+    assert L.moe_permute_tokens(vp(16), None, vp(16), None, 4, 1, 64, 4, vp(16), None) == -1
+    assert L.moe_permute_tokens(vp(16), None, vp(16), vp(16), 4, 0, 64, 4, vp(16), None) == -3
+    assert L.moe_permute_tokens(vp(8), None, vp(16), vp(16), 4, 1, 64, 4, vp(16), None) == -2
+    assert L.moe_permute_tokens(None, None, None, None, 4, 1, 64, 0, None, None) == 0  # nothing to do
     assert L.moe_unpermute(vp(16), None, vp(16), 2, 1, 64, 4, None, None, None, None) == -1
     # MXFP8 backward: sizes need multiples of 128 (d, n) and 32 (M_cap); mx required
     assert L.moe_grouped_mlp_bwd_mx(None, None, None, vp(16), 4, 128, 192, 128, 0, 0, None, None,
