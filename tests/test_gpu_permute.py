@@ -60,6 +60,25 @@ def test_permute_tokens_equals_row_order(T, k, E, d, align, cap_cut, scaled):
         assert np.array_equal(f64(b), ref)
 
 
+def test_permute_tokens_full_size_zipf():
+    """The bench's routed steps permute x and dO in token order: on the Zipf
+    layer's own routing (T = 4096, top-8, E = 256, d = 7168) both orders
+    write the same bits, plain and scaled."""
+    import dropless_grouped_gemm_gb300 as M
+    w = W.WORKLOADS["zipf_t4096_d7168_e256_top8_n2048_swiglu"]
+    idx, probs = W.route_inputs(w)
+    r = M.route_offsets(cuda_i32(idx), w.E, w.align, w.M_cap)
+    x = W.normal((w.T, w.d), (w.cfg_id, W.X, 0), w.x_std, "cuda")
+    sc = torch.from_numpy(probs.reshape(-1)).cuda()
+    for scale in (None, sc):
+        a = M.permute(x, r["pair_of_row"], w.k, scale=scale)
+        b = M.permute(x, r["pair_of_row"], w.k, scale=scale, row_of_pair=r["row_of_pair"])
+        torch.cuda.synchronize()
+        assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+        del a, b
+    assert int(r["err"].item()) == 0
+
+
 def test_permute_scaled():
     import dropless_grouped_gemm_gb300 as M
     T, k, E, d = 257, 4, 16, 512
